@@ -1,0 +1,131 @@
+"""Seeded synthetic inputs for the Gated DeltaNet kernels and their oracle.
+
+This module is the ONE thing the CUDA path and the fp64 oracle share: it only
+draws random numbers and shapes them; it holds none of the recurrence's
+arithmetic.  Every tensor is drawn in fp32 on the host with a seeded
+``torch.Generator`` and then cast, so both sides see identical values.
+
+Recipe (the pages run RL on named datasets; these synthetic tensors stand in
+for the activations a GDN layer receives there):
+
+* q, k ~ randn, then L2-normalised per head row in fp32, then cast;
+* v ~ randn;  b ~ randn and beta = sigmoid(b) (the kernels take beta already
+  activated, in (0, 1));  g = -softplus(randn) (a log-decay, so a = exp(g) is
+  in (0, 1));
+* init_state = 0 or randn * init_scale (fp32);
+* lengths: uniform in [lo, hi], or lognormal with the stated mean (before the
+  cap) and sigma = 1, rounded and clipped to [1, cap].
+
+Layouts: q, k [T, HK, dk]; v [T, HV, dv]; g, beta [T, HV] fp32;
+state [N, HV, dv, dk] fp32; cu_seqlens int32 [N + 1].
+"""
+from dataclasses import dataclass
+from typing import List, Optional, Sequence
+
+import math
+import torch
+
+
+@dataclass
+class GDNInputs:
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    g: torch.Tensor
+    beta: torch.Tensor
+    cu_seqlens: torch.Tensor
+    init_state: Optional[torch.Tensor]
+    lengths: List[int]
+
+    @property
+    def shape(self):
+        T, HK, dk = self.q.shape
+        HV, dv = self.v.shape[1], self.v.shape[2]
+        return dict(N=len(self.lengths), T=T, HK=HK, HV=HV, dk=dk, dv=dv)
+
+    def to(self, device):
+        mv = lambda t: None if t is None else t.to(device)  # noqa: E731
+        return GDNInputs(mv(self.q), mv(self.k), mv(self.v), mv(self.g), mv(self.beta),
+                         mv(self.cu_seqlens), mv(self.init_state), list(self.lengths))
+
+
+def _gen(seed: int) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return g
+
+
+def cu_from_lengths(lengths: Sequence[int]) -> torch.Tensor:
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + int(n))
+    return torch.tensor(cu, dtype=torch.int32)
+
+
+def uniform_lengths(n: int, lo: int, hi: int, seed: int) -> List[int]:
+    gen = _gen(seed)
+    return [int(x) for x in torch.randint(lo, hi + 1, (n,), generator=gen)]
+
+
+def lognormal_lengths(n: int, mean: float, cap: int, seed: int, sigma: float = 1.0) -> List[int]:
+    """Lognormal lengths with E[len] = mean before rounding and capping."""
+    gen = _gen(seed)
+    mu = math.log(mean) - sigma * sigma / 2.0
+    z = torch.randn(n, generator=gen, dtype=torch.float64)
+    return [int(min(max(round(math.exp(mu + sigma * float(x))), 1), cap)) for x in z]
+
+
+def _unit_rows(x: torch.Tensor) -> torch.Tensor:
+    return x / x.norm(dim=-1, keepdim=True).clamp_min(1e-30)
+
+
+def make_inputs(lengths: Sequence[int], HK: int, HV: int, dk: int, dv: int,
+                dtype=torch.bfloat16, seed: int = 0, init_scale: Optional[float] = None,
+                normalise_qk: bool = True) -> GDNInputs:
+    """Packed varlen inputs for ``len(lengths)`` sequences (see module doc)."""
+    gen = _gen(seed)
+    T = int(sum(lengths))
+    q = torch.randn(T, HK, dk, generator=gen)
+    k = torch.randn(T, HK, dk, generator=gen)
+    if normalise_qk:
+        q, k = _unit_rows(q), _unit_rows(k)
+    v = torch.randn(T, HV, dv, generator=gen)
+    b = torch.randn(T, HV, generator=gen)
+    g = -torch.nn.functional.softplus(torch.randn(T, HV, generator=gen))
+    beta = torch.sigmoid(b)
+    s0 = None
+    if init_scale is not None:
+        N = len(lengths)
+        s0 = (torch.randn(N, HV, dv, dk, generator=gen) * init_scale) if init_scale else \
+            torch.zeros(N, HV, dv, dk)
+    return GDNInputs(q.to(dtype).contiguous(), k.to(dtype).contiguous(), v.to(dtype).contiguous(),
+                     g.contiguous(), beta.contiguous(), cu_from_lengths(lengths), s0, list(lengths))
+
+
+def concat(parts: Sequence[GDNInputs]) -> GDNInputs:
+    """Pack several input sets (same head shapes) into one varlen batch, in order."""
+    lengths = [n for p in parts for n in p.lengths]
+    cat = lambda name: torch.cat([getattr(p, name) for p in parts], 0)  # noqa: E731
+    s0 = None
+    if any(p.init_state is not None for p in parts):
+        s0 = torch.cat([p.init_state if p.init_state is not None else
+                        torch.zeros(len(p.lengths), *parts[0].v.shape[1:], parts[0].q.shape[2])
+                        for p in parts], 0)
+    return GDNInputs(cat("q"), cat("k"), cat("v"), cat("g"), cat("beta"), cu_from_lengths(lengths),
+                     s0, lengths)
+
+
+def tiny_config(seed: int = 0) -> GDNInputs:
+    """1 sequence, T=64, 2 heads, dk=dv=16, fp32, zero initial state."""
+    return make_inputs([64], HK=2, HV=2, dk=16, dv=16, dtype=torch.float32, seed=seed,
+                       init_scale=0.0)
+
+
+def grad_out(T: int, HV: int, dv: int, dtype=torch.bfloat16, seed: int = 6) -> torch.Tensor:
+    """Upstream gradient dO ~ randn [T, HV, dv]."""
+    return torch.randn(T, HV, dv, generator=_gen(seed)).to(dtype).contiguous()
+
+
+def random_states(N: int, HV: int, dv: int, dk: int, seed: int, scale: float = 1.0) -> torch.Tensor:
+    """fp32 states ~ randn * scale, layout [N, HV, dv, dk]."""
+    return (torch.randn(N, HV, dv, dk, generator=_gen(seed)) * scale).contiguous()
