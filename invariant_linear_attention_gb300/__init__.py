@@ -1,0 +1,20 @@
+"""Batch-invariant Gated DeltaNet kernels for GB300 (sm_103a).
+
+One recurrent kernel serves prefill, decode and the trainer forward with
+bit-identical results per sequence (whatever shares the batch, however the
+tokens arrive); a chunked WY-form backward supplies gradients.  The compute
+lives in libgdn.so (C ABI: include/gdn.h); this package is its ctypes
+binding plus the seeded synthetic-input generators.
+"""
+from .binding import (  # noqa: F401
+    GdnError,
+    GdnShape,
+    gdn_chunk_bwd,
+    gdn_decode_step,
+    gdn_recurrent_fwd,
+    gdn_workspace_size,
+    lib,
+    make_shape,
+    read_device_error,
+    status_string,
+)

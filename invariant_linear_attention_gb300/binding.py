@@ -1,0 +1,228 @@
+"""Thin ctypes binding over libgdn.so (include/gdn.h).
+
+Argument marshalling only: tensors are checked for device, dtype, layout and
+alignment, outputs and workspaces are allocated with PyTorch when the caller
+does not pass them, and the raw device pointers plus the current CUDA stream
+go to the C entry points, which run every step of the computation in the
+library's own kernels.  There is no fallback: if the library is missing or a
+call fails, a RuntimeError is raised.
+"""
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgdn.so")
+_lib = None
+
+GDN_OK = 0
+GDN_F32, GDN_BF16 = 0, 1
+OP_FWD, OP_DECODE, OP_BWD = 0, 1, 2
+DEVERR_CU_SEQLENS, DEVERR_TIMEOUT = 1, 2
+
+_P = ctypes.c_void_p
+
+SYMBOLS = ("gdn_workspace_size", "gdn_recurrent_fwd", "gdn_decode_step", "gdn_chunk_bwd",
+           "gdn_read_device_error", "gdn_status_string")
+
+
+class GdnShape(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int), ("T_total", ctypes.c_int), ("HK", ctypes.c_int),
+                ("HV", ctypes.c_int), ("dk", ctypes.c_int), ("dv", ctypes.c_int),
+                ("dtype", ctypes.c_int), ("use_qk_l2norm", ctypes.c_int), ("dv_slice", ctypes.c_int)]
+
+
+class GdnError(RuntimeError):
+    def __init__(self, code, what):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)} ({code})")
+
+
+def lib():
+    """Load libgdn.so once; raise if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is missing: build it with invariant_linear_attention_gb300."
+                               "build_lib.build() (or __graft_entry__.build())")
+        L = ctypes.CDLL(_LIB_PATH)
+        L.gdn_workspace_size.argtypes = [ctypes.POINTER(GdnShape), ctypes.c_int]
+        L.gdn_workspace_size.restype = ctypes.c_size_t
+        L.gdn_recurrent_fwd.argtypes = [ctypes.POINTER(GdnShape)] + [_P] * 10 + [ctypes.c_size_t, _P]
+        L.gdn_recurrent_fwd.restype = ctypes.c_int
+        L.gdn_decode_step.argtypes = [ctypes.POINTER(GdnShape)] + [_P] * 7 + [ctypes.c_int, _P, _P]
+        L.gdn_decode_step.restype = ctypes.c_int
+        L.gdn_chunk_bwd.argtypes = [ctypes.POINTER(GdnShape)] + [_P] * 16 + [ctypes.c_size_t, _P]
+        L.gdn_chunk_bwd.restype = ctypes.c_int
+        L.gdn_read_device_error.argtypes = [_P, ctypes.POINTER(ctypes.c_uint), _P]
+        L.gdn_read_device_error.restype = ctypes.c_int
+        L.gdn_status_string.argtypes = [ctypes.c_int]
+        L.gdn_status_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().gdn_status_string(int(code)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t):
+    if t.dtype == torch.bfloat16:
+        return GDN_BF16
+    if t.dtype == torch.float32:
+        return GDN_F32
+    raise TypeError(f"q/k/v must be bfloat16 or float32, got {t.dtype}")
+
+
+def _need(t, name, dtype=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def make_shape(q, v, N, use_qk_l2norm=True, dv_slice=0, T_total=None):
+    T, HK, dk = q.shape
+    HV, dv = v.shape[1], v.shape[2]
+    return GdnShape(int(N), int(T if T_total is None else T_total), int(HK), int(HV), int(dk), int(dv),
+                    _dtype_code(q), int(bool(use_qk_l2norm)), int(dv_slice))
+
+
+def gdn_workspace_size(shape: GdnShape, op: int) -> int:
+    return int(lib().gdn_workspace_size(ctypes.byref(shape), int(op)))
+
+
+def _check(rc, what):
+    if rc != GDN_OK:
+        raise GdnError(rc, what)
+
+
+def gdn_recurrent_fwd(q, k, v, g, beta, cu_seqlens, init_state=None, out=None, final_state=None,
+                      workspace=None, use_qk_l2norm=True, dv_slice=0, output_final_state=True,
+                      stream=None):
+    """Batch-invariant recurrent forward over a packed varlen batch.
+
+    q, k [T, HK, dk] and v [T, HV, dv] (bf16 or fp32, same dtype), g, beta
+    [T, HV] fp32, cu_seqlens int32 [N+1] on the device, init_state
+    [N, HV, dv, dk] fp32 or None.  Returns (out [T, HV, dv], final_state
+    [N, HV, dv, dk] fp32 or None).  final_state may be init_state (in place).
+    """
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, dev)
+    _need(g, "g", torch.float32, dev)
+    _need(beta, "beta", torch.float32, dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    N = cu_seqlens.numel() - 1
+    T, HK, dk = q.shape
+    HV, dv = v.shape[1], v.shape[2]
+    if k.shape != q.shape or v.shape[0] != T or g.shape != (T, HV) or beta.shape != (T, HV):
+        raise ValueError("inconsistent shapes")
+    if init_state is not None:
+        _need(init_state, "init_state", torch.float32, dev)
+        if init_state.shape != (N, HV, dv, dk):
+            raise ValueError("init_state must be [N, HV, dv, dk]")
+    shape = make_shape(q, v, N, use_qk_l2norm, dv_slice)
+    if out is None:
+        out = torch.empty_like(v)
+    _need(out, "out", q.dtype, dev)
+    if final_state is None and output_final_state:
+        final_state = torch.empty(N, HV, dv, dk, dtype=torch.float32, device=dev)
+    if final_state is not None:
+        _need(final_state, "final_state", torch.float32, dev)
+    need = gdn_workspace_size(shape, OP_FWD)
+    if workspace is None:
+        workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, dev)
+    with torch.cuda.device(dev):
+        rc = lib().gdn_recurrent_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                     _ptr(init_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+                                     _ptr(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream))
+    _check(rc, "gdn_recurrent_fwd")
+    return out, final_state
+
+
+def gdn_decode_step(q, k, v, g, beta, state, state_indices=None, out=None, use_qk_l2norm=True,
+                    dv_slice=0, stream=None):
+    """One token per sequence on the cached fp32 state pool, updated in place.
+
+    q, k [B, HK, dk], v [B, HV, dv], g, beta [B, HV]; state [slots, HV, dv, dk]
+    fp32; state_indices int32 [B] or None (slot b).  Returns out [B, HV, dv].
+    """
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, dev)
+    _need(g, "g", torch.float32, dev)
+    _need(beta, "beta", torch.float32, dev)
+    _need(state, "state", torch.float32, dev)
+    B = q.shape[0]
+    if state_indices is not None:
+        _need(state_indices, "state_indices", torch.int32, dev)
+    shape = make_shape(q, v, B, use_qk_l2norm, dv_slice)
+    if out is None:
+        out = torch.empty_like(v)
+    _need(out, "out", q.dtype, dev)
+    with torch.cuda.device(dev):
+        rc = lib().gdn_decode_step(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                   _ptr(state), _ptr(state_indices), int(state.shape[0]), _ptr(out),
+                                   _stream(stream))
+    _check(rc, "gdn_decode_step")
+    return out
+
+
+def gdn_chunk_bwd(q, k, v, g, beta, cu_seqlens, d_out, init_state=None, d_final_state=None,
+                  workspace=None, use_qk_l2norm=True, need_d_init_state=True, stream=None):
+    """Chunked (WY) backward.  Returns dict dq, dk, dv (dtype of q), dg, dbeta, d_init_state (fp32)."""
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (d_out, "d_out")):
+        _need(t, n, q.dtype, dev)
+    _need(g, "g", torch.float32, dev)
+    _need(beta, "beta", torch.float32, dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    N = cu_seqlens.numel() - 1
+    T, HK, dk = q.shape
+    HV, dv = v.shape[1], v.shape[2]
+    for t, n in ((init_state, "init_state"), (d_final_state, "d_final_state")):
+        if t is not None:
+            _need(t, n, torch.float32, dev)
+    shape = make_shape(q, v, N, use_qk_l2norm, 0)
+    res = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+               dg=torch.empty(T, HV, dtype=torch.float32, device=dev),
+               dbeta=torch.empty(T, HV, dtype=torch.float32, device=dev),
+               d_init_state=torch.empty(N, HV, dv, dk, dtype=torch.float32, device=dev)
+               if need_d_init_state else None)
+    need = gdn_workspace_size(shape, OP_BWD)
+    if workspace is None:
+        workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, dev)
+    with torch.cuda.device(dev):
+        rc = lib().gdn_chunk_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                 _ptr(init_state), _ptr(cu_seqlens), _ptr(d_out), _ptr(d_final_state),
+                                 _ptr(res["dq"]), _ptr(res["dk"]), _ptr(res["dv"]), _ptr(res["dg"]),
+                                 _ptr(res["dbeta"]), _ptr(res["d_init_state"]), _ptr(workspace),
+                                 ctypes.c_size_t(workspace.numel()), _stream(stream))
+    _check(rc, "gdn_chunk_bwd")
+    return res
+
+
+def read_device_error(workspace, stream=None) -> int:
+    """Device error bits left in a FWD/BWD workspace (synchronises the stream)."""
+    bits = ctypes.c_uint(0)
+    rc = lib().gdn_read_device_error(_ptr(workspace), ctypes.byref(bits), _stream(stream))
+    _check(rc, "gdn_read_device_error")
+    return int(bits.value)

@@ -1,0 +1,844 @@
+// gdn_bwd.cu -- chunked (WY-form) backward of the gated delta rule.
+//
+// The pages keep the chunked kernel for the backward only, where batch
+// invariance does not matter ("Defending Against the Training-Inference
+// Numeric Mismatch in RL (Especially Linear Attention)", section 3.2).  The
+// chunk form used here (chunk C = 64 tokens, restarting at every sequence
+// start, last chunk partial) is the WY / UT representation of the delta rule
+// (Yang et al. 2024; Gated Delta Networks, ICLR 2025).  Within a chunk with
+// start state S0 (dv x dk) and in-chunk positions r:
+//     gam = cumsum(g), Gam = exp(gam), E[r,s] = exp(gam_r - gam_s), b_s = exp(gam_last - gam_s)
+//     A = strict_lower(diag(beta) (E * K K^T)),  T = (I + A)^-1
+//     W = T diag(beta Gam) K,   U~ = T diag(beta) V,   U = U~ - W S0^T
+//     O = diag(Gam) Q S0^T + (lower(E) * Q K^T) U,      S_end = Gam_last S0 + U^T diag(b) K
+// Backward, for D = dL/dS_end and dO:
+//     dU   = P^T dO + diag(b) K D^T                  (P = lower(E) * Q K^T)
+//     dS0  = Gam_last D + dO^T diag(Gam) Q - dU^T W   (the D of the previous chunk)
+//     dQ   = diag(Gam) dO S0 + dQK K,  dK = dQK^T Q + diag(b) U D + diag(beta Gam) T^T dW + (dKK + dKK^T) K
+//     dW = -dU S0, dV = diag(beta) T^T dU, dA = -T^T dT T^T, dT = dW (beta Gam K)^T + dU (beta V)^T
+//     plus the dbeta and dgam terms; dg = reverse cumsum of dgam inside the chunk.
+// Kernels (all fp32 SIMT in this version):
+//     bwd_offsets   chunk offsets per sequence (+ cu_seqlens validation)
+//     bwd_norm      q^, k^ and 1/|.| per (token, k-head)
+//     bwd_wy        per (chunk, head): gam, T, W, U~, Q K^T              [chunk-parallel]
+//     bwd_state_fwd per (sequence, head, dv slice): chunk-start states S_c and U   [sequential]
+//     bwd_state_bwd per (sequence, head, dv slice): D_c (end-of-chunk grads) and dU; d_init_state
+//     bwd_intra_s   per (chunk, head): the products with S0 and D (dQ_S, dW, U D)  [chunk-parallel]
+//     bwd_intra_c   per (chunk, head): the C x C products, dV, dbeta, dg          [chunk-parallel]
+//     bwd_fold      per (token, k-head): sum over the value heads of a k-head, L2-norm backward
+// Gradients are deterministic (fixed orders everywhere, no atomics on data).
+#include <algorithm>
+
+#include "gdn_host.h"
+#include "gdn_step.cuh"
+
+namespace gdn {
+
+constexpr int kC = 64;        // chunk length
+constexpr int kMaxD = 128;    // max dk, dv
+constexpr int kLdD = kMaxD + 1;  // smem leading dim of C x d / d x d matrices (odd: conflict-free columns)
+constexpr int kLdC = kC + 1;     // smem leading dim of C x C matrices
+constexpr int kRowsSlice = 32;   // dv rows per CTA in the sequential state passes
+constexpr int kNT = 256;         // threads of the chunk-parallel kernels
+constexpr int kNTs = 128;        // threads of the state-pass kernels
+
+struct BwdParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* g;
+    const float* beta;
+    const float* init_state;
+    const int32_t* cu;
+    const void* dout;
+    const float* dfinal;
+    void* dq_out;
+    void* dk_out;
+    void* dv_out;
+    float* dg;
+    float* dbeta;
+    float* dinit;
+    unsigned* err;
+    int32_t* coff;     // [N+1] chunk offsets
+    float* qn;         // [T, HK, dk]
+    float* kn;         // [T, HK, dk]
+    float* qinv;       // [T, HK]
+    float* kinv;       // [T, HK]
+    float* gam;        // [T, HV]
+    float* Wb;         // per chunk-head C x dk  (W, later dW)
+    float* Utb;        // per chunk-head C x dv  (U~)
+    float* Tb;         // per chunk-head C x C
+    float* QKb;        // per chunk-head C x C
+    float* Sb;         // per chunk-head dv x dk (chunk-start state)
+    float* Db;         // per chunk-head dv x dk (dL/d state at chunk end)
+    float* Ub;         // per chunk-head C x dv
+    float* dUb;        // per chunk-head C x dv
+    float* dgamA;      // per chunk-head C
+    float* dqh;        // [T, HV, dk]
+    float* dkh;        // [T, HV, dk]
+    int N, T, HK, HV, G, dk, dv, use_norm, nchm, dtype;
+};
+
+__device__ __forceinline__ size_t ch_index(const BwdParams& p, int c, int h) { return (size_t)c * p.HV + h; }
+
+__device__ __forceinline__ float ld_any(const void* base, size_t i, int dtype) {
+    return dtype == GDN_BF16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[i])
+                             : reinterpret_cast<const float*>(base)[i];
+}
+__device__ __forceinline__ void st_any(void* base, size_t i, int dtype, float x) {
+    if (dtype == GDN_BF16) reinterpret_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(x);
+    else reinterpret_cast<float*>(base)[i] = x;
+}
+
+// Locate global chunk c: sequence n (largest n with coff[n] <= c), token range [t0, t0 + len).
+__device__ __forceinline__ bool chunk_of(const BwdParams& p, int c, int& n, int& t0, int& len) {
+    if (c >= p.coff[p.N]) return false;
+    int lo = 0, hi = p.N - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.coff[mid] <= c) lo = mid;
+        else hi = mid - 1;
+    }
+    n = lo;
+    int bos = min(max(p.cu[n], 0), p.T), eos = min(max(p.cu[n + 1], bos), p.T);
+    t0 = bos + (c - p.coff[n]) * kC;
+    len = min(kC, eos - t0);
+    return len > 0;
+}
+
+// CTA-wide C(m, n) = sum_k A(m, k) B(k, n) over fp32 operands (shared or global),
+// A(m, k) = A[m * as0 + k * as1], B(k, n) = B[k * bs0 + n * bs1].  Every output is
+// produced by exactly one thread, once, through f(m, n, value); the k order is
+// increasing, so results are deterministic.  4 x 4 register micro-tiles with
+// rows m = tm + i * TMc and columns n = tn + j * TNc.
+template <typename F>
+__device__ __forceinline__ void cta_gemm(int M, int N, int K, const float* __restrict__ A, int as0, int as1,
+                                         const float* __restrict__ B, int bs0, int bs1, F&& f) {
+    const int tmc = M >> 2, tnc = N >> 2;
+    for (int tile = threadIdx.x; tile < tmc * tnc; tile += blockDim.x) {
+        const int tm = tile / tnc, tn = tile - tm * tnc;
+        float acc[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+        const float* a0 = A + (size_t)tm * as0;
+        const float* b0 = B + (size_t)tn * bs1;
+        for (int kk = 0; kk < K; ++kk) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = a0[(size_t)(i * tmc) * as0 + (size_t)kk * as1];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) b[j] = b0[(size_t)kk * bs0 + (size_t)(j * tnc) * bs1];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) f(tm + i * tmc, tn + j * tnc, acc[i][j]);
+    }
+}
+
+// Copy rows [0, len) of a global [rows, stride] fp32 matrix (row r at base + r * gstride) into
+// shared memory (leading dim ld), zero-filling rows len .. R-1.  cols <= ld.
+__device__ __forceinline__ void load_rows_f32(float* dst, int ld, const float* base, size_t gstride, int R, int len,
+                                              int cols) {
+    for (int i = threadIdx.x; i < R * cols; i += blockDim.x) {
+        const int r = i / cols, c = i - r * cols;
+        dst[r * ld + c] = r < len ? base[(size_t)r * gstride + c] : 0.f;
+    }
+}
+
+__device__ __forceinline__ void load_rows_any(float* dst, int ld, const void* base, size_t off, size_t gstride,
+                                              int R, int len, int cols, int dtype) {
+    for (int i = threadIdx.x; i < R * cols; i += blockDim.x) {
+        const int r = i / cols, c = i - r * cols;
+        dst[r * ld + c] = r < len ? ld_any(base, off + (size_t)r * gstride + c, dtype) : 0.f;
+    }
+}
+
+// ---------------------------------------------------------------------------
+__global__ void bwd_offsets_kernel(BwdParams p) {
+    if (threadIdx.x != 0) return;
+    int acc = 0;
+    for (int n = 0; n < p.N; ++n) {
+        const int a = p.cu[n], b = p.cu[n + 1];
+        if ((n == 0 && a != 0) || b < a || (n == p.N - 1 && b != p.T)) atomicOr(p.err, GDN_DEVERR_CU_SEQLENS);
+        const int lo = min(max(a, 0), p.T), hi = min(max(b, lo), p.T);
+        p.coff[n] = acc;
+        acc += (hi - lo + kC - 1) / kC;
+    }
+    p.coff[p.N] = min(acc, p.nchm);
+}
+
+// one warp per (token, k-head): q^, k^ and the reciprocal norms
+__global__ void bwd_norm_kernel(BwdParams p) {
+    const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (w >= p.T * p.HK) return;
+    for (int which = 0; which < 2; ++which) {
+        const void* src = which ? p.k : p.q;
+        float x[4];
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int j = lane + 32 * i;
+            x[i] = j < p.dk ? ld_any(src, (size_t)w * p.dk + j, p.dtype) : 0.f;
+            ss = fmaf(x[i], x[i], ss);
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(kFull, ss, off);
+        const float inv = p.use_norm ? __frsqrt_rn(ss + kNormEps) : 1.f;
+        float* dst = (which ? p.kn : p.qn) + (size_t)w * p.dk;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int j = lane + 32 * i;
+            if (j < p.dk) dst[j] = x[i] * inv;
+        }
+        if (lane == 0) (which ? p.kinv : p.qinv)[w] = inv;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// per (chunk, head): gam, T = (I + A)^-1, W, U~, QK
+__global__ void __launch_bounds__(kNT) bwd_wy_kernel(BwdParams p) {
+    extern __shared__ float sm[];
+    const int c = blockIdx.x, h = blockIdx.y;
+    int n, t0, len;
+    if (!chunk_of(p, c, n, t0, len)) return;
+    const int hk = h / p.G, dk = p.dk, dv = p.dv;
+    float* sK = sm;                  // C x kLdD
+    float* sQ = sK + kC * kLdD;      // C x kLdD (later V)
+    float* sA = sQ + kC * kLdD;      // C x kLdC
+    float* sT = sA + kC * kLdC;      // C x kLdC
+    float* sTt = sT + kC * kLdC;     // C x kLdC
+    float* sg = sTt + kC * kLdC;     // gam [C]
+    float* sGb = sg + kC;            // beta * Gam [C]
+    float* sb = sGb + kC;            // beta [C]
+
+    load_rows_f32(sK, kLdD, p.kn + ((size_t)t0 * p.HK + hk) * dk, (size_t)p.HK * dk, kC, len, dk);
+    load_rows_f32(sQ, kLdD, p.qn + ((size_t)t0 * p.HK + hk) * dk, (size_t)p.HK * dk, kC, len, dk);
+    if (threadIdx.x < 32) {
+        // inclusive cumsum of g over the chunk, one warp, fixed order (lane-serial blocks of 2)
+        float g0 = 0.f, g1 = 0.f;
+        const int r0 = 2 * threadIdx.x, r1 = r0 + 1;
+        if (r0 < len) g0 = p.g[(size_t)(t0 + r0) * p.HV + h];
+        if (r1 < len) g1 = p.g[(size_t)(t0 + r1) * p.HV + h];
+        float s = g0 + g1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(kFull, s, off);
+            if ((int)threadIdx.x >= off) s += y;
+        }
+        const float excl = s - (g0 + g1);
+        const float c0 = excl + g0, c1 = c0 + g1;
+        sg[r0] = c0;
+        sg[r1] = c1;
+        const float b0 = r0 < len ? p.beta[(size_t)(t0 + r0) * p.HV + h] : 0.f;
+        const float b1 = r1 < len ? p.beta[(size_t)(t0 + r1) * p.HV + h] : 0.f;
+        sb[r0] = b0;
+        sb[r1] = b1;
+        sGb[r0] = b0 * expf(c0);
+        sGb[r1] = b1 * expf(c1);
+        if (r0 < len) p.gam[(size_t)(t0 + r0) * p.HV + h] = c0;
+        if (r1 < len) p.gam[(size_t)(t0 + r1) * p.HV + h] = c1;
+    }
+    __syncthreads();
+    const size_t ci = ch_index(p, c, h);
+    // A = strict_lower(beta_r E[r,s] (K K^T)[r,s]);  QK = Q K^T (stored)
+    cta_gemm(kC, kC, dk, sK, kLdD, 1, sK, 1, kLdD, [&](int r, int s, float kk) {
+        sA[r * kLdC + s] = (s < r) ? sb[r] * expf(sg[r] - sg[s]) * kk : 0.f;
+    });
+    float* QK = p.QKb + ci * kC * kC;
+    cta_gemm(kC, kC, dk, sQ, kLdD, 1, sK, 1, kLdD, [&](int r, int s, float x) { QK[r * kC + s] = x; });
+    __syncthreads();
+    // T = (I + A)^-1: thread j solves column j by forward substitution (columns are independent)
+    if (threadIdx.x < kC) {
+        const int j = threadIdx.x;
+        for (int r = 0; r < kC; ++r) {
+            float x = (r == j) ? 1.f : 0.f;
+            for (int s = j; s < r; ++s) x = fmaf(-sA[r * kLdC + s], sT[s * kLdC + j], x);
+            sT[r * kLdC + j] = (r < j) ? 0.f : x;
+        }
+    }
+    // V into sQ (Q is no longer needed)
+    __syncthreads();
+    load_rows_any(sQ, kLdD, p.v, ((size_t)t0 * p.HV + h) * dv, (size_t)p.HV * dv, kC, len, dv, p.dtype);
+    float* Tg = p.Tb + ci * kC * kC;
+    for (int i = threadIdx.x; i < kC * kC; i += blockDim.x) {
+        const int r = i / kC, s = i - r * kC;
+        Tg[i] = sT[r * kLdC + s];
+        sTt[r * kLdC + s] = sT[r * kLdC + s] * sGb[s];
+    }
+    __syncthreads();
+    float* W = p.Wb + ci * kC * dk;
+    cta_gemm(kC, dk, kC, sTt, kLdC, 1, sK, kLdD, 1, [&](int r, int j, float x) { W[r * dk + j] = x; });
+    __syncthreads();
+    for (int i = threadIdx.x; i < kC * kC; i += blockDim.x) {
+        const int r = i / kC, s = i - r * kC;
+        sTt[r * kLdC + s] = sT[r * kLdC + s] * sb[s];
+    }
+    __syncthreads();
+    float* Ut = p.Utb + ci * kC * dv;
+    cta_gemm(kC, dv, kC, sTt, kLdC, 1, sQ, kLdD, 1, [&](int r, int j, float x) { Ut[r * dv + j] = x; });
+}
+
+// ---------------------------------------------------------------------------
+// per (sequence, head, slice of R rows): S_c for every chunk, U = U~ - W S^T, S <- Gam_C S + U^T diag(b) K
+__global__ void __launch_bounds__(kNTs) bwd_state_fwd_kernel(BwdParams p, int R) {
+    extern __shared__ float sm[];
+    const int n = blockIdx.x, h = blockIdx.y, r0 = blockIdx.z * R;
+    const int hk = h / p.G, dk = p.dk, dv = p.dv;
+    float* sS = sm;                   // R x kLdD
+    float* sW = sS + R * kLdD;        // C x kLdD
+    float* sK = sW + kC * kLdD;       // C x kLdD (scaled by b)
+    float* sU = sK + kC * kLdD;       // C x (R + 1)
+    float* sg = sU + kC * (R + 1);    // gam [C]
+    const int ldU = R + 1;
+    const float* s0 = p.init_state ? p.init_state + (((size_t)n * p.HV + h) * dv + r0) * dk : nullptr;
+    for (int i = threadIdx.x; i < R * dk; i += blockDim.x) {
+        const int r = i / dk, j = i - r * dk;
+        sS[r * kLdD + j] = s0 ? s0[(size_t)r * dk + j] : 0.f;
+    }
+    const int bos = min(max(p.cu[n], 0), p.T), eos = min(max(p.cu[n + 1], bos), p.T);
+    const int nch = (eos - bos + kC - 1) / kC;
+    for (int j = 0; j < nch; ++j) {
+        const int c = p.coff[n] + j;
+        if (c >= p.nchm) break;
+        const int t0 = bos + j * kC, len = min(kC, eos - t0);
+        const size_t ci = ch_index(p, c, h);
+        __syncthreads();
+        // chunk-start state out
+        float* Sg = p.Sb + ci * dv * dk + (size_t)r0 * dk;
+        for (int i = threadIdx.x; i < R * dk; i += blockDim.x) {
+            const int r = i / dk, jj = i - r * dk;
+            Sg[i] = sS[r * kLdD + jj];
+        }
+        load_rows_f32(sW, kLdD, p.Wb + ci * kC * dk, dk, kC, kC, dk);
+        load_rows_f32(sK, kLdD, p.kn + ((size_t)t0 * p.HK + hk) * dk, (size_t)p.HK * dk, kC, len, dk);
+        for (int i = threadIdx.x; i < kC; i += blockDim.x) sg[i] = i < len ? p.gam[(size_t)(t0 + i) * p.HV + h] : 0.f;
+        __syncthreads();
+        const float gl = sg[len - 1];
+        for (int i = threadIdx.x; i < kC * dk; i += blockDim.x) {
+            const int r = i / dk, jj = i - r * dk;
+            if (r < len) sK[r * kLdD + jj] *= expf(gl - sg[r]);
+        }
+        // U = U~ - W S^T  (C x R)
+        const float* Ut = p.Utb + ci * kC * dv + r0;
+        float* Ug = p.Ub + ci * kC * dv + r0;
+        cta_gemm(kC, R, dk, sW, kLdD, 1, sS, 1, kLdD, [&](int r, int i, float x) {
+            const float u = Ut[(size_t)r * dv + i] - x;
+            sU[r * ldU + i] = u;
+            Ug[(size_t)r * dv + i] = u;
+        });
+        __syncthreads();
+        // S <- Gam_last S + U^T (b K)
+        const float Gl = expf(gl);
+        cta_gemm(R, dk, kC, sU, 1, ldU, sK, kLdD, 1,
+                 [&](int i, int jj, float x) { sS[i * kLdD + jj] = fmaf(Gl, sS[i * kLdD + jj], x); });
+    }
+}
+
+// per (sequence, head, slice of R rows), chunks in reverse: D_c (gradient at chunk end), dU; d_init_state
+__global__ void __launch_bounds__(kNTs) bwd_state_bwd_kernel(BwdParams p, int R) {
+    extern __shared__ float sm[];
+    const int n = blockIdx.x, h = blockIdx.y, r0 = blockIdx.z * R;
+    const int hk = h / p.G, dk = p.dk, dv = p.dv;
+    const int ldR = R + 1;
+    float* sD = sm;                    // R x kLdD
+    float* sQ = sD + R * kLdD;         // C x kLdD (scaled by Gam)
+    float* sW = sQ + kC * kLdD;        // C x kLdD (then K scaled by b)
+    float* sP = sW + kC * kLdD;        // C x kLdC
+    float* sO = sP + kC * kLdC;        // C x ldR  (dO slice)
+    float* sdU = sO + kC * ldR;        // C x ldR
+    float* sg = sdU + kC * ldR;        // gam [C]
+    const float* df = p.dfinal ? p.dfinal + (((size_t)n * p.HV + h) * dv + r0) * dk : nullptr;
+    for (int i = threadIdx.x; i < R * dk; i += blockDim.x) {
+        const int r = i / dk, j = i - r * dk;
+        sD[r * kLdD + j] = df ? df[(size_t)r * dk + j] : 0.f;
+    }
+    const int bos = min(max(p.cu[n], 0), p.T), eos = min(max(p.cu[n + 1], bos), p.T);
+    const int nch = (eos - bos + kC - 1) / kC;
+    for (int j = nch - 1; j >= 0; --j) {
+        const int c = p.coff[n] + j;
+        if (c >= p.nchm) continue;
+        const int t0 = bos + j * kC, len = min(kC, eos - t0);
+        const size_t ci = ch_index(p, c, h);
+        __syncthreads();
+        float* Dg = p.Db + ci * dv * dk + (size_t)r0 * dk;
+        for (int i = threadIdx.x; i < R * dk; i += blockDim.x) {
+            const int r = i / dk, jj = i - r * dk;
+            Dg[i] = sD[r * kLdD + jj];
+        }
+        for (int i = threadIdx.x; i < kC; i += blockDim.x) sg[i] = i < len ? p.gam[(size_t)(t0 + i) * p.HV + h] : 0.f;
+        load_rows_any(sO, ldR, p.dout, ((size_t)t0 * p.HV + h) * dv + r0, (size_t)p.HV * dv, kC, len, R, p.dtype);
+        load_rows_f32(sQ, kLdD, p.qn + ((size_t)t0 * p.HK + hk) * dk, (size_t)p.HK * dk, kC, len, dk);
+        load_rows_f32(sW, kLdD, p.kn + ((size_t)t0 * p.HK + hk) * dk, (size_t)p.HK * dk, kC, len, dk);
+        __syncthreads();
+        const float gl = sg[len - 1];
+        const float* QK = p.QKb + ci * kC * kC;
+        for (int i = threadIdx.x; i < kC * kC; i += blockDim.x) {
+            const int r = i / kC, s = i - r * kC;
+            sP[r * kLdC + s] = (s <= r && r < len) ? QK[i] * expf(sg[r] - sg[s]) : 0.f;
+        }
+        for (int i = threadIdx.x; i < kC * dk; i += blockDim.x) {
+            const int r = i / dk, jj = i - r * dk;
+            if (r < len) sW[r * kLdD + jj] *= expf(gl - sg[r]);  // b K
+        }
+        __syncthreads();
+        // dU = P^T dO + (b K) D^T   (C x R)
+        cta_gemm(kC, R, kC, sP, 1, kLdC, sO, ldR, 1, [&](int s, int i, float x) { sdU[s * ldR + i] = x; });
+        __syncthreads();
+        float* dUg = p.dUb + ci * kC * dv + r0;
+        cta_gemm(kC, R, dk, sW, kLdD, 1, sD, 1, kLdD, [&](int s, int i, float x) {
+            const float u = sdU[s * ldR + i] + x;
+            sdU[s * ldR + i] = u;
+            dUg[(size_t)s * dv + i] = u;
+        });
+        __syncthreads();
+        // W into sW, Gam Q in sQ
+        load_rows_f32(sW, kLdD, p.Wb + ci * kC * dk, dk, kC, kC, dk);
+        for (int i = threadIdx.x; i < kC * dk; i += blockDim.x) {
+            const int r = i / dk, jj = i - r * dk;
+            if (r < len) sQ[r * kLdD + jj] *= expf(sg[r]);
+        }
+        __syncthreads();
+        // D <- Gam_last D + dO^T (Gam Q) - dU^T W
+        const float Gl = expf(gl);
+        cta_gemm(R, dk, kC, sO, 1, ldR, sQ, kLdD, 1, [&](int i, int jj, float x) {
+            sD[i * kLdD + jj] = fmaf(Gl, sD[i * kLdD + jj], x);
+        });
+        __syncthreads();
+        cta_gemm(R, dk, kC, sdU, 1, ldR, sW, kLdD, 1,
+                 [&](int i, int jj, float x) { sD[i * kLdD + jj] -= x; });
+    }
+    __syncthreads();
+    if (p.dinit) {
+        float* di = p.dinit + (((size_t)n * p.HV + h) * dv + r0) * dk;
+        for (int i = threadIdx.x; i < R * dk; i += blockDim.x) {
+            const int r = i / dk, j = i - r * dk;
+            di[i] = sD[r * kLdD + j];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Deterministic CTA sum of one float per thread (fixed tree); all threads get the result.
+__device__ __forceinline__ float cta_sum(float x, float* red) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) x += __shfl_xor_sync(kFull, x, off);
+    const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[w] = x;
+    __syncthreads();
+    float s = 0.f;
+    for (int i = 0; i < nw; ++i) s += red[i];
+    return s;
+}
+
+// per (chunk, head): products with S0 and D.
+//   dQ_S = diag(Gam) dO S0 -> dqh;  dgam_r += q^_r . dQ_S,r;  dW = -dU S0 -> Wb
+//   dgam_last += Gam_last <D, S0>;  UD = U D: dkh = diag(b) UD, db_s = k^_s . UD_s
+__global__ void __launch_bounds__(kNT) bwd_intra_s_kernel(BwdParams p) {
+    extern __shared__ float sm[];
+    const int c = blockIdx.x, h = blockIdx.y;
+    int n, t0, len;
+    if (!chunk_of(p, c, n, t0, len)) return;
+    const int hk = h / p.G, dk = p.dk, dv = p.dv;
+    float* sBig = sm;                   // dv x kLdD  (S0, then D)
+    float* sA = sBig + kMaxD * kLdD;    // C x kLdD   (dO, then U)
+    float* sB = sA + kC * kLdD;         // C x kLdD   (Q, then K)
+    float* sC = sB + kC * kLdD;         // C x kLdD   (dU, then UD)
+    float* sX = sC + kC * kLdD;         // C x kLdD   (dQ_S)
+    float* sg = sX + kC * kLdD;         // gam [C]
+    float* sdg = sg + kC;               // dgam [C]
+    float* red = sdg + kC;              // [32]
+    const size_t ci = ch_index(p, c, h);
+    load_rows_f32(sBig, kLdD, p.Sb + ci * dv * dk, dk, dv, dv, dk);
+    load_rows_any(sA, kLdD, p.dout, ((size_t)t0 * p.HV + h) * dv, (size_t)p.HV * dv, kC, len, dv, p.dtype);
+    load_rows_f32(sB, kLdD, p.qn + ((size_t)t0 * p.HK + hk) * dk, (size_t)p.HK * dk, kC, len, dk);
+    load_rows_f32(sC, kLdD, p.dUb + ci * kC * dv, dv, kC, kC, dv);
+    for (int i = threadIdx.x; i < kC; i += blockDim.x) {
+        sg[i] = i < len ? p.gam[(size_t)(t0 + i) * p.HV + h] : 0.f;
+        sdg[i] = 0.f;
+    }
+    __syncthreads();
+    const float gl = sg[len - 1];
+    // dQ_S = diag(Gam) dO S0
+    cta_gemm(kC, dk, dv, sA, kLdD, 1, sBig, kLdD, 1,
+             [&](int r, int j, float x) { sX[r * kLdD + j] = (r < len) ? expf(sg[r]) * x : 0.f; });
+    // dW = -dU S0
+    float* dW = p.Wb + ci * kC * dk;
+    cta_gemm(kC, dk, dv, sC, kLdD, 1, sBig, kLdD, 1, [&](int r, int j, float x) { dW[r * dk + j] = -x; });
+    __syncthreads();
+    float* dq = p.dqh;
+    for (int i = threadIdx.x; i < kC * dk; i += blockDim.x) {
+        const int r = i / dk, j = i - r * dk;
+        if (r < len) dq[((size_t)(t0 + r) * p.HV + h) * dk + j] = sX[r * kLdD + j];
+    }
+    // dgam_r += q^_r . dQ_S,r  (one warp per row, fixed order)
+    {
+        const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+        for (int r = w; r < len; r += nw) {
+            float s = 0.f;
+            for (int j = lane; j < dk; j += 32) s = fmaf(sB[r * kLdD + j], sX[r * kLdD + j], s);
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
+            if (lane == 0) sdg[r] += s;
+        }
+    }
+    // <D, S0> with D read from global against S0 in shared memory
+    const float* Dg = p.Db + ci * dv * dk;
+    float part = 0.f;
+    for (int i = threadIdx.x; i < dv * dk; i += blockDim.x) {
+        const int r = i / dk, j = i - r * dk;
+        part = fmaf(Dg[i], sBig[r * kLdD + j], part);
+    }
+    const float dS = cta_sum(part, red);
+    __syncthreads();
+    // D phase: D into sBig, U into sA, K into sB
+    load_rows_f32(sBig, kLdD, Dg, dk, dv, dv, dk);
+    load_rows_f32(sA, kLdD, p.Ub + ci * kC * dv, dv, kC, kC, dv);
+    load_rows_f32(sB, kLdD, p.kn + ((size_t)t0 * p.HK + hk) * dk, (size_t)p.HK * dk, kC, len, dk);
+    __syncthreads();
+    cta_gemm(kC, dk, dv, sA, kLdD, 1, sBig, kLdD, 1, [&](int r, int j, float x) { sC[r * kLdD + j] = x; });
+    __syncthreads();
+    float* dkk = p.dkh;
+    for (int i = threadIdx.x; i < kC * dk; i += blockDim.x) {
+        const int r = i / dk, j = i - r * dk;
+        if (r < len) dkk[((size_t)(t0 + r) * p.HV + h) * dk + j] = expf(gl - sg[r]) * sC[r * kLdD + j];
+    }
+    __syncthreads();
+    {
+        const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+        for (int r = w; r < len; r += nw) {
+            float s = 0.f;
+            for (int j = lane; j < dk; j += 32) s = fmaf(sB[r * kLdD + j], sC[r * kLdD + j], s);
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
+            if (lane == 0) sX[r] = expf(gl - sg[r]) * s;  // b_s db_s (sX reused as scratch)
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float tot = 0.f;
+        for (int r = 0; r < len; ++r) tot += sX[r];
+        for (int r = 0; r < len; ++r) sdg[r] -= sX[r];
+        sdg[len - 1] += tot + expf(gl) * dS;
+    }
+    __syncthreads();
+    float* dga = p.dgamA + ci * kC;
+    for (int i = threadIdx.x; i < kC; i += blockDim.x) dga[i] = sdg[i];
+}
+
+// per (chunk, head): the C x C part.
+__global__ void __launch_bounds__(kNT) bwd_intra_c_kernel(BwdParams p) {
+    extern __shared__ float sm[];
+    const int c = blockIdx.x, h = blockIdx.y;
+    int n, t0, len;
+    if (!chunk_of(p, c, n, t0, len)) return;
+    const int hk = h / p.G, dk = p.dk, dv = p.dv;
+    float* sK = sm;                    // C x kLdD
+    float* sA = sK + kC * kLdD;        // dO -> dW
+    float* sB = sA + kC * kLdD;        // U -> V
+    float* sCb = sB + kC * kLdD;       // Q -> dU
+    float* s1 = sCb + kC * kLdD;       // QK -> F1 -> dT -> dA -> dKK
+    float* s2 = s1 + kC * kLdC;        // dQK -> F2 -> Z -> KK -> dKK + dKK^T
+    float* sT = s2 + kC * kLdC;        // T
+    float* sE = sT + kC * kLdC;        // dE accumulator
+    float* sg = sE + kC * kLdC;        // gam
+    float* sbe = sg + kC;              // beta
+    float* sdg = sbe + kC;             // dgam
+    float* sdb = sdg + kC;             // dbeta
+    const size_t ci = ch_index(p, c, h);
+    load_rows_f32(sK, kLdD, p.kn + ((size_t)t0 * p.HK + hk) * dk, (size_t)p.HK * dk, kC, len, dk);
+    load_rows_any(sA, kLdD, p.dout, ((size_t)t0 * p.HV + h) * dv, (size_t)p.HV * dv, kC, len, dv, p.dtype);
+    load_rows_f32(sB, kLdD, p.Ub + ci * kC * dv, dv, kC, kC, dv);
+    load_rows_f32(sCb, kLdD, p.qn + ((size_t)t0 * p.HK + hk) * dk, (size_t)p.HK * dk, kC, len, dk);
+    load_rows_f32(s1, kLdC, p.QKb + ci * kC * kC, kC, kC, kC, kC);
+    load_rows_f32(sT, kLdC, p.Tb + ci * kC * kC, kC, kC, kC, kC);
+    const float* dga = p.dgamA + ci * kC;
+    for (int i = threadIdx.x; i < kC; i += blockDim.x) {
+        sg[i] = i < len ? p.gam[(size_t)(t0 + i) * p.HV + h] : 0.f;
+        sbe[i] = i < len ? p.beta[(size_t)(t0 + i) * p.HV + h] : 0.f;
+        sdg[i] = dga[i];
+        sdb[i] = 0.f;
+    }
+    for (int i = threadIdx.x; i < kC * kLdC; i += blockDim.x) sE[i] = 0.f;
+    __syncthreads();
+    // c1: dP = dO U^T -> dQK = lower(dP) * E, dE = lower(dP) * QK
+    cta_gemm(kC, kC, dv, sA, kLdD, 1, sB, 1, kLdD, [&](int r, int s, float x) {
+        const bool in = (s <= r) && (r < len);
+        const float e = in ? expf(sg[r] - sg[s]) : 0.f;
+        s2[r * kLdC + s] = in ? x * e : 0.f;
+        sE[r * kLdC + s] = in ? x * s1[r * kLdC + s] : 0.f;
+    });
+    __syncthreads();
+    float* dq = p.dqh;
+    float* dkk = p.dkh;
+    cta_gemm(kC, dk, kC, s2, kLdC, 1, sK, kLdD, 1, [&](int r, int j, float x) {
+        if (r < len) dq[((size_t)(t0 + r) * p.HV + h) * dk + j] += x;
+    });
+    __syncthreads();
+    cta_gemm(kC, dk, kC, s2, 1, kLdC, sCb, kLdD, 1, [&](int s, int j, float x) {
+        if (s < len) dkk[((size_t)(t0 + s) * p.HV + h) * dk + j] += x;
+    });
+    __syncthreads();
+    // c2: dW -> sA, V -> sB, dU -> sCb
+    load_rows_f32(sA, kLdD, p.Wb + ci * kC * dk, dk, kC, kC, dk);
+    load_rows_any(sB, kLdD, p.v, ((size_t)t0 * p.HV + h) * dv, (size_t)p.HV * dv, kC, len, dv, p.dtype);
+    load_rows_f32(sCb, kLdD, p.dUb + ci * kC * dv, dv, kC, kC, dv);
+    __syncthreads();
+    // F1 = dW K^T, F2 = dU V^T
+    cta_gemm(kC, kC, dk, sA, kLdD, 1, sK, 1, kLdD, [&](int s, int r, float x) { s1[s * kLdC + r] = x; });
+    cta_gemm(kC, kC, dv, sCb, kLdD, 1, sB, 1, kLdD, [&](int s, int r, float x) { s2[s * kLdC + r] = x; });
+    __syncthreads();
+    // column dots with T: dbeta_r, dgam_r; then dT(s,r) = beta_r (Gam_r F1 + F2)
+    if (threadIdx.x < kC) {
+        const int r = threadIdx.x;
+        float a1 = 0.f, a2 = 0.f;
+        for (int s = 0; s < kC; ++s) {
+            a1 = fmaf(sT[s * kLdC + r], s1[s * kLdC + r], a1);
+            a2 = fmaf(sT[s * kLdC + r], s2[s * kLdC + r], a2);
+        }
+        const float Gr = expf(sg[r]);
+        sdb[r] += Gr * a1 + a2;
+        sdg[r] += Gr * sbe[r] * a1;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < kC * kC; i += blockDim.x) {
+        const int s = i / kC, r = i - s * kC;
+        s1[s * kLdC + r] = sbe[r] * fmaf(expf(sg[r]), s1[s * kLdC + r], s2[s * kLdC + r]);
+    }
+    __syncthreads();
+    // dK += diag(beta Gam) T^T dW;  dV = diag(beta) T^T dU
+    cta_gemm(kC, dk, kC, sT, 1, kLdC, sA, kLdD, 1, [&](int r, int j, float x) {
+        if (r < len) dkk[((size_t)(t0 + r) * p.HV + h) * dk + j] += sbe[r] * expf(sg[r]) * x;
+    });
+    cta_gemm(kC, dv, kC, sT, 1, kLdC, sCb, kLdD, 1, [&](int r, int j, float x) {
+        if (r < len) st_any(p.dv_out, ((size_t)(t0 + r) * p.HV + h) * dv + j, p.dtype, sbe[r] * x);
+    });
+    // c4: Z = dT T^T -> s2;  dA = -T^T Z (strictly lower) -> s1
+    cta_gemm(kC, kC, kC, s1, kLdC, 1, sT, 1, kLdC, [&](int a, int b, float x) { s2[a * kLdC + b] = x; });
+    __syncthreads();
+    cta_gemm(kC, kC, kC, sT, 1, kLdC, s2, kLdC, 1,
+             [&](int r, int s, float x) { s1[r * kLdC + s] = (s < r) ? -x : 0.f; });
+    __syncthreads();
+    // c5: KK = K K^T -> s2; dbeta_r += sum_s dA E KK; dKK = dA beta_r E -> s1; dE += dA beta_r KK
+    cta_gemm(kC, kC, dk, sK, kLdD, 1, sK, 1, kLdD, [&](int r, int s, float x) { s2[r * kLdC + s] = x; });
+    __syncthreads();
+    if (threadIdx.x < kC) {
+        const int r = threadIdx.x;
+        float acc = 0.f;
+        for (int s = 0; s < r; ++s) {
+            const float a = s1[r * kLdC + s], e = expf(sg[r] - sg[s]), kk = s2[r * kLdC + s];
+            acc = fmaf(a * e, kk, acc);
+            s1[r * kLdC + s] = a * sbe[r] * e;
+            sE[r * kLdC + s] = fmaf(a * sbe[r], kk, sE[r * kLdC + s]);
+        }
+        sdb[r] += acc;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < kC * kC; i += blockDim.x) {
+        const int r = i / kC, s = i - r * kC;
+        s2[r * kLdC + s] = s1[r * kLdC + s] + s1[s * kLdC + r];
+    }
+    __syncthreads();
+    cta_gemm(kC, dk, kC, s2, kLdC, 1, sK, kLdD, 1, [&](int r, int j, float x) {
+        if (r < len) dkk[((size_t)(t0 + r) * p.HV + h) * dk + j] += x;
+    });
+    // c6: dgam from E (row sums minus column sums of dE * E), then dg = reverse cumsum
+    if (threadIdx.x < kC) {
+        const int r = threadIdx.x;
+        float rs = 0.f, cs = 0.f;
+        for (int s = 0; s < kC; ++s) {
+            rs = fmaf(sE[r * kLdC + s], expf(sg[r] - sg[s]), rs);
+            cs = fmaf(sE[s * kLdC + r], expf(sg[s] - sg[r]), cs);
+        }
+        sdg[r] += rs - cs;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float acc = 0.f;
+        for (int r = len - 1; r >= 0; --r) {
+            acc += sdg[r];
+            p.dg[(size_t)(t0 + r) * p.HV + h] = acc;
+            p.dbeta[(size_t)(t0 + r) * p.HV + h] = sdb[r];
+        }
+    }
+}
+
+// per (token, k-head): sum the G value heads in increasing order, then the L2-norm backward
+__global__ void bwd_fold_kernel(BwdParams p) {
+    const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (w >= p.T * p.HK) return;
+    const int t = w / p.HK, hk = w - t * p.HK;
+    for (int which = 0; which < 2; ++which) {
+        const float* src = which ? p.dkh : p.dqh;
+        const float* xh = (which ? p.kn : p.qn) + (size_t)w * p.dk;
+        float d[4], x[4];
+        float dot = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int j = lane + 32 * i;
+            d[i] = 0.f;
+            x[i] = j < p.dk ? xh[j] : 0.f;
+            if (j < p.dk)
+                for (int hh = hk * p.G; hh < (hk + 1) * p.G; ++hh) d[i] += src[((size_t)t * p.HV + hh) * p.dk + j];
+            dot = fmaf(x[i], d[i], dot);
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) dot += __shfl_xor_sync(kFull, dot, off);
+        const float inv = (which ? p.kinv : p.qinv)[w];
+        void* dst = which ? p.dk_out : p.dq_out;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int j = lane + 32 * i;
+            if (j < p.dk) {
+                const float gval = p.use_norm ? (d[i] - x[i] * dot) * inv : d[i];
+                st_any(dst, (size_t)w * p.dk + j, p.dtype, gval);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+struct BwdLayout {
+    size_t coff, qn, kn, qinv, kinv, gam, W, Ut, T, QK, S, D, U, dU, dgA, dqh, dkh, total;
+    int nchm;
+};
+
+static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static BwdLayout bwd_layout(const gdn_shape* s) {
+    BwdLayout L;
+    const size_t T = s->T_total, HK = s->HK, HV = s->HV, dk = s->dk, dv = s->dv;
+    L.nchm = s->N + (s->T_total + kC - 1) / kC;
+    const size_t CH = (size_t)L.nchm * HV;
+    size_t o = kWsHeader;
+    auto take = [&](size_t bytes) { size_t at = o; o += al256(bytes); return at; };
+    L.coff = take((s->N + 1) * 4);
+    L.qn = take(T * HK * dk * 4);
+    L.kn = take(T * HK * dk * 4);
+    L.qinv = take(T * HK * 4);
+    L.kinv = take(T * HK * 4);
+    L.gam = take(T * HV * 4);
+    L.W = take(CH * kC * dk * 4);
+    L.Ut = take(CH * kC * dv * 4);
+    L.T = take(CH * kC * kC * 4);
+    L.QK = take(CH * kC * kC * 4);
+    L.S = take(CH * dv * dk * 4);
+    L.D = take(CH * dv * dk * 4);
+    L.U = take(CH * kC * dv * 4);
+    L.dU = take(CH * kC * dv * 4);
+    L.dgA = take(CH * kC * 4);
+    L.dqh = take(T * HV * dk * 4);
+    L.dkh = take(T * HV * dk * 4);
+    L.total = o;
+    return L;
+}
+
+size_t bwd_workspace_size(const gdn_shape* s) { return bwd_layout(s).total; }
+
+template <typename K>
+static bool set_smem(K kern, size_t bytes) {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) == cudaSuccess;
+}
+
+}  // namespace gdn
+
+extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const void* k, const void* v,
+                                    const float* g, const float* beta, const float* init_state,
+                                    const int32_t* cu_seqlens, const void* d_out, const float* d_final_state,
+                                    void* dq, void* dk, void* dv, float* dg, float* dbeta, float* d_init_state,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+    using namespace gdn;
+    gdn_status st = check_shape(s);
+    if (st != GDN_OK) return st;
+    if (!cu_seqlens) return GDN_ERR_INVALID_ARG;
+    if (s->N == 0) return GDN_OK;
+    if (s->T_total > 0 && (!q || !k || !v || !g || !beta || !d_out || !dq || !dk || !dv || !dg || !dbeta))
+        return GDN_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, g, beta, init_state, cu_seqlens, d_out, d_final_state, dq, dk, dv, dg, dbeta,
+                          d_init_state, workspace};
+    for (const void* ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return GDN_ERR_INVALID_ARG;
+    const void* outs[] = {dq, dk, dv, dg, dbeta, d_init_state};
+    const void* ins[] = {q, k, v, g, beta, init_state, d_out, d_final_state};
+    for (const void* o : outs)
+        for (const void* i : ins)
+            if (o && o == i) return GDN_ERR_INVALID_ARG;
+    const BwdLayout L = bwd_layout(s);
+    if (!workspace || workspace_bytes < L.total) return GDN_ERR_WORKSPACE;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+
+    BwdParams p;
+    p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.init_state = init_state; p.cu = cu_seqlens;
+    p.dout = d_out; p.dfinal = d_final_state; p.dq_out = dq; p.dk_out = dk; p.dv_out = dv; p.dg = dg; p.dbeta = dbeta;
+    p.dinit = d_init_state;
+    p.err = reinterpret_cast<unsigned*>(ws);
+    p.coff = reinterpret_cast<int32_t*>(ws + L.coff);
+    p.qn = reinterpret_cast<float*>(ws + L.qn);
+    p.kn = reinterpret_cast<float*>(ws + L.kn);
+    p.qinv = reinterpret_cast<float*>(ws + L.qinv);
+    p.kinv = reinterpret_cast<float*>(ws + L.kinv);
+    p.gam = reinterpret_cast<float*>(ws + L.gam);
+    p.Wb = reinterpret_cast<float*>(ws + L.W);
+    p.Utb = reinterpret_cast<float*>(ws + L.Ut);
+    p.Tb = reinterpret_cast<float*>(ws + L.T);
+    p.QKb = reinterpret_cast<float*>(ws + L.QK);
+    p.Sb = reinterpret_cast<float*>(ws + L.S);
+    p.Db = reinterpret_cast<float*>(ws + L.D);
+    p.Ub = reinterpret_cast<float*>(ws + L.U);
+    p.dUb = reinterpret_cast<float*>(ws + L.dU);
+    p.dgamA = reinterpret_cast<float*>(ws + L.dgA);
+    p.dqh = reinterpret_cast<float*>(ws + L.dqh);
+    p.dkh = reinterpret_cast<float*>(ws + L.dkh);
+    p.N = s->N; p.T = s->T_total; p.HK = s->HK; p.HV = s->HV; p.G = s->HV / s->HK; p.dk = s->dk; p.dv = s->dv;
+    p.use_norm = s->use_qk_l2norm ? 1 : 0;
+    p.nchm = L.nchm;
+    p.dtype = s->dtype;
+
+    if (cudaMemsetAsync(ws, 0, sizeof(unsigned), cs) != cudaSuccess) return GDN_ERR_CUDA;
+    bwd_offsets_kernel<<<1, 32, 0, cs>>>(p);
+    if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
+    if (s->T_total > 0) {
+        const int vec = s->T_total * s->HK;
+        bwd_norm_kernel<<<(vec + 7) / 8, 256, 0, cs>>>(p);
+        if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
+    }
+    const dim3 gch(L.nchm, s->HV);
+    const size_t smem_wy = sizeof(float) * (2 * kC * kLdD + 3 * kC * kLdC + 3 * kC);
+    if (!set_smem(bwd_wy_kernel, smem_wy)) return GDN_ERR_CUDA;
+    bwd_wy_kernel<<<gch, kNT, smem_wy, cs>>>(p);
+    if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
+
+    const int R = std::min(kRowsSlice, s->dv);
+    const dim3 gseq(s->N, s->HV, s->dv / R);
+    const size_t smem_sf = sizeof(float) * (R * kLdD + 2 * kC * kLdD + kC * (R + 1) + kC);
+    if (!set_smem(bwd_state_fwd_kernel, smem_sf)) return GDN_ERR_CUDA;
+    bwd_state_fwd_kernel<<<gseq, kNTs, smem_sf, cs>>>(p, R);
+    if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
+    const size_t smem_sb = sizeof(float) * (R * kLdD + 2 * kC * kLdD + kC * kLdC + 2 * kC * (R + 1) + kC);
+    if (!set_smem(bwd_state_bwd_kernel, smem_sb)) return GDN_ERR_CUDA;
+    bwd_state_bwd_kernel<<<gseq, kNTs, smem_sb, cs>>>(p, R);
+    if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
+
+    const size_t smem_is = sizeof(float) * (kMaxD * kLdD + 4 * kC * kLdD + 2 * kC + 32);
+    if (!set_smem(bwd_intra_s_kernel, smem_is)) return GDN_ERR_CUDA;
+    bwd_intra_s_kernel<<<gch, kNT, smem_is, cs>>>(p);
+    if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
+    const size_t smem_ic = sizeof(float) * (4 * kC * kLdD + 4 * kC * kLdC + 4 * kC);
+    if (!set_smem(bwd_intra_c_kernel, smem_ic)) return GDN_ERR_CUDA;
+    bwd_intra_c_kernel<<<gch, kNT, smem_ic, cs>>>(p);
+    if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
+    if (s->T_total > 0) {
+        const int vec = s->T_total * s->HK;
+        bwd_fold_kernel<<<(vec + 7) / 8, 256, 0, cs>>>(p);
+        if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
+    }
+    return GDN_OK;
+}

@@ -1,0 +1,137 @@
+// gdn_decode.cu -- one decode token per sequence on a cached fp32 state.
+//
+// The same recurrent step as the prefill kernel (gdn_step.cuh), applied once
+// to the state the cache holds, so a prompt run by gdn_recurrent_fwd and
+// continued token by token here yields exactly the bits of one pass over the
+// whole sequence ("switch both prefill and decode to the recurrent kernel":
+// "Defending Against the Training-Inference Numeric Mismatch in RL
+// (Especially Linear Attention)", section 3.2).  The state round trip
+// (dv x dk fp32 read and written per (sequence, head)) makes this HBM-bound:
+// each thread issues all of its row loads up front, the q/k normalisation
+// runs while they are in flight, and the new rows are streamed back.
+#include <algorithm>
+
+#include "gdn_host.h"
+#include "gdn_step.cuh"
+
+namespace gdn {
+
+struct DecodeParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* g;
+    const float* beta;
+    float* state;
+    const int32_t* idx;
+    void* out;
+    int N, HK, HV, G, dv, dvs, nslices, num_slots, use_norm;
+};
+
+template <typename Tin, int DK>
+__global__ void __launch_bounds__(128) gdn_decode_kernel(const DecodeParams p) {
+    constexpr int R = 2;
+    __shared__ __align__(16) float qn[DK];
+    __shared__ __align__(16) float kn[DK];
+    __shared__ float2 ab;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+    const int e = tid & 1, pair = tid >> 1;
+    const int dvs = p.dvs;
+    const bool active = 2 * pair < dvs;
+    const int unit = blockIdx.x;
+    const int slice = unit % p.nslices;
+    const int h = (unit / p.nslices) % p.HV;
+    const int b = unit / (p.nslices * p.HV);
+    const int hk = h / p.G;
+    const int slot = p.idx ? p.idx[b] : b;
+    if (slot < 0 || slot >= p.num_slots) return;  // uniform over the CTA
+
+    const int row = slice * dvs + 2 * pair;
+    float* srow = p.state + (((size_t)slot * p.HV + h) * p.dv + row) * DK;
+    RowFrag<DK> S[R];
+    if (active) load_rows<DK, R>(S, srow, e);
+
+    const Tin* q = reinterpret_cast<const Tin*>(p.q) + ((size_t)b * p.HK + hk) * DK;
+    const Tin* k = reinterpret_cast<const Tin*>(p.k) + ((size_t)b * p.HK + hk) * DK;
+    for (int j = warp; j < 2; j += nwarps) {
+        if (j) l2norm_warp<DK>(k, kn, lane, p.use_norm);
+        else l2norm_warp<DK>(q, qn, lane, p.use_norm);
+    }
+    if (tid == 0) {
+        const size_t gi = (size_t)b * p.HV + h;
+        ab = make_float2(gate_alpha(p.g[gi]), p.beta[gi]);
+    }
+    float vv[R] = {0.f, 0.f}, o[R];
+    const size_t vo = ((size_t)b * p.HV + h) * p.dv + row;
+    if (active) {
+        const float2 v2 = ld2_in(reinterpret_cast<const Tin*>(p.v) + vo);
+        vv[0] = v2.x;
+        vv[1] = v2.y;
+    }
+    __syncthreads();
+    const float2 gab = ab;
+    token_step<DK, R>(S, kn, qn, e, gab.x, gab.y, vv, o);
+    if (active) {
+        if (e == 0) st2_out(reinterpret_cast<Tin*>(p.out) + vo, o[0], o[1]);
+        store_rows<DK, R>(S, srow, e);
+    }
+}
+
+template <typename Tin, int DK>
+static gdn_status launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
+    const int units = p.N * p.HV * p.nslices;
+    gdn_decode_kernel<Tin, DK><<<units, std::max(32, p.dvs), 0, stream>>>(p);
+    return launch_status();
+}
+
+template <typename Tin>
+static gdn_status launch_decode_dk(int dk, const DecodeParams& p, cudaStream_t stream) {
+    switch (dk) {
+        case 16: return launch_decode_t<Tin, 16>(p, stream);
+        case 32: return launch_decode_t<Tin, 32>(p, stream);
+        case 64: return launch_decode_t<Tin, 64>(p, stream);
+        case 128: return launch_decode_t<Tin, 128>(p, stream);
+    }
+    return GDN_ERR_UNSUPPORTED;
+}
+
+}  // namespace gdn
+
+extern "C" gdn_status gdn_decode_step(const gdn_shape* s, const void* q, const void* k, const void* v,
+                                      const float* g, const float* beta, float* state,
+                                      const int32_t* state_indices, int num_slots, void* out, void* stream) {
+    using namespace gdn;
+    gdn_status st = check_shape(s);
+    if (st != GDN_OK) return st;
+    if (s->T_total != s->N) return GDN_ERR_INVALID_ARG;
+    if (s->N == 0) return GDN_OK;
+    if (!q || !k || !v || !g || !beta || !state || !out || num_slots <= 0) return GDN_ERR_INVALID_ARG;
+    if (!state_indices && num_slots < s->N) return GDN_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, g, beta, state, state_indices, out};
+    for (const void* ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return GDN_ERR_INVALID_ARG;
+    if (out == q || out == k || out == v || out == state) return GDN_ERR_INVALID_ARG;
+
+    DecodeParams p;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.g = g;
+    p.beta = beta;
+    p.state = state;
+    p.idx = state_indices;
+    p.out = out;
+    p.N = s->N;
+    p.HK = s->HK;
+    p.HV = s->HV;
+    p.G = s->HV / s->HK;
+    p.dv = s->dv;
+    p.dvs = pick_dv_slice(s);
+    p.nslices = s->dv / p.dvs;
+    p.num_slots = num_slots;
+    p.use_norm = s->use_qk_l2norm ? 1 : 0;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (s->dtype == GDN_BF16) return launch_decode_dk<__nv_bfloat16>(s->dk, p, cs);
+    return launch_decode_dk<float>(s->dk, p, cs);
+}

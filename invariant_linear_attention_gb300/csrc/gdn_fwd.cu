@@ -1,0 +1,295 @@
+// gdn_fwd.cu -- varlen scheduler + batch-invariant recurrent forward.
+//
+// One CTA owns one unit (sequence n, value head h, slice of dv rows) for the
+// whole sequence: its rows of the fp32 state S stay in registers from the
+// first token to the last, so there is no state hand-off between CTAs and
+// nothing is reduced across sequences or split over dk ("the recurrent kernel
+// reads only that sequence's own state and walks that sequence's tokens in a
+// fixed order": "Defending Against the Training-Inference Numeric Mismatch in
+// RL (Especially Linear Attention)", section 3.2).
+//
+// Per chunk of TC tokens, thread 0 streams q/k (k-head hk) and the v slice
+// with three TMA tensor copies into a double-buffered shared-memory stage.
+// The CTA then L2-normalises q and k (one warp per vector, fixed butterfly),
+// computes a = exp(g), and every thread walks the chunk's tokens over its
+// two rows with the shared step of gdn_step.cuh.  Outputs go straight from
+// registers to global memory.
+#include <algorithm>
+
+#include "gdn_async.cuh"
+#include "gdn_host.h"
+#include "gdn_step.cuh"
+
+namespace gdn {
+
+constexpr int kTC = 16;      // tokens per chunk
+constexpr int kStages = 2;   // TMA stages
+constexpr int kRowsPerThread = 2;
+constexpr int kMaxSlice = 128;
+
+struct FwdParams {
+    const float* g;
+    const float* beta;
+    const float* init_state;
+    const int32_t* cu;
+    void* out;
+    float* final_state;
+    const int32_t* work;
+    unsigned* err;
+    int N, T, HV, G, dv, dvs, nslices, use_norm;
+    int tb;  // tokens per TMA box: min(kTC, T)
+};
+
+template <typename Tin, int DK>
+struct alignas(128) FwdSmem {
+    Tin q[kStages][kTC * DK];
+    Tin k[kStages][kTC * DK];
+    Tin v[kStages][kTC * kMaxSlice];
+    float qn[kTC * DK];
+    float kn[kTC * DK];
+    float2 ab[kTC];
+    uint64_t bar[kStages];
+    int abort_flag;
+};
+
+// ---------------------------------------------------------------------------
+// Varlen scheduler: rank every sequence by length (longest first, ties by
+// index: a stable order), then emit its units (n, h, slice) in that order.
+// Launch order only decides which SM runs a unit when; it never changes a bit.
+// Also validates cu_seqlens and flags GDN_DEVERR_CU_SEQLENS in the error word.
+__global__ void gdn_sched_kernel(const int32_t* __restrict__ cu, int N, int T, int HV, int nslices,
+                                 int32_t* __restrict__ work, unsigned* __restrict__ err) {
+    constexpr int kTile = 1024;
+    __shared__ int lens[kTile];
+    const int n = blockIdx.x * blockDim.x + threadIdx.x;
+    int my_len = 0;
+    if (n < N) {
+        const int a = cu[n], b = cu[n + 1];
+        if ((n == 0 && a != 0) || b < a || (n == N - 1 && b != T)) atomicOr(err, GDN_DEVERR_CU_SEQLENS);
+        const int lo = min(max(a, 0), T), hi = min(max(b, lo), T);
+        my_len = hi - lo;
+    }
+    int rank = 0;
+    for (int base = 0; base < N; base += kTile) {
+        __syncthreads();
+        for (int i = threadIdx.x; i < kTile && base + i < N; i += blockDim.x) {
+            const int a = cu[base + i], b = cu[base + i + 1];
+            const int lo = min(max(a, 0), T), hi = min(max(b, lo), T);
+            lens[i] = hi - lo;
+        }
+        __syncthreads();
+        if (n < N) {
+            const int cnt = min(kTile, N - base);
+            for (int i = 0; i < cnt; ++i) {
+                const int lm = lens[i], m = base + i;
+                rank += (lm > my_len) || (lm == my_len && m < n);
+            }
+        }
+    }
+    if (n < N) {
+        for (int h = 0; h < HV; ++h)
+            for (int s = 0; s < nslices; ++s)
+                work[((size_t)rank * HV + h) * nslices + s] = (n * HV + h) * nslices + s;
+    }
+}
+
+// ---------------------------------------------------------------------------
+template <typename Tin, int DK>
+__global__ void __launch_bounds__(128)
+    gdn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+    constexpr int R = kRowsPerThread;
+    extern __shared__ unsigned char smem_raw[];
+    FwdSmem<Tin, DK>& sm =
+        *reinterpret_cast<FwdSmem<Tin, DK>*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+    const int e = tid & 1, pair = tid >> 1;
+    const int dvs = p.dvs;
+    const bool active = 2 * pair < dvs;
+
+    const int unit = p.work[blockIdx.x];
+    const int slice = unit % p.nslices;
+    const int h = (unit / p.nslices) % p.HV;
+    const int n = unit / (p.nslices * p.HV);
+    const int hk = h / p.G;
+    int bos = p.cu[n], eos = p.cu[n + 1];
+    bos = min(max(bos, 0), p.T);
+    eos = min(max(eos, bos), p.T);
+    const int L = eos - bos;
+    const int row = slice * dvs + 2 * pair;  // first of this thread's rows
+    const size_t soff = (((size_t)n * p.HV + h) * p.dv + row) * DK;
+
+    RowFrag<DK> S[R];
+    if (active && p.init_state) load_rows<DK, R>(S, p.init_state + soff, e);
+    else zero_rows<DK, R>(S);
+
+    if (L > 0) {
+        const int nchunks = (L + kTC - 1) / kTC;
+        const uint32_t bytes = (uint32_t)((2 * p.tb * DK + p.tb * dvs) * sizeof(Tin));
+        auto issue = [&](int c) {
+            const int st = c % kStages, t0 = bos + c * kTC;
+            mbar_arrive_expect_tx(&sm.bar[st], bytes);
+            tma_load_3d(sm.q[st], &tm_q, &sm.bar[st], 0, hk, t0);
+            tma_load_3d(sm.k[st], &tm_k, &sm.bar[st], 0, hk, t0);
+            tma_load_3d(sm.v[st], &tm_v, &sm.bar[st], slice * dvs, h, t0);
+        };
+        if (tid == 0) {
+            for (int s = 0; s < kStages; ++s) mbar_init(&sm.bar[s], 1);
+            sm.abort_flag = 0;
+            fence_barrier_init();
+        }
+        __syncthreads();
+        if (tid == 0)
+            for (int c = 0; c < min(kStages, nchunks); ++c) issue(c);
+
+        // gate inputs of the next chunk, prefetched into registers one chunk ahead
+        float2 gb = make_float2(0.f, 0.f);
+        if (tid < min(kTC, L)) {
+            const size_t gi = (size_t)(bos + tid) * p.HV + h;
+            gb = make_float2(p.g[gi], p.beta[gi]);
+        }
+        Tin* __restrict__ out = reinterpret_cast<Tin*>(p.out);
+
+        for (int c = 0; c < nchunks; ++c) {
+            const int st = c % kStages;
+            const int t0 = bos + c * kTC;
+            const int tc = min(kTC, eos - t0);
+            if (!mbar_wait_bounded(&sm.bar[st], (uint32_t)((c / kStages) & 1))) sm.abort_flag = 1;
+            for (int j = warp; j < 2 * tc; j += nwarps) {
+                const int t = j >> 1;
+                if (j & 1) l2norm_warp<DK>(sm.k[st] + t * DK, sm.kn + t * DK, lane, p.use_norm);
+                else l2norm_warp<DK>(sm.q[st] + t * DK, sm.qn + t * DK, lane, p.use_norm);
+            }
+            if (tid < tc) sm.ab[tid] = make_float2(gate_alpha(gb.x), gb.y);
+            __syncthreads();
+            if (sm.abort_flag) {
+                if (tid == 0) atomicOr(p.err, GDN_DEVERR_TIMEOUT);
+                return;
+            }
+            if (c + 1 < nchunks && tid < min(kTC, eos - (t0 + kTC))) {
+                const size_t gi = (size_t)(t0 + kTC + tid) * p.HV + h;
+                gb = make_float2(p.g[gi], p.beta[gi]);
+            }
+            const Tin* __restrict__ vs = sm.v[st];
+            for (int t = 0; t < tc; ++t) {
+                const float2 ab = sm.ab[t];
+                float vv[R], o[R];
+                const float2 v2 = active ? ld2_in(vs + t * dvs + 2 * pair) : make_float2(0.f, 0.f);
+                vv[0] = v2.x;
+                vv[1] = v2.y;
+                token_step<DK, R>(S, sm.kn + t * DK, sm.qn + t * DK, e, ab.x, ab.y, vv, o);
+                if (active && e == 0) st2_out(out + ((size_t)(t0 + t) * p.HV + h) * p.dv + row, o[0], o[1]);
+            }
+            __syncthreads();
+            if (tid == 0 && c + kStages < nchunks) issue(c + kStages);
+        }
+    }
+    if (active && p.final_state) store_rows<DK, R>(S, p.final_state + soff, e);
+}
+
+template <typename Tin, int DK>
+static gdn_status launch_fwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                               const FwdParams& p, int units, cudaStream_t stream) {
+    const size_t smem = sizeof(FwdSmem<Tin, DK>) + 128;
+    auto kern = gdn_fwd_kernel<Tin, DK>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    const int nt = std::max(32, p.dvs);
+    kern<<<units, nt, smem, stream>>>(mq, mk, mv, p);
+    return launch_status();
+}
+
+template <typename Tin>
+static gdn_status launch_fwd_dk(int dk, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                                const FwdParams& p, int units, cudaStream_t stream) {
+    switch (dk) {
+        case 16: return launch_fwd_t<Tin, 16>(mq, mk, mv, p, units, stream);
+        case 32: return launch_fwd_t<Tin, 32>(mq, mk, mv, p, units, stream);
+        case 64: return launch_fwd_t<Tin, 64>(mq, mk, mv, p, units, stream);
+        case 128: return launch_fwd_t<Tin, 128>(mq, mk, mv, p, units, stream);
+    }
+    return GDN_ERR_UNSUPPORTED;
+}
+
+size_t fwd_workspace_size(const gdn_shape* s) {
+    const int dvs = pick_dv_slice(s);
+    return kWsHeader + (((size_t)s->N * s->HV * (s->dv / dvs) * sizeof(int32_t) + 255) & ~size_t(255));
+}
+
+// Shared by the allocating entry point and any caller that supplies the
+// work-list and error-word buffers itself.
+gdn_status run_recurrent_fwd(const gdn_shape* s, const void* q, const void* k, const void* v, const float* g,
+                             const float* beta, const float* init_state, const int32_t* cu, void* out,
+                             float* final_state, int32_t* work, unsigned* err, cudaStream_t stream) {
+    const int dvs = pick_dv_slice(s);
+    const int nslices = s->dv / dvs;
+    const int units = s->N * s->HV * nslices;
+    if (s->N == 0) return GDN_OK;
+
+    CUtensorMap mq{}, mk{}, mv{};
+    if (s->T_total > 0) {
+        gdn_status st;
+        // box height min(kTC, T): a sequence shorter than kTC never needs more rows than T
+        const uint32_t tb = (uint32_t)std::min(kTC, s->T_total);
+        if ((st = encode_map_3d(&mq, q, s->dtype, s->dk, s->HK, s->T_total, s->dk, tb)) != GDN_OK) return st;
+        if ((st = encode_map_3d(&mk, k, s->dtype, s->dk, s->HK, s->T_total, s->dk, tb)) != GDN_OK) return st;
+        if ((st = encode_map_3d(&mv, v, s->dtype, s->dv, s->HV, s->T_total, dvs, tb)) != GDN_OK) return st;
+    }
+    if (cudaMemsetAsync(err, 0, sizeof(unsigned), stream) != cudaSuccess) return GDN_ERR_CUDA;
+    gdn_sched_kernel<<<(s->N + 255) / 256, 256, 0, stream>>>(cu, s->N, s->T_total, s->HV, nslices, work, err);
+    if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
+
+    FwdParams p;
+    p.g = g;
+    p.beta = beta;
+    p.init_state = init_state;
+    p.cu = cu;
+    p.out = out;
+    p.final_state = final_state;
+    p.work = work;
+    p.err = err;
+    p.N = s->N;
+    p.T = s->T_total;
+    p.HV = s->HV;
+    p.G = s->HV / s->HK;
+    p.dv = s->dv;
+    p.dvs = dvs;
+    p.nslices = nslices;
+    p.use_norm = s->use_qk_l2norm ? 1 : 0;
+    p.tb = std::min(kTC, s->T_total);
+    if (s->dtype == GDN_BF16) return launch_fwd_dk<__nv_bfloat16>(s->dk, mq, mk, mv, p, units, stream);
+    return launch_fwd_dk<float>(s->dk, mq, mk, mv, p, units, stream);
+}
+
+gdn_status check_fwd_args(const gdn_shape* s, const void* q, const void* k, const void* v, const float* g,
+                          const float* beta, const float* init_state, const int32_t* cu, const void* out,
+                          const float* final_state) {
+    gdn_status st = check_shape(s);
+    if (st != GDN_OK) return st;
+    if (!cu) return GDN_ERR_INVALID_ARG;
+    if (s->T_total > 0 && (!q || !k || !v || !g || !beta || !out)) return GDN_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, g, beta, init_state, cu, out, final_state};
+    for (const void* ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return GDN_ERR_INVALID_ARG;
+    // out must not alias an input it is computed from
+    if (out && (out == q || out == k || out == v)) return GDN_ERR_INVALID_ARG;
+    return GDN_OK;
+}
+
+}  // namespace gdn
+
+extern "C" gdn_status gdn_recurrent_fwd(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                                        const float* g, const float* beta, const float* init_state,
+                                        const int32_t* cu_seqlens, void* out, float* final_state,
+                                        void* workspace, size_t workspace_bytes, void* stream) {
+    using namespace gdn;
+    gdn_status st = check_fwd_args(shape, q, k, v, g, beta, init_state, cu_seqlens, out, final_state);
+    if (st != GDN_OK) return st;
+    if (shape->N == 0) return GDN_OK;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < fwd_workspace_size(shape)) return GDN_ERR_WORKSPACE;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    return run_recurrent_fwd(shape, q, k, v, g, beta, init_state, cu_seqlens, out, final_state,
+                             reinterpret_cast<int32_t*>(ws + kWsHeader), reinterpret_cast<unsigned*>(ws),
+                             static_cast<cudaStream_t>(stream));
+}

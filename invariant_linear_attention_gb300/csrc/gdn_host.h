@@ -1,0 +1,45 @@
+// gdn_host.h -- host-side helpers shared by the entry points: argument
+// validation, tensor-map encoding, device error word.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/gdn.h"
+
+namespace gdn {
+
+// Workspace header: one 32-bit device error word, padded to 256 bytes.
+constexpr size_t kWsHeader = 256;
+
+inline bool dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t elem_size(gdn_dtype t) { return t == GDN_BF16 ? 2 : 4; }
+
+// Basic shape check common to every op.
+inline gdn_status check_shape(const gdn_shape* s) {
+    if (!s) return GDN_ERR_INVALID_ARG;
+    if (s->N < 0 || s->T_total < 0 || s->HK <= 0 || s->HV <= 0 || s->HV % s->HK) return GDN_ERR_INVALID_ARG;
+    if (s->dtype != GDN_F32 && s->dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+    if (!dim_ok(s->dk) || !dim_ok(s->dv)) return GDN_ERR_UNSUPPORTED;
+    if (s->dv_slice != 0 && (!dim_ok(s->dv_slice) || s->dv_slice > s->dv)) return GDN_ERR_UNSUPPORTED;
+    // element counts must fit the 32-bit token/head index arithmetic used on the device
+    if ((long long)s->T_total * s->HV * (s->dk > s->dv ? s->dk : s->dv) >= (1LL << 40)) return GDN_ERR_UNSUPPORTED;
+    if ((long long)s->N * s->HV * (s->dv / 16) >= (1LL << 31)) return GDN_ERR_UNSUPPORTED;
+    return GDN_OK;
+}
+
+// Rows of S per CTA.  Automatic choice: the whole head (dv <= 128).
+inline int pick_dv_slice(const gdn_shape* s) { return s->dv_slice ? s->dv_slice : s->dv; }
+
+// Encode a rank-3 tiled tensor map over a [d2][d1][d0] row-major tensor with box {b0, 1, b2}.
+gdn_status encode_map_3d(CUtensorMap* map, const void* base, gdn_dtype dt, uint64_t d0, uint64_t d1, uint64_t d2,
+                         uint32_t b0, uint32_t b2);
+
+inline gdn_status launch_status() {
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace gdn

@@ -1,0 +1,205 @@
+// gdn_step.cuh -- the per-row token step shared by every forward-direction
+// kernel (recurrent prefill/trainer forward and the decode step).
+//
+// Bit-invariance rests on this file: every kernel that advances a state row
+// does it with exactly these IEEE operations in exactly this order, so the
+// bits of a row depend only on that row's inputs.  Rows of S never interact
+// in the gated delta rule (u_i = S_i . k^ and o_i = S_i . q^ involve row i
+// only), so how rows are spread over threads, warps and CTAs is free; the
+// lane->dk mapping, the in-lane summation order and the butterfly are not.
+//
+// Layout of one state row (dk fp32 values) over a lane pair: row r lives in
+// lanes 2p and 2p+1 of a warp; lane parity e holds the float4 chunks
+// c = 2i + e, i = 0 .. dk/8-1 (chunk c = elements 4c .. 4c+3).  A dk
+// contraction is: four per-component fma chains over i in increasing order
+// (starting from +0), then (x + y) + (z + w), then one xor-1 shuffle add.
+// All arithmetic uses explicit round-to-nearest intrinsics so no FMA
+// contraction or reassociation can differ between kernels.
+//
+// The recurrence (gated delta rule, recurrent form as in "Defending Against
+// the Training-Inference Numeric Mismatch in RL (Especially Linear
+// Attention)", section 3.2):
+//     u = S k^,  w = b (v - a u),  S <- a S + w k^T,  o = S q^
+// which equals S <- a S (I - b k^ k^T) + b v k^T with o read after the update.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+
+constexpr float kNormEps = 1e-6f;
+constexpr unsigned kFull = 0xffffffffu;
+
+template <int DK>
+struct RowFrag {
+    static_assert(DK % 8 == 0, "dk must be a multiple of 8");
+    float4 c[DK / 8];
+};
+
+__device__ __forceinline__ float ld_in(const float* p) { return *p; }
+__device__ __forceinline__ float ld_in(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
+// Four consecutive input elements widened to fp32 (pointer 8-byte aligned for bf16,
+// 16-byte aligned for fp32).
+__device__ __forceinline__ float4 ld4_in(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 ld4_in(const __nv_bfloat16* p) {
+    uint2 raw = *reinterpret_cast<const uint2*>(p);
+    __nv_bfloat162 lo = *reinterpret_cast<__nv_bfloat162*>(&raw.x);
+    __nv_bfloat162 hi = *reinterpret_cast<__nv_bfloat162*>(&raw.y);
+    float2 a = __bfloat1622float2(lo), b = __bfloat1622float2(hi);
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// Two adjacent values (rows 2p, 2p+1) of v widened to fp32.
+__device__ __forceinline__ float2 ld2_in(const float* p) { return *reinterpret_cast<const float2*>(p); }
+__device__ __forceinline__ float2 ld2_in(const __nv_bfloat16* p) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+
+// Store two adjacent outputs (rows 2p, 2p+1), rounding to nearest for bf16.
+__device__ __forceinline__ void st2_out(float* p, float a, float b) {
+    *reinterpret_cast<float2*>(p) = make_float2(a, b);
+}
+__device__ __forceinline__ void st2_out(__nv_bfloat16* p, float a, float b) {
+    *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(a, b);
+}
+
+// L2-normalise one dk vector with one full warp: lane l owns elements
+// 4l .. 4l+3 (lanes l >= dk/4 own nothing and contribute +0).  Sum of squares
+// in-lane as ((x*x + y*y) + z*z) + w*w via fma, then an xor butterfly over
+// offsets 16, 8, 4, 2, 1 (every lane ends with the same bits), then
+// x * (1 / sqrt(ss + eps)) with a correctly rounded reciprocal square root.
+// Writes the fp32 result to dst (16-byte aligned).  Must be called by all 32
+// lanes of the warp.
+template <int DK, typename Tin>
+__device__ __forceinline__ void l2norm_warp(const Tin* __restrict__ src, float* __restrict__ dst,
+                                            int lane, bool use_norm) {
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    const bool own = lane < DK / 4;
+    if (own) x = ld4_in(src + 4 * lane);
+    if (use_norm) {
+        float ss = __fmul_rn(x.x, x.x);
+        ss = __fmaf_rn(x.y, x.y, ss);
+        ss = __fmaf_rn(x.z, x.z, ss);
+        ss = __fmaf_rn(x.w, x.w, ss);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(kFull, ss, off));
+        const float inv = __frsqrt_rn(__fadd_rn(ss, kNormEps));
+        x.x = __fmul_rn(x.x, inv);
+        x.y = __fmul_rn(x.y, inv);
+        x.z = __fmul_rn(x.z, inv);
+        x.w = __fmul_rn(x.w, inv);
+    }
+    if (own) *reinterpret_cast<float4*>(dst + 4 * lane) = x;
+}
+
+// Gate values for one token: a = exp(g) (CUDA's expf, same call everywhere), b as given.
+__device__ __forceinline__ float gate_alpha(float g) { return expf(g); }
+
+// Pair-level finish of a dk contraction: (x + y) + (z + w), then + partner lane.
+__device__ __forceinline__ float finish_dot(float ax, float ay, float az, float aw) {
+    const float p = __fadd_rn(__fadd_rn(ax, ay), __fadd_rn(az, aw));
+    return __fadd_rn(p, __shfl_xor_sync(kFull, p, 1));
+}
+
+// u[r] = S_r . x for the R rows a thread holds; x is a dk fp32 vector in shared memory.
+// Must be called by all 32 lanes of the warp.
+template <int DK, int R>
+__device__ __forceinline__ void rows_dot(const RowFrag<DK> (&s)[R], const float* __restrict__ x,
+                                         int e, float (&u)[R]) {
+    float ax[R], ay[R], az[R], aw[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) ax[r] = ay[r] = az[r] = aw[r] = 0.f;
+#pragma unroll
+    for (int i = 0; i < DK / 8; ++i) {
+        const float4 k4 = *reinterpret_cast<const float4*>(x + 4 * (2 * i + e));
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            ax[r] = __fmaf_rn(s[r].c[i].x, k4.x, ax[r]);
+            ay[r] = __fmaf_rn(s[r].c[i].y, k4.y, ay[r]);
+            az[r] = __fmaf_rn(s[r].c[i].z, k4.z, az[r]);
+            aw[r] = __fmaf_rn(s[r].c[i].w, k4.w, aw[r]);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) u[r] = finish_dot(ax[r], ay[r], az[r], aw[r]);
+}
+
+// w = b (v - a u)
+__device__ __forceinline__ float delta_w(float a, float b, float v, float u) {
+    return __fmul_rn(b, __fsub_rn(v, __fmul_rn(a, u)));
+}
+
+// S_r <- a S_r + w_r k^T (per element fma(w, k_j, a * S_rj)), then o[r] = S_r . q.
+// Must be called by all 32 lanes of the warp.
+template <int DK, int R>
+__device__ __forceinline__ void rows_update_out(RowFrag<DK> (&s)[R], const float* __restrict__ k,
+                                                const float* __restrict__ q, int e, float a,
+                                                const float (&w)[R], float (&o)[R]) {
+    float ox[R], oy[R], oz[R], ow[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) ox[r] = oy[r] = oz[r] = ow[r] = 0.f;
+#pragma unroll
+    for (int i = 0; i < DK / 8; ++i) {
+        const float4 k4 = *reinterpret_cast<const float4*>(k + 4 * (2 * i + e));
+        const float4 q4 = *reinterpret_cast<const float4*>(q + 4 * (2 * i + e));
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float4& S = s[r].c[i];
+            S.x = __fmaf_rn(w[r], k4.x, __fmul_rn(a, S.x));
+            S.y = __fmaf_rn(w[r], k4.y, __fmul_rn(a, S.y));
+            S.z = __fmaf_rn(w[r], k4.z, __fmul_rn(a, S.z));
+            S.w = __fmaf_rn(w[r], k4.w, __fmul_rn(a, S.w));
+            ox[r] = __fmaf_rn(S.x, q4.x, ox[r]);
+            oy[r] = __fmaf_rn(S.y, q4.y, oy[r]);
+            oz[r] = __fmaf_rn(S.z, q4.z, oz[r]);
+            ow[r] = __fmaf_rn(S.w, q4.w, ow[r]);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) o[r] = finish_dot(ox[r], oy[r], oz[r], ow[r]);
+}
+
+// One full token for the R rows of a thread: u, w, update, o.
+template <int DK, int R>
+__device__ __forceinline__ void token_step(RowFrag<DK> (&s)[R], const float* __restrict__ kn,
+                                           const float* __restrict__ qn, int e, float a, float b,
+                                           const float (&v)[R], float (&o)[R]) {
+    float u[R], w[R];
+    rows_dot<DK, R>(s, kn, e, u);
+#pragma unroll
+    for (int r = 0; r < R; ++r) w[r] = delta_w(a, b, v[r], u[r]);
+    rows_update_out<DK, R>(s, kn, qn, e, a, w, o);
+}
+
+// Global <-> register transfer of the R rows a thread holds.  row0 points at
+// the first row (row stride dk floats); rows r = 0..R-1 are consecutive.
+template <int DK, int R>
+__device__ __forceinline__ void load_rows(RowFrag<DK> (&s)[R], const float* __restrict__ row0, int e) {
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int i = 0; i < DK / 8; ++i)
+            s[r].c[i] = __ldcs(reinterpret_cast<const float4*>(row0 + (size_t)r * DK + 4 * (2 * i + e)));
+}
+
+template <int DK, int R>
+__device__ __forceinline__ void zero_rows(RowFrag<DK> (&s)[R]) {
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int i = 0; i < DK / 8; ++i) s[r].c[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+template <int DK, int R>
+__device__ __forceinline__ void store_rows(const RowFrag<DK> (&s)[R], float* __restrict__ row0, int e) {
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int i = 0; i < DK / 8; ++i)
+            __stcs(reinterpret_cast<float4*>(row0 + (size_t)r * DK + 4 * (2 * i + e)), s[r].c[i]);
+}
+
+}  // namespace gdn

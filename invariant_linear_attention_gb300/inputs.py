@@ -2,8 +2,9 @@
 
 This module is the ONE thing the CUDA path and the fp64 oracle share: it only
 draws random numbers and shapes them; it holds none of the recurrence's
-arithmetic.  Every tensor is drawn in fp32 on the host with a seeded
-``torch.Generator`` and then cast, so both sides see identical values.
+arithmetic.  Every tensor is drawn in fp32 with a seeded ``torch.Generator``
+(on the host, or on the GPU for multi-GB workloads) and then cast; the oracle
+receives a host copy of exactly the values the kernels read.
 
 Recipe (the pages run RL on named datasets; these synthetic tensors stand in
 for the activations a GDN layer receives there):
@@ -43,16 +44,23 @@ class GDNInputs:
         HV, dv = self.v.shape[1], self.v.shape[2]
         return dict(N=len(self.lengths), T=T, HK=HK, HV=HV, dk=dk, dv=dv)
 
+    def cpu(self):
+        return self.to("cpu")
+
     def to(self, device):
         mv = lambda t: None if t is None else t.to(device)  # noqa: E731
         return GDNInputs(mv(self.q), mv(self.k), mv(self.v), mv(self.g), mv(self.beta),
                          mv(self.cu_seqlens), mv(self.init_state), list(self.lengths))
 
 
-def _gen(seed: int) -> torch.Generator:
-    g = torch.Generator(device="cpu")
+def _gen(seed: int, device="cpu") -> torch.Generator:
+    g = torch.Generator(device=device)
     g.manual_seed(int(seed))
     return g
+
+
+def _randn(shape, gen, device):
+    return torch.empty(shape, dtype=torch.float32, device=device).normal_(generator=gen)
 
 
 def cu_from_lengths(lengths: Sequence[int]) -> torch.Tensor:
@@ -81,25 +89,31 @@ def _unit_rows(x: torch.Tensor) -> torch.Tensor:
 
 def make_inputs(lengths: Sequence[int], HK: int, HV: int, dk: int, dv: int,
                 dtype=torch.bfloat16, seed: int = 0, init_scale: Optional[float] = None,
-                normalise_qk: bool = True) -> GDNInputs:
-    """Packed varlen inputs for ``len(lengths)`` sequences (see module doc)."""
-    gen = _gen(seed)
+                normalise_qk: bool = True, device="cpu") -> GDNInputs:
+    """Packed varlen inputs for ``len(lengths)`` sequences (see module doc).
+
+    ``device`` picks where the seeded generator draws (a CUDA generator is
+    much faster for multi-GB workloads); the values for a given seed depend
+    on the device type, and both sides of a comparison must use one draw.
+    """
+    gen = _gen(seed, device)
     T = int(sum(lengths))
-    q = torch.randn(T, HK, dk, generator=gen)
-    k = torch.randn(T, HK, dk, generator=gen)
+    q = _randn((T, HK, dk), gen, device)
+    k = _randn((T, HK, dk), gen, device)
     if normalise_qk:
         q, k = _unit_rows(q), _unit_rows(k)
-    v = torch.randn(T, HV, dv, generator=gen)
-    b = torch.randn(T, HV, generator=gen)
-    g = -torch.nn.functional.softplus(torch.randn(T, HV, generator=gen))
+    q, k = q.to(dtype).contiguous(), k.to(dtype).contiguous()
+    v = _randn((T, HV, dv), gen, device).to(dtype).contiguous()
+    b = _randn((T, HV), gen, device)
+    g = -torch.nn.functional.softplus(_randn((T, HV), gen, device))
     beta = torch.sigmoid(b)
     s0 = None
     if init_scale is not None:
         N = len(lengths)
-        s0 = (torch.randn(N, HV, dv, dk, generator=gen) * init_scale) if init_scale else \
-            torch.zeros(N, HV, dv, dk)
-    return GDNInputs(q.to(dtype).contiguous(), k.to(dtype).contiguous(), v.to(dtype).contiguous(),
-                     g.contiguous(), beta.contiguous(), cu_from_lengths(lengths), s0, list(lengths))
+        s0 = (_randn((N, HV, dv, dk), gen, device) * init_scale) if init_scale else \
+            torch.zeros(N, HV, dv, dk, device=device)
+    return GDNInputs(q, k, v, g.contiguous(), beta.contiguous(), cu_from_lengths(lengths).to(device), s0,
+                     list(lengths))
 
 
 def concat(parts: Sequence[GDNInputs]) -> GDNInputs:
@@ -109,10 +123,11 @@ def concat(parts: Sequence[GDNInputs]) -> GDNInputs:
     s0 = None
     if any(p.init_state is not None for p in parts):
         s0 = torch.cat([p.init_state if p.init_state is not None else
-                        torch.zeros(len(p.lengths), *parts[0].v.shape[1:], parts[0].q.shape[2])
+                        torch.zeros(len(p.lengths), *parts[0].v.shape[1:], parts[0].q.shape[2],
+                                    device=parts[0].q.device)
                         for p in parts], 0)
-    return GDNInputs(cat("q"), cat("k"), cat("v"), cat("g"), cat("beta"), cu_from_lengths(lengths),
-                     s0, lengths)
+    return GDNInputs(cat("q"), cat("k"), cat("v"), cat("g"), cat("beta"),
+                     cu_from_lengths(lengths).to(parts[0].q.device), s0, lengths)
 
 
 def tiny_config(seed: int = 0) -> GDNInputs:
@@ -121,11 +136,12 @@ def tiny_config(seed: int = 0) -> GDNInputs:
                        init_scale=0.0)
 
 
-def grad_out(T: int, HV: int, dv: int, dtype=torch.bfloat16, seed: int = 6) -> torch.Tensor:
+def grad_out(T: int, HV: int, dv: int, dtype=torch.bfloat16, seed: int = 6, device="cpu") -> torch.Tensor:
     """Upstream gradient dO ~ randn [T, HV, dv]."""
-    return torch.randn(T, HV, dv, generator=_gen(seed)).to(dtype).contiguous()
+    return _randn((T, HV, dv), _gen(seed, device), device).to(dtype).contiguous()
 
 
-def random_states(N: int, HV: int, dv: int, dk: int, seed: int, scale: float = 1.0) -> torch.Tensor:
+def random_states(N: int, HV: int, dv: int, dk: int, seed: int, scale: float = 1.0,
+                  device="cpu") -> torch.Tensor:
     """fp32 states ~ randn * scale, layout [N, HV, dv, dk]."""
-    return (torch.randn(N, HV, dv, dk, generator=_gen(seed)) * scale).contiguous()
+    return (_randn((N, HV, dv, dk), _gen(seed, device), device) * scale).contiguous()

@@ -1,0 +1,112 @@
+"""CPU-only checks of the C ABI: the library loads, exports every function
+include/gdn.h declares, and rejects bad arguments on the host (these calls
+return before any CUDA call, so no GPU is needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import invariant_linear_attention_gb300 as gdn
+from invariant_linear_attention_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from invariant_linear_attention_gb300 import build_lib
+    build_lib.build()
+    return gdn.lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"gdn_recurrent_fwd", "gdn_decode_step", "gdn_chunk_bwd", "gdn_workspace_size"} <= set(names)
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in gdn.h but not exported"
+    assert set(binding.SYMBOLS) == set(names)
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4):
+        assert gdn.status_string(code).startswith("GDN_")
+
+
+def shape(**kw):
+    base = dict(N=2, T_total=10, HK=2, HV=4, dk=128, dv=128, dtype=binding.GDN_BF16, use_qk_l2norm=1, dv_slice=0)
+    base.update(kw)
+    return binding.GdnShape(**base)
+
+
+def test_workspace_sizes(lib):
+    s = shape(N=64)
+    fwd = gdn.gdn_workspace_size(s, binding.OP_FWD)
+    assert fwd >= 256 + 64 * 4 * 4
+    assert gdn.gdn_workspace_size(s, binding.OP_DECODE) == 0
+    assert gdn.gdn_workspace_size(shape(N=64, dv_slice=32), binding.OP_FWD) > fwd
+    assert gdn.gdn_workspace_size(shape(dk=48), binding.OP_FWD) == 0  # unsupported
+    assert gdn.gdn_workspace_size(shape(HV=3), binding.OP_FWD) == 0   # HV % HK != 0
+
+
+def call_fwd(lib, s, ptrs, ws_bytes=1 << 20):
+    P = ctypes.c_void_p
+    args = [P(p) if p else None for p in ptrs]
+    return lib.gdn_recurrent_fwd(ctypes.byref(s), *args[:9], args[9], ctypes.c_size_t(ws_bytes), None)
+
+
+FAKE = 0x10000  # never dereferenced: every case below fails validation first
+
+
+@pytest.mark.parametrize("case,expect", [
+    ("null_q", -1), ("null_cu", -1), ("misaligned_v", -1), ("out_aliases_q", -1),
+    ("bad_dk", -2), ("bad_dtype", -2), ("bad_slice", -2), ("hv_not_multiple", -1),
+    ("no_workspace", -3), ("small_workspace", -3),
+])
+def test_fwd_host_validation(lib, case, expect):
+    s = shape()
+    q, k, v, g, b, s0, cu, out, fs, ws = [FAKE + i * 0x1000 for i in range(10)]
+    ws_bytes = 1 << 20
+    if case == "null_q":
+        q = 0
+    elif case == "null_cu":
+        cu = 0
+    elif case == "misaligned_v":
+        v += 4
+    elif case == "out_aliases_q":
+        out = q
+    elif case == "bad_dk":
+        s.dk = 96
+    elif case == "bad_dtype":
+        s.dtype = 7
+    elif case == "bad_slice":
+        s.dv_slice = 24
+    elif case == "hv_not_multiple":
+        s.HV = 3
+    elif case == "no_workspace":
+        ws = 0
+    elif case == "small_workspace":
+        ws_bytes = 16
+    assert call_fwd(lib, s, [q, k, v, g, b, s0, cu, out, fs, ws], ws_bytes) == expect
+
+
+def test_decode_host_validation(lib):
+    P = ctypes.c_void_p
+    s = shape(N=4, T_total=4)
+    ptr = [P(FAKE + i * 0x1000) for i in range(8)]
+    # T_total != N
+    bad = shape(N=4, T_total=5)
+    assert lib.gdn_decode_step(ctypes.byref(bad), *ptr[:6], None, 4, ptr[7], None) == -1
+    # no indices and too few slots
+    assert lib.gdn_decode_step(ctypes.byref(s), *ptr[:6], None, 3, ptr[7], None) == -1
+    # out aliases the state
+    assert lib.gdn_decode_step(ctypes.byref(s), *ptr[:6], None, 4, ptr[5], None) == -1
+    # unsupported dv
+    assert lib.gdn_decode_step(ctypes.byref(shape(N=4, T_total=4, dv=20)), *ptr[:6], None, 4, ptr[7],
+                               None) == -2
