@@ -279,14 +279,7 @@ def main():
     total_ms = start.elapsed_time(stop)
     fwd_ms = [a.elapsed_time(b) for a, b, _ in recs]
     dec_ms = [b.elapsed_time(c) for _, b, c in recs]
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-
-    ms_step = total_ms / steps
-    tokens_step = T + DEC_B
-    value = tokens_step * world / (ms_step / 1e3)
+    ms_step, value = aggregate(total_ms, steps, T + DEC_B, world, dev)
     fwd_avg = sum(fwd_ms) / len(fwd_ms)
     dec_avg = sum(dec_ms) / len(dec_ms)
 
@@ -362,6 +355,18 @@ def main():
         print(json.dumps(result), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def aggregate(total_ms, steps, tokens_per_step, world, device):
+    """Whole-job throughput over `world` replicas: the slowest rank's time
+    (max over ranks) and the tokens all ranks processed.  Returns
+    (ms_per_step, tokens/s).  The only collective in the benchmark."""
+    if world > 1:
+        t = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / steps
+    return ms_step, tokens_per_step * world / (ms_step / 1e3)
 
 
 def normwise(a, ref):

@@ -25,7 +25,9 @@
  * across sequences or split over dk.
  *
  * Memory and ownership.  Every tensor pointer is a caller-owned DEVICE
- * pointer to dense row-major data, 16-byte aligned.  The library allocates
+ * pointer to dense row-major data: q, k, v, out, d_out, dq, dk, dv, every
+ * state and the workspace 16-byte aligned; g, beta, dg, dbeta, cu_seqlens and
+ * state_indices 4-byte aligned.  The library allocates
  * no device memory; scratch comes from the caller's workspace, sized by
  * gdn_workspace_size.  All calls are asynchronous on `stream` (a
  * cudaStream_t; NULL = legacy default stream).  The return value reports

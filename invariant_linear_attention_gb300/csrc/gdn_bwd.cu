@@ -761,10 +761,12 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
     if (s->N == 0) return GDN_OK;
     if (s->T_total > 0 && (!q || !k || !v || !g || !beta || !d_out || !dq || !dk || !dv || !dg || !dbeta))
         return GDN_ERR_INVALID_ARG;
-    const void* ptrs[] = {q, k, v, g, beta, init_state, cu_seqlens, d_out, d_final_state, dq, dk, dv, dg, dbeta,
-                          d_init_state, workspace};
-    for (const void* ptr : ptrs)
+    const void* vec[] = {q, k, v, init_state, d_out, d_final_state, dq, dk, dv, d_init_state, workspace};
+    for (const void* ptr : vec)
         if (ptr && !aligned16(ptr)) return GDN_ERR_INVALID_ARG;
+    const void* sca[] = {g, beta, cu_seqlens, dg, dbeta};
+    for (const void* ptr : sca)
+        if (ptr && !aligned4(ptr)) return GDN_ERR_INVALID_ARG;
     const void* outs[] = {dq, dk, dv, dg, dbeta, d_init_state};
     const void* ins[] = {q, k, v, g, beta, init_state, d_out, d_final_state};
     for (const void* o : outs)

@@ -108,9 +108,12 @@ extern "C" gdn_status gdn_decode_step(const gdn_shape* s, const void* q, const v
     if (s->N == 0) return GDN_OK;
     if (!q || !k || !v || !g || !beta || !state || !out || num_slots <= 0) return GDN_ERR_INVALID_ARG;
     if (!state_indices && num_slots < s->N) return GDN_ERR_INVALID_ARG;
-    const void* ptrs[] = {q, k, v, g, beta, state, state_indices, out};
-    for (const void* ptr : ptrs)
+    const void* vec[] = {q, k, v, state, out};
+    for (const void* ptr : vec)
         if (ptr && !aligned16(ptr)) return GDN_ERR_INVALID_ARG;
+    const void* sca[] = {g, beta, state_indices};
+    for (const void* ptr : sca)
+        if (ptr && !aligned4(ptr)) return GDN_ERR_INVALID_ARG;
     if (out == q || out == k || out == v || out == state) return GDN_ERR_INVALID_ARG;
 
     DecodeParams p;

@@ -269,9 +269,13 @@ gdn_status check_fwd_args(const gdn_shape* s, const void* q, const void* k, cons
     if (st != GDN_OK) return st;
     if (!cu) return GDN_ERR_INVALID_ARG;
     if (s->T_total > 0 && (!q || !k || !v || !g || !beta || !out)) return GDN_ERR_INVALID_ARG;
-    const void* ptrs[] = {q, k, v, g, beta, init_state, cu, out, final_state};
-    for (const void* ptr : ptrs)
+    // vector / TMA operands need 16 bytes, scalar-loaded ones 4
+    const void* vec[] = {q, k, v, init_state, out, final_state};
+    for (const void* ptr : vec)
         if (ptr && !aligned16(ptr)) return GDN_ERR_INVALID_ARG;
+    const void* sca[] = {g, beta, cu};
+    for (const void* ptr : sca)
+        if (ptr && !aligned4(ptr)) return GDN_ERR_INVALID_ARG;
     // out must not alias an input it is computed from
     if (out && (out == q || out == k || out == v)) return GDN_ERR_INVALID_ARG;
     return GDN_OK;

@@ -16,6 +16,7 @@ constexpr size_t kWsHeader = 256;
 
 inline bool dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 inline size_t elem_size(gdn_dtype t) { return t == GDN_BF16 ? 2 : 4; }
 
 // Basic shape check common to every op.

@@ -106,9 +106,24 @@ __device__ __forceinline__ float finish_dot(float ax, float ay, float az, float 
 
 // u[r] = S_r . x for the R rows a thread holds; x is a dk fp32 vector in shared memory.
 // Must be called by all 32 lanes of the warp.
+//
+// Two instruction forms give the same bits: the packed form issues the (x, y)
+// and (z, w) accumulator chains as one two-lane fma.rn.f32x2 each (sm_100+),
+// which halves the issue slots the FP32 pipe work takes; every lane of it is
+// the same IEEE round-to-nearest fma as the scalar form.  GDN_STEP_PACKED
+// selects the packed form.
+#if !defined(GDN_STEP_PACKED) && !defined(GDN_STEP_SCALAR)
+#define GDN_STEP_SCALAR
+#endif
+#ifndef GDN_STEP_SCALAR
+__device__ __forceinline__ float2 lo2(const float4& v) { return make_float2(v.x, v.y); }
+__device__ __forceinline__ float2 hi2(const float4& v) { return make_float2(v.z, v.w); }
+#endif
+
 template <int DK, int R>
 __device__ __forceinline__ void rows_dot(const RowFrag<DK> (&s)[R], const float* __restrict__ x,
                                          int e, float (&u)[R]) {
+#ifdef GDN_STEP_SCALAR
     float ax[R], ay[R], az[R], aw[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) ax[r] = ay[r] = az[r] = aw[r] = 0.f;
@@ -125,6 +140,22 @@ __device__ __forceinline__ void rows_dot(const RowFrag<DK> (&s)[R], const float*
     }
 #pragma unroll
     for (int r = 0; r < R; ++r) u[r] = finish_dot(ax[r], ay[r], az[r], aw[r]);
+#else
+    float2 axy[R], azw[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) axy[r] = azw[r] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < DK / 8; ++i) {
+        const float4 k4 = *reinterpret_cast<const float4*>(x + 4 * (2 * i + e));
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            axy[r] = __ffma2_rn(lo2(s[r].c[i]), lo2(k4), axy[r]);
+            azw[r] = __ffma2_rn(hi2(s[r].c[i]), hi2(k4), azw[r]);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) u[r] = finish_dot(axy[r].x, axy[r].y, azw[r].x, azw[r].y);
+#endif
 }
 
 // w = b (v - a u)
@@ -133,11 +164,12 @@ __device__ __forceinline__ float delta_w(float a, float b, float v, float u) {
 }
 
 // S_r <- a S_r + w_r k^T (per element fma(w, k_j, a * S_rj)), then o[r] = S_r . q.
-// Must be called by all 32 lanes of the warp.
+// Must be called by all 32 lanes of the warp.  Same two forms as rows_dot.
 template <int DK, int R>
 __device__ __forceinline__ void rows_update_out(RowFrag<DK> (&s)[R], const float* __restrict__ k,
                                                 const float* __restrict__ q, int e, float a,
                                                 const float (&w)[R], float (&o)[R]) {
+#ifdef GDN_STEP_SCALAR
     float ox[R], oy[R], oz[R], ow[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) ox[r] = oy[r] = oz[r] = ow[r] = 0.f;
@@ -160,6 +192,29 @@ __device__ __forceinline__ void rows_update_out(RowFrag<DK> (&s)[R], const float
     }
 #pragma unroll
     for (int r = 0; r < R; ++r) o[r] = finish_dot(ox[r], oy[r], oz[r], ow[r]);
+#else
+    float2 oxy[R], ozw[R];
+    const float2 a2 = make_float2(a, a);
+#pragma unroll
+    for (int r = 0; r < R; ++r) oxy[r] = ozw[r] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < DK / 8; ++i) {
+        const float4 k4 = *reinterpret_cast<const float4*>(k + 4 * (2 * i + e));
+        const float4 q4 = *reinterpret_cast<const float4*>(q + 4 * (2 * i + e));
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float4& S = s[r].c[i];
+            const float2 w2 = make_float2(w[r], w[r]);
+            const float2 sxy = __ffma2_rn(w2, lo2(k4), __fmul2_rn(a2, lo2(S)));
+            const float2 szw = __ffma2_rn(w2, hi2(k4), __fmul2_rn(a2, hi2(S)));
+            S = make_float4(sxy.x, sxy.y, szw.x, szw.y);
+            oxy[r] = __ffma2_rn(sxy, lo2(q4), oxy[r]);
+            ozw[r] = __ffma2_rn(szw, hi2(q4), ozw[r]);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) o[r] = finish_dot(oxy[r].x, oxy[r].y, ozw[r].x, ozw[r].y);
+#endif
 }
 
 // One full token for the R rows of a thread: u, w, update, o.
