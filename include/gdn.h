@@ -130,6 +130,31 @@ gdn_status gdn_chunk_bwd(const gdn_shape* shape, const void* q, const void* k, c
                          float* dbeta, float* d_init_state, void* workspace,
                          size_t workspace_bytes, void* stream);
 
+/*
+ * gdn_recurrent_fwd without a caller workspace.  The pages have no
+ * counterpart to this entry point; it exists for callers that cannot call
+ * cudaMalloc: a host program whose device memory is owned by another
+ * allocator (a framework's caching allocator or a serving engine that
+ * reserves the whole device at start-up) and that has no buffer to lend, or
+ * a path where allocating is not allowed because cudaMalloc / cudaFree may
+ * synchronise the device.  Same arguments, results and bits as
+ * gdn_recurrent_fwd minus the workspace; it allocates nothing.
+ *
+ * Its scratch is a fixed array inside the library's device memory, sized for
+ * N * HV * (dv / dv_slice) <= 65536 work units (about 256 KB, held on every
+ * device that loads the library until the process exits).  Larger shapes
+ * return GDN_ERR_WORKSPACE.  The first call on a device looks the array's
+ * address up (cudaGetSymbolAddress, with that device current); make that
+ * first call before any stream capture.  All calls share the array: calls
+ * that overlap on the GPU (on different streams, or from several threads)
+ * race on it and must be serialised by the caller.  Its device error bits are
+ * not readable through gdn_read_device_error.
+ */
+gdn_status gdn_recurrent_fwd_noalloc(const gdn_shape* shape, const void* q, const void* k,
+                                     const void* v, const float* g, const float* beta,
+                                     const float* init_state, const int32_t* cu_seqlens,
+                                     void* out, float* final_state, void* stream);
+
 /* Read (and clear) the device error bits a FWD or BWD call left in its
  * workspace.  Synchronises `stream`.  *bits = 0 means no device error. */
 gdn_status gdn_read_device_error(void* workspace, unsigned int* bits, void* stream);

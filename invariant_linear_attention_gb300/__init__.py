@@ -12,6 +12,7 @@ from .binding import (  # noqa: F401
     gdn_chunk_bwd,
     gdn_decode_step,
     gdn_recurrent_fwd,
+    gdn_recurrent_fwd_noalloc,
     gdn_workspace_size,
     lib,
     make_shape,

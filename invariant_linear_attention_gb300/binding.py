@@ -23,7 +23,7 @@ DEVERR_CU_SEQLENS, DEVERR_TIMEOUT = 1, 2
 _P = ctypes.c_void_p
 
 SYMBOLS = ("gdn_workspace_size", "gdn_recurrent_fwd", "gdn_decode_step", "gdn_chunk_bwd",
-           "gdn_read_device_error", "gdn_status_string")
+           "gdn_read_device_error", "gdn_status_string", "gdn_recurrent_fwd_noalloc")
 
 
 class GdnShape(ctypes.Structure):
@@ -50,6 +50,8 @@ def lib():
         L.gdn_workspace_size.restype = ctypes.c_size_t
         L.gdn_recurrent_fwd.argtypes = [ctypes.POINTER(GdnShape)] + [_P] * 10 + [ctypes.c_size_t, _P]
         L.gdn_recurrent_fwd.restype = ctypes.c_int
+        L.gdn_recurrent_fwd_noalloc.argtypes = [ctypes.POINTER(GdnShape)] + [_P] * 10
+        L.gdn_recurrent_fwd_noalloc.restype = ctypes.c_int
         L.gdn_decode_step.argtypes = [ctypes.POINTER(GdnShape)] + [_P] * 7 + [ctypes.c_int, _P, _P]
         L.gdn_decode_step.restype = ctypes.c_int
         L.gdn_chunk_bwd.argtypes = [ctypes.POINTER(GdnShape)] + [_P] * 16 + [ctypes.c_size_t, _P]
@@ -154,6 +156,36 @@ def gdn_recurrent_fwd(q, k, v, g, beta, cu_seqlens, init_state=None, out=None, f
                                      _ptr(init_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
                                      _ptr(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream))
     _check(rc, "gdn_recurrent_fwd")
+    return out, final_state
+
+
+def gdn_recurrent_fwd_noalloc(q, k, v, g, beta, cu_seqlens, init_state=None, out=None, final_state=None,
+                              use_qk_l2norm=True, dv_slice=0, output_final_state=True, stream=None):
+    """gdn_recurrent_fwd through the entry point that needs no workspace (its
+    scratch is a fixed array inside the library; calls must not overlap on the
+    GPU).  Same arguments and results as gdn_recurrent_fwd minus `workspace`;
+    out / final_state are allocated here only when the caller passes none."""
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, dev)
+    _need(g, "g", torch.float32, dev)
+    _need(beta, "beta", torch.float32, dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    N = cu_seqlens.numel() - 1
+    T, HK, dk = q.shape
+    HV, dv = v.shape[1], v.shape[2]
+    if init_state is not None:
+        _need(init_state, "init_state", torch.float32, dev)
+    shape = make_shape(q, v, N, use_qk_l2norm, dv_slice)
+    if out is None:
+        out = torch.empty_like(v)
+    if final_state is None and output_final_state:
+        final_state = torch.empty(N, HV, dv, dk, dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        rc = lib().gdn_recurrent_fwd_noalloc(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                             _ptr(beta), _ptr(init_state), _ptr(cu_seqlens), _ptr(out),
+                                             _ptr(final_state), _stream(stream))
+    _check(rc, "gdn_recurrent_fwd_noalloc")
     return out, final_state
 
 

@@ -15,6 +15,7 @@
 // two rows with the shared step of gdn_step.cuh.  Outputs go straight from
 // registers to global memory.
 #include <algorithm>
+#include <mutex>
 
 #include "gdn_async.cuh"
 #include "gdn_host.h"
@@ -295,5 +296,54 @@ extern "C" gdn_status gdn_recurrent_fwd(const gdn_shape* shape, const void* q, c
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     return run_recurrent_fwd(shape, q, k, v, g, beta, init_state, cu_seqlens, out, final_state,
                              reinterpret_cast<int32_t*>(ws + kWsHeader), reinterpret_cast<unsigned*>(ws),
+                             static_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant.  Its scratch (device error word + work list) is a
+// fixed array in the library's own device memory instead of a caller-supplied
+// workspace.  Every device that loads the library holds this array (about
+// 256 KB) until the process exits.  All calls share it, so two calls whose
+// work overlaps on the GPU race on it; the error word is cleared by each call
+// and the work list is rewritten in full by each call.
+namespace gdn {
+
+constexpr int kStaticUnits = 1 << 16;    // max N * HV * (dv / dv_slice)
+constexpr int kStaticHeaderWords = 64;   // 256 bytes: word 0 is the error word
+static __device__ __align__(256) int32_t g_fwd_static_scratch[kStaticHeaderWords + kStaticUnits];
+
+// Device address of the array on the current device, looked up once per device
+// (with that device current) and cached.  nullptr if the lookup fails.
+static int32_t* static_scratch_on_current_device() {
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static int32_t* addr[kMaxDevices] = {};
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_fwd_static_scratch) != cudaSuccess || !p) return nullptr;
+        addr[dev] = static_cast<int32_t*>(p);
+    }
+    return addr[dev];
+}
+
+}  // namespace gdn
+
+extern "C" gdn_status gdn_recurrent_fwd_noalloc(const gdn_shape* shape, const void* q, const void* k,
+                                                const void* v, const float* g, const float* beta,
+                                                const float* init_state, const int32_t* cu_seqlens, void* out,
+                                                float* final_state, void* stream) {
+    using namespace gdn;
+    gdn_status st = check_fwd_args(shape, q, k, v, g, beta, init_state, cu_seqlens, out, final_state);
+    if (st != GDN_OK) return st;
+    if (shape->N == 0) return GDN_OK;
+    const long long units = (long long)shape->N * shape->HV * (shape->dv / pick_dv_slice(shape));
+    if (units > kStaticUnits) return GDN_ERR_WORKSPACE;
+    int32_t* base = static_scratch_on_current_device();
+    if (!base) return GDN_ERR_CUDA;
+    return run_recurrent_fwd(shape, q, k, v, g, beta, init_state, cu_seqlens, out, final_state,
+                             base + kStaticHeaderWords, reinterpret_cast<unsigned*>(base),
                              static_cast<cudaStream_t>(stream));
 }
