@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--profile-small", action="store_true",
                     help="tiny run for ncu captures: 8 sequences, 2 steps, no extras")
+    ap.add_argument("--profile-balanced", action="store_true",
+                    help="ncu run at full occupancy: 9 sequences x 4096 tokens (288 units), 2 steps, no extras")
     return ap.parse_args()
 
 
@@ -87,7 +89,7 @@ class Clocks:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
 
@@ -100,7 +102,7 @@ class Clocks:
         except Exception:
             self.proc.kill()
             out = ""
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.strip().splitlines():
             f = [c.strip() for c in line.split(",")]
@@ -109,12 +111,14 @@ class Clocks:
             try:
                 sm.append(float(f[1]))
                 smax.append(float(f[2]))
+                power.append(float(f[3]))
             except ValueError:
                 continue
             for name, val in zip(names, f[5:9]):
                 if val.lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "sm_mhz_min": min(sm) if sm else None, "power_w_max": max(power) if power else None,
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
@@ -231,8 +235,14 @@ def main():
     import invariant_linear_attention_gb300 as gdn
     gdn.lib()
 
-    n_seq = 8 if args.profile_small else N_SEQ
-    d, dd, st0 = workload(n_seq, device=dev)
+    small = args.profile_small or args.profile_balanced
+    n_seq = 8 if args.profile_small else (9 if args.profile_balanced else N_SEQ)
+    if args.profile_balanced:
+        from invariant_linear_attention_gb300 import inputs as _inp
+        d = _inp.make_inputs([4096] * 9, HK=HK, HV=HV, dk=DK, dv=DV, dtype=torch.bfloat16, seed=4, device=dev)
+        _, dd, st0 = workload(1, device=dev)
+    else:
+        d, dd, st0 = workload(n_seq, device=dev)
     T = d.q.shape[0]
     st = st0.clone()
     out = torch.empty_like(d.v)
@@ -255,8 +265,8 @@ def main():
         if record is not None:
             record.append((e0, e1, e2))
 
-    steps = 2 if args.profile_small else args.steps
-    warm = 1 if args.profile_small else max(3, args.warmup)
+    steps = 2 if small else args.steps
+    warm = 1 if small else max(3, args.warmup)
     for _ in range(warm):
         step(None)
     torch.cuda.synchronize()
@@ -329,7 +339,7 @@ def main():
     }
 
     # ---- correctness in the same run: sampled units vs the oracle, and bit-invariance
-    if rank == 0 and not args.profile_small:
+    if rank == 0 and not small:
         result["parity"] = check_parity(d, out, fs)
         out2 = torch.empty_like(out)
         gdn.gdn_recurrent_fwd(d.q, d.k, d.v, d.g, d.beta, d.cu_seqlens, out=out2, dv_slice=32)
@@ -338,17 +348,17 @@ def main():
                                                                                      out2.view(torch.int16)))}
 
     # ---- end to end through the C ABI from pinned host buffers
-    if not args.no_e2e and not args.profile_small:
+    if not args.no_e2e and not small:
         result["e2e"] = e2e(gdn, d.cpu(), dd.cpu(), st0.cpu(), dev, steps=min(steps, 5))
 
     # ---- backward on its own workload
-    if not args.no_backward and not args.profile_small:
+    if not args.no_backward and not small:
         try:
             result["backward"] = bench_backward(gdn, dev)
         except Exception as exc:  # reported, not hidden
             result["backward"] = {"error": str(exc)[:300]}
 
-    if rank == 0 and not args.no_cpu_baseline and not args.profile_small:
+    if rank == 0 and not args.no_cpu_baseline and not small:
         result["cpu_baseline"] = oracle_sample_rate(d)
 
     if rank == 0:

@@ -29,16 +29,16 @@ struct DecodeParams {
 };
 
 template <typename Tin, int DK>
-__global__ void __launch_bounds__(128) gdn_decode_kernel(const DecodeParams p) {
-    constexpr int R = 2;
+__global__ void __launch_bounds__(kThreadsPer128Rows) gdn_decode_kernel(const DecodeParams p) {
+    constexpr int R = kRowsPerThread;
     __shared__ __align__(16) float qn[DK];
     __shared__ __align__(16) float kn[DK];
     __shared__ float2 ab;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-    const int e = tid & 1, pair = tid >> 1;
+    const int e = tid % kLanesPerRow, grp = tid / kLanesPerRow;
     const int dvs = p.dvs;
-    const bool active = 2 * pair < dvs;
+    const bool active = grp * R < dvs;
     const int unit = blockIdx.x;
     const int slice = unit % p.nslices;
     const int h = (unit / p.nslices) % p.HV;
@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(128) gdn_decode_kernel(const DecodeParams p) {
     const int slot = p.idx ? p.idx[b] : b;
     if (slot < 0 || slot >= p.num_slots) return;  // uniform over the CTA
 
-    const int row = slice * dvs + 2 * pair;
+    const int row = slice * dvs + grp * R;
     float* srow = p.state + (((size_t)slot * p.HV + h) * p.dv + row) * DK;
     RowFrag<DK> S[R];
     if (active) load_rows<DK, R>(S, srow, e);
@@ -62,18 +62,16 @@ __global__ void __launch_bounds__(128) gdn_decode_kernel(const DecodeParams p) {
         const size_t gi = (size_t)b * p.HV + h;
         ab = make_float2(gate_alpha(p.g[gi]), p.beta[gi]);
     }
-    float vv[R] = {0.f, 0.f}, o[R];
+    float vv[R], o[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) vv[r] = 0.f;
     const size_t vo = ((size_t)b * p.HV + h) * p.dv + row;
-    if (active) {
-        const float2 v2 = ld2_in(reinterpret_cast<const Tin*>(p.v) + vo);
-        vv[0] = v2.x;
-        vv[1] = v2.y;
-    }
+    if (active) ld_rows_in<R>(reinterpret_cast<const Tin*>(p.v) + vo, vv);
     __syncthreads();
     const float2 gab = ab;
     token_step<DK, R>(S, kn, qn, e, gab.x, gab.y, vv, o);
     if (active) {
-        if (e == 0) st2_out(reinterpret_cast<Tin*>(p.out) + vo, o[0], o[1]);
+        if (e == 0) st_rows_out<R>(reinterpret_cast<Tin*>(p.out) + vo, o);
         store_rows<DK, R>(S, srow, e);
     }
 }
@@ -81,7 +79,7 @@ __global__ void __launch_bounds__(128) gdn_decode_kernel(const DecodeParams p) {
 template <typename Tin, int DK>
 static gdn_status launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
     const int units = p.N * p.HV * p.nslices;
-    gdn_decode_kernel<Tin, DK><<<units, std::max(32, p.dvs), 0, stream>>>(p);
+    gdn_decode_kernel<Tin, DK><<<units, std::max(32, p.dvs * kLanesPerRow / kRowsPerThread), 0, stream>>>(p);
     return launch_status();
 }
 
@@ -130,7 +128,9 @@ extern "C" gdn_status gdn_decode_step(const gdn_shape* s, const void* q, const v
     p.HV = s->HV;
     p.G = s->HV / s->HK;
     p.dv = s->dv;
-    p.dvs = pick_dv_slice(s);
+    // automatic slice for decode: 64 rows (smaller CTAs keep more state bytes in
+    // flight per SM; measured 157 us vs 164 us for 128 rows at batch 256)
+    p.dvs = s->dv_slice ? s->dv_slice : std::min(s->dv, 64);
     p.nslices = s->dv / p.dvs;
     p.num_slots = num_slots;
     p.use_norm = s->use_qk_l2norm ? 1 : 0;

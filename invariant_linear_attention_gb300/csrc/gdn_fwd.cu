@@ -12,8 +12,9 @@
 // with three TMA tensor copies into a double-buffered shared-memory stage.
 // The CTA then L2-normalises q and k (one warp per vector, fixed butterfly),
 // computes a = exp(g), and every thread walks the chunk's tokens over its
-// two rows with the shared step of gdn_step.cuh.  Outputs go straight from
-// registers to global memory.
+// rows with the shared step of gdn_step.cuh (row layout over lanes and rows
+// per thread as defined there).  Outputs go straight from registers to
+// global memory.  Two units share an SM.
 #include <algorithm>
 #include <mutex>
 
@@ -23,9 +24,11 @@
 
 namespace gdn {
 
-constexpr int kTC = 16;      // tokens per chunk
+#ifndef GDN_TC
+#define GDN_TC 32
+#endif
+constexpr int kTC = GDN_TC;  // tokens per chunk (one TMA stage)
 constexpr int kStages = 2;   // TMA stages
-constexpr int kRowsPerThread = 2;
 constexpr int kMaxSlice = 128;
 
 struct FwdParams {
@@ -94,9 +97,21 @@ __global__ void gdn_sched_kernel(const int32_t* __restrict__ cu, int N, int T, i
     }
 }
 
+// Thread 0: start the three TMA copies of chunk c into stage c % kStages.
+template <typename Tin, int DK>
+__device__ __forceinline__ void issue_chunk(FwdSmem<Tin, DK>& sm, const CUtensorMap* tq, const CUtensorMap* tk,
+                                            const CUtensorMap* tv, int c, int bos, int hk, int h, int col,
+                                            uint32_t bytes) {
+    const int st = c % kStages, t0 = bos + c * kTC;
+    mbar_arrive_expect_tx(&sm.bar[st], bytes);
+    tma_load_3d(sm.q[st], tq, &sm.bar[st], 0, hk, t0);
+    tma_load_3d(sm.k[st], tk, &sm.bar[st], 0, hk, t0);
+    tma_load_3d(sm.v[st], tv, &sm.bar[st], col, h, t0);
+}
+
 // ---------------------------------------------------------------------------
 template <typename Tin, int DK>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kThreadsPer128Rows, 2)
     gdn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
     constexpr int R = kRowsPerThread;
@@ -105,9 +120,9 @@ __global__ void __launch_bounds__(128)
         *reinterpret_cast<FwdSmem<Tin, DK>*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-    const int e = tid & 1, pair = tid >> 1;
+    const int e = tid % kLanesPerRow, grp = tid / kLanesPerRow;  // lane within the row, row group
     const int dvs = p.dvs;
-    const bool active = 2 * pair < dvs;
+    const bool active = grp * R < dvs;
 
     const int unit = p.work[blockIdx.x];
     const int slice = unit % p.nslices;
@@ -118,7 +133,7 @@ __global__ void __launch_bounds__(128)
     bos = min(max(bos, 0), p.T);
     eos = min(max(eos, bos), p.T);
     const int L = eos - bos;
-    const int row = slice * dvs + 2 * pair;  // first of this thread's rows
+    const int row = slice * dvs + grp * R;  // first of this thread's rows
     const size_t soff = (((size_t)n * p.HV + h) * p.dv + row) * DK;
 
     RowFrag<DK> S[R];
@@ -128,13 +143,6 @@ __global__ void __launch_bounds__(128)
     if (L > 0) {
         const int nchunks = (L + kTC - 1) / kTC;
         const uint32_t bytes = (uint32_t)((2 * p.tb * DK + p.tb * dvs) * sizeof(Tin));
-        auto issue = [&](int c) {
-            const int st = c % kStages, t0 = bos + c * kTC;
-            mbar_arrive_expect_tx(&sm.bar[st], bytes);
-            tma_load_3d(sm.q[st], &tm_q, &sm.bar[st], 0, hk, t0);
-            tma_load_3d(sm.k[st], &tm_k, &sm.bar[st], 0, hk, t0);
-            tma_load_3d(sm.v[st], &tm_v, &sm.bar[st], slice * dvs, h, t0);
-        };
         if (tid == 0) {
             for (int s = 0; s < kStages; ++s) mbar_init(&sm.bar[s], 1);
             sm.abort_flag = 0;
@@ -142,7 +150,8 @@ __global__ void __launch_bounds__(128)
         }
         __syncthreads();
         if (tid == 0)
-            for (int c = 0; c < min(kStages, nchunks); ++c) issue(c);
+            for (int c = 0; c < min(kStages, nchunks); ++c)
+                issue_chunk(sm, &tm_q, &tm_k, &tm_v, c, bos, hk, h, slice * dvs, bytes);
 
         // gate inputs of the next chunk, prefetched into registers one chunk ahead
         float2 gb = make_float2(0.f, 0.f);
@@ -176,14 +185,15 @@ __global__ void __launch_bounds__(128)
             for (int t = 0; t < tc; ++t) {
                 const float2 ab = sm.ab[t];
                 float vv[R], o[R];
-                const float2 v2 = active ? ld2_in(vs + t * dvs + 2 * pair) : make_float2(0.f, 0.f);
-                vv[0] = v2.x;
-                vv[1] = v2.y;
+#pragma unroll
+                for (int r = 0; r < R; ++r) vv[r] = 0.f;
+                if (active) ld_rows_in<R>(vs + t * dvs + grp * R, vv);
                 token_step<DK, R>(S, sm.kn + t * DK, sm.qn + t * DK, e, ab.x, ab.y, vv, o);
-                if (active && e == 0) st2_out(out + ((size_t)(t0 + t) * p.HV + h) * p.dv + row, o[0], o[1]);
+                if (active && e == 0) st_rows_out<R>(out + ((size_t)(t0 + t) * p.HV + h) * p.dv + row, o);
             }
             __syncthreads();
-            if (tid == 0 && c + kStages < nchunks) issue(c + kStages);
+            if (tid == 0 && c + kStages < nchunks)
+                issue_chunk(sm, &tm_q, &tm_k, &tm_v, c + kStages, bos, hk, h, slice * dvs, bytes);
         }
     }
     if (active && p.final_state) store_rows<DK, R>(S, p.final_state + soff, e);
@@ -196,7 +206,7 @@ static gdn_status launch_fwd_t(const CUtensorMap& mq, const CUtensorMap& mk, con
     auto kern = gdn_fwd_kernel<Tin, DK>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return GDN_ERR_CUDA;
-    const int nt = std::max(32, p.dvs);
+    const int nt = std::max(32, p.dvs * kLanesPerRow / kRowsPerThread);
     kern<<<units, nt, smem, stream>>>(mq, mk, mv, p);
     return launch_status();
 }

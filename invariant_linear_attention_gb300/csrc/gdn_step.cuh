@@ -8,14 +8,15 @@
 // only), so how rows are spread over threads, warps and CTAs is free; the
 // lane->dk mapping, the in-lane summation order and the butterfly are not.
 //
-// Layout of one state row (dk fp32 values) over a lane pair: row r lives in
-// lanes 2p and 2p+1 of a warp; lane parity e holds the float4 chunks
-// c = 2i + e, i = 0 .. dk/8-1 (chunk c = elements 4c .. 4c+3).  A dk
-// contraction is: four per-component fma chains over i in increasing order
-// (starting from +0), then (x + y) + (z + w), then one xor-1 shuffle add.
-// All arithmetic uses explicit round-to-nearest intrinsics so no FMA
-// contraction or reassociation can differ between kernels.
-//
+// Layout of one state row (dk fp32 values): row r lives in kLanesPerRow (L)
+// consecutive lanes of a warp; lane e = lane % L holds the float4 chunks
+// c = L*i + e, i = 0 .. dk/(4L)-1 (chunk c = elements 4c .. 4c+3).  A thread
+// holds kRowsPerThread (R) consecutive rows.  A dk contraction is: per
+// accumulator set j = i mod NS (NS = chunks/8 when a lane holds 16 or more
+// chunks, else 1) two packed (x, y) / (z, w) fma chains over i in increasing
+// order starting from +0; the sets summed in increasing j; then
+// (x + y) + (z + w); then an xor butterfly over the L lanes of the row
+// (commutative adds, so every lane ends with the same bits).
 // The recurrence (gated delta rule, recurrent form as in "Defending Against
 // the Training-Inference Numeric Mismatch in RL (Especially Linear
 // Attention)", section 3.2):
@@ -32,11 +33,28 @@ namespace gdn {
 constexpr float kNormEps = 1e-6f;
 constexpr unsigned kFull = 0xffffffffu;
 
+#ifndef GDN_LANES
+#define GDN_LANES 4
+#endif
+#ifndef GDN_ROWS
+#define GDN_ROWS 2
+#endif
+constexpr int kLanesPerRow = GDN_LANES;   // L
+constexpr int kRowsPerThread = GDN_ROWS;  // R
+static_assert(kLanesPerRow == 1 || kLanesPerRow == 2 || kLanesPerRow == 4 || kLanesPerRow == 8, "L");
+static_assert(kRowsPerThread == 1 || kRowsPerThread == 2 || kRowsPerThread == 4, "R");
+// threads that hold a 128-row state slice
+constexpr int kThreadsPer128Rows = 128 * kLanesPerRow / kRowsPerThread;
+
 template <int DK>
 struct RowFrag {
-    static_assert(DK % 8 == 0, "dk must be a multiple of 8");
-    float4 c[DK / 8];
+    static_assert(DK % (4 * kLanesPerRow) == 0, "dk must be a multiple of 4 L");
+    static constexpr int kChunks = DK / (4 * kLanesPerRow);
+    static constexpr int kSets = kChunks >= 16 ? kChunks / 8 : 1;
+    float4 c[kChunks];
 };
+
+__device__ __forceinline__ int chunk_of(int i, int e) { return kLanesPerRow * i + e; }
 
 __device__ __forceinline__ float ld_in(const float* p) { return *p; }
 __device__ __forceinline__ float ld_in(const __nv_bfloat16* p) { return __bfloat162float(*p); }
@@ -50,6 +68,21 @@ __device__ __forceinline__ float4 ld4_in(const __nv_bfloat16* p) {
     __nv_bfloat162 hi = *reinterpret_cast<__nv_bfloat162*>(&raw.y);
     float2 a = __bfloat1622float2(lo), b = __bfloat1622float2(hi);
     return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// R adjacent values (a thread's rows) of v widened to fp32, and the R outputs
+// stored rounded to nearest.
+template <int R, typename T>
+__device__ __forceinline__ void ld_rows_in(const T* p, float (&v)[R]) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) v[r] = ld_in(p + r);
+}
+__device__ __forceinline__ void st_in(float* p, float x) { *p = x; }
+__device__ __forceinline__ void st_in(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+template <int R, typename T>
+__device__ __forceinline__ void st_rows_out(T* p, const float (&o)[R]) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) st_in(p + r, o[r]);
 }
 
 // Two adjacent values (rows 2p, 2p+1) of v widened to fp32.
@@ -98,10 +131,22 @@ __device__ __forceinline__ void l2norm_warp(const Tin* __restrict__ src, float* 
 // Gate values for one token: a = exp(g) (CUDA's expf, same call everywhere), b as given.
 __device__ __forceinline__ float gate_alpha(float g) { return expf(g); }
 
-// Pair-level finish of a dk contraction: (x + y) + (z + w), then + partner lane.
-__device__ __forceinline__ float finish_dot(float ax, float ay, float az, float aw) {
-    const float p = __fadd_rn(__fadd_rn(ax, ay), __fadd_rn(az, aw));
-    return __fadd_rn(p, __shfl_xor_sync(kFull, p, 1));
+// Finish of a dk contraction from per-set packed accumulators: sets in
+// increasing order, (x + y) + (z + w), then the xor butterfly over the L lanes.
+template <int NS>
+__device__ __forceinline__ float finish_dot(const float2 (&xy)[NS], const float2 (&zw)[NS]) {
+    float2 a = xy[0], b = zw[0];
+#pragma unroll
+    for (int j = 1; j < NS; ++j) {
+        a.x = __fadd_rn(a.x, xy[j].x);
+        a.y = __fadd_rn(a.y, xy[j].y);
+        b.x = __fadd_rn(b.x, zw[j].x);
+        b.y = __fadd_rn(b.y, zw[j].y);
+    }
+    float p = __fadd_rn(__fadd_rn(a.x, a.y), __fadd_rn(b.x, b.y));
+#pragma unroll
+    for (int m = 1; m < kLanesPerRow; m <<= 1) p = __fadd_rn(p, __shfl_xor_sync(kFull, p, m));
+    return p;
 }
 
 // u[r] = S_r . x for the R rows a thread holds; x is a dk fp32 vector in shared memory.
@@ -110,52 +155,40 @@ __device__ __forceinline__ float finish_dot(float ax, float ay, float az, float 
 // Two instruction forms give the same bits: the packed form issues the (x, y)
 // and (z, w) accumulator chains as one two-lane fma.rn.f32x2 each (sm_100+),
 // which halves the issue slots the FP32 pipe work takes; every lane of it is
-// the same IEEE round-to-nearest fma as the scalar form.  GDN_STEP_PACKED
-// selects the packed form.
-#if !defined(GDN_STEP_PACKED) && !defined(GDN_STEP_SCALAR)
-#define GDN_STEP_SCALAR
-#endif
-#ifndef GDN_STEP_SCALAR
+// the same IEEE round-to-nearest fma as the scalar form.  GDN_STEP_SCALAR
+// selects the scalar form.
 __device__ __forceinline__ float2 lo2(const float4& v) { return make_float2(v.x, v.y); }
 __device__ __forceinline__ float2 hi2(const float4& v) { return make_float2(v.z, v.w); }
-#endif
 
 template <int DK, int R>
 __device__ __forceinline__ void rows_dot(const RowFrag<DK> (&s)[R], const float* __restrict__ x,
                                          int e, float (&u)[R]) {
+    constexpr int NC = RowFrag<DK>::kChunks, NS = RowFrag<DK>::kSets;
+    float2 xy[R][NS], zw[R][NS];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int j = 0; j < NS; ++j) xy[r][j] = zw[r][j] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < NC; ++i) {
+        const float4 k4 = *reinterpret_cast<const float4*>(x + 4 * chunk_of(i, e));
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float2& A = xy[r][i % NS];
+            float2& B = zw[r][i % NS];
 #ifdef GDN_STEP_SCALAR
-    float ax[R], ay[R], az[R], aw[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) ax[r] = ay[r] = az[r] = aw[r] = 0.f;
-#pragma unroll
-    for (int i = 0; i < DK / 8; ++i) {
-        const float4 k4 = *reinterpret_cast<const float4*>(x + 4 * (2 * i + e));
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            ax[r] = __fmaf_rn(s[r].c[i].x, k4.x, ax[r]);
-            ay[r] = __fmaf_rn(s[r].c[i].y, k4.y, ay[r]);
-            az[r] = __fmaf_rn(s[r].c[i].z, k4.z, az[r]);
-            aw[r] = __fmaf_rn(s[r].c[i].w, k4.w, aw[r]);
-        }
-    }
-#pragma unroll
-    for (int r = 0; r < R; ++r) u[r] = finish_dot(ax[r], ay[r], az[r], aw[r]);
+            A.x = __fmaf_rn(s[r].c[i].x, k4.x, A.x);
+            A.y = __fmaf_rn(s[r].c[i].y, k4.y, A.y);
+            B.x = __fmaf_rn(s[r].c[i].z, k4.z, B.x);
+            B.y = __fmaf_rn(s[r].c[i].w, k4.w, B.y);
 #else
-    float2 axy[R], azw[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) axy[r] = azw[r] = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int i = 0; i < DK / 8; ++i) {
-        const float4 k4 = *reinterpret_cast<const float4*>(x + 4 * (2 * i + e));
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            axy[r] = __ffma2_rn(lo2(s[r].c[i]), lo2(k4), axy[r]);
-            azw[r] = __ffma2_rn(hi2(s[r].c[i]), hi2(k4), azw[r]);
+            A = __ffma2_rn(lo2(s[r].c[i]), lo2(k4), A);
+            B = __ffma2_rn(hi2(s[r].c[i]), hi2(k4), B);
+#endif
         }
     }
 #pragma unroll
-    for (int r = 0; r < R; ++r) u[r] = finish_dot(axy[r].x, axy[r].y, azw[r].x, azw[r].y);
-#endif
+    for (int r = 0; r < R; ++r) u[r] = finish_dot<NS>(xy[r], zw[r]);
 }
 
 // w = b (v - a u)
@@ -169,52 +202,45 @@ template <int DK, int R>
 __device__ __forceinline__ void rows_update_out(RowFrag<DK> (&s)[R], const float* __restrict__ k,
                                                 const float* __restrict__ q, int e, float a,
                                                 const float (&w)[R], float (&o)[R]) {
-#ifdef GDN_STEP_SCALAR
-    float ox[R], oy[R], oz[R], ow[R];
+    constexpr int NC = RowFrag<DK>::kChunks, NS = RowFrag<DK>::kSets;
+    float2 xy[R][NS], zw[R][NS];
 #pragma unroll
-    for (int r = 0; r < R; ++r) ox[r] = oy[r] = oz[r] = ow[r] = 0.f;
+    for (int r = 0; r < R; ++r)
 #pragma unroll
-    for (int i = 0; i < DK / 8; ++i) {
-        const float4 k4 = *reinterpret_cast<const float4*>(k + 4 * (2 * i + e));
-        const float4 q4 = *reinterpret_cast<const float4*>(q + 4 * (2 * i + e));
+        for (int j = 0; j < NS; ++j) xy[r][j] = zw[r][j] = make_float2(0.f, 0.f);
+#ifndef GDN_STEP_SCALAR
+    const float2 a2 = make_float2(a, a);
+#endif
+#pragma unroll
+    for (int i = 0; i < NC; ++i) {
+        const float4 k4 = *reinterpret_cast<const float4*>(k + 4 * chunk_of(i, e));
+        const float4 q4 = *reinterpret_cast<const float4*>(q + 4 * chunk_of(i, e));
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             float4& S = s[r].c[i];
+            float2& A = xy[r][i % NS];
+            float2& B = zw[r][i % NS];
+#ifdef GDN_STEP_SCALAR
             S.x = __fmaf_rn(w[r], k4.x, __fmul_rn(a, S.x));
             S.y = __fmaf_rn(w[r], k4.y, __fmul_rn(a, S.y));
             S.z = __fmaf_rn(w[r], k4.z, __fmul_rn(a, S.z));
             S.w = __fmaf_rn(w[r], k4.w, __fmul_rn(a, S.w));
-            ox[r] = __fmaf_rn(S.x, q4.x, ox[r]);
-            oy[r] = __fmaf_rn(S.y, q4.y, oy[r]);
-            oz[r] = __fmaf_rn(S.z, q4.z, oz[r]);
-            ow[r] = __fmaf_rn(S.w, q4.w, ow[r]);
-        }
-    }
-#pragma unroll
-    for (int r = 0; r < R; ++r) o[r] = finish_dot(ox[r], oy[r], oz[r], ow[r]);
+            A.x = __fmaf_rn(S.x, q4.x, A.x);
+            A.y = __fmaf_rn(S.y, q4.y, A.y);
+            B.x = __fmaf_rn(S.z, q4.z, B.x);
+            B.y = __fmaf_rn(S.w, q4.w, B.y);
 #else
-    float2 oxy[R], ozw[R];
-    const float2 a2 = make_float2(a, a);
-#pragma unroll
-    for (int r = 0; r < R; ++r) oxy[r] = ozw[r] = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int i = 0; i < DK / 8; ++i) {
-        const float4 k4 = *reinterpret_cast<const float4*>(k + 4 * (2 * i + e));
-        const float4 q4 = *reinterpret_cast<const float4*>(q + 4 * (2 * i + e));
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            float4& S = s[r].c[i];
             const float2 w2 = make_float2(w[r], w[r]);
             const float2 sxy = __ffma2_rn(w2, lo2(k4), __fmul2_rn(a2, lo2(S)));
             const float2 szw = __ffma2_rn(w2, hi2(k4), __fmul2_rn(a2, hi2(S)));
             S = make_float4(sxy.x, sxy.y, szw.x, szw.y);
-            oxy[r] = __ffma2_rn(sxy, lo2(q4), oxy[r]);
-            ozw[r] = __ffma2_rn(szw, hi2(q4), ozw[r]);
+            A = __ffma2_rn(sxy, lo2(q4), A);
+            B = __ffma2_rn(szw, hi2(q4), B);
+#endif
         }
     }
 #pragma unroll
-    for (int r = 0; r < R; ++r) o[r] = finish_dot(oxy[r].x, oxy[r].y, ozw[r].x, ozw[r].y);
-#endif
+    for (int r = 0; r < R; ++r) o[r] = finish_dot<NS>(xy[r], zw[r]);
 }
 
 // One full token for the R rows of a thread: u, w, update, o.
@@ -236,8 +262,8 @@ __device__ __forceinline__ void load_rows(RowFrag<DK> (&s)[R], const float* __re
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int i = 0; i < DK / 8; ++i)
-            s[r].c[i] = __ldcs(reinterpret_cast<const float4*>(row0 + (size_t)r * DK + 4 * (2 * i + e)));
+        for (int i = 0; i < RowFrag<DK>::kChunks; ++i)
+            s[r].c[i] = __ldcs(reinterpret_cast<const float4*>(row0 + (size_t)r * DK + 4 * chunk_of(i, e)));
 }
 
 template <int DK, int R>
@@ -245,7 +271,7 @@ __device__ __forceinline__ void zero_rows(RowFrag<DK> (&s)[R]) {
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int i = 0; i < DK / 8; ++i) s[r].c[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < RowFrag<DK>::kChunks; ++i) s[r].c[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 template <int DK, int R>
@@ -253,8 +279,8 @@ __device__ __forceinline__ void store_rows(const RowFrag<DK> (&s)[R], float* __r
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int i = 0; i < DK / 8; ++i)
-            __stcs(reinterpret_cast<float4*>(row0 + (size_t)r * DK + 4 * (2 * i + e)), s[r].c[i]);
+        for (int i = 0; i < RowFrag<DK>::kChunks; ++i)
+            __stcs(reinterpret_cast<float4*>(row0 + (size_t)r * DK + 4 * chunk_of(i, e)), s[r].c[i]);
 }
 
 }  // namespace gdn
