@@ -17,7 +17,9 @@
 //     dQ   = diag(Gam) dO S0 + dQK K,  dK = dQK^T Q + diag(b) U D + diag(beta Gam) T^T dW + (dKK + dKK^T) K
 //     dW = -dU S0, dV = diag(beta) T^T dU, dA = -T^T dT T^T, dT = dW (beta Gam K)^T + dU (beta V)^T
 //     plus the dbeta and dgam terms; dg = reverse cumsum of dgam inside the chunk.
-// Kernels (all fp32 SIMT in this version):
+// Every dense product goes through one CTA-wide helper: TF32 tensor cores
+// (mma.sync m16n8k8, 3xTF32 split for about fp32 accuracy) by default, or the
+// fp32 SIMT loop below when built with GDN_BWD_SIMT.  Kernels:
 //     bwd_offsets   chunk offsets per sequence (+ cu_seqlens validation)
 //     bwd_norm      q^, k^ and 1/|.| per (token, k-head)
 //     bwd_wy        per (chunk, head): gam, T, W, U~, Q K^T              [chunk-parallel]
@@ -29,18 +31,20 @@
 // Gradients are deterministic (fixed orders everywhere, no atomics on data).
 #include <algorithm>
 
+#include "gdn_async.cuh"
 #include "gdn_host.h"
+#include "gdn_mma.cuh"
 #include "gdn_step.cuh"
 
 namespace gdn {
 
 constexpr int kC = 64;        // chunk length
 constexpr int kMaxD = 128;    // max dk, dv
-constexpr int kLdD = kMaxD + 1;  // smem leading dim of C x d / d x d matrices (odd: conflict-free columns)
-constexpr int kLdC = kC + 1;     // smem leading dim of C x C matrices
-constexpr int kRowsSlice = 32;   // dv rows per CTA in the sequential state passes
+// smem leading dims = 4 (mod 32): row-major tensor-core fragment loads hit 32 distinct banks
+constexpr int kLdD = kMaxD + 4;  // C x d and d x d matrices
+constexpr int kLdC = kC + 4;     // C x C matrices
 constexpr int kNT = 256;         // threads of the chunk-parallel kernels
-constexpr int kNTs = 128;        // threads of the state-pass kernels
+constexpr int kNTs = 512;        // threads of the state-pass kernels (one CTA holds all dv rows)
 
 struct BwdParams {
     const void* q;
@@ -68,7 +72,10 @@ struct BwdParams {
     float* Wb;         // per chunk-head C x dk  (W, later dW)
     float* Utb;        // per chunk-head C x dv  (U~)
     float* Tb;         // per chunk-head C x C
-    float* QKb;        // per chunk-head C x C
+    float* QKb;        // per chunk-head C x C: Q K^T
+    float* Pb;         // per chunk-head C x C: P = lower(E) * Q K^T (rows >= len zero)
+    float* BKb;        // per chunk-head C x dk: diag(b) K, b_r = exp(gam_last - gam_r)
+    float* GQb;        // per chunk-head C x dk: diag(Gam) Q
     float* Sb;         // per chunk-head dv x dk (chunk-start state)
     float* Db;         // per chunk-head dv x dk (dL/d state at chunk end)
     float* Ub;         // per chunk-head C x dv
@@ -142,21 +149,95 @@ __device__ __forceinline__ void cta_gemm(int M, int N, int K, const float* __res
     }
 }
 
-// Copy rows [0, len) of a global [rows, stride] fp32 matrix (row r at base + r * gstride) into
-// shared memory (leading dim ld), zero-filling rows len .. R-1.  cols <= ld.
+// The backward's product: tensor cores unless GDN_BWD_SIMT.  The operand
+// precision follows the input dtype: bf16 inputs (8 significant bits) run
+// plain TF32, fp32 inputs the 3xTF32 split (about fp32 accuracy).
+template <typename F>
+__device__ __forceinline__ void bgemm_impl(bool split, int M, int N, int K, const float* __restrict__ A, int as0,
+                                           int as1, const float* __restrict__ B, int bs0, int bs1, F&& f) {
+#ifdef GDN_BWD_SIMT
+    cta_gemm(M, N, K, A, as0, as1, B, bs0, bs1, f);
+#else
+    cta_gemm_tc(split, M, N, K, A, as0, as1, B, bs0, bs1, f);
+#endif
+}
+#define bgemm(...) bgemm_impl(p.dtype == GDN_F32, __VA_ARGS__)
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// Copy rows [0, len) of a global fp32 matrix (row r at base + r * gstride) into shared memory
+// (leading dim ld), zero-filling rows len .. R-1.  cols, gstride and ld are multiples of 4 and
+// both bases 16-byte aligned: the copy is 16-byte cp.async, all in flight at once, and each
+// thread waits for its own copies before returning (callers still barrier before reading).
 __device__ __forceinline__ void load_rows_f32(float* dst, int ld, const float* base, size_t gstride, int R, int len,
                                               int cols) {
-    for (int i = threadIdx.x; i < R * cols; i += blockDim.x) {
-        const int r = i / cols, c = i - r * cols;
-        dst[r * ld + c] = r < len ? base[(size_t)r * gstride + c] : 0.f;
+    const int c4 = cols >> 2;
+    for (int i = threadIdx.x; i < R * c4; i += blockDim.x) {
+        const int r = i / c4, c = (i - r * c4) << 2;
+        float* d = dst + r * ld + c;
+        if (r < len) cp_async16(d, base + (size_t)r * gstride + c);
+        else *reinterpret_cast<float4*>(d) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    cp_async_wait_all();
+}
+
+// load_rows_f32 without the final wait: the copies complete at the caller's cp_async_wait_all().
+__device__ __forceinline__ void load_rows_f32_async(float* dst, int ld, const float* base, size_t gstride, int R,
+                                                    int len, int cols) {
+    const int c4 = cols >> 2;
+    for (int i = threadIdx.x; i < R * c4; i += blockDim.x) {
+        const int r = i / c4, c = (i - r * c4) << 2;
+        float* d = dst + r * ld + c;
+        if (r < len) cp_async16(d, base + (size_t)r * gstride + c);
+        else *reinterpret_cast<float4*>(d) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 }
 
+// Same for a bf16 or fp32 source widened to fp32 (4 elements per access, 4 accesses in flight).
+__device__ __forceinline__ float4 ld4_any(const void* base, size_t i, int dtype) {
+    if (dtype == GDN_BF16) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(base) + i);
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+        return make_float4(a.x, a.y, b.x, b.y);
+    }
+    return *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + i);
+}
 __device__ __forceinline__ void load_rows_any(float* dst, int ld, const void* base, size_t off, size_t gstride,
                                               int R, int len, int cols, int dtype) {
-    for (int i = threadIdx.x; i < R * cols; i += blockDim.x) {
-        const int r = i / cols, c = i - r * cols;
-        dst[r * ld + c] = r < len ? ld_any(base, off + (size_t)r * gstride + c, dtype) : 0.f;
+    const int c4 = cols >> 2, total = R * c4;
+    for (int i0 = threadIdx.x; i0 < total; i0 += 4 * blockDim.x) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * blockDim.x;
+            const int r = i / c4, c = (i - r * c4) << 2;
+            v[u] = (i < total && r < len) ? ld4_any(base, off + (size_t)r * gstride + c, dtype)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * blockDim.x;
+            if (i < total) {
+                const int r = i / c4, c = (i - r * c4) << 2;
+                *reinterpret_cast<float4*>(dst + r * ld + c) = v[u];
+            }
+        }
+    }
+}
+
+// Store rows [0, R) of a shared matrix (leading dim ld) to global (row stride gstride), float4 at a time.
+__device__ __forceinline__ void store_rows_f32(float* base, size_t gstride, const float* src, int ld, int R,
+                                               int cols) {
+    const int c4 = cols >> 2;
+    for (int i = threadIdx.x; i < R * c4; i += blockDim.x) {
+        const int r = i / c4, c = (i - r * c4) << 2;
+        *reinterpret_cast<float4*>(base + (size_t)r * gstride + c) = *reinterpret_cast<const float4*>(src + r * ld + c);
     }
 }
 
@@ -240,26 +321,54 @@ __global__ void __launch_bounds__(kNT) bwd_wy_kernel(BwdParams p) {
         const float b1 = r1 < len ? p.beta[(size_t)(t0 + r1) * p.HV + h] : 0.f;
         sb[r0] = b0;
         sb[r1] = b1;
-        sGb[r0] = b0 * expf(c0);
-        sGb[r1] = b1 * expf(c1);
+        sGb[r0] = b0 * __expf(c0);
+        sGb[r1] = b1 * __expf(c1);
         if (r0 < len) p.gam[(size_t)(t0 + r0) * p.HV + h] = c0;
         if (r1 < len) p.gam[(size_t)(t0 + r1) * p.HV + h] = c1;
     }
     __syncthreads();
     const size_t ci = ch_index(p, c, h);
     // A = strict_lower(beta_r E[r,s] (K K^T)[r,s]);  QK = Q K^T (stored)
-    cta_gemm(kC, kC, dk, sK, kLdD, 1, sK, 1, kLdD, [&](int r, int s, float kk) {
-        sA[r * kLdC + s] = (s < r) ? sb[r] * expf(sg[r] - sg[s]) * kk : 0.f;
+    bgemm(kC, kC, dk, sK, kLdD, 1, sK, 1, kLdD, [&](int r, int s, float kk) {
+        sA[r * kLdC + s] = (s < r) ? sb[r] * __expf(sg[r] - sg[s]) * kk : 0.f;
     });
     float* QK = p.QKb + ci * kC * kC;
-    cta_gemm(kC, kC, dk, sQ, kLdD, 1, sK, 1, kLdD, [&](int r, int s, float x) { QK[r * kC + s] = x; });
+    float* P = p.Pb + ci * kC * kC;
+    bgemm(kC, kC, dk, sQ, kLdD, 1, sK, 1, kLdD, [&](int r, int s, float x) {
+        QK[r * kC + s] = x;
+        P[r * kC + s] = (s <= r && r < len) ? x * __expf(sg[r] - sg[s]) : 0.f;
+    });
+    {
+        // diag(b) K and diag(Gam) Q for the sequential passes (rows >= len are zero already)
+        const float gl = sg[len - 1];
+        float* BK = p.BKb + ci * kC * dk;
+        float* GQ = p.GQb + ci * kC * dk;
+        const int c4 = dk >> 2;
+        for (int i = threadIdx.x; i < kC * c4; i += blockDim.x) {
+            const int r = i / c4, j = (i - r * c4) << 2;
+            const float b = r < len ? __expf(gl - sg[r]) : 0.f, G = r < len ? __expf(sg[r]) : 0.f;
+            const float4 k4 = *reinterpret_cast<const float4*>(sK + r * kLdD + j);
+            const float4 q4 = *reinterpret_cast<const float4*>(sQ + r * kLdD + j);
+            *reinterpret_cast<float4*>(BK + r * dk + j) = make_float4(b * k4.x, b * k4.y, b * k4.z, b * k4.w);
+            *reinterpret_cast<float4*>(GQ + r * dk + j) = make_float4(G * q4.x, G * q4.y, G * q4.z, G * q4.w);
+        }
+    }
     __syncthreads();
     // T = (I + A)^-1: thread j solves column j by forward substitution (columns are independent)
     if (threadIdx.x < kC) {
         const int j = threadIdx.x;
         for (int r = 0; r < kC; ++r) {
-            float x = (r == j) ? 1.f : 0.f;
-            for (int s = j; s < r; ++s) x = fmaf(-sA[r * kLdC + s], sT[s * kLdC + j], x);
+            // x = delta_rj - sum_{j <= s < r} A[r][s] T[s][j], as four interleaved partial sums
+            float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+            int s = j;
+            for (; s + 3 < r; s += 4) {
+                x0 = fmaf(sA[r * kLdC + s], sT[s * kLdC + j], x0);
+                x1 = fmaf(sA[r * kLdC + s + 1], sT[(s + 1) * kLdC + j], x1);
+                x2 = fmaf(sA[r * kLdC + s + 2], sT[(s + 2) * kLdC + j], x2);
+                x3 = fmaf(sA[r * kLdC + s + 3], sT[(s + 3) * kLdC + j], x3);
+            }
+            for (; s < r; ++s) x0 = fmaf(sA[r * kLdC + s], sT[s * kLdC + j], x0);
+            const float x = ((r == j) ? 1.f : 0.f) - ((x0 + x1) + (x2 + x3));
             sT[r * kLdC + j] = (r < j) ? 0.f : x;
         }
     }
@@ -274,7 +383,7 @@ __global__ void __launch_bounds__(kNT) bwd_wy_kernel(BwdParams p) {
     }
     __syncthreads();
     float* W = p.Wb + ci * kC * dk;
-    cta_gemm(kC, dk, kC, sTt, kLdC, 1, sK, kLdD, 1, [&](int r, int j, float x) { W[r * dk + j] = x; });
+    bgemm(kC, dk, kC, sTt, kLdC, 1, sK, kLdD, 1, [&](int r, int j, float x) { W[r * dk + j] = x; });
     __syncthreads();
     for (int i = threadIdx.x; i < kC * kC; i += blockDim.x) {
         const int r = i / kC, s = i - r * kC;
@@ -282,7 +391,7 @@ __global__ void __launch_bounds__(kNT) bwd_wy_kernel(BwdParams p) {
     }
     __syncthreads();
     float* Ut = p.Utb + ci * kC * dv;
-    cta_gemm(kC, dv, kC, sTt, kLdC, 1, sQ, kLdD, 1, [&](int r, int j, float x) { Ut[r * dv + j] = x; });
+    bgemm(kC, dv, kC, sTt, kLdC, 1, sQ, kLdD, 1, [&](int r, int j, float x) { Ut[r * dv + j] = x; });
 }
 
 // ---------------------------------------------------------------------------
@@ -293,10 +402,10 @@ __global__ void __launch_bounds__(kNTs) bwd_state_fwd_kernel(BwdParams p, int R)
     const int hk = h / p.G, dk = p.dk, dv = p.dv;
     float* sS = sm;                   // R x kLdD
     float* sW = sS + R * kLdD;        // C x kLdD
-    float* sK = sW + kC * kLdD;       // C x kLdD (scaled by b)
-    float* sU = sK + kC * kLdD;       // C x (R + 1)
-    float* sg = sU + kC * (R + 1);    // gam [C]
-    const int ldU = R + 1;
+    float* sK = sW + kC * kLdD;       // C x kLdD: diag(b) K
+    float* sU = sK + kC * kLdD;       // C x (R + 4)
+    float* sUt = sU + kC * (R + 4);   // C x (R + 4): U~ slice
+    const int ldU = R + 4;
     const float* s0 = p.init_state ? p.init_state + (((size_t)n * p.HV + h) * dv + r0) * dk : nullptr;
     for (int i = threadIdx.x; i < R * dk; i += blockDim.x) {
         const int r = i / dk, j = i - r * dk;
@@ -310,34 +419,25 @@ __global__ void __launch_bounds__(kNTs) bwd_state_fwd_kernel(BwdParams p, int R)
         const int t0 = bos + j * kC, len = min(kC, eos - t0);
         const size_t ci = ch_index(p, c, h);
         __syncthreads();
-        // chunk-start state out
-        float* Sg = p.Sb + ci * dv * dk + (size_t)r0 * dk;
-        for (int i = threadIdx.x; i < R * dk; i += blockDim.x) {
-            const int r = i / dk, jj = i - r * dk;
-            Sg[i] = sS[r * kLdD + jj];
-        }
-        load_rows_f32(sW, kLdD, p.Wb + ci * kC * dk, dk, kC, kC, dk);
-        load_rows_f32(sK, kLdD, p.kn + ((size_t)t0 * p.HK + hk) * dk, (size_t)p.HK * dk, kC, len, dk);
-        for (int i = threadIdx.x; i < kC; i += blockDim.x) sg[i] = i < len ? p.gam[(size_t)(t0 + i) * p.HV + h] : 0.f;
+        // chunk-start state out; stage W, diag(b) K and the U~ slice
+        store_rows_f32(p.Sb + ci * dv * dk + (size_t)r0 * dk, dk, sS, kLdD, R, dk);
+        load_rows_f32_async(sW, kLdD, p.Wb + ci * kC * dk, dk, kC, kC, dk);
+        load_rows_f32_async(sK, kLdD, p.BKb + ci * kC * dk, dk, kC, kC, dk);
+        load_rows_f32_async(sUt, ldU, p.Utb + ci * kC * dv + r0, dv, kC, kC, R);
+        const float Gl = __expf(p.gam[(size_t)(t0 + len - 1) * p.HV + h]);
+        cp_async_wait_all();
         __syncthreads();
-        const float gl = sg[len - 1];
-        for (int i = threadIdx.x; i < kC * dk; i += blockDim.x) {
-            const int r = i / dk, jj = i - r * dk;
-            if (r < len) sK[r * kLdD + jj] *= expf(gl - sg[r]);
-        }
         // U = U~ - W S^T  (C x R)
-        const float* Ut = p.Utb + ci * kC * dv + r0;
         float* Ug = p.Ub + ci * kC * dv + r0;
-        cta_gemm(kC, R, dk, sW, kLdD, 1, sS, 1, kLdD, [&](int r, int i, float x) {
-            const float u = Ut[(size_t)r * dv + i] - x;
+        bgemm(kC, R, dk, sW, kLdD, 1, sS, 1, kLdD, [&](int r, int i, float x) {
+            const float u = sUt[r * ldU + i] - x;
             sU[r * ldU + i] = u;
             Ug[(size_t)r * dv + i] = u;
         });
         __syncthreads();
         // S <- Gam_last S + U^T (b K)
-        const float Gl = expf(gl);
-        cta_gemm(R, dk, kC, sU, 1, ldU, sK, kLdD, 1,
-                 [&](int i, int jj, float x) { sS[i * kLdD + jj] = fmaf(Gl, sS[i * kLdD + jj], x); });
+        bgemm(R, dk, kC, sU, 1, ldU, sK, kLdD, 1,
+              [&](int i, int jj, float x) { sS[i * kLdD + jj] = fmaf(Gl, sS[i * kLdD + jj], x); });
     }
 }
 
@@ -345,15 +445,14 @@ __global__ void __launch_bounds__(kNTs) bwd_state_fwd_kernel(BwdParams p, int R)
 __global__ void __launch_bounds__(kNTs) bwd_state_bwd_kernel(BwdParams p, int R) {
     extern __shared__ float sm[];
     const int n = blockIdx.x, h = blockIdx.y, r0 = blockIdx.z * R;
-    const int hk = h / p.G, dk = p.dk, dv = p.dv;
-    const int ldR = R + 1;
+    const int dk = p.dk, dv = p.dv;
+    const int ldR = R + 4;
     float* sD = sm;                    // R x kLdD
-    float* sQ = sD + R * kLdD;         // C x kLdD (scaled by Gam)
-    float* sW = sQ + kC * kLdD;        // C x kLdD (then K scaled by b)
-    float* sP = sW + kC * kLdD;        // C x kLdC
-    float* sO = sP + kC * kLdC;        // C x ldR  (dO slice)
+    float* sQ = sD + R * kLdD;         // C x kLdD: diag(Gam) Q
+    float* sW = sQ + kC * kLdD;        // C x kLdD: diag(b) K, then W
+    float* sP = sW + kC * kLdD;        // C x kLdC: P
+    float* sO = sP + kC * kLdC;        // C x ldR:  dO slice
     float* sdU = sO + kC * ldR;        // C x ldR
-    float* sg = sdU + kC * ldR;        // gam [C]
     const float* df = p.dfinal ? p.dfinal + (((size_t)n * p.HV + h) * dv + r0) * dk : nullptr;
     for (int i = threadIdx.x; i < R * dk; i += blockDim.x) {
         const int r = i / dk, j = i - r * dk;
@@ -367,61 +466,34 @@ __global__ void __launch_bounds__(kNTs) bwd_state_bwd_kernel(BwdParams p, int R)
         const int t0 = bos + j * kC, len = min(kC, eos - t0);
         const size_t ci = ch_index(p, c, h);
         __syncthreads();
-        float* Dg = p.Db + ci * dv * dk + (size_t)r0 * dk;
-        for (int i = threadIdx.x; i < R * dk; i += blockDim.x) {
-            const int r = i / dk, jj = i - r * dk;
-            Dg[i] = sD[r * kLdD + jj];
-        }
-        for (int i = threadIdx.x; i < kC; i += blockDim.x) sg[i] = i < len ? p.gam[(size_t)(t0 + i) * p.HV + h] : 0.f;
+        store_rows_f32(p.Db + ci * dv * dk + (size_t)r0 * dk, dk, sD, kLdD, R, dk);
+        load_rows_f32_async(sQ, kLdD, p.GQb + ci * kC * dk, dk, kC, kC, dk);
+        load_rows_f32_async(sW, kLdD, p.BKb + ci * kC * dk, dk, kC, kC, dk);
+        load_rows_f32_async(sP, kLdC, p.Pb + ci * kC * kC, kC, kC, kC, kC);
         load_rows_any(sO, ldR, p.dout, ((size_t)t0 * p.HV + h) * dv + r0, (size_t)p.HV * dv, kC, len, R, p.dtype);
-        load_rows_f32(sQ, kLdD, p.qn + ((size_t)t0 * p.HK + hk) * dk, (size_t)p.HK * dk, kC, len, dk);
-        load_rows_f32(sW, kLdD, p.kn + ((size_t)t0 * p.HK + hk) * dk, (size_t)p.HK * dk, kC, len, dk);
-        __syncthreads();
-        const float gl = sg[len - 1];
-        const float* QK = p.QKb + ci * kC * kC;
-        for (int i = threadIdx.x; i < kC * kC; i += blockDim.x) {
-            const int r = i / kC, s = i - r * kC;
-            sP[r * kLdC + s] = (s <= r && r < len) ? QK[i] * expf(sg[r] - sg[s]) : 0.f;
-        }
-        for (int i = threadIdx.x; i < kC * dk; i += blockDim.x) {
-            const int r = i / dk, jj = i - r * dk;
-            if (r < len) sW[r * kLdD + jj] *= expf(gl - sg[r]);  // b K
-        }
+        const float Gl = __expf(p.gam[(size_t)(t0 + len - 1) * p.HV + h]);
+        cp_async_wait_all();
         __syncthreads();
         // dU = P^T dO + (b K) D^T   (C x R)
-        cta_gemm(kC, R, kC, sP, 1, kLdC, sO, ldR, 1, [&](int s, int i, float x) { sdU[s * ldR + i] = x; });
+        bgemm(kC, R, kC, sP, 1, kLdC, sO, ldR, 1, [&](int s, int i, float x) { sdU[s * ldR + i] = x; });
         __syncthreads();
         float* dUg = p.dUb + ci * kC * dv + r0;
-        cta_gemm(kC, R, dk, sW, kLdD, 1, sD, 1, kLdD, [&](int s, int i, float x) {
+        bgemm(kC, R, dk, sW, kLdD, 1, sD, 1, kLdD, [&](int s, int i, float x) {
             const float u = sdU[s * ldR + i] + x;
             sdU[s * ldR + i] = u;
             dUg[(size_t)s * dv + i] = u;
         });
         __syncthreads();
-        // W into sW, Gam Q in sQ
-        load_rows_f32(sW, kLdD, p.Wb + ci * kC * dk, dk, kC, kC, dk);
-        for (int i = threadIdx.x; i < kC * dk; i += blockDim.x) {
-            const int r = i / dk, jj = i - r * dk;
-            if (r < len) sQ[r * kLdD + jj] *= expf(sg[r]);
-        }
+        // W into sW (overlapping the next product), then D <- Gam_last D + dO^T (Gam Q) - dU^T W
+        load_rows_f32_async(sW, kLdD, p.Wb + ci * kC * dk, dk, kC, kC, dk);
+        bgemm(R, dk, kC, sO, 1, ldR, sQ, kLdD, 1,
+              [&](int i, int jj, float x) { sD[i * kLdD + jj] = fmaf(Gl, sD[i * kLdD + jj], x); });
+        cp_async_wait_all();
         __syncthreads();
-        // D <- Gam_last D + dO^T (Gam Q) - dU^T W
-        const float Gl = expf(gl);
-        cta_gemm(R, dk, kC, sO, 1, ldR, sQ, kLdD, 1, [&](int i, int jj, float x) {
-            sD[i * kLdD + jj] = fmaf(Gl, sD[i * kLdD + jj], x);
-        });
-        __syncthreads();
-        cta_gemm(R, dk, kC, sdU, 1, ldR, sW, kLdD, 1,
-                 [&](int i, int jj, float x) { sD[i * kLdD + jj] -= x; });
+        bgemm(R, dk, kC, sdU, 1, ldR, sW, kLdD, 1, [&](int i, int jj, float x) { sD[i * kLdD + jj] -= x; });
     }
     __syncthreads();
-    if (p.dinit) {
-        float* di = p.dinit + (((size_t)n * p.HV + h) * dv + r0) * dk;
-        for (int i = threadIdx.x; i < R * dk; i += blockDim.x) {
-            const int r = i / dk, j = i - r * dk;
-            di[i] = sD[r * kLdD + j];
-        }
-    }
+    if (p.dinit) store_rows_f32(p.dinit + (((size_t)n * p.HV + h) * dv + r0) * dk, dk, sD, kLdD, R, dk);
 }
 
 // ---------------------------------------------------------------------------
@@ -467,11 +539,11 @@ __global__ void __launch_bounds__(kNT) bwd_intra_s_kernel(BwdParams p) {
     __syncthreads();
     const float gl = sg[len - 1];
     // dQ_S = diag(Gam) dO S0
-    cta_gemm(kC, dk, dv, sA, kLdD, 1, sBig, kLdD, 1,
-             [&](int r, int j, float x) { sX[r * kLdD + j] = (r < len) ? expf(sg[r]) * x : 0.f; });
+    bgemm(kC, dk, dv, sA, kLdD, 1, sBig, kLdD, 1,
+             [&](int r, int j, float x) { sX[r * kLdD + j] = (r < len) ? __expf(sg[r]) * x : 0.f; });
     // dW = -dU S0
     float* dW = p.Wb + ci * kC * dk;
-    cta_gemm(kC, dk, dv, sC, kLdD, 1, sBig, kLdD, 1, [&](int r, int j, float x) { dW[r * dk + j] = -x; });
+    bgemm(kC, dk, dv, sC, kLdD, 1, sBig, kLdD, 1, [&](int r, int j, float x) { dW[r * dk + j] = -x; });
     __syncthreads();
     float* dq = p.dqh;
     for (int i = threadIdx.x; i < kC * dk; i += blockDim.x) {
@@ -492,9 +564,28 @@ __global__ void __launch_bounds__(kNT) bwd_intra_s_kernel(BwdParams p) {
     // <D, S0> with D read from global against S0 in shared memory
     const float* Dg = p.Db + ci * dv * dk;
     float part = 0.f;
-    for (int i = threadIdx.x; i < dv * dk; i += blockDim.x) {
-        const int r = i / dk, j = i - r * dk;
-        part = fmaf(Dg[i], sBig[r * kLdD + j], part);
+    {
+        const int c4 = dk >> 2, total = dv * c4;
+        for (int i0 = threadIdx.x; i0 < total; i0 += 4 * blockDim.x) {
+            float4 d4[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u * blockDim.x;
+                d4[u] = i < total ? *reinterpret_cast<const float4*>(Dg + (size_t)4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u * blockDim.x;
+                if (i < total) {
+                    const int r = i / c4, j = (i - r * c4) << 2;
+                    const float* sp = sBig + r * kLdD + j;
+                    part = fmaf(d4[u].x, sp[0], part);
+                    part = fmaf(d4[u].y, sp[1], part);
+                    part = fmaf(d4[u].z, sp[2], part);
+                    part = fmaf(d4[u].w, sp[3], part);
+                }
+            }
+        }
     }
     const float dS = cta_sum(part, red);
     __syncthreads();
@@ -503,12 +594,12 @@ __global__ void __launch_bounds__(kNT) bwd_intra_s_kernel(BwdParams p) {
     load_rows_f32(sA, kLdD, p.Ub + ci * kC * dv, dv, kC, kC, dv);
     load_rows_f32(sB, kLdD, p.kn + ((size_t)t0 * p.HK + hk) * dk, (size_t)p.HK * dk, kC, len, dk);
     __syncthreads();
-    cta_gemm(kC, dk, dv, sA, kLdD, 1, sBig, kLdD, 1, [&](int r, int j, float x) { sC[r * kLdD + j] = x; });
+    bgemm(kC, dk, dv, sA, kLdD, 1, sBig, kLdD, 1, [&](int r, int j, float x) { sC[r * kLdD + j] = x; });
     __syncthreads();
     float* dkk = p.dkh;
     for (int i = threadIdx.x; i < kC * dk; i += blockDim.x) {
         const int r = i / dk, j = i - r * dk;
-        if (r < len) dkk[((size_t)(t0 + r) * p.HV + h) * dk + j] = expf(gl - sg[r]) * sC[r * kLdD + j];
+        if (r < len) dkk[((size_t)(t0 + r) * p.HV + h) * dk + j] = __expf(gl - sg[r]) * sC[r * kLdD + j];
     }
     __syncthreads();
     {
@@ -518,7 +609,7 @@ __global__ void __launch_bounds__(kNT) bwd_intra_s_kernel(BwdParams p) {
             for (int j = lane; j < dk; j += 32) s = fmaf(sB[r * kLdD + j], sC[r * kLdD + j], s);
 #pragma unroll
             for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
-            if (lane == 0) sX[r] = expf(gl - sg[r]) * s;  // b_s db_s (sX reused as scratch)
+            if (lane == 0) sX[r] = __expf(gl - sg[r]) * s;  // b_s db_s (sX reused as scratch)
         }
     }
     __syncthreads();
@@ -526,7 +617,7 @@ __global__ void __launch_bounds__(kNT) bwd_intra_s_kernel(BwdParams p) {
         float tot = 0.f;
         for (int r = 0; r < len; ++r) tot += sX[r];
         for (int r = 0; r < len; ++r) sdg[r] -= sX[r];
-        sdg[len - 1] += tot + expf(gl) * dS;
+        sdg[len - 1] += tot + __expf(gl) * dS;
     }
     __syncthreads();
     float* dga = p.dgamA + ci * kC;
@@ -569,20 +660,20 @@ __global__ void __launch_bounds__(kNT) bwd_intra_c_kernel(BwdParams p) {
     for (int i = threadIdx.x; i < kC * kLdC; i += blockDim.x) sE[i] = 0.f;
     __syncthreads();
     // c1: dP = dO U^T -> dQK = lower(dP) * E, dE = lower(dP) * QK
-    cta_gemm(kC, kC, dv, sA, kLdD, 1, sB, 1, kLdD, [&](int r, int s, float x) {
+    bgemm(kC, kC, dv, sA, kLdD, 1, sB, 1, kLdD, [&](int r, int s, float x) {
         const bool in = (s <= r) && (r < len);
-        const float e = in ? expf(sg[r] - sg[s]) : 0.f;
+        const float e = in ? __expf(sg[r] - sg[s]) : 0.f;
         s2[r * kLdC + s] = in ? x * e : 0.f;
         sE[r * kLdC + s] = in ? x * s1[r * kLdC + s] : 0.f;
     });
     __syncthreads();
     float* dq = p.dqh;
     float* dkk = p.dkh;
-    cta_gemm(kC, dk, kC, s2, kLdC, 1, sK, kLdD, 1, [&](int r, int j, float x) {
+    bgemm(kC, dk, kC, s2, kLdC, 1, sK, kLdD, 1, [&](int r, int j, float x) {
         if (r < len) dq[((size_t)(t0 + r) * p.HV + h) * dk + j] += x;
     });
     __syncthreads();
-    cta_gemm(kC, dk, kC, s2, 1, kLdC, sCb, kLdD, 1, [&](int s, int j, float x) {
+    bgemm(kC, dk, kC, s2, 1, kLdC, sCb, kLdD, 1, [&](int s, int j, float x) {
         if (s < len) dkk[((size_t)(t0 + s) * p.HV + h) * dk + j] += x;
     });
     __syncthreads();
@@ -592,8 +683,8 @@ __global__ void __launch_bounds__(kNT) bwd_intra_c_kernel(BwdParams p) {
     load_rows_f32(sCb, kLdD, p.dUb + ci * kC * dv, dv, kC, kC, dv);
     __syncthreads();
     // F1 = dW K^T, F2 = dU V^T
-    cta_gemm(kC, kC, dk, sA, kLdD, 1, sK, 1, kLdD, [&](int s, int r, float x) { s1[s * kLdC + r] = x; });
-    cta_gemm(kC, kC, dv, sCb, kLdD, 1, sB, 1, kLdD, [&](int s, int r, float x) { s2[s * kLdC + r] = x; });
+    bgemm(kC, kC, dk, sA, kLdD, 1, sK, 1, kLdD, [&](int s, int r, float x) { s1[s * kLdC + r] = x; });
+    bgemm(kC, kC, dv, sCb, kLdD, 1, sB, 1, kLdD, [&](int s, int r, float x) { s2[s * kLdC + r] = x; });
     __syncthreads();
     // column dots with T: dbeta_r, dgam_r; then dT(s,r) = beta_r (Gam_r F1 + F2)
     if (threadIdx.x < kC) {
@@ -603,37 +694,37 @@ __global__ void __launch_bounds__(kNT) bwd_intra_c_kernel(BwdParams p) {
             a1 = fmaf(sT[s * kLdC + r], s1[s * kLdC + r], a1);
             a2 = fmaf(sT[s * kLdC + r], s2[s * kLdC + r], a2);
         }
-        const float Gr = expf(sg[r]);
+        const float Gr = __expf(sg[r]);
         sdb[r] += Gr * a1 + a2;
         sdg[r] += Gr * sbe[r] * a1;
     }
     __syncthreads();
     for (int i = threadIdx.x; i < kC * kC; i += blockDim.x) {
         const int s = i / kC, r = i - s * kC;
-        s1[s * kLdC + r] = sbe[r] * fmaf(expf(sg[r]), s1[s * kLdC + r], s2[s * kLdC + r]);
+        s1[s * kLdC + r] = sbe[r] * fmaf(__expf(sg[r]), s1[s * kLdC + r], s2[s * kLdC + r]);
     }
     __syncthreads();
     // dK += diag(beta Gam) T^T dW;  dV = diag(beta) T^T dU
-    cta_gemm(kC, dk, kC, sT, 1, kLdC, sA, kLdD, 1, [&](int r, int j, float x) {
-        if (r < len) dkk[((size_t)(t0 + r) * p.HV + h) * dk + j] += sbe[r] * expf(sg[r]) * x;
+    bgemm(kC, dk, kC, sT, 1, kLdC, sA, kLdD, 1, [&](int r, int j, float x) {
+        if (r < len) dkk[((size_t)(t0 + r) * p.HV + h) * dk + j] += sbe[r] * __expf(sg[r]) * x;
     });
-    cta_gemm(kC, dv, kC, sT, 1, kLdC, sCb, kLdD, 1, [&](int r, int j, float x) {
+    bgemm(kC, dv, kC, sT, 1, kLdC, sCb, kLdD, 1, [&](int r, int j, float x) {
         if (r < len) st_any(p.dv_out, ((size_t)(t0 + r) * p.HV + h) * dv + j, p.dtype, sbe[r] * x);
     });
     // c4: Z = dT T^T -> s2;  dA = -T^T Z (strictly lower) -> s1
-    cta_gemm(kC, kC, kC, s1, kLdC, 1, sT, 1, kLdC, [&](int a, int b, float x) { s2[a * kLdC + b] = x; });
+    bgemm(kC, kC, kC, s1, kLdC, 1, sT, 1, kLdC, [&](int a, int b, float x) { s2[a * kLdC + b] = x; });
     __syncthreads();
-    cta_gemm(kC, kC, kC, sT, 1, kLdC, s2, kLdC, 1,
+    bgemm(kC, kC, kC, sT, 1, kLdC, s2, kLdC, 1,
              [&](int r, int s, float x) { s1[r * kLdC + s] = (s < r) ? -x : 0.f; });
     __syncthreads();
     // c5: KK = K K^T -> s2; dbeta_r += sum_s dA E KK; dKK = dA beta_r E -> s1; dE += dA beta_r KK
-    cta_gemm(kC, kC, dk, sK, kLdD, 1, sK, 1, kLdD, [&](int r, int s, float x) { s2[r * kLdC + s] = x; });
+    bgemm(kC, kC, dk, sK, kLdD, 1, sK, 1, kLdD, [&](int r, int s, float x) { s2[r * kLdC + s] = x; });
     __syncthreads();
     if (threadIdx.x < kC) {
         const int r = threadIdx.x;
         float acc = 0.f;
         for (int s = 0; s < r; ++s) {
-            const float a = s1[r * kLdC + s], e = expf(sg[r] - sg[s]), kk = s2[r * kLdC + s];
+            const float a = s1[r * kLdC + s], e = __expf(sg[r] - sg[s]), kk = s2[r * kLdC + s];
             acc = fmaf(a * e, kk, acc);
             s1[r * kLdC + s] = a * sbe[r] * e;
             sE[r * kLdC + s] = fmaf(a * sbe[r], kk, sE[r * kLdC + s]);
@@ -646,7 +737,7 @@ __global__ void __launch_bounds__(kNT) bwd_intra_c_kernel(BwdParams p) {
         s2[r * kLdC + s] = s1[r * kLdC + s] + s1[s * kLdC + r];
     }
     __syncthreads();
-    cta_gemm(kC, dk, kC, s2, kLdC, 1, sK, kLdD, 1, [&](int r, int j, float x) {
+    bgemm(kC, dk, kC, s2, kLdC, 1, sK, kLdD, 1, [&](int r, int j, float x) {
         if (r < len) dkk[((size_t)(t0 + r) * p.HV + h) * dk + j] += x;
     });
     // c6: dgam from E (row sums minus column sums of dE * E), then dg = reverse cumsum
@@ -654,8 +745,8 @@ __global__ void __launch_bounds__(kNT) bwd_intra_c_kernel(BwdParams p) {
         const int r = threadIdx.x;
         float rs = 0.f, cs = 0.f;
         for (int s = 0; s < kC; ++s) {
-            rs = fmaf(sE[r * kLdC + s], expf(sg[r] - sg[s]), rs);
-            cs = fmaf(sE[s * kLdC + r], expf(sg[s] - sg[r]), cs);
+            rs = fmaf(sE[r * kLdC + s], __expf(sg[r] - sg[s]), rs);
+            cs = fmaf(sE[s * kLdC + r], __expf(sg[s] - sg[r]), cs);
         }
         sdg[r] += rs - cs;
     }
@@ -706,7 +797,7 @@ __global__ void bwd_fold_kernel(BwdParams p) {
 
 // ---------------------------------------------------------------------------
 struct BwdLayout {
-    size_t coff, qn, kn, qinv, kinv, gam, W, Ut, T, QK, S, D, U, dU, dgA, dqh, dkh, total;
+    size_t coff, qn, kn, qinv, kinv, gam, W, Ut, T, QK, P, BK, GQ, S, D, U, dU, dgA, dqh, dkh, total;
     int nchm;
 };
 
@@ -729,6 +820,9 @@ static BwdLayout bwd_layout(const gdn_shape* s) {
     L.Ut = take(CH * kC * dv * 4);
     L.T = take(CH * kC * kC * 4);
     L.QK = take(CH * kC * kC * 4);
+    L.P = take(CH * kC * kC * 4);
+    L.BK = take(CH * kC * dk * 4);
+    L.GQ = take(CH * kC * dk * 4);
     L.S = take(CH * dv * dk * 4);
     L.D = take(CH * dv * dk * 4);
     L.U = take(CH * kC * dv * 4);
@@ -792,6 +886,9 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
     p.Utb = reinterpret_cast<float*>(ws + L.Ut);
     p.Tb = reinterpret_cast<float*>(ws + L.T);
     p.QKb = reinterpret_cast<float*>(ws + L.QK);
+    p.Pb = reinterpret_cast<float*>(ws + L.P);
+    p.BKb = reinterpret_cast<float*>(ws + L.BK);
+    p.GQb = reinterpret_cast<float*>(ws + L.GQ);
     p.Sb = reinterpret_cast<float*>(ws + L.S);
     p.Db = reinterpret_cast<float*>(ws + L.D);
     p.Ub = reinterpret_cast<float*>(ws + L.U);
@@ -818,13 +915,13 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
     bwd_wy_kernel<<<gch, kNT, smem_wy, cs>>>(p);
     if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
 
-    const int R = std::min(kRowsSlice, s->dv);
+    const int R = s->dv;  // one CTA per (sequence, head) holds every row of the state
     const dim3 gseq(s->N, s->HV, s->dv / R);
-    const size_t smem_sf = sizeof(float) * (R * kLdD + 2 * kC * kLdD + kC * (R + 1) + kC);
+    const size_t smem_sf = sizeof(float) * (R * kLdD + 2 * kC * kLdD + 2 * kC * (R + 4));
     if (!set_smem(bwd_state_fwd_kernel, smem_sf)) return GDN_ERR_CUDA;
     bwd_state_fwd_kernel<<<gseq, kNTs, smem_sf, cs>>>(p, R);
     if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
-    const size_t smem_sb = sizeof(float) * (R * kLdD + 2 * kC * kLdD + kC * kLdC + 2 * kC * (R + 1) + kC);
+    const size_t smem_sb = sizeof(float) * (R * kLdD + 2 * kC * kLdD + kC * kLdC + 2 * kC * (R + 4));
     if (!set_smem(bwd_state_bwd_kernel, smem_sb)) return GDN_ERR_CUDA;
     bwd_state_bwd_kernel<<<gseq, kNTs, smem_sb, cs>>>(p, R);
     if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
