@@ -166,10 +166,20 @@ __global__ void __launch_bounds__(kThreadsPer128Rows, 2)
             const int t0 = bos + c * kTC;
             const int tc = min(kTC, eos - t0);
             if (!mbar_wait_bounded(&sm.bar[st], (uint32_t)((c / kStages) & 1))) sm.abort_flag = 1;
-            for (int j = warp; j < 2 * tc; j += nwarps) {
-                const int t = j >> 1;
-                if (j & 1) l2norm_warp<DK>(sm.k[st] + t * DK, sm.kn + t * DK, lane, p.use_norm);
-                else l2norm_warp<DK>(sm.q[st] + t * DK, sm.qn + t * DK, lane, p.use_norm);
+            // normalise the chunk's 2*tc q/k vectors, four per warp at a time
+            for (int j0 = warp; j0 < 2 * tc; j0 += 4 * nwarps) {
+                const Tin* src[4];
+                float* dst[4];
+                int nv = 0;
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const int j = j0 + v * nwarps, t = j >> 1;
+                    const bool ok = j < 2 * tc;
+                    nv += ok;
+                    src[v] = ok ? ((j & 1) ? sm.k[st] + t * DK : sm.q[st] + t * DK) : sm.q[st];
+                    dst[v] = ok ? ((j & 1) ? sm.kn + t * DK : sm.qn + t * DK) : sm.qn;
+                }
+                l2norm_warp_multi<DK, 4>(src, dst, nv, lane, p.use_norm);
             }
             if (tid < tc) sm.ab[tid] = make_float2(gate_alpha(gb.x), gb.y);
             __syncthreads();
@@ -182,15 +192,32 @@ __global__ void __launch_bounds__(kThreadsPer128Rows, 2)
                 gb = make_float2(p.g[gi], p.beta[gi]);
             }
             const Tin* __restrict__ vs = sm.v[st];
+            // Token loop, software-pipelined by one token: the lane butterfly of
+            // token t's output runs next to token t+1's u butterfly (it is off
+            // the recurrence's critical path); every operation is unchanged.
+            float opend[R];
             for (int t = 0; t < tc; ++t) {
                 const float2 ab = sm.ab[t];
-                float vv[R], o[R];
+                float vv[R], u[R], w[R], oprev[R];
 #pragma unroll
                 for (int r = 0; r < R; ++r) vv[r] = 0.f;
                 if (active) ld_rows_in<R>(vs + t * dvs + grp * R, vv);
-                token_step<DK, R>(S, sm.kn + t * DK, sm.qn + t * DK, e, ab.x, ab.y, vv, o);
-                if (active && e == 0) st_rows_out<R>(out + ((size_t)(t0 + t) * p.HV + h) * p.dv + row, o);
+                rows_dot_part<DK, R>(S, sm.kn + t * DK, e, u);
+                if (t > 0) {
+#pragma unroll
+                    for (int r = 0; r < R; ++r) oprev[r] = lanes_reduce(opend[r]);
+                }
+#pragma unroll
+                for (int r = 0; r < R; ++r) u[r] = lanes_reduce(u[r]);
+                if (t > 0 && active && e == 0)
+                    st_rows_out<R>(out + ((size_t)(t0 + t - 1) * p.HV + h) * p.dv + row, oprev);
+#pragma unroll
+                for (int r = 0; r < R; ++r) w[r] = delta_w(ab.x, ab.y, vv[r], u[r]);
+                rows_update_part<DK, R>(S, sm.kn + t * DK, sm.qn + t * DK, e, ab.x, w, opend);
             }
+#pragma unroll
+            for (int r = 0; r < R; ++r) opend[r] = lanes_reduce(opend[r]);
+            if (active && e == 0) st_rows_out<R>(out + ((size_t)(t0 + tc - 1) * p.HV + h) * p.dv + row, opend);
             __syncthreads();
             if (tid == 0 && c + kStages < nchunks)
                 issue_chunk(sm, &tm_q, &tm_k, &tm_v, c + kStages, bos, hk, h, slice * dvs, bytes);

@@ -46,12 +46,17 @@ static_assert(kRowsPerThread == 1 || kRowsPerThread == 2 || kRowsPerThread == 4,
 // threads that hold a 128-row state slice
 constexpr int kThreadsPer128Rows = 128 * kLanesPerRow / kRowsPerThread;
 
+// accumulator chain length: a lane's chunks are summed in kSets interleaved sets
+#ifndef GDN_CHAIN
+#define GDN_CHAIN 8
+#endif
 template <int DK>
 struct RowFrag {
     static_assert(DK % (4 * kLanesPerRow) == 0, "dk must be a multiple of 4 L");
     static constexpr int kChunks = DK / (4 * kLanesPerRow);
-    static constexpr int kSets = kChunks >= 16 ? kChunks / 8 : 1;
-    float4 c[kChunks];
+    static constexpr int kSets = kChunks >= 2 * GDN_CHAIN ? kChunks / GDN_CHAIN : 1;
+    // chunk i = elements (4c .. 4c+3), kept as the register pairs (x, y) = p[2i], (z, w) = p[2i+1]
+    float2 p[2 * kChunks];
 };
 
 __device__ __forceinline__ int chunk_of(int i, int e) { return kLanesPerRow * i + e; }
@@ -128,13 +133,54 @@ __device__ __forceinline__ void l2norm_warp(const Tin* __restrict__ src, float* 
     if (own) *reinterpret_cast<float4*>(dst + 4 * lane) = x;
 }
 
+// NV vectors at once with exactly l2norm_warp's per-vector operations (the
+// independent chains interleave); vectors v >= nvalid are skipped.
+template <int DK, int NV, typename Tin>
+__device__ __forceinline__ void l2norm_warp_multi(const Tin* const (&src)[NV], float* const (&dst)[NV], int nvalid,
+                                                  int lane, bool use_norm) {
+    float4 x[NV];
+    const bool own = lane < DK / 4;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        x[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (own && v < nvalid) x[v] = ld4_in(src[v] + 4 * lane);
+    }
+    if (use_norm) {
+        float ss[NV];
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            ss[v] = __fmul_rn(x[v].x, x[v].x);
+            ss[v] = __fmaf_rn(x[v].y, x[v].y, ss[v]);
+            ss[v] = __fmaf_rn(x[v].z, x[v].z, ss[v]);
+            ss[v] = __fmaf_rn(x[v].w, x[v].w, ss[v]);
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+#pragma unroll
+            for (int v = 0; v < NV; ++v) ss[v] = __fadd_rn(ss[v], __shfl_xor_sync(kFull, ss[v], off));
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const float inv = __frsqrt_rn(__fadd_rn(ss[v], kNormEps));
+            x[v].x = __fmul_rn(x[v].x, inv);
+            x[v].y = __fmul_rn(x[v].y, inv);
+            x[v].z = __fmul_rn(x[v].z, inv);
+            x[v].w = __fmul_rn(x[v].w, inv);
+        }
+    }
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+        if (own && v < nvalid) *reinterpret_cast<float4*>(dst[v] + 4 * lane) = x[v];
+}
+
 // Gate values for one token: a = exp(g) (CUDA's expf, same call everywhere), b as given.
 __device__ __forceinline__ float gate_alpha(float g) { return expf(g); }
 
-// Finish of a dk contraction from per-set packed accumulators: sets in
-// increasing order, (x + y) + (z + w), then the xor butterfly over the L lanes.
+// Finish of a dk contraction, in two parts that together are one fixed tree:
+// lane_partial: the sets in increasing order, then (x + y) + (z + w);
+// lanes_reduce: the xor butterfly over the L lanes of the row.  Splitting them
+// only lets a caller overlap one contraction's butterfly with other work.
 template <int NS>
-__device__ __forceinline__ float finish_dot(const float2 (&xy)[NS], const float2 (&zw)[NS]) {
+__device__ __forceinline__ float lane_partial(const float2 (&xy)[NS], const float2 (&zw)[NS]) {
     float2 a = xy[0], b = zw[0];
 #pragma unroll
     for (int j = 1; j < NS; ++j) {
@@ -143,10 +189,16 @@ __device__ __forceinline__ float finish_dot(const float2 (&xy)[NS], const float2
         b.x = __fadd_rn(b.x, zw[j].x);
         b.y = __fadd_rn(b.y, zw[j].y);
     }
-    float p = __fadd_rn(__fadd_rn(a.x, a.y), __fadd_rn(b.x, b.y));
+    return __fadd_rn(__fadd_rn(a.x, a.y), __fadd_rn(b.x, b.y));
+}
+__device__ __forceinline__ float lanes_reduce(float p) {
 #pragma unroll
     for (int m = 1; m < kLanesPerRow; m <<= 1) p = __fadd_rn(p, __shfl_xor_sync(kFull, p, m));
     return p;
+}
+template <int NS>
+__device__ __forceinline__ float finish_dot(const float2 (&xy)[NS], const float2 (&zw)[NS]) {
+    return lanes_reduce(lane_partial<NS>(xy, zw));
 }
 
 // u[r] = S_r . x for the R rows a thread holds; x is a dk fp32 vector in shared memory.
@@ -161,8 +213,8 @@ __device__ __forceinline__ float2 lo2(const float4& v) { return make_float2(v.x,
 __device__ __forceinline__ float2 hi2(const float4& v) { return make_float2(v.z, v.w); }
 
 template <int DK, int R>
-__device__ __forceinline__ void rows_dot(const RowFrag<DK> (&s)[R], const float* __restrict__ x,
-                                         int e, float (&u)[R]) {
+__device__ __forceinline__ void rows_dot_part(const RowFrag<DK> (&s)[R], const float* __restrict__ x,
+                                              int e, float (&u)[R]) {
     constexpr int NC = RowFrag<DK>::kChunks, NS = RowFrag<DK>::kSets;
     float2 xy[R][NS], zw[R][NS];
 #pragma unroll
@@ -177,18 +229,26 @@ __device__ __forceinline__ void rows_dot(const RowFrag<DK> (&s)[R], const float*
             float2& A = xy[r][i % NS];
             float2& B = zw[r][i % NS];
 #ifdef GDN_STEP_SCALAR
-            A.x = __fmaf_rn(s[r].c[i].x, k4.x, A.x);
-            A.y = __fmaf_rn(s[r].c[i].y, k4.y, A.y);
-            B.x = __fmaf_rn(s[r].c[i].z, k4.z, B.x);
-            B.y = __fmaf_rn(s[r].c[i].w, k4.w, B.y);
+            A.x = __fmaf_rn(s[r].p[2 * i].x, k4.x, A.x);
+            A.y = __fmaf_rn(s[r].p[2 * i].y, k4.y, A.y);
+            B.x = __fmaf_rn(s[r].p[2 * i + 1].x, k4.z, B.x);
+            B.y = __fmaf_rn(s[r].p[2 * i + 1].y, k4.w, B.y);
 #else
-            A = __ffma2_rn(lo2(s[r].c[i]), lo2(k4), A);
-            B = __ffma2_rn(hi2(s[r].c[i]), hi2(k4), B);
+            A = __ffma2_rn(s[r].p[2 * i], lo2(k4), A);
+            B = __ffma2_rn(s[r].p[2 * i + 1], hi2(k4), B);
 #endif
         }
     }
 #pragma unroll
-    for (int r = 0; r < R; ++r) u[r] = finish_dot<NS>(xy[r], zw[r]);
+    for (int r = 0; r < R; ++r) u[r] = lane_partial<NS>(xy[r], zw[r]);
+}
+
+template <int DK, int R>
+__device__ __forceinline__ void rows_dot(const RowFrag<DK> (&s)[R], const float* __restrict__ x,
+                                         int e, float (&u)[R]) {
+    rows_dot_part<DK, R>(s, x, e, u);
+#pragma unroll
+    for (int r = 0; r < R; ++r) u[r] = lanes_reduce(u[r]);
 }
 
 // w = b (v - a u)
@@ -199,9 +259,9 @@ __device__ __forceinline__ float delta_w(float a, float b, float v, float u) {
 // S_r <- a S_r + w_r k^T (per element fma(w, k_j, a * S_rj)), then o[r] = S_r . q.
 // Must be called by all 32 lanes of the warp.  Same two forms as rows_dot.
 template <int DK, int R>
-__device__ __forceinline__ void rows_update_out(RowFrag<DK> (&s)[R], const float* __restrict__ k,
-                                                const float* __restrict__ q, int e, float a,
-                                                const float (&w)[R], float (&o)[R]) {
+__device__ __forceinline__ void rows_update_part(RowFrag<DK> (&s)[R], const float* __restrict__ k,
+                                                 const float* __restrict__ q, int e, float a,
+                                                 const float (&w)[R], float (&o)[R]) {
     constexpr int NC = RowFrag<DK>::kChunks, NS = RowFrag<DK>::kSets;
     float2 xy[R][NS], zw[R][NS];
 #pragma unroll
@@ -217,30 +277,39 @@ __device__ __forceinline__ void rows_update_out(RowFrag<DK> (&s)[R], const float
         const float4 q4 = *reinterpret_cast<const float4*>(q + 4 * chunk_of(i, e));
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            float4& S = s[r].c[i];
+            float2& Sxy = s[r].p[2 * i];
+            float2& Szw = s[r].p[2 * i + 1];
             float2& A = xy[r][i % NS];
             float2& B = zw[r][i % NS];
 #ifdef GDN_STEP_SCALAR
-            S.x = __fmaf_rn(w[r], k4.x, __fmul_rn(a, S.x));
-            S.y = __fmaf_rn(w[r], k4.y, __fmul_rn(a, S.y));
-            S.z = __fmaf_rn(w[r], k4.z, __fmul_rn(a, S.z));
-            S.w = __fmaf_rn(w[r], k4.w, __fmul_rn(a, S.w));
-            A.x = __fmaf_rn(S.x, q4.x, A.x);
-            A.y = __fmaf_rn(S.y, q4.y, A.y);
-            B.x = __fmaf_rn(S.z, q4.z, B.x);
-            B.y = __fmaf_rn(S.w, q4.w, B.y);
+            Sxy.x = __fmaf_rn(w[r], k4.x, __fmul_rn(a, Sxy.x));
+            Sxy.y = __fmaf_rn(w[r], k4.y, __fmul_rn(a, Sxy.y));
+            Szw.x = __fmaf_rn(w[r], k4.z, __fmul_rn(a, Szw.x));
+            Szw.y = __fmaf_rn(w[r], k4.w, __fmul_rn(a, Szw.y));
+            A.x = __fmaf_rn(Sxy.x, q4.x, A.x);
+            A.y = __fmaf_rn(Sxy.y, q4.y, A.y);
+            B.x = __fmaf_rn(Szw.x, q4.z, B.x);
+            B.y = __fmaf_rn(Szw.y, q4.w, B.y);
 #else
             const float2 w2 = make_float2(w[r], w[r]);
-            const float2 sxy = __ffma2_rn(w2, lo2(k4), __fmul2_rn(a2, lo2(S)));
-            const float2 szw = __ffma2_rn(w2, hi2(k4), __fmul2_rn(a2, hi2(S)));
-            S = make_float4(sxy.x, sxy.y, szw.x, szw.y);
-            A = __ffma2_rn(sxy, lo2(q4), A);
-            B = __ffma2_rn(szw, hi2(q4), B);
+            Sxy = __ffma2_rn(w2, lo2(k4), __fmul2_rn(a2, Sxy));
+            Szw = __ffma2_rn(w2, hi2(k4), __fmul2_rn(a2, Szw));
+            A = __ffma2_rn(Sxy, lo2(q4), A);
+            B = __ffma2_rn(Szw, hi2(q4), B);
 #endif
         }
     }
 #pragma unroll
-    for (int r = 0; r < R; ++r) o[r] = finish_dot<NS>(xy[r], zw[r]);
+    for (int r = 0; r < R; ++r) o[r] = lane_partial<NS>(xy[r], zw[r]);
+}
+
+template <int DK, int R>
+__device__ __forceinline__ void rows_update_out(RowFrag<DK> (&s)[R], const float* __restrict__ k,
+                                                const float* __restrict__ q, int e, float a,
+                                                const float (&w)[R], float (&o)[R]) {
+    rows_update_part<DK, R>(s, k, q, e, a, w, o);
+#pragma unroll
+    for (int r = 0; r < R; ++r) o[r] = lanes_reduce(o[r]);
 }
 
 // One full token for the R rows of a thread: u, w, update, o.
@@ -262,8 +331,11 @@ __device__ __forceinline__ void load_rows(RowFrag<DK> (&s)[R], const float* __re
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int i = 0; i < RowFrag<DK>::kChunks; ++i)
-            s[r].c[i] = __ldcs(reinterpret_cast<const float4*>(row0 + (size_t)r * DK + 4 * chunk_of(i, e)));
+        for (int i = 0; i < RowFrag<DK>::kChunks; ++i) {
+            const float4 v = __ldcs(reinterpret_cast<const float4*>(row0 + (size_t)r * DK + 4 * chunk_of(i, e)));
+            s[r].p[2 * i] = make_float2(v.x, v.y);
+            s[r].p[2 * i + 1] = make_float2(v.z, v.w);
+        }
 }
 
 template <int DK, int R>
@@ -271,7 +343,7 @@ __device__ __forceinline__ void zero_rows(RowFrag<DK> (&s)[R]) {
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int i = 0; i < RowFrag<DK>::kChunks; ++i) s[r].c[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < 2 * RowFrag<DK>::kChunks; ++i) s[r].p[i] = make_float2(0.f, 0.f);
 }
 
 template <int DK, int R>
@@ -280,7 +352,8 @@ __device__ __forceinline__ void store_rows(const RowFrag<DK> (&s)[R], float* __r
     for (int r = 0; r < R; ++r)
 #pragma unroll
         for (int i = 0; i < RowFrag<DK>::kChunks; ++i)
-            __stcs(reinterpret_cast<float4*>(row0 + (size_t)r * DK + 4 * chunk_of(i, e)), s[r].c[i]);
+            __stcs(reinterpret_cast<float4*>(row0 + (size_t)r * DK + 4 * chunk_of(i, e)),
+                   make_float4(s[r].p[2 * i].x, s[r].p[2 * i].y, s[r].p[2 * i + 1].x, s[r].p[2 * i + 1].y));
 }
 
 }  // namespace gdn
