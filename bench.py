@@ -54,6 +54,8 @@ def parse():
                     help="tiny run for ncu captures: 8 sequences, 2 steps, no extras")
     ap.add_argument("--profile-balanced", action="store_true",
                     help="ncu run at full occupancy: 9 sequences x 4096 tokens (288 units), 2 steps, no extras")
+    ap.add_argument("--profile-backward", action="store_true",
+                    help="ncu run of the backward alone: 2 x 4096 tokens, 2 calls")
     return ap.parse_args()
 
 
@@ -221,10 +223,27 @@ def run_reference(args):
     }), flush=True)
 
 
+def profile_backward():
+    """Two gdn_chunk_bwd calls on 2 x 4096 tokens (HK=16, HV=32, dk=dv=128, bf16), for ncu."""
+    import invariant_linear_attention_gb300 as gdn
+    from invariant_linear_attention_gb300 import inputs
+    dev = torch.device("cuda", 0)
+    x = inputs.make_inputs([BWD_L] * 2, HK=HK, HV=HV, dk=DK, dv=DV, dtype=torch.bfloat16, seed=6, device=dev)
+    dO = inputs.grad_out(2 * BWD_L, HV, DV, seed=6, device=dev)
+    ws = torch.zeros(gdn.gdn_workspace_size(gdn.make_shape(x.q, x.v, 2), 2), dtype=torch.uint8, device=dev)
+    for _ in range(2):
+        gdn.gdn_chunk_bwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, dO, workspace=ws)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_backward": "ok"}))
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.profile_backward:
+        profile_backward()
         return
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -334,6 +353,11 @@ def main():
                              f"call time (scheduler included); peak = {sms} SMs x 128 FP32 lanes x 2 flop x "
                              f"{max_mhz:.0f} MHz (derived from unit counts and max clock); the algorithm's "
                              f"3 FMA + 1 MUL mix caps frac at 0.875"},
+        "decode_roofline": {"bound": "hbm", "kernel": "gdn_decode_kernel", "achieved": dec_gbs, "peak": hbm_peak,
+                            "unit": "GB/s", "frac": dec_gbs / hbm_peak,
+                            "traffic": (lambda t: t["bytes_per_launch"] if t else None)(
+                                load_traffic("gdn_decode_kernel", src_sha(DEC_SRC))),
+                            "note": "2 x B x HV x dv x dk x 4 B state round trip + token I/O per step"},
         "gpu_launches": 3 * steps,
         "clocks": clk,
     }
