@@ -371,6 +371,10 @@ def main():
         result["invariance"] = {"dv_slice_128_vs_32_bitwise_equal": bool(torch.equal(out.view(torch.int16),
                                                                                      out2.view(torch.int16)))}
 
+    # ---- prefix-cache snapshots every 256 tokens on the same prefill
+    if rank == 0 and not small:
+        result["prefill_snapshots"] = bench_snapshots(gdn, d, dev, ws)
+
     # ---- end to end through the C ABI from pinned host buffers
     if not args.no_e2e and not small:
         result["e2e"] = e2e(gdn, d.cpu(), dd.cpu(), st0.cpu(), dev, steps=min(steps, 5))
@@ -475,6 +479,30 @@ def e2e(gdn, x, dec, dec_state, dev, steps):
     tokens = x.q.shape[0] + dec.q.shape[0]
     return {"value": tokens / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+def bench_snapshots(gdn, d, dev, ws, every=256, reps=3):
+    """The throughput prefill with fp32 state snapshots every `every` tokens of each sequence."""
+    snap_cu = gdn.snapshot_offsets(d.lengths, every).to(dev)
+    slots = int(snap_cu[-1].item())
+    snaps = torch.empty(slots, HV, DV, DK, dtype=torch.float32, device=dev)
+    out = torch.empty_like(d.v)
+    fs = torch.empty(len(d.lengths), HV, DV, DK, dtype=torch.float32, device=dev)
+    run = lambda: gdn.gdn_recurrent_fwd_snapshots(d.q, d.k, d.v, d.g, d.beta, d.cu_seqlens, every,  # noqa: E731
+                                                  snap_cu=snap_cu, snap_states=snaps, out=out, final_state=fs,
+                                                  workspace=ws)
+    run()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        run()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    T = d.q.shape[0]
+    return {"every": every, "snapshots": slots, "snapshot_bytes": slots * HV * DV * DK * 4, "ms": ms,
+            "tokens_per_s": T / (ms / 1e3)}
 
 
 def bench_backward(gdn, dev, steps=3):

@@ -101,6 +101,32 @@ gdn_status gdn_recurrent_fwd(const gdn_shape* shape, const void* q, const void* 
                              void* stream);
 
 /*
+ * gdn_recurrent_fwd that also keeps state snapshots for prefix caching (the
+ * pages reuse vLLM's state snapshotting under --mamba-cache-mode align so that
+ * prefix caching keeps working with the recurrent kernel: "Defending Against
+ * the Training-Inference Numeric Mismatch in RL (Especially Linear
+ * Attention)", section 3.2).  For every sequence n, after each snap_every-th
+ * token of that sequence (token counts snap_every, 2*snap_every, ...), the
+ * fp32 state is written to snap_states[snap_cu[n] + m - 1] for the m-th
+ * snapshot, as long as that slot is below snap_cu[n + 1] and num_snap_slots;
+ * snap_states is [num_snap_slots, HV, dv, dk], snap_cu int32 [N + 1] on the
+ * device (the caller sizes it, e.g. with floor(len_n / snap_every) slots per
+ * sequence).  snap_every must be a positive multiple of 32 (snapshots are
+ * taken at the kernel's 32-token chunk boundaries), else GDN_ERR_UNSUPPORTED;
+ * snap_states must not alias init_state or final_state.  Each snapshot is bit
+ * for bit the final_state of gdn_recurrent_fwd over that prefix, so resuming
+ * from it reproduces the rest of the sequence exactly.  Same workspace, launches
+ * and outputs as gdn_recurrent_fwd.
+ */
+gdn_status gdn_recurrent_fwd_snapshots(const gdn_shape* shape, const void* q, const void* k,
+                                       const void* v, const float* g, const float* beta,
+                                       const float* init_state, const int32_t* cu_seqlens,
+                                       void* out, float* final_state, int snap_every,
+                                       const int32_t* snap_cu, int num_snap_slots,
+                                       float* snap_states, void* workspace,
+                                       size_t workspace_bytes, void* stream);
+
+/*
  * One decode token per sequence on a cached fp32 state, updated in place.
  * shape->T_total must equal shape->N; q, k, v, g, beta, out hold one token
  * per sequence.  state is a pool [num_slots, HV, dv, dk]; sequence b uses

@@ -13,9 +13,11 @@ from .binding import (  # noqa: F401
     gdn_decode_step,
     gdn_recurrent_fwd,
     gdn_recurrent_fwd_noalloc,
+    gdn_recurrent_fwd_snapshots,
     gdn_workspace_size,
     lib,
     make_shape,
     read_device_error,
+    snapshot_offsets,
     status_string,
 )

@@ -23,7 +23,8 @@ DEVERR_CU_SEQLENS, DEVERR_TIMEOUT = 1, 2
 _P = ctypes.c_void_p
 
 SYMBOLS = ("gdn_workspace_size", "gdn_recurrent_fwd", "gdn_decode_step", "gdn_chunk_bwd",
-           "gdn_read_device_error", "gdn_status_string", "gdn_recurrent_fwd_noalloc")
+           "gdn_read_device_error", "gdn_status_string", "gdn_recurrent_fwd_noalloc",
+           "gdn_recurrent_fwd_snapshots")
 
 
 class GdnShape(ctypes.Structure):
@@ -52,6 +53,9 @@ def lib():
         L.gdn_recurrent_fwd.restype = ctypes.c_int
         L.gdn_recurrent_fwd_noalloc.argtypes = [ctypes.POINTER(GdnShape)] + [_P] * 10
         L.gdn_recurrent_fwd_noalloc.restype = ctypes.c_int
+        L.gdn_recurrent_fwd_snapshots.argtypes = ([ctypes.POINTER(GdnShape)] + [_P] * 9 +
+                                                  [ctypes.c_int, _P, ctypes.c_int, _P, _P, ctypes.c_size_t, _P])
+        L.gdn_recurrent_fwd_snapshots.restype = ctypes.c_int
         L.gdn_decode_step.argtypes = [ctypes.POINTER(GdnShape)] + [_P] * 7 + [ctypes.c_int, _P, _P]
         L.gdn_decode_step.restype = ctypes.c_int
         L.gdn_chunk_bwd.argtypes = [ctypes.POINTER(GdnShape)] + [_P] * 16 + [ctypes.c_size_t, _P]
@@ -187,6 +191,57 @@ def gdn_recurrent_fwd_noalloc(q, k, v, g, beta, cu_seqlens, init_state=None, out
                                              _ptr(final_state), _stream(stream))
     _check(rc, "gdn_recurrent_fwd_noalloc")
     return out, final_state
+
+
+def snapshot_offsets(lengths, snap_every):
+    """int32 [N+1] slot offsets giving each sequence floor(len / snap_every) snapshot slots."""
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + int(n) // int(snap_every))
+    return torch.tensor(cu, dtype=torch.int32)
+
+
+def gdn_recurrent_fwd_snapshots(q, k, v, g, beta, cu_seqlens, snap_every, snap_cu=None, snap_states=None,
+                                init_state=None, out=None, final_state=None, workspace=None,
+                                use_qk_l2norm=True, dv_slice=0, stream=None):
+    """gdn_recurrent_fwd plus fp32 state snapshots after every snap_every-th token of
+    each sequence (prefix caching).  snap_cu: int32 [N+1] device slot offsets (built
+    from cu_seqlens with a host copy when None).  Returns (out, final_state,
+    snap_states [slots, HV, dv, dk], snap_cu)."""
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, dev)
+    _need(g, "g", torch.float32, dev)
+    _need(beta, "beta", torch.float32, dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    N = cu_seqlens.numel() - 1
+    T, HK, dk = q.shape
+    HV, dv = v.shape[1], v.shape[2]
+    if init_state is not None:
+        _need(init_state, "init_state", torch.float32, dev)
+    if snap_cu is None:
+        cuh = cu_seqlens.cpu().tolist()
+        snap_cu = snapshot_offsets([cuh[i + 1] - cuh[i] for i in range(N)], snap_every).to(dev)
+    _need(snap_cu, "snap_cu", torch.int32, dev)
+    slots = int(snap_cu[-1].item()) if snap_states is None else int(snap_states.shape[0])
+    if snap_states is None:
+        snap_states = torch.empty(max(slots, 0), HV, dv, dk, dtype=torch.float32, device=dev)
+    _need(snap_states, "snap_states", torch.float32, dev)
+    shape = make_shape(q, v, N, use_qk_l2norm, dv_slice)
+    if out is None:
+        out = torch.empty_like(v)
+    if final_state is None:
+        final_state = torch.empty(N, HV, dv, dk, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.zeros(max(gdn_workspace_size(shape, OP_FWD), 256), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        rc = lib().gdn_recurrent_fwd_snapshots(
+            ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state),
+            _ptr(cu_seqlens), _ptr(out), _ptr(final_state), int(snap_every), _ptr(snap_cu), slots,
+            _ptr(snap_states) if slots > 0 else None, _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+            _stream(stream))
+    _check(rc, "gdn_recurrent_fwd_snapshots")
+    return out, final_state, snap_states, snap_cu
 
 
 def gdn_decode_step(q, k, v, g, beta, state, state_indices=None, out=None, use_qk_l2norm=True,

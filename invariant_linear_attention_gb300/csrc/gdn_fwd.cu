@@ -17,6 +17,7 @@
 // global memory.  Two units share an SM.
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "gdn_async.cuh"
 #include "gdn_host.h"
@@ -42,6 +43,15 @@ struct FwdParams {
     unsigned* err;
     int N, T, HV, G, dv, dvs, nslices, use_norm;
     int tb;  // tokens per TMA box: min(kTC, T)
+};
+
+// Parameters of the snapshot-taking forward: the plain forward's, plus where
+// to put a copy of the state after every snap_every-th token of a sequence.
+// A separate type keeps the plain kernel's parameters (and code) untouched.
+struct SnapParams : FwdParams {
+    float* snap;
+    const int32_t* snap_cu;
+    int snap_every, snap_slots;
 };
 
 template <typename Tin, int DK>
@@ -110,10 +120,10 @@ __device__ __forceinline__ void issue_chunk(FwdSmem<Tin, DK>& sm, const CUtensor
 }
 
 // ---------------------------------------------------------------------------
-template <typename Tin, int DK>
+template <typename Tin, int DK, typename Prm>
 __global__ void __launch_bounds__(kThreadsPer128Rows, 2)
     gdn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                   const __grid_constant__ CUtensorMap tm_v, const Prm p) {
     constexpr int R = kRowsPerThread;
     extern __shared__ unsigned char smem_raw[];
     FwdSmem<Tin, DK>& sm =
@@ -218,6 +228,15 @@ __global__ void __launch_bounds__(kThreadsPer128Rows, 2)
 #pragma unroll
             for (int r = 0; r < R; ++r) opend[r] = lanes_reduce(opend[r]);
             if (active && e == 0) st_rows_out<R>(out + ((size_t)(t0 + tc - 1) * p.HV + h) * p.dv + row, opend);
+            if constexpr (std::is_same<Prm, SnapParams>::value) {
+                // the state after `done` tokens of this sequence, at every snap_every-th token
+                const int done = t0 + tc - bos;
+                if (done % p.snap_every == 0) {
+                    const int slot = p.snap_cu[n] + done / p.snap_every - 1;
+                    if (active && slot >= 0 && slot < p.snap_cu[n + 1] && slot < p.snap_slots)
+                        store_rows<DK, R>(S, p.snap + (((size_t)slot * p.HV + h) * p.dv + row) * DK, e);
+                }
+            }
             __syncthreads();
             if (tid == 0 && c + kStages < nchunks)
                 issue_chunk(sm, &tm_q, &tm_k, &tm_v, c + kStages, bos, hk, h, slice * dvs, bytes);
@@ -226,11 +245,11 @@ __global__ void __launch_bounds__(kThreadsPer128Rows, 2)
     if (active && p.final_state) store_rows<DK, R>(S, p.final_state + soff, e);
 }
 
-template <typename Tin, int DK>
+template <typename Tin, int DK, typename Prm>
 static gdn_status launch_fwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                               const FwdParams& p, int units, cudaStream_t stream) {
+                               const Prm& p, int units, cudaStream_t stream) {
     const size_t smem = sizeof(FwdSmem<Tin, DK>) + 128;
-    auto kern = gdn_fwd_kernel<Tin, DK>;
+    auto kern = gdn_fwd_kernel<Tin, DK, Prm>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return GDN_ERR_CUDA;
     const int nt = std::max(32, p.dvs * kLanesPerRow / kRowsPerThread);
@@ -238,14 +257,14 @@ static gdn_status launch_fwd_t(const CUtensorMap& mq, const CUtensorMap& mk, con
     return launch_status();
 }
 
-template <typename Tin>
+template <typename Tin, typename Prm>
 static gdn_status launch_fwd_dk(int dk, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                                const FwdParams& p, int units, cudaStream_t stream) {
+                                const Prm& p, int units, cudaStream_t stream) {
     switch (dk) {
-        case 16: return launch_fwd_t<Tin, 16>(mq, mk, mv, p, units, stream);
-        case 32: return launch_fwd_t<Tin, 32>(mq, mk, mv, p, units, stream);
-        case 64: return launch_fwd_t<Tin, 64>(mq, mk, mv, p, units, stream);
-        case 128: return launch_fwd_t<Tin, 128>(mq, mk, mv, p, units, stream);
+        case 16: return launch_fwd_t<Tin, 16, Prm>(mq, mk, mv, p, units, stream);
+        case 32: return launch_fwd_t<Tin, 32, Prm>(mq, mk, mv, p, units, stream);
+        case 64: return launch_fwd_t<Tin, 64, Prm>(mq, mk, mv, p, units, stream);
+        case 128: return launch_fwd_t<Tin, 128, Prm>(mq, mk, mv, p, units, stream);
     }
     return GDN_ERR_UNSUPPORTED;
 }
@@ -259,7 +278,9 @@ size_t fwd_workspace_size(const gdn_shape* s) {
 // work-list and error-word buffers itself.
 gdn_status run_recurrent_fwd(const gdn_shape* s, const void* q, const void* k, const void* v, const float* g,
                              const float* beta, const float* init_state, const int32_t* cu, void* out,
-                             float* final_state, int32_t* work, unsigned* err, cudaStream_t stream) {
+                             float* final_state, int32_t* work, unsigned* err, cudaStream_t stream,
+                             float* snap = nullptr, const int32_t* snap_cu = nullptr, int snap_every = 0,
+                             int snap_slots = 0) {
     const int dvs = pick_dv_slice(s);
     const int nslices = s->dv / dvs;
     const int units = s->N * s->HV * nslices;
@@ -296,6 +317,16 @@ gdn_status run_recurrent_fwd(const gdn_shape* s, const void* q, const void* k, c
     p.nslices = nslices;
     p.use_norm = s->use_qk_l2norm ? 1 : 0;
     p.tb = std::min(kTC, s->T_total);
+    if (snap && snap_cu && snap_slots > 0 && snap_every > 0) {
+        SnapParams sp;
+        static_cast<FwdParams&>(sp) = p;
+        sp.snap = snap;
+        sp.snap_cu = snap_cu;
+        sp.snap_every = snap_every;
+        sp.snap_slots = snap_slots;
+        if (s->dtype == GDN_BF16) return launch_fwd_dk<__nv_bfloat16>(s->dk, mq, mk, mv, sp, units, stream);
+        return launch_fwd_dk<float>(s->dk, mq, mk, mv, sp, units, stream);
+    }
     if (s->dtype == GDN_BF16) return launch_fwd_dk<__nv_bfloat16>(s->dk, mq, mk, mv, p, units, stream);
     return launch_fwd_dk<float>(s->dk, mq, mk, mv, p, units, stream);
 }
@@ -334,6 +365,27 @@ extern "C" gdn_status gdn_recurrent_fwd(const gdn_shape* shape, const void* q, c
     return run_recurrent_fwd(shape, q, k, v, g, beta, init_state, cu_seqlens, out, final_state,
                              reinterpret_cast<int32_t*>(ws + kWsHeader), reinterpret_cast<unsigned*>(ws),
                              static_cast<cudaStream_t>(stream));
+}
+
+extern "C" gdn_status gdn_recurrent_fwd_snapshots(const gdn_shape* shape, const void* q, const void* k,
+                                                  const void* v, const float* g, const float* beta,
+                                                  const float* init_state, const int32_t* cu_seqlens, void* out,
+                                                  float* final_state, int snap_every, const int32_t* snap_cu,
+                                                  int num_snap_slots, float* snap_states, void* workspace,
+                                                  size_t workspace_bytes, void* stream) {
+    using namespace gdn;
+    gdn_status st = check_fwd_args(shape, q, k, v, g, beta, init_state, cu_seqlens, out, final_state);
+    if (st != GDN_OK) return st;
+    if (snap_every <= 0 || snap_every % kTC) return GDN_ERR_UNSUPPORTED;
+    if (num_snap_slots < 0 || (num_snap_slots > 0 && (!snap_states || !snap_cu))) return GDN_ERR_INVALID_ARG;
+    if ((snap_states && !aligned16(snap_states)) || (snap_cu && !aligned4(snap_cu))) return GDN_ERR_INVALID_ARG;
+    if (snap_states && (snap_states == init_state || snap_states == final_state)) return GDN_ERR_INVALID_ARG;
+    if (shape->N == 0) return GDN_OK;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < fwd_workspace_size(shape)) return GDN_ERR_WORKSPACE;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    return run_recurrent_fwd(shape, q, k, v, g, beta, init_state, cu_seqlens, out, final_state,
+                             reinterpret_cast<int32_t*>(ws + kWsHeader), reinterpret_cast<unsigned*>(ws),
+                             static_cast<cudaStream_t>(stream), snap_states, snap_cu, snap_every, num_snap_slots);
 }
 
 // ---------------------------------------------------------------------------

@@ -110,3 +110,19 @@ def test_decode_host_validation(lib):
     # unsupported dv
     assert lib.gdn_decode_step(ctypes.byref(shape(N=4, T_total=4, dv=20)), *ptr[:6], None, 4, ptr[7],
                                None) == -2
+
+
+def test_snapshot_host_validation(lib):
+    P = ctypes.c_void_p
+    s = shape()
+    q, k, v, g, b, s0, cu, out, fs, ws, sc, ss = [P(FAKE + i * 0x1000) for i in range(12)]
+    f = lib.gdn_recurrent_fwd_snapshots
+    # interval not a multiple of the 32-token chunk, or not positive
+    assert f(ctypes.byref(s), q, k, v, g, b, s0, cu, out, fs, 48, sc, 4, ss, ws, 1 << 20, None) == -2
+    assert f(ctypes.byref(s), q, k, v, g, b, s0, cu, out, fs, 0, sc, 4, ss, ws, 1 << 20, None) == -2
+    # slots but no buffer; misaligned buffer; buffer aliasing the final state
+    assert f(ctypes.byref(s), q, k, v, g, b, s0, cu, out, fs, 64, sc, 4, None, ws, 1 << 20, None) == -1
+    assert f(ctypes.byref(s), q, k, v, g, b, s0, cu, out, fs, 64, sc, 4, P(FAKE + 8), ws, 1 << 20, None) == -1
+    assert f(ctypes.byref(s), q, k, v, g, b, s0, cu, out, fs, 64, sc, 4, fs, ws, 1 << 20, None) == -1
+    # workspace rules as for gdn_recurrent_fwd
+    assert f(ctypes.byref(s), q, k, v, g, b, s0, cu, out, fs, 64, sc, 4, ss, None, 1 << 20, None) == -3
