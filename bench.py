@@ -13,6 +13,9 @@ are far larger than L2, so no flush is needed between steps.
 
 The chunked backward is timed separately on its own workload (8 x 4096
 tokens, same heads) and reported under "backward"; it is not part of `value`.
+The layer ops around the recurrence (gate activations, the W=4 causal conv
+with its conv state, the gated RMSNorm) are timed on the prefill workload's
+tokens and reported under "layer_ops", also outside `value`.
 
 --impl reference times the fp64 CPU oracle (the only other implementation
 of this computation here) on the host cores, on a bounded sample of the same
@@ -375,6 +378,13 @@ def main():
     if rank == 0 and not small:
         result["prefill_snapshots"] = bench_snapshots(gdn, d, dev, ws)
 
+    # ---- the layer ops around the recurrence (gates, conv + conv state, gated RMSNorm)
+    if rank == 0 and not small:
+        try:
+            result["layer_ops"] = bench_layer_ops(gdn, d.lengths, dev, hbm_peak)
+        except Exception as exc:  # reported, not hidden
+            result["layer_ops"] = {"error": str(exc)[:300]}
+
     # ---- end to end through the C ABI from pinned host buffers
     if not args.no_e2e and not small:
         result["e2e"] = e2e(gdn, d.cpu(), dd.cpu(), st0.cpu(), dev, steps=min(steps, 5))
@@ -503,6 +513,77 @@ def bench_snapshots(gdn, d, dev, ws, every=256, reps=3):
     T = d.q.shape[0]
     return {"every": every, "snapshots": slots, "snapshot_bytes": slots * HV * DV * DK * 4, "ms": ms,
             "tokens_per_s": T / (ms / 1e3)}
+
+
+def _time_ms(fn, reps):
+    """Device time per call: `reps` calls captured in one CUDA graph and replayed
+    (the per-call host cost of the Python binding would otherwise dominate the
+    microsecond-scale ops).  Every call's outputs are preallocated."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()  # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(reps):
+            fn()
+    graph.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    graph.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def bench_layer_ops(gdn, lengths, dev, hbm_peak, reps=5):
+    """Gate activations, causal conv (W=4 over the q/k/v projections, C = 2*HK*dk + HV*dv)
+    and gated RMSNorm on the prefill workload's tokens, plus the decode-side conv
+    update at the decode batch.  Each is HBM-bound; the algorithmic bytes are every
+    input read once and every output written once."""
+    from invariant_linear_attention_gb300 import inputs
+    L = inputs.make_layer_inputs(lengths, HK=HK, HV=HV, dk=DK, dv=DV, W=4, seed=7, device=dev)
+    T, C = L.x.shape
+    N, W = len(lengths), 4
+    pool = L.conv_state.clone()
+    y = torch.empty_like(L.x)
+    g = torch.empty(T, HV, dtype=torch.float32, device=dev)
+    beta = torch.empty_like(g)
+    yo = torch.empty_like(L.o)
+    res = {}
+
+    def rec(name, ms, nbytes):
+        gbs = nbytes / (ms / 1e3) / 1e9
+        res[name] = {"ms": ms, "bytes": nbytes, "gbs": gbs, "hbm_frac": gbs / hbm_peak}
+
+    rec("gates", _time_ms(lambda: gdn.gdn_gates(L.a, L.b, L.A_log, L.dt_bias, g=g, beta=beta), reps),
+        T * HV * (2 * 2 + 2 * 4))
+    # the conv state is read and rewritten in place every call: each call starts from the previous final state
+    rec("conv_fwd", _time_ms(lambda: gdn.gdn_causal_conv1d_fwd(L.x, L.conv_w, L.cu_seqlens, bias=L.conv_b,
+                                                               conv_state=pool, out=y), reps),
+        T * C * 2 * 2 + 2 * N * (W - 1) * C * 2 + C * (W + 1) * 4)
+    rec("gated_rmsnorm", _time_ms(lambda: gdn.gdn_gated_rmsnorm(L.o, L.z, L.norm_w, out=yo), reps),
+        T * HV * DV * 2 * 3 + DV * 4)
+    D = inputs.make_layer_inputs([1] * DEC_B, HK=HK, HV=HV, dk=DK, dv=DV, W=4, seed=8, device=dev)
+    dpool = D.conv_state.clone()
+    dy = torch.empty_like(D.x)
+    dg = torch.empty(DEC_B, HV, dtype=torch.float32, device=dev)
+    db = torch.empty_like(dg)
+    dyo = torch.empty_like(D.o)
+    rec("decode_conv_update", _time_ms(lambda: gdn.gdn_causal_conv1d_update(D.x, D.conv_w, dpool, bias=D.conv_b,
+                                                                            out=dy), 20),
+        DEC_B * C * 2 * 2 + 2 * DEC_B * (W - 1) * C * 2 + C * (W + 1) * 4)
+    rec("decode_gates", _time_ms(lambda: gdn.gdn_gates(D.a, D.b, D.A_log, D.dt_bias, g=dg, beta=db), 20),
+        DEC_B * HV * (2 * 2 + 2 * 4))
+    rec("decode_gated_rmsnorm", _time_ms(lambda: gdn.gdn_gated_rmsnorm(D.o, D.z, D.norm_w, out=dyo), 20),
+        DEC_B * HV * DV * 2 * 3 + DV * 4)
+    res["workload"] = (f"prefill tokens T={T} in {N} sequences; conv C={C} channels (2*HK*dk + HV*dv), W=4, bf16, "
+                       f"SiLU; RMSNorm over dv={DV} for T*HV rows, bf16; decode ops at batch {DEC_B}; device time "
+                       f"per call from CUDA-graph replay")
+    return res
 
 
 def bench_backward(gdn, dev, steps=3):

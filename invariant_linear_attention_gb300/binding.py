@@ -24,13 +24,19 @@ _P = ctypes.c_void_p
 
 SYMBOLS = ("gdn_workspace_size", "gdn_recurrent_fwd", "gdn_decode_step", "gdn_chunk_bwd",
            "gdn_read_device_error", "gdn_status_string", "gdn_recurrent_fwd_noalloc",
-           "gdn_recurrent_fwd_snapshots")
+           "gdn_recurrent_fwd_snapshots", "gdn_gates", "gdn_gated_rmsnorm", "gdn_causal_conv1d_fwd",
+           "gdn_causal_conv1d_update")
 
 
 class GdnShape(ctypes.Structure):
     _fields_ = [("N", ctypes.c_int), ("T_total", ctypes.c_int), ("HK", ctypes.c_int),
                 ("HV", ctypes.c_int), ("dk", ctypes.c_int), ("dv", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("use_qk_l2norm", ctypes.c_int), ("dv_slice", ctypes.c_int)]
+
+
+class ConvShape(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int), ("T_total", ctypes.c_int), ("C", ctypes.c_int), ("W", ctypes.c_int),
+                ("dtype", ctypes.c_int), ("activation", ctypes.c_int)]
 
 
 class GdnError(RuntimeError):
@@ -62,6 +68,15 @@ def lib():
         L.gdn_chunk_bwd.restype = ctypes.c_int
         L.gdn_read_device_error.argtypes = [_P, ctypes.POINTER(ctypes.c_uint), _P]
         L.gdn_read_device_error.restype = ctypes.c_int
+        L.gdn_gates.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int] + [_P] * 7
+        L.gdn_gates.restype = ctypes.c_int
+        L.gdn_gated_rmsnorm.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int, _P, _P, _P, ctypes.c_float,
+                                        _P, _P]
+        L.gdn_gated_rmsnorm.restype = ctypes.c_int
+        L.gdn_causal_conv1d_fwd.argtypes = [ctypes.POINTER(ConvShape)] + [_P] * 6 + [ctypes.c_int, _P, _P, _P]
+        L.gdn_causal_conv1d_fwd.restype = ctypes.c_int
+        L.gdn_causal_conv1d_update.argtypes = [ctypes.POINTER(ConvShape)] + [_P] * 5 + [ctypes.c_int, _P, _P]
+        L.gdn_causal_conv1d_update.restype = ctypes.c_int
         L.gdn_status_string.argtypes = [ctypes.c_int]
         L.gdn_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -313,3 +328,111 @@ def read_device_error(workspace, stream=None) -> int:
     rc = lib().gdn_read_device_error(_ptr(workspace), ctypes.byref(bits), _stream(stream))
     _check(rc, "gdn_read_device_error")
     return int(bits.value)
+
+
+# ---------------------------------------------------------------- layer ops (include/gdn_layer.h)
+
+def gdn_gates(a, b, A_log, dt_bias=None, g=None, beta=None, stream=None):
+    """(g, beta) [T, HV] fp32 from the raw projections a, b [T, HV] (bf16 or fp32):
+    g = -exp(A_log) * softplus(a + dt_bias), beta = sigmoid(b)."""
+    dev = a.device
+    _need(a, "a", None, dev)
+    _need(b, "b", a.dtype, dev)
+    _need(A_log, "A_log", torch.float32, dev)
+    if dt_bias is not None:
+        _need(dt_bias, "dt_bias", torch.float32, dev)
+    if a.dim() != 2 or b.shape != a.shape or A_log.shape != (a.shape[1],):
+        raise ValueError("a, b must be [T, HV] and A_log [HV]")
+    T, HV = a.shape
+    g = torch.empty(T, HV, dtype=torch.float32, device=dev) if g is None else g
+    beta = torch.empty(T, HV, dtype=torch.float32, device=dev) if beta is None else beta
+    _need(g, "g", torch.float32, dev)
+    _need(beta, "beta", torch.float32, dev)
+    with torch.cuda.device(dev):
+        rc = lib().gdn_gates(int(T), int(HV), _dtype_code(a), _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias),
+                             _ptr(g), _ptr(beta), _stream(stream))
+    _check(rc, "gdn_gates")
+    return g, beta
+
+
+def gdn_gated_rmsnorm(o, z, weight, eps=1e-6, out=None, stream=None):
+    """y = o / sqrt(mean(o^2, -1) + eps) * weight * silu(z) over the last axis of
+    o [..., d] (bf16 or fp32); z like o or None; weight [d] fp32.  out may be o."""
+    dev = o.device
+    _need(o, "o", None, dev)
+    if z is not None:
+        _need(z, "z", o.dtype, dev)
+        if z.shape != o.shape:
+            raise ValueError("z must have o's shape")
+    _need(weight, "weight", torch.float32, dev)
+    d = o.shape[-1]
+    if weight.shape != (d,):
+        raise ValueError("weight must be [d]")
+    out = torch.empty_like(o) if out is None else out
+    _need(out, "out", o.dtype, dev)
+    with torch.cuda.device(dev):
+        rc = lib().gdn_gated_rmsnorm(int(o.numel() // d), int(d), _dtype_code(o), _ptr(o), _ptr(z), _ptr(weight),
+                                     float(eps), _ptr(out), _stream(stream))
+    _check(rc, "gdn_gated_rmsnorm")
+    return out
+
+
+def _conv_shape(x, weight, N, activation):
+    T, C = x.shape
+    if weight.dim() != 2 or weight.shape[0] != C:
+        raise ValueError("weight must be [C, W]")
+    return ConvShape(int(N), int(T), int(C), int(weight.shape[1]), _dtype_code(x), int(bool(activation)))
+
+
+def gdn_causal_conv1d_fwd(x, weight, cu_seqlens, bias=None, conv_state=None, state_indices=None,
+                          has_initial_state=None, activation=True, out=None, stream=None):
+    """Causal depthwise conv over packed varlen x [T, C] with taps weight [C, W]
+    fp32.  conv_state [slots, W-1, C] (dtype of x) is read as the initial state
+    and overwritten with the final state of each sequence's slot (in place).
+    Returns y [T, C]."""
+    dev = x.device
+    _need(x, "x", None, dev)
+    _need(weight, "weight", torch.float32, dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    for t, n, dt in ((bias, "bias", torch.float32), (conv_state, "conv_state", x.dtype),
+                     (state_indices, "state_indices", torch.int32),
+                     (has_initial_state, "has_initial_state", torch.int32)):
+        if t is not None:
+            _need(t, n, dt, dev)
+    N = cu_seqlens.numel() - 1
+    shape = _conv_shape(x, weight, N, activation)
+    if conv_state is not None and tuple(conv_state.shape[1:]) != (shape.W - 1, shape.C):
+        raise ValueError("conv_state must be [slots, W-1, C]")
+    out = torch.empty_like(x) if out is None else out
+    _need(out, "out", x.dtype, dev)
+    slots = 0 if conv_state is None else int(conv_state.shape[0])
+    with torch.cuda.device(dev):
+        rc = lib().gdn_causal_conv1d_fwd(ctypes.byref(shape), _ptr(x), _ptr(weight), _ptr(bias), _ptr(cu_seqlens),
+                                         _ptr(conv_state), _ptr(state_indices), slots, _ptr(has_initial_state),
+                                         _ptr(out), _stream(stream))
+    _check(rc, "gdn_causal_conv1d_fwd")
+    return out
+
+
+def gdn_causal_conv1d_update(x, weight, conv_state, state_indices=None, bias=None, activation=True, out=None,
+                             stream=None):
+    """One decode token per sequence: x [B, C]; conv_state [slots, W-1, C]
+    updated in place.  Returns y [B, C] (rows of skipped sequences untouched)."""
+    dev = x.device
+    _need(x, "x", None, dev)
+    _need(weight, "weight", torch.float32, dev)
+    _need(conv_state, "conv_state", x.dtype, dev)
+    for t, n, dt in ((bias, "bias", torch.float32), (state_indices, "state_indices", torch.int32)):
+        if t is not None:
+            _need(t, n, dt, dev)
+    shape = _conv_shape(x, weight, x.shape[0], activation)
+    if tuple(conv_state.shape[1:]) != (shape.W - 1, shape.C):
+        raise ValueError("conv_state must be [slots, W-1, C]")
+    out = torch.empty_like(x) if out is None else out
+    _need(out, "out", x.dtype, dev)
+    with torch.cuda.device(dev):
+        rc = lib().gdn_causal_conv1d_update(ctypes.byref(shape), _ptr(x), _ptr(weight), _ptr(bias),
+                                            _ptr(conv_state), _ptr(state_indices), int(conv_state.shape[0]),
+                                            _ptr(out), _stream(stream))
+    _check(rc, "gdn_causal_conv1d_update")
+    return out

@@ -39,7 +39,7 @@ def _sources():
 
 def _deps():
     return _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h"))) + \
-        [os.path.join(ROOT, "include", "gdn.h")]
+        sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 
 def _up_to_date():

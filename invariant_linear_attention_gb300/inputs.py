@@ -19,6 +19,14 @@ for the activations a GDN layer receives there):
 
 Layouts: q, k [T, HK, dk]; v [T, HV, dv]; g, beta [T, HV] fp32;
 state [N, HV, dv, dk] fp32; cu_seqlens int32 [N + 1].
+
+The layer ops around the recurrence (make_layer_inputs) get: gate
+projections a, b ~ randn [T, HV]; A_log = log(uniform(1, 16)) and
+dt_bias ~ randn * 0.5 - 2 per head (fp32); conv input x ~ randn [T, C] with
+C = 2 * HK * dk + HV * dv (the q, k and v projections side by side), taps
+~ randn / sqrt(W) and bias ~ randn * 0.1 (fp32), conv state ~ randn
+[N, W-1, C]; norm input o ~ randn and gate z ~ randn [T, HV, dv]; norm
+weight ~ 1 + 0.1 * randn [dv] (fp32).
 """
 from dataclasses import dataclass
 from typing import List, Optional, Sequence
@@ -145,3 +153,46 @@ def random_states(N: int, HV: int, dv: int, dk: int, seed: int, scale: float = 1
                   device="cpu") -> torch.Tensor:
     """fp32 states ~ randn * scale, layout [N, HV, dv, dk]."""
     return (_randn((N, HV, dv, dk), _gen(seed, device), device) * scale).contiguous()
+
+
+@dataclass
+class LayerInputs:
+    a: torch.Tensor            # [T, HV] gate projections (dtype)
+    b: torch.Tensor            # [T, HV]
+    A_log: torch.Tensor        # [HV] fp32
+    dt_bias: torch.Tensor      # [HV] fp32
+    x: torch.Tensor            # [T, C] conv input (dtype)
+    conv_w: torch.Tensor       # [C, W] fp32
+    conv_b: torch.Tensor       # [C] fp32
+    conv_state: torch.Tensor   # [N, W-1, C] (dtype)
+    o: torch.Tensor            # [T, HV, dv] norm input (dtype)
+    z: torch.Tensor            # [T, HV, dv] norm gate (dtype)
+    norm_w: torch.Tensor       # [dv] fp32
+    cu_seqlens: torch.Tensor
+    lengths: List[int]
+
+    def to(self, device):
+        kw = {f: (getattr(self, f).to(device) if isinstance(getattr(self, f), torch.Tensor) else getattr(self, f))
+              for f in self.__dataclass_fields__}
+        return LayerInputs(**kw)
+
+
+def make_layer_inputs(lengths: Sequence[int], HK: int, HV: int, dk: int, dv: int, W: int = 4,
+                      dtype=torch.bfloat16, seed: int = 0, device="cpu", C: Optional[int] = None) -> LayerInputs:
+    """Seeded inputs for the gate, conv and norm ops (see module doc)."""
+    gen = _gen(seed, device)
+    T, N = int(sum(lengths)), len(lengths)
+    C = 2 * HK * dk + HV * dv if C is None else int(C)
+    a = _randn((T, HV), gen, device).to(dtype).contiguous()
+    b = _randn((T, HV), gen, device).to(dtype).contiguous()
+    A_log = torch.log(torch.empty(HV, device=device).uniform_(1.0, 16.0, generator=gen))
+    dt_bias = _randn((HV,), gen, device) * 0.5 - 2.0
+    x = _randn((T, C), gen, device).to(dtype).contiguous()
+    conv_w = (_randn((C, W), gen, device) / math.sqrt(W)).contiguous()
+    conv_b = _randn((C,), gen, device) * 0.1
+    conv_state = _randn((N, W - 1, C), gen, device).to(dtype).contiguous()
+    o = _randn((T, HV, dv), gen, device).to(dtype).contiguous()
+    z = _randn((T, HV, dv), gen, device).to(dtype).contiguous()
+    norm_w = 1.0 + 0.1 * _randn((dv,), gen, device)
+    return LayerInputs(a, b, A_log, dt_bias, x, conv_w, conv_b, conv_state, o, z, norm_w,
+                       cu_from_lengths(lengths).to(device), list(lengths))

@@ -14,9 +14,10 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def declared_functions():
-    text = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    text = "".join(open(os.path.join(ROOT, "include", f)).read()
+                   for f in sorted(os.listdir(os.path.join(ROOT, "include"))) if f.endswith(".h"))
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(gdn_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(gdn_[a-z0-9_]+)\s*\(", text)))
 
 
 @pytest.fixture(scope="module")
@@ -30,7 +31,7 @@ def test_exports_every_declared_symbol(lib):
     names = declared_functions()
     assert {"gdn_recurrent_fwd", "gdn_decode_step", "gdn_chunk_bwd", "gdn_workspace_size"} <= set(names)
     for name in names:
-        assert hasattr(lib, name), f"{name} declared in gdn.h but not exported"
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
     assert set(binding.SYMBOLS) == set(names)
 
 
@@ -126,3 +127,38 @@ def test_snapshot_host_validation(lib):
     assert f(ctypes.byref(s), q, k, v, g, b, s0, cu, out, fs, 64, sc, 4, fs, ws, 1 << 20, None) == -1
     # workspace rules as for gdn_recurrent_fwd
     assert f(ctypes.byref(s), q, k, v, g, b, s0, cu, out, fs, 64, sc, 4, ss, None, 1 << 20, None) == -3
+
+
+def conv_shape(**kw):
+    base = dict(N=2, T_total=10, C=64, W=4, dtype=binding.GDN_BF16, activation=1)
+    base.update(kw)
+    return binding.ConvShape(**base)
+
+
+def test_layer_ops_host_validation(lib):
+    P = ctypes.c_void_p
+    a, b, al, dt, g, be = [P(FAKE + i * 0x1000) for i in range(6)]
+    # gates: bad dtype, null output, misaligned A_log; empty input launches nothing
+    assert lib.gdn_gates(8, 4, 7, a, b, al, dt, g, be, None) == -2
+    assert lib.gdn_gates(8, 4, binding.GDN_BF16, a, b, al, dt, None, be, None) == -1
+    assert lib.gdn_gates(8, 4, binding.GDN_BF16, a, b, P(FAKE + 2), dt, g, be, None) == -1
+    assert lib.gdn_gates(0, 4, binding.GDN_BF16, a, b, al, dt, g, be, None) == 0
+    o, z, w, y = [P(FAKE + i * 0x1000) for i in range(4)]
+    # rmsnorm: d not a multiple of the 16-byte vector, d too large, misaligned o, negative eps
+    assert lib.gdn_gated_rmsnorm(4, 12, binding.GDN_BF16, o, z, w, 1e-6, y, None) == -2
+    assert lib.gdn_gated_rmsnorm(4, 4096, binding.GDN_BF16, o, z, w, 1e-6, y, None) == -2
+    assert lib.gdn_gated_rmsnorm(4, 128, binding.GDN_BF16, P(FAKE + 8), z, w, 1e-6, y, None) == -1
+    assert lib.gdn_gated_rmsnorm(4, 128, binding.GDN_BF16, o, z, w, -1.0, y, None) == -1
+    x, cw, cb, cu, st, idx, hi, cy = [P(FAKE + i * 0x1000) for i in range(8)]
+    fwd = lib.gdn_causal_conv1d_fwd
+    assert fwd(ctypes.byref(conv_shape(W=9)), x, cw, cb, cu, st, idx, 4, hi, cy, None) == -2
+    assert fwd(ctypes.byref(conv_shape(C=60)), x, cw, cb, cu, st, idx, 4, hi, cy, None) == -2
+    assert fwd(ctypes.byref(conv_shape()), x, cw, cb, cu, st, idx, 4, hi, x, None) == -1       # y aliases x
+    assert fwd(ctypes.byref(conv_shape()), x, cw, cb, None, st, idx, 4, hi, cy, None) == -1    # no cu_seqlens
+    assert fwd(ctypes.byref(conv_shape()), x, cw, cb, cu, st, None, 1, hi, cy, None) == -1     # slots < N
+    assert fwd(ctypes.byref(conv_shape()), P(FAKE + 4), cw, cb, cu, st, idx, 4, hi, cy, None) == -1
+    upd = lib.gdn_causal_conv1d_update
+    assert upd(ctypes.byref(conv_shape(N=4, T_total=5)), x, cw, cb, st, idx, 4, cy, None) == -1
+    assert upd(ctypes.byref(conv_shape(N=4, T_total=4)), x, cw, cb, None, idx, 4, cy, None) == -1
+    assert upd(ctypes.byref(conv_shape(N=4, T_total=4)), x, cw, cb, st, None, 3, cy, None) == -1
+    assert upd(ctypes.byref(conv_shape(N=4, T_total=4, dtype=3)), x, cw, cb, st, idx, 4, cy, None) == -2
