@@ -16,5 +16,10 @@ Parity status of each function (what pins it is in ``tests/test_oracle_pins.py``
                           equal in exact arithmetic to it for chunk size 1).
 * ``gdn_bwd``          -- pinned by central finite differences of ``gdn_fwd``
                           on every input, plus the beta=0 and one-token cases.
+* ``gdn_replay_state`` -- pinned: the state rebuilt from the cache equals
+                          ``gdn_fwd``'s final state; its d rows equal the
+                          chunked WY form's U rows.
+* ``layer_ops``        -- gates, causal conv, gated RMSNorm: pinned in
+                          ``tests/test_oracle_layer_pins.py``.
 """
-from .oracle import gdn_fwd, gdn_bwd, gdn_fwd_chunked, max_threads  # noqa: F401
+from .oracle import gdn_fwd, gdn_bwd, gdn_fwd_chunked, gdn_replay_state, max_threads  # noqa: F401

@@ -172,3 +172,52 @@ def gdn_fwd_chunked(q, k, v, g, beta, cu_seqlens, init_state=None, chunk=64,
                 S = Gam[-1] * S + U.T @ (np.exp(gam[-1] - gam)[:, None] * K)
             fs[n, h] = S
     return o, fs
+
+
+def gdn_replay_state(q, k, v, g, beta, cu_seqlens, init_state=None, chunk=64, use_qk_l2norm=True, eps=EPS):
+    """The chunk-replay cache of every sequence after all its tokens (fp64).
+
+    The delta-rule step written as S_t = a_t S_{t-1} + d_t k^_t^T with
+    d_t = b_t (v_t - a_t S_{t-1} k^_t) (expand a_t S_{t-1} (I - b_t k^ k^T) +
+    b_t v_t k^T).  With chunks of `chunk` tokens from each sequence start, a
+    sequence that has seen P tokens is described by the state at the start of
+    its current chunk, S0 = S_{C*floor(P/C)}, plus, for the r = P mod C tokens
+    of that chunk, k^_i, d_i and gam_i = g_{start} + ... + g_i (the chunk's
+    cumulative log-decay).  This is the state a decode that replays the
+    chunked computation order needs ("Finish RL Training Faster:
+    Bitwise-Consistent, High-Performance, Agent-Driven", the Nemotron
+    experiment: decode replays prefill's chunked order).
+
+    Returns per sequence n: dict(S0 [HV,dv,dk], K [r,HV,dk], D [r,HV,dv],
+    gam [r,HV], r) and the per-token d [T,HV,dv].
+    """
+    q, k, v, g, beta, s0 = map(_f64, (q, k, v, g, beta, init_state))
+    cu = np.asarray(cu_seqlens.cpu() if hasattr(cu_seqlens, "cpu") else cu_seqlens, dtype=np.int64)
+    T, N, HK, HV, dk, dv = _shapes(q, v, cu)
+    G = HV // HK
+    kn = _l2n(k, use_qk_l2norm, eps)
+    d_all = np.zeros((T, HV, dv))
+    res = []
+    for n in range(N):
+        a, e = int(cu[n]), int(cu[n + 1])
+        P = e - a
+        c0 = a + (P // chunk) * chunk  # first token of the current (partial) chunk
+        S0 = np.zeros((HV, dv, dk))
+        for h in range(HV):
+            S = np.zeros((dv, dk)) if s0 is None else s0[n, h].copy()
+            for t in range(a, e):
+                if t == c0:
+                    S0[h] = S
+                kt = kn[t, h // G]
+                at = np.exp(g[t, h])
+                d = beta[t, h] * (v[t, h] - at * (S @ kt))
+                d_all[t, h] = d
+                S = at * S + np.outer(d, kt)
+            if c0 == e:
+                S0[h] = S
+        r = e - c0
+        gam = np.zeros((r, HV))
+        for h in range(HV):
+            gam[:, h] = np.cumsum(g[c0:e, h])
+        res.append(dict(S0=S0, K=kn[c0:e][:, np.arange(HV) // G], D=d_all[c0:e].copy(), gam=gam, r=r))
+    return res, d_all

@@ -243,3 +243,44 @@ def test_backward_special_cases():
     gr1 = oracle.gdn_bwd(q[:1], k[:1], v[:1], g[:1], beta[:1], [0, 1], dO[:1],
                          init_state=np.zeros((1, 1, 3, 4)))
     assert np.all(gr1["dg"] == 0.0)
+
+
+def test_replay_state_pins():
+    """The chunk-replay cache: rebuilding the state from it (S_P = exp(gam_r) S0 +
+    sum_i exp(gam_r - gam_i) d_i k_i^T) gives the C recurrence's final state, and
+    its d rows are the chunked WY form's U rows (an independent algorithm)."""
+    rng = np.random.default_rng(11)
+    lengths = [70, 64, 5, 0, 130]
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    T, HK, HV, dk, dv = int(cu[-1]), 1, 2, 8, 6
+    q, k = rng.standard_normal((T, HK, dk)), rng.standard_normal((T, HK, dk))
+    v = rng.standard_normal((T, HV, dv))
+    g = -np.log1p(np.exp(rng.standard_normal((T, HV))))
+    beta = 1 / (1 + np.exp(-rng.standard_normal((T, HV))))
+    s0 = rng.standard_normal((len(lengths), HV, dv, dk)) * 0.3
+    states, d_all = oracle.gdn_replay_state(q, k, v, g, beta, cu, init_state=s0, chunk=64)
+    _, fs = oracle.gdn_fwd(q, k, v, g, beta, cu, init_state=s0)
+    for n, st in enumerate(states):
+        assert st["r"] == lengths[n] % 64
+        for h in range(HV):
+            S = st["S0"][h].copy()
+            if st["r"]:
+                gam = st["gam"][:, h]
+                S = np.exp(gam[-1]) * S + sum(np.exp(gam[-1] - gam[i]) * np.outer(st["D"][i, h], st["K"][i, h])
+                                              for i in range(st["r"]))
+            np.testing.assert_allclose(S, fs[n, h], rtol=1e-12, atol=1e-12)
+    # d rows against the chunked form's U = T diag(b) V - W S0^T, computed independently
+    kn = k / np.sqrt((k * k).sum(-1, keepdims=True) + 1e-6)
+    n, h = 4, 1
+    a = int(cu[n])
+    S = s0[n, h].copy()
+    for c0 in range(a, int(cu[n + 1]), 64):
+        c1 = min(c0 + 64, int(cu[n + 1]))
+        K, V, b = kn[c0:c1, 0], v[c0:c1, h], beta[c0:c1, h]
+        gam = np.cumsum(g[c0:c1, h])
+        E = np.exp(gam[:, None] - gam[None, :])
+        A = np.tril(b[:, None] * E * (K @ K.T), -1)
+        Tm = np.linalg.inv(np.eye(c1 - c0) + A)
+        U = Tm @ (b[:, None] * V) - (Tm @ ((b * np.exp(gam))[:, None] * K)) @ S.T
+        np.testing.assert_allclose(d_all[c0:c1, h], U, rtol=1e-11, atol=1e-12)
+        S = np.exp(gam[-1]) * S + U.T @ (np.exp(gam[-1] - gam)[:, None] * K)
