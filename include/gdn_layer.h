@@ -26,8 +26,8 @@
  * prefill over the whole sequence).
  *
  * Memory and ownership as in gdn.h: caller-owned, dense row-major DEVICE
- * pointers; x, y, o, z, the conv state and the RMSNorm weight 16-byte
- * aligned; g, beta, A_log, dt_bias, the conv weight and bias, cu_seqlens,
+ * pointers; x, y, o, z, the conv state, the conv weight and the RMSNorm
+ * weight 16-byte aligned; g, beta, A_log, dt_bias, the conv bias, cu_seqlens,
  * state_indices and has_initial_state 4-byte aligned (a and b: their element
  * size).  Misalignment returns GDN_ERR_INVALID_ARG.  Nothing is allocated;
  * every call is one asynchronous launch on `stream` (a cudaStream_t; NULL =

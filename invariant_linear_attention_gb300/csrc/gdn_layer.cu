@@ -208,13 +208,40 @@ struct ConvTaps {
     float b[VN];
 };
 
+// The CTA's taps (blockDim.x * VN channels x W, contiguous in the [C, W]
+// weight) are staged through shared memory: coalesced 16-byte loads in, then
+// each thread reads its own PT = VN*W/4 float4s at an odd float4 stride, which
+// is free of bank conflicts.  (Read straight from global memory, each warp
+// instruction would touch 32 different cache lines.)  Must be called by every
+// thread of the CTA; the weight pointer is 16-byte aligned.
 template <int W, int VN>
-__device__ __forceinline__ void load_taps(ConvTaps<W, VN>& t, const float* __restrict__ w,
-                                          const float* __restrict__ bias, int c0) {
+struct TapStage {
+    static constexpr int PT = VN * W / 4;                  // float4s per thread
+    static constexpr int ST = (PT & 1) ? PT : PT + 1;      // odd stride in float4s
+    static constexpr int kFloat4s = 128 * ST;              // for a 128-thread CTA
+};
+
+template <int W, int VN>
+__device__ __forceinline__ void load_taps(ConvTaps<W, VN>& t, float4* stage, const float* __restrict__ w,
+                                          const float* __restrict__ bias, int cblk0, int C) {
+    constexpr int PT = TapStage<W, VN>::PT, ST = TapStage<W, VN>::ST;
+    const int nch = min(C - cblk0, (int)blockDim.x * VN);
+    const int nf4 = nch * W / 4;
+    const float4* src = reinterpret_cast<const float4*>(w + (int64_t)cblk0 * W);
+    for (int f = threadIdx.x; f < nf4; f += blockDim.x) stage[(f / PT) * ST + f % PT] = __ldg(src + f);
+    __syncthreads();
+    const int c0 = cblk0 + threadIdx.x * VN;
+    if (c0 >= C) return;
+    float flat[VN * W];  // channel-major: flat[e * W + i] = w[c0 + e][i]
+#pragma unroll
+    for (int j = 0; j < PT; ++j) {
+        const float4 v = stage[threadIdx.x * ST + j];
+        flat[4 * j] = v.x, flat[4 * j + 1] = v.y, flat[4 * j + 2] = v.z, flat[4 * j + 3] = v.w;
+    }
 #pragma unroll
     for (int e = 0; e < VN; ++e) {
 #pragma unroll
-        for (int i = 0; i < W; ++i) t.w[i][e] = __ldg(w + (int64_t)(c0 + e) * W + i);
+        for (int i = 0; i < W; ++i) t.w[i][e] = flat[e * W + i];
         t.b[e] = bias ? __ldg(bias + c0 + e) : 0.f;
     }
 }
@@ -257,8 +284,9 @@ __global__ void __launch_bounds__(128) conv_fwd_kernel(const ConvParams p) {
     constexpr int VN = V16<T>::n;
     constexpr int WM = W - 1;
     constexpr int U = 4;  // rows per register buffer (two buffers)
-    const int c0 = (blockIdx.y * blockDim.x + threadIdx.x) * VN;
-    if (c0 >= p.C) return;
+    __shared__ float4 stage[TapStage<W, VN>::kFloat4s];
+    const int cblk0 = blockIdx.y * blockDim.x * VN;
+    const int c0 = cblk0 + threadIdx.x * VN;
     const int j = blockIdx.x;
     // largest n in [0, N) with f(n) <= j
     int lo = 0, hi = p.N - 1;
@@ -277,11 +305,12 @@ __global__ void __launch_bounds__(128) conv_fwd_kernel(const ConvParams p) {
     T* y = static_cast<T*>(p.y);
     const int slot = !p.state ? -1 : (p.idx ? __ldg(p.idx + n) : n);
     const bool has_slot = slot >= 0 && slot < p.num_slots;
-    T* st = has_slot ? static_cast<T*>(p.state) + (int64_t)slot * WM * p.C + c0 : nullptr;
+    T* st = has_slot && c0 < p.C ? static_cast<T*>(p.state) + (int64_t)slot * WM * p.C + c0 : nullptr;
     const bool use_init = has_slot && (!p.has_init || __ldg(p.has_init + n) != 0);
 
     ConvTaps<W, VN> taps;
-    load_taps<W, VN>(taps, p.w, p.bias, c0);
+    load_taps<W, VN>(taps, stage, p.w, p.bias, cblk0, p.C);  // CTA-uniform up to here
+    if (c0 >= p.C) return;
     float win[WM][VN];
 #pragma unroll
     for (int i = 0; i < WM; ++i) {
@@ -344,16 +373,18 @@ template <typename T, int W>
 __global__ void __launch_bounds__(128) conv_update_kernel(const ConvParams p) {
     constexpr int VN = V16<T>::n;
     constexpr int WM = W - 1;
-    const int c0 = (blockIdx.y * blockDim.x + threadIdx.x) * VN;
+    __shared__ float4 stage[TapStage<W, VN>::kFloat4s];
+    const int cblk0 = blockIdx.y * blockDim.x * VN;
+    const int c0 = cblk0 + threadIdx.x * VN;
     const int b = blockIdx.x;
-    if (c0 >= p.C) return;
     const int slot = p.idx ? __ldg(p.idx + b) : b;
-    if (slot < 0 || slot >= p.num_slots) return;
+    if (slot < 0 || slot >= p.num_slots) return;  // CTA-uniform
+    ConvTaps<W, VN> taps;
+    load_taps<W, VN>(taps, stage, p.w, p.bias, cblk0, p.C);
+    if (c0 >= p.C) return;
     const T* x = static_cast<const T*>(p.x);
     T* y = static_cast<T*>(p.y);
     T* st = static_cast<T*>(p.state) + (int64_t)slot * WM * p.C + c0;
-    ConvTaps<W, VN> taps;
-    load_taps<W, VN>(taps, p.w, p.bias, c0);
     float win[WM][VN], xc[VN], out[VN];
 #pragma unroll
     for (int i = 0; i < WM; ++i) unpack(ld16(st + (int64_t)i * p.C), win[i]);
@@ -487,7 +518,7 @@ extern "C" gdn_status gdn_causal_conv1d_fwd(const gdn_conv_shape* shape, const v
     if (!weight || !cu_seqlens || (shape->T_total > 0 && (!x || !y))) return GDN_ERR_INVALID_ARG;
     if (x && x == y) return GDN_ERR_INVALID_ARG;
     if ((x && !aligned16(x)) || (y && !aligned16(y)) || (conv_state && !aligned16(conv_state)) ||
-        !aligned4(weight) || (bias && !aligned4(bias)) || !aligned4(cu_seqlens) ||
+        !aligned16(weight) || (bias && !aligned4(bias)) || !aligned4(cu_seqlens) ||
         (state_indices && !aligned4(state_indices)) || (has_initial_state && !aligned4(has_initial_state)))
         return GDN_ERR_INVALID_ARG;
     if (conv_state && num_slots < 0) return GDN_ERR_INVALID_ARG;
@@ -514,7 +545,7 @@ extern "C" gdn_status gdn_causal_conv1d_update(const gdn_conv_shape* shape, cons
     if (!x || !y || !weight || !conv_state || num_slots < 0) return GDN_ERR_INVALID_ARG;
     if (!state_indices && num_slots < shape->N) return GDN_ERR_INVALID_ARG;
     if (x == y) return GDN_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(y) || !aligned16(conv_state) || !aligned4(weight) || (bias && !aligned4(bias)) ||
+    if (!aligned16(x) || !aligned16(y) || !aligned16(conv_state) || !aligned16(weight) || (bias && !aligned4(bias)) ||
         (state_indices && !aligned4(state_indices)))
         return GDN_ERR_INVALID_ARG;
     const int vn = shape->dtype == GDN_BF16 ? 8 : 4;
