@@ -5,7 +5,8 @@ bit-identical results per sequence (whatever shares the batch, however the
 tokens arrive); a chunked WY-form backward supplies gradients.  The compute
 lives in libgdn.so (C ABI: include/gdn.h for the recurrence,
 include/gdn_layer.h for the gate activations, the short causal conv with its
-state cache, and the gated RMSNorm around it); this package is its ctypes
+state cache, and the gated RMSNorm around it, include/gdn_replay.h for the
+chunk-order-replaying variant); this package is its ctypes
 binding plus the seeded synthetic-input generators.
 """
 from .binding import (  # noqa: F401
@@ -21,10 +22,15 @@ from .binding import (  # noqa: F401
     gdn_recurrent_fwd,
     gdn_recurrent_fwd_noalloc,
     gdn_recurrent_fwd_snapshots,
+    gdn_replay_decode,
+    gdn_replay_prefill,
     gdn_workspace_size,
     lib,
     make_shape,
     read_device_error,
+    replay_block_floats,
+    replay_state_new,
+    replay_views,
     snapshot_offsets,
     status_string,
 )

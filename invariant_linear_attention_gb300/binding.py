@@ -25,7 +25,8 @@ _P = ctypes.c_void_p
 SYMBOLS = ("gdn_workspace_size", "gdn_recurrent_fwd", "gdn_decode_step", "gdn_chunk_bwd",
            "gdn_read_device_error", "gdn_status_string", "gdn_recurrent_fwd_noalloc",
            "gdn_recurrent_fwd_snapshots", "gdn_gates", "gdn_gated_rmsnorm", "gdn_causal_conv1d_fwd",
-           "gdn_causal_conv1d_update")
+           "gdn_causal_conv1d_update", "gdn_replay_block_floats", "gdn_replay_workspace_size",
+           "gdn_replay_prefill", "gdn_replay_decode")
 
 
 class GdnShape(ctypes.Structure):
@@ -77,6 +78,15 @@ def lib():
         L.gdn_causal_conv1d_fwd.restype = ctypes.c_int
         L.gdn_causal_conv1d_update.argtypes = [ctypes.POINTER(ConvShape)] + [_P] * 5 + [ctypes.c_int, _P, _P]
         L.gdn_causal_conv1d_update.restype = ctypes.c_int
+        L.gdn_replay_block_floats.argtypes = [ctypes.c_int, ctypes.c_int]
+        L.gdn_replay_block_floats.restype = ctypes.c_size_t
+        L.gdn_replay_workspace_size.argtypes = [ctypes.POINTER(GdnShape)]
+        L.gdn_replay_workspace_size.restype = ctypes.c_size_t
+        L.gdn_replay_prefill.argtypes = [ctypes.POINTER(GdnShape)] + [_P] * 9 + [ctypes.c_int, _P, _P,
+                                                                                ctypes.c_size_t, _P]
+        L.gdn_replay_prefill.restype = ctypes.c_int
+        L.gdn_replay_decode.argtypes = [ctypes.POINTER(GdnShape)] + [_P] * 8 + [ctypes.c_int, _P, _P]
+        L.gdn_replay_decode.restype = ctypes.c_int
         L.gdn_status_string.argtypes = [ctypes.c_int]
         L.gdn_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -435,4 +445,89 @@ def gdn_causal_conv1d_update(x, weight, conv_state, state_indices=None, bias=Non
                                             _ptr(conv_state), _ptr(state_indices), int(conv_state.shape[0]),
                                             _ptr(out), _stream(stream))
     _check(rc, "gdn_causal_conv1d_update")
+    return out
+
+
+# ---------------------------------------------------------------- chunk-replay variant (include/gdn_replay.h)
+
+REPLAY_CHUNK = 64
+
+
+def replay_block_floats(dk, dv):
+    """Floats per (slot, head) in a replay-state pool."""
+    return int(lib().gdn_replay_block_floats(int(dk), int(dv)))
+
+
+def replay_state_new(slots, HV, dk, dv, init_state=None, device="cuda"):
+    """A zeroed replay-state pool [slots, HV, B] fp32 whose chunk-start states are
+    init_state [slots, HV, dv, dk] (zeros when None)."""
+    rs = torch.zeros(slots, HV, replay_block_floats(dk, dv), dtype=torch.float32, device=device)
+    if init_state is not None:
+        replay_views(rs, dk, dv)["S0"].copy_(init_state)
+    return rs
+
+
+def replay_views(rs, dk, dv):
+    """Views of a replay-state pool: S0 [slots, HV, dv, dk], K [.., C, dk], D [.., C, dv], gam [.., C]."""
+    C = REPLAY_CHUNK
+    a, b, c = dv * dk, dv * dk + C * dk, dv * dk + C * (dk + dv)
+    sl, HV = rs.shape[0], rs.shape[1]
+    return dict(S0=rs[..., :a].unflatten(-1, (dv, dk)), K=rs[..., a:b].unflatten(-1, (C, dk)),
+                D=rs[..., b:c].unflatten(-1, (C, dv)), gam=rs[..., c:c + C])
+
+
+def gdn_replay_prefill(q, k, v, g, beta, cu_seqlens, replay_state, seq_pos=None, state_indices=None, out=None,
+                       workspace=None, use_qk_l2norm=True, stream=None):
+    """Chunked prefill that continues every sequence from its replay state (at
+    position seq_pos[n], int32 on the device; None: 0) and leaves the state
+    after its last token.  Returns out [T, HV, dv]."""
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, dev)
+    _need(g, "g", torch.float32, dev)
+    _need(beta, "beta", torch.float32, dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    _need(replay_state, "replay_state", torch.float32, dev)
+    for t, n in ((seq_pos, "seq_pos"), (state_indices, "state_indices")):
+        if t is not None:
+            _need(t, n, torch.int32, dev)
+    N = cu_seqlens.numel() - 1
+    shape = make_shape(q, v, N, use_qk_l2norm, 0)
+    if replay_state.shape[1:] != (shape.HV, replay_block_floats(shape.dk, shape.dv)):
+        raise ValueError("replay_state must be [slots, HV, replay_block_floats(dk, dv)]")
+    out = torch.empty_like(v) if out is None else out
+    _need(out, "out", q.dtype, dev)
+    if workspace is None:
+        workspace = torch.zeros(max(int(lib().gdn_replay_workspace_size(ctypes.byref(shape))), 256),
+                                dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        rc = lib().gdn_replay_prefill(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                      _ptr(cu_seqlens), _ptr(seq_pos), _ptr(replay_state), _ptr(state_indices),
+                                      int(replay_state.shape[0]), _ptr(out), _ptr(workspace),
+                                      ctypes.c_size_t(workspace.numel()), _stream(stream))
+    _check(rc, "gdn_replay_prefill")
+    return out
+
+
+def gdn_replay_decode(q, k, v, g, beta, replay_state, seq_pos, state_indices=None, out=None, use_qk_l2norm=True,
+                      stream=None):
+    """One token per sequence replaying the chunked order; seq_pos [B] int32 (tokens
+    already processed).  Returns out [B, HV, dv] (rows of skipped slots untouched)."""
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, dev)
+    _need(g, "g", torch.float32, dev)
+    _need(beta, "beta", torch.float32, dev)
+    _need(replay_state, "replay_state", torch.float32, dev)
+    _need(seq_pos, "seq_pos", torch.int32, dev)
+    if state_indices is not None:
+        _need(state_indices, "state_indices", torch.int32, dev)
+    shape = make_shape(q, v, q.shape[0], use_qk_l2norm, 0)
+    out = torch.empty_like(v) if out is None else out
+    _need(out, "out", q.dtype, dev)
+    with torch.cuda.device(dev):
+        rc = lib().gdn_replay_decode(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                     _ptr(seq_pos), _ptr(replay_state), _ptr(state_indices),
+                                     int(replay_state.shape[0]), _ptr(out), _stream(stream))
+    _check(rc, "gdn_replay_decode")
     return out

@@ -269,6 +269,15 @@ static gdn_status launch_fwd_dk(int dk, const CUtensorMap& mq, const CUtensorMap
     return GDN_ERR_UNSUPPORTED;
 }
 
+// Host launcher of the varlen scheduler for the other kernels that run one
+// CTA per (sequence, head) unit (the chunk-replay prefill).
+gdn_status launch_unit_sched(const int32_t* cu, int N, int T, int HV, int nslices, int32_t* work, unsigned* err,
+                             cudaStream_t stream) {
+    if (cudaMemsetAsync(err, 0, sizeof(unsigned), stream) != cudaSuccess) return GDN_ERR_CUDA;
+    gdn_sched_kernel<<<(N + 255) / 256, 256, 0, stream>>>(cu, N, T, HV, nslices, work, err);
+    return launch_status();
+}
+
 size_t fwd_workspace_size(const gdn_shape* s) {
     const int dvs = pick_dv_slice(s);
     return kWsHeader + (((size_t)s->N * s->HV * (s->dv / dvs) * sizeof(int32_t) + 255) & ~size_t(255));

@@ -1,0 +1,476 @@
+// gdn_replay.cu -- chunk-order-replaying prefill and decode for the gated
+// delta rule (the alternative to running the recurrent kernel everywhere).
+//
+// Both kernels evaluate every term through the device functions in the first
+// section below, with the same operands in the same order, which is what
+// makes decode bit-identical to prefill.  The state S0 lives in registers in
+// the row layout of gdn_step.cuh (its dk contractions are rows_dot); the
+// chunk's rows, the coefficient rows and the per-row quantities live in
+// shared memory.
+//
+// Prefill: one CTA per (sequence, head) walks its chunks.  Per chunk:
+//   A  q^, k^ of the new rows (l2norm_warp), g and b;
+//   B  the cumulative log-decay gam (one thread, in order);
+//   C  S0 k^_j and S0 q^_j (rows_dot) -> x_j = v_j - Gam_j S0 k^_j, o0_j = Gam_j S0 q^_j;
+//   D  the coefficient rows c_j, p_j (one thread per (j, i), fixed-order dots);
+//   E  d_j by forward substitution (one thread per row of d, rows j in order);
+//   F  o_j (one thread per (j, row));
+//   G  at the chunk end, S0 <- Gam_last S0 + sum_i exp(gam_last - gam_i) d_i k^_i^T.
+// Decode: one CTA per (sequence, head) does the same for its one new row j,
+// reading S0 and rows 0 .. j-1 from the replay state.
+#include <algorithm>
+
+#include "../../include/gdn_replay.h"
+#include "gdn_host.h"
+#include "gdn_step.cuh"
+
+namespace gdn {
+
+gdn_status launch_unit_sched(const int32_t* cu, int N, int T, int HV, int nslices, int32_t* work, unsigned* err,
+                             cudaStream_t stream);
+
+namespace {
+
+constexpr int kRC = GDN_REPLAY_CHUNK;
+constexpr int kLdD = 128;  // row stride (floats) of the d / x / o0 tiles: dv <= 128
+
+// ---------------------------------------------------------------- shared arithmetic
+// <a, b> over dk: four interleaved fma chains over the float4s in increasing
+// order, then (s0 + s1) + (s2 + s3).  a, b 16-byte aligned.
+template <int DK>
+__device__ __forceinline__ float vdot(const float* __restrict__ a, const float* __restrict__ b) {
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+    for (int c = 0; c < DK / 4; ++c) {
+        const float4 x = *reinterpret_cast<const float4*>(a + 4 * c);
+        const float4 y = *reinterpret_cast<const float4*>(b + 4 * c);
+        s0 = __fmaf_rn(x.x, y.x, s0);
+        s1 = __fmaf_rn(x.y, y.y, s1);
+        s2 = __fmaf_rn(x.z, y.z, s2);
+        s3 = __fmaf_rn(x.w, y.w, s3);
+    }
+    return __fadd_rn(__fadd_rn(s0, s1), __fadd_rn(s2, s3));
+}
+// gam_j = g_0 + ... + g_j, accumulated in order from the chunk start
+__device__ __forceinline__ float next_gamma(float prev, float g, int j) { return j == 0 ? g : __fadd_rn(prev, g); }
+__device__ __forceinline__ float decay(float gj, float gi) { return expf(__fsub_rn(gj, gi)); }
+__device__ __forceinline__ float coef(float gj, float gi, float dot) { return __fmul_rn(decay(gj, gi), dot); }
+__device__ __forceinline__ float resid(float v, float Gam, float sk) { return __fsub_rn(v, __fmul_rn(Gam, sk)); }
+__device__ __forceinline__ float out0(float Gam, float sq) { return __fmul_rn(Gam, sq); }
+// d_j[r] = b_j (x_j[r] - sum_{i<j} c_i d_i[r]): one fma chain in increasing i
+__device__ __forceinline__ float delta_row(float b, float x, const float* c, const float* D, int r, int j) {
+    float acc = 0.f;
+    for (int i = 0; i < j; ++i) acc = __fmaf_rn(c[i], D[i * kLdD + r], acc);
+    return __fmul_rn(b, __fsub_rn(x, acc));
+}
+// o_j[r] = o0_j[r] + sum_{i<=j} p_i d_i[r]: one fma chain in increasing i
+__device__ __forceinline__ float out_row(float o0, const float* p, const float* D, int r, int j) {
+    float acc = o0;
+    for (int i = 0; i <= j; ++i) acc = __fmaf_rn(p[i], D[i * kLdD + r], acc);
+    return acc;
+}
+// Chunk end, for the R rows a thread holds: every element is first scaled by
+// Gam_last, then gets fma(w_i, k^_i, .) for i in increasing order with
+// w_i = ew_i * d_i[row] (ew_i = exp(gam_last - gam_i)).  No shuffles.
+template <int DK, int R>
+__device__ __forceinline__ void rows_chunk_update(RowFrag<DK> (&S)[R], const float* kn, int ldk, const float* D,
+                                                  const float* ew, float gam_last_exp, int row0, int e) {
+    constexpr int NC = RowFrag<DK>::kChunks;
+    const float2 g2 = make_float2(gam_last_exp, gam_last_exp);
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int c = 0; c < 2 * NC; ++c) S[r].p[c] = __fmul2_rn(g2, S[r].p[c]);
+    for (int i = 0; i < kRC; ++i) {
+        float2 w2[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float w = __fmul_rn(ew[i], D[i * kLdD + row0 + r]);
+            w2[r] = make_float2(w, w);
+        }
+        const float* ki = kn + i * ldk;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            const float4 k4 = *reinterpret_cast<const float4*>(ki + 4 * chunk_of(c, e));
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                S[r].p[2 * c] = __ffma2_rn(w2[r], lo2(k4), S[r].p[2 * c]);
+                S[r].p[2 * c + 1] = __ffma2_rn(w2[r], hi2(k4), S[r].p[2 * c + 1]);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- parameters
+struct ReplayParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* g;
+    const float* beta;
+    const int32_t* cu;
+    const int32_t* seq_pos;
+    float* rs;
+    const int32_t* idx;
+    void* out;
+    const int32_t* work;
+    int num_slots, N, T, HK, HV, G, dv, use_norm;
+    long long blk;  // floats per (slot, head)
+};
+
+__host__ __device__ inline long long block_floats(int dk, int dv) {
+    return (long long)dv * dk + (long long)kRC * (dk + dv + 1);
+}
+
+// ---------------------------------------------------------------- prefill
+template <int DK>
+struct PrefillSmem {
+    float kn[kRC][DK + 4];  // padded rows: float4 reads of different rows hit different banks
+    float qn[kRC][DK + 4];
+    float X[kRC][kLdD];
+    float Q0[kRC][kLdD];
+    float D[kRC][kLdD];
+    float cm[kRC][kRC + 1];
+    float pm[kRC][kRC + 1];
+    float gam[kRC], Gam[kRC], beta[kRC], graw[kRC], ew[kRC];
+};
+
+template <typename Tin, int DK>
+__global__ void __launch_bounds__(kThreadsPer128Rows, 1) replay_prefill_kernel(const ReplayParams p) {
+    constexpr int R = kRowsPerThread;
+    extern __shared__ unsigned char smem_raw[];
+    PrefillSmem<DK>& sm =
+        *reinterpret_cast<PrefillSmem<DK>*>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5, nt = blockDim.x;
+    const int e = tid % kLanesPerRow, grp = tid / kLanesPerRow;
+    const int dv = p.dv;
+    const int row = grp * R;
+    const bool active = row < dv;
+    const int unit = p.work[blockIdx.x];
+    const int h = unit % p.HV, n = unit / p.HV, hk = h / p.G;
+    const int bos = min(max(p.cu[n], 0), p.T), eos = min(max(p.cu[n + 1], bos), p.T);
+    if (eos == bos) return;
+    const int slot = p.idx ? p.idx[n] : n;
+    if (slot < 0 || slot >= p.num_slots) return;
+    float* gS = p.rs + ((long long)slot * p.HV + h) * p.blk;
+    float* gK = gS + (size_t)dv * DK;
+    float* gD = gK + (size_t)kRC * DK;
+    float* gG = gD + (size_t)kRC * dv;
+    const int pos0 = (p.seq_pos ? max(p.seq_pos[n], 0) : 0) % kRC;
+    const Tin* q = static_cast<const Tin*>(p.q);
+    const Tin* k = static_cast<const Tin*>(p.k);
+    const Tin* v = static_cast<const Tin*>(p.v);
+    Tin* out = static_cast<Tin*>(p.out);
+
+    RowFrag<DK> S[R];
+    if (active) load_rows<DK, R>(S, gS + (size_t)row * DK, e);
+    else zero_rows<DK, R>(S);
+    // rows 0 .. pos0-1 of the open chunk
+    for (int x = tid; x < pos0 * (DK / 4); x += nt) {
+        const int i = x / (DK / 4), c = x % (DK / 4);
+        *reinterpret_cast<float4*>(&sm.kn[i][4 * c]) = *reinterpret_cast<const float4*>(gK + (size_t)i * DK + 4 * c);
+    }
+    for (int x = tid; x < pos0 * dv; x += nt) sm.D[x / dv][x % dv] = gD[x];
+    for (int i = tid; i < pos0; i += nt) sm.gam[i] = gG[i];
+
+    int j0 = pos0;
+    bool completed = false;
+    for (int t = bos; t < eos;) {
+        const int nj = min(kRC - j0, eos - t);
+        __syncthreads();  // the previous chunk's readers are done; the cached rows are in
+        // A: q^, k^, g, b of the new rows j0 .. j0+nj-1
+        for (int w = warp; w < 2 * nj; w += nwarps) {
+            const int jj = w >> 1;
+            const size_t off = ((size_t)(t + jj) * p.HK + hk) * DK;
+            if (w & 1) l2norm_warp<DK>(k + off, &sm.kn[j0 + jj][0], lane, p.use_norm != 0);
+            else l2norm_warp<DK>(q + off, &sm.qn[j0 + jj][0], lane, p.use_norm != 0);
+        }
+        if (tid < nj) {
+            const size_t gi = (size_t)(t + tid) * p.HV + h;
+            sm.graw[j0 + tid] = p.g[gi];
+            sm.beta[j0 + tid] = p.beta[gi];
+        }
+        __syncthreads();
+        // B
+        if (tid == 0) {
+            float gm = j0 > 0 ? sm.gam[j0 - 1] : 0.f;
+            for (int j = j0; j < j0 + nj; ++j) {
+                gm = next_gamma(gm, sm.graw[j], j);
+                sm.gam[j] = gm;
+                sm.Gam[j] = expf(gm);
+            }
+        }
+        __syncthreads();
+        // C
+        for (int j = j0; j < j0 + nj; ++j) {
+            float sk[R], sq[R];
+            rows_dot<DK, R>(S, &sm.kn[j][0], e, sk);
+            rows_dot<DK, R>(S, &sm.qn[j][0], e, sq);
+            if (active && e == 0) {
+                const float Gj = sm.Gam[j];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const float vv = ld_in(v + ((size_t)(t + j - j0) * p.HV + h) * dv + row + r);
+                    sm.X[j][row + r] = resid(vv, Gj, sk[r]);
+                    sm.Q0[j][row + r] = out0(Gj, sq[r]);
+                }
+            }
+        }
+        // D
+        for (int x = tid; x < nj * kRC; x += nt) {
+            const int j = j0 + x / kRC, i = x % kRC;
+            if (i <= j) {
+                const float gj = sm.gam[j], gi = sm.gam[i];
+                if (i < j) sm.cm[j][i] = coef(gj, gi, vdot<DK>(&sm.kn[j][0], &sm.kn[i][0]));
+                sm.pm[j][i] = coef(gj, gi, vdot<DK>(&sm.qn[j][0], &sm.kn[i][0]));
+            }
+        }
+        __syncthreads();
+        // E
+        if (tid < dv)
+            for (int j = j0; j < j0 + nj; ++j)
+                sm.D[j][tid] = delta_row(sm.beta[j], sm.X[j][tid], &sm.cm[j][0], &sm.D[0][0], tid, j);
+        __syncthreads();
+        // F
+        for (int x = tid; x < nj * dv; x += nt) {
+            const int jj = x / dv, r = x % dv, j = j0 + jj;
+            st_in(out + ((size_t)(t + jj) * p.HV + h) * dv + r, out_row(sm.Q0[j][r], &sm.pm[j][0], &sm.D[0][0], r, j));
+        }
+        t += nj;
+        if (j0 + nj == kRC) {
+            // G
+            if (tid < kRC) sm.ew[tid] = decay(sm.gam[kRC - 1], sm.gam[tid]);
+            __syncthreads();
+            if (active) rows_chunk_update<DK, R>(S, &sm.kn[0][0], DK + 4, &sm.D[0][0], sm.ew, sm.Gam[kRC - 1], row, e);
+            j0 = 0;
+            completed = true;
+        } else {
+            j0 += nj;
+        }
+    }
+    __syncthreads();
+    // write back the chunk-start state (when a chunk ended) and the open chunk's new rows
+    if (completed && active) store_rows<DK, R>(S, gS + (size_t)row * DK, e);
+    const int r0 = completed ? 0 : pos0;
+    for (int x = tid; x < (j0 - r0) * (DK / 4); x += nt) {
+        const int i = r0 + x / (DK / 4), c = x % (DK / 4);
+        *reinterpret_cast<float4*>(gK + (size_t)i * DK + 4 * c) = *reinterpret_cast<const float4*>(&sm.kn[i][4 * c]);
+    }
+    for (int x = tid; x < (j0 - r0) * dv; x += nt) {
+        const int i = r0 + x / dv, r = x % dv;
+        gD[(size_t)i * dv + r] = sm.D[i][r];
+    }
+    for (int i = r0 + tid; i < j0; i += nt) gG[i] = sm.gam[i];
+}
+
+// ---------------------------------------------------------------- decode
+template <int DK>
+struct DecodeSmem {
+    float kn[kRC][DK + 4];
+    float D[kRC][kLdD];
+    float qn[DK];
+    float c[kRC], pp[kRC], gam[kRC], ew[kRC];
+    float X[kLdD], Q0[kLdD];
+    float Gj, bj;
+};
+
+template <typename Tin, int DK>
+__global__ void __launch_bounds__(kThreadsPer128Rows) replay_decode_kernel(const ReplayParams p) {
+    constexpr int R = kRowsPerThread;
+    extern __shared__ unsigned char smem_raw[];
+    DecodeSmem<DK>& sm =
+        *reinterpret_cast<DecodeSmem<DK>*>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5, nt = blockDim.x;
+    const int e = tid % kLanesPerRow, grp = tid / kLanesPerRow;
+    const int dv = p.dv;
+    const int row = grp * R;
+    const bool active = row < dv;
+    const int b = blockIdx.x / p.HV, h = blockIdx.x % p.HV, hk = h / p.G;
+    const int slot = p.idx ? p.idx[b] : b;
+    if (slot < 0 || slot >= p.num_slots) return;
+    float* gS = p.rs + ((long long)slot * p.HV + h) * p.blk;
+    float* gK = gS + (size_t)dv * DK;
+    float* gD = gK + (size_t)kRC * DK;
+    float* gG = gD + (size_t)kRC * dv;
+    const int j = max(p.seq_pos[b], 0) % kRC;
+    const Tin* q = static_cast<const Tin*>(p.q);
+    const Tin* k = static_cast<const Tin*>(p.k);
+    const Tin* v = static_cast<const Tin*>(p.v);
+
+    for (int x = tid; x < j * (DK / 4); x += nt) {
+        const int i = x / (DK / 4), c = x % (DK / 4);
+        *reinterpret_cast<float4*>(&sm.kn[i][4 * c]) = *reinterpret_cast<const float4*>(gK + (size_t)i * DK + 4 * c);
+    }
+    for (int x = tid; x < j * dv; x += nt) sm.D[x / dv][x % dv] = gD[x];
+    for (int i = tid; i < j; i += nt) sm.gam[i] = gG[i];
+    const size_t off = ((size_t)b * p.HK + hk) * DK;
+    if (warp == 0) l2norm_warp<DK>(q + off, sm.qn, lane, p.use_norm != 0);
+    if (warp == (nwarps > 1 ? 1 : 0)) l2norm_warp<DK>(k + off, &sm.kn[j][0], lane, p.use_norm != 0);
+    RowFrag<DK> S[R];
+    if (active) load_rows<DK, R>(S, gS + (size_t)row * DK, e);
+    else zero_rows<DK, R>(S);
+    __syncthreads();
+    if (tid == 0) {
+        const size_t gi = (size_t)b * p.HV + h;
+        const float gm = next_gamma(j > 0 ? sm.gam[j - 1] : 0.f, p.g[gi], j);
+        sm.gam[j] = gm;
+        sm.Gj = expf(gm);
+        sm.bj = p.beta[gi];
+    }
+    __syncthreads();
+    float sk[R], sq[R];
+    rows_dot<DK, R>(S, &sm.kn[j][0], e, sk);
+    rows_dot<DK, R>(S, sm.qn, e, sq);
+    if (active && e == 0) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float vv = ld_in(v + ((size_t)b * p.HV + h) * dv + row + r);
+            sm.X[row + r] = resid(vv, sm.Gj, sk[r]);
+            sm.Q0[row + r] = out0(sm.Gj, sq[r]);
+        }
+    }
+    const float gj = sm.gam[j];
+    for (int i = tid; i <= j; i += nt) {
+        const float gi = sm.gam[i];
+        if (i < j) sm.c[i] = coef(gj, gi, vdot<DK>(&sm.kn[j][0], &sm.kn[i][0]));
+        sm.pp[i] = coef(gj, gi, vdot<DK>(sm.qn, &sm.kn[i][0]));
+    }
+    __syncthreads();
+    if (tid < dv) sm.D[j][tid] = delta_row(sm.bj, sm.X[tid], sm.c, &sm.D[0][0], tid, j);
+    __syncthreads();
+    if (tid < dv)
+        st_in(static_cast<Tin*>(p.out) + ((size_t)b * p.HV + h) * dv + tid,
+              out_row(sm.Q0[tid], sm.pp, &sm.D[0][0], tid, j));
+    // the new row of the open chunk
+    for (int c = tid; c < DK / 4; c += nt)
+        *reinterpret_cast<float4*>(gK + (size_t)j * DK + 4 * c) = *reinterpret_cast<const float4*>(&sm.kn[j][4 * c]);
+    if (tid < dv) gD[(size_t)j * dv + tid] = sm.D[j][tid];
+    if (tid == 0) gG[j] = gj;
+    if (j == kRC - 1) {
+        if (tid < kRC) sm.ew[tid] = decay(gj, sm.gam[tid]);
+        __syncthreads();
+        if (active) {
+            rows_chunk_update<DK, R>(S, &sm.kn[0][0], DK + 4, &sm.D[0][0], sm.ew, sm.Gj, row, e);
+            store_rows<DK, R>(S, gS + (size_t)row * DK, e);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- launch
+template <typename Tin, int DK>
+gdn_status launch_prefill_t(const ReplayParams& p, int units, int nt, cudaStream_t s) {
+    const size_t smem = sizeof(PrefillSmem<DK>) + 16;
+    auto kern = replay_prefill_kernel<Tin, DK>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    kern<<<units, nt, smem, s>>>(p);
+    return launch_status();
+}
+
+template <typename Tin, int DK>
+gdn_status launch_decode_t(const ReplayParams& p, int units, int nt, cudaStream_t s) {
+    const size_t smem = sizeof(DecodeSmem<DK>) + 16;
+    auto kern = replay_decode_kernel<Tin, DK>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    kern<<<units, nt, smem, s>>>(p);
+    return launch_status();
+}
+
+template <bool kPrefill, typename Tin>
+gdn_status launch_dk(int dk, const ReplayParams& p, int units, int nt, cudaStream_t s) {
+    switch (dk) {
+        case 16: return kPrefill ? launch_prefill_t<Tin, 16>(p, units, nt, s) : launch_decode_t<Tin, 16>(p, units, nt, s);
+        case 32: return kPrefill ? launch_prefill_t<Tin, 32>(p, units, nt, s) : launch_decode_t<Tin, 32>(p, units, nt, s);
+        case 64: return kPrefill ? launch_prefill_t<Tin, 64>(p, units, nt, s) : launch_decode_t<Tin, 64>(p, units, nt, s);
+        case 128:
+            return kPrefill ? launch_prefill_t<Tin, 128>(p, units, nt, s) : launch_decode_t<Tin, 128>(p, units, nt, s);
+    }
+    return GDN_ERR_UNSUPPORTED;
+}
+
+gdn_status check_replay(const gdn_shape* s, const void* q, const void* k, const void* v, const float* g,
+                        const float* beta, const float* rs, const int32_t* idx, int num_slots, const void* out) {
+    gdn_status st = check_shape(s);
+    if (st != GDN_OK) return st;
+    if (!rs || num_slots < 0) return GDN_ERR_INVALID_ARG;
+    if (!idx && num_slots < s->N) return GDN_ERR_INVALID_ARG;
+    if (s->T_total > 0 && (!q || !k || !v || !g || !beta || !out)) return GDN_ERR_INVALID_ARG;
+    if ((q && !aligned16(q)) || (k && !aligned16(k)) || (v && !aligned16(v)) || (out && !aligned16(out)) ||
+        !aligned16(rs) || (g && !aligned4(g)) || (beta && !aligned4(beta)) || (idx && !aligned4(idx)))
+        return GDN_ERR_INVALID_ARG;
+    if (out && (out == q || out == k || out == v || out == rs)) return GDN_ERR_INVALID_ARG;
+    return GDN_OK;
+}
+
+ReplayParams make_params(const gdn_shape* s, const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, const int32_t* cu, const int32_t* seq_pos, float* rs,
+                         const int32_t* idx, int num_slots, void* out, const int32_t* work) {
+    ReplayParams p;
+    p.q = q, p.k = k, p.v = v, p.g = g, p.beta = beta, p.cu = cu, p.seq_pos = seq_pos, p.rs = rs, p.idx = idx;
+    p.out = out, p.work = work, p.num_slots = num_slots, p.N = s->N, p.T = s->T_total, p.HK = s->HK;
+    p.HV = s->HV, p.G = s->HV / s->HK, p.dv = s->dv, p.use_norm = s->use_qk_l2norm ? 1 : 0;
+    p.blk = block_floats(s->dk, s->dv);
+    return p;
+}
+
+}  // namespace
+}  // namespace gdn
+
+extern "C" size_t gdn_replay_block_floats(int dk, int dv) {
+    using namespace gdn;
+    if (!dim_ok(dk) || !dim_ok(dv)) return 0;
+    return (size_t)block_floats(dk, dv);
+}
+
+extern "C" size_t gdn_replay_workspace_size(const gdn_shape* s) {
+    using namespace gdn;
+    if (check_shape(s) != GDN_OK) return 0;
+    return kWsHeader + (((size_t)s->N * s->HV * sizeof(int32_t) + 255) & ~size_t(255));
+}
+
+extern "C" gdn_status gdn_replay_prefill(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                                         const float* g, const float* beta, const int32_t* cu_seqlens,
+                                         const int32_t* seq_pos, float* replay_state, const int32_t* state_indices,
+                                         int num_slots, void* out, void* workspace, size_t workspace_bytes,
+                                         void* stream) {
+    using namespace gdn;
+    gdn_status st = check_replay(shape, q, k, v, g, beta, replay_state, state_indices, num_slots, out);
+    if (st != GDN_OK) return st;
+    if (!cu_seqlens || !aligned4(cu_seqlens) || (seq_pos && !aligned4(seq_pos))) return GDN_ERR_INVALID_ARG;
+    if (shape->N == 0) return GDN_OK;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < gdn_replay_workspace_size(shape))
+        return GDN_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    int32_t* work = reinterpret_cast<int32_t*>(ws + kWsHeader);
+    st = launch_unit_sched(cu_seqlens, shape->N, shape->T_total, shape->HV, 1, work, reinterpret_cast<unsigned*>(ws),
+                           s);
+    if (st != GDN_OK) return st;
+    const ReplayParams p = make_params(shape, q, k, v, g, beta, cu_seqlens, seq_pos, replay_state, state_indices,
+                                       num_slots, out, work);
+    const int nt = std::max(32, shape->dv * kLanesPerRow / kRowsPerThread);
+    const int units = shape->N * shape->HV;
+    return shape->dtype == GDN_BF16 ? launch_dk<true, __nv_bfloat16>(shape->dk, p, units, nt, s)
+                                    : launch_dk<true, float>(shape->dk, p, units, nt, s);
+}
+
+extern "C" gdn_status gdn_replay_decode(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                                        const float* g, const float* beta, const int32_t* seq_pos,
+                                        float* replay_state, const int32_t* state_indices, int num_slots, void* out,
+                                        void* stream) {
+    using namespace gdn;
+    gdn_status st = check_replay(shape, q, k, v, g, beta, replay_state, state_indices, num_slots, out);
+    if (st != GDN_OK) return st;
+    if (shape->T_total != shape->N) return GDN_ERR_INVALID_ARG;
+    if (!seq_pos || !aligned4(seq_pos)) return GDN_ERR_INVALID_ARG;
+    if (shape->N == 0) return GDN_OK;
+    const ReplayParams p = make_params(shape, q, k, v, g, beta, nullptr, seq_pos, replay_state, state_indices,
+                                       num_slots, out, nullptr);
+    const int nt = std::max(32, shape->dv * kLanesPerRow / kRowsPerThread);
+    const long long units = (long long)shape->N * shape->HV;
+    if (units >= (1LL << 31)) return GDN_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return shape->dtype == GDN_BF16 ? launch_dk<false, __nv_bfloat16>(shape->dk, p, (int)units, nt, s)
+                                    : launch_dk<false, float>(shape->dk, p, (int)units, nt, s);
+}

@@ -162,3 +162,24 @@ def test_layer_ops_host_validation(lib):
     assert upd(ctypes.byref(conv_shape(N=4, T_total=4)), x, cw, cb, None, idx, 4, cy, None) == -1
     assert upd(ctypes.byref(conv_shape(N=4, T_total=4)), x, cw, cb, st, None, 3, cy, None) == -1
     assert upd(ctypes.byref(conv_shape(N=4, T_total=4, dtype=3)), x, cw, cb, st, idx, 4, cy, None) == -2
+
+
+def test_replay_host_validation(lib):
+    P = ctypes.c_void_p
+    assert lib.gdn_replay_block_floats(128, 128) == 128 * 128 + 64 * (128 + 128 + 1)
+    assert lib.gdn_replay_block_floats(48, 128) == 0
+    s = shape(N=4, T_total=4)
+    assert lib.gdn_replay_workspace_size(ctypes.byref(s)) >= 256 + 4 * 4 * 4
+    q, k, v, g, b, cu, sp, rs, idx, out, ws = [P(FAKE + i * 0x1000) for i in range(11)]
+    pre = lib.gdn_replay_prefill
+    assert pre(ctypes.byref(s), q, k, v, g, b, None, sp, rs, idx, 4, out, ws, 1 << 20, None) == -1   # no cu
+    assert pre(ctypes.byref(s), q, k, v, g, b, cu, sp, None, idx, 4, out, ws, 1 << 20, None) == -1   # no state
+    assert pre(ctypes.byref(s), q, k, v, g, b, cu, sp, rs, None, 3, out, ws, 1 << 20, None) == -1    # slots < N
+    assert pre(ctypes.byref(s), q, k, v, g, b, cu, sp, rs, idx, 4, q, ws, 1 << 20, None) == -1      # out aliases q
+    assert pre(ctypes.byref(s), q, k, v, g, b, cu, sp, rs, idx, 4, out, None, 1 << 20, None) == -3
+    assert pre(ctypes.byref(shape(N=4, T_total=4, dk=96)), q, k, v, g, b, cu, sp, rs, idx, 4, out, ws, 1 << 20,
+               None) == -2
+    dec = lib.gdn_replay_decode
+    assert dec(ctypes.byref(s), q, k, v, g, b, None, rs, idx, 4, out, None) == -1                    # no seq_pos
+    assert dec(ctypes.byref(shape(N=4, T_total=5)), q, k, v, g, b, sp, rs, idx, 4, out, None) == -1
+    assert dec(ctypes.byref(s), q, k, v, g, b, sp, P(FAKE + 8), idx, 4, out, None) == -1             # misaligned
