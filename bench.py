@@ -23,6 +23,7 @@ workload.  Under torchrun every rank runs its own replica of the workload
 (the path has no exchange step); rank 0 prints one JSON line.
 """
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -385,6 +386,13 @@ def main():
         except Exception as exc:  # reported, not hidden
             result["layer_ops"] = {"error": str(exc)[:300]}
 
+    # ---- the chunk-order-replaying variant on the same workloads, for comparison
+    if rank == 0 and not small:
+        try:
+            result["chunk_replay"] = bench_replay(gdn, d, dd, dev, hbm_peak, fwd_avg, dec_avg)
+        except Exception as exc:  # reported, not hidden
+            result["chunk_replay"] = {"error": str(exc)[:300]}
+
     # ---- end to end through the C ABI from pinned host buffers
     if not args.no_e2e and not small:
         result["e2e"] = e2e(gdn, d.cpu(), dd.cpu(), st0.cpu(), dev, steps=min(steps, 5))
@@ -584,6 +592,59 @@ def bench_layer_ops(gdn, lengths, dev, hbm_peak, reps=5):
                        f"SiLU; RMSNorm over dv={DV} for T*HV rows, bf16; decode ops at batch {DEC_B}; device time "
                        f"per call from CUDA-graph replay")
     return res
+
+
+def bench_replay(gdn, d, dd, dev, hbm_peak, rec_prefill_ms, rec_decode_ms, reps=3):
+    """The chunk-order-replaying variant (chunked prefill, decode replaying its
+    order) on the prefill workload and on the decode batch, next to the
+    recurrent kernel's times from the main step.  Decode positions are drawn
+    uniformly over the 64-token chunk (seed 9), so on average half a chunk of
+    cached rows is read per step; its algorithmic bytes per (sequence, head)
+    are the chunk-start state read (dv*dk*4), the cached k^/d/gam rows read,
+    the new row written, plus the state write at a chunk end."""
+    N = len(d.lengths)
+    rs = gdn.replay_state_new(N, HV, DK, DV, device=dev)
+    out = torch.empty_like(d.v)
+    sh = gdn.make_shape(d.q, d.v, N)
+    ws = torch.zeros(max(int(gdn.lib().gdn_replay_workspace_size(ctypes.byref(sh))), 256), dtype=torch.uint8,
+                     device=dev)
+    run = lambda: gdn.gdn_replay_prefill(d.q, d.k, d.v, d.g, d.beta, d.cu_seqlens, rs, out=out,  # noqa: E731
+                                         workspace=ws)
+    run()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        rs.zero_()
+        run()
+    b.record()
+    torch.cuda.synchronize()
+    # the zeroing is timed on its own and taken out
+    z0, z1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    z0.record()
+    for _ in range(reps):
+        rs.zero_()
+    z1.record()
+    torch.cuda.synchronize()
+    pre_ms = (a.elapsed_time(b) - z0.elapsed_time(z1)) / reps
+    T = d.q.shape[0]
+    B = dd.q.shape[0]
+    gen = torch.Generator(device="cpu").manual_seed(9)
+    seq_pos = torch.randint(0, 64, (B,), generator=gen, dtype=torch.int32).to(dev)
+    pool = gdn.replay_state_new(B, HV, DK, DV, device=dev)
+    pool.normal_()
+    dout = torch.empty_like(dd.v)
+    dec_ms = _time_ms(lambda: gdn.gdn_replay_decode(dd.q, dd.k, dd.v, dd.g, dd.beta, pool, seq_pos, out=dout), 20)
+    j = seq_pos.double()
+    row_bytes = (DK + DV + 1) * 4
+    per_unit = DV * DK * 4 + j * row_bytes + row_bytes + (j == 63).double() * DV * DK * 4
+    dec_bytes = float(per_unit.sum().item()) * HV + B * (2 * HK * DK * 2 + 2 * HV * DV * 2 + HV * 8)
+    gbs = dec_bytes / (dec_ms / 1e3) / 1e9
+    return {"prefill": {"ms": pre_ms, "tokens_per_s": T / (pre_ms / 1e3), "vs_recurrent_time": pre_ms / rec_prefill_ms},
+            "decode": {"ms": dec_ms, "steps_per_s": 1e3 / dec_ms, "vs_recurrent_time": dec_ms / rec_decode_ms,
+                       "bytes": dec_bytes, "gbs": gbs, "hbm_frac": gbs / hbm_peak},
+            "state_bytes_per_head": gdn.replay_block_floats(DK, DV) * 4,
+            "note": "chunk 64; decode positions uniform in the chunk (seed 9); replay state ~2x the plain state"}
 
 
 def bench_backward(gdn, dev, steps=3):

@@ -280,7 +280,7 @@ struct ConvParams {
 // a sequence is the only reader of its initial conv state and can also write
 // the final state afterwards: in-place slots are safe.
 template <typename T, int W>
-__global__ void __launch_bounds__(128) conv_fwd_kernel(const ConvParams p) {
+__global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) conv_fwd_kernel(const ConvParams p) {
     constexpr int VN = V16<T>::n;
     constexpr int WM = W - 1;
     constexpr int U = 4;  // rows per register buffer (two buffers)

@@ -57,17 +57,31 @@ __device__ __forceinline__ float decay(float gj, float gi) { return expf(__fsub_
 __device__ __forceinline__ float coef(float gj, float gi, float dot) { return __fmul_rn(decay(gj, gi), dot); }
 __device__ __forceinline__ float resid(float v, float Gam, float sk) { return __fsub_rn(v, __fmul_rn(Gam, sk)); }
 __device__ __forceinline__ float out0(float Gam, float sq) { return __fmul_rn(Gam, sq); }
-// d_j[r] = b_j (x_j[r] - sum_{i<j} c_i d_i[r]): one fma chain in increasing i
-__device__ __forceinline__ float delta_row(float b, float x, const float* c, const float* D, int r, int j) {
-    float acc = 0.f;
-    for (int i = 0; i < j; ++i) acc = __fmaf_rn(c[i], D[i * kLdD + r], acc);
-    return __fmul_rn(b, __fsub_rn(x, acc));
-}
-// o_j[r] = o0_j[r] + sum_{i<=j} p_i d_i[r]: one fma chain in increasing i
-__device__ __forceinline__ float out_row(float o0, const float* p, const float* D, int r, int j) {
-    float acc = o0;
-    for (int i = 0; i <= j; ++i) acc = __fmaf_rn(p[i], D[i * kLdD + r], acc);
+// sum_{i<n} c_i D[i][r] added to acc: one fma chain in increasing i.  The
+// operands are fetched eight at a time ahead of their fmas (shared-memory
+// latency overlaps the chain); the chain itself is unchanged.
+__device__ __forceinline__ float chain(float acc, const float* c, const float* D, int r, int n) {
+    int i = 0;
+    for (; i + 8 <= n; i += 8) {
+        float cv[8], dv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            cv[u] = c[i + u];
+            dv[u] = D[(i + u) * kLdD + r];
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc = __fmaf_rn(cv[u], dv[u], acc);
+    }
+    for (; i < n; ++i) acc = __fmaf_rn(c[i], D[i * kLdD + r], acc);
     return acc;
+}
+// d_j[r] = b_j (x_j[r] - sum_{i<j} c_i d_i[r])
+__device__ __forceinline__ float delta_row(float b, float x, const float* c, const float* D, int r, int j) {
+    return __fmul_rn(b, __fsub_rn(x, chain(0.f, c, D, r, j)));
+}
+// o_j[r] = o0_j[r] + sum_{i<=j} p_i d_i[r]
+__device__ __forceinline__ float out_row(float o0, const float* p, const float* D, int r, int j) {
+    return chain(o0, p, D, r, j + 1);
 }
 // Chunk end, for the R rows a thread holds: every element is first scaled by
 // Gam_last, then gets fma(w_i, k^_i, .) for i in increasing order with
@@ -275,7 +289,7 @@ struct DecodeSmem {
 };
 
 template <typename Tin, int DK>
-__global__ void __launch_bounds__(kThreadsPer128Rows) replay_decode_kernel(const ReplayParams p) {
+__global__ void __launch_bounds__(kThreadsPer128Rows, 2) replay_decode_kernel(const ReplayParams p) {
     constexpr int R = kRowsPerThread;
     extern __shared__ unsigned char smem_raw[];
     DecodeSmem<DK>& sm =
@@ -306,10 +320,17 @@ __global__ void __launch_bounds__(kThreadsPer128Rows) replay_decode_kernel(const
     const size_t off = ((size_t)b * p.HK + hk) * DK;
     if (warp == 0) l2norm_warp<DK>(q + off, sm.qn, lane, p.use_norm != 0);
     if (warp == (nwarps > 1 ? 1 : 0)) l2norm_warp<DK>(k + off, &sm.kn[j][0], lane, p.use_norm != 0);
-    RowFrag<DK> S[R];
-    if (active) load_rows<DK, R>(S, gS + (size_t)row * DK, e);
-    else zero_rows<DK, R>(S);
-    __syncthreads();
+    float sk[R], sq[R];
+    {
+        // S0 is needed twice: here for S0 k^ and S0 q^, and at a chunk end (one
+        // step in 64), where it is read again rather than kept live throughout
+        RowFrag<DK> S[R];
+        if (active) load_rows<DK, R>(S, gS + (size_t)row * DK, e);
+        else zero_rows<DK, R>(S);
+        __syncthreads();
+        rows_dot<DK, R>(S, &sm.kn[j][0], e, sk);
+        rows_dot<DK, R>(S, sm.qn, e, sq);
+    }
     if (tid == 0) {
         const size_t gi = (size_t)b * p.HV + h;
         const float gm = next_gamma(j > 0 ? sm.gam[j - 1] : 0.f, p.g[gi], j);
@@ -318,9 +339,6 @@ __global__ void __launch_bounds__(kThreadsPer128Rows) replay_decode_kernel(const
         sm.bj = p.beta[gi];
     }
     __syncthreads();
-    float sk[R], sq[R];
-    rows_dot<DK, R>(S, &sm.kn[j][0], e, sk);
-    rows_dot<DK, R>(S, sm.qn, e, sq);
     if (active && e == 0) {
 #pragma unroll
         for (int r = 0; r < R; ++r) {
@@ -350,6 +368,8 @@ __global__ void __launch_bounds__(kThreadsPer128Rows) replay_decode_kernel(const
         if (tid < kRC) sm.ew[tid] = decay(gj, sm.gam[tid]);
         __syncthreads();
         if (active) {
+            RowFrag<DK> S[R];
+            load_rows<DK, R>(S, gS + (size_t)row * DK, e);
             rows_chunk_update<DK, R>(S, &sm.kn[0][0], DK + 4, &sm.D[0][0], sm.ew, sm.Gj, row, e);
             store_rows<DK, R>(S, gS + (size_t)row * DK, e);
         }
