@@ -192,12 +192,27 @@ __global__ void __launch_bounds__(kThreadsPer128Rows, 1) replay_prefill_kernel(c
     for (int t = bos; t < eos;) {
         const int nj = min(kRC - j0, eos - t);
         __syncthreads();  // the previous chunk's readers are done; the cached rows are in
-        // A: q^, k^, g, b of the new rows j0 .. j0+nj-1
-        for (int w = warp; w < 2 * nj; w += nwarps) {
-            const int jj = w >> 1;
-            const size_t off = ((size_t)(t + jj) * p.HK + hk) * DK;
-            if (w & 1) l2norm_warp<DK>(k + off, &sm.kn[j0 + jj][0], lane, p.use_norm != 0);
-            else l2norm_warp<DK>(q + off, &sm.qn[j0 + jj][0], lane, p.use_norm != 0);
+        // A: q^, k^, g, b and v of the new rows j0 .. j0+nj-1.  Eight vectors per
+        // warp are normalised together (their loads are in flight at once); v
+        // goes into the x tile with one coalesced pass.
+        for (int w0 = warp; w0 < 2 * nj; w0 += 8 * nwarps) {
+            const Tin* src[8];
+            float* dst[8];
+            int nv = 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int w = w0 + u * nwarps, jj = w >> 1;
+                const bool ok = w < 2 * nj;
+                nv += ok;
+                const size_t off = ((size_t)(t + (ok ? jj : 0)) * p.HK + hk) * DK;
+                src[u] = (w & 1) ? k + off : q + off;
+                dst[u] = ok ? ((w & 1) ? &sm.kn[j0 + jj][0] : &sm.qn[j0 + jj][0]) : &sm.qn[j0][0];
+            }
+            l2norm_warp_multi<DK, 8>(src, dst, nv, lane, p.use_norm != 0);
+        }
+        for (int x = tid; x < nj * dv; x += nt) {
+            const int jj = x / dv, r = x % dv;
+            sm.X[j0 + jj][r] = ld_in(v + ((size_t)(t + jj) * p.HV + h) * dv + r);
         }
         if (tid < nj) {
             const size_t gi = (size_t)(t + tid) * p.HV + h;
@@ -224,8 +239,7 @@ __global__ void __launch_bounds__(kThreadsPer128Rows, 1) replay_prefill_kernel(c
                 const float Gj = sm.Gam[j];
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    const float vv = ld_in(v + ((size_t)(t + j - j0) * p.HV + h) * dv + row + r);
-                    sm.X[j][row + r] = resid(vv, Gj, sk[r]);
+                    sm.X[j][row + r] = resid(sm.X[j][row + r], Gj, sk[r]);
                     sm.Q0[j][row + r] = out0(Gj, sq[r]);
                 }
             }
