@@ -60,6 +60,10 @@ def parse():
                     help="ncu run at full occupancy: 9 sequences x 4096 tokens (288 units), 2 steps, no extras")
     ap.add_argument("--profile-backward", action="store_true",
                     help="ncu run of the backward alone: 2 x 4096 tokens, 2 calls")
+    ap.add_argument("--profile-extras", action="store_true",
+                    help="ncu run of the layer ops and the chunk-replay variant, one call each: layer ops on 8 "
+                         "lognormal sequences (31,823 tokens), replay prefill on 9 x 2048 tokens, replay decode and "
+                         "conv update at batch 256")
     return ap.parse_args()
 
 
@@ -248,6 +252,9 @@ def main():
         return
     if args.profile_backward:
         profile_backward()
+        return
+    if args.profile_extras:
+        profile_extras()
         return
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -645,6 +652,30 @@ def bench_replay(gdn, d, dd, dev, hbm_peak, rec_prefill_ms, rec_decode_ms, reps=
                        "bytes": dec_bytes, "gbs": gbs, "hbm_frac": gbs / hbm_peak},
             "state_bytes_per_head": gdn.replay_block_floats(DK, DV) * 4,
             "note": "chunk 64; decode positions uniform in the chunk (seed 9); replay state ~2x the plain state"}
+
+
+def profile_extras():
+    """One call of each layer op and of the replay prefill / decode (for ncu captures)."""
+    import invariant_linear_attention_gb300 as gdn
+    from invariant_linear_attention_gb300 import inputs
+    dev = torch.device("cuda", 0)
+    lengths = inputs.lognormal_lengths(8, MEAN_LEN, CAP, seed=4)
+    L = inputs.make_layer_inputs(lengths, HK=HK, HV=HV, dk=DK, dv=DV, W=4, seed=7, device=dev)
+    D = inputs.make_layer_inputs([1] * DEC_B, HK=HK, HV=HV, dk=DK, dv=DV, W=4, seed=8, device=dev)
+    x = inputs.make_inputs([2048] * 9, HK=HK, HV=HV, dk=DK, dv=DV, dtype=torch.bfloat16, seed=4, device=dev)
+    dd = inputs.make_inputs([1] * DEC_B, HK=HK, HV=HV, dk=DK, dv=DV, dtype=torch.bfloat16, seed=5, device=dev)
+    rs = gdn.replay_state_new(9, HV, DK, DV, device=dev)
+    pool = gdn.replay_state_new(DEC_B, HV, DK, DV, device=dev).normal_()
+    seq_pos = torch.randint(0, 64, (DEC_B,), generator=torch.Generator().manual_seed(9), dtype=torch.int32).to(dev)
+    torch.cuda.synchronize()
+    gdn.gdn_causal_conv1d_fwd(L.x, L.conv_w, L.cu_seqlens, bias=L.conv_b, conv_state=L.conv_state)
+    gdn.gdn_gated_rmsnorm(L.o, L.z, L.norm_w)
+    gdn.gdn_gates(L.a, L.b, L.A_log, L.dt_bias)
+    gdn.gdn_causal_conv1d_update(D.x, D.conv_w, D.conv_state, bias=D.conv_b)
+    gdn.gdn_replay_prefill(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, rs)
+    gdn.gdn_replay_decode(dd.q, dd.k, dd.v, dd.g, dd.beta, pool, seq_pos)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_extras": "ok", "tokens": int(L.x.shape[0])}))
 
 
 def bench_backward(gdn, dev, steps=3):
