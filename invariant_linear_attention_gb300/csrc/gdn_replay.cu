@@ -57,12 +57,18 @@ __device__ __forceinline__ float decay(float gj, float gi) { return expf(__fsub_
 __device__ __forceinline__ float coef(float gj, float gi, float dot) { return __fmul_rn(decay(gj, gi), dot); }
 __device__ __forceinline__ float resid(float v, float Gam, float sk) { return __fsub_rn(v, __fmul_rn(Gam, sk)); }
 __device__ __forceinline__ float out0(float Gam, float sq) { return __fmul_rn(Gam, sq); }
-// sum_{i<n} c_i D[i][r] added to acc: one fma chain in increasing i.  The
-// operands are fetched eight at a time ahead of their fmas (shared-memory
-// latency overlaps the chain); the chain itself is unchanged.
-__device__ __forceinline__ float chain(float acc, const float* c, const float* D, int r, int n) {
-    int i = 0;
-    for (; i + 8 <= n; i += 8) {
+constexpr int kSub = 16;  // rows per sub-block of the forward substitution
+#ifndef GDN_REPLAY_TI
+#define GDN_REPLAY_TI 4
+#endif
+constexpr int kTI = GDN_REPLAY_TI;  // columns per coefficient task
+
+// acc + sum_{i0<=i<i1} c_i D[i][r]: one fma chain in increasing i.  The operands
+// are fetched eight at a time ahead of their fmas (shared-memory latency
+// overlaps the chain); the chain itself is unchanged.
+__device__ __forceinline__ float chain(float acc, const float* c, const float* D, int r, int i0, int i1) {
+    int i = i0;
+    for (; i + 8 <= i1; i += 8) {
         float cv[8], dv[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -72,17 +78,108 @@ __device__ __forceinline__ float chain(float acc, const float* c, const float* D
 #pragma unroll
         for (int u = 0; u < 8; ++u) acc = __fmaf_rn(cv[u], dv[u], acc);
     }
-    for (; i < n; ++i) acc = __fmaf_rn(c[i], D[i * kLdD + r], acc);
+    for (; i < i1; ++i) acc = __fmaf_rn(c[i], D[i * kLdD + r], acc);
     return acc;
 }
-// d_j[r] = b_j (x_j[r] - sum_{i<j} c_i d_i[r])
+// The same chain for the four columns r .. r+3 at once (r a multiple of 4):
+// four independent chains, each exactly chain()'s sequence of operations.
+__device__ __forceinline__ float4 chain4(float4 acc, const float* c, const float* D, int r, int i0, int i1) {
+    for (int i = i0; i < i1; ++i) {
+        const float ci = c[i];
+        const float4 d = *reinterpret_cast<const float4*>(D + i * kLdD + r);
+        acc.x = __fmaf_rn(ci, d.x, acc.x);
+        acc.y = __fmaf_rn(ci, d.y, acc.y);
+        acc.z = __fmaf_rn(ci, d.z, acc.z);
+        acc.w = __fmaf_rn(ci, d.w, acc.w);
+    }
+    return acc;
+}
+// T_j[r] = sum_{i<j} c_i d_i[r], as a left fold over the 16-row sub-blocks of
+// per-block chains: ((P_0 + P_1) + P_2) + ..., P_b = chain over i in
+// [16b, min(16b + 16, j)) from 0.  (Prefill computes the completed blocks'
+// P_b in parallel; decode folds them in the same order.)
+__device__ __forceinline__ float delta_sum(const float* c, const float* D, int r, int j) {
+    float T = chain(0.f, c, D, r, 0, min(kSub, j));
+    for (int b = 1; b <= j / kSub; ++b) T = __fadd_rn(T, chain(0.f, c, D, r, b * kSub, min(b * kSub + kSub, j)));
+    return T;
+}
+// d_j[r] = b_j (x_j[r] - T_j[r])
 __device__ __forceinline__ float delta_row(float b, float x, const float* c, const float* D, int r, int j) {
-    return __fmul_rn(b, __fsub_rn(x, chain(0.f, c, D, r, j)));
+    return __fmul_rn(b, __fsub_rn(x, delta_sum(c, D, r, j)));
 }
-// o_j[r] = o0_j[r] + sum_{i<=j} p_i d_i[r]
+// o_j[r] = o0_j[r] + sum_{i<=j} p_i d_i[r]: one chain in increasing i
 __device__ __forceinline__ float out_row(float o0, const float* p, const float* D, int r, int j) {
-    return chain(o0, p, D, r, j + 1);
+    return chain(o0, p, D, r, 0, j + 1);
 }
+
+// NV contractions S_r . x_v at once, each with exactly rows_dot's operations
+// (gdn_step.cuh: per-lane packed chains over the lane's chunks in order, the
+// sets in order, (x + y) + (z + w), the lane butterfly); interleaving only
+// gives the scheduler independent work.  All 32 lanes of the warp call it.
+template <int DK, int R, int NV>
+__device__ __forceinline__ void rows_dot_multi(const RowFrag<DK> (&S)[R], const float* const (&x)[NV], int e,
+                                               float (&u)[NV][R]) {
+    constexpr int NC = RowFrag<DK>::kChunks, NS = RowFrag<DK>::kSets;
+    float2 xy[NV][R][NS], zw[NV][R][NS];
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int j = 0; j < NS; ++j) xy[v][r][j] = zw[v][r][j] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < NC; ++i) {
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const float4 k4 = *reinterpret_cast<const float4*>(x[v] + 4 * chunk_of(i, e));
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+#ifdef GDN_STEP_SCALAR
+                float2& A = xy[v][r][i % NS];
+                float2& B = zw[v][r][i % NS];
+                A.x = __fmaf_rn(S[r].p[2 * i].x, k4.x, A.x);
+                A.y = __fmaf_rn(S[r].p[2 * i].y, k4.y, A.y);
+                B.x = __fmaf_rn(S[r].p[2 * i + 1].x, k4.z, B.x);
+                B.y = __fmaf_rn(S[r].p[2 * i + 1].y, k4.w, B.y);
+#else
+                xy[v][r][i % NS] = __ffma2_rn(S[r].p[2 * i], lo2(k4), xy[v][r][i % NS]);
+                zw[v][r][i % NS] = __ffma2_rn(S[r].p[2 * i + 1], hi2(k4), zw[v][r][i % NS]);
+#endif
+            }
+        }
+    }
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+#pragma unroll
+        for (int r = 0; r < R; ++r) u[v][r] = lanes_reduce(lane_partial<NS>(xy[v][r], zw[v][r]));
+}
+
+// Four outputs (columns r .. r+3) rounded to the output type.
+__device__ __forceinline__ void st4_out(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void st4_out(__nv_bfloat16* p, float4 v) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&a);
+    u.y = *reinterpret_cast<const uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(p) = u;
+}
+// 16 bytes of input widened to fp32 (8 bf16 or 4 fp32)
+__device__ __forceinline__ int widen16(const __nv_bfloat16* p, float* out) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        out[2 * i] = __uint_as_float(w[i] << 16);
+        out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+    return 8;
+}
+__device__ __forceinline__ int widen16(const float* p, float* out) {
+    const float4 f = *reinterpret_cast<const float4*>(p);
+    out[0] = f.x, out[1] = f.y, out[2] = f.z, out[3] = f.w;
+    return 4;
+}
+
 // Chunk end, for the R rows a thread holds: every element is first scaled by
 // Gam_last, then gets fma(w_i, k^_i, .) for i in increasing order with
 // w_i = ew_i * d_i[row] (ew_i = exp(gam_last - gam_i)).  No shuffles.
@@ -146,6 +243,7 @@ struct PrefillSmem {
     float D[kRC][kLdD];
     float cm[kRC][kRC + 1];
     float pm[kRC][kRC + 1];
+    float Tf[kSub][kLdD];  // the completed sub-blocks' folded parts of the current sub-block's rows
     float gam[kRC], Gam[kRC], beta[kRC], graw[kRC], ew[kRC];
 };
 
@@ -210,9 +308,26 @@ __global__ void __launch_bounds__(kThreadsPer128Rows, 1) replay_prefill_kernel(c
             }
             l2norm_warp_multi<DK, 8>(src, dst, nv, lane, p.use_norm != 0);
         }
-        for (int x = tid; x < nj * dv; x += nt) {
-            const int jj = x / dv, r = x % dv;
-            sm.X[j0 + jj][r] = ld_in(v + ((size_t)(t + jj) * p.HV + h) * dv + r);
+        {
+            constexpr int VN = 16 / sizeof(Tin);
+            const int nvec = dv / VN;
+            for (int x0 = tid; x0 < nj * nvec; x0 += 4 * nt) {
+                float buf[4][8];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int x = x0 + u * nt;
+                    if (x < nj * nvec)
+                        widen16(v + ((size_t)(t + x / nvec) * p.HV + h) * dv + (x % nvec) * VN, buf[u]);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int x = x0 + u * nt;
+                    if (x < nj * nvec) {
+#pragma unroll
+                        for (int m = 0; m < VN; ++m) sm.X[j0 + x / nvec][(x % nvec) * VN + m] = buf[u][m];
+                    }
+                }
+            }
         }
         if (tid < nj) {
             const size_t gi = (size_t)(t + tid) * p.HV + h;
@@ -230,39 +345,107 @@ __global__ void __launch_bounds__(kThreadsPer128Rows, 1) replay_prefill_kernel(c
             }
         }
         __syncthreads();
-        // C
-        for (int j = j0; j < j0 + nj; ++j) {
-            float sk[R], sq[R];
-            rows_dot<DK, R>(S, &sm.kn[j][0], e, sk);
-            rows_dot<DK, R>(S, &sm.qn[j][0], e, sq);
+        // C: two rows j at a time (four contractions interleaved)
+        for (int j = j0; j < j0 + nj; j += 2) {
+            const int j2 = min(j + 1, j0 + nj - 1);
+            const float* xs[4] = {&sm.kn[j][0], &sm.qn[j][0], &sm.kn[j2][0], &sm.qn[j2][0]};
+            float u[4][R];
+            rows_dot_multi<DK, R, 4>(S, xs, e, u);
             if (active && e == 0) {
-                const float Gj = sm.Gam[j];
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    sm.X[j][row + r] = resid(sm.X[j][row + r], Gj, sk[r]);
-                    sm.Q0[j][row + r] = out0(Gj, sq[r]);
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int jj = h2 ? j2 : j;
+                    if (h2 && j2 == j) break;
+                    const float Gj = sm.Gam[jj];
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        sm.X[jj][row + r] = resid(sm.X[jj][row + r], Gj, u[2 * h2][r]);
+                        sm.Q0[jj][row + r] = out0(Gj, u[2 * h2 + 1][r]);
+                    }
                 }
             }
         }
-        // D
-        for (int x = tid; x < nj * kRC; x += nt) {
-            const int j = j0 + x / kRC, i = x % kRC;
-            if (i <= j) {
-                const float gj = sm.gam[j], gi = sm.gam[i];
-                if (i < j) sm.cm[j][i] = coef(gj, gi, vdot<DK>(&sm.kn[j][0], &sm.kn[i][0]));
-                sm.pm[j][i] = coef(gj, gi, vdot<DK>(&sm.qn[j][0], &sm.kn[i][0]));
+        // D: coefficient rows, one task per (new row j, group of kTI columns i):
+        // the dots of k^_j and q^_j with k^_i .. k^_{i+kTI-1}, each element with
+        // vdot's chains and final sum
+        for (int x = tid; x < nj * (kRC / kTI); x += nt) {
+            const int j = j0 + x % nj, i0 = kTI * (x / nj);
+            if (i0 > j) continue;
+            float sk[kTI][4], sq[kTI][4];
+#pragma unroll
+            for (int m = 0; m < kTI; ++m)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) sk[m][c] = sq[m][c] = 0.f;
+#pragma unroll 4
+            for (int c = 0; c < DK / 4; ++c) {
+                const float4 a = *reinterpret_cast<const float4*>(&sm.kn[j][4 * c]);
+                const float4 b = *reinterpret_cast<const float4*>(&sm.qn[j][4 * c]);
+#pragma unroll
+                for (int m = 0; m < kTI; ++m) {
+                    const float4 y = *reinterpret_cast<const float4*>(&sm.kn[i0 + m][4 * c]);
+                    sk[m][0] = __fmaf_rn(a.x, y.x, sk[m][0]);
+                    sk[m][1] = __fmaf_rn(a.y, y.y, sk[m][1]);
+                    sk[m][2] = __fmaf_rn(a.z, y.z, sk[m][2]);
+                    sk[m][3] = __fmaf_rn(a.w, y.w, sk[m][3]);
+                    sq[m][0] = __fmaf_rn(b.x, y.x, sq[m][0]);
+                    sq[m][1] = __fmaf_rn(b.y, y.y, sq[m][1]);
+                    sq[m][2] = __fmaf_rn(b.z, y.z, sq[m][2]);
+                    sq[m][3] = __fmaf_rn(b.w, y.w, sq[m][3]);
+                }
+            }
+            const float gj = sm.gam[j];
+#pragma unroll
+            for (int m = 0; m < kTI; ++m) {
+                const int i = i0 + m;
+                if (i <= j) {
+                    const float gi = sm.gam[i];
+                    if (i < j)
+                        sm.cm[j][i] = coef(gj, gi, __fadd_rn(__fadd_rn(sk[m][0], sk[m][1]), __fadd_rn(sk[m][2], sk[m][3])));
+                    sm.pm[j][i] = coef(gj, gi, __fadd_rn(__fadd_rn(sq[m][0], sq[m][1]), __fadd_rn(sq[m][2], sq[m][3])));
+                }
             }
         }
         __syncthreads();
-        // E
-        if (tid < dv)
-            for (int j = j0; j < j0 + nj; ++j)
-                sm.D[j][tid] = delta_row(sm.beta[j], sm.X[j][tid], &sm.cm[j][0], &sm.D[0][0], tid, j);
-        __syncthreads();
-        // F
-        for (int x = tid; x < nj * dv; x += nt) {
-            const int jj = x / dv, r = x % dv, j = j0 + jj;
-            st_in(out + ((size_t)(t + jj) * p.HV + h) * dv + r, out_row(sm.Q0[j][r], &sm.pm[j][0], &sm.D[0][0], r, j));
+        // E: d by sub-blocks of 16 rows.  E1: the completed sub-blocks' parts of
+        // the block's new rows, folded in order (4 columns per thread, all
+        // threads); E2: the in-block chains, one thread per column, rows in order.
+        for (int B = j0 / kSub; B * kSub < j0 + nj; ++B) {
+            const int jb = max(j0, B * kSub), je = min(j0 + nj, B * kSub + kSub);
+            if (B > 0) {
+                const int nq = dv / 4;
+                for (int x = tid; x < (je - jb) * nq; x += nt) {
+                    const int j = jb + x / nq, r = 4 * (x % nq);
+                    float4 T = chain4(make_float4(0.f, 0.f, 0.f, 0.f), &sm.cm[j][0], &sm.D[0][0], r, 0, kSub);
+                    for (int b = 1; b < B; ++b) {
+                        const float4 P =
+                            chain4(make_float4(0.f, 0.f, 0.f, 0.f), &sm.cm[j][0], &sm.D[0][0], r, b * kSub, b * kSub + kSub);
+                        T.x = __fadd_rn(T.x, P.x);
+                        T.y = __fadd_rn(T.y, P.y);
+                        T.z = __fadd_rn(T.z, P.z);
+                        T.w = __fadd_rn(T.w, P.w);
+                    }
+                    *reinterpret_cast<float4*>(&sm.Tf[j - B * kSub][r]) = T;
+                }
+                __syncthreads();
+            }
+            if (tid < dv) {
+                for (int j = jb; j < je; ++j) {
+                    float T = chain(0.f, &sm.cm[j][0], &sm.D[0][0], tid, B * kSub, j);
+                    if (B > 0) T = __fadd_rn(sm.Tf[j - B * kSub][tid], T);
+                    sm.D[j][tid] = __fmul_rn(sm.beta[j], __fsub_rn(sm.X[j][tid], T));
+                }
+            }
+            __syncthreads();
+        }
+        // F: outputs, four columns per thread
+        {
+            const int nq = dv / 4;
+            for (int x = tid; x < nj * nq; x += nt) {
+                const int jj = x / nq, r = 4 * (x % nq), j = j0 + jj;
+                const float4 o = chain4(*reinterpret_cast<const float4*>(&sm.Q0[j][r]), &sm.pm[j][0], &sm.D[0][0], r, 0,
+                                        j + 1);
+                st4_out(out + ((size_t)(t + jj) * p.HV + h) * dv + r, o);
+            }
         }
         t += nj;
         if (j0 + nj == kRC) {
