@@ -699,8 +699,31 @@ def bench_backward(gdn, dev, steps=3):
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
     T = x.q.shape[0]
+    # Dense contraction work of the chunked backward per (chunk, head), C = 64, dk = dv = d:
+    # the multiply-adds (M x N x K) of its 25 tensor-core products, grouped by kernel.
+    C, d = 64, DK
+    macs = (2 * C * C * d + 2 * C * d * C            # wy: K K^T, Q K^T, W, U~
+            + 2 * C * d * d                           # state forward: W S^T, U^T K
+            + C * d * C + 3 * C * d * d               # state backward
+            + 3 * C * d * d                           # intra (state products)
+            + 9 * C * C * d + 2 * C * C * C)          # intra (C x C products)
+    chunk_heads = (BWD_L // C) * BWD_N * HV
+    flops = 2.0 * macs * chunk_heads
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        pass
+    bf16 = float(peaks.get("bf16_tflops_sustained", 1700.0))
+    tf32_peak = bf16 * (1.1 / 2.25)  # TF32 = the recipe's nominal tf32/bf16 ratio of the measured bf16 peak
+    achieved = flops / (ms / 1e3) / 1e12
     return {"tokens_per_s": T / (ms / 1e3), "ms": ms, "workload": f"{BWD_N} x {BWD_L} tokens, HK={HK} HV={HV} "
-            f"dk=dv={DK}, bf16, chunk 64"}
+            f"dk=dv={DK}, bf16, chunk 64",
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf32_peak, "unit": "TFLOP/s",
+                         "frac": achieved / tf32_peak, "flops_per_chunk_head": 2 * macs,
+                         "note": "TF32 mma.sync with fp32 accumulate (bf16 inputs); peak = sustained measured bf16 "
+                                 "x 1.1/2.25 (nominal tf32/bf16); the serial chunk passes, not the products, "
+                                 "bound the time"}}
 
 
 if __name__ == "__main__":
