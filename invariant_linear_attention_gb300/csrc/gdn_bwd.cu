@@ -43,8 +43,14 @@ constexpr int kMaxD = 128;    // max dk, dv
 // smem leading dims = 4 (mod 32): row-major tensor-core fragment loads hit 32 distinct banks
 constexpr int kLdD = kMaxD + 4;  // C x d and d x d matrices
 constexpr int kLdC = kC + 4;     // C x C matrices
-constexpr int kNT = 256;         // threads of the chunk-parallel kernels
-constexpr int kNTs = 512;        // threads of the state-pass kernels (one CTA holds all dv rows)
+#ifndef GDN_BWD_NT
+#define GDN_BWD_NT 1024
+#endif
+constexpr int kNT = GDN_BWD_NT;  // threads of the chunk-parallel kernels (32 warps hide their latency)
+#ifndef GDN_BWD_NTS
+#define GDN_BWD_NTS 1024
+#endif
+constexpr int kNTs = GDN_BWD_NTS;  // threads of the state-pass kernels (one CTA holds all dv rows)
 
 struct BwdParams {
     const void* q;
