@@ -60,6 +60,8 @@ def parse():
                     help="ncu run at full occupancy: 9 sequences x 4096 tokens (288 units), 2 steps, no extras")
     ap.add_argument("--profile-backward", action="store_true",
                     help="ncu run of the backward alone: 2 x 4096 tokens, 2 calls")
+    ap.add_argument("--profile-backward-full", action="store_true",
+                    help="ncu launch list of the backward on its bench workload (8 x 4096 tokens), 2 calls")
     ap.add_argument("--profile-extras", action="store_true",
                     help="ncu run of the layer ops and the chunk-replay variant, one call each: layer ops on 8 "
                          "lognormal sequences (31,823 tokens), replay prefill on 9 x 2048 tokens, replay decode and "
@@ -231,14 +233,14 @@ def run_reference(args):
     }), flush=True)
 
 
-def profile_backward():
-    """Two gdn_chunk_bwd calls on 2 x 4096 tokens (HK=16, HV=32, dk=dv=128, bf16), for ncu."""
+def profile_backward(nseq=2):
+    """Two gdn_chunk_bwd calls on nseq x 4096 tokens (HK=16, HV=32, dk=dv=128, bf16), for ncu."""
     import invariant_linear_attention_gb300 as gdn
     from invariant_linear_attention_gb300 import inputs
     dev = torch.device("cuda", 0)
-    x = inputs.make_inputs([BWD_L] * 2, HK=HK, HV=HV, dk=DK, dv=DV, dtype=torch.bfloat16, seed=6, device=dev)
-    dO = inputs.grad_out(2 * BWD_L, HV, DV, seed=6, device=dev)
-    ws = torch.zeros(gdn.gdn_workspace_size(gdn.make_shape(x.q, x.v, 2), 2), dtype=torch.uint8, device=dev)
+    x = inputs.make_inputs([BWD_L] * nseq, HK=HK, HV=HV, dk=DK, dv=DV, dtype=torch.bfloat16, seed=6, device=dev)
+    dO = inputs.grad_out(nseq * BWD_L, HV, DV, seed=6, device=dev)
+    ws = torch.zeros(gdn.gdn_workspace_size(gdn.make_shape(x.q, x.v, nseq), 2), dtype=torch.uint8, device=dev)
     for _ in range(2):
         gdn.gdn_chunk_bwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, dO, workspace=ws)
     torch.cuda.synchronize()
@@ -250,8 +252,8 @@ def main():
     if args.impl == "reference":
         run_reference(args)
         return
-    if args.profile_backward:
-        profile_backward()
+    if args.profile_backward or args.profile_backward_full:
+        profile_backward(BWD_N if args.profile_backward_full else 2)
         return
     if args.profile_extras:
         profile_extras()
