@@ -212,12 +212,7 @@ __global__ void __launch_bounds__(kThreadsPer128Rows, 2)
 #pragma unroll
                 for (int r = 0; r < R; ++r) vv[r] = 0.f;
                 if (active) ld_rows_in<R>(vs + t * dvs + grp * R, vv);
-#ifdef GDN_KEEP_K
-                float4 kx[RowFrag<DK>::kChunks];
-                rows_dot_part_keep<DK, R>(S, sm.kn + t * DK, e, u, kx);
-#else
                 rows_dot_part<DK, R>(S, sm.kn + t * DK, e, u);
-#endif
                 if (t > 0) {
 #pragma unroll
                     for (int r = 0; r < R; ++r) oprev[r] = lanes_reduce(opend[r]);
@@ -228,11 +223,7 @@ __global__ void __launch_bounds__(kThreadsPer128Rows, 2)
                     st_rows_out<R>(out + ((size_t)(t0 + t - 1) * p.HV + h) * p.dv + row, oprev);
 #pragma unroll
                 for (int r = 0; r < R; ++r) w[r] = delta_w(ab.x, ab.y, vv[r], u[r]);
-#ifdef GDN_KEEP_K
-                rows_update_part_kept<DK, R>(S, kx, sm.qn + t * DK, e, ab.x, w, opend);
-#else
                 rows_update_part<DK, R>(S, sm.kn + t * DK, sm.qn + t * DK, e, ab.x, w, opend);
-#endif
             }
 #pragma unroll
             for (int r = 0; r < R; ++r) opend[r] = lanes_reduce(opend[r]);

@@ -243,40 +243,6 @@ __device__ __forceinline__ void rows_dot_part(const RowFrag<DK> (&s)[R], const f
     for (int r = 0; r < R; ++r) u[r] = lane_partial<NS>(xy[r], zw[r]);
 }
 
-// rows_dot_part that also hands the lane's chunks of x back (kx), for a caller
-// that needs them again in the same token (the update reuses k^): same
-// operations, one shared-memory read of x instead of two.
-template <int DK, int R>
-__device__ __forceinline__ void rows_dot_part_keep(const RowFrag<DK> (&s)[R], const float* __restrict__ x, int e,
-                                                   float (&u)[R], float4 (&kx)[RowFrag<DK>::kChunks]) {
-    constexpr int NC = RowFrag<DK>::kChunks, NS = RowFrag<DK>::kSets;
-    float2 xy[R][NS], zw[R][NS];
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-        for (int j = 0; j < NS; ++j) xy[r][j] = zw[r][j] = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int i = 0; i < NC; ++i) {
-        kx[i] = *reinterpret_cast<const float4*>(x + 4 * chunk_of(i, e));
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            float2& A = xy[r][i % NS];
-            float2& B = zw[r][i % NS];
-#ifdef GDN_STEP_SCALAR
-            A.x = __fmaf_rn(s[r].p[2 * i].x, kx[i].x, A.x);
-            A.y = __fmaf_rn(s[r].p[2 * i].y, kx[i].y, A.y);
-            B.x = __fmaf_rn(s[r].p[2 * i + 1].x, kx[i].z, B.x);
-            B.y = __fmaf_rn(s[r].p[2 * i + 1].y, kx[i].w, B.y);
-#else
-            A = __ffma2_rn(s[r].p[2 * i], lo2(kx[i]), A);
-            B = __ffma2_rn(s[r].p[2 * i + 1], hi2(kx[i]), B);
-#endif
-        }
-    }
-#pragma unroll
-    for (int r = 0; r < R; ++r) u[r] = lane_partial<NS>(xy[r], zw[r]);
-}
-
 template <int DK, int R>
 __device__ __forceinline__ void rows_dot(const RowFrag<DK> (&s)[R], const float* __restrict__ x,
                                          int e, float (&u)[R]) {
@@ -308,53 +274,6 @@ __device__ __forceinline__ void rows_update_part(RowFrag<DK> (&s)[R], const floa
 #pragma unroll
     for (int i = 0; i < NC; ++i) {
         const float4 k4 = *reinterpret_cast<const float4*>(k + 4 * chunk_of(i, e));
-        const float4 q4 = *reinterpret_cast<const float4*>(q + 4 * chunk_of(i, e));
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            float2& Sxy = s[r].p[2 * i];
-            float2& Szw = s[r].p[2 * i + 1];
-            float2& A = xy[r][i % NS];
-            float2& B = zw[r][i % NS];
-#ifdef GDN_STEP_SCALAR
-            Sxy.x = __fmaf_rn(w[r], k4.x, __fmul_rn(a, Sxy.x));
-            Sxy.y = __fmaf_rn(w[r], k4.y, __fmul_rn(a, Sxy.y));
-            Szw.x = __fmaf_rn(w[r], k4.z, __fmul_rn(a, Szw.x));
-            Szw.y = __fmaf_rn(w[r], k4.w, __fmul_rn(a, Szw.y));
-            A.x = __fmaf_rn(Sxy.x, q4.x, A.x);
-            A.y = __fmaf_rn(Sxy.y, q4.y, A.y);
-            B.x = __fmaf_rn(Szw.x, q4.z, B.x);
-            B.y = __fmaf_rn(Szw.y, q4.w, B.y);
-#else
-            const float2 w2 = make_float2(w[r], w[r]);
-            Sxy = __ffma2_rn(w2, lo2(k4), __fmul2_rn(a2, Sxy));
-            Szw = __ffma2_rn(w2, hi2(k4), __fmul2_rn(a2, Szw));
-            A = __ffma2_rn(Sxy, lo2(q4), A);
-            B = __ffma2_rn(Szw, hi2(q4), B);
-#endif
-        }
-    }
-#pragma unroll
-    for (int r = 0; r < R; ++r) o[r] = lane_partial<NS>(xy[r], zw[r]);
-}
-
-// rows_update_part with the lane's k^ chunks already in registers (from
-// rows_dot_part_keep): the same operations in the same order.
-template <int DK, int R>
-__device__ __forceinline__ void rows_update_part_kept(RowFrag<DK> (&s)[R], const float4 (&kx)[RowFrag<DK>::kChunks],
-                                                      const float* __restrict__ q, int e, float a, const float (&w)[R],
-                                                      float (&o)[R]) {
-    constexpr int NC = RowFrag<DK>::kChunks, NS = RowFrag<DK>::kSets;
-    float2 xy[R][NS], zw[R][NS];
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-        for (int j = 0; j < NS; ++j) xy[r][j] = zw[r][j] = make_float2(0.f, 0.f);
-#ifndef GDN_STEP_SCALAR
-    const float2 a2 = make_float2(a, a);
-#endif
-#pragma unroll
-    for (int i = 0; i < NC; ++i) {
-        const float4 k4 = kx[i];
         const float4 q4 = *reinterpret_cast<const float4*>(q + 4 * chunk_of(i, e));
 #pragma unroll
         for (int r = 0; r < R; ++r) {
