@@ -47,6 +47,11 @@ constexpr int kLdC = kC + 4;     // C x C matrices
 #define GDN_BWD_NT 1024
 #endif
 constexpr int kNT = GDN_BWD_NT;  // threads of the chunk-parallel kernels (32 warps hide their latency)
+#ifndef GDN_BWD_NT_WY
+#define GDN_BWD_NT_WY 512
+#endif
+// threads of bwd_wy: its ~103 KB of shared memory fits two CTAs per SM, which 512 threads allow
+constexpr int kNTwy = GDN_BWD_NT_WY;
 #ifndef GDN_BWD_NTS
 #define GDN_BWD_NTS 1024
 #endif
@@ -290,7 +295,7 @@ __global__ void bwd_norm_kernel(BwdParams p) {
 
 // ---------------------------------------------------------------------------
 // per (chunk, head): gam, T = (I + A)^-1, W, U~, QK
-__global__ void __launch_bounds__(kNT) bwd_wy_kernel(BwdParams p) {
+__global__ void __launch_bounds__(kNTwy) bwd_wy_kernel(BwdParams p) {
     extern __shared__ float sm[];
     const int c = blockIdx.x, h = blockIdx.y;
     int n, t0, len;
@@ -300,8 +305,8 @@ __global__ void __launch_bounds__(kNT) bwd_wy_kernel(BwdParams p) {
     float* sQ = sK + kC * kLdD;      // C x kLdD (later V)
     float* sA = sQ + kC * kLdD;      // C x kLdC
     float* sT = sA + kC * kLdC;      // C x kLdC
-    float* sTt = sT + kC * kLdC;     // C x kLdC
-    float* sg = sTt + kC * kLdC;     // gam [C]
+    float* sTt = sA;                 // C x kLdC, reuses A's space: written only after the solve has read A
+    float* sg = sT + kC * kLdC;      // gam [C]
     float* sGb = sg + kC;            // beta * Gam [C]
     float* sb = sGb + kC;            // beta [C]
 
@@ -916,9 +921,9 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
         if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
     }
     const dim3 gch(L.nchm, s->HV);
-    const size_t smem_wy = sizeof(float) * (2 * kC * kLdD + 3 * kC * kLdC + 3 * kC);
+    const size_t smem_wy = sizeof(float) * (2 * kC * kLdD + 2 * kC * kLdC + 3 * kC);
     if (!set_smem(bwd_wy_kernel, smem_wy)) return GDN_ERR_CUDA;
-    bwd_wy_kernel<<<gch, kNT, smem_wy, cs>>>(p);
+    bwd_wy_kernel<<<gch, kNTwy, smem_wy, cs>>>(p);
     if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
 
     const int R = s->dv;  // one CTA per (sequence, head) holds every row of the state
