@@ -475,6 +475,14 @@ __global__ void __launch_bounds__(kThreadsPer128Rows, 1) replay_prefill_kernel(c
 }
 
 // ---------------------------------------------------------------- decode
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
+                 "l"(gmem)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 template <int DK>
 struct DecodeSmem {
     float kn[kRC][DK + 4];
@@ -508,12 +516,17 @@ __global__ void __launch_bounds__(kThreadsPer128Rows, 2) replay_decode_kernel(co
     const Tin* k = static_cast<const Tin*>(p.k);
     const Tin* v = static_cast<const Tin*>(p.v);
 
+    // the open chunk's cached rows: 16-byte asynchronous copies, all in flight at once
     for (int x = tid; x < j * (DK / 4); x += nt) {
         const int i = x / (DK / 4), c = x % (DK / 4);
-        *reinterpret_cast<float4*>(&sm.kn[i][4 * c]) = *reinterpret_cast<const float4*>(gK + (size_t)i * DK + 4 * c);
+        cp_async16(&sm.kn[i][4 * c], gK + (size_t)i * DK + 4 * c);
     }
-    for (int x = tid; x < j * dv; x += nt) sm.D[x / dv][x % dv] = gD[x];
-    for (int i = tid; i < j; i += nt) sm.gam[i] = gG[i];
+    for (int x = tid; x < j * (dv / 4); x += nt) {
+        const int i = x / (dv / 4), c = x % (dv / 4);
+        cp_async16(&sm.D[i][4 * c], gD + (size_t)i * dv + 4 * c);
+    }
+    for (int x = tid; x < (j + 3) / 4; x += nt) cp_async16(&sm.gam[4 * x], gG + 4 * x);
+    cp_async_commit();
     const size_t off = ((size_t)b * p.HK + hk) * DK;
     if (warp == 0) l2norm_warp<DK>(q + off, sm.qn, lane, p.use_norm != 0);
     if (warp == (nwarps > 1 ? 1 : 0)) l2norm_warp<DK>(k + off, &sm.kn[j][0], lane, p.use_norm != 0);
@@ -524,6 +537,7 @@ __global__ void __launch_bounds__(kThreadsPer128Rows, 2) replay_decode_kernel(co
         RowFrag<DK> S[R];
         if (active) load_rows<DK, R>(S, gS + (size_t)row * DK, e);
         else zero_rows<DK, R>(S);
+        cp_async_wait_all();
         __syncthreads();
         rows_dot<DK, R>(S, &sm.kn[j][0], e, sk);
         rows_dot<DK, R>(S, sm.qn, e, sq);
