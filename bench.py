@@ -464,48 +464,90 @@ def check_parity(x, out, fs):
 
 def e2e(gdn, x, dec, dec_state, dev, steps):
     """Same step through the public API from pinned host buffers: H2D of every
-    input, both calls, D2H of both outputs, all inside the timed region."""
+    input, both calls, D2H of both outputs, all inside the timed region.
+
+    Pipelined over two device buffer sets and two copy streams: step i+1's
+    inputs go up (upload stream) and step i-1's outputs come down (download
+    stream) while step i computes.  Events order every reuse of a set: an
+    upload waits for the compute that last read the set, a compute for its
+    upload and for the download of the set's previous outputs."""
     pin = lambda t: t.pin_memory()  # noqa: E731
     hx = {k: pin(getattr(x, k)) for k in ("q", "k", "v", "g", "beta", "cu_seqlens")}
     hd = {k: pin(getattr(dec, k)) for k in ("q", "k", "v", "g", "beta")}
     hs = pin(dec_state)
-    dx = {k: torch.empty_like(t, device=dev) for k, t in hx.items()}
-    ddd = {k: torch.empty_like(t, device=dev) for k, t in hd.items()}
-    dst = torch.empty_like(hs, device=dev)
-    out_h = torch.empty_like(hx["v"]).pin_memory()
-    dout_h = torch.empty_like(hd["v"]).pin_memory()
-    out = torch.empty_like(dx["v"])
-    dout = torch.empty_like(ddd["v"])
-    shape = gdn.make_shape(dx["q"], dx["v"], len(x.lengths))
-    ws = torch.zeros(gdn.gdn_workspace_size(shape, 0), dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
+
+    def dev_set():
+        return dict(x={k: torch.empty_like(t, device=dev) for k, t in hx.items()},
+                    d={k: torch.empty_like(t, device=dev) for k, t in hd.items()},
+                    st=torch.empty_like(hs, device=dev), out=torch.empty_like(hx["v"], device=dev),
+                    dout=torch.empty_like(hd["v"], device=dev),
+                    out_h=torch.empty_like(hx["v"]).pin_memory(), dout_h=torch.empty_like(hd["v"]).pin_memory())
+
+    sets = [dev_set(), dev_set()]
+    shape = gdn.make_shape(sets[0]["x"]["q"], sets[0]["x"]["v"], len(x.lengths))
+    ws = [torch.zeros(gdn.gdn_workspace_size(shape, 0), dtype=torch.uint8, device=dev) for _ in range(2)]
+    comp = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    up_done, comp_done, down_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
     h2d = sum(t.numel() * t.element_size() for t in list(hx.values()) + list(hd.values()) + [hs])
-    d2h = out_h.numel() * out_h.element_size() + dout_h.numel() * dout_h.element_size()
+    d2h = sets[0]["out_h"].numel() * sets[0]["out_h"].element_size() + \
+        sets[0]["dout_h"].numel() * sets[0]["dout_h"].element_size()
 
-    def one():
-        for k in hx:
-            dx[k].copy_(hx[k], non_blocking=True)
-        for k in hd:
-            ddd[k].copy_(hd[k], non_blocking=True)
-        dst.copy_(hs, non_blocking=True)
-        gdn.gdn_recurrent_fwd(dx["q"], dx["k"], dx["v"], dx["g"], dx["beta"], dx["cu_seqlens"], out=out,
-                              workspace=ws, output_final_state=False)
-        gdn.gdn_decode_step(ddd["q"], ddd["k"], ddd["v"], ddd["g"], ddd["beta"], dst, out=dout)
-        out_h.copy_(out, non_blocking=True)
-        dout_h.copy_(dout, non_blocking=True)
+    def upload(i):
+        S = sets[i % 2]
+        with torch.cuda.stream(up):
+            if i >= 2:
+                up.wait_event(comp_done[i % 2])
+            for k in hx:
+                S["x"][k].copy_(hx[k], non_blocking=True)
+            for k in hd:
+                S["d"][k].copy_(hd[k], non_blocking=True)
+            S["st"].copy_(hs, non_blocking=True)
+            up_done[i % 2].record(up)
 
-    one()
+    def compute_and_download(i):
+        S = sets[i % 2]
+        comp.wait_event(up_done[i % 2])
+        if i >= 2:
+            comp.wait_event(down_done[i % 2])
+        X, D = S["x"], S["d"]
+        gdn.gdn_recurrent_fwd(X["q"], X["k"], X["v"], X["g"], X["beta"], X["cu_seqlens"], out=S["out"],
+                              workspace=ws[i % 2], output_final_state=False)
+        gdn.gdn_decode_step(D["q"], D["k"], D["v"], D["g"], D["beta"], S["st"], out=S["dout"])
+        comp_done[i % 2].record(comp)
+        with torch.cuda.stream(down):
+            down.wait_event(comp_done[i % 2])
+            S["out_h"].copy_(S["out"], non_blocking=True)
+            S["dout_h"].copy_(S["dout"], non_blocking=True)
+            down_done[i % 2].record(down)
+
+    def run(n):
+        start = torch.cuda.Event(enable_timing=True)
+        start.record(comp)
+        up.wait_event(start)
+        upload(0)
+        for i in range(n):
+            if i + 1 < n:
+                upload(i + 1)
+            compute_and_download(i)
+        comp.wait_event(down_done[(n - 1) % 2])
+        if n >= 2:
+            comp.wait_event(down_done[(n - 2) % 2])
+        stop = torch.cuda.Event(enable_timing=True)
+        stop.record(comp)
+        return start, stop
+
+    run(2)
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        one()
-    b.record(stream)
+    a, b = run(steps)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
     tokens = x.q.shape[0] + dec.q.shape[0]
     return {"value": tokens / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps}
+            "d2h_bytes_per_step": d2h, "steps": steps,
+            "note": "pinned host buffers; uploads, compute and downloads of consecutive steps overlap on three "
+                    "streams (two device buffer sets)"}
 
 
 def bench_snapshots(gdn, d, dev, ws, every=256, reps=3):
