@@ -254,3 +254,37 @@ def test_conv_full_size_sampled():
     assert min(lengths) >= 3
     last = torch.cat([L.x[int(cu[n + 1]) - 3:int(cu[n + 1])][None] for n in range(len(lengths))])
     assert torch.equal(bits(pool), bits(last))
+
+
+def test_conv_all_sequences_empty():
+    # T_total = 0 with N > 0: every slot keeps its state (initial state on) or is zeroed (off)
+    C, W = 64, 4
+    x = torch.empty(0, C, dtype=torch.bfloat16, device=DEV)
+    w = torch.randn(C, W, device=DEV)
+    pool = torch.randn(3, W - 1, C, device=DEV).to(torch.bfloat16)
+    p0 = pool.clone()
+    cu = torch.zeros(4, dtype=torch.int32, device=DEV)
+    has = torch.tensor([1, 0, 1], dtype=torch.int32, device=DEV)
+    y = gdn.gdn_causal_conv1d_fwd(x, w, cu, conv_state=pool, has_initial_state=has)
+    torch.cuda.synchronize()
+    assert y.shape == (0, C)
+    assert torch.equal(bits(pool[0]), bits(p0[0])) and torch.equal(bits(pool[2]), bits(p0[2]))
+    assert torch.all(pool[1] == 0)
+
+
+def test_norm_and_gates_full_size_sampled():
+    """The bench's shapes (T = 68,535 tokens here, HV = 32, dv = 128, bf16) at sampled rows."""
+    lengths = inputs.lognormal_lengths(16, 4096, 16384, seed=4)
+    L = inputs.make_layer_inputs(lengths, HK=16, HV=32, dk=128, dv=128, seed=70, device=DEV, C=16)
+    y = gdn.gdn_gated_rmsnorm(L.o, L.z, L.norm_w)
+    g, beta = gdn.gdn_gates(L.a, L.b, L.A_log, L.dt_bias)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(1)
+    T = L.o.shape[0]
+    ts = torch.from_numpy(rng.integers(0, T, 512)).to(DEV)
+    want = ref.gated_rmsnorm(L.o[ts], L.z[ts], L.norm_w)
+    got = to_np(y[ts])
+    assert np.all(np.abs(got - want) <= (BF16_ROUND + 4e-5) * np.abs(want) + 1e-30)
+    gr, br = ref.gates(L.a[ts], L.b[ts], L.A_log, L.dt_bias)
+    assert np.all(np.abs(to_np(g[ts]) - gr) <= 4e-6 * np.abs(gr))
+    assert np.all(np.abs(to_np(beta[ts]) - br) <= 4e-6 * np.abs(br))

@@ -101,3 +101,22 @@ def test_snapshot_slots_bounded():
     torch.cuda.synchronize()
     assert not torch.isnan(snaps[:2]).any()
     assert torch.isnan(snaps[2]).all()
+
+
+def test_decode_resumes_from_snapshot_bitwise():
+    """A snapshot taken by the prefill, continued by decode steps, gives the bits
+    of the full prefill (prefix caching followed by generation)."""
+    L, every = 200, 64
+    x = inputs.make_inputs([L], HK=2, HV=4, dk=64, dv=64, dtype=torch.bfloat16, seed=45, init_scale=0.1, device=DEV)
+    out, fs, snaps, snap_cu = gdn.gdn_recurrent_fwd_snapshots(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, every,
+                                                              init_state=x.init_state)
+    P = 2 * every
+    pool = torch.zeros(3, 4, 64, 64, device=DEV)
+    pool[1] = snaps[1]  # the state after 128 tokens
+    idx = torch.tensor([1], dtype=torch.int32, device=DEV)
+    for t in range(P, L):
+        o = gdn.gdn_decode_step(x.q[t:t + 1], x.k[t:t + 1], x.v[t:t + 1], x.g[t:t + 1], x.beta[t:t + 1], pool,
+                                state_indices=idx)
+        assert torch.equal(o.view(torch.int16), out[t:t + 1].view(torch.int16)), t
+    torch.cuda.synchronize()
+    assert torch.equal(pool[1].view(torch.int32), fs[0].view(torch.int32))
