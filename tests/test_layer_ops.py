@@ -2,7 +2,7 @@
 activations, short causal conv with its conv state cache, gated RMSNorm)
 against the fp64 oracle in oracle/layer_ops.py.
 
-Tolerances.  The spec forward bound (normwise 2e-3, bf16 rounding net of
+Tolerances.  The forward bound of the recurrence (normwise 2e-3, bf16 rounding net of
 2^-8 per element) is asserted on every output; on top of it each test checks
 the tighter per-element bound that fp32 arithmetic gives these ops:
   * gates: a few correctly rounded or 2-ulp fp32 operations per element
