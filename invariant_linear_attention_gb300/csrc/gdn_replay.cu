@@ -329,10 +329,10 @@ __global__ void __launch_bounds__(kThreadsPer128Rows, 1) replay_prefill_kernel(c
                 }
             }
         }
-        if (tid < nj) {
-            const size_t gi = (size_t)(t + tid) * p.HV + h;
-            sm.graw[j0 + tid] = p.g[gi];
-            sm.beta[j0 + tid] = p.beta[gi];
+        for (int i = tid; i < nj; i += nt) {  // nt can be 32 (dv = 16)
+            const size_t gi = (size_t)(t + i) * p.HV + h;
+            sm.graw[j0 + i] = p.g[gi];
+            sm.beta[j0 + i] = p.beta[gi];
         }
         __syncthreads();
         // B
@@ -450,7 +450,7 @@ __global__ void __launch_bounds__(kThreadsPer128Rows, 1) replay_prefill_kernel(c
         t += nj;
         if (j0 + nj == kRC) {
             // G
-            if (tid < kRC) sm.ew[tid] = decay(sm.gam[kRC - 1], sm.gam[tid]);
+            for (int i = tid; i < kRC; i += nt) sm.ew[i] = decay(sm.gam[kRC - 1], sm.gam[i]);
             __syncthreads();
             if (active) rows_chunk_update<DK, R>(S, &sm.kn[0][0], DK + 4, &sm.D[0][0], sm.ew, sm.Gam[kRC - 1], row, e);
             j0 = 0;
@@ -576,7 +576,7 @@ __global__ void __launch_bounds__(kThreadsPer128Rows, 2) replay_decode_kernel(co
     if (tid < dv) gD[(size_t)j * dv + tid] = sm.D[j][tid];
     if (tid == 0) gG[j] = gj;
     if (j == kRC - 1) {
-        if (tid < kRC) sm.ew[tid] = decay(gj, sm.gam[tid]);
+        for (int i = tid; i < kRC; i += nt) sm.ew[i] = decay(gj, sm.gam[i]);
         __syncthreads();
         if (active) {
             RowFrag<DK> S[R];

@@ -38,7 +38,8 @@ def pos(vals):
     return torch.tensor(vals, dtype=torch.int32, device=DEV)
 
 
-@pytest.mark.parametrize("dtype,dk", [(torch.float32, 64), (torch.bfloat16, 128), (torch.float32, 32)])
+@pytest.mark.parametrize("dtype,dk", [(torch.float32, 64), (torch.bfloat16, 128), (torch.float32, 32),
+                                      (torch.float32, 16)])
 def test_replay_prefill_vs_oracle(dtype, dk):
     lengths = [1, 63, 64, 65, 130, 200, 0, 7]
     N, HK, HV = len(lengths), 2, 4
@@ -69,12 +70,12 @@ def test_replay_prefill_vs_oracle(dtype, dk):
                 assert np.allclose(to_np(views["gam"][n, h, :r]), st["gam"][:, h], rtol=1e-5, atol=1e-6)
 
 
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-def test_replay_decode_bitwise_equals_prefill(dtype):
+@pytest.mark.parametrize("dtype,dk", [(torch.bfloat16, 64), (torch.float32, 64), (torch.float32, 16)])
+def test_replay_decode_bitwise_equals_prefill(dtype, dk):
     """Prefill of P tokens then decode steps (batched with other sequences, in
     permuted slots) gives the bits of one prefill over the whole sequence."""
     L = 150
-    HK, HV, dk = 2, 4, 64
+    HK, HV = 2, 4
     x = inputs.make_inputs([L], HK=HK, HV=HV, dk=dk, dv=dk, dtype=dtype, seed=82, init_scale=0.2, device=DEV)
     full_rs = gdn.replay_state_new(1, HV, dk, dk, init_state=x.init_state, device=DEV)
     full = gdn.gdn_replay_prefill(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, full_rs)
