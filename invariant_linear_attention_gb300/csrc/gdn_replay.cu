@@ -9,15 +9,17 @@
 // shared memory.
 //
 // Prefill: one CTA per (sequence, head) walks its chunks.  Per chunk:
-//   A  q^, k^ of the new rows (l2norm_warp), g and b;
+//   A  q^, k^ of the new rows (eight vectors per warp at a time), g, b, and v;
 //   B  the cumulative log-decay gam (one thread, in order);
-//   C  S0 k^_j and S0 q^_j (rows_dot) -> x_j = v_j - Gam_j S0 k^_j, o0_j = Gam_j S0 q^_j;
-//   D  the coefficient rows c_j, p_j (one thread per (j, i), fixed-order dots);
-//   E  d_j by forward substitution (one thread per row of d, rows j in order);
-//   F  o_j (one thread per (j, row));
+//   C  S0 k^_j and S0 q^_j (two rows at a time) -> x_j = v_j - Gam_j S0 k^_j,
+//      o0_j = Gam_j S0 q^_j;
+//   D  the coefficient rows c_j, p_j (one task per (row j, four columns i));
+//   E  d_j by forward substitution in 16-row sub-blocks: the completed
+//      sub-blocks' parts by all threads, then the in-block chains, rows in order;
+//   F  o_j (four columns per thread);
 //   G  at the chunk end, S0 <- Gam_last S0 + sum_i exp(gam_last - gam_i) d_i k^_i^T.
 // Decode: one CTA per (sequence, head) does the same for its one new row j,
-// reading S0 and rows 0 .. j-1 from the replay state.
+// reading S0 and rows 0 .. j-1 from the replay state (16-byte async copies).
 #include <algorithm>
 
 #include "../../include/gdn_replay.h"
