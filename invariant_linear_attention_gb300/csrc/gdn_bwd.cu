@@ -174,6 +174,19 @@ __device__ __forceinline__ void bgemm_impl(bool split, int M, int N, int K, cons
 }
 #define bgemm(...) bgemm_impl(p.dtype == GDN_F32, __VA_ARGS__)
 
+// The product added onto values held elsewhere: prior(m, n) reads what f(m, n, x, prior) updates.
+template <typename P, typename F>
+__device__ __forceinline__ void bgemm_rmw_impl(bool split, int M, int N, int K, const float* __restrict__ A, int as0,
+                                               int as1, const float* __restrict__ B, int bs0, int bs1, P&& prior,
+                                               F&& f) {
+#ifdef GDN_BWD_SIMT
+    cta_gemm(M, N, K, A, as0, as1, B, bs0, bs1, [&](int m, int n, float x) { f(m, n, x, prior(m, n)); });
+#else
+    cta_gemm_tc_rmw(split, M, N, K, A, as0, as1, B, bs0, bs1, prior, f);
+#endif
+}
+#define bgemm_rmw(...) bgemm_rmw_impl(p.dtype == GDN_F32, __VA_ARGS__)
+
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
 }
@@ -635,6 +648,14 @@ __global__ void __launch_bounds__(kNT) bwd_intra_s_kernel(BwdParams p) {
     for (int i = threadIdx.x; i < kC; i += blockDim.x) dga[i] = sdg[i];
 }
 
+// Sum over the 16 lanes of a half warp (xor butterfly, fixed order); every lane gets the sum.
+// All 32 lanes of the warp must call it.
+__device__ __forceinline__ float half_sum(float x) {
+#pragma unroll
+    for (int off = 8; off >= 1; off >>= 1) x += __shfl_xor_sync(kFull, x, off);
+    return x;
+}
+
 // per (chunk, head): the C x C part.
 __global__ void __launch_bounds__(kNT) bwd_intra_c_kernel(BwdParams p) {
     extern __shared__ float sm[];
@@ -680,12 +701,17 @@ __global__ void __launch_bounds__(kNT) bwd_intra_c_kernel(BwdParams p) {
     __syncthreads();
     float* dq = p.dqh;
     float* dkk = p.dkh;
-    bgemm(kC, dk, kC, s2, kLdC, 1, sK, kLdD, 1, [&](int r, int j, float x) {
-        if (r < len) dq[((size_t)(t0 + r) * p.HV + h) * dk + j] += x;
+    // The updates of dq and dk below are read-modify-writes of global memory: each output
+    // element's old value comes in through the prior functor, all of a tile's at once.
+    auto at = [&](int r, int j) { return ((size_t)(t0 + r) * p.HV + h) * dk + j; };
+    auto dq_old = [&](int r, int j) { return r < len ? dq[at(r, j)] : 0.f; };
+    auto dk_old = [&](int r, int j) { return r < len ? dkk[at(r, j)] : 0.f; };
+    bgemm_rmw(kC, dk, kC, s2, kLdC, 1, sK, kLdD, 1, dq_old, [&](int r, int j, float x, float o) {
+        if (r < len) dq[at(r, j)] = o + x;
     });
     __syncthreads();
-    bgemm(kC, dk, kC, s2, 1, kLdC, sCb, kLdD, 1, [&](int s, int j, float x) {
-        if (s < len) dkk[((size_t)(t0 + s) * p.HV + h) * dk + j] += x;
+    bgemm_rmw(kC, dk, kC, s2, 1, kLdC, sCb, kLdD, 1, dk_old, [&](int s, int j, float x, float o) {
+        if (s < len) dkk[at(s, j)] = o + x;
     });
     __syncthreads();
     // c2: dW -> sA, V -> sB, dU -> sCb
@@ -698,16 +724,20 @@ __global__ void __launch_bounds__(kNT) bwd_intra_c_kernel(BwdParams p) {
     bgemm(kC, kC, dv, sCb, kLdD, 1, sB, 1, kLdD, [&](int s, int r, float x) { s2[s * kLdC + r] = x; });
     __syncthreads();
     // column dots with T: dbeta_r, dgam_r; then dT(s,r) = beta_r (Gam_r F1 + F2)
-    if (threadIdx.x < kC) {
-        const int r = threadIdx.x;
+    for (int r = threadIdx.x >> 4; r < kC; r += blockDim.x >> 4) {
+        const int l = threadIdx.x & 15;
         float a1 = 0.f, a2 = 0.f;
-        for (int s = 0; s < kC; ++s) {
+        for (int s = l; s < kC; s += 16) {
             a1 = fmaf(sT[s * kLdC + r], s1[s * kLdC + r], a1);
             a2 = fmaf(sT[s * kLdC + r], s2[s * kLdC + r], a2);
         }
-        const float Gr = __expf(sg[r]);
-        sdb[r] += Gr * a1 + a2;
-        sdg[r] += Gr * sbe[r] * a1;
+        a1 = half_sum(a1);
+        a2 = half_sum(a2);
+        if (l == 0) {
+            const float Gr = __expf(sg[r]);
+            sdb[r] += Gr * a1 + a2;
+            sdg[r] += Gr * sbe[r] * a1;
+        }
     }
     __syncthreads();
     for (int i = threadIdx.x; i < kC * kC; i += blockDim.x) {
@@ -716,8 +746,8 @@ __global__ void __launch_bounds__(kNT) bwd_intra_c_kernel(BwdParams p) {
     }
     __syncthreads();
     // dK += diag(beta Gam) T^T dW;  dV = diag(beta) T^T dU
-    bgemm(kC, dk, kC, sT, 1, kLdC, sA, kLdD, 1, [&](int r, int j, float x) {
-        if (r < len) dkk[((size_t)(t0 + r) * p.HV + h) * dk + j] += sbe[r] * __expf(sg[r]) * x;
+    bgemm_rmw(kC, dk, kC, sT, 1, kLdC, sA, kLdD, 1, dk_old, [&](int r, int j, float x, float o) {
+        if (r < len) dkk[at(r, j)] = o + sbe[r] * __expf(sg[r]) * x;
     });
     bgemm(kC, dv, kC, sT, 1, kLdC, sCb, kLdD, 1, [&](int r, int j, float x) {
         if (r < len) st_any(p.dv_out, ((size_t)(t0 + r) * p.HV + h) * dv + j, p.dtype, sbe[r] * x);
@@ -731,16 +761,17 @@ __global__ void __launch_bounds__(kNT) bwd_intra_c_kernel(BwdParams p) {
     // c5: KK = K K^T -> s2; dbeta_r += sum_s dA E KK; dKK = dA beta_r E -> s1; dE += dA beta_r KK
     bgemm(kC, kC, dk, sK, kLdD, 1, sK, 1, kLdD, [&](int r, int s, float x) { s2[r * kLdC + s] = x; });
     __syncthreads();
-    if (threadIdx.x < kC) {
-        const int r = threadIdx.x;
+    for (int r = threadIdx.x >> 4; r < kC; r += blockDim.x >> 4) {
+        const int l = threadIdx.x & 15;
         float acc = 0.f;
-        for (int s = 0; s < r; ++s) {
+        for (int s = l; s < r; s += 16) {
             const float a = s1[r * kLdC + s], e = __expf(sg[r] - sg[s]), kk = s2[r * kLdC + s];
             acc = fmaf(a * e, kk, acc);
             s1[r * kLdC + s] = a * sbe[r] * e;
             sE[r * kLdC + s] = fmaf(a * sbe[r], kk, sE[r * kLdC + s]);
         }
-        sdb[r] += acc;
+        acc = half_sum(acc);
+        if (l == 0) sdb[r] += acc;
     }
     __syncthreads();
     for (int i = threadIdx.x; i < kC * kC; i += blockDim.x) {
@@ -748,18 +779,20 @@ __global__ void __launch_bounds__(kNT) bwd_intra_c_kernel(BwdParams p) {
         s2[r * kLdC + s] = s1[r * kLdC + s] + s1[s * kLdC + r];
     }
     __syncthreads();
-    bgemm(kC, dk, kC, s2, kLdC, 1, sK, kLdD, 1, [&](int r, int j, float x) {
-        if (r < len) dkk[((size_t)(t0 + r) * p.HV + h) * dk + j] += x;
+    bgemm_rmw(kC, dk, kC, s2, kLdC, 1, sK, kLdD, 1, dk_old, [&](int r, int j, float x, float o) {
+        if (r < len) dkk[at(r, j)] = o + x;
     });
     // c6: dgam from E (row sums minus column sums of dE * E), then dg = reverse cumsum
-    if (threadIdx.x < kC) {
-        const int r = threadIdx.x;
+    for (int r = threadIdx.x >> 4; r < kC; r += blockDim.x >> 4) {
+        const int l = threadIdx.x & 15;
         float rs = 0.f, cs = 0.f;
-        for (int s = 0; s < kC; ++s) {
+        for (int s = l; s < kC; s += 16) {
             rs = fmaf(sE[r * kLdC + s], __expf(sg[r] - sg[s]), rs);
             cs = fmaf(sE[s * kLdC + r], __expf(sg[s] - sg[r]), cs);
         }
-        sdg[r] += rs - cs;
+        rs = half_sum(rs);
+        cs = half_sum(cs);
+        if (l == 0) sdg[r] += rs - cs;
     }
     __syncthreads();
     if (threadIdx.x == 0) {

@@ -10,7 +10,8 @@
 // callers can fuse any elementwise epilogue.  With split (a CTA-uniform flag), each operand is
 // split into a TF32 high part and a TF32 remainder and three products
 // (hi*hi + hi*lo + lo*hi) are accumulated, which keeps about fp32 accuracy.
-// Results are deterministic (fixed tile ownership and k order).
+// Results are deterministic (fixed tile ownership and k order).  cta_gemm_tc_rmw is the same
+// product for epilogues that update a value held elsewhere (C += A B into global memory).
 //
 // Fragment layout of m16n8k8 (PTX ISA): with g = lane / 4 and t = lane % 4,
 //   A (16 x 8, row):  a0 = A[g][t], a1 = A[g+8][t], a2 = A[g][t+4], a3 = A[g+8][t+4]
@@ -37,6 +38,45 @@ __device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// One warp's 16 x (8*nb) tile of the product, k in increasing order, into acc[j][0..3]
+// (the C fragment layout above, one 8-column sub-tile per j).
+__device__ __forceinline__ void warp_tile_tc(bool split, int m0, int n0, int nb, int K, const float* __restrict__ A,
+                                             int as0, int as1, const float* __restrict__ B, int bs0, int bs1,
+                                             float (&acc)[4][4]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    const float* a_r0 = A + (size_t)(m0 + g) * as0;
+    const float* a_r1 = A + (size_t)(m0 + g + 8) * as0;
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        const float af[4] = {a_r0[(size_t)(k0 + t) * as1], a_r1[(size_t)(k0 + t) * as1],
+                             a_r0[(size_t)(k0 + t + 4) * as1], a_r1[(size_t)(k0 + t + 4) * as1]};
+        uint32_t ah[4], al[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            ah[i] = tf32_rna(af[i]);
+            if (split) al[i] = tf32_rna(af[i] - __uint_as_float(ah[i]));
+        }
+        const float* b_k0 = B + (size_t)(k0 + t) * bs0;
+        const float* b_k1 = B + (size_t)(k0 + t + 4) * bs0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (j < nb) {
+                const size_t col = (size_t)(n0 + 8 * j + g) * bs1;
+                const float b0f = b_k0[col], b1f = b_k1[col];
+                const uint32_t bh0 = tf32_rna(b0f), bh1 = tf32_rna(b1f);
+                mma_tf32_16x8x8(acc[j], ah, bh0, bh1);
+                if (split) {
+                    const uint32_t bl0 = tf32_rna(b0f - __uint_as_float(bh0));
+                    const uint32_t bl1 = tf32_rna(b1f - __uint_as_float(bh1));
+                    mma_tf32_16x8x8(acc[j], ah, bl0, bl1);
+                    mma_tf32_16x8x8(acc[j], al, bh0, bh1);
+                }
+            }
+        }
+    }
+}
+
 template <typename F>
 __device__ __forceinline__ void cta_gemm_tc(bool split, int M, int N, int K, const float* __restrict__ A, int as0, int as1,
                                             const float* __restrict__ B, int bs0, int bs1, F&& f) {
@@ -48,37 +88,7 @@ __device__ __forceinline__ void cta_gemm_tc(bool split, int M, int N, int K, con
         const int tm = tile / tiles_n, tn = tile - tm * tiles_n;
         const int m0 = tm * 16, n0 = tn * 8 * nb;
         float acc[4][4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-        const float* a_r0 = A + (size_t)(m0 + g) * as0;
-        const float* a_r1 = A + (size_t)(m0 + g + 8) * as0;
-        for (int k0 = 0; k0 < K; k0 += 8) {
-            const float af[4] = {a_r0[(size_t)(k0 + t) * as1], a_r1[(size_t)(k0 + t) * as1],
-                                 a_r0[(size_t)(k0 + t + 4) * as1], a_r1[(size_t)(k0 + t + 4) * as1]};
-            uint32_t ah[4], al[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                ah[i] = tf32_rna(af[i]);
-                if (split) al[i] = tf32_rna(af[i] - __uint_as_float(ah[i]));
-            }
-            const float* b_k0 = B + (size_t)(k0 + t) * bs0;
-            const float* b_k1 = B + (size_t)(k0 + t + 4) * bs0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (j < nb) {
-                    const size_t col = (size_t)(n0 + 8 * j + g) * bs1;
-                    const float b0f = b_k0[col], b1f = b_k1[col];
-                    const uint32_t bh0 = tf32_rna(b0f), bh1 = tf32_rna(b1f);
-                    mma_tf32_16x8x8(acc[j], ah, bh0, bh1);
-                    if (split) {
-                        const uint32_t bl0 = tf32_rna(b0f - __uint_as_float(bh0));
-                        const uint32_t bl1 = tf32_rna(b1f - __uint_as_float(bh1));
-                        mma_tf32_16x8x8(acc[j], ah, bl0, bl1);
-                        mma_tf32_16x8x8(acc[j], al, bh0, bh1);
-                    }
-                }
-            }
-        }
+        warp_tile_tc(split, m0, n0, nb, K, A, as0, as1, B, bs0, bs1, acc);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             if (j < nb) {
@@ -87,6 +97,47 @@ __device__ __forceinline__ void cta_gemm_tc(bool split, int M, int N, int K, con
                 f(m0 + g, n + 1, acc[j][1]);
                 f(m0 + g + 8, n, acc[j][2]);
                 f(m0 + g + 8, n + 1, acc[j][3]);
+            }
+        }
+    }
+}
+
+// The same product with a read-modify-write epilogue: prior(m, n) fetches the value an output
+// element updates, f(m, n, value, prior value) writes it.  Every prior of a warp tile is fetched
+// before any element of it is written, so the fetches (from global memory, say) are in flight
+// together instead of one after another behind each write.  prior and f must touch only the
+// element (m, n) they are given.
+template <typename P, typename F>
+__device__ __forceinline__ void cta_gemm_tc_rmw(bool split, int M, int N, int K, const float* __restrict__ A, int as0,
+                                                int as1, const float* __restrict__ B, int bs0, int bs1, P&& prior,
+                                                F&& f) {
+    const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int nb = N >= 32 ? 4 : N / 8;
+    const int tiles_m = M >> 4, tiles_n = N / (8 * nb);
+    for (int tile = warp; tile < tiles_m * tiles_n; tile += nw) {
+        const int tm = tile / tiles_n, tn = tile - tm * tiles_n;
+        const int m0 = tm * 16, n0 = tn * 8 * nb;
+        float acc[4][4], old[4][4];
+        warp_tile_tc(split, m0, n0, nb, K, A, as0, as1, B, bs0, bs1, acc);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (j < nb) {
+                const int n = n0 + 8 * j + 2 * t;
+                old[j][0] = prior(m0 + g, n);
+                old[j][1] = prior(m0 + g, n + 1);
+                old[j][2] = prior(m0 + g + 8, n);
+                old[j][3] = prior(m0 + g + 8, n + 1);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (j < nb) {
+                const int n = n0 + 8 * j + 2 * t;
+                f(m0 + g, n, acc[j][0], old[j][0]);
+                f(m0 + g, n + 1, acc[j][1], old[j][1]);
+                f(m0 + g + 8, n, acc[j][2], old[j][2]);
+                f(m0 + g + 8, n + 1, acc[j][3], old[j][3]);
             }
         }
     }
