@@ -35,6 +35,7 @@
 #include "gdn_host.h"
 #include "gdn_mma.cuh"
 #include "gdn_step.cuh"
+#include "gdn_umma.cuh"
 
 namespace gdn {
 
@@ -423,7 +424,7 @@ __global__ void __launch_bounds__(kNTwy) bwd_wy_kernel(BwdParams p) {
 __global__ void __launch_bounds__(kNTs) bwd_state_fwd_kernel(BwdParams p, int R) {
     extern __shared__ float sm[];
     const int n = blockIdx.x, h = blockIdx.y, r0 = blockIdx.z * R;
-    const int hk = h / p.G, dk = p.dk, dv = p.dv;
+    const int dk = p.dk, dv = p.dv;
     float* sS = sm;                   // R x kLdD
     float* sW = sS + R * kLdD;        // C x kLdD
     float* sK = sW + kC * kLdD;       // C x kLdD: diag(b) K
@@ -518,6 +519,305 @@ __global__ void __launch_bounds__(kNTs) bwd_state_bwd_kernel(BwdParams p, int R)
     }
     __syncthreads();
     if (p.dinit) store_rows_f32(p.dinit + (((size_t)n * p.HV + h) * dv + r0) * dk, dk, sD, kLdD, R, dk);
+}
+
+// ---------------------------------------------------------------------------
+// The serial state passes on the fifth-generation tensor cores (bf16 inputs, dv = 128, dk in
+// {32, 64, 128}).  One CTA of 512 threads per (sequence, head).  Every product has the M = 128
+// state rows as its rows, so thread (warp w, lane l) owns state row i = 32 (w mod 4) + l in
+// every epilogue, and the column group w / 4 of it: its slice of the fp32 state (or state
+// gradient) stays in registers for the whole sequence.  The tensor core reads TF32-rounded
+// copies of every operand from shared memory in the K-major core-matrix layout of
+// gdn_umma.cuh; accumulators live in TMEM (columns [0, 64) and [128, 128 + dk)).
+constexpr int kNTtc = 512;
+constexpr uint32_t kSboC = kC * 32;  // 8 rows x 64 values x 4 bytes
+
+// Staging of one operand: every thread first loads its items (all loads in flight together),
+// then writes them, rounded to TF32, into the operand's K-major core-matrix layout.
+
+// dst(n, k) = src[n * KK + k] for n < NN, k < KK.  A warp covers 8 rows x 16 values: 64
+// contiguous bytes of each of 8 source rows, one 128-byte core-matrix block per quarter of the
+// warp's 16-byte stores.
+template <int NN, int KK>
+struct RowsTc {
+    static constexpr int kItems = NN * KK / 4 / kNTtc;
+    float4 v[kItems];
+    __device__ __forceinline__ void load(const float* __restrict__ src) {
+#pragma unroll
+        for (int it = 0; it < kItems; ++it) {
+            const int n = row(it), k = col(it);
+            v[it] = *reinterpret_cast<const float4*>(src + (size_t)n * KK + k);
+        }
+    }
+    __device__ __forceinline__ void put(uint8_t* dst) const {
+#pragma unroll
+        for (int it = 0; it < kItems; ++it)
+            *reinterpret_cast<float4*>(dst + umma_koff(row(it), col(it), KK * 32)) = tf32_round4(v[it]);
+    }
+    __device__ __forceinline__ static int row(int it) {
+        const int e = threadIdx.x + it * kNTtc, lane = e & 31, blk = e >> 5;
+        return (blk / (KK / 16)) * 8 + (lane & 7);
+    }
+    __device__ __forceinline__ static int col(int it) {
+        const int e = threadIdx.x + it * kNTtc, lane = e & 31, blk = e >> 5;
+        return ((blk % (KK / 16)) * 4 + (lane >> 3)) * 4;
+    }
+};
+
+// dst(n, k) = src[k * NN + n] (the transpose of a row-major KK x NN block).  Consecutive threads
+// take consecutive n: coalesced loads, conflict-free 16-byte stores.
+template <int NN, int KK>
+struct ColsTc {
+    static constexpr int kItems = NN * KK / 4 / kNTtc;
+    float4 v[kItems];
+    __device__ __forceinline__ void load(const float* __restrict__ src) {
+#pragma unroll
+        for (int it = 0; it < kItems; ++it) {
+            const int e = threadIdx.x + it * kNTtc, n = e % NN, k = (e / NN) * 4;
+            v[it] = make_float4(src[(size_t)k * NN + n], src[(size_t)(k + 1) * NN + n], src[(size_t)(k + 2) * NN + n],
+                                src[(size_t)(k + 3) * NN + n]);
+        }
+    }
+    __device__ __forceinline__ void put(uint8_t* dst) const {
+#pragma unroll
+        for (int it = 0; it < kItems; ++it) {
+            const int e = threadIdx.x + it * kNTtc, n = e % NN, k = (e / NN) * 4;
+            *reinterpret_cast<float4*>(dst + umma_koff(n, k, KK * 32)) = tf32_round4(v[it]);
+        }
+    }
+};
+
+// Issue-side barrier: shared-memory writes of every thread are visible to the tensor core and
+// earlier TMEM reads are ordered before the next MMA.
+__device__ __forceinline__ void tc_sync() {
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+}
+
+// Bounded wait for the MMAs committed to bar; every thread gets the CTA-wide verdict.
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t& phase) {
+    const bool ok = __syncthreads_and(mbar_wait_bounded(bar, phase));
+    phase ^= 1u;
+    tc_fence_after();
+    return ok;
+}
+
+// Store this thread's slice of a row-major 128 x DK fp32 matrix (row i, columns c0 ..) to global.
+template <int NS>
+__device__ __forceinline__ void store_slice(float* dst, const float (&x)[NS]) {
+#pragma unroll
+    for (int m = 0; m < NS; m += 4) *reinterpret_cast<float4*>(dst + m) = make_float4(x[m], x[m + 1], x[m + 2], x[m + 3]);
+}
+// Write this thread's slice (row i, columns c0 .. c0 + NS) as the TF32 operand copy (sbo per 8 rows).
+template <int NS>
+__device__ __forceinline__ void put_slice_tc(uint8_t* dst, int i, int c0, uint32_t sbo, const float (&x)[NS], float sign) {
+#pragma unroll
+    for (int m = 0; m < NS; m += 4)
+        *reinterpret_cast<float4*>(dst + umma_koff(i, c0 + m, sbo)) =
+            make_float4(tf32_round(sign * x[m]), tf32_round(sign * x[m + 1]), tf32_round(sign * x[m + 2]),
+                        tf32_round(sign * x[m + 3]));
+}
+
+// per (sequence, head), chunks in order: S_c out, U = U~ - W S^T, S <- Gam_last S + U^T diag(b) K
+template <int DK>
+__global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p) {
+    constexpr int kDv = 128, kS = DK / 4;
+    constexpr uint32_t kSboD = DK * 32;
+    extern __shared__ __align__(128) uint8_t smb[];
+    uint8_t* sS = smb;                          // A of U^T = S W^T:       128 x DK
+    uint8_t* sW = sS + kDv * DK * 4;            // B of U^T:               64 x DK
+    uint8_t* sUt = sW + kC * DK * 4;            // A of U^T diag(b) K:     128 x 64
+    uint8_t* sBKt = sUt + kDv * kC * 4;         // B (transposed diag(b) K): DK x 64
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sBKt + DK * kC * 4);
+    uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
+    const int n = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+    const int i = (warp & 3) * 32 + (tid & 31), cg = warp >> 2;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    float S[kS];
+    const float* s0 = p.init_state ? p.init_state + (((size_t)n * p.HV + h) * kDv + i) * DK + cg * kS : nullptr;
+#pragma unroll
+    for (int c = 0; c < kS; ++c) S[c] = s0 ? s0[c] : 0.f;
+    put_slice_tc<kS>(sS, i, cg * kS, kSboD, S, 1.f);
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) tmem_alloc(slot, 256);
+    tc_sync();
+    const uint32_t tmem = *slot;
+    uint32_t phase = 0;
+    bool ok = true;
+    const int bos = min(max(p.cu[n], 0), p.T), eos = min(max(p.cu[n + 1], bos), p.T);
+    const int nch = (eos - bos + kC - 1) / kC;
+    for (int j = 0; j < nch && ok; ++j) {
+        const int c = p.coff[n] + j;
+        if (c >= p.nchm) break;
+        const int t0 = bos + j * kC, len = min(kC, eos - t0);
+        const size_t ci = ch_index(p, c, h);
+        store_slice<kS>(p.Sb + (ci * kDv + i) * DK + cg * kS, S);
+        {
+            RowsTc<kC, DK> w;
+            ColsTc<DK, kC> bk;
+            w.load(p.Wb + ci * kC * DK);
+            bk.load(p.BKb + ci * kC * DK);
+            w.put(sW);
+            bk.put(sBKt);
+        }
+        const float Gl = __expf(p.gam[(size_t)(t0 + len - 1) * p.HV + h]);
+        tc_sync();
+        if (tid == 0) {
+            umma_tf32_k(tmem, smem_u32(sS), kSboD, smem_u32(sW), kSboD, umma_idesc_tf32(kDv, kC), DK, false);
+            umma_commit(bar);
+        }
+        if (!(ok = tc_wait(bar, phase))) break;
+        {   // U[r][i] = U~[r][i] - (S W^T)[i][r] for this thread's 16 values of r
+            const float* ut = p.Utb + ci * kC * kDv + i;
+            float u[16], x[16];
+#pragma unroll
+            for (int m = 0; m < 16; ++m) u[m] = ut[(size_t)(cg * 16 + m) * kDv];
+            tmem_ld<2>(tmem + lane_base + cg * 16, x);
+            float* ug = p.Ub + ci * kC * kDv + i;
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                x[m] = u[m] - x[m];
+                ug[(size_t)(cg * 16 + m) * kDv] = x[m];
+            }
+            put_slice_tc<16>(sUt, i, cg * 16, kSboC, x, 1.f);
+        }
+        tc_sync();
+        if (tid == 0) {
+            umma_tf32_k(tmem + 128, smem_u32(sUt), kSboC, smem_u32(sBKt), kSboC, umma_idesc_tf32(kDv, DK), kC, false);
+            umma_commit(bar);
+        }
+        if (!(ok = tc_wait(bar, phase))) break;
+        {   // S <- Gam_last S + (U^T diag(b) K)
+            float x[kS];
+            tmem_ld<kS / 8>(tmem + lane_base + 128 + cg * kS, x);
+#pragma unroll
+            for (int m = 0; m < kS; ++m) S[m] = fmaf(Gl, S[m], x[m]);
+            put_slice_tc<kS>(sS, i, cg * kS, kSboD, S, 1.f);
+        }
+    }
+    if (!ok && tid == 0) atomicOr(p.err, GDN_DEVERR_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// per (sequence, head), chunks in reverse: D_c out (gradient at chunk end), dU, d_init_state.
+//   dU^T = dO^T P + D (diag(b) K)^T,   D <- Gam_last D + dO^T diag(Gam) Q - dU^T W
+template <int DK>
+__global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p) {
+    constexpr int kDv = 128, kS = DK / 4;
+    constexpr uint32_t kSboD = DK * 32;
+    extern __shared__ __align__(128) uint8_t smb[];
+    uint8_t* sD = smb;                          // A: D                    128 x DK
+    uint8_t* sOt = sD + kDv * DK * 4;           // A: dO^T                 128 x 64
+    uint8_t* sPt = sOt + kDv * kC * 4;          // B: P^T                  64 x 64
+    uint8_t* sBK = sPt + kC * kC * 4;           // B: diag(b) K, then W^T  64 x DK / DK x 64
+    uint8_t* sGQt = sBK + kC * DK * 4;          // B: (diag(Gam) Q)^T      DK x 64
+    uint8_t* sdUt = sGQt + DK * kC * 4;         // A: -dU^T                128 x 64
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sdUt + kDv * kC * 4);
+    uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
+    const int n = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+    const int i = (warp & 3) * 32 + (tid & 31), cg = warp >> 2;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    float D[kS];
+    const float* df = p.dfinal ? p.dfinal + (((size_t)n * p.HV + h) * kDv + i) * DK + cg * kS : nullptr;
+#pragma unroll
+    for (int c = 0; c < kS; ++c) D[c] = df ? df[c] : 0.f;
+    put_slice_tc<kS>(sD, i, cg * kS, kSboD, D, 1.f);
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) tmem_alloc(slot, 256);
+    tc_sync();
+    const uint32_t tmem = *slot;
+    uint32_t phase = 0;
+    bool ok = true;
+    const int bos = min(max(p.cu[n], 0), p.T), eos = min(max(p.cu[n + 1], bos), p.T);
+    const int nch = (eos - bos + kC - 1) / kC;
+    for (int j = nch - 1; j >= 0 && ok; --j) {
+        const int c = p.coff[n] + j;
+        if (c >= p.nchm) continue;
+        const int t0 = bos + j * kC, len = min(kC, eos - t0);
+        const size_t ci = ch_index(p, c, h);
+        store_slice<kS>(p.Db + (ci * kDv + i) * DK + cg * kS, D);
+        {
+            // dO^T: (i, r) = dO[t0 + r][h][i], rows r >= len zero
+            constexpr int kItems = kDv * kC / 4 / kNTtc;
+            float4 o[kItems];
+            const size_t st = (size_t)p.HV * kDv;
+#pragma unroll
+            for (int it = 0; it < kItems; ++it) {
+                const int e = tid + it * kNTtc, ii = e % kDv, r = (e / kDv) * 4;
+                const size_t base = ((size_t)(t0 + r) * p.HV + h) * kDv + ii;
+                o[it] = make_float4(r < len ? ld_any(p.dout, base, p.dtype) : 0.f,
+                                    r + 1 < len ? ld_any(p.dout, base + st, p.dtype) : 0.f,
+                                    r + 2 < len ? ld_any(p.dout, base + 2 * st, p.dtype) : 0.f,
+                                    r + 3 < len ? ld_any(p.dout, base + 3 * st, p.dtype) : 0.f);
+            }
+            ColsTc<kC, kC> pt;
+            RowsTc<kC, DK> bk;
+            ColsTc<DK, kC> gq;
+            pt.load(p.Pb + ci * kC * kC);
+            bk.load(p.BKb + ci * kC * DK);
+            gq.load(p.GQb + ci * kC * DK);
+#pragma unroll
+            for (int it = 0; it < kItems; ++it) {
+                const int e = tid + it * kNTtc, ii = e % kDv, r = (e / kDv) * 4;
+                *reinterpret_cast<float4*>(sOt + umma_koff(ii, r, kSboC)) = tf32_round4(o[it]);
+            }
+            pt.put(sPt);
+            bk.put(sBK);
+            gq.put(sGQt);
+        }
+        const float Gl = __expf(p.gam[(size_t)(t0 + len - 1) * p.HV + h]);
+        tc_sync();
+        if (tid == 0) {
+            const uint32_t id = umma_idesc_tf32(kDv, kC);
+            umma_tf32_k(tmem, smem_u32(sOt), kSboC, smem_u32(sPt), kSboC, id, kC, false);
+            umma_tf32_k(tmem, smem_u32(sD), kSboD, smem_u32(sBK), kSboD, id, DK, true);
+            umma_commit(bar);
+        }
+        if (!(ok = tc_wait(bar, phase))) break;
+        {   // dU[s][i] for this thread's 16 values of s; -dU^T as the next product's A
+            float x[16];
+            tmem_ld<2>(tmem + lane_base + cg * 16, x);
+            float* dug = p.dUb + ci * kC * kDv + i;
+#pragma unroll
+            for (int m = 0; m < 16; ++m) dug[(size_t)(cg * 16 + m) * kDv] = x[m];
+            put_slice_tc<16>(sdUt, i, cg * 16, kSboC, x, -1.f);
+        }
+        {
+            ColsTc<DK, kC> w;  // W^T over diag(b) K, which the first product used
+            w.load(p.Wb + ci * kC * DK);
+            w.put(sBK);
+        }
+        tc_sync();
+        if (tid == 0) {
+            const uint32_t id = umma_idesc_tf32(kDv, DK);
+            umma_tf32_k(tmem + 128, smem_u32(sOt), kSboC, smem_u32(sGQt), kSboC, id, kC, false);
+            umma_tf32_k(tmem + 128, smem_u32(sdUt), kSboC, smem_u32(sBK), kSboC, id, kC, true);
+            umma_commit(bar);
+        }
+        if (!(ok = tc_wait(bar, phase))) break;
+        {   // D <- Gam_last D + (dO^T diag(Gam) Q - dU^T W)
+            float x[kS];
+            tmem_ld<kS / 8>(tmem + lane_base + 128 + cg * kS, x);
+#pragma unroll
+            for (int m = 0; m < kS; ++m) D[m] = fmaf(Gl, D[m], x[m]);
+            put_slice_tc<kS>(sD, i, cg * kS, kSboD, D, 1.f);
+        }
+    }
+    if (ok && p.dinit) store_slice<kS>(p.dinit + (((size_t)n * p.HV + h) * kDv + i) * DK + cg * kS, D);
+    if (!ok && tid == 0) atomicOr(p.err, GDN_DEVERR_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
 // ---------------------------------------------------------------------------
@@ -885,6 +1185,22 @@ static bool set_smem(K kern, size_t bytes) {
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) == cudaSuccess;
 }
 
+// The two state passes on tcgen05: one CTA of 512 threads per (sequence, head).
+template <int DK>
+static gdn_status launch_state_tc(const BwdParams& p, int N, int HV, cudaStream_t cs) {
+    const dim3 grid(N, HV);
+    const size_t tail = 64;  // mbarrier + TMEM address slot
+    const size_t smem_f = (size_t)4 * (128 * DK + kC * DK + 128 * kC + DK * kC) + tail;
+    const size_t smem_b = (size_t)4 * (128 * DK + 128 * kC + kC * kC + kC * DK + DK * kC + 128 * kC) + tail;
+    if (!set_smem(bwd_state_fwd_tc_kernel<DK>, smem_f)) return GDN_ERR_CUDA;
+    bwd_state_fwd_tc_kernel<DK><<<grid, kNTtc, smem_f, cs>>>(p);
+    if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
+    if (!set_smem(bwd_state_bwd_tc_kernel<DK>, smem_b)) return GDN_ERR_CUDA;
+    bwd_state_bwd_tc_kernel<DK><<<grid, kNTtc, smem_b, cs>>>(p);
+    if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
+    return GDN_OK;
+}
+
 }  // namespace gdn
 
 extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const void* k, const void* v,
@@ -959,16 +1275,27 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
     bwd_wy_kernel<<<gch, kNTwy, smem_wy, cs>>>(p);
     if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
 
-    const int R = s->dv;  // one CTA per (sequence, head) holds every row of the state
-    const dim3 gseq(s->N, s->HV, s->dv / R);
-    const size_t smem_sf = sizeof(float) * (R * kLdD + 2 * kC * kLdD + 2 * kC * (R + 4));
-    if (!set_smem(bwd_state_fwd_kernel, smem_sf)) return GDN_ERR_CUDA;
-    bwd_state_fwd_kernel<<<gseq, kNTs, smem_sf, cs>>>(p, R);
-    if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
-    const size_t smem_sb = sizeof(float) * (R * kLdD + 2 * kC * kLdD + kC * kLdC + 2 * kC * (R + 4));
-    if (!set_smem(bwd_state_bwd_kernel, smem_sb)) return GDN_ERR_CUDA;
-    bwd_state_bwd_kernel<<<gseq, kNTs, smem_sb, cs>>>(p, R);
-    if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
+    const bool tc_state = s->dtype == GDN_BF16 && s->dv == 128 && (s->dk == 32 || s->dk == 64 || s->dk == 128);
+    if (tc_state) {
+        gdn_status st = GDN_ERR_UNSUPPORTED;
+        switch (s->dk) {
+            case 32: st = launch_state_tc<32>(p, s->N, s->HV, cs); break;
+            case 64: st = launch_state_tc<64>(p, s->N, s->HV, cs); break;
+            case 128: st = launch_state_tc<128>(p, s->N, s->HV, cs); break;
+        }
+        if (st != GDN_OK) return st;
+    } else {
+        const int R = s->dv;  // one CTA per (sequence, head) holds every row of the state
+        const dim3 gseq(s->N, s->HV, s->dv / R);
+        const size_t smem_sf = sizeof(float) * (R * kLdD + 2 * kC * kLdD + 2 * kC * (R + 4));
+        if (!set_smem(bwd_state_fwd_kernel, smem_sf)) return GDN_ERR_CUDA;
+        bwd_state_fwd_kernel<<<gseq, kNTs, smem_sf, cs>>>(p, R);
+        if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
+        const size_t smem_sb = sizeof(float) * (R * kLdD + 2 * kC * kLdD + kC * kLdC + 2 * kC * (R + 4));
+        if (!set_smem(bwd_state_bwd_kernel, smem_sb)) return GDN_ERR_CUDA;
+        bwd_state_bwd_kernel<<<gseq, kNTs, smem_sb, cs>>>(p, R);
+        if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
+    }
 
     const size_t smem_is = sizeof(float) * (kMaxD * kLdD + 4 * kC * kLdD + 2 * kC + 32);
     if (!set_smem(bwd_intra_s_kernel, smem_is)) return GDN_ERR_CUDA;

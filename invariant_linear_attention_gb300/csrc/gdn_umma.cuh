@@ -1,0 +1,115 @@
+// gdn_umma.cuh -- fifth-generation tensor core (tcgen05) building blocks for the
+// chunked backward's serial state passes: TF32 products with operands in shared
+// memory, fp32 accumulators in tensor memory (TMEM), completion on an mbarrier.
+//
+// Operand layout ("K-major, no swizzle"): a matrix X with rows n and reduction
+// index k is stored as 8-row x 16-byte core matrices (8 rows of 4 fp32 each,
+// 128 contiguous bytes).  Core matrices that follow each other along k are 128
+// bytes apart (the descriptor's leading byte offset); groups of 8 rows are
+// `sbo` bytes apart (its stride byte offset).  With every k of a row group
+// stored together, sbo = 8 rows x K x 4 bytes, and element (n, k) sits at
+//     (n / 8) * sbo + (k / 4) * 128 + (n % 8) * 16 + (k % 4) * 4.
+// One MMA instruction of kind::tf32 consumes 8 values of k (two core matrices),
+// so the descriptor of step s starts 256 * s bytes into the operand.
+//
+// Accumulator layout for M = 128 with one CTA: row m of D is TMEM lane m, column
+// n is TMEM column (base + n).  A warp reads only the 32 lanes of its quarter
+// (warp index mod 4).
+//
+// Values enter the tensor core as TF32: the producers round each operand to
+// TF32 (round to nearest, ties away) when they write it, as the mma.sync
+// path does for bf16 inputs.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn_async.cuh"
+
+namespace gdn {
+
+__host__ __device__ constexpr uint32_t umma_koff(int n, int k, uint32_t sbo) {
+    return (uint32_t)(n >> 3) * sbo + (uint32_t)(k >> 2) * 128u + (uint32_t)(n & 7) * 16u + (uint32_t)(k & 3) * 4u;
+}
+
+// Shared-memory matrix descriptor: start address, leading byte offset 128, stride byte offset
+// sbo (all >> 4), descriptor version 1 (bits 46-48 = 0b001), no swizzle.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)(128u >> 4) << 16) | ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) |
+           ((uint64_t)1 << 46);
+}
+
+// Instruction descriptor for kind::tf32: D fp32 (bits 4-5 = 1), A and B TF32 (bits 7-9 and
+// 10-12 = 2), both K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t umma_idesc_tf32(int M, int N) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ float tf32_round(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+__device__ __forceinline__ float4 tf32_round4(float4 v) {
+    return make_float4(tf32_round(v.x), tf32_round(v.y), tf32_round(v.z), tf32_round(v.w));
+}
+
+// TMEM allocation by one whole warp; the address lands in *slot (shared memory).
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// Make this thread's generic-proxy shared-memory writes visible to the tensor core.
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// D (+)= A B^T over one K = 8 step; issued by a single thread.
+__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+
+// D (+)= A B^T for A (M x K) and B (N x K) in the layout above, K a multiple of 8.
+__device__ __forceinline__ void umma_tf32_k(uint32_t d_tmem, uint32_t a_saddr, uint32_t a_sbo, uint32_t b_saddr,
+                                            uint32_t b_sbo, uint32_t idesc, int K, bool accumulate) {
+    for (int s = 0; s < K / 8; ++s)
+        umma_tf32(d_tmem, umma_desc(a_saddr + 256u * s, a_sbo), umma_desc(b_saddr + 256u * s, b_sbo), idesc,
+                  accumulate || s > 0);
+}
+
+// Arrive on bar once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Columns [col, col + 8 * NX) of this warp's 32 lanes, one lane per thread, into v.  Each load
+// and its wait form one asm statement, so no use of the registers can move ahead of the wait.
+template <int NX>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[8 * NX]) {
+#pragma unroll
+    for (int x = 0; x < NX; ++x) {
+        uint32_t r[8];
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t"
+            "tcgen05.wait::ld.sync.aligned;"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+            : "r"(taddr + 8u * x)
+            : "memory");
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[8 * x + j] = __uint_as_float(r[j]);
+    }
+}
+
+}  // namespace gdn
