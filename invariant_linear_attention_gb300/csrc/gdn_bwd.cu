@@ -191,6 +191,9 @@ __device__ __forceinline__ void bgemm_rmw_impl(bool split, int M, int N, int K, 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
 }
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
@@ -554,6 +557,19 @@ struct RowsTc {
         for (int it = 0; it < kItems; ++it)
             *reinterpret_cast<float4*>(dst + umma_koff(row(it), col(it), KK * 32)) = tf32_round4(v[it]);
     }
+    // The same copy by 16-byte cp.async (no registers); round_in_place once this thread's copies landed.
+    __device__ __forceinline__ static void issue_async(uint8_t* dst, const float* __restrict__ src) {
+#pragma unroll
+        for (int it = 0; it < kItems; ++it)
+            cp_async16(dst + umma_koff(row(it), col(it), KK * 32), src + (size_t)row(it) * KK + col(it));
+    }
+    __device__ __forceinline__ static void round_in_place(uint8_t* dst) {
+#pragma unroll
+        for (int it = 0; it < kItems; ++it) {
+            float4* q = reinterpret_cast<float4*>(dst + umma_koff(row(it), col(it), KK * 32));
+            *q = tf32_round4(*q);
+        }
+    }
     __device__ __forceinline__ static int row(int it) {
         const int e = threadIdx.x + it * kNTtc, lane = e & 31, blk = e >> 5;
         return (blk / (KK / 16)) * 8 + (lane & 7);
@@ -583,6 +599,23 @@ struct ColsTc {
         for (int it = 0; it < kItems; ++it) {
             const int e = threadIdx.x + it * kNTtc, n = e % NN, k = (e / NN) * 4;
             *reinterpret_cast<float4*>(dst + umma_koff(n, k, KK * 32)) = tf32_round4(v[it]);
+        }
+    }
+    // The same copy by 4-byte cp.async (no registers); round_in_place once this thread's copies landed.
+    __device__ __forceinline__ static void issue_async(uint8_t* dst, const float* __restrict__ src) {
+#pragma unroll
+        for (int it = 0; it < kItems; ++it) {
+            const int e = threadIdx.x + it * kNTtc, n = e % NN, k = (e / NN) * 4;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) cp_async4(dst + umma_koff(n, k + t, KK * 32), src + (size_t)(k + t) * NN + n);
+        }
+    }
+    __device__ __forceinline__ static void round_in_place(uint8_t* dst) {
+#pragma unroll
+        for (int it = 0; it < kItems; ++it) {
+            const int e = threadIdx.x + it * kNTtc, n = e % NN, k = (e / NN) * 4;
+            float4* q = reinterpret_cast<float4*>(dst + umma_koff(n, k, KK * 32));
+            *q = tf32_round4(*q);
         }
     }
 };
@@ -620,21 +653,46 @@ __device__ __forceinline__ void put_slice_tc(uint8_t* dst, int i, int c0, uint32
                         tf32_round(sign * x[m + 3]));
 }
 
-// per (sequence, head), chunks in order: S_c out, U = U~ - W S^T, S <- Gam_last S + U^T diag(b) K
+// per (sequence, head), chunks in order: S_c out, U = U~ - W S^T, S <- Gam_last S + U^T diag(b) K.
+// Software-pipelined: while chunk j computes, chunk j+1's W and U~ arrive in shared memory by
+// 16-byte cp.async (W into its operand buffer once the first product has read it, U~ into its
+// own buffer once the first epilogue has read it) and its diag(b) K comes into registers.
 template <int DK>
 __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p) {
     constexpr int kDv = 128, kS = DK / 4;
     constexpr uint32_t kSboD = DK * 32;
     extern __shared__ __align__(128) uint8_t smb[];
-    uint8_t* sS = smb;                          // A of U^T = S W^T:       128 x DK
-    uint8_t* sW = sS + kDv * DK * 4;            // B of U^T:               64 x DK
-    uint8_t* sUt = sW + kC * DK * 4;            // A of U^T diag(b) K:     128 x 64
+    uint8_t* sS = smb;                          // A of U^T = S W^T:         128 x DK
+    uint8_t* sW = sS + kDv * DK * 4;            // B of U^T:                 64 x DK
+    uint8_t* sUt = sW + kC * DK * 4;            // A of U^T diag(b) K:       128 x 64
     uint8_t* sBKt = sUt + kDv * kC * 4;         // B (transposed diag(b) K): DK x 64
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sBKt + DK * kC * 4);
+    float* sUtil = reinterpret_cast<float*>(sBKt + DK * kC * 4);  // U~, row-major 64 x 128
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sUtil + kC * kDv);
     uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
     const int n = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
     const int i = (warp & 3) * 32 + (tid & 31), cg = warp >> 2;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    using WRows = RowsTc<kC, DK>;
+    // W of chunk ci into its operand layout (unrounded until the copies land)
+    auto issue_w = [&](size_t ci) {
+        const float* src = p.Wb + ci * kC * DK;
+#pragma unroll
+        for (int it = 0; it < WRows::kItems; ++it) {
+            const int r = WRows::row(it), k = WRows::col(it);
+            cp_async16(sW + umma_koff(r, k, kSboD), src + (size_t)r * DK + k);
+        }
+    };
+    auto round_w = [&]() {
+#pragma unroll
+        for (int it = 0; it < WRows::kItems; ++it) {
+            float4* q = reinterpret_cast<float4*>(sW + umma_koff(WRows::row(it), WRows::col(it), kSboD));
+            *q = tf32_round4(*q);
+        }
+    };
+    auto issue_ut = [&](size_t ci) {
+        const float* src = p.Utb + ci * kC * kDv;
+        for (int e = tid; e < kC * kDv / 4; e += kNTtc) cp_async16(sUtil + 4 * e, src + 4 * e);
+    };
     float S[kS];
     const float* s0 = p.init_state ? p.init_state + (((size_t)n * p.HV + h) * kDv + i) * DK + cg * kS : nullptr;
 #pragma unroll
@@ -645,43 +703,45 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p)
         fence_barrier_init();
     }
     if (warp == 0) tmem_alloc(slot, 256);
+    const int bos = min(max(p.cu[n], 0), p.T), eos = min(max(p.cu[n + 1], bos), p.T);
+    const int nch = (eos - bos + kC - 1) / kC;
+    auto has = [&](int j) { return j < nch && p.coff[n] + j < p.nchm; };
+    ColsTc<DK, kC> bk;  // (diag(b) K)^T of the chunk about to run, in registers
+    if (has(0)) {
+        const size_t ci = ch_index(p, p.coff[n], h);
+        issue_w(ci);
+        issue_ut(ci);
+        bk.load(p.BKb + ci * kC * DK);
+    }
     tc_sync();
     const uint32_t tmem = *slot;
     uint32_t phase = 0;
     bool ok = true;
-    const int bos = min(max(p.cu[n], 0), p.T), eos = min(max(p.cu[n + 1], bos), p.T);
-    const int nch = (eos - bos + kC - 1) / kC;
-    for (int j = 0; j < nch && ok; ++j) {
+    for (int j = 0; has(j) && ok; ++j) {
         const int c = p.coff[n] + j;
-        if (c >= p.nchm) break;
         const int t0 = bos + j * kC, len = min(kC, eos - t0);
-        const size_t ci = ch_index(p, c, h);
+        const size_t ci = ch_index(p, c, h), cn = ch_index(p, c + 1, h);
+        const bool next = has(j + 1);
         store_slice<kS>(p.Sb + (ci * kDv + i) * DK + cg * kS, S);
-        {
-            RowsTc<kC, DK> w;
-            ColsTc<DK, kC> bk;
-            w.load(p.Wb + ci * kC * DK);
-            bk.load(p.BKb + ci * kC * DK);
-            w.put(sW);
-            bk.put(sBKt);
-        }
+        cp_async_wait_all();  // this thread's copies of W and U~ (commits what is still open)
+        round_w();
+        bk.put(sBKt);
         const float Gl = __expf(p.gam[(size_t)(t0 + len - 1) * p.HV + h]);
         tc_sync();
         if (tid == 0) {
             umma_tf32_k(tmem, smem_u32(sS), kSboD, smem_u32(sW), kSboD, umma_idesc_tf32(kDv, kC), DK, false);
             umma_commit(bar);
         }
+        if (next) bk.load(p.BKb + cn * kC * DK);
         if (!(ok = tc_wait(bar, phase))) break;
+        if (next) issue_w(cn);
         {   // U[r][i] = U~[r][i] - (S W^T)[i][r] for this thread's 16 values of r
-            const float* ut = p.Utb + ci * kC * kDv + i;
-            float u[16], x[16];
-#pragma unroll
-            for (int m = 0; m < 16; ++m) u[m] = ut[(size_t)(cg * 16 + m) * kDv];
+            float x[16];
             tmem_ld<2>(tmem + lane_base + cg * 16, x);
             float* ug = p.Ub + ci * kC * kDv + i;
 #pragma unroll
             for (int m = 0; m < 16; ++m) {
-                x[m] = u[m] - x[m];
+                x[m] = sUtil[(cg * 16 + m) * kDv + i] - x[m];
                 ug[(size_t)(cg * 16 + m) * kDv] = x[m];
             }
             put_slice_tc<16>(sUt, i, cg * 16, kSboC, x, 1.f);
@@ -691,6 +751,7 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p)
             umma_tf32_k(tmem + 128, smem_u32(sUt), kSboC, smem_u32(sBKt), kSboC, umma_idesc_tf32(kDv, DK), kC, false);
             umma_commit(bar);
         }
+        if (next) issue_ut(cn);
         if (!(ok = tc_wait(bar, phase))) break;
         {   // S <- Gam_last S + (U^T diag(b) K)
             float x[kS];
@@ -700,6 +761,7 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p)
             put_slice_tc<kS>(sS, i, cg * kS, kSboD, S, 1.f);
         }
     }
+    cp_async_wait_all();
     if (!ok && tid == 0) atomicOr(p.err, GDN_DEVERR_TIMEOUT);
     tc_fence_before();
     __syncthreads();
@@ -708,22 +770,55 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p)
 
 // per (sequence, head), chunks in reverse: D_c out (gradient at chunk end), dU, d_init_state.
 //   dU^T = dO^T P + D (diag(b) K)^T,   D <- Gam_last D + dO^T diag(Gam) Q - dU^T W
+// The first product and dO^T (diag(Gam) Q) go out together, so once they complete the buffers of
+// dO^T, P^T, diag(b) K and (diag(Gam) Q)^T are free: W^T (loaded into registers meanwhile)
+// takes dO^T's place for the last product, and the next chunk's P, diag(b) K and diag(Gam) Q
+// start arriving by cp.async; the next chunk's dO comes into registers during the last product.
 template <int DK>
 __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p) {
     constexpr int kDv = 128, kS = DK / 4;
     constexpr uint32_t kSboD = DK * 32;
     extern __shared__ __align__(128) uint8_t smb[];
-    uint8_t* sD = smb;                          // A: D                    128 x DK
-    uint8_t* sOt = sD + kDv * DK * 4;           // A: dO^T                 128 x 64
-    uint8_t* sPt = sOt + kDv * kC * 4;          // B: P^T                  64 x 64
-    uint8_t* sBK = sPt + kC * kC * 4;           // B: diag(b) K, then W^T  64 x DK / DK x 64
-    uint8_t* sGQt = sBK + kC * DK * 4;          // B: (diag(Gam) Q)^T      DK x 64
-    uint8_t* sdUt = sGQt + DK * kC * 4;         // A: -dU^T                128 x 64
+    uint8_t* sD = smb;                          // A: D                         128 x DK
+    uint8_t* sOt = sD + kDv * DK * 4;           // A: dO^T (128 x 64), then B: W^T (DK x 64)
+    uint8_t* sPt = sOt + kDv * kC * 4;          // B: P^T                       64 x 64
+    uint8_t* sBK = sPt + kC * kC * 4;           // B: diag(b) K                 64 x DK
+    uint8_t* sGQt = sBK + kC * DK * 4;          // B: (diag(Gam) Q)^T           DK x 64
+    uint8_t* sdUt = sGQt + DK * kC * 4;         // A: -dU^T                     128 x 64
     uint64_t* bar = reinterpret_cast<uint64_t*>(sdUt + kDv * kC * 4);
     uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
     const int n = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
     const int i = (warp & 3) * 32 + (tid & 31), cg = warp >> 2;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    using PT = ColsTc<kC, kC>;
+    using BK = RowsTc<kC, DK>;
+    using GT = ColsTc<DK, kC>;
+    constexpr int kOItems = kDv * kC / 4 / kNTtc;
+    float4 o[kOItems];  // dO^T of the chunk about to run: (i, r) = dO[t0 + r][h][i], rows r >= len zero
+    auto load_dO = [&](int t0, int len) {
+        const size_t st = (size_t)p.HV * kDv;
+#pragma unroll
+        for (int it = 0; it < kOItems; ++it) {
+            const int e = tid + it * kNTtc, ii = e % kDv, r = (e / kDv) * 4;
+            const size_t base = ((size_t)(t0 + r) * p.HV + h) * kDv + ii;
+            o[it] = make_float4(r < len ? ld_any(p.dout, base, p.dtype) : 0.f,
+                                r + 1 < len ? ld_any(p.dout, base + st, p.dtype) : 0.f,
+                                r + 2 < len ? ld_any(p.dout, base + 2 * st, p.dtype) : 0.f,
+                                r + 3 < len ? ld_any(p.dout, base + 3 * st, p.dtype) : 0.f);
+        }
+    };
+    auto put_dO = [&]() {
+#pragma unroll
+        for (int it = 0; it < kOItems; ++it) {
+            const int e = tid + it * kNTtc, ii = e % kDv, r = (e / kDv) * 4;
+            *reinterpret_cast<float4*>(sOt + umma_koff(ii, r, kSboC)) = tf32_round4(o[it]);
+        }
+    };
+    auto issue_chunk = [&](size_t ci) {
+        PT::issue_async(sPt, p.Pb + ci * kC * kC);
+        BK::issue_async(sBK, p.BKb + ci * kC * DK);
+        GT::issue_async(sGQt, p.GQb + ci * kC * DK);
+    };
     float D[kS];
     const float* df = p.dfinal ? p.dfinal + (((size_t)n * p.HV + h) * kDv + i) * DK + cg * kS : nullptr;
 #pragma unroll
@@ -734,57 +829,45 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p)
         fence_barrier_init();
     }
     if (warp == 0) tmem_alloc(slot, 256);
+    const int bos = min(max(p.cu[n], 0), p.T), eos = min(max(p.cu[n + 1], bos), p.T);
+    const int nch = (eos - bos + kC - 1) / kC;
+    const int jtop = min(nch, p.nchm - p.coff[n]) - 1;  // last chunk inside the workspace
+    if (jtop >= 0) {
+        const int t0 = bos + jtop * kC;
+        issue_chunk(ch_index(p, p.coff[n] + jtop, h));
+        load_dO(t0, min(kC, eos - t0));
+        put_dO();
+    }
     tc_sync();
     const uint32_t tmem = *slot;
     uint32_t phase = 0;
     bool ok = true;
-    const int bos = min(max(p.cu[n], 0), p.T), eos = min(max(p.cu[n + 1], bos), p.T);
-    const int nch = (eos - bos + kC - 1) / kC;
-    for (int j = nch - 1; j >= 0 && ok; --j) {
+    for (int j = jtop; j >= 0 && ok; --j) {
         const int c = p.coff[n] + j;
-        if (c >= p.nchm) continue;
         const int t0 = bos + j * kC, len = min(kC, eos - t0);
         const size_t ci = ch_index(p, c, h);
+        const bool prev = j > 0;
+        const int tp = t0 - kC;  // the chunk before this one is always full
         store_slice<kS>(p.Db + (ci * kDv + i) * DK + cg * kS, D);
-        {
-            // dO^T: (i, r) = dO[t0 + r][h][i], rows r >= len zero
-            constexpr int kItems = kDv * kC / 4 / kNTtc;
-            float4 o[kItems];
-            const size_t st = (size_t)p.HV * kDv;
-#pragma unroll
-            for (int it = 0; it < kItems; ++it) {
-                const int e = tid + it * kNTtc, ii = e % kDv, r = (e / kDv) * 4;
-                const size_t base = ((size_t)(t0 + r) * p.HV + h) * kDv + ii;
-                o[it] = make_float4(r < len ? ld_any(p.dout, base, p.dtype) : 0.f,
-                                    r + 1 < len ? ld_any(p.dout, base + st, p.dtype) : 0.f,
-                                    r + 2 < len ? ld_any(p.dout, base + 2 * st, p.dtype) : 0.f,
-                                    r + 3 < len ? ld_any(p.dout, base + 3 * st, p.dtype) : 0.f);
-            }
-            ColsTc<kC, kC> pt;
-            RowsTc<kC, DK> bk;
-            ColsTc<DK, kC> gq;
-            pt.load(p.Pb + ci * kC * kC);
-            bk.load(p.BKb + ci * kC * DK);
-            gq.load(p.GQb + ci * kC * DK);
-#pragma unroll
-            for (int it = 0; it < kItems; ++it) {
-                const int e = tid + it * kNTtc, ii = e % kDv, r = (e / kDv) * 4;
-                *reinterpret_cast<float4*>(sOt + umma_koff(ii, r, kSboC)) = tf32_round4(o[it]);
-            }
-            pt.put(sPt);
-            bk.put(sBK);
-            gq.put(sGQt);
-        }
+        cp_async_wait_all();  // this thread's copies of P, diag(b) K, diag(Gam) Q
+        PT::round_in_place(sPt);
+        BK::round_in_place(sBK);
+        GT::round_in_place(sGQt);
         const float Gl = __expf(p.gam[(size_t)(t0 + len - 1) * p.HV + h]);
         tc_sync();
         if (tid == 0) {
-            const uint32_t id = umma_idesc_tf32(kDv, kC);
-            umma_tf32_k(tmem, smem_u32(sOt), kSboC, smem_u32(sPt), kSboC, id, kC, false);
-            umma_tf32_k(tmem, smem_u32(sD), kSboD, smem_u32(sBK), kSboD, id, DK, true);
+            const uint32_t i1 = umma_idesc_tf32(kDv, kC), i2 = umma_idesc_tf32(kDv, DK);
+            umma_tf32_k(tmem, smem_u32(sOt), kSboC, smem_u32(sPt), kSboC, i1, kC, false);
+            umma_tf32_k(tmem, smem_u32(sD), kSboD, smem_u32(sBK), kSboD, i1, DK, true);
+            umma_tf32_k(tmem + 128, smem_u32(sOt), kSboC, smem_u32(sGQt), kSboC, i2, kC, false);
             umma_commit(bar);
         }
+        GT w;
+        w.load(p.Wb + ci * kC * DK);
         if (!(ok = tc_wait(bar, phase))) break;
-        {   // dU[s][i] for this thread's 16 values of s; -dU^T as the next product's A
+        w.put(sOt);  // W^T where dO^T was
+        if (prev) issue_chunk(ci - p.HV);
+        {   // dU[s][i] for this thread's 16 values of s; -dU^T as the last product's A
             float x[16];
             tmem_ld<2>(tmem + lane_base + cg * 16, x);
             float* dug = p.dUb + ci * kC * kDv + i;
@@ -792,18 +875,12 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p)
             for (int m = 0; m < 16; ++m) dug[(size_t)(cg * 16 + m) * kDv] = x[m];
             put_slice_tc<16>(sdUt, i, cg * 16, kSboC, x, -1.f);
         }
-        {
-            ColsTc<DK, kC> w;  // W^T over diag(b) K, which the first product used
-            w.load(p.Wb + ci * kC * DK);
-            w.put(sBK);
-        }
         tc_sync();
         if (tid == 0) {
-            const uint32_t id = umma_idesc_tf32(kDv, DK);
-            umma_tf32_k(tmem + 128, smem_u32(sOt), kSboC, smem_u32(sGQt), kSboC, id, kC, false);
-            umma_tf32_k(tmem + 128, smem_u32(sdUt), kSboC, smem_u32(sBK), kSboC, id, kC, true);
+            umma_tf32_k(tmem + 128, smem_u32(sdUt), kSboC, smem_u32(sOt), kSboC, umma_idesc_tf32(kDv, DK), kC, true);
             umma_commit(bar);
         }
+        if (prev) load_dO(tp, kC);
         if (!(ok = tc_wait(bar, phase))) break;
         {   // D <- Gam_last D + (dO^T diag(Gam) Q - dU^T W)
             float x[kS];
@@ -812,7 +889,9 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p)
             for (int m = 0; m < kS; ++m) D[m] = fmaf(Gl, D[m], x[m]);
             put_slice_tc<kS>(sD, i, cg * kS, kSboD, D, 1.f);
         }
+        if (prev) put_dO();  // the last product has read W^T
     }
+    cp_async_wait_all();
     if (ok && p.dinit) store_slice<kS>(p.dinit + (((size_t)n * p.HV + h) * kDv + i) * DK + cg * kS, D);
     if (!ok && tid == 0) atomicOr(p.err, GDN_DEVERR_TIMEOUT);
     tc_fence_before();
@@ -1190,7 +1269,7 @@ template <int DK>
 static gdn_status launch_state_tc(const BwdParams& p, int N, int HV, cudaStream_t cs) {
     const dim3 grid(N, HV);
     const size_t tail = 64;  // mbarrier + TMEM address slot
-    const size_t smem_f = (size_t)4 * (128 * DK + kC * DK + 128 * kC + DK * kC) + tail;
+    const size_t smem_f = (size_t)4 * (128 * DK + kC * DK + 128 * kC + DK * kC + kC * 128) + tail;
     const size_t smem_b = (size_t)4 * (128 * DK + 128 * kC + kC * kC + kC * DK + DK * kC + 128 * kC) + tail;
     if (!set_smem(bwd_state_fwd_tc_kernel<DK>, smem_f)) return GDN_ERR_CUDA;
     bwd_state_fwd_tc_kernel<DK><<<grid, kNTtc, smem_f, cs>>>(p);
