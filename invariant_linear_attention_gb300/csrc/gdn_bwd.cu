@@ -533,6 +533,10 @@ __global__ void __launch_bounds__(kNTs) bwd_state_bwd_kernel(BwdParams p, int R)
 // copies of every operand from shared memory in the K-major core-matrix layout of
 // gdn_umma.cuh; accumulators live in TMEM (columns [0, 64) and [128, 128 + dk)).
 constexpr int kNTtc = 512;
+// At dk = 128 the chunk states S_c and D_c go out transposed (dk x dv), the layout in which
+// bwd_intra_s_tc_kernel takes them as K-major operands; other dk keep the row-major layout.
+template <int DK>
+constexpr bool kStateTransposed = DK == 128;
 constexpr uint32_t kSboC = kC * 32;  // 8 rows x 64 values x 4 bytes
 
 // Staging of one operand: every thread first loads its items (all loads in flight together),
@@ -643,6 +647,17 @@ __device__ __forceinline__ void store_slice(float* dst, const float (&x)[NS]) {
 #pragma unroll
     for (int m = 0; m < NS; m += 4) *reinterpret_cast<float4*>(dst + m) = make_float4(x[m], x[m + 1], x[m + 2], x[m + 3]);
 }
+// Store this thread's slice (row i, columns c0 .. c0 + NS) of a 128 x DK matrix to global: row-major
+// (dst points at element (i, c0)), or transposed, DK x 128 (dst points at element (c0, i)).
+template <int NS, bool kTransposed>
+__device__ __forceinline__ void store_state_slice(float* dst, const float (&x)[NS]) {
+    if constexpr (kTransposed) {
+#pragma unroll
+        for (int m = 0; m < NS; ++m) dst[(size_t)m * 128] = x[m];
+    } else {
+        store_slice<NS>(dst, x);
+    }
+}
 // Write this thread's slice (row i, columns c0 .. c0 + NS) as the TF32 operand copy (sbo per 8 rows).
 template <int NS>
 __device__ __forceinline__ void put_slice_tc(uint8_t* dst, int i, int c0, uint32_t sbo, const float (&x)[NS], float sign) {
@@ -661,6 +676,7 @@ template <int DK>
 __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p) {
     constexpr int kDv = 128, kS = DK / 4;
     constexpr uint32_t kSboD = DK * 32;
+    constexpr bool kStateT = kStateTransposed<DK>;
     extern __shared__ __align__(128) uint8_t smb[];
     uint8_t* sS = smb;                          // A of U^T = S W^T:         128 x DK
     uint8_t* sW = sS + kDv * DK * 4;            // B of U^T:                 64 x DK
@@ -722,7 +738,8 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p)
         const int t0 = bos + j * kC, len = min(kC, eos - t0);
         const size_t ci = ch_index(p, c, h), cn = ch_index(p, c + 1, h);
         const bool next = has(j + 1);
-        store_slice<kS>(p.Sb + (ci * kDv + i) * DK + cg * kS, S);
+        if constexpr (kStateT) store_state_slice<kS, true>(p.Sb + (ci * DK + cg * kS) * kDv + i, S);
+        else store_state_slice<kS, false>(p.Sb + (ci * kDv + i) * DK + cg * kS, S);
         cp_async_wait_all();  // this thread's copies of W and U~ (commits what is still open)
         round_w();
         bk.put(sBKt);
@@ -778,6 +795,7 @@ template <int DK>
 __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p) {
     constexpr int kDv = 128, kS = DK / 4;
     constexpr uint32_t kSboD = DK * 32;
+    constexpr bool kStateT = kStateTransposed<DK>;
     extern __shared__ __align__(128) uint8_t smb[];
     uint8_t* sD = smb;                          // A: D                         128 x DK
     uint8_t* sOt = sD + kDv * DK * 4;           // A: dO^T (128 x 64), then B: W^T (DK x 64)
@@ -848,7 +866,8 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p)
         const size_t ci = ch_index(p, c, h);
         const bool prev = j > 0;
         const int tp = t0 - kC;  // the chunk before this one is always full
-        store_slice<kS>(p.Db + (ci * kDv + i) * DK + cg * kS, D);
+        if constexpr (kStateT) store_state_slice<kS, true>(p.Db + (ci * DK + cg * kS) * kDv + i, D);
+        else store_state_slice<kS, false>(p.Db + (ci * kDv + i) * DK + cg * kS, D);
         cp_async_wait_all();  // this thread's copies of P, diag(b) K, diag(Gam) Q
         PT::round_in_place(sPt);
         BK::round_in_place(sBK);
@@ -1025,6 +1044,188 @@ __global__ void __launch_bounds__(kNT) bwd_intra_s_kernel(BwdParams p) {
     __syncthreads();
     float* dga = p.dgamA + ci * kC;
     for (int i = threadIdx.x; i < kC; i += blockDim.x) dga[i] = sdg[i];
+}
+
+// Sums over the 32 lanes of a warp of each of NV values (NV = 32 or 16), by a transpose-reduce
+// butterfly in a fixed order; afterwards lane l holds the sum for value l % NV.
+template <int NV>
+__device__ __forceinline__ float warp_transpose_sum(float (&v)[NV]) {
+    const int lane = threadIdx.x & 31;
+    if constexpr (NV == 16) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] += __shfl_xor_sync(kFull, v[k], 16);
+    }
+#pragma unroll
+    for (int half = NV / 2; half >= 1; half >>= 1) {
+        const bool upper = (lane & half) != 0;
+#pragma unroll
+        for (int k = 0; k < half; ++k) {
+            const float send = upper ? v[k] : v[k + half];
+            const float keep = upper ? v[k + half] : v[k];
+            v[k] = keep + __shfl_xor_sync(kFull, send, half);
+        }
+    }
+    return v[0];
+}
+
+// per (chunk, head), dk = dv = 128, bf16 inputs: the products with S0 and D on tcgen05, in
+// transposed form (rows = the dk index j, 128 of them):
+//   X = S0^T [dO; dU]^T:  dQ_S[r][j] = Gam_r X[j][r] -> dqh,  dW[r][j] = -X[j][64 + r] -> Wb
+//   Y = D^T U^T:          dkh[r][j] = b_r Y[j][r],  b_r = exp(gam_last - gam_r)
+// and dgam_r = q^_r . dQ_S,r - b_r k^_r . Y_r  (+ sum_r b_r k^_r . Y_r + Gam_last <D, S0> on the
+// last row).  S0^T and D^T come from the tcgen05 state passes, which write them transposed.
+// The thread owning row j of an accumulator stores column j of each output row: coalesced.
+constexpr size_t kIntraSTcSmem = (size_t)4 * (2 * 128 * 128 + 2 * 4 * kC + 3 * kC + 16) + 16;
+
+__global__ void __launch_bounds__(kNTtc, 1) bwd_intra_s_tc_kernel(BwdParams p) {
+    constexpr int kD = 128;
+    constexpr uint32_t kSbo = kD * 32;
+    extern __shared__ __align__(128) uint8_t smb[];
+    uint8_t* sA = smb;                                          // A: S0^T, then D^T     128 x 128
+    uint8_t* sB = sA + kD * kD * 4;                             // B: [dO; dU], then U   128 x 128
+    float* red = reinterpret_cast<float*>(sB + kD * kD * 4);    // [2][4 quarters][64] partial sums
+    float* sg = red + 2 * 4 * kC;                               // gam
+    float* sdg = sg + kC;                                       // dgam
+    float* sbd = sdg + kC;                                      // b_r db_r
+    float* scr = sbd + kC;                                      // cta_sum scratch (16 warps)
+    uint64_t* bar = reinterpret_cast<uint64_t*>(scr + 16);
+    uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
+    const int c = blockIdx.x, h = blockIdx.y;
+    int n, t0, len;
+    if (!chunk_of(p, c, n, t0, len)) return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, q = warp & 3, cg = warp >> 2;
+    const int j = q * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    const int hk = h / p.G;
+    const size_t ci = ch_index(p, c, h);
+    using M128 = RowsTc<kD, kD>;
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) tmem_alloc(slot, 256);
+    M128 s0;  // S0^T in fp32, kept for <D, S0>
+    s0.load(p.Sb + ci * kD * kD);
+    {
+        float4 b[M128::kItems];  // B rows 0..63: dO[t0 + r][h] (zero for r >= len); rows 64..127: dU[r]
+#pragma unroll
+        for (int it = 0; it < M128::kItems; ++it) {
+            const int r = M128::row(it), k = M128::col(it);
+            if (r < kC) b[it] = r < len ? ld4_any(p.dout, ((size_t)(t0 + r) * p.HV + h) * kD + k, p.dtype)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+            else b[it] = *reinterpret_cast<const float4*>(p.dUb + (ci * kC + (r - kC)) * kD + k);
+        }
+        s0.put(sA);
+#pragma unroll
+        for (int it = 0; it < M128::kItems; ++it)
+            *reinterpret_cast<float4*>(sB + umma_koff(M128::row(it), M128::col(it), kSbo)) = tf32_round4(b[it]);
+    }
+    for (int r = tid; r < kC; r += blockDim.x) sg[r] = r < len ? p.gam[(size_t)(t0 + r) * p.HV + h] : 0.f;
+    tc_sync();
+    const uint32_t tmem = *slot;
+    uint32_t phase = 0;
+    float dot = 0.f;
+    bool ok;
+    do {
+        if (tid == 0) {
+            umma_tf32_k(tmem, smem_u32(sA), kSbo, smem_u32(sB), kSbo, umma_idesc_tf32(kD, kD), kD, false);
+            umma_commit(bar);
+        }
+        if (!(ok = tc_wait(bar, phase))) break;
+        {
+            float x[32];
+            tmem_ld<4>(tmem + lane_base + cg * 32, x);
+            if (cg < 2) {  // dQ_S rows r = 32 cg + m, and q^_r . dQ_S,r
+                float qv[32];
+#pragma unroll
+                for (int m = 0; m < 32; ++m) {
+                    const int r = cg * 32 + m;
+                    qv[m] = r < len ? p.qn[((size_t)(t0 + r) * p.HK + hk) * kD + j] : 0.f;
+                }
+#pragma unroll
+                for (int m = 0; m < 32; ++m) {
+                    const int r = cg * 32 + m;
+                    const float d = r < len ? __expf(sg[r]) * x[m] : 0.f;
+                    if (r < len) p.dqh[((size_t)(t0 + r) * p.HV + h) * kD + j] = d;
+                    x[m] = qv[m] * d;
+                }
+                const float part = warp_transpose_sum<32>(x);
+                red[q * kC + cg * 32 + lane] = part;
+            } else {  // dW rows r = 32 (cg - 2) + m
+                float* dW = p.Wb + ci * kC * kD + j;
+#pragma unroll
+                for (int m = 0; m < 32; ++m) dW[(size_t)((cg - 2) * 32 + m) * kD] = -x[m];
+            }
+        }
+        tc_fence_before();
+        __syncthreads();  // the first product and every read of its result are done
+        {
+            M128 dt;
+            RowsTc<kC, kD> u;
+            dt.load(p.Db + ci * kD * kD);
+            u.load(p.Ub + ci * kC * kD);
+#pragma unroll
+            for (int it = 0; it < M128::kItems; ++it) {
+                dot = fmaf(dt.v[it].x, s0.v[it].x, dot);
+                dot = fmaf(dt.v[it].y, s0.v[it].y, dot);
+                dot = fmaf(dt.v[it].z, s0.v[it].z, dot);
+                dot = fmaf(dt.v[it].w, s0.v[it].w, dot);
+            }
+            dt.put(sA);
+            u.put(sB);
+        }
+        tc_sync();
+        if (tid == 0) {
+            umma_tf32_k(tmem + 128, smem_u32(sA), kSbo, smem_u32(sB), kSbo, umma_idesc_tf32(kD, kC), kD, false);
+            umma_commit(bar);
+        }
+        if (!(ok = tc_wait(bar, phase))) break;
+        {  // dkh rows r = 16 cg + m, and k^_r . (U D)_r
+            const float gl = sg[len - 1];
+            float x[16], kv[16];
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                const int r = cg * 16 + m;
+                kv[m] = r < len ? p.kn[((size_t)(t0 + r) * p.HK + hk) * kD + j] : 0.f;
+            }
+            tmem_ld<2>(tmem + lane_base + 128 + cg * 16, x);
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                const int r = cg * 16 + m;
+                if (r < len) p.dkh[((size_t)(t0 + r) * p.HV + h) * kD + j] = __expf(gl - sg[r]) * x[m];
+                x[m] = kv[m] * x[m];
+            }
+            const float part = warp_transpose_sum<16>(x);
+            if (lane < 16) red[4 * kC + q * kC + cg * 16 + lane] = part;
+        }
+    } while (false);
+    const float dS = cta_sum(dot, scr);  // all threads, whatever ok says
+    if (ok) {
+        const float gl = sg[len - 1];
+        for (int r = tid; r < kC; r += blockDim.x) {
+            float dg = 0.f, bd = 0.f;
+            if (r < len) {
+                dg = ((red[r] + red[kC + r]) + red[2 * kC + r]) + red[3 * kC + r];
+                bd = __expf(gl - sg[r]) *
+                     (((red[4 * kC + r] + red[5 * kC + r]) + red[6 * kC + r]) + red[7 * kC + r]);
+            }
+            sdg[r] = dg - bd;
+            sbd[r] = bd;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float tot = 0.f;
+            for (int r = 0; r < len; ++r) tot += sbd[r];
+            sdg[len - 1] += tot + __expf(gl) * dS;
+        }
+        __syncthreads();
+        float* dga = p.dgamA + ci * kC;
+        for (int r = tid; r < kC; r += blockDim.x) dga[r] = sdg[r];
+    }
+    if (!ok && tid == 0) atomicOr(p.err, GDN_DEVERR_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
 // Sum over the 16 lanes of a half warp (xor butterfly, fixed order); every lane gets the sum.
@@ -1376,9 +1577,14 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
         if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
     }
 
-    const size_t smem_is = sizeof(float) * (kMaxD * kLdD + 4 * kC * kLdD + 2 * kC + 32);
-    if (!set_smem(bwd_intra_s_kernel, smem_is)) return GDN_ERR_CUDA;
-    bwd_intra_s_kernel<<<gch, kNT, smem_is, cs>>>(p);
+    if (tc_state && s->dk == 128) {
+        if (!set_smem(bwd_intra_s_tc_kernel, kIntraSTcSmem)) return GDN_ERR_CUDA;
+        bwd_intra_s_tc_kernel<<<gch, kNTtc, kIntraSTcSmem, cs>>>(p);
+    } else {
+        const size_t smem_is = sizeof(float) * (kMaxD * kLdD + 4 * kC * kLdD + 2 * kC + 32);
+        if (!set_smem(bwd_intra_s_kernel, smem_is)) return GDN_ERR_CUDA;
+        bwd_intra_s_kernel<<<gch, kNT, smem_is, cs>>>(p);
+    }
     if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
     const size_t smem_ic = sizeof(float) * (4 * kC * kLdD + 4 * kC * kLdC + 4 * kC);
     if (!set_smem(bwd_intra_c_kernel, smem_ic)) return GDN_ERR_CUDA;

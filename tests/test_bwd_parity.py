@@ -58,7 +58,7 @@ def test_tiny_config_fp32():
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 32), (32, 64)])
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 128), (32, 128), (64, 32), (32, 64)])
 def test_varlen_chunks(dtype, dk, dv):
     lengths = [65, 1, 0, 64, 130, 37]
     x = inputs.make_inputs(lengths, HK=2, HV=4, dk=dk, dv=dv, dtype=dtype, seed=21, init_scale=0.2)
