@@ -1236,6 +1236,249 @@ __device__ __forceinline__ float half_sum(float x) {
     return x;
 }
 
+// per (chunk, head), dk = dv = 128, bf16 inputs: bwd_wy_kernel on tcgen05.
+//   [K; Q] K^T (M = 128: rows 0..63 give K K^T, rows 64..127 give Q K^T; the B operand is the
+//   first 64 rows of the same shared-memory copy), A and P from them, T = (I + A)^-1 by blocked
+//   forward substitution (16 x 16 blocks), then W^T = K^T (T diag(beta Gam))^T
+//   and U~^T = V^T (T diag(beta))^T with the dk / dv index as the M = 128 rows, so each epilogue
+//   thread stores one column of W and U~: coalesced.
+constexpr int kLdT = kC + 1;  // fp32 A and T in shared memory: row-per-lane writes hit distinct banks
+constexpr size_t kWyTcSmem = (size_t)65536 + 2 * 4 * kC * kLdT + 2 * 4 * kC * kC + 4 * 3 * kC + 16;
+
+__global__ void __launch_bounds__(kNTtc, 1) bwd_wy_tc_kernel(BwdParams p) {
+    constexpr int kD = 128;
+    constexpr uint32_t kSbo = kD * 32;
+    extern __shared__ __align__(128) uint8_t smb[];
+    uint8_t* sX = smb;                                          // A: [K; Q] 128 x 128, then K^T | V^T (128 x 64 each)
+    float* sAf = reinterpret_cast<float*>(sX + 65536);          // A (fp32, 64 x kLdT)
+    float* sTf = sAf + kC * kLdT;                               // T (fp32, 64 x kLdT)
+    uint8_t* sB2 = reinterpret_cast<uint8_t*>(sTf + kC * kLdT); // B: T diag(beta Gam)  64 x 64
+    uint8_t* sB3 = sB2 + 4 * kC * kC;                           // B: T diag(beta)      64 x 64
+    float* sg = reinterpret_cast<float*>(sB3 + 4 * kC * kC);    // gam
+    float* sGb = sg + kC;                                       // beta Gam
+    float* sb = sGb + kC;                                       // beta
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sb + kC);
+    uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
+    const int c = blockIdx.x, h = blockIdx.y;
+    int n, t0, len;
+    if (!chunk_of(p, c, n, t0, len)) return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, q = warp & 3, cg = warp >> 2;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    const int hk = h / p.G;
+    const size_t ci = ch_index(p, c, h);
+    using M128 = RowsTc<kD, kD>;
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) tmem_alloc(slot, 256);
+    // K (rows 0..63) and Q (rows 64..127), rows >= len zero, in flight while warp 0 takes the cumsum
+    float4 kq[M128::kItems];
+#pragma unroll
+    for (int it = 0; it < M128::kItems; ++it) {
+        const int r = M128::row(it) & (kC - 1), k = M128::col(it);
+        const float* src = M128::row(it) < kC ? p.kn : p.qn;
+        kq[it] = r < len ? *reinterpret_cast<const float4*>(src + ((size_t)(t0 + r) * p.HK + hk) * kD + k)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (warp == 0) {
+        // inclusive cumsum of g over the chunk, fixed order (lane-serial blocks of 2)
+        float g0 = 0.f, g1 = 0.f;
+        const int r0 = 2 * lane, r1 = r0 + 1;
+        if (r0 < len) g0 = p.g[(size_t)(t0 + r0) * p.HV + h];
+        if (r1 < len) g1 = p.g[(size_t)(t0 + r1) * p.HV + h];
+        float s = g0 + g1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(kFull, s, off);
+            if (lane >= off) s += y;
+        }
+        const float excl = s - (g0 + g1);
+        const float c0 = excl + g0, c1 = c0 + g1;
+        sg[r0] = c0;
+        sg[r1] = c1;
+        const float b0 = r0 < len ? p.beta[(size_t)(t0 + r0) * p.HV + h] : 0.f;
+        const float b1 = r1 < len ? p.beta[(size_t)(t0 + r1) * p.HV + h] : 0.f;
+        sb[r0] = b0;
+        sb[r1] = b1;
+        sGb[r0] = b0 * __expf(c0);
+        sGb[r1] = b1 * __expf(c1);
+        if (r0 < len) p.gam[(size_t)(t0 + r0) * p.HV + h] = c0;
+        if (r1 < len) p.gam[(size_t)(t0 + r1) * p.HV + h] = c1;
+    }
+    __syncthreads();
+    {
+        // the operand copy, and diag(b) K, diag(Gam) Q for the sequential passes (rows >= len zero)
+        const float gl = sg[len - 1];
+        float* BK = p.BKb + ci * kC * kD;
+        float* GQ = p.GQb + ci * kC * kD;
+#pragma unroll
+        for (int it = 0; it < M128::kItems; ++it) {
+            const int m = M128::row(it), r = m & (kC - 1), k = M128::col(it);
+            const float4 v = kq[it];
+            *reinterpret_cast<float4*>(sX + umma_koff(m, k, kSbo)) = tf32_round4(v);
+            const float f = r < len ? __expf(m < kC ? gl - sg[r] : sg[r]) : 0.f;
+            *reinterpret_cast<float4*>((m < kC ? BK : GQ) + (size_t)r * kD + k) =
+                make_float4(f * v.x, f * v.y, f * v.z, f * v.w);
+        }
+    }
+    tc_sync();
+    const uint32_t tmem = *slot;
+    uint32_t phase = 0;
+    bool ok;
+    do {
+        if (tid == 0) {
+            umma_tf32_k(tmem, smem_u32(sX), kSbo, smem_u32(sX), kSbo, umma_idesc_tf32(kD, kC), kD, false);
+            umma_commit(bar);
+        }
+        if (!(ok = tc_wait(bar, phase))) break;
+        {
+            // rows m < 64: A[r][s] = beta_r E[r][s] (K K^T)[r][s] for s < r;  rows m >= 64: Q K^T and P
+            float x[16];
+            tmem_ld<2>(tmem + lane_base + cg * 16, x);
+            const int m = q * 32 + lane, r = m & (kC - 1);
+            if (m < kC) {
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const int s = cg * 16 + t;
+                    sAf[r * kLdT + s] = s < r ? sb[r] * __expf(sg[r] - sg[s]) * x[t] : 0.f;
+                }
+            } else {
+                float* QK = p.QKb + (ci * kC + r) * kC + cg * 16;
+                float* P = p.Pb + (ci * kC + r) * kC + cg * 16;
+#pragma unroll
+                for (int t = 0; t < 16; t += 4) {
+                    *reinterpret_cast<float4*>(QK + t) = make_float4(x[t], x[t + 1], x[t + 2], x[t + 3]);
+                    float e[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int s = cg * 16 + t + u;
+                        e[u] = (s <= r && r < len) ? x[t + u] * __expf(sg[r] - sg[s]) : 0.f;
+                    }
+                    *reinterpret_cast<float4*>(P + t) = make_float4(e[0], e[1], e[2], e[3]);
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();  // A complete; the first product has read sX
+        {
+            // K^T (j, s) = K[t0 + s][hk][j] and V^T (i, s) = V[t0 + s][h][i], s >= len zero, into sX
+            constexpr int kItems = kD * kC / 4 / kNTtc;
+            float4 kt[kItems], vt[kItems];
+            const size_t sk = (size_t)p.HK * kD, sv = (size_t)p.HV * kD;
+#pragma unroll
+            for (int it = 0; it < kItems; ++it) {
+                const int e = tid + it * kNTtc, jj = e % kD, s = (e / kD) * 4;
+                const size_t bk = ((size_t)(t0 + s) * p.HK + hk) * kD + jj, bv = ((size_t)(t0 + s) * p.HV + h) * kD + jj;
+                kt[it] = make_float4(s < len ? p.kn[bk] : 0.f, s + 1 < len ? p.kn[bk + sk] : 0.f,
+                                     s + 2 < len ? p.kn[bk + 2 * sk] : 0.f, s + 3 < len ? p.kn[bk + 3 * sk] : 0.f);
+                vt[it] = make_float4(s < len ? ld_any(p.v, bv, p.dtype) : 0.f,
+                                     s + 1 < len ? ld_any(p.v, bv + sv, p.dtype) : 0.f,
+                                     s + 2 < len ? ld_any(p.v, bv + 2 * sv, p.dtype) : 0.f,
+                                     s + 3 < len ? ld_any(p.v, bv + 3 * sv, p.dtype) : 0.f);
+            }
+            // T = (I + A)^-1 by 16 x 16 blocks.  Diagonal blocks: column c by the 8 lanes tid / 8,
+            // lane l holding T[16 b + jl + l + 8 m][c] (b = c / 16, jl = c % 16), rows in order,
+            // each row's dot over s = jl + l + 8 m then an 8-lane butterfly.  The 4 columns of a warp
+            // share a block and run the rows from the first of them, so every butterfly has all 32
+            // lanes.  Then block rows i = 1..3: M_ij = sum_{k=j..i-1} A_ik T_kj, T_ij = -T_ii M_ij.
+            {
+                const int col = tid >> 3, l = tid & 7, b0 = (col >> 4) * 16, jl = col & 15;
+                float t[2] = {0.f, 0.f};
+                for (int r = jl & ~3; r < 16; ++r) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int m = 0; m < 2; ++m) {
+                        const int s = jl + l + 8 * m;
+                        if (s < 16) acc = fmaf(sAf[(b0 + r) * kLdT + b0 + s], t[m], acc);
+                    }
+#pragma unroll
+                    for (int off = 4; off >= 1; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
+                    const float x = (r == jl ? 1.f : 0.f) - acc;
+                    const int d = r - jl;
+                    if (d >= 0 && (d & 7) == l) t[d >> 3] = x;
+                }
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                    const int r = jl + l + 8 * m;
+                    if (r < 16) sTf[(b0 + r) * kLdT + col] = t[m];
+                }
+                for (int r = l; r < b0 + jl; r += 8) sTf[r * kLdT + col] = 0.f;  // above the diagonal
+            }
+            float* sM = reinterpret_cast<float*>(sB2);  // scratch for M_ij, up to 3 blocks
+            for (int i = 1; i < 4; ++i) {
+                __syncthreads();
+                for (int e = tid; e < i * 256; e += kNTtc) {
+                    const int jb = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+                    float acc = 0.f;
+                    for (int k = jb; k < i; ++k)
+#pragma unroll
+                        for (int s = 0; s < 16; ++s)
+                            acc = fmaf(sAf[(16 * i + rr) * kLdT + 16 * k + s], sTf[(16 * k + s) * kLdT + 16 * jb + cc], acc);
+                    sM[e] = acc;
+                }
+                __syncthreads();
+                for (int e = tid; e < i * 256; e += kNTtc) {
+                    const int jb = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int s = 0; s < 16; ++s)
+                        acc = fmaf(sTf[(16 * i + rr) * kLdT + 16 * i + s], sM[(jb << 8) + (s << 4) + cc], acc);
+                    sTf[(16 * i + rr) * kLdT + 16 * jb + cc] = -acc;
+                }
+            }
+            __syncthreads();
+#pragma unroll
+            for (int it = 0; it < kItems; ++it) {
+                const int e = tid + it * kNTtc, jj = e % kD, s = (e / kD) * 4;
+                *reinterpret_cast<float4*>(sX + umma_koff(jj, s, kSboC)) = tf32_round4(kt[it]);
+                *reinterpret_cast<float4*>(sX + 32768 + umma_koff(jj, s, kSboC)) = tf32_round4(vt[it]);
+            }
+        }
+        __syncthreads();
+        {
+            // T out; B operands T diag(beta Gam) and T diag(beta) (rows r, k = s)
+            float* Tg = p.Tb + ci * kC * kC;
+            for (int e = tid; e < kC * kC / 4; e += kNTtc) {
+                const int r = e / (kC / 4), s = (e % (kC / 4)) * 4;
+                const float* tr = sTf + r * kLdT + s;
+                const float4 tv = make_float4(tr[0], tr[1], tr[2], tr[3]);
+                *reinterpret_cast<float4*>(Tg + r * kC + s) = tv;
+                *reinterpret_cast<float4*>(sB2 + umma_koff(r, s, kSboC)) = tf32_round4(
+                    make_float4(tv.x * sGb[s], tv.y * sGb[s + 1], tv.z * sGb[s + 2], tv.w * sGb[s + 3]));
+                *reinterpret_cast<float4*>(sB3 + umma_koff(r, s, kSboC)) = tf32_round4(
+                    make_float4(tv.x * sb[s], tv.y * sb[s + 1], tv.z * sb[s + 2], tv.w * sb[s + 3]));
+            }
+        }
+        tc_sync();
+        if (tid == 0) {
+            const uint32_t id = umma_idesc_tf32(kD, kC);
+            umma_tf32_k(tmem + 64, smem_u32(sX), kSboC, smem_u32(sB2), kSboC, id, kC, false);
+            umma_tf32_k(tmem + 128, smem_u32(sX) + 32768, kSboC, smem_u32(sB3), kSboC, id, kC, false);
+            umma_commit(bar);
+        }
+        if (!(ok = tc_wait(bar, phase))) break;
+        {
+            // W[r][j] = (W^T)[j][r] and U~[r][i] = (U~^T)[i][r] for r = 16 cg + t
+            const int jj = q * 32 + lane;
+            float w[16], u[16];
+            tmem_ld<2>(tmem + lane_base + 64 + cg * 16, w);
+            tmem_ld<2>(tmem + lane_base + 128 + cg * 16, u);
+            float* W = p.Wb + ci * kC * kD + jj;
+            float* Ut = p.Utb + ci * kC * kD + jj;
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+                W[(size_t)(cg * 16 + t) * kD] = w[t];
+                Ut[(size_t)(cg * 16 + t) * kD] = u[t];
+            }
+        }
+    } while (false);
+    if (!ok && tid == 0) atomicOr(p.err, GDN_DEVERR_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
 // per (chunk, head): the C x C part.
 __global__ void __launch_bounds__(kNT) bwd_intra_c_kernel(BwdParams p) {
     extern __shared__ float sm[];
@@ -1550,12 +1793,17 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
         if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
     }
     const dim3 gch(L.nchm, s->HV);
-    const size_t smem_wy = sizeof(float) * (2 * kC * kLdD + 2 * kC * kLdC + 3 * kC);
-    if (!set_smem(bwd_wy_kernel, smem_wy)) return GDN_ERR_CUDA;
-    bwd_wy_kernel<<<gch, kNTwy, smem_wy, cs>>>(p);
+    const bool tc_state = s->dtype == GDN_BF16 && s->dv == 128 && (s->dk == 32 || s->dk == 64 || s->dk == 128);
+    if (tc_state && s->dk == 128) {
+        if (!set_smem(bwd_wy_tc_kernel, kWyTcSmem)) return GDN_ERR_CUDA;
+        bwd_wy_tc_kernel<<<gch, kNTtc, kWyTcSmem, cs>>>(p);
+    } else {
+        const size_t smem_wy = sizeof(float) * (2 * kC * kLdD + 2 * kC * kLdC + 3 * kC);
+        if (!set_smem(bwd_wy_kernel, smem_wy)) return GDN_ERR_CUDA;
+        bwd_wy_kernel<<<gch, kNTwy, smem_wy, cs>>>(p);
+    }
     if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
 
-    const bool tc_state = s->dtype == GDN_BF16 && s->dv == 128 && (s->dk == 32 || s->dk == 64 || s->dk == 128);
     if (tc_state) {
         gdn_status st = GDN_ERR_UNSUPPORTED;
         switch (s->dk) {
