@@ -17,9 +17,13 @@
 //     dQ   = diag(Gam) dO S0 + dQK K,  dK = dQK^T Q + diag(b) U D + diag(beta Gam) T^T dW + (dKK + dKK^T) K
 //     dW = -dU S0, dV = diag(beta) T^T dU, dA = -T^T dT T^T, dT = dW (beta Gam K)^T + dU (beta V)^T
 //     plus the dbeta and dgam terms; dg = reverse cumsum of dgam inside the chunk.
-// Every dense product goes through one CTA-wide helper: TF32 tensor cores
-// (mma.sync m16n8k8, 3xTF32 split for about fp32 accuracy) by default, or the
-// fp32 SIMT loop below when built with GDN_BWD_SIMT.  Kernels:
+// Dense products run on the tensor cores in TF32 with fp32 accumulation.  For bf16
+// inputs with dv = 128 the serial state passes, and at dk = dv = 128 also bwd_wy and
+// bwd_intra_s, use the fifth-generation tensor cores (tcgen05: operands in shared
+// memory, accumulators in TMEM; gdn_umma.cuh) in *_tc kernels, with every product
+// laid out so its 128 rows are a dk or dv index.  Everything else goes through one
+// CTA-wide mma.sync helper (m16n8k8; 3xTF32 split for fp32 inputs, about fp32
+// accuracy), or the fp32 SIMT loop below when built with GDN_BWD_SIMT.  Kernels:
 //     bwd_offsets   chunk offsets per sequence (+ cu_seqlens validation)
 //     bwd_norm      q^, k^ and 1/|.| per (token, k-head)
 //     bwd_wy        per (chunk, head): gam, T, W, U~, Q K^T              [chunk-parallel]
