@@ -54,7 +54,10 @@ __device__ __forceinline__ float4 tf32_round4(float4 v) {
     return make_float4(tf32_round(v.x), tf32_round(v.y), tf32_round(v.z), tf32_round(v.w));
 }
 
-// TMEM allocation by one whole warp; the address lands in *slot (shared memory).
+// TMEM allocation by one whole warp; the address lands in *slot (shared memory).  An allocation
+// waits while the SM's 512 columns are taken.  The kernels here allocate 256 columns each and run
+// 512 threads at 72 to 128 registers (over 36K registers per CTA), so no two of their CTAs share
+// an SM and the allocation never waits.
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)), "r"(ncols)
                  : "memory");
