@@ -77,6 +77,16 @@ def test_no_init_no_dfinal_no_l2norm():
     check(got, ref, x.cu_seqlens)
 
 
+def test_no_l2norm_bf16_head128():
+    """use_qk_l2norm off (inputs drawn unit-norm, then rounded to bf16) through the tcgen05
+    kernels (bf16, dk = dv = 128)."""
+    lengths = [150, 64, 9]
+    x = inputs.make_inputs(lengths, HK=1, HV=2, dk=128, dv=128, dtype=torch.bfloat16, seed=28, init_scale=0.1)
+    dO = inputs.grad_out(sum(lengths), 2, 128, seed=29)
+    got, ref = run(x, dO, None, use_qk_l2norm=False)
+    check(got, ref, x.cu_seqlens)
+
+
 def test_backward_workload_sampled():
     """gdn_chunk_bwd on 8 x 4096 tokens, HK=16, HV=32, dk=dv=128, bf16, as the
     benchmark launches it; the oracle recomputes sampled (sequence, k-head)
