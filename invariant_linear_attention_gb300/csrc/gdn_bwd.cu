@@ -1632,6 +1632,336 @@ __global__ void __launch_bounds__(kNT) bwd_intra_c_kernel(BwdParams p) {
     }
 }
 
+// dst(n, k) = get4(n, k) (four consecutive k) for n < NN, k < KK, rounded to TF32, in the RowsTc
+// thread mapping; all loads are issued before any store.
+template <int NN, int KK, typename G>
+__device__ __forceinline__ void stage_rows_fn(uint8_t* dst, G get4) {
+    using R = RowsTc<NN, KK>;
+    float4 v[R::kItems];
+#pragma unroll
+    for (int it = 0; it < R::kItems; ++it) v[it] = get4(R::row(it), R::col(it));
+#pragma unroll
+    for (int it = 0; it < R::kItems; ++it)
+        *reinterpret_cast<float4*>(dst + umma_koff(R::row(it), R::col(it), KK * 32)) = tf32_round4(v[it]);
+}
+// dst(n, k) = get(k, n) for n < NN, k < KK (a transpose), rounded to TF32; consecutive threads
+// take consecutive n.
+template <int NN, int KK, typename G>
+__device__ __forceinline__ void stage_cols_fn(uint8_t* dst, G get) {
+    constexpr int kItems = NN * KK / 4 / kNTtc;
+    float4 v[kItems];
+#pragma unroll
+    for (int it = 0; it < kItems; ++it) {
+        const int e = threadIdx.x + it * kNTtc, n = e % NN, k = (e / NN) * 4;
+        v[it] = make_float4(get(k, n), get(k + 1, n), get(k + 2, n), get(k + 3, n));
+    }
+#pragma unroll
+    for (int it = 0; it < kItems; ++it) {
+        const int e = threadIdx.x + it * kNTtc, n = e % NN, k = (e / NN) * 4;
+        *reinterpret_cast<float4*>(dst + umma_koff(n, k, KK * 32)) = tf32_round4(v[it]);
+    }
+}
+
+// per (chunk, head), dk = dv = 128, bf16 inputs: bwd_intra_c_kernel on tcgen05.  The C x C
+// products (dP = dO U^T, K K^T, F1 = dW K^T, F2 = dU V^T, Z = dT T^T, T^T Z) use M = 64: row m
+// of the result sits in TMEM lane 32 (m / 16) + m % 16, so lanes 0..15 of each warp hold 16 rows.
+// The products that update dq, dk, dv are taken transposed with the dk / dv index as their 128
+// rows; dk's three terms accumulate in TMEM and meet global memory once.
+//   TMEM columns: 0 dP, then Z | 64 K K^T | 128 dq^T | 192 dk^T | 256 dv^T | 320 F1 | 384 F2 | 448 T^T Z
+//   shared memory: five 32 KB operand buffers R1..R5 and two 16 KB ones C1, C2, reused by phase
+constexpr size_t kIntraCTcSmem = (size_t)5 * 32768 + 2 * 16384 + 4 * kC * kLdT + 4 * (4 * kC + 3 * 4 * kC) + 16;
+
+__global__ void __launch_bounds__(kNTtc, 1) bwd_intra_c_tc_kernel(BwdParams p) {
+    constexpr int kD = 128;
+    constexpr uint32_t kSboD = kD * 32;  // 128 values per row
+    extern __shared__ __align__(128) uint8_t smb[];
+    uint8_t* R1 = smb;
+    uint8_t* R2 = R1 + 32768;
+    uint8_t* R3 = R2 + 32768;
+    uint8_t* R4 = R3 + 32768;
+    uint8_t* R5 = R4 + 32768;
+    uint8_t* C1 = R5 + 32768;
+    uint8_t* C2 = C1 + 16384;
+    float* sE = reinterpret_cast<float*>(C2 + 16384);  // dE accumulator, 64 x kLdT
+    float* sg = sE + kC * kLdT;                         // gam
+    float* sbe = sg + kC;                               // beta
+    float* sdg = sbe + kC;                              // dgam
+    float* sdb = sdg + kC;                              // dbeta
+    float* part1 = sdb + kC;                            // [4][64] column-dot partials (F1)
+    float* part2 = part1 + 4 * kC;                      // [4][64] column-dot partials (F2)
+    float* rowp = part2 + 4 * kC;                       // [4][64] row-loop partials
+    uint64_t* bar = reinterpret_cast<uint64_t*>(rowp + 4 * kC);
+    uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
+    const int c = blockIdx.x, h = blockIdx.y;
+    int n, t0, len;
+    if (!chunk_of(p, c, n, t0, len)) return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, q = warp & 3, cg = warp >> 2;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    const int hk = h / p.G;
+    const size_t ci = ch_index(p, c, h);
+    const bool row_lane = lane < 16;    // lanes holding a row of an M = 64 result
+    const int r64 = 16 * q + (lane & 15);  // that row
+    const int jj = 32 * q + lane;          // the dk / dv index of an M = 128 result
+    const float* Tg = p.Tb + ci * kC * kC;
+    const size_t sk = (size_t)p.HK * kD, sv = (size_t)p.HV * kD;
+    const float* kb = p.kn + ((size_t)t0 * p.HK + hk) * kD;  // K^ row s at kb + s * sk
+    const float* qb = p.qn + ((size_t)t0 * p.HK + hk) * kD;
+    const size_t ob = ((size_t)t0 * p.HV + h) * kD;           // dO / V row r at ob + r * sv
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) tmem_alloc(slot, 512);
+    // phase A: K^ -> R1, dO -> R2, U -> R3, dW -> R4, dU -> R5 (rows = chunk positions)
+    stage_rows_fn<kC, kD>(R1, [&](int s, int k) {
+        return s < len ? *reinterpret_cast<const float4*>(kb + s * sk + k) : z4;
+    });
+    stage_rows_fn<kC, kD>(R2, [&](int r, int k) { return r < len ? ld4_any(p.dout, ob + r * sv + k, p.dtype) : z4; });
+    stage_rows_fn<kC, kD>(R3, [&](int s, int k) {
+        return *reinterpret_cast<const float4*>(p.Ub + (ci * kC + s) * kD + k);
+    });
+    stage_rows_fn<kC, kD>(R4, [&](int s, int k) {
+        return *reinterpret_cast<const float4*>(p.Wb + (ci * kC + s) * kD + k);
+    });
+    stage_rows_fn<kC, kD>(R5, [&](int s, int k) {
+        return *reinterpret_cast<const float4*>(p.dUb + (ci * kC + s) * kD + k);
+    });
+    for (int i = tid; i < kC; i += kNTtc) {
+        sg[i] = i < len ? p.gam[(size_t)(t0 + i) * p.HV + h] : 0.f;
+        sbe[i] = i < len ? p.beta[(size_t)(t0 + i) * p.HV + h] : 0.f;
+        sdg[i] = p.dgamA[ci * kC + i];
+        sdb[i] = 0.f;
+    }
+    tc_sync();
+    const uint32_t tmem = *slot;
+    const uint32_t id64 = umma_idesc_tf32(kC, kC), id128 = umma_idesc_tf32(kD, kC);
+    uint32_t phase = 0;
+    bool ok;
+    do {
+        if (tid == 0) {
+            umma_tf32_k(tmem + 0, smem_u32(R2), kSboD, smem_u32(R3), kSboD, id64, kD, false);    // dP
+            umma_tf32_k(tmem + 64, smem_u32(R1), kSboD, smem_u32(R1), kSboD, id64, kD, false);   // K K^T
+            umma_tf32_k(tmem + 320, smem_u32(R4), kSboD, smem_u32(R1), kSboD, id64, kD, false);  // F1
+            umma_commit(bar);
+        }
+        if (!(ok = tc_wait(bar, phase))) break;
+        // phase B: dQK = lower(dP) E, dE = lower(dP) QK; dQK (C1) and its transpose (C2)
+        {
+            float x[16];
+            tmem_ld<2>(tmem + lane_base + 0 + cg * 16, x);
+            if (row_lane) {
+                const int r = r64;
+                const float* qk = p.QKb + (ci * kC + r) * kC + cg * 16;
+                float qv[16];
+#pragma unroll
+                for (int t = 0; t < 16; t += 4) {
+                    const float4 v = *reinterpret_cast<const float4*>(qk + t);
+                    qv[t] = v.x; qv[t + 1] = v.y; qv[t + 2] = v.z; qv[t + 3] = v.w;
+                }
+                float d[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const int s = cg * 16 + t;
+                    const bool in = s <= r && r < len;
+                    d[t] = in ? x[t] * __expf(sg[r] - sg[s]) : 0.f;
+                    sE[r * kLdT + s] = in ? x[t] * qv[t] : 0.f;
+                    *reinterpret_cast<float*>(C2 + umma_koff(s, r, kSboC)) = tf32_round(d[t]);
+                }
+#pragma unroll
+                for (int t = 0; t < 16; t += 4)
+                    *reinterpret_cast<float4*>(C1 + umma_koff(r, cg * 16 + t, kSboC)) =
+                        tf32_round4(make_float4(d[t], d[t + 1], d[t + 2], d[t + 3]));
+            }
+        }
+        // V -> R2 (rows s), K^T -> R3 (rows j, k = s), Q^T -> R1 (rows j, k = r)
+        stage_rows_fn<kC, kD>(R2, [&](int s, int k) { return s < len ? ld4_any(p.v, ob + s * sv + k, p.dtype) : z4; });
+        stage_cols_fn<kD, kC>(R3, [&](int s, int j) { return s < len ? kb[s * sk + j] : 0.f; });
+        stage_cols_fn<kD, kC>(R1, [&](int r, int j) { return r < len ? qb[r * sk + j] : 0.f; });
+        tc_sync();
+        if (tid == 0) {
+            umma_tf32_k(tmem + 384, smem_u32(R5), kSboD, smem_u32(R2), kSboD, id64, kD, false);   // F2
+            umma_tf32_k(tmem + 128, smem_u32(R3), kSboC, smem_u32(C1), kSboC, id128, kC, false);  // dq^T
+            umma_tf32_k(tmem + 192, smem_u32(R1), kSboC, smem_u32(C2), kSboC, id128, kC, false);  // dk^T
+            umma_commit(bar);
+        }
+        if (!(ok = tc_wait(bar, phase))) break;
+        // phase C: column dots with T, dT (-> R4, rows s, k = r); dq update
+        {
+            float f1[16], f2[16];
+            tmem_ld<2>(tmem + lane_base + 320 + cg * 16, f1);
+            tmem_ld<2>(tmem + lane_base + 384 + cg * 16, f2);
+            float v1[16], v2[16];
+            if (row_lane) {
+                const int s = r64;
+                const float* tr = Tg + s * kC + cg * 16;
+                float dt[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const int r = cg * 16 + t;
+                    const float tv = tr[t];
+                    v1[t] = tv * f1[t];
+                    v2[t] = tv * f2[t];
+                    dt[t] = sbe[r] * fmaf(__expf(sg[r]), f1[t], f2[t]);
+                }
+#pragma unroll
+                for (int t = 0; t < 16; t += 4)
+                    *reinterpret_cast<float4*>(R4 + umma_koff(s, cg * 16 + t, kSboC)) =
+                        tf32_round4(make_float4(dt[t], dt[t + 1], dt[t + 2], dt[t + 3]));
+            } else {
+#pragma unroll
+                for (int t = 0; t < 16; ++t) v1[t] = v2[t] = 0.f;
+            }
+            const float a1 = warp_transpose_sum<16>(v1), a2 = warp_transpose_sum<16>(v2);
+            if (lane < 16) {
+                part1[q * kC + cg * 16 + lane] = a1;
+                part2[q * kC + cg * 16 + lane] = a2;
+            }
+            float x[16], old[16];
+            float* dq = p.dqh + ((size_t)t0 * p.HV + h) * kD + jj;
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+                const int r = cg * 16 + t;
+                old[t] = r < len ? dq[(size_t)r * p.HV * kD] : 0.f;
+            }
+            tmem_ld<2>(tmem + lane_base + 128 + cg * 16, x);
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+                const int r = cg * 16 + t;
+                if (r < len) dq[(size_t)r * p.HV * kD] = old[t] + x[t];
+            }
+        }
+        // dW^T -> R2, dU^T -> R1 (rows j / i, k = s); diag(beta Gam)-scaled T^T -> C1, diag(beta)-scaled
+        // T^T -> C2 (rows r, k = s); T -> R4 + 16 KB (rows b, k = c)
+        stage_cols_fn<kD, kC>(R2, [&](int s, int j) { return p.Wb[(ci * kC + s) * kD + j]; });
+        stage_cols_fn<kD, kC>(R1, [&](int s, int i) { return p.dUb[(ci * kC + s) * kD + i]; });
+        stage_cols_fn<kC, kC>(C1, [&](int s, int r) { return Tg[s * kC + r] * sbe[r] * __expf(sg[r]); });
+        stage_cols_fn<kC, kC>(C2, [&](int s, int r) { return Tg[s * kC + r] * sbe[r]; });
+        stage_rows_fn<kC, kC>(R4 + 16384, [&](int b, int k) { return *reinterpret_cast<const float4*>(Tg + b * kC + k); });
+        __syncthreads();
+        for (int r = tid; r < kC; r += kNTtc) {
+            const float a1 = ((part1[r] + part1[kC + r]) + part1[2 * kC + r]) + part1[3 * kC + r];
+            const float a2 = ((part2[r] + part2[kC + r]) + part2[2 * kC + r]) + part2[3 * kC + r];
+            const float Gr = __expf(sg[r]);
+            sdb[r] += Gr * a1 + a2;
+            sdg[r] += Gr * sbe[r] * a1;
+        }
+        tc_sync();
+        if (tid == 0) {
+            umma_tf32_k(tmem + 192, smem_u32(R2), kSboC, smem_u32(C1), kSboC, id128, kC, true);          // dk^T
+            umma_tf32_k(tmem + 256, smem_u32(R1), kSboC, smem_u32(C2), kSboC, id128, kC, false);         // dv^T
+            umma_tf32_k(tmem + 0, smem_u32(R4), kSboC, smem_u32(R4) + 16384, kSboC, id64, kC, false);    // Z
+            umma_commit(bar);
+        }
+        if (!(ok = tc_wait(bar, phase))) break;
+        // phase D: dv out; Z^T -> R5 (rows s, k = a); T^T -> R5 + 16 KB (rows r, k = a)
+        {
+            float x[16];
+            tmem_ld<2>(tmem + lane_base + 256 + cg * 16, x);
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+                const int r = cg * 16 + t;
+                if (r < len) st_any(p.dv_out, ((size_t)(t0 + r) * p.HV + h) * kD + jj, p.dtype, x[t]);
+            }
+            tmem_ld<2>(tmem + lane_base + 0 + cg * 16, x);
+            if (row_lane) {
+#pragma unroll
+                for (int t = 0; t < 16; ++t)
+                    *reinterpret_cast<float*>(R5 + umma_koff(cg * 16 + t, r64, kSboC)) = tf32_round(x[t]);
+            }
+        }
+        stage_cols_fn<kC, kC>(R5 + 16384, [&](int a, int r) { return Tg[a * kC + r]; });
+        tc_sync();
+        if (tid == 0) {
+            umma_tf32_k(tmem + 448, smem_u32(R5) + 16384, kSboC, smem_u32(R5), kSboC, id64, kC, false);  // T^T Z
+            umma_commit(bar);
+        }
+        if (!(ok = tc_wait(bar, phase))) break;
+        // phase E: dA = -strict_lower(T^T Z); dbeta_r += sum_s dA E KK; dKK = dA beta_r E (fp32 in R2);
+        // dE += dA beta_r KK
+        float* sdKK = reinterpret_cast<float*>(R2);  // 64 x kLdT
+        {
+            float a[16], kk[16];
+            tmem_ld<2>(tmem + lane_base + 448 + cg * 16, a);
+            tmem_ld<2>(tmem + lane_base + 64 + cg * 16, kk);
+            float acc = 0.f;
+            if (row_lane) {
+                const int r = r64;
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const int s = cg * 16 + t;
+                    const float da = s < r ? -a[t] : 0.f, e = __expf(sg[r] - sg[s]);
+                    acc = fmaf(da * e, kk[t], acc);
+                    sdKK[r * kLdT + s] = da * sbe[r] * e;
+                    sE[r * kLdT + s] = fmaf(da * sbe[r], kk[t], sE[r * kLdT + s]);
+                }
+                rowp[cg * kC + r] = acc;
+            }
+        }
+        __syncthreads();
+        for (int r = tid; r < kC; r += kNTtc) sdb[r] += ((rowp[r] + rowp[kC + r]) + rowp[2 * kC + r]) + rowp[3 * kC + r];
+        // dKK + dKK^T -> C1 (rows r, k = s)
+        for (int e = tid; e < kC * kC / 4; e += kNTtc) {
+            const int r = e / (kC / 4), s = (e % (kC / 4)) * 4;
+            float4 v;
+            v.x = sdKK[r * kLdT + s] + sdKK[s * kLdT + r];
+            v.y = sdKK[r * kLdT + s + 1] + sdKK[(s + 1) * kLdT + r];
+            v.z = sdKK[r * kLdT + s + 2] + sdKK[(s + 2) * kLdT + r];
+            v.w = sdKK[r * kLdT + s + 3] + sdKK[(s + 3) * kLdT + r];
+            *reinterpret_cast<float4*>(C1 + umma_koff(r, s, kSboC)) = tf32_round4(v);
+        }
+        tc_sync();
+        if (tid == 0) {
+            umma_tf32_k(tmem + 192, smem_u32(R3), kSboC, smem_u32(C1), kSboC, id128, kC, true);  // dk^T
+            umma_commit(bar);
+        }
+        if (!(ok = tc_wait(bar, phase))) break;
+        // phase F: dk update (all three terms at once)
+        {
+            float x[16], old[16];
+            float* dkk = p.dkh + ((size_t)t0 * p.HV + h) * kD + jj;
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+                const int r = cg * 16 + t;
+                old[t] = r < len ? dkk[(size_t)r * p.HV * kD] : 0.f;
+            }
+            tmem_ld<2>(tmem + lane_base + 192 + cg * 16, x);
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+                const int r = cg * 16 + t;
+                if (r < len) dkk[(size_t)r * p.HV * kD] = old[t] + x[t];
+            }
+        }
+    } while (false);
+    if (ok) {
+        // dgam from E (row sums minus column sums of dE * E), then dg = reverse cumsum
+        for (int r = tid >> 4; r < kC; r += kNTtc >> 4) {
+            const int l = tid & 15;
+            float rs = 0.f, cs = 0.f;
+            for (int s = l; s < kC; s += 16) {
+                rs = fmaf(sE[r * kLdT + s], __expf(sg[r] - sg[s]), rs);
+                cs = fmaf(sE[s * kLdT + r], __expf(sg[s] - sg[r]), cs);
+            }
+            rs = half_sum(rs);
+            cs = half_sum(cs);
+            if (l == 0) sdg[r] += rs - cs;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float acc = 0.f;
+            for (int r = len - 1; r >= 0; --r) {
+                acc += sdg[r];
+                p.dg[(size_t)(t0 + r) * p.HV + h] = acc;
+                p.dbeta[(size_t)(t0 + r) * p.HV + h] = sdb[r];
+            }
+        }
+    }
+    if (!ok && tid == 0) atomicOr(p.err, GDN_DEVERR_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
 // per (token, k-head): sum the G value heads in increasing order, then the L2-norm backward
 __global__ void bwd_fold_kernel(BwdParams p) {
     const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
@@ -1838,9 +2168,14 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
         bwd_intra_s_kernel<<<gch, kNT, smem_is, cs>>>(p);
     }
     if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
-    const size_t smem_ic = sizeof(float) * (4 * kC * kLdD + 4 * kC * kLdC + 4 * kC);
-    if (!set_smem(bwd_intra_c_kernel, smem_ic)) return GDN_ERR_CUDA;
-    bwd_intra_c_kernel<<<gch, kNT, smem_ic, cs>>>(p);
+    if (tc_state && s->dk == 128) {
+        if (!set_smem(bwd_intra_c_tc_kernel, kIntraCTcSmem)) return GDN_ERR_CUDA;
+        bwd_intra_c_tc_kernel<<<gch, kNTtc, kIntraCTcSmem, cs>>>(p);
+    } else {
+        const size_t smem_ic = sizeof(float) * (4 * kC * kLdD + 4 * kC * kLdC + 4 * kC);
+        if (!set_smem(bwd_intra_c_kernel, smem_ic)) return GDN_ERR_CUDA;
+        bwd_intra_c_kernel<<<gch, kNT, smem_ic, cs>>>(p);
+    }
     if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
     if (s->T_total > 0) {
         const int vec = s->T_total * s->HK;
