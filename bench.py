@@ -765,10 +765,9 @@ def bench_backward(gdn, dev, steps=3):
             f"dk=dv={DK}, bf16, chunk 64",
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf32_peak, "unit": "TFLOP/s",
                          "frac": achieved / tf32_peak, "flops_per_chunk_head": 2 * macs,
-                         "note": "TF32 with fp32 accumulate (bf16 inputs): tcgen05 in the WY stage, the state passes "
-                                 "and the state products, mma.sync in the intra-chunk C x C products; peak = "
-                                 "sustained measured bf16 x 1.1/2.25 (nominal tf32/bf16); per-chunk latency, "
-                                 "not tensor throughput, bounds the time"}}
+                         "note": "TF32 with fp32 accumulate (bf16 inputs) on tcgen05 in every contracting kernel; "
+                                 "peak = sustained measured bf16 x 1.1/2.25 (nominal tf32/bf16); per-chunk "
+                                 "latency, not tensor throughput, bounds the time"}}
 
 
 if __name__ == "__main__":

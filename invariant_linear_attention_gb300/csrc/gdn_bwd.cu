@@ -18,12 +18,13 @@
 //     dW = -dU S0, dV = diag(beta) T^T dU, dA = -T^T dT T^T, dT = dW (beta Gam K)^T + dU (beta V)^T
 //     plus the dbeta and dgam terms; dg = reverse cumsum of dgam inside the chunk.
 // Dense products run on the tensor cores in TF32 with fp32 accumulation.  For bf16
-// inputs with dv = 128 the serial state passes, and at dk = dv = 128 also bwd_wy and
-// bwd_intra_s, use the fifth-generation tensor cores (tcgen05: operands in shared
-// memory, accumulators in TMEM; gdn_umma.cuh) in *_tc kernels, with every product
-// laid out so its 128 rows are a dk or dv index.  Everything else goes through one
-// CTA-wide mma.sync helper (m16n8k8; 3xTF32 split for fp32 inputs, about fp32
-// accuracy), or the fp32 SIMT loop below when built with GDN_BWD_SIMT.  Kernels:
+// inputs with dv = 128 the serial state passes, and at dk = dv = 128 all four chunk
+// stages (bwd_wy, both state passes, bwd_intra_s, bwd_intra_c), use the fifth-generation
+// tensor cores (tcgen05: operands in shared memory, accumulators in TMEM; gdn_umma.cuh)
+// in *_tc kernels.  Products that produce dk- or dv-wide results are laid out with that
+// index as their 128 rows; the C x C ones use M = 64.  Other shapes and fp32 inputs go
+// through one CTA-wide mma.sync helper (m16n8k8; 3xTF32 split for fp32 inputs, about
+// fp32 accuracy), or the fp32 SIMT loop below when built with GDN_BWD_SIMT.  Kernels:
 //     bwd_offsets   chunk offsets per sequence (+ cu_seqlens validation)
 //     bwd_norm      q^, k^ and 1/|.| per (token, k-head)
 //     bwd_wy        per (chunk, head): gam, T, W, U~, Q K^T              [chunk-parallel]
