@@ -1968,20 +1968,36 @@ __global__ void bwd_fold_kernel(BwdParams p) {
     const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (w >= p.T * p.HK) return;
     const int t = w / p.HK, hk = w - t * p.HK;
-    for (int which = 0; which < 2; ++which) {
-        const float* src = which ? p.dkh : p.dqh;
-        const float* xh = (which ? p.kn : p.qn) + (size_t)w * p.dk;
-        float d[4], x[4];
-        float dot = 0.f;
+    // every load of a head step (dq and dk together) is issued before any is used; each element
+    // still sums the heads in increasing order
+    float dsum[2][4], x[2][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int j = lane + 32 * i;
+        x[0][i] = j < p.dk ? p.qn[(size_t)w * p.dk + j] : 0.f;
+        x[1][i] = j < p.dk ? p.kn[(size_t)w * p.dk + j] : 0.f;
+        dsum[0][i] = dsum[1][i] = 0.f;
+    }
+    for (int hh = hk * p.G; hh < (hk + 1) * p.G; ++hh) {
+        const size_t base = ((size_t)t * p.HV + hh) * p.dk;
+        float a[4], b[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int j = lane + 32 * i;
-            d[i] = 0.f;
-            x[i] = j < p.dk ? xh[j] : 0.f;
-            if (j < p.dk)
-                for (int hh = hk * p.G; hh < (hk + 1) * p.G; ++hh) d[i] += src[((size_t)t * p.HV + hh) * p.dk + j];
-            dot = fmaf(x[i], d[i], dot);
+            a[i] = j < p.dk ? p.dqh[base + j] : 0.f;
+            b[i] = j < p.dk ? p.dkh[base + j] : 0.f;
         }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            dsum[0][i] += a[i];
+            dsum[1][i] += b[i];
+        }
+    }
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+        float dot = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dot = fmaf(x[which][i], dsum[which][i], dot);
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) dot += __shfl_xor_sync(kFull, dot, off);
         const float inv = (which ? p.kinv : p.qinv)[w];
@@ -1990,7 +2006,7 @@ __global__ void bwd_fold_kernel(BwdParams p) {
         for (int i = 0; i < 4; ++i) {
             const int j = lane + 32 * i;
             if (j < p.dk) {
-                const float gval = p.use_norm ? (d[i] - x[i] * dot) * inv : d[i];
+                const float gval = p.use_norm ? (dsum[which][i] - x[which][i] * dot) * inv : dsum[which][i];
                 st_any(dst, (size_t)w * p.dk + j, p.dtype, gval);
             }
         }
