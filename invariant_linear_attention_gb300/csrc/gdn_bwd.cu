@@ -1663,6 +1663,22 @@ __device__ __forceinline__ void stage_cols_fn(uint8_t* dst, G get) {
     }
 }
 
+// The RowsTc layout filled by 16-byte cp.async (no registers): ptr(n, k) gives the source of
+// four consecutive k, or nullptr for zeros; the caller rounds with RowsTc::round_in_place once its
+// own copies have landed.
+template <int NN, int KK, typename P>
+__device__ __forceinline__ void async_rows(uint8_t* dst, P ptr) {
+    using R = RowsTc<NN, KK>;
+#pragma unroll
+    for (int it = 0; it < R::kItems; ++it) {
+        const int n = R::row(it), k = R::col(it);
+        const float* src = ptr(n, k);
+        uint8_t* d = dst + umma_koff(n, k, KK * 32);
+        if (src) cp_async16(d, src);
+        else *reinterpret_cast<float4*>(d) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
 // per (chunk, head), dk = dv = 128, bf16 inputs: bwd_intra_c_kernel on tcgen05.  The C x C
 // products (dP = dO U^T, K K^T, F1 = dW K^T, F2 = dU V^T, Z = dT T^T, T^T Z) use M = 64: row m
 // of the result sits in TMEM lane 32 (m / 16) + m % 16, so lanes 0..15 of each warp hold 16 rows.
@@ -1714,26 +1730,25 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_intra_c_tc_kernel(BwdParams p) {
         fence_barrier_init();
     }
     if (warp == 0) tmem_alloc(slot, 512);
-    // phase A: K^ -> R1, dO -> R2, U -> R3, dW -> R4, dU -> R5 (rows = chunk positions)
-    stage_rows_fn<kC, kD>(R1, [&](int s, int k) {
-        return s < len ? *reinterpret_cast<const float4*>(kb + s * sk + k) : z4;
-    });
+    // phase A: K^ -> R1, dO -> R2, U -> R3, dW -> R4, dU -> R5 (rows = chunk positions); the fp32
+    // ones by 16-byte cp.async, all in flight together with dO's loads
+    using RowsD = RowsTc<kC, kD>;
+    async_rows<kC, kD>(R1, [&](int s, int k) { return s < len ? kb + s * sk + k : nullptr; });
+    async_rows<kC, kD>(R3, [&](int s, int k) { return p.Ub + (ci * kC + s) * kD + k; });
+    async_rows<kC, kD>(R4, [&](int s, int k) { return p.Wb + (ci * kC + s) * kD + k; });
+    async_rows<kC, kD>(R5, [&](int s, int k) { return p.dUb + (ci * kC + s) * kD + k; });
     stage_rows_fn<kC, kD>(R2, [&](int r, int k) { return r < len ? ld4_any(p.dout, ob + r * sv + k, p.dtype) : z4; });
-    stage_rows_fn<kC, kD>(R3, [&](int s, int k) {
-        return *reinterpret_cast<const float4*>(p.Ub + (ci * kC + s) * kD + k);
-    });
-    stage_rows_fn<kC, kD>(R4, [&](int s, int k) {
-        return *reinterpret_cast<const float4*>(p.Wb + (ci * kC + s) * kD + k);
-    });
-    stage_rows_fn<kC, kD>(R5, [&](int s, int k) {
-        return *reinterpret_cast<const float4*>(p.dUb + (ci * kC + s) * kD + k);
-    });
     for (int i = tid; i < kC; i += kNTtc) {
         sg[i] = i < len ? p.gam[(size_t)(t0 + i) * p.HV + h] : 0.f;
         sbe[i] = i < len ? p.beta[(size_t)(t0 + i) * p.HV + h] : 0.f;
         sdg[i] = p.dgamA[ci * kC + i];
         sdb[i] = 0.f;
     }
+    cp_async_wait_all();
+    RowsD::round_in_place(R1);
+    RowsD::round_in_place(R3);
+    RowsD::round_in_place(R4);
+    RowsD::round_in_place(R5);
     tc_sync();
     const uint32_t tmem = *slot;
     const uint32_t id64 = umma_idesc_tf32(kC, kC), id128 = umma_idesc_tf32(kD, kC);
