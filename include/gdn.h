@@ -147,7 +147,9 @@ gdn_status gdn_decode_step(const gdn_shape* shape, const void* q, const void* k,
  * summed over the value heads that share a k-head), dv (dtype), dg and dbeta
  * (fp32, [T,HV]) and d_init_state (fp32, may be NULL).  init_state and
  * d_final_state may be NULL (zero).  Gradients are not bit-invariant (the
- * pages need invariance only for the forward); they are deterministic.
+ * pages need invariance only for the forward); they are deterministic.  Dense
+ * products run on the tensor cores: TF32 operands with fp32 accumulation for
+ * bf16 inputs, a 3xTF32 split (about fp32 accuracy) for fp32 inputs.
  */
 gdn_status gdn_chunk_bwd(const gdn_shape* shape, const void* q, const void* k, const void* v,
                          const float* g, const float* beta, const float* init_state,

@@ -1,5 +1,6 @@
 // gdn_mma.cuh -- CTA-wide dense contraction on the tensor cores (TF32 in, fp32
-// accumulate) for the chunked backward's intra-chunk products.
+// accumulate) with the mma.sync instruction, for the chunked backward's kernels at the
+// shapes and dtypes the tcgen05 kernels do not take (fp32 inputs, dv != 128, dk < 128).
 //
 // cta_gemm_tc(split, M, N, K, A, as0, as1, B, bs0, bs1, f) computes
 //     C(m, n) = sum_k A(m, k) B(k, n),  A(m, k) = A[m*as0 + k*as1],  B(k, n) = B[k*bs0 + n*bs1]
