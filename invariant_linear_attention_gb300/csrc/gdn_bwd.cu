@@ -1367,20 +1367,17 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_wy_tc_kernel(BwdParams p) {
         tc_fence_before();
         __syncthreads();  // A complete; the first product has read sX
         {
-            // K^T (j, s) = K[t0 + s][hk][j] and V^T (i, s) = V[t0 + s][h][i], s >= len zero, into sX
-            constexpr int kItems = kD * kC / 4 / kNTtc;
-            float4 kt[kItems], vt[kItems];
-            const size_t sk = (size_t)p.HK * kD, sv = (size_t)p.HV * kD;
+            // K (row s, four consecutive j) and V rows, s >= len zero, by vector loads in flight during
+            // the solve; written transposed into sX after it: K^T (j, s) and V^T (i, s)
+            using RowsK = RowsTc<kC, kD>;
+            float4 kr[RowsK::kItems], vr[RowsK::kItems];
 #pragma unroll
-            for (int it = 0; it < kItems; ++it) {
-                const int e = tid + it * kNTtc, jj = e % kD, s = (e / kD) * 4;
-                const size_t bk = ((size_t)(t0 + s) * p.HK + hk) * kD + jj, bv = ((size_t)(t0 + s) * p.HV + h) * kD + jj;
-                kt[it] = make_float4(s < len ? p.kn[bk] : 0.f, s + 1 < len ? p.kn[bk + sk] : 0.f,
-                                     s + 2 < len ? p.kn[bk + 2 * sk] : 0.f, s + 3 < len ? p.kn[bk + 3 * sk] : 0.f);
-                vt[it] = make_float4(s < len ? ld_any(p.v, bv, p.dtype) : 0.f,
-                                     s + 1 < len ? ld_any(p.v, bv + sv, p.dtype) : 0.f,
-                                     s + 2 < len ? ld_any(p.v, bv + 2 * sv, p.dtype) : 0.f,
-                                     s + 3 < len ? ld_any(p.v, bv + 3 * sv, p.dtype) : 0.f);
+            for (int it = 0; it < RowsK::kItems; ++it) {
+                const int s = RowsK::row(it), k = RowsK::col(it);
+                kr[it] = s < len ? *reinterpret_cast<const float4*>(p.kn + ((size_t)(t0 + s) * p.HK + hk) * kD + k)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                vr[it] = s < len ? ld4_any(p.v, ((size_t)(t0 + s) * p.HV + h) * kD + k, p.dtype)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
             }
             // T = (I + A)^-1 by 16 x 16 blocks.  Diagonal blocks: column c by the 8 lanes tid / 8,
             // lane l holding T[16 b + jl + l + 8 m][c] (b = c / 16, jl = c % 16), rows in order,
@@ -1434,10 +1431,15 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_wy_tc_kernel(BwdParams p) {
             }
             __syncthreads();
 #pragma unroll
-            for (int it = 0; it < kItems; ++it) {
-                const int e = tid + it * kNTtc, jj = e % kD, s = (e / kD) * 4;
-                *reinterpret_cast<float4*>(sX + umma_koff(jj, s, kSboC)) = tf32_round4(kt[it]);
-                *reinterpret_cast<float4*>(sX + 32768 + umma_koff(jj, s, kSboC)) = tf32_round4(vt[it]);
+            for (int it = 0; it < RowsK::kItems; ++it) {
+                const int s = RowsK::row(it), k = RowsK::col(it);
+                const float kv[4] = {kr[it].x, kr[it].y, kr[it].z, kr[it].w};
+                const float vv[4] = {vr[it].x, vr[it].y, vr[it].z, vr[it].w};
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    *reinterpret_cast<float*>(sX + umma_koff(k + t, s, kSboC)) = tf32_round(kv[t]);
+                    *reinterpret_cast<float*>(sX + 32768 + umma_koff(k + t, s, kSboC)) = tf32_round(vv[t]);
+                }
             }
         }
         __syncthreads();
