@@ -537,6 +537,8 @@ __global__ void __launch_bounds__(kNTs) bwd_state_bwd_kernel(BwdParams p, int R)
 // gradient) stays in registers for the whole sequence.  The tensor core reads TF32-rounded
 // copies of every operand from shared memory in the K-major core-matrix layout of
 // gdn_umma.cuh; accumulators live in TMEM (columns [0, 64) and [128, 128 + dk)).
+// Every *_tc kernel runs exactly kNTtc threads per CTA: their thread-to-element mappings (16
+// warps = 4 TMEM lane quarters x 4 column groups, and the staging strides) assume it.
 constexpr int kNTtc = 512;
 // At dk = 128 the chunk states S_c and D_c go out transposed (dk x dv), the layout in which
 // bwd_intra_s_tc_kernel takes them as K-major operands; other dk keep the row-major layout.
