@@ -97,6 +97,49 @@ def test_fwd_host_validation(lib, case, expect):
     assert call_fwd(lib, s, [q, k, v, g, b, s0, cu, out, fs, ws], ws_bytes) == expect
 
 
+def call_bwd(lib, s, ptrs, ws_bytes):
+    P = ctypes.c_void_p
+    args = [P(p) if p else None for p in ptrs]
+    return lib.gdn_chunk_bwd(ctypes.byref(s), *args[:16], ctypes.c_size_t(ws_bytes), None)
+
+
+@pytest.mark.parametrize("case,expect", [
+    ("null_q", -1), ("null_cu", -1), ("null_dg", -1), ("misaligned_dq", -1), ("dq_aliases_q", -1),
+    ("dinit_aliases_init", -1), ("bad_dk", -2), ("bad_dtype", -2), ("hv_not_multiple", -1),
+    ("no_workspace", -3), ("small_workspace", -3), ("no_sequences", 0),
+])
+def test_bwd_host_validation(lib, case, expect):
+    """gdn_chunk_bwd rejects bad arguments before any CUDA call (N = 0 returns at once)."""
+    s = shape()
+    (q, k, v, g, b, s0, cu, dO, dsT, dq, dk, dv, dg, db, ds0, ws) = [FAKE + i * 0x1000 for i in range(16)]
+    ws_bytes = 1 << 20
+    if case == "null_q":
+        q = 0
+    elif case == "null_cu":
+        cu = 0
+    elif case == "null_dg":
+        dg = 0
+    elif case == "misaligned_dq":
+        dq += 4
+    elif case == "dq_aliases_q":
+        dq = q
+    elif case == "dinit_aliases_init":
+        ds0 = s0
+    elif case == "bad_dk":
+        s.dk = 96
+    elif case == "bad_dtype":
+        s.dtype = 7
+    elif case == "hv_not_multiple":
+        s.HV = 3
+    elif case == "no_workspace":
+        ws = 0
+    elif case == "small_workspace":
+        ws_bytes = 16
+    elif case == "no_sequences":
+        s.N, s.T_total = 0, 0
+    assert call_bwd(lib, s, [q, k, v, g, b, s0, cu, dO, dsT, dq, dk, dv, dg, db, ds0, ws], ws_bytes) == expect
+
+
 def test_decode_host_validation(lib):
     P = ctypes.c_void_p
     s = shape(N=4, T_total=4)
