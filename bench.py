@@ -226,7 +226,9 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"prefill sample: first {m} of 64 lognormal sequences ({tok} tokens), "
-                               f"HK=16 HV=32 dk=dv=128", "parallelism": "host threads"},
+                               f"HK=16 HV=32 dk=dv=128", "parallelism": "host threads",
+                   "note": f"tokens/s over a bounded sample ({tok} of the {cu[-1]} tokens the GPU arm runs per "
+                           f"step): the two arms time different token sets of the same workload"},
         "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
                          "sample": f"first {m} sequences, {tok} tokens per step"},
         "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -415,6 +417,7 @@ def main():
 
     if rank == 0 and not args.no_cpu_baseline and not small:
         result["cpu_baseline"] = oracle_sample_rate(d)
+        result["cpu_baseline"]["decode"] = oracle_decode_rate(dd.cpu(), st0.cpu())
 
     if rank == 0:
         print(json.dumps(result), flush=True)
@@ -460,6 +463,53 @@ def check_parity(x, out, fs):
     return {"units": [list(p) for p in picks], "max_normwise_rel_err": worst, "tol": 2e-3,
             "pass": worst < 2e-3 * (1 + 2.0 ** -8),
             "note": "bf16 out compared net of its 2^-8 output rounding; fp32 final state plain"}
+
+
+def check_bwd_parity(x, dO, grads, n=5, hk=9):
+    """One (sequence, k-head) group of the last timed gdn_chunk_bwd call against the
+    fp64 BPTT oracle: its G value heads' dv, dg, dbeta, d_init_state and the folded
+    dq, dk of the k-head, each as a normwise relative error (max |x - ref| / max |ref|)."""
+    import oracle
+    G = HV // HK
+    cu = x.cu_seqlens.tolist()
+    a, b = cu[n], cu[n + 1]
+    hs = slice(hk * G, (hk + 1) * G)
+    t0 = time.perf_counter()
+    ref = oracle.gdn_bwd(x.q[a:b, hk:hk + 1], x.k[a:b, hk:hk + 1], x.v[a:b, hs], x.g[a:b, hs], x.beta[a:b, hs],
+                         [0, b - a], dO[a:b, hs])
+    dt = time.perf_counter() - t0
+    mine = {"dq": grads["dq"][a:b, hk:hk + 1], "dk": grads["dk"][a:b, hk:hk + 1], "dv": grads["dv"][a:b, hs],
+            "dg": grads["dg"][a:b, hs], "dbeta": grads["dbeta"][a:b, hs]}
+    if grads.get("d_init_state") is not None:
+        mine["d_init_state"] = grads["d_init_state"][n:n + 1, hs]
+    errs = {k: normwise(v.float().cpu().numpy(), ref[k]) for k, v in mine.items()}
+    worst = max(errs.values())
+    return {"sequence": n, "k_head": hk, "value_heads": [hk * G, (hk + 1) * G - 1], "normwise_rel_err": errs,
+            "max": worst, "tol": 1e-2, "pass": worst < 1e-2, "oracle_seconds": dt}
+
+
+def oracle_decode_rate(dec, dec_state, seconds=4.0):
+    """fp64 oracle decode steps/s on the host cores: the whole batch-256 decode step
+    (one token per sequence from its cached state), repeated for about `seconds`."""
+    import oracle
+    B = dec.q.shape[0]
+    cu = list(range(B + 1))
+    st = dec_state
+
+    def one():
+        oracle.gdn_fwd(dec.q, dec.k, dec.v, dec.g, dec.beta, cu, init_state=st)
+
+    one()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        one()
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= seconds:
+            break
+    return {"value": n / dt, "unit": "steps/s", "tokens_per_s": n * B / dt, "cores": oracle.max_threads(),
+            "kind": "oracle", "sample": f"{n} whole decode steps at batch {B} (HV={HV}, dk=dv={DK}, random fp32 "
+                                        f"states), fp64 C recurrence, OpenMP over (sequence, head)", "seconds": dt}
 
 
 def e2e(gdn, x, dec, dec_state, dev, steps):
@@ -544,10 +594,28 @@ def e2e(gdn, x, dec, dec_state, dev, steps):
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
     tokens = x.q.shape[0] + dec.q.shape[0]
+    # the link on its own: one step's uploads, then its downloads, each alone on its stream
+    rate = {}
+    for name, fn, nbytes, strm in (("h2d", lambda: upload(0), h2d, up), ("d2h", None, d2h, down)):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(strm)
+        if fn is not None:
+            fn()
+        else:
+            with torch.cuda.stream(down):
+                sets[0]["out_h"].copy_(sets[0]["out"], non_blocking=True)
+                sets[0]["dout_h"].copy_(sets[0]["dout"], non_blocking=True)
+        e1.record(strm)
+        torch.cuda.synchronize()
+        rate[name] = nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9
     return {"value": tokens / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps,
+            "h2d_gbs_alone": rate["h2d"], "d2h_gbs_alone": rate["d2h"],
+            "h2d_gbs_in_step": h2d / (ms / 1e3) / 1e9,
+            "bound": "host link" if h2d / (rate["h2d"] * 1e9) * 1e3 > 0.8 * ms else "compute",
             "note": "pinned host buffers; uploads, compute and downloads of consecutive steps overlap on three "
-                    "streams (two device buffer sets)"}
+                    "streams (two device buffer sets); *_gbs_alone = one step's copies timed on their own"}
 
 
 def bench_snapshots(gdn, d, dev, ws, every=256, reps=3):
@@ -731,7 +799,9 @@ def bench_backward(gdn, dev, steps=3):
     dO = dO.to(dev)
     shape = gdn.make_shape(d.q, d.v, BWD_N)
     ws = torch.zeros(gdn.gdn_workspace_size(shape, 2), dtype=torch.uint8, device=dev)
-    run = lambda: gdn.gdn_chunk_bwd(d.q, d.k, d.v, d.g, d.beta, d.cu_seqlens, dO, workspace=ws)  # noqa: E731
+    grads = {}
+    run = lambda: grads.update(gdn.gdn_chunk_bwd(d.q, d.k, d.v, d.g, d.beta, d.cu_seqlens, dO,  # noqa: E731
+                                                 workspace=ws))
     for _ in range(2):
         run()
     torch.cuda.synchronize()
@@ -742,6 +812,7 @@ def bench_backward(gdn, dev, steps=3):
     b.record()
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
+    parity = check_bwd_parity(x, dO.cpu(), grads)
     T = x.q.shape[0]
     # Dense contraction work of the chunked backward per (chunk, head), C = 64, dk = dv = d:
     # the multiply-adds (M x N x K) of its 25 tensor-core products, grouped by kernel.
@@ -762,7 +833,7 @@ def bench_backward(gdn, dev, steps=3):
     tf32_peak = bf16 * (1.1 / 2.25)  # TF32 = the recipe's nominal tf32/bf16 ratio of the measured bf16 peak
     achieved = flops / (ms / 1e3) / 1e12
     return {"tokens_per_s": T / (ms / 1e3), "ms": ms, "workload": f"{BWD_N} x {BWD_L} tokens, HK={HK} HV={HV} "
-            f"dk=dv={DK}, bf16, chunk 64",
+            f"dk=dv={DK}, bf16, chunk 64", "parity": parity,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf32_peak, "unit": "TFLOP/s",
                          "frac": achieved / tf32_peak, "flops_per_chunk_head": 2 * macs,
                          "note": "TF32 with fp32 accumulate (bf16 inputs) on tcgen05 in every contracting kernel; "

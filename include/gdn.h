@@ -29,7 +29,8 @@
  * state and the workspace 16-byte aligned; g, beta, dg, dbeta, cu_seqlens and
  * state_indices 4-byte aligned.  The library allocates
  * no device memory; scratch comes from the caller's workspace, sized by
- * gdn_workspace_size.  All calls are asynchronous on `stream` (a
+ * gdn_workspace_size, except for gdn_recurrent_fwd_noalloc, whose scratch is
+ * a fixed array inside the library (described at that entry point).  All calls are asynchronous on `stream` (a
  * cudaStream_t; NULL = legacy default stream).  The return value reports
  * host-side validation and launch errors only; device faults surface at the
  * caller's next synchronisation.  No call throws.  Layouts:
@@ -132,7 +133,10 @@ gdn_status gdn_recurrent_fwd_snapshots(const gdn_shape* shape, const void* q, co
  * per sequence.  state is a pool [num_slots, HV, dv, dk]; sequence b uses
  * slot state_indices[b] (state_indices NULL: slot b, needs num_slots >= N).
  * A negative or out-of-range slot skips sequence b (its out row is left
- * untouched).  Bit-identical to continuing gdn_recurrent_fwd by one token.
+ * untouched).  The non-negative entries of state_indices must be distinct:
+ * the library does not check this, and two batch rows on one slot would read
+ * and write that slot at the same time (a race with an undefined result).
+ * Bit-identical to continuing gdn_recurrent_fwd by one token.
  * One launch, no workspace, no host synchronisation: capturable as-is.
  */
 gdn_status gdn_decode_step(const gdn_shape* shape, const void* q, const void* k, const void* v,
@@ -173,7 +177,10 @@ gdn_status gdn_chunk_bwd(const gdn_shape* shape, const void* q, const void* k, c
  * device that loads the library until the process exits).  Larger shapes
  * return GDN_ERR_WORKSPACE.  The first call on a device looks the array's
  * address up (cudaGetSymbolAddress, with that device current); make that
- * first call before any stream capture.  All calls share the array: calls
+ * first call before any stream capture.  The address is kept for the life of
+ * the process: after cudaDeviceReset on a device, do not call this entry
+ * point on that device again (the kept address may be stale).  All calls
+ * share the array: calls
  * that overlap on the GPU (on different streams, or from several threads)
  * race on it and must be serialised by the caller.  Its device error bits are
  * not readable through gdn_read_device_error.

@@ -290,8 +290,9 @@ __global__ void bwd_offsets_kernel(BwdParams p) {
 
 // one warp per (token, k-head): q^, k^ and the reciprocal norms
 __global__ void bwd_norm_kernel(BwdParams p) {
-    const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    if (w >= p.T * p.HK) return;
+    const long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (w >= (long long)p.T * p.HK) return;
     for (int which = 0; which < 2; ++which) {
         const void* src = which ? p.k : p.q;
         float x[4];
@@ -1984,9 +1985,10 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_intra_c_tc_kernel(BwdParams p) {
 
 // per (token, k-head): sum the G value heads in increasing order, then the L2-norm backward
 __global__ void bwd_fold_kernel(BwdParams p) {
-    const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    if (w >= p.T * p.HK) return;
-    const int t = w / p.HK, hk = w - t * p.HK;
+    const long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (w >= (long long)p.T * p.HK) return;
+    const int t = (int)(w / p.HK), hk = (int)(w - (long long)t * p.HK);
     // every load of a head step (dq and dk together) is issued before any is used; each element
     // still sums the heads in increasing order
     float dsum[2][4], x[2][4];
@@ -2158,8 +2160,8 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
     bwd_offsets_kernel<<<1, 32, 0, cs>>>(p);
     if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
     if (s->T_total > 0) {
-        const int vec = s->T_total * s->HK;
-        bwd_norm_kernel<<<(vec + 7) / 8, 256, 0, cs>>>(p);
+        const long long vec = (long long)s->T_total * s->HK;  // one warp each, 8 per CTA
+        bwd_norm_kernel<<<(unsigned)((vec + 7) / 8), 256, 0, cs>>>(p);
         if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
     }
     const dim3 gch(L.nchm, s->HV);
@@ -2214,8 +2216,8 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
     }
     if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
     if (s->T_total > 0) {
-        const int vec = s->T_total * s->HK;
-        bwd_fold_kernel<<<(vec + 7) / 8, 256, 0, cs>>>(p);
+        const long long vec = (long long)s->T_total * s->HK;  // one warp each, 8 per CTA
+        bwd_fold_kernel<<<(unsigned)((vec + 7) / 8), 256, 0, cs>>>(p);
         if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
     }
     return GDN_OK;

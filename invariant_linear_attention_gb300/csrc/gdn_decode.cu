@@ -13,6 +13,7 @@
 
 #include "gdn_host.h"
 #include "gdn_step.cuh"
+#include "gdn_token_step.cuh"
 
 namespace gdn {
 
@@ -29,16 +30,17 @@ struct DecodeParams {
 };
 
 template <typename Tin, int DK>
-__global__ void __launch_bounds__(kThreadsPer128Rows) gdn_decode_kernel(const DecodeParams p) {
-    constexpr int R = kRowsPerThread;
+__global__ void __launch_bounds__(ts::threads_for_rows<DK>(128)) gdn_decode_kernel(const DecodeParams p) {
+    constexpr int RG = 2;  // two slot groups: their reduce-scatters interleave (a decode step has one token)
+    using Y = ts::Layout<DK, RG>;
     __shared__ __align__(16) float qn[DK];
     __shared__ __align__(16) float kn[DK];
     __shared__ float2 ab;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-    const int e = tid % kLanesPerRow, grp = tid / kLanesPerRow;
+    const ts::Place pl = ts::place_of<DK, RG>(tid);
     const int dvs = p.dvs;
-    const bool active = grp * R < dvs;
+    const bool active = pl.grp * Y::R < dvs;
     const int unit = blockIdx.x;
     const int slice = unit % p.nslices;
     const int h = (unit / p.nslices) % p.HV;
@@ -47,10 +49,11 @@ __global__ void __launch_bounds__(kThreadsPer128Rows) gdn_decode_kernel(const De
     const int slot = p.idx ? p.idx[b] : b;
     if (slot < 0 || slot >= p.num_slots) return;  // uniform over the CTA
 
-    const int row = slice * dvs + grp * R;
+    const int row = slice * dvs + pl.grp * Y::R;
     float* srow = p.state + (((size_t)slot * p.HV + h) * p.dv + row) * DK;
-    RowFrag<DK> S[R];
-    if (active) load_rows<DK, R>(S, srow, e);
+    ts::Rows<DK> S;
+    if (active) ts::load_rows<DK, RG>(S, srow, pl);
+    else ts::zero_rows<DK>(S);
 
     const Tin* q = reinterpret_cast<const Tin*>(p.q) + ((size_t)b * p.HK + hk) * DK;
     const Tin* k = reinterpret_cast<const Tin*>(p.k) + ((size_t)b * p.HK + hk) * DK;
@@ -62,24 +65,28 @@ __global__ void __launch_bounds__(kThreadsPer128Rows) gdn_decode_kernel(const De
         const size_t gi = (size_t)b * p.HV + h;
         ab = make_float2(gate_alpha(p.g[gi]), p.beta[gi]);
     }
-    float vv[R], o[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) vv[r] = 0.f;
     const size_t vo = ((size_t)b * p.HV + h) * p.dv + row;
-    if (active) ld_rows_in<R>(reinterpret_cast<const Tin*>(p.v) + vo, vv);
+    const int lr0 = ts::row_of<DK, RG>(0, 0, pl.own), lr1 = ts::row_of<DK, RG>(1, 0, pl.own);
+    const Tin* v = reinterpret_cast<const Tin*>(p.v) + vo;
+    const float vown[2] = {active ? ld_in(v + lr0) : 0.f, active ? ld_in(v + lr1) : 0.f};
     __syncthreads();
     const float2 gab = ab;
-    token_step<DK, R>(S, kn, qn, e, gab.x, gab.y, vv, o);
+    float o[2];
+    ts::token_step<DK, RG>(S, kn, qn, pl, lane, gab.x, gab.y, vown, o);
     if (active) {
-        if (e == 0) st_rows_out<R>(reinterpret_cast<Tin*>(p.out) + vo, o);
-        store_rows<DK, R>(S, srow, e);
+        if (ts::stores_row<DK, RG>(pl)) {
+            Tin* out = reinterpret_cast<Tin*>(p.out) + vo;
+            st_in(out + lr0, o[0]);
+            st_in(out + lr1, o[1]);
+        }
+        ts::store_rows<DK, RG>(S, srow, pl);
     }
 }
 
 template <typename Tin, int DK>
 static gdn_status launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
     const int units = p.N * p.HV * p.nslices;
-    gdn_decode_kernel<Tin, DK><<<units, std::max(32, p.dvs * kLanesPerRow / kRowsPerThread), 0, stream>>>(p);
+    gdn_decode_kernel<Tin, DK><<<units, ts::threads_for_rows<DK>(p.dvs), 0, stream>>>(p);
     return launch_status();
 }
 

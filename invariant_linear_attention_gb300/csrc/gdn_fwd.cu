@@ -22,6 +22,7 @@
 #include "gdn_async.cuh"
 #include "gdn_host.h"
 #include "gdn_step.cuh"
+#include "gdn_token_step.cuh"
 
 namespace gdn {
 
@@ -121,18 +122,20 @@ __device__ __forceinline__ void issue_chunk(FwdSmem<Tin, DK>& sm, const CUtensor
 
 // ---------------------------------------------------------------------------
 template <typename Tin, int DK, typename Prm>
-__global__ void __launch_bounds__(kThreadsPer128Rows, 2)
+__global__ void __launch_bounds__(ts::threads_for_rows<DK>(kMaxSlice), 2)
     gdn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const Prm p) {
-    constexpr int R = kRowsPerThread;
+    constexpr int RG = 4;  // one slot group: one reduce-scatter over all four rows of a thread
+    using Y = ts::Layout<DK, RG>;
     extern __shared__ unsigned char smem_raw[];
     FwdSmem<Tin, DK>& sm =
         *reinterpret_cast<FwdSmem<Tin, DK>*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-    const int e = tid % kLanesPerRow, grp = tid / kLanesPerRow;  // lane within the row, row group
+    const ts::Place pl = ts::place_of<DK, RG>(tid);
     const int dvs = p.dvs;
-    const bool active = grp * R < dvs;
+    const bool active = pl.grp * Y::R < dvs;
+    const bool storer = active && ts::stores_row<DK, RG>(pl);
 
     const int unit = p.work[blockIdx.x];
     const int slice = unit % p.nslices;
@@ -143,12 +146,13 @@ __global__ void __launch_bounds__(kThreadsPer128Rows, 2)
     bos = min(max(bos, 0), p.T);
     eos = min(max(eos, bos), p.T);
     const int L = eos - bos;
-    const int row = slice * dvs + grp * R;  // first of this thread's rows
+    const int row = slice * dvs + pl.grp * Y::R;  // first row of this thread's group
+    const int orow = row + pl.own;                 // the row whose output this thread may store
     const size_t soff = (((size_t)n * p.HV + h) * p.dv + row) * DK;
 
-    RowFrag<DK> S[R];
-    if (active && p.init_state) load_rows<DK, R>(S, p.init_state + soff, e);
-    else zero_rows<DK, R>(S);
+    ts::Rows<DK> S;
+    if (active && p.init_state) ts::load_rows<DK, RG>(S, p.init_state + soff, pl);
+    else ts::zero_rows<DK>(S);
 
     if (L > 0) {
         const int nchunks = (L + kTC - 1) / kTC;
@@ -194,47 +198,46 @@ __global__ void __launch_bounds__(kThreadsPer128Rows, 2)
             if (tid < tc) sm.ab[tid] = make_float2(gate_alpha(gb.x), gb.y);
             __syncthreads();
             if (sm.abort_flag) {
-                if (tid == 0) atomicOr(p.err, GDN_DEVERR_TIMEOUT);
+                if (tid == 0) {
+                    atomicOr(p.err, GDN_DEVERR_TIMEOUT);
+                    // leave no bulk copy of this CTA in flight into shared memory that a later
+                    // CTA may own: wait (bounded again) for this chunk's stage and the next one's
+                    mbar_wait_bounded(&sm.bar[st], (uint32_t)((c / kStages) & 1));
+                    if (c + 1 < nchunks)
+                        mbar_wait_bounded(&sm.bar[(c + 1) % kStages], (uint32_t)(((c + 1) / kStages) & 1));
+                }
                 return;
             }
             if (c + 1 < nchunks && tid < min(kTC, eos - (t0 + kTC))) {
                 const size_t gi = (size_t)(t0 + kTC + tid) * p.HV + h;
                 gb = make_float2(p.g[gi], p.beta[gi]);
             }
-            const Tin* __restrict__ vs = sm.v[st];
-            // Token loop, software-pipelined by one token: the lane butterfly of
-            // token t's output runs next to token t+1's u butterfly (it is off
+            const Tin* __restrict__ vs = sm.v[st] + pl.grp * Y::R + pl.own;
+            // Token loop, software-pipelined by one token: the reduce-scatter of
+            // token t's output runs next to token t+1's u reduction (it is off
             // the recurrence's critical path); every operation is unchanged.
-            float opend[R];
+            float op[RG];
             for (int t = 0; t < tc; ++t) {
                 const float2 ab = sm.ab[t];
-                float vv[R], u[R], w[R], oprev[R];
-#pragma unroll
-                for (int r = 0; r < R; ++r) vv[r] = 0.f;
-                if (active) ld_rows_in<R>(vs + t * dvs + grp * R, vv);
-                rows_dot_part<DK, R>(S, sm.kn + t * DK, e, u);
-                if (t > 0) {
-#pragma unroll
-                    for (int r = 0; r < R; ++r) oprev[r] = lanes_reduce(opend[r]);
-                }
-#pragma unroll
-                for (int r = 0; r < R; ++r) u[r] = lanes_reduce(u[r]);
-                if (t > 0 && active && e == 0)
-                    st_rows_out<R>(out + ((size_t)(t0 + t - 1) * p.HV + h) * p.dv + row, oprev);
-#pragma unroll
-                for (int r = 0; r < R; ++r) w[r] = delta_w(ab.x, ab.y, vv[r], u[r]);
-                rows_update_part<DK, R>(S, sm.kn + t * DK, sm.qn + t * DK, e, ab.x, w, opend);
+                const float vown = active ? ld_in(vs + t * dvs) : 0.f;
+                float up[RG], w[RG];
+                ts::dot_part<DK, RG, 0>(S, sm.kn + t * DK, pl.e, up);
+                float oprev = 0.f;
+                if (t > 0) oprev = ts::reduce_scatter<DK, RG>(op);
+                const float u = ts::reduce_scatter<DK, RG>(up);
+                if (t > 0 && storer) st_in(out + ((size_t)(t0 + t - 1) * p.HV + h) * p.dv + orow, oprev);
+                ts::gather_rows<DK, RG>(ts::delta_w(ab.x, ab.y, vown, u), lane, pl.own, w);
+                ts::update_part<DK, RG, 0>(S, sm.kn + t * DK, sm.qn + t * DK, pl.e, ab.x, w, op);
             }
-#pragma unroll
-            for (int r = 0; r < R; ++r) opend[r] = lanes_reduce(opend[r]);
-            if (active && e == 0) st_rows_out<R>(out + ((size_t)(t0 + tc - 1) * p.HV + h) * p.dv + row, opend);
+            const float olast = ts::reduce_scatter<DK, RG>(op);
+            if (storer) st_in(out + ((size_t)(t0 + tc - 1) * p.HV + h) * p.dv + orow, olast);
             if constexpr (std::is_same<Prm, SnapParams>::value) {
                 // the state after `done` tokens of this sequence, at every snap_every-th token
                 const int done = t0 + tc - bos;
                 if (done % p.snap_every == 0) {
                     const int slot = p.snap_cu[n] + done / p.snap_every - 1;
                     if (active && slot >= 0 && slot < p.snap_cu[n + 1] && slot < p.snap_slots)
-                        store_rows<DK, R>(S, p.snap + (((size_t)slot * p.HV + h) * p.dv + row) * DK, e);
+                        ts::store_rows<DK, RG>(S, p.snap + (((size_t)slot * p.HV + h) * p.dv + row) * DK, pl);
                 }
             }
             __syncthreads();
@@ -242,7 +245,7 @@ __global__ void __launch_bounds__(kThreadsPer128Rows, 2)
                 issue_chunk(sm, &tm_q, &tm_k, &tm_v, c + kStages, bos, hk, h, slice * dvs, bytes);
         }
     }
-    if (active && p.final_state) store_rows<DK, R>(S, p.final_state + soff, e);
+    if (active && p.final_state) ts::store_rows<DK, RG>(S, p.final_state + soff, pl);
 }
 
 template <typename Tin, int DK, typename Prm>
@@ -252,7 +255,7 @@ static gdn_status launch_fwd_t(const CUtensorMap& mq, const CUtensorMap& mk, con
     auto kern = gdn_fwd_kernel<Tin, DK, Prm>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return GDN_ERR_CUDA;
-    const int nt = std::max(32, p.dvs * kLanesPerRow / kRowsPerThread);
+    const int nt = ts::threads_for_rows<DK>(p.dvs);
     kern<<<units, nt, smem, stream>>>(mq, mk, mv, p);
     return launch_status();
 }
@@ -411,7 +414,9 @@ constexpr int kStaticHeaderWords = 64;   // 256 bytes: word 0 is the error word
 static __device__ __align__(256) int32_t g_fwd_static_scratch[kStaticHeaderWords + kStaticUnits];
 
 // Device address of the array on the current device, looked up once per device
-// (with that device current) and cached.  nullptr if the lookup fails.
+// (with that device current) and cached for the life of the process; a
+// cudaDeviceReset of that device invalidates it (the header says so).
+// nullptr if the lookup fails.
 static int32_t* static_scratch_on_current_device() {
     constexpr int kMaxDevices = 64;
     static std::mutex mu;

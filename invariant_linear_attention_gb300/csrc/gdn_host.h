@@ -26,8 +26,10 @@ inline gdn_status check_shape(const gdn_shape* s) {
     if (s->dtype != GDN_F32 && s->dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
     if (!dim_ok(s->dk) || !dim_ok(s->dv)) return GDN_ERR_UNSUPPORTED;
     if (s->dv_slice != 0 && (!dim_ok(s->dv_slice) || s->dv_slice > s->dv)) return GDN_ERR_UNSUPPORTED;
-    // element counts must fit the 32-bit token/head index arithmetic used on the device
-    if ((long long)s->T_total * s->HV * (s->dk > s->dv ? s->dk : s->dv) >= (1LL << 40)) return GDN_ERR_UNSUPPORTED;
+    // The kernels index (token, head) pairs and work units with 32-bit integers and
+    // elements with 64-bit offsets: T_total * HV (>= T_total * HK) and the unit count
+    // N * HV * (dv / 16) must stay below 2^31.
+    if ((long long)s->T_total * s->HV >= (1LL << 31)) return GDN_ERR_UNSUPPORTED;
     if ((long long)s->N * s->HV * (s->dv / 16) >= (1LL << 31)) return GDN_ERR_UNSUPPORTED;
     return GDN_OK;
 }

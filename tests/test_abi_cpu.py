@@ -68,7 +68,7 @@ FAKE = 0x10000  # never dereferenced: every case below fails validation first
 @pytest.mark.parametrize("case,expect", [
     ("null_q", -1), ("null_cu", -1), ("misaligned_v", -1), ("out_aliases_q", -1),
     ("bad_dk", -2), ("bad_dtype", -2), ("bad_slice", -2), ("hv_not_multiple", -1),
-    ("no_workspace", -3), ("small_workspace", -3),
+    ("no_workspace", -3), ("small_workspace", -3), ("token_head_index_over_32_bits", -2),
 ])
 def test_fwd_host_validation(lib, case, expect):
     s = shape()
@@ -94,6 +94,8 @@ def test_fwd_host_validation(lib, case, expect):
         ws = 0
     elif case == "small_workspace":
         ws_bytes = 16
+    elif case == "token_head_index_over_32_bits":
+        s.T_total, s.HV = 1 << 26, 32  # T_total * HV = 2^31
     assert call_fwd(lib, s, [q, k, v, g, b, s0, cu, out, fs, ws], ws_bytes) == expect
 
 
@@ -106,7 +108,7 @@ def call_bwd(lib, s, ptrs, ws_bytes):
 @pytest.mark.parametrize("case,expect", [
     ("null_q", -1), ("null_cu", -1), ("null_dg", -1), ("misaligned_dq", -1), ("dq_aliases_q", -1),
     ("dinit_aliases_init", -1), ("bad_dk", -2), ("bad_dtype", -2), ("hv_not_multiple", -1),
-    ("no_workspace", -3), ("small_workspace", -3), ("no_sequences", 0),
+    ("no_workspace", -3), ("small_workspace", -3), ("no_sequences", 0), ("token_head_index_over_32_bits", -2),
 ])
 def test_bwd_host_validation(lib, case, expect):
     """gdn_chunk_bwd rejects bad arguments before any CUDA call (N = 0 returns at once)."""
@@ -137,6 +139,8 @@ def test_bwd_host_validation(lib, case, expect):
         ws_bytes = 16
     elif case == "no_sequences":
         s.N, s.T_total = 0, 0
+    elif case == "token_head_index_over_32_bits":
+        s.T_total, s.HV = 1 << 26, 32  # T_total * HV = 2^31
     assert call_bwd(lib, s, [q, k, v, g, b, s0, cu, dO, dsT, dq, dk, dv, dg, db, ds0, ws], ws_bytes) == expect
 
 
