@@ -9,11 +9,11 @@
  *     S_t  = a_t S_{t-1} (I - b_t k^_t k^_t^T) + b_t v_t k^_t^T (S: dv x dk, fp32)
  *     o_t  = S_t q^_t                                           (read after the update)
  *
- * This is the gated delta rule that "Defending Against the Training-Inference
- * Numeric Mismatch in RL (Especially Linear Attention)" (section 3.2) runs
- * with ONE recurrent kernel for the trainer's forward, the generator's
- * prefill and its decode, over an fp32 state cache (section 4.2 setup
- * tables), and with a chunked kernel for the backward only.
+ * This is the gated delta rule of "Defending Against the Training-Inference
+ * Numeric Mismatch in RL (Especially Linear Attention)" (section 3.2): one
+ * recurrent kernel serves the RL trainer's forward pass and the rollout
+ * engine's prefill and decode alike, the state cache is fp32 (section 4.2
+ * setup tables), and the chunked form is kept for gradients only.
  *
  * Invariance contract.  The bits of o and of the final state of a sequence
  * depend only on that sequence's own inputs: not on which other sequences
@@ -102,11 +102,11 @@ gdn_status gdn_recurrent_fwd(const gdn_shape* shape, const void* q, const void* 
                              void* stream);
 
 /*
- * gdn_recurrent_fwd that also keeps state snapshots for prefix caching (the
- * pages reuse vLLM's state snapshotting under --mamba-cache-mode align so that
- * prefix caching keeps working with the recurrent kernel: "Defending Against
- * the Training-Inference Numeric Mismatch in RL (Especially Linear
- * Attention)", section 3.2).  For every sequence n, after each snap_every-th
+ * gdn_recurrent_fwd that also keeps state snapshots for prefix caching (on
+ * the pages, vLLM's --mamba-cache-mode align snapshots keep prefix caching
+ * working once every path runs the recurrent kernel: "Defending Against the
+ * Training-Inference Numeric Mismatch in RL (Especially Linear Attention)",
+ * section 3.2).  For every sequence n, after each snap_every-th
  * token of that sequence (token counts snap_every, 2*snap_every, ...), the
  * fp32 state is written to snap_states[snap_cu[n] + m - 1] for the m-th
  * snapshot, as long as that slot is below snap_cu[n + 1] and num_snap_slots;

@@ -1,8 +1,8 @@
 // gdn_bwd.cu -- chunked (WY-form) backward of the gated delta rule.
 //
-// The pages keep the chunked kernel for the backward only, where batch
-// invariance does not matter ("Defending Against the Training-Inference
-// Numeric Mismatch in RL (Especially Linear Attention)", section 3.2).  The
+// On the pages the chunked form is used only for gradients, which need no
+// batch invariance ("Defending Against the Training-Inference Numeric
+// Mismatch in RL (Especially Linear Attention)", section 3.2).  The
 // chunk form used here (chunk C = 64 tokens, restarting at every sequence
 // start, last chunk partial) is the WY / UT representation of the delta rule
 // (Yang et al. 2024; Gated Delta Networks, ICLR 2025).  Within a chunk with

@@ -1,11 +1,11 @@
 // gdn_decode.cu -- one decode token per sequence on a cached fp32 state.
 //
-// The same recurrent step as the prefill kernel (gdn_step.cuh), applied once
-// to the state the cache holds, so a prompt run by gdn_recurrent_fwd and
+// The same recurrent step as the prefill kernel (gdn_token_step.cuh), applied
+// once to the state the cache holds, so a prompt run by gdn_recurrent_fwd and
 // continued token by token here yields exactly the bits of one pass over the
-// whole sequence ("switch both prefill and decode to the recurrent kernel":
-// "Defending Against the Training-Inference Numeric Mismatch in RL
-// (Especially Linear Attention)", section 3.2).  The state round trip
+// whole sequence: the page "Defending Against the Training-Inference Numeric
+// Mismatch in RL (Especially Linear Attention)", section 3.2, gets its
+// prefill/decode parity by running one recurrent kernel for both.  The state round trip
 // (dv x dk fp32 read and written per (sequence, head)) makes this HBM-bound:
 // each thread issues all of its row loads up front, the q/k normalisation
 // runs while they are in flight, and the new rows are streamed back.
@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(ts::threads_for_rows<DK>(128)) gdn_decode_kern
     __syncthreads();
     const float2 gab = ab;
     float o[2];
-    ts::token_step<DK, RG>(S, kn, qn, pl, lane, gab.x, gab.y, vown, o);
+    ts::token_step<DK, RG>(S, kn, qn, pl, gab.x, gab.y, vown, o);
     if (active) {
         if (ts::stores_row<DK, RG>(pl)) {
             Tin* out = reinterpret_cast<Tin*>(p.out) + vo;

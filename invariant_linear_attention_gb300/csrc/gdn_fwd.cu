@@ -1,20 +1,28 @@
 // gdn_fwd.cu -- varlen scheduler + batch-invariant recurrent forward.
 //
-// One CTA owns one unit (sequence n, value head h, slice of dv rows) for the
-// whole sequence: its rows of the fp32 state S stay in registers from the
-// first token to the last, so there is no state hand-off between CTAs and
-// nothing is reduced across sequences or split over dk ("the recurrent kernel
-// reads only that sequence's own state and walks that sequence's tokens in a
-// fixed order": "Defending Against the Training-Inference Numeric Mismatch in
-// RL (Especially Linear Attention)", section 3.2).
+// One CTA owns one unit (sequence n, value head h, a slice of the dv rows of
+// S) for the whole sequence: its rows of the fp32 state stay in registers from
+// the first token to the last, so no state passes between CTAs and nothing is
+// reduced across sequences or split over dk.  This is the property the
+// recurrent kernel of "Defending Against the Training-Inference Numeric
+// Mismatch in RL (Especially Linear Attention)", section 3.2, relies on for
+// batch invariance: each sequence's state sees only its own tokens, in order.
 //
-// Per chunk of TC tokens, thread 0 streams q/k (k-head hk) and the v slice
+// Per chunk of TC tokens, thread 0 streams q/k (k-head hk) and the v rows
 // with three TMA tensor copies into a double-buffered shared-memory stage.
 // The CTA then L2-normalises q and k (one warp per vector, fixed butterfly),
 // computes a = exp(g), and every thread walks the chunk's tokens over its
-// rows with the shared step of gdn_step.cuh (row layout over lanes and rows
-// per thread as defined there).  Outputs go straight from registers to
-// global memory.  Two units share an SM.
+// rows with the shared step of gdn_token_step.cuh.  Outputs go straight from
+// registers to global memory.  Two CTAs share an SM.
+//
+// Slices.  By default a unit is a whole head (dv rows, 4 rows per thread).
+// The scheduler gives a long sequence's heads 2 or 4 slices of dv/2 or dv/4
+// rows (2 or 1 rows per thread, same CTA size) when the sequence is more than
+// 1.5 or 3 times the average work per CTA slot: its chains then run on more
+// SMs at once, with fewer rows each.  A row's operations do not depend on the rows
+// per thread (the tree of gdn_token_step.cuh is the same for every slot
+// grouping), so slicing never changes a bit.  A caller-forced dv_slice gives
+// every head that many uniform slices instead.
 #include <algorithm>
 #include <mutex>
 #include <type_traits>
@@ -40,10 +48,14 @@ struct FwdParams {
     const int32_t* cu;
     void* out;
     float* final_state;
-    const int32_t* work;
+    const int32_t* work;   // work items, longest sequence first (fwd_sched_kernel)
+    const int32_t* nwork;  // how many there are
     unsigned* err;
-    int N, T, HV, G, dv, dvs, nslices, use_norm;
-    int tb;  // tokens per TMA box: min(kTC, T)
+    int N, T, HV, G, dv, use_norm;
+    int rows4;   // rows of a unit at 4 rows per thread: dv, or the forced dv_slice
+    int forced;  // 1: the caller fixed dv_slice (uniform slices), 0: automatic slices
+    int vw;      // v columns per TMA box: dv (automatic) or dv_slice (forced)
+    int tb;      // tokens per TMA box: min(kTC, T)
 };
 
 // Parameters of the snapshot-taking forward: the plain forward's, plus where
@@ -108,6 +120,76 @@ __global__ void gdn_sched_kernel(const int32_t* __restrict__ cu, int N, int T, i
     }
 }
 
+// Work item of the forward: (n * HV + h) << 5 | (first row / 16) << 2 | log2(rows per thread).
+__host__ __device__ constexpr int32_t fwd_item(int nh, int row0, int rlog) {
+    return (int32_t)((nh << 5) | ((row0 >> 4) << 2) | rlog);
+}
+
+// Slices of each head of a sequence of length len: forced_ns when the caller
+// fixed dv_slice; otherwise, when splitting is allowed, 2 if the sequence is
+// longer than 1.5 times the average work per CTA slot (T * HV / slots) and 4
+// if longer than 3 times it, else 1.  Below 1.5 the whole heads already
+// balance: a sliced head does the same work with more shared-memory traffic
+// per FMA (fewer rows per thread), which only pays when it frees idle SMs.
+__device__ __forceinline__ int fwd_slices(int len, int forced_ns, int split, int slots, long long work) {
+    if (forced_ns > 0) return forced_ns;
+    if (!split) return 1;
+    const long long l = (long long)len * slots;
+    return l > 3 * work ? 4 : (2 * l > 3 * work ? 2 : 1);
+}
+
+// The forward's varlen scheduler: ranks sequences by length (longest first,
+// ties by index: a stable order), gives each the slice count above, and writes
+// every (sequence, head, slice) work item in rank order, so the hardware's
+// in-order CTA dispatch runs the longest chains first (LPT).  *nwork gets the
+// item count.  Validates cu_seqlens into the error word.  Neither the order
+// nor the slicing changes a bit.  With valid cu_seqlens the items fit the
+// host's bound `cap`; items past it (possible only for malformed cu_seqlens,
+// whose clamped lengths may add up to more than T) are not written.
+__global__ void fwd_sched_kernel(const int32_t* __restrict__ cu, int N, int T, int HV, int dv, int forced_ns,
+                                 int split, int slots, long long cap, int32_t* __restrict__ work,
+                                 int32_t* __restrict__ nwork, unsigned* __restrict__ err) {
+    constexpr int kTile = 1024;
+    __shared__ int lens[kTile];
+    const long long total = (long long)T * HV;
+    const int n = blockIdx.x * blockDim.x + threadIdx.x;
+    int my_len = 0;
+    if (n < N) {
+        const int a = cu[n], b = cu[n + 1];
+        if ((n == 0 && a != 0) || b < a || (n == N - 1 && b != T)) atomicOr(err, GDN_DEVERR_CU_SEQLENS);
+        const int lo = min(max(a, 0), T), hi = min(max(b, lo), T);
+        my_len = hi - lo;
+    }
+    long long offset = 0;
+    for (int base = 0; base < N; base += kTile) {
+        __syncthreads();
+        for (int i = threadIdx.x; i < kTile && base + i < N; i += blockDim.x) {
+            const int a = cu[base + i], b = cu[base + i + 1];
+            const int lo = min(max(a, 0), T), hi = min(max(b, lo), T);
+            lens[i] = hi - lo;
+        }
+        __syncthreads();
+        if (n < N) {
+            const int cnt = min(kTile, N - base);
+            for (int i = 0; i < cnt; ++i) {
+                const int lm = lens[i], m = base + i;
+                if ((lm > my_len) || (lm == my_len && m < n))
+                    offset += (long long)HV * fwd_slices(lm, forced_ns, split, slots, total);
+            }
+        }
+    }
+    if (n < N) {
+        const int ns = fwd_slices(my_len, forced_ns, split, slots, total);
+        const int rows = dv / ns, rlog = forced_ns > 0 ? 2 : (ns == 4 ? 0 : (ns == 2 ? 1 : 2));
+        for (int h = 0; h < HV; ++h)
+            for (int sl = 0; sl < ns; ++sl) {
+                const long long idx = offset + (long long)h * ns + sl;
+                if (idx < cap) work[idx] = fwd_item(n * HV + h, sl * rows, rlog);
+            }
+        atomicAdd(nwork, HV * ns);
+    }
+}
+
 // Thread 0: start the three TMA copies of chunk c into stage c % kStages.
 template <typename Tin, int DK>
 __device__ __forceinline__ void issue_chunk(FwdSmem<Tin, DK>& sm, const CUtensorMap* tq, const CUtensorMap* tk,
@@ -121,42 +203,36 @@ __device__ __forceinline__ void issue_chunk(FwdSmem<Tin, DK>& sm, const CUtensor
 }
 
 // ---------------------------------------------------------------------------
-template <typename Tin, int DK, typename Prm>
-__global__ void __launch_bounds__(ts::threads_for_rows<DK>(kMaxSlice), 2)
-    gdn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const Prm p) {
-    constexpr int RG = 4;  // one slot group: one reduce-scatter over all four rows of a thread
-    using Y = ts::Layout<DK, RG>;
-    extern __shared__ unsigned char smem_raw[];
-    FwdSmem<Tin, DK>& sm =
-        *reinterpret_cast<FwdSmem<Tin, DK>*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-
+// One unit (sequence n, head h, rows row0 .. row0 + rows - 1) with R rows per
+// thread, all of them in one slot group of gdn_token_step.cuh.
+template <typename Tin, int DK, typename Prm, int R>
+__device__ __forceinline__ void fwd_unit(FwdSmem<Tin, DK>& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                                         const CUtensorMap* tm_v, const Prm& p, int n, int h, int row0) {
+    using Y = ts::Layout<DK, R, R>;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-    const ts::Place pl = ts::place_of<DK, RG>(tid);
-    const int dvs = p.dvs;
-    const bool active = pl.grp * Y::R < dvs;
-    const bool storer = active && ts::stores_row<DK, RG>(pl);
-
-    const int unit = p.work[blockIdx.x];
-    const int slice = unit % p.nslices;
-    const int h = (unit / p.nslices) % p.HV;
-    const int n = unit / (p.nslices * p.HV);
+    const ts::Place pl = ts::place_of<DK, R>(tid);
+    const int rows = p.rows4 * R / 4;
+    // every thread holds rows unless a warp spans more rows than the smallest unit (16 rows)
+    constexpr bool kAllActive = 32 * R / Y::L <= 16;
+    const bool active = kAllActive || pl.grp * R < rows;
+    const bool storer = active && ts::stores_row<DK, R>(pl);
     const int hk = h / p.G;
+    const int vcol = p.forced ? row0 : 0;  // first v column of the TMA box
     int bos = p.cu[n], eos = p.cu[n + 1];
     bos = min(max(bos, 0), p.T);
     eos = min(max(eos, bos), p.T);
     const int L = eos - bos;
-    const int row = slice * dvs + pl.grp * Y::R;  // first row of this thread's group
-    const int orow = row + pl.own;                 // the row whose output this thread may store
+    const int row = row0 + pl.grp * R;  // first row of this thread's group
+    const int orow = row + pl.own;      // the row whose output this thread may store
     const size_t soff = (((size_t)n * p.HV + h) * p.dv + row) * DK;
 
     ts::Rows<DK> S;
-    if (active && p.init_state) ts::load_rows<DK, RG>(S, p.init_state + soff, pl);
+    if (active && p.init_state) ts::load_rows<DK, R, R>(S, p.init_state + soff, pl);
     else ts::zero_rows<DK>(S);
 
     if (L > 0) {
         const int nchunks = (L + kTC - 1) / kTC;
-        const uint32_t bytes = (uint32_t)((2 * p.tb * DK + p.tb * dvs) * sizeof(Tin));
+        const uint32_t bytes = (uint32_t)((2 * p.tb * DK + p.tb * p.vw) * sizeof(Tin));
         if (tid == 0) {
             for (int s = 0; s < kStages; ++s) mbar_init(&sm.bar[s], 1);
             sm.abort_flag = 0;
@@ -165,7 +241,7 @@ __global__ void __launch_bounds__(ts::threads_for_rows<DK>(kMaxSlice), 2)
         __syncthreads();
         if (tid == 0)
             for (int c = 0; c < min(kStages, nchunks); ++c)
-                issue_chunk(sm, &tm_q, &tm_k, &tm_v, c, bos, hk, h, slice * dvs, bytes);
+                issue_chunk(sm, tm_q, tm_k, tm_v, c, bos, hk, h, vcol, bytes);
 
         // gate inputs of the next chunk, prefetched into registers one chunk ahead
         float2 gb = make_float2(0.f, 0.f);
@@ -212,62 +288,82 @@ __global__ void __launch_bounds__(ts::threads_for_rows<DK>(kMaxSlice), 2)
                 const size_t gi = (size_t)(t0 + kTC + tid) * p.HV + h;
                 gb = make_float2(p.g[gi], p.beta[gi]);
             }
-            const Tin* __restrict__ vs = sm.v[st] + pl.grp * Y::R + pl.own;
+            const Tin* __restrict__ vs = sm.v[st] + (orow - vcol);
             // Token loop, software-pipelined by one token: the reduce-scatter of
             // token t's output runs next to token t+1's u reduction (it is off
             // the recurrence's critical path); every operation is unchanged.
-            float op[RG];
+            float op[R];
+#pragma unroll
+            for (int j = 0; j < R; ++j) op[j] = 0.f;
+            Tin* __restrict__ orow_ptr = out + ((size_t)t0 * p.HV + h) * p.dv + orow;  // token t0's output row
+            const size_t ostride = (size_t)p.HV * p.dv;
             for (int t = 0; t < tc; ++t) {
                 const float2 ab = sm.ab[t];
-                const float vown = active ? ld_in(vs + t * dvs) : 0.f;
-                float up[RG], w[RG];
-                ts::dot_part<DK, RG, 0>(S, sm.kn + t * DK, pl.e, up);
-                float oprev = 0.f;
-                if (t > 0) oprev = ts::reduce_scatter<DK, RG>(op);
-                const float u = ts::reduce_scatter<DK, RG>(up);
-                if (t > 0 && storer) st_in(out + ((size_t)(t0 + t - 1) * p.HV + h) * p.dv + orow, oprev);
-                ts::gather_rows<DK, RG>(ts::delta_w(ab.x, ab.y, vown, u), lane, pl.own, w);
-                ts::update_part<DK, RG, 0>(S, sm.kn + t * DK, sm.qn + t * DK, pl.e, ab.x, w, op);
+                const float abt = __fmul_rn(ab.x, ab.y);
+                const float bv = __fmul_rn(ab.y, active ? ld_in(vs + t * p.vw) : 0.f);
+                float up[R], w[R];
+                ts::dot_part<DK, R, 0>(S, sm.kn + t * DK, pl.e, up);
+                const float oprev = ts::reduce_scatter<DK, R>(op);  // token t - 1's output (t > 0)
+                const float u = ts::reduce_scatter<DK, R>(up);
+                if (t > 0 && storer) st_in(orow_ptr + (t - 1) * ostride, oprev);
+                ts::gather_rows<DK, R>(ts::delta_w(abt, bv, u), w);
+                ts::update_part<DK, R, 0>(S, sm.kn + t * DK, sm.qn + t * DK, pl.e, ab.x, w, op);
             }
-            const float olast = ts::reduce_scatter<DK, RG>(op);
-            if (storer) st_in(out + ((size_t)(t0 + tc - 1) * p.HV + h) * p.dv + orow, olast);
+            const float olast = ts::reduce_scatter<DK, R>(op);
+            if (storer) st_in(orow_ptr + (tc - 1) * ostride, olast);
             if constexpr (std::is_same<Prm, SnapParams>::value) {
                 // the state after `done` tokens of this sequence, at every snap_every-th token
                 const int done = t0 + tc - bos;
                 if (done % p.snap_every == 0) {
                     const int slot = p.snap_cu[n] + done / p.snap_every - 1;
                     if (active && slot >= 0 && slot < p.snap_cu[n + 1] && slot < p.snap_slots)
-                        ts::store_rows<DK, RG>(S, p.snap + (((size_t)slot * p.HV + h) * p.dv + row) * DK, pl);
+                        ts::store_rows<DK, R, R>(S, p.snap + (((size_t)slot * p.HV + h) * p.dv + row) * DK, pl);
                 }
             }
             __syncthreads();
             if (tid == 0 && c + kStages < nchunks)
-                issue_chunk(sm, &tm_q, &tm_k, &tm_v, c + kStages, bos, hk, h, slice * dvs, bytes);
+                issue_chunk(sm, tm_q, tm_k, tm_v, c + kStages, bos, hk, h, vcol, bytes);
         }
     }
-    if (active && p.final_state) ts::store_rows<DK, RG>(S, p.final_state + soff, pl);
+    if (active && p.final_state) ts::store_rows<DK, R, R>(S, p.final_state + soff, pl);
+}
+
+// The grid is an upper bound on the number of work items; the CTAs past it exit.
+template <typename Tin, int DK, typename Prm>
+__global__ void __launch_bounds__(ts::threads_for_rows<DK>(kMaxSlice), 2)
+    gdn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const Prm p) {
+    if ((int)blockIdx.x >= *p.nwork) return;
+    extern __shared__ unsigned char smem_raw[];
+    FwdSmem<Tin, DK>& sm =
+        *reinterpret_cast<FwdSmem<Tin, DK>*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    const int item = p.work[blockIdx.x];
+    const int nh = item >> 5, row0 = ((item >> 2) & 7) << 4, rlog = item & 3;
+    const int h = nh % p.HV, n = nh / p.HV;
+    if (rlog == 2) fwd_unit<Tin, DK, Prm, 4>(sm, &tm_q, &tm_k, &tm_v, p, n, h, row0);
+    else if (rlog == 1) fwd_unit<Tin, DK, Prm, 2>(sm, &tm_q, &tm_k, &tm_v, p, n, h, row0);
+    else fwd_unit<Tin, DK, Prm, 1>(sm, &tm_q, &tm_k, &tm_v, p, n, h, row0);
 }
 
 template <typename Tin, int DK, typename Prm>
 static gdn_status launch_fwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                               const Prm& p, int units, cudaStream_t stream) {
+                               const Prm& p, long long grid, cudaStream_t stream) {
     const size_t smem = sizeof(FwdSmem<Tin, DK>) + 128;
     auto kern = gdn_fwd_kernel<Tin, DK, Prm>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return GDN_ERR_CUDA;
-    const int nt = ts::threads_for_rows<DK>(p.dvs);
-    kern<<<units, nt, smem, stream>>>(mq, mk, mv, p);
+    kern<<<(unsigned)grid, ts::threads_for_rows<DK>(p.rows4), smem, stream>>>(mq, mk, mv, p);
     return launch_status();
 }
 
 template <typename Tin, typename Prm>
 static gdn_status launch_fwd_dk(int dk, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                                const Prm& p, int units, cudaStream_t stream) {
+                                const Prm& p, long long grid, cudaStream_t stream) {
     switch (dk) {
-        case 16: return launch_fwd_t<Tin, 16, Prm>(mq, mk, mv, p, units, stream);
-        case 32: return launch_fwd_t<Tin, 32, Prm>(mq, mk, mv, p, units, stream);
-        case 64: return launch_fwd_t<Tin, 64, Prm>(mq, mk, mv, p, units, stream);
-        case 128: return launch_fwd_t<Tin, 128, Prm>(mq, mk, mv, p, units, stream);
+        case 16: return launch_fwd_t<Tin, 16, Prm>(mq, mk, mv, p, grid, stream);
+        case 32: return launch_fwd_t<Tin, 32, Prm>(mq, mk, mv, p, grid, stream);
+        case 64: return launch_fwd_t<Tin, 64, Prm>(mq, mk, mv, p, grid, stream);
+        case 128: return launch_fwd_t<Tin, 128, Prm>(mq, mk, mv, p, grid, stream);
     }
     return GDN_ERR_UNSUPPORTED;
 }
@@ -281,22 +377,65 @@ gdn_status launch_unit_sched(const int32_t* cu, int N, int T, int HV, int nslice
     return launch_status();
 }
 
-size_t fwd_workspace_size(const gdn_shape* s) {
+// Slicing plan of a forward call.  Automatic slices (dv_slice == 0) may split
+// the heads of long sequences in 2 or 4 when dk >= 32 and dv >= 64 (units of
+// at least 16 rows); a forced dv_slice gives every head dv / dv_slice slices.
+struct FwdPlan {
+    int forced_ns;  // slices per head when forced, else 0
+    int split;      // automatic splitting allowed
+    int rows4;      // rows of a unit at 4 rows per thread
+};
+
+static FwdPlan fwd_plan(const gdn_shape* s) {
+    FwdPlan pl;
     const int dvs = pick_dv_slice(s);
-    return kWsHeader + (((size_t)s->N * s->HV * (s->dv / dvs) * sizeof(int32_t) + 255) & ~size_t(255));
+    pl.forced_ns = s->dv_slice ? s->dv / dvs : 0;
+    pl.split = !s->dv_slice && s->dk >= 32 && s->dv >= 64;
+    pl.rows4 = dvs;
+    return pl;
 }
 
-// Shared by the allocating entry point and any caller that supplies the
-// work-list and error-word buffers itself.
+// Work items a call can produce on a device with `slots` CTA slots: forced,
+// N * HV * forced_ns; automatic, N * HV plus up to 3 * HV more for each
+// sequence longer than 1.5 T * HV / slots, of which there are fewer than slots / HV.
+// slots = 0 gives the bound for any device (every head split in 4).
+long long fwd_max_items(const gdn_shape* s, int slots) {
+    const FwdPlan pl = fwd_plan(s);
+    const long long nh = (long long)s->N * s->HV;
+    if (pl.forced_ns) return nh * pl.forced_ns;
+    if (!pl.split) return nh;
+    if (slots <= 0) return 4 * nh;
+    return nh + 3LL * s->HV * std::min<long long>(s->N, slots / s->HV + 1);
+}
+
+// Workspace: the 256-byte header (word 0: device error bits, word 1: the
+// number of work items) and the work list.
+size_t fwd_workspace_size(const gdn_shape* s) {
+    return kWsHeader + (((size_t)fwd_max_items(s, 0) * sizeof(int32_t) + 255) & ~size_t(255));
+}
+
+// CTA slots of the current device: two forward CTAs per SM.
+static int fwd_slots() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return 0;
+    return 2 * sms;
+}
+
+// Shared by the allocating entry points and the allocation-free one: `header`
+// is the workspace header (error word, item count) and `work` the list, room
+// for fwd_max_items(s, slots) items.
 gdn_status run_recurrent_fwd(const gdn_shape* s, const void* q, const void* k, const void* v, const float* g,
                              const float* beta, const float* init_state, const int32_t* cu, void* out,
-                             float* final_state, int32_t* work, unsigned* err, cudaStream_t stream,
+                             float* final_state, int32_t* work, unsigned* header, int slots, cudaStream_t stream,
                              float* snap = nullptr, const int32_t* snap_cu = nullptr, int snap_every = 0,
                              int snap_slots = 0) {
-    const int dvs = pick_dv_slice(s);
-    const int nslices = s->dv / dvs;
-    const int units = s->N * s->HV * nslices;
     if (s->N == 0) return GDN_OK;
+    const FwdPlan plan = fwd_plan(s);
+    const int split = plan.split && slots > 0;
+    const long long grid = split ? fwd_max_items(s, slots) : fwd_max_items(s, 0) / (plan.split ? 4 : 1);
+    const int vw = plan.forced_ns ? plan.rows4 : s->dv;
 
     CUtensorMap mq{}, mk{}, mv{};
     if (s->T_total > 0) {
@@ -305,10 +444,13 @@ gdn_status run_recurrent_fwd(const gdn_shape* s, const void* q, const void* k, c
         const uint32_t tb = (uint32_t)std::min(kTC, s->T_total);
         if ((st = encode_map_3d(&mq, q, s->dtype, s->dk, s->HK, s->T_total, s->dk, tb)) != GDN_OK) return st;
         if ((st = encode_map_3d(&mk, k, s->dtype, s->dk, s->HK, s->T_total, s->dk, tb)) != GDN_OK) return st;
-        if ((st = encode_map_3d(&mv, v, s->dtype, s->dv, s->HV, s->T_total, dvs, tb)) != GDN_OK) return st;
+        if ((st = encode_map_3d(&mv, v, s->dtype, s->dv, s->HV, s->T_total, vw, tb)) != GDN_OK) return st;
     }
-    if (cudaMemsetAsync(err, 0, sizeof(unsigned), stream) != cudaSuccess) return GDN_ERR_CUDA;
-    gdn_sched_kernel<<<(s->N + 255) / 256, 256, 0, stream>>>(cu, s->N, s->T_total, s->HV, nslices, work, err);
+    unsigned* err = header;
+    int32_t* nwork = reinterpret_cast<int32_t*>(header + 1);
+    if (cudaMemsetAsync(header, 0, 2 * sizeof(unsigned), stream) != cudaSuccess) return GDN_ERR_CUDA;
+    fwd_sched_kernel<<<(s->N + 255) / 256, 256, 0, stream>>>(cu, s->N, s->T_total, s->HV, s->dv, plan.forced_ns,
+                                                           split, slots, grid, work, nwork, err);
     if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
 
     FwdParams p;
@@ -319,15 +461,17 @@ gdn_status run_recurrent_fwd(const gdn_shape* s, const void* q, const void* k, c
     p.out = out;
     p.final_state = final_state;
     p.work = work;
+    p.nwork = nwork;
     p.err = err;
     p.N = s->N;
     p.T = s->T_total;
     p.HV = s->HV;
     p.G = s->HV / s->HK;
     p.dv = s->dv;
-    p.dvs = dvs;
-    p.nslices = nslices;
     p.use_norm = s->use_qk_l2norm ? 1 : 0;
+    p.rows4 = plan.rows4;
+    p.forced = plan.forced_ns ? 1 : 0;
+    p.vw = vw;
     p.tb = std::min(kTC, s->T_total);
     if (snap && snap_cu && snap_slots > 0 && snap_every > 0) {
         SnapParams sp;
@@ -336,11 +480,11 @@ gdn_status run_recurrent_fwd(const gdn_shape* s, const void* q, const void* k, c
         sp.snap_cu = snap_cu;
         sp.snap_every = snap_every;
         sp.snap_slots = snap_slots;
-        if (s->dtype == GDN_BF16) return launch_fwd_dk<__nv_bfloat16>(s->dk, mq, mk, mv, sp, units, stream);
-        return launch_fwd_dk<float>(s->dk, mq, mk, mv, sp, units, stream);
+        if (s->dtype == GDN_BF16) return launch_fwd_dk<__nv_bfloat16>(s->dk, mq, mk, mv, sp, grid, stream);
+        return launch_fwd_dk<float>(s->dk, mq, mk, mv, sp, grid, stream);
     }
-    if (s->dtype == GDN_BF16) return launch_fwd_dk<__nv_bfloat16>(s->dk, mq, mk, mv, p, units, stream);
-    return launch_fwd_dk<float>(s->dk, mq, mk, mv, p, units, stream);
+    if (s->dtype == GDN_BF16) return launch_fwd_dk<__nv_bfloat16>(s->dk, mq, mk, mv, p, grid, stream);
+    return launch_fwd_dk<float>(s->dk, mq, mk, mv, p, grid, stream);
 }
 
 gdn_status check_fwd_args(const gdn_shape* s, const void* q, const void* k, const void* v, const float* g,
@@ -376,7 +520,7 @@ extern "C" gdn_status gdn_recurrent_fwd(const gdn_shape* shape, const void* q, c
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     return run_recurrent_fwd(shape, q, k, v, g, beta, init_state, cu_seqlens, out, final_state,
                              reinterpret_cast<int32_t*>(ws + kWsHeader), reinterpret_cast<unsigned*>(ws),
-                             static_cast<cudaStream_t>(stream));
+                             fwd_slots(), static_cast<cudaStream_t>(stream));
 }
 
 extern "C" gdn_status gdn_recurrent_fwd_snapshots(const gdn_shape* shape, const void* q, const void* k,
@@ -397,11 +541,12 @@ extern "C" gdn_status gdn_recurrent_fwd_snapshots(const gdn_shape* shape, const 
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     return run_recurrent_fwd(shape, q, k, v, g, beta, init_state, cu_seqlens, out, final_state,
                              reinterpret_cast<int32_t*>(ws + kWsHeader), reinterpret_cast<unsigned*>(ws),
-                             static_cast<cudaStream_t>(stream), snap_states, snap_cu, snap_every, num_snap_slots);
+                             fwd_slots(), static_cast<cudaStream_t>(stream), snap_states, snap_cu, snap_every,
+                             num_snap_slots);
 }
 
 // ---------------------------------------------------------------------------
-// Allocation-free variant.  Its scratch (device error word + work list) is a
+// Allocation-free variant.  Its scratch (device error word, item count and work list) is a
 // fixed array in the library's own device memory instead of a caller-supplied
 // workspace.  Every device that loads the library holds this array (about
 // 256 KB) until the process exits.  All calls share it, so two calls whose
@@ -409,7 +554,7 @@ extern "C" gdn_status gdn_recurrent_fwd_snapshots(const gdn_shape* shape, const 
 // and the work list is rewritten in full by each call.
 namespace gdn {
 
-constexpr int kStaticUnits = 1 << 16;    // max N * HV * (dv / dv_slice)
+constexpr int kStaticUnits = 1 << 16;    // max work items (fwd_max_items)
 constexpr int kStaticHeaderWords = 64;   // 256 bytes: word 0 is the error word
 static __device__ __align__(256) int32_t g_fwd_static_scratch[kStaticHeaderWords + kStaticUnits];
 
@@ -442,11 +587,11 @@ extern "C" gdn_status gdn_recurrent_fwd_noalloc(const gdn_shape* shape, const vo
     gdn_status st = check_fwd_args(shape, q, k, v, g, beta, init_state, cu_seqlens, out, final_state);
     if (st != GDN_OK) return st;
     if (shape->N == 0) return GDN_OK;
-    const long long units = (long long)shape->N * shape->HV * (shape->dv / pick_dv_slice(shape));
-    if (units > kStaticUnits) return GDN_ERR_WORKSPACE;
+    const int slots = fwd_slots();
+    if (fwd_max_items(shape, slots) > kStaticUnits) return GDN_ERR_WORKSPACE;
     int32_t* base = static_scratch_on_current_device();
     if (!base) return GDN_ERR_CUDA;
     return run_recurrent_fwd(shape, q, k, v, g, beta, init_state, cu_seqlens, out, final_state,
-                             base + kStaticHeaderWords, reinterpret_cast<unsigned*>(base),
+                             base + kStaticHeaderWords, reinterpret_cast<unsigned*>(base), slots,
                              static_cast<cudaStream_t>(stream));
 }

@@ -28,9 +28,11 @@ inline gdn_status check_shape(const gdn_shape* s) {
     if (s->dv_slice != 0 && (!dim_ok(s->dv_slice) || s->dv_slice > s->dv)) return GDN_ERR_UNSUPPORTED;
     // The kernels index (token, head) pairs and work units with 32-bit integers and
     // elements with 64-bit offsets: T_total * HV (>= T_total * HK) and the unit count
-    // N * HV * (dv / 16) must stay below 2^31.
+    // N * HV * (dv / 16) must stay below 2^31, and a forward work item packs
+    // n * HV + h into 26 bits.
     if ((long long)s->T_total * s->HV >= (1LL << 31)) return GDN_ERR_UNSUPPORTED;
     if ((long long)s->N * s->HV * (s->dv / 16) >= (1LL << 31)) return GDN_ERR_UNSUPPORTED;
+    if ((long long)s->N * s->HV >= (1LL << 26)) return GDN_ERR_UNSUPPORTED;
     return GDN_OK;
 }
 

@@ -12,12 +12,13 @@
 // The recurrence (gated delta rule, recurrent form as in "Defending Against
 // the Training-Inference Numeric Mismatch in RL (Especially Linear
 // Attention)", section 3.2):
-//     u = S k^,  w = b (v - a u),  S <- a S + w k^T,  o = S q^
+//     u = S k^,  w = b v - (a b) u,  S <- a S + w k^T,  o = S q^
 // which equals S <- a S (I - b k^ k^T) + b v k^T with o read after the update.
 //
-// Layout.  A row group of L consecutive lanes holds R = 4 rows of S: lane e
-// of the group (e = lane % L) holds the float4 column chunks c = L*i + e,
-// i = 0 .. NC-1 (NC = dk / (4 L)), of all R rows, so the k^/q^ chunks a group
+// Layout.  A row group of L consecutive lanes holds R rows of S (4, or 2 or 1
+// when a head is split over several CTAs): lane e of the group (e = lane % L)
+// holds the float4 column chunks c = L*i + e, i = 0 .. NC-1 (NC = dk / (4 L)),
+// of all R rows, so the k^/q^ chunks a group
 // reads at one step are 16*L contiguous bytes of shared memory.  For the
 // cross-lane reduction the rows form NG = R / RG slot groups of RG rows;
 // within slot group g, slot j of lane e holds row g*RG + (j ^ own(e)),
@@ -33,9 +34,9 @@
 // as (x, y) then (z, w), starting from +0; then even + odd; then one add per
 // lane stride L/2, L/4, ..., 1, each adding the partner lane's partial.  The
 // owner lanes of a row compute w for it, and every lane gathers the RG values
-// of w it needs with RG independent shuffles (one level of latency).  The
-// prefill kernel uses RG = 4 and the decode kernel RG = 2; the per-row
-// operations, and so the bits, are the same.
+// of w it needs with RG - 1 independent shuffles (one level of latency).  The
+// prefill kernel uses RG = R (4, 2 or 1) and the decode kernel R = 4 in two
+// groups of RG = 2; the per-row operations, and so the bits, are the same.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -49,10 +50,10 @@ namespace ts {
 
 constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
 
-template <int DK, int RG_ = 4>
+template <int DK, int RG_ = 4, int R_ = 4>
 struct Layout {
     static constexpr int L = DK >= 32 ? 8 : 4;  // lanes per row group
-    static constexpr int R = 4;                 // rows per thread
+    static constexpr int R = R_;                // rows per thread (4, or 2 / 1 for a sliced head)
     static constexpr int RG = RG_;              // rows per slot group
     static constexpr int NG = R / RG;           // slot groups per thread
     static constexpr int NC = DK / (4 * L);     // float4 chunks per lane and row
@@ -61,17 +62,17 @@ struct Layout {
     static_assert(RG <= L && R % RG == 0 && 32 % L == 0, "RG <= L, RG divides R, L divides the warp");
 };
 
-// Threads a CTA needs for `rows` rows of S (at least one warp).
+// Threads a CTA needs for `rows` rows of S at 4 rows per thread (at least one warp).
 template <int DK>
 __host__ __device__ constexpr int threads_for_rows(int rows) {
-    return rows * Layout<DK>::L / Layout<DK>::R < 32 ? 32 : rows * Layout<DK>::L / Layout<DK>::R;
+    return rows * Layout<DK>::L / 4 < 32 ? 32 : rows * Layout<DK>::L / 4;
 }
 
-// The R rows a thread holds: slot s = g * RG + j; chunk i of a slot is
-// (x, y) = p[s][2i], (z, w) = p[s][2i + 1].
+// The rows a thread holds (room for 4; a thread with R rows uses slots 0 .. R-1):
+// slot s = g * RG + j; chunk i of a slot is (x, y) = p[s][2i], (z, w) = p[s][2i + 1].
 template <int DK>
 struct Rows {
-    float2 p[Layout<DK>::R][2 * Layout<DK>::NC];
+    float2 p[4][2 * Layout<DK>::NC];
 };
 
 // Where a thread sits: its lane in the row group, the row it owns within each
@@ -137,19 +138,21 @@ __device__ __forceinline__ float reduce_scatter(float (&p)[RG]) {
     return p[0];
 }
 
-// w[j] for every slot j of a group, from the owner lanes' values (RG independent shuffles).
+// w[j] for every slot j of a group, from the owner lanes' values: slot j holds
+// row j ^ own(e), owned by lane e ^ (j << SH) of the same row group, so slot 0
+// is the lane's own value and the others take RG - 1 independent xor shuffles.
 template <int DK, int RG>
-__device__ __forceinline__ void gather_rows(float mine, int lane, int own, float (&w)[RG]) {
+__device__ __forceinline__ void gather_rows(float mine, float (&w)[RG]) {
     using Y = Layout<DK, RG>;
-    const int base = lane & ~(Y::L - 1);
+    w[0] = mine;
 #pragma unroll
-    for (int j = 0; j < RG; ++j) w[j] = __shfl_sync(kFull, mine, base | ((j ^ own) << Y::SH));
+    for (int j = 1; j < RG; ++j) w[j] = __shfl_xor_sync(kFull, mine, j << Y::SH);
 }
 
-// w = b (v - a u)
-__device__ __forceinline__ float delta_w(float a, float b, float v, float u) {
-    return __fmul_rn(b, __fsub_rn(v, __fmul_rn(a, u)));
-}
+// w = b (v - a u), evaluated as fma(-(a b), u, b v): ab = a * b is the token's
+// and bv = b * v the row's, both known before u, so one rounding step is left
+// on the recurrence's critical path.
+__device__ __forceinline__ float delta_w(float ab, float bv, float u) { return __fmaf_rn(-ab, u, bv); }
 
 // For every slot j of group G: S <- a S + w[j] k^T (per element fma(w, k_c, a * S_c)),
 // and p[j] = lane partial of the updated row . q.
@@ -185,17 +188,18 @@ __device__ __forceinline__ void update_part(Rows<DK>& s, const float* __restrict
 // group g, v_own[g] its v.  All 32 lanes of the warp call it.
 template <int DK, int RG>
 __device__ __forceinline__ void token_step(Rows<DK>& s, const float* __restrict__ kn, const float* __restrict__ qn,
-                                           const Place& pl, int lane, float a, float b,
+                                           const Place& pl, float a, float b,
                                            const float (&v_own)[Layout<DK, RG>::NG],
                                            float (&o)[Layout<DK, RG>::NG]) {
     static_assert(Layout<DK, RG>::NG == 2, "two slot groups");
     float p0[RG], p1[RG], w0[RG], w1[RG];
     dot_part<DK, RG, 0>(s, kn, pl.e, p0);
     dot_part<DK, RG, 1>(s, kn, pl.e, p1);
+    const float ab = __fmul_rn(a, b);
     const float u0 = reduce_scatter<DK, RG>(p0);
     const float u1 = reduce_scatter<DK, RG>(p1);
-    gather_rows<DK, RG>(delta_w(a, b, v_own[0], u0), lane, pl.own, w0);
-    gather_rows<DK, RG>(delta_w(a, b, v_own[1], u1), lane, pl.own, w1);
+    gather_rows<DK, RG>(delta_w(ab, __fmul_rn(b, v_own[0]), u0), w0);
+    gather_rows<DK, RG>(delta_w(ab, __fmul_rn(b, v_own[1]), u1), w1);
     update_part<DK, RG, 0>(s, kn, qn, pl.e, a, w0, p0);
     update_part<DK, RG, 1>(s, kn, qn, pl.e, a, w1, p1);
     o[0] = reduce_scatter<DK, RG>(p0);
@@ -205,9 +209,9 @@ __device__ __forceinline__ void token_step(Rows<DK>& s, const float* __restrict_
 // Global <-> register transfer of a thread's rows.  rows points at the first
 // row of the thread's group (row stride dk floats).  Every 32-byte sector is
 // read or written whole by neighbouring lanes.
-template <int DK, int RG>
+template <int DK, int RG, int R = 4>
 __device__ __forceinline__ void load_rows(Rows<DK>& s, const float* __restrict__ rows, const Place& pl) {
-    using Y = Layout<DK, RG>;
+    using Y = Layout<DK, RG, R>;
 #pragma unroll
     for (int g = 0; g < Y::NG; ++g)
 #pragma unroll
@@ -224,14 +228,14 @@ __device__ __forceinline__ void load_rows(Rows<DK>& s, const float* __restrict__
 template <int DK>
 __device__ __forceinline__ void zero_rows(Rows<DK>& s) {
 #pragma unroll
-    for (int j = 0; j < Layout<DK>::R; ++j)
+    for (int j = 0; j < 4; ++j)
 #pragma unroll
         for (int i = 0; i < 2 * Layout<DK>::NC; ++i) s.p[j][i] = make_float2(0.f, 0.f);
 }
 
-template <int DK, int RG>
+template <int DK, int RG, int R = 4>
 __device__ __forceinline__ void store_rows(const Rows<DK>& s, float* __restrict__ rows, const Place& pl) {
-    using Y = Layout<DK, RG>;
+    using Y = Layout<DK, RG, R>;
 #pragma unroll
     for (int g = 0; g < Y::NG; ++g)
 #pragma unroll

@@ -49,9 +49,12 @@ def shape(**kw):
 def test_workspace_sizes(lib):
     s = shape(N=64)
     fwd = gdn.gdn_workspace_size(s, binding.OP_FWD)
-    assert fwd >= 256 + 64 * 4 * 4
+    # automatic slices may split every head of a long sequence in 4: room for 4 * N * HV items
+    assert fwd >= 256 + 4 * 64 * 4 * 4
     assert gdn.gdn_workspace_size(s, binding.OP_DECODE) == 0
-    assert gdn.gdn_workspace_size(shape(N=64, dv_slice=32), binding.OP_FWD) > fwd
+    assert gdn.gdn_workspace_size(shape(N=64, dv_slice=16), binding.OP_FWD) > fwd  # 8 slices per head
+    # no automatic splitting below dv = 64 (units keep at least 16 rows): one item per head
+    assert gdn.gdn_workspace_size(shape(N=64, dv=32), binding.OP_FWD) == 256 + 64 * 4 * 4
     assert gdn.gdn_workspace_size(shape(dk=48), binding.OP_FWD) == 0  # unsupported
     assert gdn.gdn_workspace_size(shape(HV=3), binding.OP_FWD) == 0   # HV % HK != 0
 

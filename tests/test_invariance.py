@@ -61,6 +61,28 @@ def test_batch_invariance(init_scale):
                 assert torch.equal(fs[pos:pos + 1].view(torch.int32), ref_s.view(torch.int32)), (i, bsz, dv_slice)
 
 
+def test_per_length_slices_are_bit_neutral():
+    """The scheduler splits the heads of a sequence longer than 1.5 (3) times the
+    average work per CTA slot over 2 (4) CTAs, with fewer rows per thread.  With
+    152 SMs (304 slots) and HV = 32 these lengths give one 4-way split (3000
+    tokens), one 2-way split (1200) and 18 whole heads (100); any other device
+    splits differently, and the bits must not change either way: automatic
+    slices, forced whole heads, forced quarter heads and each sequence alone
+    agree."""
+    lengths = [100] * 9 + [3000] + [100] * 9 + [1200]
+    x = inputs.make_inputs(lengths, seed=11, init_scale=0.1, **SHAPE)
+    auto_o, auto_s = fwd(x)
+    for dv_slice in (128, 32):
+        o, s = fwd(x, dv_slice=dv_slice)
+        assert torch.equal(o.view(torch.int16), auto_o.view(torch.int16)), dv_slice
+        assert torch.equal(s.view(torch.int32), auto_s.view(torch.int32)), dv_slice
+    cu = x.cu_seqlens.tolist()
+    for i in (9, 19, 0):
+        o, s = fwd(seq(x, i))
+        assert torch.equal(o.view(torch.int16), auto_o[cu[i]:cu[i + 1]].view(torch.int16)), i
+        assert torch.equal(s.view(torch.int32), auto_s[i:i + 1].view(torch.int32)), i
+
+
 def _decode_tokens(x, n_prompt, state, graph=False):
     """Run tokens n_prompt.. of every sequence (all the same length) through gdn_decode_step."""
     N = len(x.lengths)
