@@ -160,8 +160,9 @@ def load_traffic(kernel, sha):
 
 
 FWD_SRC = ["invariant_linear_attention_gb300/csrc/gdn_fwd.cu", "invariant_linear_attention_gb300/csrc/gdn_step.cuh",
-           "invariant_linear_attention_gb300/csrc/gdn_async.cuh"]
-DEC_SRC = ["invariant_linear_attention_gb300/csrc/gdn_decode.cu", "invariant_linear_attention_gb300/csrc/gdn_step.cuh"]
+           "invariant_linear_attention_gb300/csrc/gdn_token_step.cuh", "invariant_linear_attention_gb300/csrc/gdn_async.cuh"]
+DEC_SRC = ["invariant_linear_attention_gb300/csrc/gdn_decode.cu", "invariant_linear_attention_gb300/csrc/gdn_step.cuh",
+           "invariant_linear_attention_gb300/csrc/gdn_token_step.cuh"]
 
 
 def oracle_sample_rate(x, seconds=12.0):

@@ -74,7 +74,7 @@ struct alignas(128) FwdSmem {
     Tin v[kStages][kTC * kMaxSlice];
     float qn[kTC * DK];
     float kn[kTC * DK];
-    float2 ab[kTC];
+    float4 ab[kTC];  // per token: (a, a, b, a * b)
     uint64_t bar[kStages];
     int abort_flag;
 };
@@ -271,7 +271,10 @@ __device__ __forceinline__ void fwd_unit(FwdSmem<Tin, DK>& sm, const CUtensorMap
                 }
                 l2norm_warp_multi<DK, 4>(src, dst, nv, lane, p.use_norm);
             }
-            if (tid < tc) sm.ab[tid] = make_float2(gate_alpha(gb.x), gb.y);
+            if (tid < tc) {
+                const float a = gate_alpha(gb.x);
+                sm.ab[tid] = make_float4(a, a, gb.y, __fmul_rn(a, gb.y));
+            }
             __syncthreads();
             if (sm.abort_flag) {
                 if (tid == 0) {
@@ -288,29 +291,35 @@ __device__ __forceinline__ void fwd_unit(FwdSmem<Tin, DK>& sm, const CUtensorMap
                 const size_t gi = (size_t)(t0 + kTC + tid) * p.HV + h;
                 gb = make_float2(p.g[gi], p.beta[gi]);
             }
-            const Tin* __restrict__ vs = sm.v[st] + (orow - vcol);
+            const Tin* __restrict__ vt = sm.v[st] + (orow - vcol);  // this thread's v, token by token
             // Token loop, software-pipelined by one token: the reduce-scatter of
             // token t's output runs next to token t+1's u reduction (it is off
             // the recurrence's critical path); every operation is unchanged.
             float op[R];
 #pragma unroll
             for (int j = 0; j < R; ++j) op[j] = 0.f;
-            Tin* __restrict__ orow_ptr = out + ((size_t)t0 * p.HV + h) * p.dv + orow;  // token t0's output row
             const size_t ostride = (size_t)p.HV * p.dv;
+            Tin* __restrict__ optr = out + ((size_t)t0 * p.HV + h) * p.dv + orow - ostride;  // token t - 1's row
+            const float* kt = sm.kn;
+            const float* qt = sm.qn;
             for (int t = 0; t < tc; ++t) {
-                const float2 ab = sm.ab[t];
-                const float abt = __fmul_rn(ab.x, ab.y);
-                const float bv = __fmul_rn(ab.y, active ? ld_in(vs + t * p.vw) : 0.f);
-                float up[R], w[R];
-                ts::dot_part<DK, R, 0>(S, sm.kn + t * DK, pl.e, up);
+                const float4 ab = sm.ab[t];
+                const float bv = __fmul_rn(ab.z, active ? ld_in(vt) : 0.f);
+                float up[R];
+                float2 w[R];
+                ts::dot_part<DK, R, 0>(S, kt, pl.e, up);
                 const float oprev = ts::reduce_scatter<DK, R>(op);  // token t - 1's output (t > 0)
                 const float u = ts::reduce_scatter<DK, R>(up);
-                if (t > 0 && storer) st_in(orow_ptr + (t - 1) * ostride, oprev);
-                ts::gather_rows<DK, R>(ts::delta_w(abt, bv, u), w);
-                ts::update_part<DK, R, 0>(S, sm.kn + t * DK, sm.qn + t * DK, pl.e, ab.x, w, op);
+                if (t > 0 && storer) st_in(optr, oprev);
+                ts::gather_rows<DK, R>(ts::delta_w(ab.w, bv, u), w);
+                ts::update_part<DK, R, 0>(S, kt, qt, pl.e, make_float2(ab.x, ab.y), w, op);
+                vt += p.vw;
+                optr += ostride;
+                kt += DK;
+                qt += DK;
             }
             const float olast = ts::reduce_scatter<DK, R>(op);
-            if (storer) st_in(orow_ptr + (tc - 1) * ostride, olast);
+            if (storer) st_in(optr, olast);
             if constexpr (std::is_same<Prm, SnapParams>::value) {
                 // the state after `done` tokens of this sequence, at every snap_every-th token
                 const int done = t0 + tc - bos;

@@ -34,7 +34,7 @@
 // as (x, y) then (z, w), starting from +0; then even + odd; then one add per
 // lane stride L/2, L/4, ..., 1, each adding the partner lane's partial.  The
 // owner lanes of a row compute w for it, and every lane gathers the RG values
-// of w it needs with RG - 1 independent shuffles (one level of latency).  The
+// of w it needs with RG - 1 independent xor shuffles (one level of latency).  The
 // prefill kernel uses RG = R (4, 2 or 1) and the decode kernel R = 4 in two
 // groups of RG = 2; the per-row operations, and so the bits, are the same.
 #pragma once
@@ -138,15 +138,19 @@ __device__ __forceinline__ float reduce_scatter(float (&p)[RG]) {
     return p[0];
 }
 
-// w[j] for every slot j of a group, from the owner lanes' values: slot j holds
-// row j ^ own(e), owned by lane e ^ (j << SH) of the same row group, so slot 0
-// is the lane's own value and the others take RG - 1 independent xor shuffles.
+// w[j] for every slot j of a group, from the owner lanes' values, each as the
+// pair (w, w) the packed update multiplies by: slot j holds row j ^ own(e),
+// owned by lane e ^ (j << SH) of the same row group, so slot 0 is the lane's
+// own value and the others take RG - 1 independent xor shuffles.
 template <int DK, int RG>
-__device__ __forceinline__ void gather_rows(float mine, float (&w)[RG]) {
+__device__ __forceinline__ void gather_rows(float mine, float2 (&w)[RG]) {
     using Y = Layout<DK, RG>;
-    w[0] = mine;
+    w[0] = make_float2(mine, mine);
 #pragma unroll
-    for (int j = 1; j < RG; ++j) w[j] = __shfl_xor_sync(kFull, mine, j << Y::SH);
+    for (int j = 1; j < RG; ++j) {
+        const float x = __shfl_xor_sync(kFull, mine, j << Y::SH);
+        w[j] = make_float2(x, x);
+    }
 }
 
 // w = b (v - a u), evaluated as fma(-(a b), u, b v): ab = a * b is the token's
@@ -158,19 +162,18 @@ __device__ __forceinline__ float delta_w(float ab, float bv, float u) { return _
 // and p[j] = lane partial of the updated row . q.
 template <int DK, int RG, int G>
 __device__ __forceinline__ void update_part(Rows<DK>& s, const float* __restrict__ k, const float* __restrict__ q,
-                                            int e, float a, const float (&w)[RG], float (&p)[RG]) {
+                                            int e, float2 a2, const float2 (&w)[RG], float (&p)[RG]) {
     using Y = Layout<DK, RG>;
     float2 A[RG];
 #pragma unroll
     for (int j = 0; j < RG; ++j) A[j] = make_float2(0.f, 0.f);
-    const float2 a2 = make_float2(a, a);
 #pragma unroll
     for (int i = 0; i < Y::NC; ++i) {
         const float4 k4 = *reinterpret_cast<const float4*>(k + 4 * (Y::L * i + e));
         const float4 q4 = *reinterpret_cast<const float4*>(q + 4 * (Y::L * i + e));
 #pragma unroll
         for (int j = 0; j < RG; ++j) {
-            const float2 w2 = make_float2(w[j], w[j]);
+            const float2 w2 = w[j];
             float2& Sxy = s.p[G * RG + j][2 * i];
             float2& Szw = s.p[G * RG + j][2 * i + 1];
             Sxy = __ffma2_rn(w2, lo2(k4), __fmul2_rn(a2, Sxy));
@@ -192,7 +195,8 @@ __device__ __forceinline__ void token_step(Rows<DK>& s, const float* __restrict_
                                            const float (&v_own)[Layout<DK, RG>::NG],
                                            float (&o)[Layout<DK, RG>::NG]) {
     static_assert(Layout<DK, RG>::NG == 2, "two slot groups");
-    float p0[RG], p1[RG], w0[RG], w1[RG];
+    float p0[RG], p1[RG];
+    float2 w0[RG], w1[RG];
     dot_part<DK, RG, 0>(s, kn, pl.e, p0);
     dot_part<DK, RG, 1>(s, kn, pl.e, p1);
     const float ab = __fmul_rn(a, b);
@@ -200,8 +204,8 @@ __device__ __forceinline__ void token_step(Rows<DK>& s, const float* __restrict_
     const float u1 = reduce_scatter<DK, RG>(p1);
     gather_rows<DK, RG>(delta_w(ab, __fmul_rn(b, v_own[0]), u0), w0);
     gather_rows<DK, RG>(delta_w(ab, __fmul_rn(b, v_own[1]), u1), w1);
-    update_part<DK, RG, 0>(s, kn, qn, pl.e, a, w0, p0);
-    update_part<DK, RG, 1>(s, kn, qn, pl.e, a, w1, p1);
+    update_part<DK, RG, 0>(s, kn, qn, pl.e, make_float2(a, a), w0, p0);
+    update_part<DK, RG, 1>(s, kn, qn, pl.e, make_float2(a, a), w1, p1);
     o[0] = reduce_scatter<DK, RG>(p0);
     o[1] = reduce_scatter<DK, RG>(p1);
 }
