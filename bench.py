@@ -364,11 +364,14 @@ def main():
                      "peak": peak / 1e12, "unit": "TFLOP/s", "frac": achieved / peak,
                      "fp32_pipe_frac": (pipe_ops_tok * T / (fwd_avg / 1e3)) / (peak / 2),
                      "traffic": traffic["bytes_per_launch"] * (T / traffic["tokens"]) if traffic else None,
+                     "ncu_fma_pipe_active_pct": traffic.get("fma_pipe_active_pct") if traffic else None,
                      "algorithmic_bytes": alg_bytes_fwd,
                      "note": f"7*dk*dv flops per token per value head (FMA=2, MUL=1) over the gdn_recurrent_fwd "
                              f"call time (scheduler included); peak = {sms} SMs x 128 FP32 lanes x 2 flop x "
                              f"{max_mhz:.0f} MHz (derived from unit counts and max clock); the algorithm's "
-                             f"3 FMA + 1 MUL mix caps frac at 0.875"},
+                             f"3 FMA + 1 MUL mix caps frac at 0.875; traffic and the ncu FMA-pipe % come from "
+                             f"profiles/ncu_traffic.json (one launch on 9 x 4096 tokens, same kernel source), "
+                             f"null when the source has changed since"},
         "decode_roofline": {"bound": "hbm", "kernel": "gdn_decode_kernel", "achieved": dec_gbs, "peak": hbm_peak,
                             "unit": "GB/s", "frac": dec_gbs / hbm_peak,
                             "traffic": (lambda t: t["bytes_per_launch"] if t else None)(
@@ -407,7 +410,7 @@ def main():
 
     # ---- end to end through the C ABI from pinned host buffers
     if not args.no_e2e and not small:
-        result["e2e"] = e2e(gdn, d.cpu(), dd.cpu(), st0.cpu(), dev, steps=min(steps, 5))
+        result["e2e"] = e2e(gdn, d.cpu(), dd.cpu(), st0.cpu(), dev, steps=min(steps, 5), device_ms=fwd_avg + dec_avg)
 
     # ---- backward on its own workload
     if not args.no_backward and not small:
@@ -513,7 +516,7 @@ def oracle_decode_rate(dec, dec_state, seconds=4.0):
                                         f"states), fp64 C recurrence, OpenMP over (sequence, head)", "seconds": dt}
 
 
-def e2e(gdn, x, dec, dec_state, dev, steps):
+def e2e(gdn, x, dec, dec_state, dev, steps, device_ms=None):
     """Same step through the public API from pinned host buffers: H2D of every
     input, both calls, D2H of both outputs, all inside the timed region.
 
@@ -614,9 +617,13 @@ def e2e(gdn, x, dec, dec_state, dev, steps):
             "d2h_bytes_per_step": d2h, "steps": steps,
             "h2d_gbs_alone": rate["h2d"], "d2h_gbs_alone": rate["d2h"],
             "h2d_gbs_in_step": h2d / (ms / 1e3) / 1e9,
-            "bound": "host link" if h2d / (rate["h2d"] * 1e9) * 1e3 > 0.8 * ms else "compute",
+            "device_ms_per_step": device_ms,
+            # the step is the copies' when it takes clearly longer than its kernels alone
+            "bound": ("host link" if device_ms is None or ms > 1.2 * device_ms else "device"),
             "note": "pinned host buffers; uploads, compute and downloads of consecutive steps overlap on three "
-                    "streams (two device buffer sets); *_gbs_alone = one step's copies timed on their own"}
+                    "streams (two device buffer sets); *_gbs_alone = one step's copies timed on their own; "
+                    "h2d_gbs_in_step = the step's uploads over the pipelined step time (uploads and downloads "
+                    "share the host link)"}
 
 
 def bench_snapshots(gdn, d, dev, ws, every=256, reps=3):

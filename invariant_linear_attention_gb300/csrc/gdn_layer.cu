@@ -66,12 +66,20 @@ __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float
 // exp / log1p and a correctly rounded divide.
 __device__ __forceinline__ float sigmoid_f(float x) { return __fdiv_rn(1.f, __fadd_rn(1.f, expf(-x))); }
 __device__ __forceinline__ float softplus_f(float x) { return x > 20.f ? x : log1pf(expf(x)); }
-// SiLU on the streaming paths (conv output, RMSNorm gate): the hardware
-// exponential and the fast divide, a few ulp (far below the bf16 rounding of
-// the outputs) at a fraction of the instruction count, which these HBM-bound
-// kernels would otherwise be limited by.  Deterministic, and one function for
-// every kernel, so prefill and decode agree bit for bit.
-__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, __fadd_rn(1.f, __expf(-x))); }
+// SiLU on the streaming paths (conv output, RMSNorm gate): x * (1 / (1 + e^-x))
+// with the hardware exponential and the hardware approximate reciprocal, a
+// few ulp (far below the bf16 rounding of the outputs) at a fraction of the
+// instruction count, which these HBM-bound kernels would otherwise be limited
+// by.  The reciprocal is the bare rcp.approx.ftz instruction: for x < -87 the
+// exponential overflows to +inf and 1 / inf = 0, the limit SiLU has there.
+// Deterministic, and one function for every kernel, so prefill and decode
+// agree bit for bit.
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ float silu_fast(float x) { return __fmul_rn(x, rcp_approx(__fadd_rn(1.f, __expf(-x)))); }
 
 // ---------------------------------------------------------------- gates
 __device__ __forceinline__ void gate_one(float av, float bv, int h, const float* __restrict__ A_log,
@@ -94,6 +102,9 @@ __global__ void __launch_bounds__(256) gates_kernel(int64_t n, int HV, const Tin
 
 // Vector form (HV % 8 == 0): a thread takes 8 consecutive elements of one
 // token, 16-byte (bf16) or 2 x 16-byte (fp32) loads and 2 x 16-byte stores.
+// The grid stride (in elements) is a multiple of HV, so a thread keeps the
+// same 8 heads on every iteration: their -exp(A_log) and dt_bias are taken
+// once, before the token loop.
 template <typename Tin>
 __global__ void __launch_bounds__(256) gates_kernel_v8(int64_t n8, int HV, const Tin* __restrict__ a,
                                                        const Tin* __restrict__ b, const float* __restrict__ A_log,
@@ -101,9 +112,17 @@ __global__ void __launch_bounds__(256) gates_kernel_v8(int64_t n8, int HV, const
                                                        float* __restrict__ beta) {
     constexpr int VN = V16<Tin>::n;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < n8; v += stride) {
+    const int64_t v0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (v0 >= n8) return;
+    const int h0 = (int)((v0 * 8) % HV);
+    float nA[8], dtb[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        nA[e] = -expf(__ldg(A_log + h0 + e));
+        dtb[e] = dt_bias ? __ldg(dt_bias + h0 + e) : 0.f;
+    }
+    for (int64_t v = v0; v < n8; v += stride) {
         const int64_t i = v * 8;
-        const int h0 = (int)(i % HV);
         float av[8], bv[8], go[8], bo[8];
 #pragma unroll
         for (int j = 0; j < 8; j += VN) {
@@ -116,7 +135,11 @@ __global__ void __launch_bounds__(256) gates_kernel_v8(int64_t n8, int HV, const
             for (int e = 0; e < VN; ++e) bv[j + e] = t[e];
         }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) gate_one(av[e], bv[e], h0 + e, A_log, dt_bias, go[e], bo[e]);
+        for (int e = 0; e < 8; ++e) {
+            const float xg = dt_bias ? __fadd_rn(av[e], dtb[e]) : av[e];
+            go[e] = __fmul_rn(nA[e], softplus_f(xg));
+            bo[e] = sigmoid_f(bv[e]);
+        }
 #pragma unroll
         for (int j = 0; j < 8; j += 4) {
             const float ga[4] = {go[j], go[j + 1], go[j + 2], go[j + 3]};
@@ -326,36 +349,48 @@ __global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) conv_fwd_kernel(const C
     }
     const bool act = p.act != 0;
     // two register buffers of U rows: the loads of the next U rows are in
-    // flight while the current ones are computed and stored
+    // flight while the current ones are computed and stored.  Whole blocks of
+    // rows run without per-row conditions, so the window slides by register
+    // renaming inside a block; only the tail block checks each row.
     uint4 ra[U], rb[U];
     auto load = [&](uint4(&r)[U], int b0) {
 #pragma unroll
         for (int u = 0; u < U; ++u)
             if (b0 + u < t1) r[u] = ld16_stream(x + (int64_t)(b0 + u) * p.C + c0);
     };
-    auto consume = [&](const uint4(&r)[U], int b0) {
+    auto row = [&](const uint4& r, int t) {
+        float xc[VN], out[VN];
+        unpack(r, xc);
+        conv_point<W, VN>(taps, win, xc, act, out);
+        st16_stream(y + (int64_t)t * p.C + c0, pack(out));
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (b0 + u < t1) {
-                float xc[VN], out[VN];
-                unpack(r[u], xc);
-                conv_point<W, VN>(taps, win, xc, act, out);
-                st16_stream(y + (int64_t)(b0 + u) * p.C + c0, pack(out));
+        for (int i = 0; i + 1 < WM; ++i)
 #pragma unroll
-                for (int i = 0; i + 1 < WM; ++i)
+            for (int e = 0; e < VN; ++e) win[i][e] = win[i + 1][e];
 #pragma unroll
-                    for (int e = 0; e < VN; ++e) win[i][e] = win[i + 1][e];
+        for (int e = 0; e < VN; ++e) win[WM - 1][e] = xc[e];
+    };
+    auto consume_full = [&](const uint4(&r)[U], int b0) {
 #pragma unroll
-                for (int e = 0; e < VN; ++e) win[WM - 1][e] = xc[e];
-            }
-        }
+        for (int u = 0; u < U; ++u) row(r[u], b0 + u);
+    };
+    auto consume_tail = [&](const uint4(&r)[U], int b0) {
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (b0 + u < t1) row(r[u], b0 + u);
     };
     load(ra, t0);
-    for (int base = t0; base < t1; base += 2 * U) {
+    int base = t0;
+    for (; base + 2 * U <= t1; base += 2 * U) {
         load(rb, base + U);
-        consume(ra, base);
+        consume_full(ra, base);
         load(ra, base + 2 * U);
-        consume(rb, base + U);
+        consume_full(rb, base + U);
+    }
+    if (base < t1) {
+        load(rb, base + U);
+        consume_tail(ra, base);
+        consume_tail(rb, base + U);
     }
     if (k == 0 && has_slot) {
         // final state: the last W-1 rows of (initial state ++ the sequence)
@@ -369,6 +404,11 @@ __global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) conv_fwd_kernel(const C
     }
 }
 
+// Decode update: a CTA takes kUpdRows consecutive batch rows of one channel
+// block, so the staged taps serve all of them, and a thread's rows are
+// independent (all their loads in flight together).
+constexpr int kUpdRows = 8;
+
 template <typename T, int W>
 __global__ void __launch_bounds__(128) conv_update_kernel(const ConvParams p) {
     constexpr int VN = V16<T>::n;
@@ -376,24 +416,30 @@ __global__ void __launch_bounds__(128) conv_update_kernel(const ConvParams p) {
     __shared__ float4 stage[TapStage<W, VN>::kFloat4s];
     const int cblk0 = blockIdx.y * blockDim.x * VN;
     const int c0 = cblk0 + threadIdx.x * VN;
-    const int b = blockIdx.x;
-    const int slot = p.idx ? __ldg(p.idx + b) : b;
-    if (slot < 0 || slot >= p.num_slots) return;  // CTA-uniform
+    const int b0 = blockIdx.x * kUpdRows;
     ConvTaps<W, VN> taps;
-    load_taps<W, VN>(taps, stage, p.w, p.bias, cblk0, p.C);
+    load_taps<W, VN>(taps, stage, p.w, p.bias, cblk0, p.C);  // CTA-uniform up to here
     if (c0 >= p.C) return;
     const T* x = static_cast<const T*>(p.x);
     T* y = static_cast<T*>(p.y);
-    T* st = static_cast<T*>(p.state) + (int64_t)slot * WM * p.C + c0;
-    float win[WM][VN], xc[VN], out[VN];
+    const bool act = p.act != 0;
+#pragma unroll 2
+    for (int r = 0; r < kUpdRows; ++r) {
+        const int b = b0 + r;
+        if (b >= p.N) break;
+        const int slot = p.idx ? __ldg(p.idx + b) : b;
+        if (slot < 0 || slot >= p.num_slots) continue;
+        T* st = static_cast<T*>(p.state) + (int64_t)slot * WM * p.C + c0;
+        float win[WM][VN], xc[VN], out[VN];
 #pragma unroll
-    for (int i = 0; i < WM; ++i) unpack(ld16(st + (int64_t)i * p.C), win[i]);
-    unpack(ld16(x + (int64_t)b * p.C + c0), xc);
-    conv_point<W, VN>(taps, win, xc, p.act != 0, out);
-    st16(y + (int64_t)b * p.C + c0, pack(out));
+        for (int i = 0; i < WM; ++i) unpack(ld16(st + (int64_t)i * p.C), win[i]);
+        unpack(ld16(x + (int64_t)b * p.C + c0), xc);
+        conv_point<W, VN>(taps, win, xc, act, out);
+        st16(y + (int64_t)b * p.C + c0, pack(out));
 #pragma unroll
-    for (int i = 0; i + 1 < WM; ++i) st16(st + (int64_t)i * p.C, pack(win[i + 1]));
-    st16(st + (int64_t)(WM - 1) * p.C, pack(xc));
+        for (int i = 0; i + 1 < WM; ++i) st16(st + (int64_t)i * p.C, pack(win[i + 1]));
+        st16(st + (int64_t)(WM - 1) * p.C, pack(xc));
+    }
 }
 
 gdn_status check_conv(const gdn_conv_shape* s) {
@@ -450,10 +496,25 @@ extern "C" gdn_status gdn_gates(int64_t T, int HV, gdn_dtype in_dtype, const voi
         (dt_bias && !aligned4(dt_bias)))
         return GDN_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const bool vec = HV % 8 == 0 && aligned16(a) && aligned16(b) && aligned16(g) && aligned16(beta);
+    bool vec = HV % 8 == 0 && aligned16(a) && aligned16(b) && aligned16(g) && aligned16(beta);
+    // The vector form runs a few tokens per thread and keeps each thread on the same heads:
+    // when the grid does not cover every item at once, its stride of 2048 * grid elements must
+    // be a multiple of HV (true for any grid when HV divides 2048).  If no grid up to the cap
+    // qualifies, the scalar form runs instead.
+    int grid = 0;
+    if (vec) {
+        const int64_t want = (n / 8 + 255) / 256;
+        grid = (int)(want < kSMs * 4 ? want : kSMs * 4);
+        if (grid < want) {
+            while (grid > 1 && (2048LL * grid) % HV) --grid;
+            if ((2048LL * grid) % HV) vec = false;
+        }
+    }
     const int64_t items = vec ? n / 8 : n;
-    const int64_t want = (items + 255) / 256;
-    const int grid = (int)(want < kSMs * 16 ? want : kSMs * 16);
+    if (!vec) {
+        const int64_t want = (n + 255) / 256;
+        grid = (int)(want < kSMs * 16 ? want : kSMs * 16);
+    }
     if (in_dtype == GDN_BF16) {
         auto a_ = static_cast<const __nv_bfloat16*>(a);
         auto b_ = static_cast<const __nv_bfloat16*>(b);
@@ -551,7 +612,7 @@ extern "C" gdn_status gdn_causal_conv1d_update(const gdn_conv_shape* shape, cons
     const int vn = shape->dtype == GDN_BF16 ? 8 : 4;
     ConvParams p{shape->N, shape->T_total, shape->C, 1, x, weight, bias, nullptr, conv_state, state_indices,
                  num_slots, nullptr, y, shape->activation};
-    const dim3 grid((unsigned)shape->N, (unsigned)((shape->C / vn + 127) / 128));
+    const dim3 grid((unsigned)((shape->N + kUpdRows - 1) / kUpdRows), (unsigned)((shape->C / vn + 127) / 128));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return shape->dtype == GDN_BF16 ? dispatch_w<UpdK, __nv_bfloat16>(shape->W, grid, s, p)
                                     : dispatch_w<UpdK, float>(shape->W, grid, s, p);
