@@ -410,7 +410,11 @@ def main():
 
     # ---- end to end through the C ABI from pinned host buffers
     if not args.no_e2e and not small:
-        result["e2e"] = e2e(gdn, d.cpu(), dd.cpu(), st0.cpu(), dev, steps=min(steps, 5), device_ms=fwd_avg + dec_avg)
+        try:
+            result["e2e"] = e2e(gdn, d.cpu(), dd.cpu(), st0.cpu(), dev, steps=min(steps, 5),
+                                device_ms=fwd_avg + dec_avg)
+        except Exception as exc:  # reported, not hidden
+            result["e2e"] = {"error": str(exc)[:300]}
 
     # ---- backward on its own workload
     if not args.no_backward and not small:
