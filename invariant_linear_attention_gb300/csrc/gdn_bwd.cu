@@ -1246,8 +1246,8 @@ __device__ __forceinline__ float half_sum(float x) {
 
 // per (chunk, head), dk = dv = 128, bf16 inputs: bwd_wy_kernel on tcgen05.
 //   [K; Q] K^T (M = 128: rows 0..63 give K K^T, rows 64..127 give Q K^T; the B operand is the
-//   first 64 rows of the same shared-memory copy), A and P from them, T = (I + A)^-1 by blocked
-//   forward substitution (16 x 16 blocks), then W^T = K^T (T diag(beta Gam))^T
+//   first 64 rows of the same shared-memory copy), A and P from them, T = (I + A)^-1 by
+//   column-parallel forward substitution, then W^T = K^T (T diag(beta Gam))^T
 //   and U~^T = V^T (T diag(beta))^T with the dk / dv index as the M = 128 rows, so each epilogue
 //   thread stores one column of W and U~: coalesced.
 constexpr int kLdT = kC + 1;  // fp32 A and T in shared memory: row-per-lane writes hit distinct banks
@@ -1382,55 +1382,39 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_wy_tc_kernel(BwdParams p) {
                 vr[it] = s < len ? ld4_any(p.v, ((size_t)(t0 + s) * p.HV + h) * kD + k, p.dtype)
                                  : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            // T = (I + A)^-1 by 16 x 16 blocks.  Diagonal blocks: column c by the 8 lanes tid / 8,
-            // lane l holding T[16 b + jl + l + 8 m][c] (b = c / 16, jl = c % 16), rows in order,
-            // each row's dot over s = jl + l + 8 m then an 8-lane butterfly.  The 4 columns of a warp
-            // share a block and run the rows from the first of them, so every butterfly has all 32
-            // lanes.  Then block rows i = 1..3: M_ij = sum_{k=j..i-1} A_ik T_kj, T_ij = -T_ii M_ij.
+            // T = (I + A)^-1, one column per forward substitution: column j solves (I + A) t = e_j.
+            // Warp w takes columns {w, 31 - w, 32 + w, 63 - w} as four independent chains; lane l
+            // keeps the partial sums sigma_r = sum_{s < r} A[r][s] t[s] of rows r = l and l + 32.
+            // Right-looking, s = 0 .. 63 in order: the owner of row s holds its final sigma_s, so
+            // t[s] = (s == j) - sigma_s (0 above the diagonal); it is broadcast and every lane adds
+            // A[r][s] t[s] to its rows' partials (A is strictly lower, so rows r <= s add 0).  At
+            // the end T[r][j] = (r == j) - sigma_r for every row.  All indices are compile-time.
             {
-                const int col = tid >> 3, l = tid & 7, b0 = (col >> 4) * 16, jl = col & 15;
-                float t[2] = {0.f, 0.f};
-                for (int r = jl & ~3; r < 16; ++r) {
-                    float acc = 0.f;
+                const int w = tid >> 5;
+                const int cols[4] = {w, 31 - w, 32 + w, 63 - w};
+                float part[4][2];
 #pragma unroll
-                    for (int m = 0; m < 2; ++m) {
-                        const int s = jl + l + 8 * m;
-                        if (s < 16) acc = fmaf(sAf[(b0 + r) * kLdT + b0 + s], t[m], acc);
+                for (int c = 0; c < 4; ++c) part[c][0] = part[c][1] = 0.f;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+                    for (int sl = 0; sl < 32; ++sl) {
+                        const int s = 32 * hf + sl;
+                        const float a0 = sAf[lane * kLdT + s], a1 = sAf[(lane + 32) * kLdT + s];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const float own = (s == cols[c] ? 1.f : 0.f) - part[c][hf];
+                            const float ts = __shfl_sync(kFull, own, sl);
+                            part[c][0] = fmaf(a0, ts, part[c][0]);
+                            part[c][1] = fmaf(a1, ts, part[c][1]);
+                        }
                     }
-#pragma unroll
-                    for (int off = 4; off >= 1; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
-                    const float x = (r == jl ? 1.f : 0.f) - acc;
-                    const int d = r - jl;
-                    if (d >= 0 && (d & 7) == l) t[d >> 3] = x;
                 }
 #pragma unroll
-                for (int m = 0; m < 2; ++m) {
-                    const int r = jl + l + 8 * m;
-                    if (r < 16) sTf[(b0 + r) * kLdT + col] = t[m];
-                }
-                for (int r = l; r < b0 + jl; r += 8) sTf[r * kLdT + col] = 0.f;  // above the diagonal
-            }
-            float* sM = reinterpret_cast<float*>(sB2);  // scratch for M_ij, up to 3 blocks
-            for (int i = 1; i < 4; ++i) {
-                __syncthreads();
-                for (int e = tid; e < i * 256; e += kNTtc) {
-                    const int jb = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-                    float acc = 0.f;
-                    for (int k = jb; k < i; ++k)
+                for (int c = 0; c < 4; ++c)
 #pragma unroll
-                        for (int s = 0; s < 16; ++s)
-                            acc = fmaf(sAf[(16 * i + rr) * kLdT + 16 * k + s], sTf[(16 * k + s) * kLdT + 16 * jb + cc], acc);
-                    sM[e] = acc;
-                }
-                __syncthreads();
-                for (int e = tid; e < i * 256; e += kNTtc) {
-                    const int jb = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-                    float acc = 0.f;
-#pragma unroll
-                    for (int s = 0; s < 16; ++s)
-                        acc = fmaf(sTf[(16 * i + rr) * kLdT + 16 * i + s], sM[(jb << 8) + (s << 4) + cc], acc);
-                    sTf[(16 * i + rr) * kLdT + 16 * jb + cc] = -acc;
-                }
+                    for (int m = 0; m < 2; ++m)
+                        sTf[(lane + 32 * m) * kLdT + cols[c]] = (lane + 32 * m == cols[c] ? 1.f : 0.f) - part[c][m];
             }
             __syncthreads();
 #pragma unroll
