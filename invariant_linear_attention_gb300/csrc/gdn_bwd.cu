@@ -542,7 +542,7 @@ __global__ void __launch_bounds__(kNTs) bwd_state_bwd_kernel(BwdParams p, int R)
 // warps = 4 TMEM lane quarters x 4 column groups, and the staging strides) assume it.
 constexpr int kNTtc = 512;
 // At dk = 128 the chunk states S_c and D_c go out transposed (dk x dv), the layout in which
-// bwd_intra_s_tc_kernel takes them as K-major operands; other dk keep the row-major layout.
+// bwd_intra_tc_kernel takes them as K-major operands; other dk keep the row-major layout.
 template <int DK>
 constexpr bool kStateTransposed = DK == 128;
 constexpr uint32_t kSboC = kC * 32;  // 8 rows x 64 values x 4 bytes
@@ -1076,166 +1076,6 @@ __device__ __forceinline__ float warp_transpose_sum(float (&v)[NV]) {
     return v[0];
 }
 
-// per (chunk, head), dk = dv = 128, bf16 inputs: the products with S0 and D on tcgen05, in
-// transposed form (rows = the dk index j, 128 of them):
-//   X = S0^T [dO; dU]^T:  dQ_S[r][j] = Gam_r X[j][r] -> dqh,  dW[r][j] = -X[j][64 + r] -> Wb
-//   Y = D^T U^T:          dkh[r][j] = b_r Y[j][r],  b_r = exp(gam_last - gam_r)
-// and dgam_r = q^_r . dQ_S,r - b_r k^_r . Y_r  (+ sum_r b_r k^_r . Y_r + Gam_last <D, S0> on the
-// last row).  S0^T and D^T come from the tcgen05 state passes, which write them transposed.
-// The thread owning row j of an accumulator stores column j of each output row: coalesced.
-constexpr size_t kIntraSTcSmem = (size_t)4 * (2 * 128 * 128 + 2 * 4 * kC + 3 * kC + 16) + 16;
-
-__global__ void __launch_bounds__(kNTtc, 1) bwd_intra_s_tc_kernel(BwdParams p) {
-    constexpr int kD = 128;
-    constexpr uint32_t kSbo = kD * 32;
-    extern __shared__ __align__(128) uint8_t smb[];
-    uint8_t* sA = smb;                                          // A: S0^T, then D^T     128 x 128
-    uint8_t* sB = sA + kD * kD * 4;                             // B: [dO; dU], then U   128 x 128
-    float* red = reinterpret_cast<float*>(sB + kD * kD * 4);    // [2][4 quarters][64] partial sums
-    float* sg = red + 2 * 4 * kC;                               // gam
-    float* sdg = sg + kC;                                       // dgam
-    float* sbd = sdg + kC;                                      // b_r db_r
-    float* scr = sbd + kC;                                      // cta_sum scratch (16 warps)
-    uint64_t* bar = reinterpret_cast<uint64_t*>(scr + 16);
-    uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
-    const int c = blockIdx.x, h = blockIdx.y;
-    int n, t0, len;
-    if (!chunk_of(p, c, n, t0, len)) return;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, q = warp & 3, cg = warp >> 2;
-    const int j = q * 32 + lane;
-    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    const int hk = h / p.G;
-    const size_t ci = ch_index(p, c, h);
-    using M128 = RowsTc<kD, kD>;
-    if (tid == 0) {
-        mbar_init(bar, 1);
-        fence_barrier_init();
-    }
-    if (warp == 0) tmem_alloc(slot, 256);
-    M128 s0;  // S0^T in fp32, kept for <D, S0>
-    s0.load(p.Sb + ci * kD * kD);
-    {
-        float4 b[M128::kItems];  // B rows 0..63: dO[t0 + r][h] (zero for r >= len); rows 64..127: dU[r]
-#pragma unroll
-        for (int it = 0; it < M128::kItems; ++it) {
-            const int r = M128::row(it), k = M128::col(it);
-            if (r < kC) b[it] = r < len ? ld4_any(p.dout, ((size_t)(t0 + r) * p.HV + h) * kD + k, p.dtype)
-                                        : make_float4(0.f, 0.f, 0.f, 0.f);
-            else b[it] = *reinterpret_cast<const float4*>(p.dUb + (ci * kC + (r - kC)) * kD + k);
-        }
-        s0.put(sA);
-#pragma unroll
-        for (int it = 0; it < M128::kItems; ++it)
-            *reinterpret_cast<float4*>(sB + umma_koff(M128::row(it), M128::col(it), kSbo)) = tf32_round4(b[it]);
-    }
-    for (int r = tid; r < kC; r += blockDim.x) sg[r] = r < len ? p.gam[(size_t)(t0 + r) * p.HV + h] : 0.f;
-    tc_sync();
-    const uint32_t tmem = *slot;
-    uint32_t phase = 0;
-    float dot = 0.f;
-    bool ok;
-    do {
-        if (tid == 0) {
-            umma_tf32_k(tmem, smem_u32(sA), kSbo, smem_u32(sB), kSbo, umma_idesc_tf32(kD, kD), kD, false);
-            umma_commit(bar);
-        }
-        if (!(ok = tc_wait(bar, phase))) break;
-        {
-            float x[32];
-            tmem_ld<4>(tmem + lane_base + cg * 32, x);
-            if (cg < 2) {  // dQ_S rows r = 32 cg + m, and q^_r . dQ_S,r
-                float qv[32];
-#pragma unroll
-                for (int m = 0; m < 32; ++m) {
-                    const int r = cg * 32 + m;
-                    qv[m] = r < len ? p.qn[((size_t)(t0 + r) * p.HK + hk) * kD + j] : 0.f;
-                }
-#pragma unroll
-                for (int m = 0; m < 32; ++m) {
-                    const int r = cg * 32 + m;
-                    const float d = r < len ? __expf(sg[r]) * x[m] : 0.f;
-                    if (r < len) p.dqh[((size_t)(t0 + r) * p.HV + h) * kD + j] = d;
-                    x[m] = qv[m] * d;
-                }
-                const float part = warp_transpose_sum<32>(x);
-                red[q * kC + cg * 32 + lane] = part;
-            } else {  // dW rows r = 32 (cg - 2) + m
-                float* dW = p.Wb + ci * kC * kD + j;
-#pragma unroll
-                for (int m = 0; m < 32; ++m) dW[(size_t)((cg - 2) * 32 + m) * kD] = -x[m];
-            }
-        }
-        tc_fence_before();
-        __syncthreads();  // the first product and every read of its result are done
-        {
-            M128 dt;
-            RowsTc<kC, kD> u;
-            dt.load(p.Db + ci * kD * kD);
-            u.load(p.Ub + ci * kC * kD);
-#pragma unroll
-            for (int it = 0; it < M128::kItems; ++it) {
-                dot = fmaf(dt.v[it].x, s0.v[it].x, dot);
-                dot = fmaf(dt.v[it].y, s0.v[it].y, dot);
-                dot = fmaf(dt.v[it].z, s0.v[it].z, dot);
-                dot = fmaf(dt.v[it].w, s0.v[it].w, dot);
-            }
-            dt.put(sA);
-            u.put(sB);
-        }
-        tc_sync();
-        if (tid == 0) {
-            umma_tf32_k(tmem + 128, smem_u32(sA), kSbo, smem_u32(sB), kSbo, umma_idesc_tf32(kD, kC), kD, false);
-            umma_commit(bar);
-        }
-        if (!(ok = tc_wait(bar, phase))) break;
-        {  // dkh rows r = 16 cg + m, and k^_r . (U D)_r
-            const float gl = sg[len - 1];
-            float x[16], kv[16];
-#pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const int r = cg * 16 + m;
-                kv[m] = r < len ? p.kn[((size_t)(t0 + r) * p.HK + hk) * kD + j] : 0.f;
-            }
-            tmem_ld<2>(tmem + lane_base + 128 + cg * 16, x);
-#pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const int r = cg * 16 + m;
-                if (r < len) p.dkh[((size_t)(t0 + r) * p.HV + h) * kD + j] = __expf(gl - sg[r]) * x[m];
-                x[m] = kv[m] * x[m];
-            }
-            const float part = warp_transpose_sum<16>(x);
-            if (lane < 16) red[4 * kC + q * kC + cg * 16 + lane] = part;
-        }
-    } while (false);
-    const float dS = cta_sum(dot, scr);  // all threads, whatever ok says
-    if (ok) {
-        const float gl = sg[len - 1];
-        for (int r = tid; r < kC; r += blockDim.x) {
-            float dg = 0.f, bd = 0.f;
-            if (r < len) {
-                dg = ((red[r] + red[kC + r]) + red[2 * kC + r]) + red[3 * kC + r];
-                bd = __expf(gl - sg[r]) *
-                     (((red[4 * kC + r] + red[5 * kC + r]) + red[6 * kC + r]) + red[7 * kC + r]);
-            }
-            sdg[r] = dg - bd;
-            sbd[r] = bd;
-        }
-        __syncthreads();
-        if (tid == 0) {
-            float tot = 0.f;
-            for (int r = 0; r < len; ++r) tot += sbd[r];
-            sdg[len - 1] += tot + __expf(gl) * dS;
-        }
-        __syncthreads();
-        float* dga = p.dgamA + ci * kC;
-        for (int r = tid; r < kC; r += blockDim.x) dga[r] = sdg[r];
-    }
-    if (!ok && tid == 0) atomicOr(p.err, GDN_DEVERR_TIMEOUT);
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 256);
-}
-
 // Sum over the 16 lanes of a half warp (xor butterfly, fixed order); every lane gets the sum.
 // All 32 lanes of the warp must call it.
 __device__ __forceinline__ float half_sum(float x) {
@@ -1668,16 +1508,25 @@ __device__ __forceinline__ void async_rows(uint8_t* dst, P ptr) {
     }
 }
 
-// per (chunk, head), dk = dv = 128, bf16 inputs: bwd_intra_c_kernel on tcgen05.  The C x C
-// products (dP = dO U^T, K K^T, F1 = dW K^T, F2 = dU V^T, Z = dT T^T, T^T Z) use M = 64: row m
-// of the result sits in TMEM lane 32 (m / 16) + m % 16, so lanes 0..15 of each warp hold 16 rows.
-// The products that update dq, dk, dv are taken transposed with the dk / dv index as their 128
-// rows; dk's three terms accumulate in TMEM and meet global memory once.
-//   TMEM columns: 0 dP, then Z | 64 K K^T | 128 dq^T | 192 dk^T | 256 dv^T | 320 F1 | 384 F2 | 448 T^T Z
-//   shared memory: five 32 KB operand buffers R1..R5 and two 16 KB ones C1, C2, reused by phase
+// per (chunk, head), dk = dv = 128, bf16 inputs: bwd_intra_s_kernel and bwd_intra_c_kernel in one
+// kernel on tcgen05.  The products with the chunk states come first, in transposed form (rows = the
+// dk index j):
+//   X_q = S0^T dO^T:  dQ_S[r][j] = Gam_r X_q[j][r]      X_w = S0^T dU^T:  dW[s][j] = -X_w[j][s]
+//   Y = D^T U^T:      (diag(b) U D)[r][j] = b_r Y[j][r]  and dW = -(dU S0) once more with M = 64
+// and dgam_r = q^_r . dQ_S,r - b_r k^_r . Y_r (+ sum_r b_r k^_r . Y_r + Gam_last <D, S0> on the last
+// row).  Gam_r X_q and b_r Y go back into TMEM (tcgen05.st) as the first terms of the dq^T and
+// dk^T accumulators; dW stays on chip, as F1's operand and, from X_w, as the transposed one.
+// The C x C products (dP = dO U^T, K K^T, F1 = dW K^T, F2 = dU V^T, Z = dT T^T, T^T Z) use M = 64:
+// row m of the result sits in TMEM lane 32 (m / 16) + m % 16, so lanes 0..15 of each warp hold 16
+// rows.  The products that update dq, dk, dv are taken transposed with the dk / dv index as their
+// 128 rows; dq's two and dk's four terms accumulate in TMEM and meet global memory once.
+//   TMEM columns: 0 dP, then Z | 64 K K^T | 128 X_q, then dq^T | 192 Y, then dk^T | 256 X_w, then
+//   dv^T | 320 dU S0 (128 wide), then F1 | 384 F2 | 448 T^T Z
+//   shared memory: five 32 KB operand buffers R1..R5 and two 16 KB ones C1, C2 (together one
+//   32 KB buffer at first), reused by phase; S0^T and D^T enter in two K-halves of 32 KB
 constexpr size_t kIntraCTcSmem = (size_t)5 * 32768 + 2 * 16384 + 4 * kC * kLdT + 4 * (4 * kC + 3 * 4 * kC) + 16;
 
-__global__ void __launch_bounds__(kNTtc, 1) bwd_intra_c_tc_kernel(BwdParams p) {
+__global__ void __launch_bounds__(kNTtc, 1) bwd_intra_tc_kernel(BwdParams p) {
     constexpr int kD = 128;
     constexpr uint32_t kSboD = kD * 32;  // 128 values per row
     extern __shared__ __align__(128) uint8_t smb[];
@@ -1719,38 +1568,148 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_intra_c_tc_kernel(BwdParams p) {
         fence_barrier_init();
     }
     if (warp == 0) tmem_alloc(slot, 512);
-    // phase A: K^ -> R1, dO -> R2, U -> R3, dW -> R4, dU -> R5 (rows = chunk positions); the fp32
-    // ones by 16-byte cp.async, all in flight together with dO's loads
+    // phase A: K^ -> R1, dO -> R2, U -> R3, dU -> R5 (rows = chunk positions), S0^T in two K-halves
+    // -> R4 and C1|C2 (rows j, k = i); the fp32 ones by 16-byte cp.async, all in flight together
+    // with dO's loads
     using RowsD = RowsTc<kC, kD>;
+    using HalfS = RowsTc<kD, kC>;             // one K-half (64 values of i) of a 128 x 128 state
+    const float* S0t = p.Sb + ci * kD * kD;   // S0^T: row j (dk index), dv index contiguous
+    const float* Dt = p.Db + ci * kD * kD;    // D^T, the same layout
     async_rows<kC, kD>(R1, [&](int s, int k) { return s < len ? kb + s * sk + k : nullptr; });
     async_rows<kC, kD>(R3, [&](int s, int k) { return p.Ub + (ci * kC + s) * kD + k; });
-    async_rows<kC, kD>(R4, [&](int s, int k) { return p.Wb + (ci * kC + s) * kD + k; });
     async_rows<kC, kD>(R5, [&](int s, int k) { return p.dUb + (ci * kC + s) * kD + k; });
+    async_rows<kD, kC>(R4, [&](int j, int i) { return S0t + j * kD + i; });
+    async_rows<kD, kC>(C1, [&](int j, int i) { return S0t + j * kD + kC + i; });
     stage_rows_fn<kC, kD>(R2, [&](int r, int k) { return r < len ? ld4_any(p.dout, ob + r * sv + k, p.dtype) : z4; });
     for (int i = tid; i < kC; i += kNTtc) {
         sg[i] = i < len ? p.gam[(size_t)(t0 + i) * p.HV + h] : 0.f;
         sbe[i] = i < len ? p.beta[(size_t)(t0 + i) * p.HV + h] : 0.f;
-        sdg[i] = p.dgamA[ci * kC + i];
         sdb[i] = 0.f;
     }
     cp_async_wait_all();
     RowsD::round_in_place(R1);
     RowsD::round_in_place(R3);
-    RowsD::round_in_place(R4);
     RowsD::round_in_place(R5);
+    HalfS::round_in_place(R4);
+    HalfS::round_in_place(C1);
     tc_sync();
     const uint32_t tmem = *slot;
-    const uint32_t id64 = umma_idesc_tf32(kC, kC), id128 = umma_idesc_tf32(kD, kC);
+    const uint32_t id64 = umma_idesc_tf32(kC, kC), id128 = umma_idesc_tf32(kD, kC), id64w = umma_idesc_tf32(kC, kD);
     uint32_t phase = 0;
     bool ok;
     do {
         if (tid == 0) {
-            umma_tf32_k(tmem + 0, smem_u32(R2), kSboD, smem_u32(R3), kSboD, id64, kD, false);    // dP
+            const uint32_t h0 = smem_u32(R4), h1 = smem_u32(C1), o2 = smem_u32(R2), u5 = smem_u32(R5);
+            umma_tf32_k(tmem + 0, o2, kSboD, smem_u32(R3), kSboD, id64, kD, false);              // dP
             umma_tf32_k(tmem + 64, smem_u32(R1), kSboD, smem_u32(R1), kSboD, id64, kD, false);   // K K^T
-            umma_tf32_k(tmem + 320, smem_u32(R4), kSboD, smem_u32(R1), kSboD, id64, kD, false);  // F1
+            umma_tf32_k(tmem + 128, h0, kSboC, o2, kSboD, id128, kC, false);                     // X_q
+            umma_tf32_k(tmem + 128, h1, kSboC, o2 + 2048, kSboD, id128, kC, true);
+            umma_tf32_k(tmem + 256, h0, kSboC, u5, kSboD, id128, kC, false);                     // X_w
+            umma_tf32_k(tmem + 256, h1, kSboC, u5 + 2048, kSboD, id128, kC, true);
+            umma_tf32_k(tmem + 320, u5, kSboD, h0, kSboC, id64w, kC, false);                     // dU S0
+            umma_tf32_k(tmem + 320, u5 + 2048, kSboD, h1, kSboC, id64w, kC, true);
             umma_commit(bar);
         }
+        // D^T (and S0^T in fp32, for <D, S0>) by K-halves; the first half's loads fly during the products
+        float dot = 0.f;
+        float4 dh[HalfS::kItems], sh[HalfS::kItems];
+        auto load_half = [&](int hf) {
+#pragma unroll
+            for (int it = 0; it < HalfS::kItems; ++it) {
+                const int j = HalfS::row(it), i = HalfS::col(it) + kC * hf;
+                dh[it] = *reinterpret_cast<const float4*>(Dt + j * kD + i);
+                sh[it] = *reinterpret_cast<const float4*>(S0t + j * kD + i);
+            }
+        };
+        auto put_half = [&](uint8_t* dst) {
+#pragma unroll
+            for (int it = 0; it < HalfS::kItems; ++it) {
+                dot = fmaf(dh[it].x, sh[it].x, dot);
+                dot = fmaf(dh[it].y, sh[it].y, dot);
+                dot = fmaf(dh[it].z, sh[it].z, dot);
+                dot = fmaf(dh[it].w, sh[it].w, dot);
+                *reinterpret_cast<float4*>(dst + umma_koff(HalfS::row(it), HalfS::col(it), kSboC)) = tf32_round4(dh[it]);
+            }
+        };
+        load_half(0);
         if (!(ok = tc_wait(bar, phase))) break;
+        // phase A2: the products above have read dO and both halves of S0^T
+        put_half(R2);
+        load_half(1);
+        put_half(C1);
+        {  // dW = -(dU S0) -> R4 (rows s, k = j): F1's A operand
+            float x[32];
+            tmem_ld<4>(tmem + lane_base + 320 + cg * 32, x);
+            if (row_lane) {
+#pragma unroll
+                for (int t = 0; t < 32; t += 4)
+                    *reinterpret_cast<float4*>(R4 + umma_koff(r64, cg * 32 + t, kSboD)) =
+                        tf32_round4(make_float4(-x[t], -x[t + 1], -x[t + 2], -x[t + 3]));
+            }
+        }
+        tc_sync();
+        if (tid == 0) {
+            umma_tf32_k(tmem + 192, smem_u32(R2), kSboC, smem_u32(R3), kSboD, id128, kC, false);         // Y
+            umma_tf32_k(tmem + 192, smem_u32(C1), kSboC, smem_u32(R3) + 2048, kSboD, id128, kC, true);
+            umma_tf32_k(tmem + 320, smem_u32(R4), kSboD, smem_u32(R1), kSboD, id64, kD, false);          // F1
+            umma_commit(bar);
+        }
+        const float gl = sg[len - 1];
+        {  // Gam_r X_q back into TMEM as dq^T's first term; q^_r . dQ_S,r
+            float x[16], v[16];
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                const int r = cg * 16 + m;
+                v[m] = r < len ? qb[(size_t)r * sk + jj] : 0.f;
+            }
+            tmem_ld<2>(tmem + lane_base + 128 + cg * 16, x);
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                const int r = cg * 16 + m;
+                const float d = r < len ? __expf(sg[r]) * x[m] : 0.f;
+                x[m] = d;
+                v[m] *= d;
+            }
+            tmem_st<2>(tmem + lane_base + 128 + cg * 16, x);
+            const float part = warp_transpose_sum<16>(v);
+            if (lane < 16) part1[q * kC + cg * 16 + lane] = part;
+        }
+        float kv[16];
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const int r = cg * 16 + m;
+            kv[m] = r < len ? kb[(size_t)r * sk + jj] : 0.f;
+        }
+        if (!(ok = tc_wait(bar, phase))) break;
+        {  // b_r Y back into TMEM as dk^T's first term; k^_r . Y_r
+            float x[16];
+            tmem_ld<2>(tmem + lane_base + 192 + cg * 16, x);
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                const int r = cg * 16 + m;
+                kv[m] *= x[m];
+                x[m] = r < len ? __expf(gl - sg[r]) * x[m] : 0.f;
+            }
+            tmem_st<2>(tmem + lane_base + 192 + cg * 16, x);
+            const float part = warp_transpose_sum<16>(kv);
+            if (lane < 16) part2[q * kC + cg * 16 + lane] = part;
+        }
+        const float dS = cta_sum(dot, rowp + kC);  // its barriers also publish part1 / part2
+        for (int r = tid; r < kC; r += kNTtc) {
+            float dg = 0.f, bd = 0.f;
+            if (r < len) {
+                dg = ((part1[r] + part1[kC + r]) + part1[2 * kC + r]) + part1[3 * kC + r];
+                bd = __expf(gl - sg[r]) * (((part2[r] + part2[kC + r]) + part2[2 * kC + r]) + part2[3 * kC + r]);
+            }
+            sdg[r] = dg - bd;
+            rowp[r] = bd;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float tot = 0.f;
+            for (int r = 0; r < len; ++r) tot += rowp[r];
+            sdg[len - 1] += tot + __expf(gl) * dS;
+        }
         // phase B: dQK = lower(dP) E, dE = lower(dP) QK; dQK (C1) and its transpose (C2)
         {
             float x[16];
@@ -1786,8 +1745,8 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_intra_c_tc_kernel(BwdParams p) {
         tc_sync();
         if (tid == 0) {
             umma_tf32_k(tmem + 384, smem_u32(R5), kSboD, smem_u32(R2), kSboD, id64, kD, false);   // F2
-            umma_tf32_k(tmem + 128, smem_u32(R3), kSboC, smem_u32(C1), kSboC, id128, kC, false);  // dq^T
-            umma_tf32_k(tmem + 192, smem_u32(R1), kSboC, smem_u32(C2), kSboC, id128, kC, false);  // dk^T
+            umma_tf32_k(tmem + 128, smem_u32(R3), kSboC, smem_u32(C1), kSboC, id128, kC, true);   // dq^T
+            umma_tf32_k(tmem + 192, smem_u32(R1), kSboC, smem_u32(C2), kSboC, id128, kC, true);   // dk^T
             umma_commit(bar);
         }
         if (!(ok = tc_wait(bar, phase))) break;
@@ -1822,23 +1781,25 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_intra_c_tc_kernel(BwdParams p) {
                 part1[q * kC + cg * 16 + lane] = a1;
                 part2[q * kC + cg * 16 + lane] = a2;
             }
-            float x[16], old[16];
+            float x[16];
             float* dq = p.dqh + ((size_t)t0 * p.HV + h) * kD + jj;
-#pragma unroll
-            for (int t = 0; t < 16; ++t) {
-                const int r = cg * 16 + t;
-                old[t] = r < len ? dq[(size_t)r * p.HV * kD] : 0.f;
-            }
             tmem_ld<2>(tmem + lane_base + 128 + cg * 16, x);
 #pragma unroll
             for (int t = 0; t < 16; ++t) {
                 const int r = cg * 16 + t;
-                if (r < len) dq[(size_t)r * p.HV * kD] = old[t] + x[t];
+                if (r < len) dq[(size_t)r * p.HV * kD] = x[t];
             }
         }
-        // dW^T -> R2, dU^T -> R1 (rows j / i, k = s); diag(beta Gam)-scaled T^T -> C1, diag(beta)-scaled
-        // T^T -> C2 (rows r, k = s); T -> R4 + 16 KB (rows b, k = c)
-        stage_cols_fn<kD, kC>(R2, [&](int s, int j) { return p.Wb[(ci * kC + s) * kD + j]; });
+        // dW^T = -X_w -> R2, dU^T -> R1 (rows j / i, k = s); diag(beta Gam)-scaled T^T -> C1,
+        // diag(beta)-scaled T^T -> C2 (rows r, k = s); T -> R4 + 16 KB (rows b, k = c)
+        {
+            float x[16];
+            tmem_ld<2>(tmem + lane_base + 256 + cg * 16, x);
+#pragma unroll
+            for (int t = 0; t < 16; t += 4)
+                *reinterpret_cast<float4*>(R2 + umma_koff(jj, cg * 16 + t, kSboC)) =
+                    tf32_round4(make_float4(-x[t], -x[t + 1], -x[t + 2], -x[t + 3]));
+        }
         stage_cols_fn<kD, kC>(R1, [&](int s, int i) { return p.dUb[(ci * kC + s) * kD + i]; });
         stage_cols_fn<kC, kC>(C1, [&](int s, int r) { return Tg[s * kC + r] * sbe[r] * __expf(sg[r]); });
         stage_cols_fn<kC, kC>(C2, [&](int s, int r) { return Tg[s * kC + r] * sbe[r]; });
@@ -1921,20 +1882,15 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_intra_c_tc_kernel(BwdParams p) {
             umma_commit(bar);
         }
         if (!(ok = tc_wait(bar, phase))) break;
-        // phase F: dk update (all three terms at once)
+        // phase F: dk out (all four terms at once)
         {
-            float x[16], old[16];
+            float x[16];
             float* dkk = p.dkh + ((size_t)t0 * p.HV + h) * kD + jj;
-#pragma unroll
-            for (int t = 0; t < 16; ++t) {
-                const int r = cg * 16 + t;
-                old[t] = r < len ? dkk[(size_t)r * p.HV * kD] : 0.f;
-            }
             tmem_ld<2>(tmem + lane_base + 192 + cg * 16, x);
 #pragma unroll
             for (int t = 0; t < 16; ++t) {
                 const int r = cg * 16 + t;
-                if (r < len) dkk[(size_t)r * p.HV * kD] = old[t] + x[t];
+                if (r < len) dkk[(size_t)r * p.HV * kD] = x[t];
             }
         }
     } while (false);
@@ -2182,18 +2138,13 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
     }
 
     if (tc_state && s->dk == 128) {
-        if (!set_smem(bwd_intra_s_tc_kernel, kIntraSTcSmem)) return GDN_ERR_CUDA;
-        bwd_intra_s_tc_kernel<<<gch, kNTtc, kIntraSTcSmem, cs>>>(p);
+        if (!set_smem(bwd_intra_tc_kernel, kIntraCTcSmem)) return GDN_ERR_CUDA;
+        bwd_intra_tc_kernel<<<gch, kNTtc, kIntraCTcSmem, cs>>>(p);
     } else {
         const size_t smem_is = sizeof(float) * (kMaxD * kLdD + 4 * kC * kLdD + 2 * kC + 32);
         if (!set_smem(bwd_intra_s_kernel, smem_is)) return GDN_ERR_CUDA;
         bwd_intra_s_kernel<<<gch, kNT, smem_is, cs>>>(p);
-    }
-    if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
-    if (tc_state && s->dk == 128) {
-        if (!set_smem(bwd_intra_c_tc_kernel, kIntraCTcSmem)) return GDN_ERR_CUDA;
-        bwd_intra_c_tc_kernel<<<gch, kNTtc, kIntraCTcSmem, cs>>>(p);
-    } else {
+        if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
         const size_t smem_ic = sizeof(float) * (4 * kC * kLdD + 4 * kC * kLdC + 4 * kC);
         if (!set_smem(bwd_intra_c_kernel, smem_ic)) return GDN_ERR_CUDA;
         bwd_intra_c_kernel<<<gch, kNT, smem_ic, cs>>>(p);

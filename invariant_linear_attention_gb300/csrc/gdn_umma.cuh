@@ -115,4 +115,19 @@ __device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[8 * NX]) {
     }
 }
 
+// The reverse of tmem_ld: v into columns [col, col + 8 * NX) of this warp's 32 lanes, then a wait
+// for the stores, so that a barrier after it orders them before the next MMA on those columns.
+template <int NX>
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const float (&v)[8 * NX]) {
+#pragma unroll
+    for (int x = 0; x < NX; ++x)
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr + 8u * x),
+                     "r"(__float_as_uint(v[8 * x])), "r"(__float_as_uint(v[8 * x + 1])), "r"(__float_as_uint(v[8 * x + 2])),
+                     "r"(__float_as_uint(v[8 * x + 3])), "r"(__float_as_uint(v[8 * x + 4])),
+                     "r"(__float_as_uint(v[8 * x + 5])), "r"(__float_as_uint(v[8 * x + 6])),
+                     "r"(__float_as_uint(v[8 * x + 7]))
+                     : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 }  // namespace gdn
