@@ -1523,10 +1523,16 @@ __device__ __forceinline__ void async_rows(uint8_t* dst, P ptr) {
 //   TMEM columns: 0 dP, then Z | 64 K K^T | 128 X_q, then dq^T | 192 Y, then dk^T | 256 X_w, then
 //   dv^T | 320 dU S0 (128 wide), then F1 | 384 F2 | 448 T^T Z
 //   shared memory: five 32 KB operand buffers R1..R5 and two 16 KB ones C1, C2 (together one
-//   32 KB buffer at first), reused by phase; S0^T and D^T enter in two K-halves of 32 KB
-constexpr size_t kIntraCTcSmem = (size_t)5 * 32768 + 2 * 16384 + 4 * kC * kLdT + 4 * (4 * kC + 3 * 4 * kC) + 16;
+//   32 KB buffer at first), reused by phase; S0^T and D^T enter in two K-halves of 32 KB.
+// K^, U, dU and S0^T arrive by tensor copies (one thread, one mbarrier) in the MN-interleaved
+// layout (k groups rows * 16 bytes apart, row groups 128 bytes apart); every operand written by
+// threads later uses the k-contiguous layout of umma_koff.
+constexpr size_t kIntraCTcSmem = (size_t)5 * 32768 + 2 * 16384 + 4 * kC * kLdT + 4 * (4 * kC + 3 * 4 * kC) + 32;
 
-__global__ void __launch_bounds__(kNTtc, 1) bwd_intra_tc_kernel(BwdParams p) {
+__global__ void __launch_bounds__(kNTtc, 1)
+    bwd_intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_u,
+                        const __grid_constant__ CUtensorMap tm_du, const __grid_constant__ CUtensorMap tm_s,
+                        BwdParams p) {
     constexpr int kD = 128;
     constexpr uint32_t kSboD = kD * 32;  // 128 values per row
     extern __shared__ __align__(128) uint8_t smb[];
@@ -1546,7 +1552,8 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_intra_tc_kernel(BwdParams p) {
     float* part2 = part1 + 4 * kC;                      // [4][64] column-dot partials (F2)
     float* rowp = part2 + 4 * kC;                       // [4][64] row-loop partials
     uint64_t* bar = reinterpret_cast<uint64_t*>(rowp + 4 * kC);
-    uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
+    uint64_t* bar_ld = bar + 1;  // the tensor copies of phase A
+    uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 2);
     const int c = blockIdx.x, h = blockIdx.y;
     int n, t0, len;
     if (!chunk_of(p, c, n, t0, len)) return;
@@ -1563,80 +1570,100 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_intra_tc_kernel(BwdParams p) {
     const float* qb = p.qn + ((size_t)t0 * p.HK + hk) * kD;
     const size_t ob = ((size_t)t0 * p.HV + h) * kD;           // dO / V row r at ob + r * sv
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    // MN-interleaved operands: 64 rows x 128 (K^, U, dU) and 128 rows x 64 (a K-half of S0^T)
+    constexpr uint32_t kLboR = kC * 16, kLboH = kD * 16, kSboI = 128, kHalfR = 16 * kLboR;
+    // phase A: K^ -> R1, U -> R3, dU -> R5 (rows = chunk positions), S0^T in two K-halves -> R4 and
+    // C1|C2 (rows j, k = i), all by tensor copies; dO -> R2 through registers meanwhile
     if (tid == 0) {
         mbar_init(bar, 1);
+        mbar_init(bar_ld, 1);
         fence_barrier_init();
+        mbar_arrive_expect_tx(bar_ld, 5u * 32768u);
+        tma_load_3d(R1, &tm_k, bar_ld, 0, t0, 32 * hk);
+        tma_load_3d(R3, &tm_u, bar_ld, 0, (int)(ci * kC), 0);
+        tma_load_3d(R5, &tm_du, bar_ld, 0, (int)(ci * kC), 0);
+        tma_load_3d(R4, &tm_s, bar_ld, 0, (int)(ci * kD), 0);
+        tma_load_3d(C1, &tm_s, bar_ld, 0, (int)(ci * kD), 16);
     }
     if (warp == 0) tmem_alloc(slot, 512);
-    // phase A: K^ -> R1, dO -> R2, U -> R3, dU -> R5 (rows = chunk positions), S0^T in two K-halves
-    // -> R4 and C1|C2 (rows j, k = i); the fp32 ones by 16-byte cp.async, all in flight together
-    // with dO's loads
-    using RowsD = RowsTc<kC, kD>;
-    using HalfS = RowsTc<kD, kC>;             // one K-half (64 values of i) of a 128 x 128 state
-    const float* S0t = p.Sb + ci * kD * kD;   // S0^T: row j (dk index), dv index contiguous
-    const float* Dt = p.Db + ci * kD * kD;    // D^T, the same layout
-    async_rows<kC, kD>(R1, [&](int s, int k) { return s < len ? kb + s * sk + k : nullptr; });
-    async_rows<kC, kD>(R3, [&](int s, int k) { return p.Ub + (ci * kC + s) * kD + k; });
-    async_rows<kC, kD>(R5, [&](int s, int k) { return p.dUb + (ci * kC + s) * kD + k; });
-    async_rows<kD, kC>(R4, [&](int j, int i) { return S0t + j * kD + i; });
-    async_rows<kD, kC>(C1, [&](int j, int i) { return S0t + j * kD + kC + i; });
+    const float* Dt = p.Db + ci * kD * kD;    // D^T: row j (dk index), dv index contiguous
+    // D^T (fp32) into registers at the float4 positions f = tid + 512 it of the S0^T halves that this
+    // thread rounds below (row j = f % 128, k group f / 128): <D, S0> then takes S0 as copied
+    float4 dreg[2][4];
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int f = tid + it * kNTtc;
+            dreg[hf][it] = *reinterpret_cast<const float4*>(Dt + (f % kD) * kD + kC * hf + 4 * (f / kD));
+        }
     stage_rows_fn<kC, kD>(R2, [&](int r, int k) { return r < len ? ld4_any(p.dout, ob + r * sv + k, p.dtype) : z4; });
     for (int i = tid; i < kC; i += kNTtc) {
         sg[i] = i < len ? p.gam[(size_t)(t0 + i) * p.HV + h] : 0.f;
         sbe[i] = i < len ? p.beta[(size_t)(t0 + i) * p.HV + h] : 0.f;
         sdb[i] = 0.f;
     }
-    cp_async_wait_all();
-    RowsD::round_in_place(R1);
-    RowsD::round_in_place(R3);
-    RowsD::round_in_place(R5);
-    HalfS::round_in_place(R4);
-    HalfS::round_in_place(C1);
+    __syncthreads();  // the barriers' initialisation is visible
+    bool ok = __syncthreads_and(mbar_wait_bounded(bar_ld, 0));
+    float dot = 0.f;  // this thread's share of <D, S0>, in fp32
+    if (ok) {
+        // TF32 rounding of the copied operands (five 32 KB buffers, any layout), and zero rows of K^
+        // past the chunk (the copy fills them from the next sequence)
+        uint8_t* const bufs[3] = {R1, R3, R5};
+#pragma unroll
+        for (int b = 0; b < 3; ++b)
+#pragma unroll
+            for (int it = 0; it < 32768 / 16 / kNTtc; ++it) {
+                float4* v = reinterpret_cast<float4*>(bufs[b]) + tid + it * kNTtc;
+                *v = tf32_round4(*v);
+            }
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+                float4* v = reinterpret_cast<float4*>(hf ? C1 : R4) + tid + it * kNTtc;
+                const float4 x = *v, d = dreg[hf][it];
+                dot = fmaf(d.x, x.x, dot);
+                dot = fmaf(d.y, x.y, dot);
+                dot = fmaf(d.z, x.z, dot);
+                dot = fmaf(d.w, x.w, dot);
+                *v = tf32_round4(x);
+            }
+        if (len < kC)
+            for (int e = tid; e < (kC - len) * (kD / 4); e += kNTtc) {
+                const int r = len + e / (kD / 4), kg = e % (kD / 4);
+                *reinterpret_cast<float4*>(R1 + kg * kLboR + r * 16) = z4;
+            }
+    } else if (tid == 0) {
+        mbar_wait_bounded(bar_ld, 0);  // let copies still in flight land before the CTA leaves
+    }
     tc_sync();
     const uint32_t tmem = *slot;
     const uint32_t id64 = umma_idesc_tf32(kC, kC), id128 = umma_idesc_tf32(kD, kC), id64w = umma_idesc_tf32(kC, kD);
     uint32_t phase = 0;
-    bool ok;
     do {
+        if (!ok) break;
         if (tid == 0) {
             const uint32_t h0 = smem_u32(R4), h1 = smem_u32(C1), o2 = smem_u32(R2), u5 = smem_u32(R5);
-            umma_tf32_k(tmem + 0, o2, kSboD, smem_u32(R3), kSboD, id64, kD, false);              // dP
-            umma_tf32_k(tmem + 64, smem_u32(R1), kSboD, smem_u32(R1), kSboD, id64, kD, false);   // K K^T
-            umma_tf32_k(tmem + 128, h0, kSboC, o2, kSboD, id128, kC, false);                     // X_q
-            umma_tf32_k(tmem + 128, h1, kSboC, o2 + 2048, kSboD, id128, kC, true);
-            umma_tf32_k(tmem + 256, h0, kSboC, u5, kSboD, id128, kC, false);                     // X_w
-            umma_tf32_k(tmem + 256, h1, kSboC, u5 + 2048, kSboD, id128, kC, true);
-            umma_tf32_k(tmem + 320, u5, kSboD, h0, kSboC, id64w, kC, false);                     // dU S0
-            umma_tf32_k(tmem + 320, u5 + 2048, kSboD, h1, kSboC, id64w, kC, true);
+            const uint32_t k1 = smem_u32(R1), u3 = smem_u32(R3);
+            umma_tf32_kx(tmem + 0, o2, 128, kSboD, u3, kLboR, kSboI, id64, kD, false);            // dP
+            umma_tf32_kx(tmem + 64, k1, kLboR, kSboI, k1, kLboR, kSboI, id64, kD, false);         // K K^T
+            umma_tf32_kx(tmem + 128, h0, kLboH, kSboI, o2, 128, kSboD, id128, kC, false);         // X_q
+            umma_tf32_kx(tmem + 128, h1, kLboH, kSboI, o2 + 2048, 128, kSboD, id128, kC, true);
+            umma_tf32_kx(tmem + 256, h0, kLboH, kSboI, u5, kLboR, kSboI, id128, kC, false);       // X_w
+            umma_tf32_kx(tmem + 256, h1, kLboH, kSboI, u5 + kHalfR, kLboR, kSboI, id128, kC, true);
+            umma_tf32_kx(tmem + 320, u5, kLboR, kSboI, h0, kLboH, kSboI, id64w, kC, false);       // dU S0
+            umma_tf32_kx(tmem + 320, u5 + kHalfR, kLboR, kSboI, h1, kLboH, kSboI, id64w, kC, true);
             umma_commit(bar);
         }
-        // D^T (and S0^T in fp32, for <D, S0>) by K-halves; the first half's loads fly during the products
-        float dot = 0.f;
-        float4 dh[HalfS::kItems], sh[HalfS::kItems];
-        auto load_half = [&](int hf) {
-#pragma unroll
-            for (int it = 0; it < HalfS::kItems; ++it) {
-                const int j = HalfS::row(it), i = HalfS::col(it) + kC * hf;
-                dh[it] = *reinterpret_cast<const float4*>(Dt + j * kD + i);
-                sh[it] = *reinterpret_cast<const float4*>(S0t + j * kD + i);
-            }
-        };
-        auto put_half = [&](uint8_t* dst) {
-#pragma unroll
-            for (int it = 0; it < HalfS::kItems; ++it) {
-                dot = fmaf(dh[it].x, sh[it].x, dot);
-                dot = fmaf(dh[it].y, sh[it].y, dot);
-                dot = fmaf(dh[it].z, sh[it].z, dot);
-                dot = fmaf(dh[it].w, sh[it].w, dot);
-                *reinterpret_cast<float4*>(dst + umma_koff(HalfS::row(it), HalfS::col(it), kSboC)) = tf32_round4(dh[it]);
-            }
-        };
-        load_half(0);
         if (!(ok = tc_wait(bar, phase))) break;
-        // phase A2: the products above have read dO and both halves of S0^T
-        put_half(R2);
-        load_half(1);
-        put_half(C1);
+        // phase A2: the products above have read dO and both halves of S0^T.  D^T -> R2 (first K-half)
+        // and C1|C2 (second), MN-interleaved like the S0^T halves
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+            for (int it = 0; it < 4; ++it)
+                reinterpret_cast<float4*>(hf ? C1 : R2)[tid + it * kNTtc] = tf32_round4(dreg[hf][it]);
         {  // dW = -(dU S0) -> R4 (rows s, k = j): F1's A operand
             float x[32];
             tmem_ld<4>(tmem + lane_base + 320 + cg * 32, x);
@@ -1649,9 +1676,10 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_intra_tc_kernel(BwdParams p) {
         }
         tc_sync();
         if (tid == 0) {
-            umma_tf32_k(tmem + 192, smem_u32(R2), kSboC, smem_u32(R3), kSboD, id128, kC, false);         // Y
-            umma_tf32_k(tmem + 192, smem_u32(C1), kSboC, smem_u32(R3) + 2048, kSboD, id128, kC, true);
-            umma_tf32_k(tmem + 320, smem_u32(R4), kSboD, smem_u32(R1), kSboD, id64, kD, false);          // F1
+            const uint32_t u3 = smem_u32(R3);
+            umma_tf32_kx(tmem + 192, smem_u32(R2), kLboH, kSboI, u3, kLboR, kSboI, id128, kC, false);        // Y
+            umma_tf32_kx(tmem + 192, smem_u32(C1), kLboH, kSboI, u3 + kHalfR, kLboR, kSboI, id128, kC, true);
+            umma_tf32_kx(tmem + 320, smem_u32(R4), 128, kSboD, smem_u32(R1), kLboR, kSboI, id64, kD, false);  // F1
             umma_commit(bar);
         }
         const float gl = sg[len - 1];
@@ -1738,13 +1766,42 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_intra_tc_kernel(BwdParams p) {
                         tf32_round4(make_float4(d[t], d[t + 1], d[t + 2], d[t + 3]));
             }
         }
-        // V -> R2 (rows s), K^T -> R3 (rows j, k = s), Q^T -> R1 (rows j, k = r)
-        stage_rows_fn<kC, kD>(R2, [&](int s, int k) { return s < len ? ld4_any(p.v, ob + s * sv + k, p.dtype) : z4; });
-        stage_cols_fn<kD, kC>(R3, [&](int s, int j) { return s < len ? kb[s * sk + j] : 0.f; });
-        stage_cols_fn<kD, kC>(R1, [&](int r, int j) { return r < len ? qb[r * sk + j] : 0.f; });
+        // V -> R2 (rows s), K^T -> R3 (rows j, k = s), Q^T -> R1 (rows j, k = r): every load issued
+        // before any store
+        {
+            using RV = RowsTc<kC, kD>;
+            constexpr int kIt = kD * kC / 4 / kNTtc;
+            float4 vv[RV::kItems], kt[kIt], qt[kIt];
+#pragma unroll
+            for (int it = 0; it < RV::kItems; ++it) {
+                const int s = RV::row(it);
+                vv[it] = s < len ? ld4_any(p.v, ob + s * sv + RV::col(it), p.dtype) : z4;
+            }
+#pragma unroll
+            for (int it = 0; it < kIt; ++it) {
+                const int e = tid + it * kNTtc, j = e % kD, s = (e / kD) * 4;
+                float a[4], b[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    a[u] = s + u < len ? kb[(s + u) * sk + j] : 0.f;
+                    b[u] = s + u < len ? qb[(s + u) * sk + j] : 0.f;
+                }
+                kt[it] = make_float4(a[0], a[1], a[2], a[3]);
+                qt[it] = make_float4(b[0], b[1], b[2], b[3]);
+            }
+#pragma unroll
+            for (int it = 0; it < RV::kItems; ++it)
+                *reinterpret_cast<float4*>(R2 + umma_koff(RV::row(it), RV::col(it), kSboD)) = tf32_round4(vv[it]);
+#pragma unroll
+            for (int it = 0; it < kIt; ++it) {
+                const int e = tid + it * kNTtc, j = e % kD, s = (e / kD) * 4;
+                *reinterpret_cast<float4*>(R3 + umma_koff(j, s, kSboC)) = tf32_round4(kt[it]);
+                *reinterpret_cast<float4*>(R1 + umma_koff(j, s, kSboC)) = tf32_round4(qt[it]);
+            }
+        }
         tc_sync();
         if (tid == 0) {
-            umma_tf32_k(tmem + 384, smem_u32(R5), kSboD, smem_u32(R2), kSboD, id64, kD, false);   // F2
+            umma_tf32_kx(tmem + 384, smem_u32(R5), kLboR, kSboI, smem_u32(R2), 128, kSboD, id64, kD, false);  // F2
             umma_tf32_k(tmem + 128, smem_u32(R3), kSboC, smem_u32(C1), kSboC, id128, kC, true);   // dq^T
             umma_tf32_k(tmem + 192, smem_u32(R1), kSboC, smem_u32(C2), kSboC, id128, kC, true);   // dk^T
             umma_commit(bar);
@@ -1908,12 +1965,26 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_intra_tc_kernel(BwdParams p) {
             if (l == 0) sdg[r] += rs - cs;
         }
         __syncthreads();
-        if (tid == 0) {
-            float acc = 0.f;
-            for (int r = len - 1; r >= 0; --r) {
-                acc += sdg[r];
-                p.dg[(size_t)(t0 + r) * p.HV + h] = acc;
-                p.dbeta[(size_t)(t0 + r) * p.HV + h] = sdb[r];
+        if (warp == 0) {
+            // dg = reverse cumsum of dgam: lane l takes rows len-1-2l and len-2-2l, a warp scan adds
+            // the lanes below
+            const int ra = len - 1 - 2 * lane, rb = ra - 1;
+            const float a = ra >= 0 ? sdg[ra] : 0.f, b = rb >= 0 ? sdg[rb] : 0.f;
+            float inc = a + b;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(kFull, inc, off);
+                if (lane >= off) inc += y;
+            }
+            const float below = __shfl_up_sync(kFull, inc, 1);
+            const float ea = (lane ? below : 0.f) + a, eb = ea + b;
+            if (ra >= 0) {
+                p.dg[(size_t)(t0 + ra) * p.HV + h] = ea;
+                p.dbeta[(size_t)(t0 + ra) * p.HV + h] = sdb[ra];
+            }
+            if (rb >= 0) {
+                p.dg[(size_t)(t0 + rb) * p.HV + h] = eb;
+                p.dbeta[(size_t)(t0 + rb) * p.HV + h] = sdb[rb];
             }
         }
     }
@@ -2138,8 +2209,19 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
     }
 
     if (tc_state && s->dk == 128) {
+        // tensor maps of the operands bwd_intra_tc_kernel copies: K^ ([T][HK][128]; a chunk's rows from
+        // token t0, head hk), U and dU ([chunk-head][64][128]), S0^T ([chunk-head][128][128], K-halves)
+        CUtensorMap mk{}, mu{}, mdu{}, ms{};
+        const uint64_t CH = (uint64_t)L.nchm * s->HV;
+        if (CH * 128 >= (1ull << 31)) return GDN_ERR_UNSUPPORTED;  // copy coordinates are 32-bit
+        if (encode_rows_f32(&mk, p.kn, (uint64_t)std::max(s->T_total, 1), (uint64_t)s->HK * 512, (uint64_t)s->HK * 32,
+                            kC, 32) != GDN_OK ||
+            encode_rows_f32(&mu, p.Ub, CH * kC, 512, 32, kC, 32) != GDN_OK ||
+            encode_rows_f32(&mdu, p.dUb, CH * kC, 512, 32, kC, 32) != GDN_OK ||
+            encode_rows_f32(&ms, p.Sb, CH * 128, 512, 32, 128, 16) != GDN_OK)
+            return GDN_ERR_CUDA;
         if (!set_smem(bwd_intra_tc_kernel, kIntraCTcSmem)) return GDN_ERR_CUDA;
-        bwd_intra_tc_kernel<<<gch, kNTtc, kIntraCTcSmem, cs>>>(p);
+        bwd_intra_tc_kernel<<<gch, kNTtc, kIntraCTcSmem, cs>>>(mk, mu, mdu, ms, p);
     } else {
         const size_t smem_is = sizeof(float) * (kMaxD * kLdD + 4 * kC * kLdD + 2 * kC + 32);
         if (!set_smem(bwd_intra_s_kernel, smem_is)) return GDN_ERR_CUDA;

@@ -32,12 +32,15 @@ __host__ __device__ constexpr uint32_t umma_koff(int n, int k, uint32_t sbo) {
     return (uint32_t)(n >> 3) * sbo + (uint32_t)(k >> 2) * 128u + (uint32_t)(n & 7) * 16u + (uint32_t)(k & 3) * 4u;
 }
 
-// Shared-memory matrix descriptor: start address, leading byte offset 128, stride byte offset
-// sbo (all >> 4), descriptor version 1 (bits 46-48 = 0b001), no swizzle.
-__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t sbo) {
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)(128u >> 4) << 16) | ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) |
-           ((uint64_t)1 << 46);
+// Shared-memory matrix descriptor: start address, leading byte offset lbo (the step between core
+// matrices along k), stride byte offset sbo (the step between row groups), all >> 4, descriptor
+// version 1 (bits 46-48 = 0b001), no swizzle.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
 }
+// The layout above (lbo = 128).
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t sbo) { return umma_desc(saddr, 128u, sbo); }
 
 // Instruction descriptor for kind::tf32: D fp32 (bits 4-5 = 1), A and B TF32 (bits 7-9 and
 // 10-12 = 2), both K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
@@ -89,6 +92,17 @@ __device__ __forceinline__ void umma_tf32_k(uint32_t d_tmem, uint32_t a_saddr, u
     for (int s = 0; s < K / 8; ++s)
         umma_tf32(d_tmem, umma_desc(a_saddr + 256u * s, a_sbo), umma_desc(b_saddr + 256u * s, b_sbo), idesc,
                   accumulate || s > 0);
+}
+
+// The same with any core-matrix strides per operand: element (n, k) of an operand at
+// (n / 8) * sbo + (k / 4) * lbo + (n % 8) * 16 + (k % 4) * 4.  The MN-interleaved layout that a
+// tensor copy with box {4 values, rows, k groups} writes has lbo = rows * 16 and sbo = 128.
+__device__ __forceinline__ void umma_tf32_kx(uint32_t d_tmem, uint32_t a_saddr, uint32_t a_lbo, uint32_t a_sbo,
+                                             uint32_t b_saddr, uint32_t b_lbo, uint32_t b_sbo, uint32_t idesc, int K,
+                                             bool accumulate) {
+    for (int s = 0; s < K / 8; ++s)
+        umma_tf32(d_tmem, umma_desc(a_saddr + 2u * a_lbo * s, a_lbo, a_sbo),
+                  umma_desc(b_saddr + 2u * b_lbo * s, b_lbo, b_sbo), idesc, accumulate || s > 0);
 }
 
 // Arrive on bar once every MMA this thread issued so far has completed.
