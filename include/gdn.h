@@ -80,6 +80,7 @@ typedef struct {
 /* Device-side error bits, readable with gdn_read_device_error. */
 #define GDN_DEVERR_CU_SEQLENS 1u /* cu_seqlens not 0-based, decreasing, or cu[N] != T_total */
 #define GDN_DEVERR_TIMEOUT 2u    /* a bounded wait on an asynchronous copy gave up */
+#define GDN_DEVERR_SMEM_ALIGN 4u /* shared memory not 1 KB aligned for a swizzled tensor-core operand */
 
 /* Bytes of device workspace `op` needs for `shape` (0 if it needs none or the
  * shape is invalid).  FWD: the varlen work list; BWD: chunk states and

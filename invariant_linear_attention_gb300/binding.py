@@ -18,7 +18,7 @@ _lib = None
 GDN_OK = 0
 GDN_F32, GDN_BF16 = 0, 1
 OP_FWD, OP_DECODE, OP_BWD = 0, 1, 2
-DEVERR_CU_SEQLENS, DEVERR_TIMEOUT = 1, 2
+DEVERR_CU_SEQLENS, DEVERR_TIMEOUT, DEVERR_SMEM_ALIGN = 1, 2, 4
 
 _P = ctypes.c_void_p
 

@@ -41,16 +41,16 @@ gdn_status encode_map_3d(CUtensorMap* map, const void* base, gdn_dtype dt, uint6
     return r == CUDA_SUCCESS ? GDN_OK : GDN_ERR_INVALID_ARG;
 }
 
-gdn_status encode_rows_f32(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_stride, uint64_t kgroups,
-                           uint32_t box_rows, uint32_t box_kg) {
+gdn_status encode_rows_f32_sw128(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t stride,
+                                 uint32_t box_rows) {
     auto fn = encode_fn();
     if (!fn) return GDN_ERR_CUDA;
-    const cuuint64_t dims[3] = {4, rows, kgroups};
-    const cuuint64_t strides[2] = {row_stride, 16};
-    const cuuint32_t box[3] = {4u, box_rows, box_kg};
-    const cuuint32_t estr[3] = {1u, 1u, 1u};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    const cuuint64_t dims[2] = {d0, d1};
+    const cuuint64_t strides[1] = {stride};
+    const cuuint32_t box[2] = {32u, box_rows};
+    const cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GDN_OK : GDN_ERR_INVALID_ARG;
 }

@@ -1210,17 +1210,19 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_wy_tc_kernel(BwdParams p) {
         tc_fence_before();
         __syncthreads();  // A complete; the first product has read sX
         {
-            // K (row s, four consecutive j) and V rows, s >= len zero, by vector loads in flight during
-            // the solve; written transposed into sX after it: K^T (j, s) and V^T (i, s)
+            // K (row s, four consecutive j) and V rows (bf16 bits, unconverted), s >= len zero, by vector
+            // loads in flight during the solve; written transposed into sX after it: K^T (j, s) and V^T (i, s)
             using RowsK = RowsTc<kC, kD>;
-            float4 kr[RowsK::kItems], vr[RowsK::kItems];
+            float4 kr[RowsK::kItems];
+            uint2 vr[RowsK::kItems];
+            const __nv_bfloat16* vb = static_cast<const __nv_bfloat16*>(p.v);
 #pragma unroll
             for (int it = 0; it < RowsK::kItems; ++it) {
                 const int s = RowsK::row(it), k = RowsK::col(it);
                 kr[it] = s < len ? *reinterpret_cast<const float4*>(p.kn + ((size_t)(t0 + s) * p.HK + hk) * kD + k)
                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-                vr[it] = s < len ? ld4_any(p.v, ((size_t)(t0 + s) * p.HV + h) * kD + k, p.dtype)
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                vr[it] = s < len ? *reinterpret_cast<const uint2*>(vb + ((size_t)(t0 + s) * p.HV + h) * kD + k)
+                                 : make_uint2(0u, 0u);
             }
             // T = (I + A)^-1, one column per forward substitution: column j solves (I + A) t = e_j.
             // Warp w takes columns {w, 31 - w, 32 + w, 63 - w} as four independent chains; lane l
@@ -1261,7 +1263,8 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_wy_tc_kernel(BwdParams p) {
             for (int it = 0; it < RowsK::kItems; ++it) {
                 const int s = RowsK::row(it), k = RowsK::col(it);
                 const float kv[4] = {kr[it].x, kr[it].y, kr[it].z, kr[it].w};
-                const float vv[4] = {vr[it].x, vr[it].y, vr[it].z, vr[it].w};
+                const float vv[4] = {__uint_as_float(vr[it].x << 16), __uint_as_float(vr[it].x & 0xFFFF0000u),
+                                     __uint_as_float(vr[it].y << 16), __uint_as_float(vr[it].y & 0xFFFF0000u)};
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
                     *reinterpret_cast<float*>(sX + umma_koff(k + t, s, kSboC)) = tf32_round(kv[t]);
@@ -1524,9 +1527,9 @@ __device__ __forceinline__ void async_rows(uint8_t* dst, P ptr) {
 //   dv^T | 320 dU S0 (128 wide), then F1 | 384 F2 | 448 T^T Z
 //   shared memory: five 32 KB operand buffers R1..R5 and two 16 KB ones C1, C2 (together one
 //   32 KB buffer at first), reused by phase; S0^T and D^T enter in two K-halves of 32 KB.
-// K^, U, dU and S0^T arrive by tensor copies (one thread, one mbarrier) in the MN-interleaved
-// layout (k groups rows * 16 bytes apart, row groups 128 bytes apart); every operand written by
-// threads later uses the k-contiguous layout of umma_koff.
+// K^, U, dU and S0^T arrive by tensor copies (one thread, one mbarrier) in the 128-byte-swizzled
+// K-major layout (boxes of 32 values x rows, four atom columns per 128 values); D^T takes the same
+// layout, written by threads; every other operand uses the layout of umma_koff.
 constexpr size_t kIntraCTcSmem = (size_t)5 * 32768 + 2 * 16384 + 4 * kC * kLdT + 4 * (4 * kC + 3 * 4 * kC) + 32;
 
 __global__ void __launch_bounds__(kNTtc, 1)
@@ -1535,7 +1538,7 @@ __global__ void __launch_bounds__(kNTtc, 1)
                         BwdParams p) {
     constexpr int kD = 128;
     constexpr uint32_t kSboD = kD * 32;  // 128 values per row
-    extern __shared__ __align__(128) uint8_t smb[];
+    extern __shared__ __align__(1024) uint8_t smb[];
     uint8_t* R1 = smb;
     uint8_t* R2 = R1 + 32768;
     uint8_t* R3 = R2 + 32768;
@@ -1570,32 +1573,40 @@ __global__ void __launch_bounds__(kNTtc, 1)
     const float* qb = p.qn + ((size_t)t0 * p.HK + hk) * kD;
     const size_t ob = ((size_t)t0 * p.HV + h) * kD;           // dO / V row r at ob + r * sv
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    // MN-interleaved operands: 64 rows x 128 (K^, U, dU) and 128 rows x 64 (a K-half of S0^T)
-    constexpr uint32_t kLboR = kC * 16, kLboH = kD * 16, kSboI = 128, kHalfR = 16 * kLboR;
+    // the swizzled atoms need 1 KB alignment of the dynamic shared memory (the same for every CTA)
+    if (smem_u32(smb) & 1023u) {
+        if (tid == 0) atomicOr(p.err, GDN_DEVERR_SMEM_ALIGN);
+        return;
+    }
     // phase A: K^ -> R1, U -> R3, dU -> R5 (rows = chunk positions), S0^T in two K-halves -> R4 and
-    // C1|C2 (rows j, k = i), all by tensor copies; dO -> R2 through registers meanwhile
+    // C1|C2 (rows j, k = i), all by tensor copies (four boxes of 32 values per operand); dO -> R2
+    // through registers meanwhile
     if (tid == 0) {
         mbar_init(bar, 1);
         mbar_init(bar_ld, 1);
         fence_barrier_init();
         mbar_arrive_expect_tx(bar_ld, 5u * 32768u);
-        tma_load_3d(R1, &tm_k, bar_ld, 0, t0, 32 * hk);
-        tma_load_3d(R3, &tm_u, bar_ld, 0, (int)(ci * kC), 0);
-        tma_load_3d(R5, &tm_du, bar_ld, 0, (int)(ci * kC), 0);
-        tma_load_3d(R4, &tm_s, bar_ld, 0, (int)(ci * kD), 0);
-        tma_load_3d(C1, &tm_s, bar_ld, 0, (int)(ci * kD), 16);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            tma_load_2d(R1 + 8192 * a, &tm_k, bar_ld, hk * kD + 32 * a, t0);
+            tma_load_2d(R3 + 8192 * a, &tm_u, bar_ld, 32 * a, (int)(ci * kC));
+            tma_load_2d(R5 + 8192 * a, &tm_du, bar_ld, 32 * a, (int)(ci * kC));
+            tma_load_2d((a < 2 ? R4 : C1) + 16384 * (a & 1), &tm_s, bar_ld, 32 * a, (int)(ci * kD));
+        }
     }
     if (warp == 0) tmem_alloc(slot, 512);
     const float* Dt = p.Db + ci * kD * kD;    // D^T: row j (dk index), dv index contiguous
-    // D^T (fp32) into registers at the float4 positions f = tid + 512 it of the S0^T halves that this
-    // thread rounds below (row j = f % 128, k group f / 128): <D, S0> then takes S0 as copied
+    // D^T (fp32) into registers, element by element where this thread finds the copied S0^T below:
+    // float4 f = tid + 512 it of a K-half (atom column f / 1024, row (f / 8) % 128, chunk position
+    // f % 8).  <D, S0> then takes S0 as copied, and D^T lands in the same layout.
     float4 dreg[2][4];
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
         for (int it = 0; it < 4; ++it) {
-            const int f = tid + it * kNTtc;
-            dreg[hf][it] = *reinterpret_cast<const float4*>(Dt + (f % kD) * kD + kC * hf + 4 * (f / kD));
+            const int f = tid + it * kNTtc, j = (f >> 3) & (kD - 1);
+            const int k = 32 * (f >> 10) + 4 * ((f & 7) ^ (j & 7));
+            dreg[hf][it] = *reinterpret_cast<const float4*>(Dt + j * kD + kC * hf + k);
         }
     stage_rows_fn<kC, kD>(R2, [&](int r, int k) { return r < len ? ld4_any(p.dout, ob + r * sv + k, p.dtype) : z4; });
     for (int i = tid; i < kC; i += kNTtc) {
@@ -1630,9 +1641,9 @@ __global__ void __launch_bounds__(kNTtc, 1)
                 *v = tf32_round4(x);
             }
         if (len < kC)
-            for (int e = tid; e < (kC - len) * (kD / 4); e += kNTtc) {
-                const int r = len + e / (kD / 4), kg = e % (kD / 4);
-                *reinterpret_cast<float4*>(R1 + kg * kLboR + r * 16) = z4;
+            for (int e = tid; e < (kC - len) * (kD / 4); e += kNTtc) {  // whole 128-byte row pieces
+                const int r = len + e / (kD / 4), a = (e >> 3) & 3, u = e & 7;
+                *reinterpret_cast<float4*>(R1 + 8192 * a + 128 * r + 16 * u) = z4;
             }
     } else if (tid == 0) {
         mbar_wait_bounded(bar_ld, 0);  // let copies still in flight land before the CTA leaves
@@ -1644,26 +1655,40 @@ __global__ void __launch_bounds__(kNTtc, 1)
     do {
         if (!ok) break;
         if (tid == 0) {
-            const uint32_t h0 = smem_u32(R4), h1 = smem_u32(C1), o2 = smem_u32(R2), u5 = smem_u32(R5);
-            const uint32_t k1 = smem_u32(R1), u3 = smem_u32(R3);
-            umma_tf32_kx(tmem + 0, o2, 128, kSboD, u3, kLboR, kSboI, id64, kD, false);            // dP
-            umma_tf32_kx(tmem + 64, k1, kLboR, kSboI, k1, kLboR, kSboI, id64, kD, false);         // K K^T
-            umma_tf32_kx(tmem + 128, h0, kLboH, kSboI, o2, 128, kSboD, id128, kC, false);         // X_q
-            umma_tf32_kx(tmem + 128, h1, kLboH, kSboI, o2 + 2048, 128, kSboD, id128, kC, true);
-            umma_tf32_kx(tmem + 256, h0, kLboH, kSboI, u5, kLboR, kSboI, id128, kC, false);       // X_w
-            umma_tf32_kx(tmem + 256, h1, kLboH, kSboI, u5 + kHalfR, kLboR, kSboI, id128, kC, true);
-            umma_tf32_kx(tmem + 320, u5, kLboR, kSboI, h0, kLboH, kSboI, id64w, kC, false);       // dU S0
-            umma_tf32_kx(tmem + 320, u5 + kHalfR, kLboR, kSboI, h1, kLboH, kSboI, id64w, kC, true);
+            const UmmaOp sK = op_sw(smem_u32(R1), kC), sU = op_sw(smem_u32(R3), kC);
+            const UmmaOp sdU0 = op_sw(smem_u32(R5), kC), sdU1 = op_sw(smem_u32(R5) + 16384, kC);  // K-halves
+            const UmmaOp sS0 = op_sw(smem_u32(R4), kD), sS1 = op_sw(smem_u32(C1), kD);
+            const UmmaOp dO = op_k(smem_u32(R2), kSboD), dO1 = op_k(smem_u32(R2) + 2048, kSboD);
+            umma_tf32_op(tmem + 0, dO, sU, id64, kD, false);        // dP
+            umma_tf32_op(tmem + 64, sK, sK, id64, kD, false);       // K K^T
+            umma_tf32_op(tmem + 128, sS0, dO, id128, kC, false);    // X_q
+            umma_tf32_op(tmem + 128, sS1, dO1, id128, kC, true);
+            umma_tf32_op(tmem + 256, sS0, sdU0, id128, kC, false);  // X_w
+            umma_tf32_op(tmem + 256, sS1, sdU1, id128, kC, true);
+            umma_tf32_op(tmem + 320, sdU0, sS0, id64w, kC, false);  // dU S0
+            umma_tf32_op(tmem + 320, sdU1, sS1, id64w, kC, true);
             umma_commit(bar);
+        }
+        float qv[16];  // q^[r][j] for the dQ_S epilogue, in flight during the products
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const int r = cg * 16 + m;
+            qv[m] = r < len ? qb[(size_t)r * sk + jj] : 0.f;
         }
         if (!(ok = tc_wait(bar, phase))) break;
         // phase A2: the products above have read dO and both halves of S0^T.  D^T -> R2 (first K-half)
-        // and C1|C2 (second), MN-interleaved like the S0^T halves
+        // and C1|C2 (second), in the layout of the S0^T halves
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
             for (int it = 0; it < 4; ++it)
                 reinterpret_cast<float4*>(hf ? C1 : R2)[tid + it * kNTtc] = tf32_round4(dreg[hf][it]);
+        float kv[16];  // k^[r][j] for the U D epilogue
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const int r = cg * 16 + m;
+            kv[m] = r < len ? kb[(size_t)r * sk + jj] : 0.f;
+        }
         {  // dW = -(dU S0) -> R4 (rows s, k = j): F1's A operand
             float x[32];
             tmem_ld<4>(tmem + lane_base + 320 + cg * 32, x);
@@ -1677,36 +1702,25 @@ __global__ void __launch_bounds__(kNTtc, 1)
         tc_sync();
         if (tid == 0) {
             const uint32_t u3 = smem_u32(R3);
-            umma_tf32_kx(tmem + 192, smem_u32(R2), kLboH, kSboI, u3, kLboR, kSboI, id128, kC, false);        // Y
-            umma_tf32_kx(tmem + 192, smem_u32(C1), kLboH, kSboI, u3 + kHalfR, kLboR, kSboI, id128, kC, true);
-            umma_tf32_kx(tmem + 320, smem_u32(R4), 128, kSboD, smem_u32(R1), kLboR, kSboI, id64, kD, false);  // F1
+            umma_tf32_op(tmem + 192, op_sw(smem_u32(R2), kD), op_sw(u3, kC), id128, kC, false);  // Y
+            umma_tf32_op(tmem + 192, op_sw(smem_u32(C1), kD), op_sw(u3 + 16384, kC), id128, kC, true);
+            umma_tf32_op(tmem + 320, op_k(smem_u32(R4), kSboD), op_sw(smem_u32(R1), kC), id64, kD, false);  // F1
             umma_commit(bar);
         }
         const float gl = sg[len - 1];
         {  // Gam_r X_q back into TMEM as dq^T's first term; q^_r . dQ_S,r
-            float x[16], v[16];
-#pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const int r = cg * 16 + m;
-                v[m] = r < len ? qb[(size_t)r * sk + jj] : 0.f;
-            }
+            float x[16];
             tmem_ld<2>(tmem + lane_base + 128 + cg * 16, x);
 #pragma unroll
             for (int m = 0; m < 16; ++m) {
                 const int r = cg * 16 + m;
                 const float d = r < len ? __expf(sg[r]) * x[m] : 0.f;
                 x[m] = d;
-                v[m] *= d;
+                qv[m] *= d;
             }
             tmem_st<2>(tmem + lane_base + 128 + cg * 16, x);
-            const float part = warp_transpose_sum<16>(v);
+            const float part = warp_transpose_sum<16>(qv);
             if (lane < 16) part1[q * kC + cg * 16 + lane] = part;
-        }
-        float kv[16];
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const int r = cg * 16 + m;
-            kv[m] = r < len ? kb[(size_t)r * sk + jj] : 0.f;
         }
         if (!(ok = tc_wait(bar, phase))) break;
         {  // b_r Y back into TMEM as dk^T's first term; k^_r . Y_r
@@ -1766,8 +1780,8 @@ __global__ void __launch_bounds__(kNTtc, 1)
                         tf32_round4(make_float4(d[t], d[t + 1], d[t + 2], d[t + 3]));
             }
         }
-        // V -> R2 (rows s), K^T -> R3 (rows j, k = s), Q^T -> R1 (rows j, k = r): every load issued
-        // before any store
+        // V -> R2 (rows s), K^T -> R3 (rows j, k = s) from the copy of K^ in R1, Q^T -> R1 (rows j, k = r):
+        // every load issued before any store
         {
             using RV = RowsTc<kC, kD>;
             constexpr int kIt = kD * kC / 4 / kNTtc;
@@ -1783,12 +1797,13 @@ __global__ void __launch_bounds__(kNTtc, 1)
                 float a[4], b[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    a[u] = s + u < len ? kb[(s + u) * sk + j] : 0.f;
+                    a[u] = *reinterpret_cast<const float*>(R1 + sw128_off(s + u, j, kC));  // zero past len
                     b[u] = s + u < len ? qb[(s + u) * sk + j] : 0.f;
                 }
                 kt[it] = make_float4(a[0], a[1], a[2], a[3]);
                 qt[it] = make_float4(b[0], b[1], b[2], b[3]);
             }
+            __syncthreads();  // every read of K^ in R1 is done
 #pragma unroll
             for (int it = 0; it < RV::kItems; ++it)
                 *reinterpret_cast<float4*>(R2 + umma_koff(RV::row(it), RV::col(it), kSboD)) = tf32_round4(vv[it]);
@@ -1801,7 +1816,7 @@ __global__ void __launch_bounds__(kNTtc, 1)
         }
         tc_sync();
         if (tid == 0) {
-            umma_tf32_kx(tmem + 384, smem_u32(R5), kLboR, kSboI, smem_u32(R2), 128, kSboD, id64, kD, false);  // F2
+            umma_tf32_op(tmem + 384, op_sw(smem_u32(R5), kC), op_k(smem_u32(R2), kSboD), id64, kD, false);  // F2
             umma_tf32_k(tmem + 128, smem_u32(R3), kSboC, smem_u32(C1), kSboC, id128, kC, true);   // dq^T
             umma_tf32_k(tmem + 192, smem_u32(R1), kSboC, smem_u32(C2), kSboC, id128, kC, true);   // dk^T
             umma_commit(bar);
@@ -1847,7 +1862,7 @@ __global__ void __launch_bounds__(kNTtc, 1)
                 if (r < len) dq[(size_t)r * p.HV * kD] = x[t];
             }
         }
-        // dW^T = -X_w -> R2, dU^T -> R1 (rows j / i, k = s); diag(beta Gam)-scaled T^T -> C1,
+        // dW^T = -X_w -> R2, dU^T -> R1 from the copy of dU in R5 (rows j / i, k = s); diag(beta Gam)-scaled T^T -> C1,
         // diag(beta)-scaled T^T -> C2 (rows r, k = s); T -> R4 + 16 KB (rows b, k = c)
         {
             float x[16];
@@ -1857,7 +1872,7 @@ __global__ void __launch_bounds__(kNTtc, 1)
                 *reinterpret_cast<float4*>(R2 + umma_koff(jj, cg * 16 + t, kSboC)) =
                     tf32_round4(make_float4(-x[t], -x[t + 1], -x[t + 2], -x[t + 3]));
         }
-        stage_cols_fn<kD, kC>(R1, [&](int s, int i) { return p.dUb[(ci * kC + s) * kD + i]; });
+        stage_cols_fn<kD, kC>(R1, [&](int s, int i) { return *reinterpret_cast<const float*>(R5 + sw128_off(s, i, kC)); });
         stage_cols_fn<kC, kC>(C1, [&](int s, int r) { return Tg[s * kC + r] * sbe[r] * __expf(sg[r]); });
         stage_cols_fn<kC, kC>(C2, [&](int s, int r) { return Tg[s * kC + r] * sbe[r]; });
         stage_rows_fn<kC, kC>(R4 + 16384, [&](int b, int k) { return *reinterpret_cast<const float4*>(Tg + b * kC + k); });
@@ -2209,16 +2224,16 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
     }
 
     if (tc_state && s->dk == 128) {
-        // tensor maps of the operands bwd_intra_tc_kernel copies: K^ ([T][HK][128]; a chunk's rows from
-        // token t0, head hk), U and dU ([chunk-head][64][128]), S0^T ([chunk-head][128][128], K-halves)
+        // tensor maps of the operands bwd_intra_tc_kernel copies: K^ ([T][HK * 128]; a chunk's rows from
+        // token t0, columns of head hk), U and dU ([chunk-head * 64][128]), S0^T ([chunk-head * 128][128])
         CUtensorMap mk{}, mu{}, mdu{}, ms{};
         const uint64_t CH = (uint64_t)L.nchm * s->HV;
         if (CH * 128 >= (1ull << 31)) return GDN_ERR_UNSUPPORTED;  // copy coordinates are 32-bit
-        if (encode_rows_f32(&mk, p.kn, (uint64_t)std::max(s->T_total, 1), (uint64_t)s->HK * 512, (uint64_t)s->HK * 32,
-                            kC, 32) != GDN_OK ||
-            encode_rows_f32(&mu, p.Ub, CH * kC, 512, 32, kC, 32) != GDN_OK ||
-            encode_rows_f32(&mdu, p.dUb, CH * kC, 512, 32, kC, 32) != GDN_OK ||
-            encode_rows_f32(&ms, p.Sb, CH * 128, 512, 32, 128, 16) != GDN_OK)
+        if (encode_rows_f32_sw128(&mk, p.kn, (uint64_t)s->HK * 128, (uint64_t)std::max(s->T_total, 1),
+                                  (uint64_t)s->HK * 512, kC) != GDN_OK ||
+            encode_rows_f32_sw128(&mu, p.Ub, 128, CH * kC, 512, kC) != GDN_OK ||
+            encode_rows_f32_sw128(&mdu, p.dUb, 128, CH * kC, 512, kC) != GDN_OK ||
+            encode_rows_f32_sw128(&ms, p.Sb, 128, CH * 128, 512, 128) != GDN_OK)
             return GDN_ERR_CUDA;
         if (!set_smem(bwd_intra_tc_kernel, kIntraCTcSmem)) return GDN_ERR_CUDA;
         bwd_intra_tc_kernel<<<gch, kNTtc, kIntraCTcSmem, cs>>>(mk, mu, mdu, ms, p);

@@ -32,15 +32,12 @@ __host__ __device__ constexpr uint32_t umma_koff(int n, int k, uint32_t sbo) {
     return (uint32_t)(n >> 3) * sbo + (uint32_t)(k >> 2) * 128u + (uint32_t)(n & 7) * 16u + (uint32_t)(k & 3) * 4u;
 }
 
-// Shared-memory matrix descriptor: start address, leading byte offset lbo (the step between core
-// matrices along k), stride byte offset sbo (the step between row groups), all >> 4, descriptor
-// version 1 (bits 46-48 = 0b001), no swizzle.
-__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
+// Shared-memory matrix descriptor: start address, leading byte offset 128, stride byte offset
+// sbo (all >> 4), descriptor version 1 (bits 46-48 = 0b001), no swizzle.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)(128u >> 4) << 16) | ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) |
+           ((uint64_t)1 << 46);
 }
-// The layout above (lbo = 128).
-__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t sbo) { return umma_desc(saddr, 128u, sbo); }
 
 // Instruction descriptor for kind::tf32: D fp32 (bits 4-5 = 1), A and B TF32 (bits 7-9 and
 // 10-12 = 2), both K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
@@ -94,15 +91,39 @@ __device__ __forceinline__ void umma_tf32_k(uint32_t d_tmem, uint32_t a_saddr, u
                   accumulate || s > 0);
 }
 
-// The same with any core-matrix strides per operand: element (n, k) of an operand at
-// (n / 8) * sbo + (k / 4) * lbo + (n % 8) * 16 + (k % 4) * 4.  The MN-interleaved layout that a
-// tensor copy with box {4 values, rows, k groups} writes has lbo = rows * 16 and sbo = 128.
-__device__ __forceinline__ void umma_tf32_kx(uint32_t d_tmem, uint32_t a_saddr, uint32_t a_lbo, uint32_t a_sbo,
-                                             uint32_t b_saddr, uint32_t b_lbo, uint32_t b_sbo, uint32_t idesc, int K,
+// An MMA operand in shared memory, in one of two layouts:
+//   rows == 0: the layout above, row groups sbo apart;
+//   rows != 0: K-major with the 128-byte swizzle: rows of 32 values (128 bytes) whose 16-byte chunks
+//     sit at position chunk ^ (row % 8), 8-row atoms of 1 KB (sbo = 1024), and atom columns of
+//     rows x 128 bytes along k -- what a tensor copy with the 128-byte swizzle writes for a box of 32
+//     values x rows.  The atoms must start on 1 KB boundaries.  A K = 8 step inside an atom column
+//     moves the start address by 32 bytes; the swizzle applies to the address bits.
+struct UmmaOp {
+    uint32_t base, sbo, rows;
+};
+__device__ __forceinline__ UmmaOp op_k(uint32_t base, uint32_t sbo) { return UmmaOp{base, sbo, 0u}; }
+__device__ __forceinline__ UmmaOp op_sw(uint32_t base, uint32_t rows) { return UmmaOp{base, 1024u, rows}; }
+
+// Descriptor of the swizzled layout: leading byte offset unused (16), stride byte offset 1024,
+// version 1, base offset 0, layout type 2 (128-byte swizzle) at bits 61-63.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024u >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+__device__ __forceinline__ uint64_t umma_op_desc(const UmmaOp& o, int s) {
+    return o.rows ? umma_desc_sw128(o.base + (uint32_t)(s >> 2) * o.rows * 128u + (uint32_t)(s & 3) * 32u)
+                  : umma_desc(o.base + 256u * s, o.sbo);
+}
+// Byte offset of element (n, k) in the swizzled layout with `rows` rows.
+__host__ __device__ constexpr uint32_t sw128_off(int n, int k, int rows) {
+    return (uint32_t)(k >> 5) * (uint32_t)rows * 128u + (uint32_t)n * 128u +
+           ((uint32_t)(((k & 31) >> 2) ^ (n & 7)) << 4) + (uint32_t)(k & 3) * 4u;
+}
+
+// D (+)= A B^T for operands in either layout, K a multiple of 8.
+__device__ __forceinline__ void umma_tf32_op(uint32_t d_tmem, const UmmaOp& a, const UmmaOp& b, uint32_t idesc, int K,
                                              bool accumulate) {
-    for (int s = 0; s < K / 8; ++s)
-        umma_tf32(d_tmem, umma_desc(a_saddr + 2u * a_lbo * s, a_lbo, a_sbo),
-                  umma_desc(b_saddr + 2u * b_lbo * s, b_lbo, b_sbo), idesc, accumulate || s > 0);
+    for (int s = 0; s < K / 8; ++s) umma_tf32(d_tmem, umma_op_desc(a, s), umma_op_desc(b, s), idesc, accumulate || s > 0);
 }
 
 // Arrive on bar once every MMA this thread issued so far has completed.
