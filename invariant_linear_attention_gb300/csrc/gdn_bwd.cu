@@ -1535,6 +1535,7 @@ constexpr size_t kIntraCTcSmem = (size_t)5 * 32768 + 2 * 16384 + 4 * kC * kLdT +
 __global__ void __launch_bounds__(kNTtc, 1)
     bwd_intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_u,
                         const __grid_constant__ CUtensorMap tm_du, const __grid_constant__ CUtensorMap tm_s,
+                        const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ CUtensorMap tm_t,
                         BwdParams p) {
     constexpr int kD = 128;
     constexpr uint32_t kSboD = kD * 32;  // 128 values per row
@@ -1567,7 +1568,6 @@ __global__ void __launch_bounds__(kNTtc, 1)
     const bool row_lane = lane < 16;    // lanes holding a row of an M = 64 result
     const int r64 = 16 * q + (lane & 15);  // that row
     const int jj = 32 * q + lane;          // the dk / dv index of an M = 128 result
-    const float* Tg = p.Tb + ci * kC * kC;
     const size_t sk = (size_t)p.HK * kD, sv = (size_t)p.HV * kD;
     const float* kb = p.kn + ((size_t)t0 * p.HK + hk) * kD;  // K^ row s at kb + s * sk
     const float* qb = p.qn + ((size_t)t0 * p.HK + hk) * kD;
@@ -1616,6 +1616,7 @@ __global__ void __launch_bounds__(kNTtc, 1)
     }
     __syncthreads();  // the barriers' initialisation is visible
     bool ok = __syncthreads_and(mbar_wait_bounded(bar_ld, 0));
+    int ld_pending = ok ? -1 : 0;  // parity of tensor copies issued and not yet seen complete
     float dot = 0.f;  // this thread's share of <D, S0>, in fp32
     if (ok) {
         // TF32 rounding of the copied operands (five 32 KB buffers, any layout), and zero rows of K^
@@ -1645,8 +1646,6 @@ __global__ void __launch_bounds__(kNTtc, 1)
                 const int r = len + e / (kD / 4), a = (e >> 3) & 3, u = e & 7;
                 *reinterpret_cast<float4*>(R1 + 8192 * a + 128 * r + 16 * u) = z4;
             }
-    } else if (tid == 0) {
-        mbar_wait_bounded(bar_ld, 0);  // let copies still in flight land before the CTA leaves
     }
     tc_sync();
     const uint32_t tmem = *slot;
@@ -1723,6 +1722,17 @@ __global__ void __launch_bounds__(kNTtc, 1)
             if (lane < 16) part1[q * kC + cg * 16 + lane] = part;
         }
         if (!(ok = tc_wait(bar, phase))) break;
+        // F1 has read dW: Q K^T -> R4 (the first 16 KB) and T -> R4 + 16 KB by tensor copies (swizzled,
+        // 64 rows x 64), for phase B and phase C
+        if (tid == 0) {
+            mbar_arrive_expect_tx(bar_ld, 32768u);
+#pragma unroll
+            for (int a = 0; a < 2; ++a) {
+                tma_load_2d(R4 + 8192 * a, &tm_qk, bar_ld, 32 * a, (int)(ci * kC));
+                tma_load_2d(R4 + 16384 + 8192 * a, &tm_t, bar_ld, 32 * a, (int)(ci * kC));
+            }
+        }
+        ld_pending = 1;
         {  // b_r Y back into TMEM as dk^T's first term; k^_r . Y_r
             float x[16];
             tmem_ld<2>(tmem + lane_base + 192 + cg * 16, x);
@@ -1752,17 +1762,18 @@ __global__ void __launch_bounds__(kNTtc, 1)
             for (int r = 0; r < len; ++r) tot += rowp[r];
             sdg[len - 1] += tot + __expf(gl) * dS;
         }
+        if (!(ok = __syncthreads_and(mbar_wait_bounded(bar_ld, 1)))) break;
+        ld_pending = -1;
         // phase B: dQK = lower(dP) E, dE = lower(dP) QK; dQK (C1) and its transpose (C2)
         {
             float x[16];
             tmem_ld<2>(tmem + lane_base + 0 + cg * 16, x);
             if (row_lane) {
                 const int r = r64;
-                const float* qk = p.QKb + (ci * kC + r) * kC + cg * 16;
                 float qv[16];
 #pragma unroll
                 for (int t = 0; t < 16; t += 4) {
-                    const float4 v = *reinterpret_cast<const float4*>(qk + t);
+                    const float4 v = *reinterpret_cast<const float4*>(R4 + sw128_off(r, cg * 16 + t, kC));
                     qv[t] = v.x; qv[t + 1] = v.y; qv[t + 2] = v.z; qv[t + 3] = v.w;
                 }
                 float d[16];
@@ -1830,7 +1841,12 @@ __global__ void __launch_bounds__(kNTtc, 1)
             float v1[16], v2[16];
             if (row_lane) {
                 const int s = r64;
-                const float* tr = Tg + s * kC + cg * 16;
+                float tr[16];
+#pragma unroll
+                for (int t = 0; t < 16; t += 4) {
+                    const float4 v = *reinterpret_cast<const float4*>(R4 + 16384 + sw128_off(s, cg * 16 + t, kC));
+                    tr[t] = v.x; tr[t + 1] = v.y; tr[t + 2] = v.z; tr[t + 3] = v.w;
+                }
                 float dt[16];
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
@@ -1862,8 +1878,9 @@ __global__ void __launch_bounds__(kNTtc, 1)
                 if (r < len) dq[(size_t)r * p.HV * kD] = x[t];
             }
         }
-        // dW^T = -X_w -> R2, dU^T -> R1 from the copy of dU in R5 (rows j / i, k = s); diag(beta Gam)-scaled T^T -> C1,
-        // diag(beta)-scaled T^T -> C2 (rows r, k = s); T -> R4 + 16 KB (rows b, k = c)
+        // dW^T = -X_w -> R2, dU^T -> R1 from the copy of dU in R5 (rows j / i, k = s); diag(beta Gam)-scaled
+        // T^T -> C1, diag(beta)-scaled T^T -> C2 (rows r, k = s), from the copy of T in R4 + 16 KB, which
+        // is then rounded in place as the B operand of Z
         {
             float x[16];
             tmem_ld<2>(tmem + lane_base + 256 + cg * 16, x);
@@ -1873,10 +1890,18 @@ __global__ void __launch_bounds__(kNTtc, 1)
                     tf32_round4(make_float4(-x[t], -x[t + 1], -x[t + 2], -x[t + 3]));
         }
         stage_cols_fn<kD, kC>(R1, [&](int s, int i) { return *reinterpret_cast<const float*>(R5 + sw128_off(s, i, kC)); });
-        stage_cols_fn<kC, kC>(C1, [&](int s, int r) { return Tg[s * kC + r] * sbe[r] * __expf(sg[r]); });
-        stage_cols_fn<kC, kC>(C2, [&](int s, int r) { return Tg[s * kC + r] * sbe[r]; });
-        stage_rows_fn<kC, kC>(R4 + 16384, [&](int b, int k) { return *reinterpret_cast<const float4*>(Tg + b * kC + k); });
+        {
+            const uint8_t* T4 = R4 + 16384;
+            auto tv = [&](int s, int r) { return *reinterpret_cast<const float*>(T4 + sw128_off(s, r, kC)); };
+            stage_cols_fn<kC, kC>(C1, [&](int s, int r) { return tv(s, r) * sbe[r] * __expf(sg[r]); });
+            stage_cols_fn<kC, kC>(C2, [&](int s, int r) { return tv(s, r) * sbe[r]; });
+        }
         __syncthreads();
+#pragma unroll
+        for (int it = 0; it < 16384 / 16 / kNTtc; ++it) {
+            float4* v = reinterpret_cast<float4*>(R4 + 16384) + tid + it * kNTtc;
+            *v = tf32_round4(*v);
+        }
         for (int r = tid; r < kC; r += kNTtc) {
             const float a1 = ((part1[r] + part1[kC + r]) + part1[2 * kC + r]) + part1[3 * kC + r];
             const float a2 = ((part2[r] + part2[kC + r]) + part2[2 * kC + r]) + part2[3 * kC + r];
@@ -1888,7 +1913,7 @@ __global__ void __launch_bounds__(kNTtc, 1)
         if (tid == 0) {
             umma_tf32_k(tmem + 192, smem_u32(R2), kSboC, smem_u32(C1), kSboC, id128, kC, true);          // dk^T
             umma_tf32_k(tmem + 256, smem_u32(R1), kSboC, smem_u32(C2), kSboC, id128, kC, false);         // dv^T
-            umma_tf32_k(tmem + 0, smem_u32(R4), kSboC, smem_u32(R4) + 16384, kSboC, id64, kC, false);    // Z
+            umma_tf32_op(tmem + 0, op_k(smem_u32(R4), kSboC), op_sw(smem_u32(R4) + 16384, kC), id64, kC, false);  // Z
             umma_commit(bar);
         }
         if (!(ok = tc_wait(bar, phase))) break;
@@ -1908,7 +1933,9 @@ __global__ void __launch_bounds__(kNTtc, 1)
                     *reinterpret_cast<float*>(R5 + umma_koff(cg * 16 + t, r64, kSboC)) = tf32_round(x[t]);
             }
         }
-        stage_cols_fn<kC, kC>(R5 + 16384, [&](int a, int r) { return Tg[a * kC + r]; });
+        stage_cols_fn<kC, kC>(R5 + 16384, [&](int a, int r) {
+            return *reinterpret_cast<const float*>(R4 + 16384 + sw128_off(a, r, kC));
+        });
         tc_sync();
         if (tid == 0) {
             umma_tf32_k(tmem + 448, smem_u32(R5) + 16384, kSboC, smem_u32(R5), kSboC, id64, kC, false);  // T^T Z
@@ -2003,7 +2030,10 @@ __global__ void __launch_bounds__(kNTtc, 1)
             }
         }
     }
-    if (!ok && tid == 0) atomicOr(p.err, GDN_DEVERR_TIMEOUT);
+    if (!ok && tid == 0) {
+        atomicOr(p.err, GDN_DEVERR_TIMEOUT);
+        if (ld_pending >= 0) mbar_wait_bounded(bar_ld, (uint32_t)ld_pending);  // copies in flight land first
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 512);
@@ -2225,18 +2255,21 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
 
     if (tc_state && s->dk == 128) {
         // tensor maps of the operands bwd_intra_tc_kernel copies: K^ ([T][HK * 128]; a chunk's rows from
-        // token t0, columns of head hk), U and dU ([chunk-head * 64][128]), S0^T ([chunk-head * 128][128])
-        CUtensorMap mk{}, mu{}, mdu{}, ms{};
+        // token t0, columns of head hk), U and dU ([chunk-head * 64][128]), S0^T ([chunk-head * 128][128]),
+        // Q K^T and T ([chunk-head * 64][64])
+        CUtensorMap mk{}, mu{}, mdu{}, ms{}, mqk{}, mt{};
         const uint64_t CH = (uint64_t)L.nchm * s->HV;
         if (CH * 128 >= (1ull << 31)) return GDN_ERR_UNSUPPORTED;  // copy coordinates are 32-bit
         if (encode_rows_f32_sw128(&mk, p.kn, (uint64_t)s->HK * 128, (uint64_t)std::max(s->T_total, 1),
                                   (uint64_t)s->HK * 512, kC) != GDN_OK ||
             encode_rows_f32_sw128(&mu, p.Ub, 128, CH * kC, 512, kC) != GDN_OK ||
             encode_rows_f32_sw128(&mdu, p.dUb, 128, CH * kC, 512, kC) != GDN_OK ||
-            encode_rows_f32_sw128(&ms, p.Sb, 128, CH * 128, 512, 128) != GDN_OK)
+            encode_rows_f32_sw128(&ms, p.Sb, 128, CH * 128, 512, 128) != GDN_OK ||
+            encode_rows_f32_sw128(&mqk, p.QKb, kC, CH * kC, 256, kC) != GDN_OK ||
+            encode_rows_f32_sw128(&mt, p.Tb, kC, CH * kC, 256, kC) != GDN_OK)
             return GDN_ERR_CUDA;
         if (!set_smem(bwd_intra_tc_kernel, kIntraCTcSmem)) return GDN_ERR_CUDA;
-        bwd_intra_tc_kernel<<<gch, kNTtc, kIntraCTcSmem, cs>>>(mk, mu, mdu, ms, p);
+        bwd_intra_tc_kernel<<<gch, kNTtc, kIntraCTcSmem, cs>>>(mk, mu, mdu, ms, mqk, mt, p);
     } else {
         const size_t smem_is = sizeof(float) * (kMaxD * kLdD + 4 * kC * kLdD + 2 * kC + 32);
         if (!set_smem(bwd_intra_s_kernel, smem_is)) return GDN_ERR_CUDA;
