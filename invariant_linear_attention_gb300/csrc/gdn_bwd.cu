@@ -691,7 +691,8 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p)
     uint8_t* sUt = sW + kC * DK * 4;            // A of U^T diag(b) K:       128 x 64
     uint8_t* sBKt = sUt + kDv * kC * 4;         // B (transposed diag(b) K): DK x 64
     float* sUtil = reinterpret_cast<float*>(sBKt + DK * kC * 4);  // U~, row-major 64 x 128
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sUtil + kC * kDv);
+    float* sfb = sUtil + kC * kDv;              // b_r = exp(gam_last - gam_r) of the chunk in bk (0 past len)
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sfb + kC);
     uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
     const int n = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
     const int i = (warp & 3) * 32 + (tid & 31), cg = warp >> 2;
@@ -730,12 +731,39 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p)
     const int bos = min(max(p.cu[n], 0), p.T), eos = min(max(p.cu[n + 1], bos), p.T);
     const int nch = (eos - bos + kC - 1) / kC;
     auto has = [&](int j) { return j < nch && p.coff[n] + j < p.nchm; };
-    ColsTc<DK, kC> bk;  // (diag(b) K)^T of the chunk about to run, in registers
+    // K^T of the chunk about to run in registers (the normalised keys, rows >= len zero), and its
+    // factors b_r in sfb; the product diag(b) K^ is taken when the operand is written (bk_put)
+    const int hk = h / p.G;
+    ColsTc<DK, kC> bk;
+    auto bk_load = [&](int jc) {
+        const int t0c = bos + jc * kC, lenc = min(kC, eos - t0c);
+        const float* kr = p.kn + ((size_t)t0c * p.HK + hk) * DK;
+        const size_t st = (size_t)p.HK * DK;
+#pragma unroll
+        for (int it = 0; it < ColsTc<DK, kC>::kItems; ++it) {
+            const int e = tid + it * kNTtc, nn = e % DK, k = (e / DK) * 4;
+            bk.v[it] = make_float4(k < lenc ? kr[k * st + nn] : 0.f, k + 1 < lenc ? kr[(k + 1) * st + nn] : 0.f,
+                                   k + 2 < lenc ? kr[(k + 2) * st + nn] : 0.f, k + 3 < lenc ? kr[(k + 3) * st + nn] : 0.f);
+        }
+        if (tid < kC) {
+            const float gl = p.gam[(size_t)(t0c + lenc - 1) * p.HV + h];
+            sfb[tid] = tid < lenc ? __expf(gl - p.gam[(size_t)(t0c + tid) * p.HV + h]) : 0.f;
+        }
+    };
+    auto bk_put = [&]() {
+#pragma unroll
+        for (int it = 0; it < ColsTc<DK, kC>::kItems; ++it) {
+            const int e = tid + it * kNTtc, nn = e % DK, k = (e / DK) * 4;
+            const float4 v = bk.v[it];
+            *reinterpret_cast<float4*>(sBKt + umma_koff(nn, k, kC * 32)) = tf32_round4(
+                make_float4(sfb[k] * v.x, sfb[k + 1] * v.y, sfb[k + 2] * v.z, sfb[k + 3] * v.w));
+        }
+    };
     if (has(0)) {
         const size_t ci = ch_index(p, p.coff[n], h);
         issue_w(ci);
         issue_ut(ci);
-        bk.load(p.BKb + ci * kC * DK);
+        bk_load(0);
     }
     tc_sync();
     const uint32_t tmem = *slot;
@@ -750,14 +778,15 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p)
         else store_state_slice<kS, false>(p.Sb + (ci * kDv + i) * DK + cg * kS, S);
         cp_async_wait_all();  // this thread's copies of W and U~ (commits what is still open)
         round_w();
-        bk.put(sBKt);
+        __syncthreads();  // sfb of this chunk is complete
+        bk_put();
         const float Gl = __expf(p.gam[(size_t)(t0 + len - 1) * p.HV + h]);
         tc_sync();
         if (tid == 0) {
             umma_tf32_k(tmem, smem_u32(sS), kSboD, smem_u32(sW), kSboD, umma_idesc_tf32(kDv, kC), DK, false);
             umma_commit(bar);
         }
-        if (next) bk.load(p.BKb + cn * kC * DK);
+        if (next) bk_load(j + 1);  // sfb: every read of it was before the barrier above
         if (!(ok = tc_wait(bar, phase))) break;
         if (next) issue_w(cn);
         {   // U[r][i] = U~[r][i] - (S W^T)[i][r] for this thread's 16 values of r
@@ -811,7 +840,9 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p)
     uint8_t* sBK = sPt + kC * kC * 4;           // B: diag(b) K                 64 x DK
     uint8_t* sGQt = sBK + kC * DK * 4;          // B: (diag(Gam) Q)^T           DK x 64
     uint8_t* sdUt = sGQt + DK * kC * 4;         // A: -dU^T                     128 x 64
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sdUt + kDv * kC * 4);
+    float* sfb = reinterpret_cast<float*>(sdUt + kDv * kC * 4);  // b_r of the chunk in sBK (0 past len)
+    float* sfg = sfb + kC;                                       // Gam_r of the chunk in sGQt (0 past len)
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sfg + kC);
     uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
     const int n = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
     const int i = (warp & 3) * 32 + (tid & 31), cg = warp >> 2;
@@ -840,10 +871,54 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p)
             *reinterpret_cast<float4*>(sOt + umma_koff(ii, r, kSboC)) = tf32_round4(o[it]);
         }
     };
-    auto issue_chunk = [&](size_t ci) {
+    const int hk = h / p.G;
+    // P^T, K^ rows and Q^^T of chunk ci (tokens t0c .., lenc of them; rows >= lenc zero) by cp.async,
+    // and the factors b_r, Gam_r: diag(b) K^ and diag(Gam) Q^ are formed when the copies are rounded
+    auto issue_chunk = [&](size_t ci, int t0c, int lenc) {
         PT::issue_async(sPt, p.Pb + ci * kC * kC);
-        BK::issue_async(sBK, p.BKb + ci * kC * DK);
-        GT::issue_async(sGQt, p.GQb + ci * kC * DK);
+        const float* kr = p.kn + ((size_t)t0c * p.HK + hk) * DK;
+        const float* qr = p.qn + ((size_t)t0c * p.HK + hk) * DK;
+        const size_t st = (size_t)p.HK * DK;
+#pragma unroll
+        for (int it = 0; it < BK::kItems; ++it) {
+            const int r = BK::row(it), k = BK::col(it);
+            uint8_t* d = sBK + umma_koff(r, k, DK * 32);
+            if (r < lenc) cp_async16(d, kr + r * st + k);
+            else *reinterpret_cast<float4*>(d) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int it = 0; it < GT::kItems; ++it) {
+            const int e = tid + it * kNTtc, nn = e % DK, k = (e / DK) * 4;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                uint8_t* d = sGQt + umma_koff(nn, k + t, kC * 32);
+                if (k + t < lenc) cp_async4(d, qr + (k + t) * st + nn);
+                else *reinterpret_cast<float*>(d) = 0.f;
+            }
+        }
+        if (tid < kC) {
+            const float gl = p.gam[(size_t)(t0c + lenc - 1) * p.HV + h];
+            const float gr = tid < lenc ? p.gam[(size_t)(t0c + tid) * p.HV + h] : 0.f;
+            sfb[tid] = tid < lenc ? __expf(gl - gr) : 0.f;
+            sfg[tid] = tid < lenc ? __expf(gr) : 0.f;
+        }
+    };
+    auto scale_round = [&]() {  // this thread's copies: diag(b) K^ and (diag(Gam) Q^)^T, rounded to TF32
+#pragma unroll
+        for (int it = 0; it < BK::kItems; ++it) {
+            const int r = BK::row(it);
+            float4* q = reinterpret_cast<float4*>(sBK + umma_koff(r, BK::col(it), DK * 32));
+            const float4 v = *q;
+            const float f = sfb[r];
+            *q = tf32_round4(make_float4(f * v.x, f * v.y, f * v.z, f * v.w));
+        }
+#pragma unroll
+        for (int it = 0; it < GT::kItems; ++it) {
+            const int e = tid + it * kNTtc, nn = e % DK, k = (e / DK) * 4;
+            float4* q = reinterpret_cast<float4*>(sGQt + umma_koff(nn, k, kC * 32));
+            const float4 v = *q;
+            *q = tf32_round4(make_float4(sfg[k] * v.x, sfg[k + 1] * v.y, sfg[k + 2] * v.z, sfg[k + 3] * v.w));
+        }
     };
     float D[kS];
     const float* df = p.dfinal ? p.dfinal + (((size_t)n * p.HV + h) * kDv + i) * DK + cg * kS : nullptr;
@@ -860,7 +935,7 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p)
     const int jtop = min(nch, p.nchm - p.coff[n]) - 1;  // last chunk inside the workspace
     if (jtop >= 0) {
         const int t0 = bos + jtop * kC;
-        issue_chunk(ch_index(p, p.coff[n] + jtop, h));
+        issue_chunk(ch_index(p, p.coff[n] + jtop, h), t0, min(kC, eos - t0));
         load_dO(t0, min(kC, eos - t0));
         put_dO();
     }
@@ -878,8 +953,8 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p)
         else store_state_slice<kS, false>(p.Db + (ci * kDv + i) * DK + cg * kS, D);
         cp_async_wait_all();  // this thread's copies of P, diag(b) K, diag(Gam) Q
         PT::round_in_place(sPt);
-        BK::round_in_place(sBK);
-        GT::round_in_place(sGQt);
+        __syncthreads();  // sfb, sfg of this chunk are complete
+        scale_round();
         const float Gl = __expf(p.gam[(size_t)(t0 + len - 1) * p.HV + h]);
         tc_sync();
         if (tid == 0) {
@@ -893,7 +968,7 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p)
         w.load(p.Wb + ci * kC * DK);
         if (!(ok = tc_wait(bar, phase))) break;
         w.put(sOt);  // W^T where dO^T was
-        if (prev) issue_chunk(ci - p.HV);
+        if (prev) issue_chunk(ci - p.HV, tp, kC);  // sfb, sfg: read before the barriers above
         {   // dU[s][i] for this thread's 16 values of s; -dU^T as the last product's A
             float x[16];
             tmem_ld<2>(tmem + lane_base + cg * 16, x);
@@ -1155,21 +1230,9 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_wy_tc_kernel(BwdParams p) {
         if (r1 < len) p.gam[(size_t)(t0 + r1) * p.HV + h] = c1;
     }
     __syncthreads();
-    {
-        // the operand copy, and diag(b) K, diag(Gam) Q for the sequential passes (rows >= len zero)
-        const float gl = sg[len - 1];
-        float* BK = p.BKb + ci * kC * kD;
-        float* GQ = p.GQb + ci * kC * kD;
 #pragma unroll
-        for (int it = 0; it < M128::kItems; ++it) {
-            const int m = M128::row(it), r = m & (kC - 1), k = M128::col(it);
-            const float4 v = kq[it];
-            *reinterpret_cast<float4*>(sX + umma_koff(m, k, kSbo)) = tf32_round4(v);
-            const float f = r < len ? __expf(m < kC ? gl - sg[r] : sg[r]) : 0.f;
-            *reinterpret_cast<float4*>((m < kC ? BK : GQ) + (size_t)r * kD + k) =
-                make_float4(f * v.x, f * v.y, f * v.z, f * v.w);
-        }
-    }
+    for (int it = 0; it < M128::kItems; ++it)  // the operand copy
+        *reinterpret_cast<float4*>(sX + umma_koff(M128::row(it), M128::col(it), kSbo)) = tf32_round4(kq[it]);
     tc_sync();
     const uint32_t tmem = *slot;
     uint32_t phase = 0;
@@ -2116,13 +2179,16 @@ static BwdLayout bwd_layout(const gdn_shape* s) {
     L.T = take(CH * kC * kC * 4);
     L.QK = take(CH * kC * kC * 4);
     L.P = take(CH * kC * kC * 4);
-    L.BK = take(CH * kC * dk * 4);
-    L.GQ = take(CH * kC * dk * 4);
+    // diag(b) K and diag(Gam) Q (and the per-chunk dgam partials) only feed the mma.sync kernels; the
+    // tcgen05 path at dk = dv = 128 (bf16) forms them on chip
+    const bool tc128 = s->dtype == GDN_BF16 && dk == 128 && dv == 128;
+    L.BK = take(tc128 ? 0 : CH * kC * dk * 4);
+    L.GQ = take(tc128 ? 0 : CH * kC * dk * 4);
     L.S = take(CH * dv * dk * 4);
     L.D = take(CH * dv * dk * 4);
     L.U = take(CH * kC * dv * 4);
     L.dU = take(CH * kC * dv * 4);
-    L.dgA = take(CH * kC * 4);
+    L.dgA = take(tc128 ? 0 : CH * kC * 4);
     L.dqh = take(T * HV * dk * 4);
     L.dkh = take(T * HV * dk * 4);
     L.total = o;
@@ -2141,8 +2207,8 @@ template <int DK>
 static gdn_status launch_state_tc(const BwdParams& p, int N, int HV, cudaStream_t cs) {
     const dim3 grid(N, HV);
     const size_t tail = 64;  // mbarrier + TMEM address slot
-    const size_t smem_f = (size_t)4 * (128 * DK + kC * DK + 128 * kC + DK * kC + kC * 128) + tail;
-    const size_t smem_b = (size_t)4 * (128 * DK + 128 * kC + kC * kC + kC * DK + DK * kC + 128 * kC) + tail;
+    const size_t smem_f = (size_t)4 * (128 * DK + kC * DK + 128 * kC + DK * kC + kC * 128 + kC) + tail;
+    const size_t smem_b = (size_t)4 * (128 * DK + 128 * kC + kC * kC + kC * DK + DK * kC + 128 * kC + 2 * kC) + tail;
     if (!set_smem(bwd_state_fwd_tc_kernel<DK>, smem_f)) return GDN_ERR_CUDA;
     bwd_state_fwd_tc_kernel<DK><<<grid, kNTtc, smem_f, cs>>>(p);
     if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
