@@ -41,17 +41,17 @@ gdn_status encode_map_3d(CUtensorMap* map, const void* base, gdn_dtype dt, uint6
     return r == CUDA_SUCCESS ? GDN_OK : GDN_ERR_INVALID_ARG;
 }
 
-gdn_status encode_rows_f32_sw128(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t stride,
-                                 uint32_t box_rows) {
+gdn_status encode_rows_sw128(CUtensorMap* map, const void* base, gdn_dtype dt, uint64_t d0, uint64_t d1, uint64_t stride,
+                             uint32_t box_rows) {
     auto fn = encode_fn();
     if (!fn) return GDN_ERR_CUDA;
     const cuuint64_t dims[2] = {d0, d1};
     const cuuint64_t strides[1] = {stride};
-    const cuuint32_t box[2] = {32u, box_rows};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / elem_size(dt)), box_rows};
     const cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(map, dt == GDN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GDN_OK : GDN_ERR_INVALID_ARG;
 }
 

@@ -1599,6 +1599,7 @@ __global__ void __launch_bounds__(kNTtc, 1)
     bwd_intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_u,
                         const __grid_constant__ CUtensorMap tm_du, const __grid_constant__ CUtensorMap tm_s,
                         const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ CUtensorMap tm_t,
+                        const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_v,
                         BwdParams p) {
     constexpr int kD = 128;
     constexpr uint32_t kSboD = kD * 32;  // 128 values per row
@@ -1785,15 +1786,19 @@ __global__ void __launch_bounds__(kNTtc, 1)
             if (lane < 16) part1[q * kC + cg * 16 + lane] = part;
         }
         if (!(ok = tc_wait(bar, phase))) break;
-        // F1 has read dW: Q K^T -> R4 (the first 16 KB) and T -> R4 + 16 KB by tensor copies (swizzled,
-        // 64 rows x 64), for phase B and phase C
+        // Y and F1 have read D^T, U and dW: by tensor copies (swizzled) Q K^T -> R4 (the first 16 KB) and
+        // T -> R4 + 16 KB (64 rows x 64 each), Q^ -> R3 (64 rows x 128), and V (bf16) -> R2 + 16 KB, for
+        // phases B and C
         if (tid == 0) {
-            mbar_arrive_expect_tx(bar_ld, 32768u);
+            mbar_arrive_expect_tx(bar_ld, 81920u);
 #pragma unroll
             for (int a = 0; a < 2; ++a) {
                 tma_load_2d(R4 + 8192 * a, &tm_qk, bar_ld, 32 * a, (int)(ci * kC));
                 tma_load_2d(R4 + 16384 + 8192 * a, &tm_t, bar_ld, 32 * a, (int)(ci * kC));
+                tma_load_2d(R2 + 16384 + 8192 * a, &tm_v, bar_ld, h * kD + 64 * a, t0);
             }
+#pragma unroll
+            for (int a = 0; a < 4; ++a) tma_load_2d(R3 + 8192 * a, &tm_q, bar_ld, hk * kD + 32 * a, t0);
         }
         ld_pending = 1;
         {  // b_r Y back into TMEM as dk^T's first term; k^_r . Y_r
@@ -1854,16 +1859,20 @@ __global__ void __launch_bounds__(kNTtc, 1)
                         tf32_round4(make_float4(d[t], d[t + 1], d[t + 2], d[t + 3]));
             }
         }
-        // V -> R2 (rows s), K^T -> R3 (rows j, k = s) from the copy of K^ in R1, Q^T -> R1 (rows j, k = r):
-        // every load issued before any store
+        // V -> R2 (rows s, from its bf16 copy in R2 + 16 KB), K^T -> R3 (rows j, k = s) from the copy of K^
+        // in R1, Q^T -> R1 (rows j, k = r) from the copy of Q^ in R3: every read before any write
         {
             using RV = RowsTc<kC, kD>;
             constexpr int kIt = kD * kC / 4 / kNTtc;
             float4 vv[RV::kItems], kt[kIt], qt[kIt];
 #pragma unroll
             for (int it = 0; it < RV::kItems; ++it) {
-                const int s = RV::row(it);
-                vv[it] = s < len ? ld4_any(p.v, ob + s * sv + RV::col(it), p.dtype) : z4;
+                const int s = RV::row(it), k = RV::col(it);  // four bf16 of a 128-byte swizzled row
+                const uint2 b = *reinterpret_cast<const uint2*>(
+                    R2 + 16384 + (k >> 6) * 8192 + s * 128 + ((((k & 63) >> 3) ^ (s & 7)) << 4) + (k & 7) * 2);
+                vv[it] = s < len ? make_float4(__uint_as_float(b.x << 16), __uint_as_float(b.x & 0xFFFF0000u),
+                                               __uint_as_float(b.y << 16), __uint_as_float(b.y & 0xFFFF0000u))
+                                 : z4;
             }
 #pragma unroll
             for (int it = 0; it < kIt; ++it) {
@@ -1872,12 +1881,12 @@ __global__ void __launch_bounds__(kNTtc, 1)
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     a[u] = *reinterpret_cast<const float*>(R1 + sw128_off(s + u, j, kC));  // zero past len
-                    b[u] = s + u < len ? qb[(s + u) * sk + j] : 0.f;
+                    b[u] = s + u < len ? *reinterpret_cast<const float*>(R3 + sw128_off(s + u, j, kC)) : 0.f;
                 }
                 kt[it] = make_float4(a[0], a[1], a[2], a[3]);
                 qt[it] = make_float4(b[0], b[1], b[2], b[3]);
             }
-            __syncthreads();  // every read of K^ in R1 is done
+            __syncthreads();  // every read of R1, R2 + 16 KB and R3 is done
 #pragma unroll
             for (int it = 0; it < RV::kItems; ++it)
                 *reinterpret_cast<float4*>(R2 + umma_koff(RV::row(it), RV::col(it), kSboD)) = tf32_round4(vv[it]);
@@ -2322,20 +2331,24 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
     if (tc_state && s->dk == 128) {
         // tensor maps of the operands bwd_intra_tc_kernel copies: K^ ([T][HK * 128]; a chunk's rows from
         // token t0, columns of head hk), U and dU ([chunk-head * 64][128]), S0^T ([chunk-head * 128][128]),
-        // Q K^T and T ([chunk-head * 64][64])
-        CUtensorMap mk{}, mu{}, mdu{}, ms{}, mqk{}, mt{};
+        // Q K^T and T ([chunk-head * 64][64]), Q^ (like K^) and V ([T][HV * 128] bf16)
+        CUtensorMap mk{}, mu{}, mdu{}, ms{}, mqk{}, mt{}, mq{}, mv{};
         const uint64_t CH = (uint64_t)L.nchm * s->HV;
         if (CH * 128 >= (1ull << 31)) return GDN_ERR_UNSUPPORTED;  // copy coordinates are 32-bit
-        if (encode_rows_f32_sw128(&mk, p.kn, (uint64_t)s->HK * 128, (uint64_t)std::max(s->T_total, 1),
+        if (encode_rows_sw128(&mk, p.kn, GDN_F32, (uint64_t)s->HK * 128, (uint64_t)std::max(s->T_total, 1),
                                   (uint64_t)s->HK * 512, kC) != GDN_OK ||
-            encode_rows_f32_sw128(&mu, p.Ub, 128, CH * kC, 512, kC) != GDN_OK ||
-            encode_rows_f32_sw128(&mdu, p.dUb, 128, CH * kC, 512, kC) != GDN_OK ||
-            encode_rows_f32_sw128(&ms, p.Sb, 128, CH * 128, 512, 128) != GDN_OK ||
-            encode_rows_f32_sw128(&mqk, p.QKb, kC, CH * kC, 256, kC) != GDN_OK ||
-            encode_rows_f32_sw128(&mt, p.Tb, kC, CH * kC, 256, kC) != GDN_OK)
+            encode_rows_sw128(&mu, p.Ub, GDN_F32, 128, CH * kC, 512, kC) != GDN_OK ||
+            encode_rows_sw128(&mdu, p.dUb, GDN_F32, 128, CH * kC, 512, kC) != GDN_OK ||
+            encode_rows_sw128(&ms, p.Sb, GDN_F32, 128, CH * 128, 512, 128) != GDN_OK ||
+            encode_rows_sw128(&mqk, p.QKb, GDN_F32, kC, CH * kC, 256, kC) != GDN_OK ||
+            encode_rows_sw128(&mt, p.Tb, GDN_F32, kC, CH * kC, 256, kC) != GDN_OK ||
+            encode_rows_sw128(&mq, p.qn, GDN_F32, (uint64_t)s->HK * 128, (uint64_t)std::max(s->T_total, 1),
+                              (uint64_t)s->HK * 512, kC) != GDN_OK ||
+            encode_rows_sw128(&mv, v, GDN_BF16, (uint64_t)s->HV * 128, (uint64_t)std::max(s->T_total, 1),
+                              (uint64_t)s->HV * 256, kC) != GDN_OK)
             return GDN_ERR_CUDA;
         if (!set_smem(bwd_intra_tc_kernel, kIntraCTcSmem)) return GDN_ERR_CUDA;
-        bwd_intra_tc_kernel<<<gch, kNTtc, kIntraCTcSmem, cs>>>(mk, mu, mdu, ms, mqk, mt, p);
+        bwd_intra_tc_kernel<<<gch, kNTtc, kIntraCTcSmem, cs>>>(mk, mu, mdu, ms, mqk, mt, mq, mv, p);
     } else {
         const size_t smem_is = sizeof(float) * (kMaxD * kLdD + 4 * kC * kLdD + 2 * kC + 32);
         if (!set_smem(bwd_intra_s_kernel, smem_is)) return GDN_ERR_CUDA;

@@ -43,11 +43,11 @@ inline int pick_dv_slice(const gdn_shape* s) { return s->dv_slice ? s->dv_slice 
 gdn_status encode_map_3d(CUtensorMap* map, const void* base, gdn_dtype dt, uint64_t d0, uint64_t d1, uint64_t d2,
                          uint32_t b0, uint32_t b2);
 
-// Encode a rank-2 tiled fp32 tensor map over rows of d0 values (row stride `stride` bytes, d1 rows)
-// with box {32 values, box_rows} and the 128-byte swizzle: one copy lands box_rows rows of 128 bytes
-// in the K-major swizzled operand layout of the tensor cores.
-gdn_status encode_rows_f32_sw128(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t stride,
-                                 uint32_t box_rows);
+// Encode a rank-2 tiled tensor map over rows of d0 elements of dt (row stride `stride` bytes, d1
+// rows) with box {128 bytes of a row, box_rows} and the 128-byte swizzle: one copy lands box_rows
+// rows of 128 bytes in the K-major swizzled operand layout of the tensor cores.
+gdn_status encode_rows_sw128(CUtensorMap* map, const void* base, gdn_dtype dt, uint64_t d0, uint64_t d1, uint64_t stride,
+                             uint32_t box_rows);
 
 inline gdn_status launch_status() {
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
