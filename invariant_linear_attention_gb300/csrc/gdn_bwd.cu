@@ -1166,13 +1166,13 @@ __device__ __forceinline__ float half_sum(float x) {
 //   and U~^T = V^T (T diag(beta))^T with the dk / dv index as the M = 128 rows, so each epilogue
 //   thread stores one column of W and U~: coalesced.
 constexpr int kLdT = kC + 1;  // fp32 A and T in shared memory: row-per-lane writes hit distinct banks
-constexpr size_t kWyTcSmem = (size_t)65536 + 2 * 4 * kC * kLdT + 2 * 4 * kC * kC + 4 * 3 * kC + 16;
+constexpr size_t kWyTcSmem = (size_t)65536 + 2 * 4 * kC * kLdT + 2 * 4 * kC * kC + 4 * 3 * kC + 32;
 
-__global__ void __launch_bounds__(kNTtc, 1) bwd_wy_tc_kernel(BwdParams p) {
+__global__ void __launch_bounds__(kNTtc, 1)
+    bwd_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q, BwdParams p) {
     constexpr int kD = 128;
-    constexpr uint32_t kSbo = kD * 32;
-    extern __shared__ __align__(128) uint8_t smb[];
-    uint8_t* sX = smb;                                          // A: [K; Q] 128 x 128, then K^T | V^T (128 x 64 each)
+    extern __shared__ __align__(1024) uint8_t smb[];
+    uint8_t* sX = smb;  // A: [K; Q] 128 x 128 (swizzled, by tensor copies), then K^T | V^T (128 x 64 each)
     float* sAf = reinterpret_cast<float*>(sX + 65536);          // A (fp32, 64 x kLdT)
     float* sTf = sAf + kC * kLdT;                               // T (fp32, 64 x kLdT)
     uint8_t* sB2 = reinterpret_cast<uint8_t*>(sTf + kC * kLdT); // B: T diag(beta Gam)  64 x 64
@@ -1181,7 +1181,8 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_wy_tc_kernel(BwdParams p) {
     float* sGb = sg + kC;                                       // beta Gam
     float* sb = sGb + kC;                                       // beta
     uint64_t* bar = reinterpret_cast<uint64_t*>(sb + kC);
-    uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
+    uint64_t* bar_ld = bar + 1;  // the tensor copies of K^ and Q^
+    uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 2);
     const int c = blockIdx.x, h = blockIdx.y;
     int n, t0, len;
     if (!chunk_of(p, c, n, t0, len)) return;
@@ -1189,21 +1190,24 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_wy_tc_kernel(BwdParams p) {
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const int hk = h / p.G;
     const size_t ci = ch_index(p, c, h);
-    using M128 = RowsTc<kD, kD>;
+    if (smem_u32(smb) & 1023u) {  // the swizzled atoms need 1 KB alignment (the same for every CTA)
+        if (tid == 0) atomicOr(p.err, GDN_DEVERR_SMEM_ALIGN);
+        return;
+    }
+    // K^ (rows 0..63) and Q^ (rows 64..127) by tensor copies, four swizzled boxes of 32 values each,
+    // in flight while warp 0 takes the cumsum
     if (tid == 0) {
         mbar_init(bar, 1);
+        mbar_init(bar_ld, 1);
         fence_barrier_init();
+        mbar_arrive_expect_tx(bar_ld, 65536u);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            tma_load_2d(sX + 16384 * a, &tm_k, bar_ld, hk * kD + 32 * a, t0);
+            tma_load_2d(sX + 16384 * a + 8192, &tm_q, bar_ld, hk * kD + 32 * a, t0);
+        }
     }
     if (warp == 0) tmem_alloc(slot, 256);
-    // K (rows 0..63) and Q (rows 64..127), rows >= len zero, in flight while warp 0 takes the cumsum
-    float4 kq[M128::kItems];
-#pragma unroll
-    for (int it = 0; it < M128::kItems; ++it) {
-        const int r = M128::row(it) & (kC - 1), k = M128::col(it);
-        const float* src = M128::row(it) < kC ? p.kn : p.qn;
-        kq[it] = r < len ? *reinterpret_cast<const float4*>(src + ((size_t)(t0 + r) * p.HK + hk) * kD + k)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
     if (warp == 0) {
         // inclusive cumsum of g over the chunk, fixed order (lane-serial blocks of 2)
         float g0 = 0.f, g1 = 0.f;
@@ -1229,17 +1233,35 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_wy_tc_kernel(BwdParams p) {
         if (r0 < len) p.gam[(size_t)(t0 + r0) * p.HV + h] = c0;
         if (r1 < len) p.gam[(size_t)(t0 + r1) * p.HV + h] = c1;
     }
-    __syncthreads();
+    __syncthreads();  // the barriers' initialisation is visible
+    bool ok = __syncthreads_and(mbar_wait_bounded(bar_ld, 0));
+    if (ok) {
+        // TF32 rounding of the copy, and zero rows past the chunk (the copy fills them from the next
+        // sequence): rows len..63 of K^ and of Q^, 128 bytes in each atom column
 #pragma unroll
-    for (int it = 0; it < M128::kItems; ++it)  // the operand copy
-        *reinterpret_cast<float4*>(sX + umma_koff(M128::row(it), M128::col(it), kSbo)) = tf32_round4(kq[it]);
+        for (int it = 0; it < 65536 / 16 / kNTtc; ++it) {
+            float4* v = reinterpret_cast<float4*>(sX) + tid + it * kNTtc;
+            *v = tf32_round4(*v);
+        }
+        if (len < kC) {
+            __syncthreads();
+            for (int e = tid; e < 2 * (kC - len) * 32; e += kNTtc) {
+                const int u = e & 7, a = (e >> 3) & 3, rr = len + (e >> 5) % (kC - len), half = (e >> 5) / (kC - len);
+                *reinterpret_cast<float4*>(sX + 16384 * a + 128 * (rr + kC * half) + 16 * u) =
+                    make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+    } else if (tid == 0) {
+        mbar_wait_bounded(bar_ld, 0);  // copies still in flight land before the CTA leaves
+    }
     tc_sync();
     const uint32_t tmem = *slot;
     uint32_t phase = 0;
-    bool ok;
     do {
+        if (!ok) break;
         if (tid == 0) {
-            umma_tf32_k(tmem, smem_u32(sX), kSbo, smem_u32(sX), kSbo, umma_idesc_tf32(kD, kC), kD, false);
+            const UmmaOp x = op_sw(smem_u32(sX), kD);
+            umma_tf32_op(tmem, x, x, umma_idesc_tf32(kD, kC), kD, false);
             umma_commit(bar);
         }
         if (!(ok = tc_wait(bar, phase))) break;
@@ -1273,8 +1295,9 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_wy_tc_kernel(BwdParams p) {
         tc_fence_before();
         __syncthreads();  // A complete; the first product has read sX
         {
-            // K (row s, four consecutive j) and V rows (bf16 bits, unconverted), s >= len zero, by vector
-            // loads in flight during the solve; written transposed into sX after it: K^T (j, s) and V^T (i, s)
+            // K (row s, four consecutive j, from the copy in sX) and V rows (bf16 bits, unconverted, by
+            // vector loads in flight during the solve), s >= len zero; written transposed into sX after
+            // it: K^T (j, s) and V^T (i, s)
             using RowsK = RowsTc<kC, kD>;
             float4 kr[RowsK::kItems];
             uint2 vr[RowsK::kItems];
@@ -1282,8 +1305,7 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_wy_tc_kernel(BwdParams p) {
 #pragma unroll
             for (int it = 0; it < RowsK::kItems; ++it) {
                 const int s = RowsK::row(it), k = RowsK::col(it);
-                kr[it] = s < len ? *reinterpret_cast<const float4*>(p.kn + ((size_t)(t0 + s) * p.HK + hk) * kD + k)
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                kr[it] = *reinterpret_cast<const float4*>(sX + sw128_off(s, k, kD));
                 vr[it] = s < len ? *reinterpret_cast<const uint2*>(vb + ((size_t)(t0 + s) * p.HV + h) * kD + k)
                                  : make_uint2(0u, 0u);
             }
@@ -2297,9 +2319,19 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
     }
     const dim3 gch(L.nchm, s->HV);
     const bool tc_state = s->dtype == GDN_BF16 && s->dv == 128 && (s->dk == 32 || s->dk == 64 || s->dk == 128);
-    if (tc_state && s->dk == 128) {
+    // tensor maps of the normalised q and k ([T][HK * 128] fp32: a chunk's rows from token t0, columns
+    // of head hk), copied by bwd_wy_tc_kernel and bwd_intra_tc_kernel
+    CUtensorMap mk{}, mq{};
+    const bool tc128 = tc_state && s->dk == 128;
+    if (tc128 &&
+        (encode_rows_sw128(&mk, p.kn, GDN_F32, (uint64_t)s->HK * 128, (uint64_t)std::max(s->T_total, 1),
+                           (uint64_t)s->HK * 512, kC) != GDN_OK ||
+         encode_rows_sw128(&mq, p.qn, GDN_F32, (uint64_t)s->HK * 128, (uint64_t)std::max(s->T_total, 1),
+                           (uint64_t)s->HK * 512, kC) != GDN_OK))
+        return GDN_ERR_CUDA;
+    if (tc128) {
         if (!set_smem(bwd_wy_tc_kernel, kWyTcSmem)) return GDN_ERR_CUDA;
-        bwd_wy_tc_kernel<<<gch, kNTtc, kWyTcSmem, cs>>>(p);
+        bwd_wy_tc_kernel<<<gch, kNTtc, kWyTcSmem, cs>>>(mk, mq, p);
     } else {
         const size_t smem_wy = sizeof(float) * (2 * kC * kLdD + 2 * kC * kLdC + 3 * kC);
         if (!set_smem(bwd_wy_kernel, smem_wy)) return GDN_ERR_CUDA;
@@ -2328,22 +2360,17 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
         if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
     }
 
-    if (tc_state && s->dk == 128) {
-        // tensor maps of the operands bwd_intra_tc_kernel copies: K^ ([T][HK * 128]; a chunk's rows from
-        // token t0, columns of head hk), U and dU ([chunk-head * 64][128]), S0^T ([chunk-head * 128][128]),
-        // Q K^T and T ([chunk-head * 64][64]), Q^ (like K^) and V ([T][HV * 128] bf16)
-        CUtensorMap mk{}, mu{}, mdu{}, ms{}, mqk{}, mt{}, mq{}, mv{};
+    if (tc128) {
+        // tensor maps of the other operands bwd_intra_tc_kernel copies: U and dU ([chunk-head * 64][128]),
+        // S0^T ([chunk-head * 128][128]), Q K^T and T ([chunk-head * 64][64]), V ([T][HV * 128] bf16)
+        CUtensorMap mu{}, mdu{}, ms{}, mqk{}, mt{}, mv{};
         const uint64_t CH = (uint64_t)L.nchm * s->HV;
         if (CH * 128 >= (1ull << 31)) return GDN_ERR_UNSUPPORTED;  // copy coordinates are 32-bit
-        if (encode_rows_sw128(&mk, p.kn, GDN_F32, (uint64_t)s->HK * 128, (uint64_t)std::max(s->T_total, 1),
-                                  (uint64_t)s->HK * 512, kC) != GDN_OK ||
-            encode_rows_sw128(&mu, p.Ub, GDN_F32, 128, CH * kC, 512, kC) != GDN_OK ||
+        if (encode_rows_sw128(&mu, p.Ub, GDN_F32, 128, CH * kC, 512, kC) != GDN_OK ||
             encode_rows_sw128(&mdu, p.dUb, GDN_F32, 128, CH * kC, 512, kC) != GDN_OK ||
             encode_rows_sw128(&ms, p.Sb, GDN_F32, 128, CH * 128, 512, 128) != GDN_OK ||
             encode_rows_sw128(&mqk, p.QKb, GDN_F32, kC, CH * kC, 256, kC) != GDN_OK ||
             encode_rows_sw128(&mt, p.Tb, GDN_F32, kC, CH * kC, 256, kC) != GDN_OK ||
-            encode_rows_sw128(&mq, p.qn, GDN_F32, (uint64_t)s->HK * 128, (uint64_t)std::max(s->T_total, 1),
-                              (uint64_t)s->HK * 512, kC) != GDN_OK ||
             encode_rows_sw128(&mv, v, GDN_BF16, (uint64_t)s->HV * 128, (uint64_t)std::max(s->T_total, 1),
                               (uint64_t)s->HV * 256, kC) != GDN_OK)
             return GDN_ERR_CUDA;
