@@ -735,6 +735,8 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p)
     // factors b_r in sfb; the product diag(b) K^ is taken when the operand is written (bk_put)
     const int hk = h / p.G;
     ColsTc<DK, kC> bk;
+    float fb_gl = 0.f, fb_gr = 0.f;  // gam_last and gam_r (r = tid < 64) of the chunk in bk, or 0 past len
+    bool fb_in = false;
     auto bk_load = [&](int jc) {
         const int t0c = bos + jc * kC, lenc = min(kC, eos - t0c);
         const float* kr = p.kn + ((size_t)t0c * p.HK + hk) * DK;
@@ -745,9 +747,10 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p)
             bk.v[it] = make_float4(k < lenc ? kr[k * st + nn] : 0.f, k + 1 < lenc ? kr[(k + 1) * st + nn] : 0.f,
                                    k + 2 < lenc ? kr[(k + 2) * st + nn] : 0.f, k + 3 < lenc ? kr[(k + 3) * st + nn] : 0.f);
         }
-        if (tid < kC) {
-            const float gl = p.gam[(size_t)(t0c + lenc - 1) * p.HV + h];
-            sfb[tid] = tid < lenc ? __expf(gl - p.gam[(size_t)(t0c + tid) * p.HV + h]) : 0.f;
+        if (tid < kC) {  // used a chunk step later: no wait for these loads here
+            fb_in = tid < lenc;
+            fb_gl = p.gam[(size_t)(t0c + lenc - 1) * p.HV + h];
+            fb_gr = fb_in ? p.gam[(size_t)(t0c + tid) * p.HV + h] : 0.f;
         }
     };
     auto bk_put = [&]() {
@@ -778,6 +781,7 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p)
         else store_state_slice<kS, false>(p.Sb + (ci * kDv + i) * DK + cg * kS, S);
         cp_async_wait_all();  // this thread's copies of W and U~ (commits what is still open)
         round_w();
+        if (tid < kC) sfb[tid] = fb_in ? __expf(fb_gl - fb_gr) : 0.f;
         __syncthreads();  // sfb of this chunk is complete
         bk_put();
         const float Gl = __expf(p.gam[(size_t)(t0 + len - 1) * p.HV + h]);
@@ -786,7 +790,7 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p)
             umma_tf32_k(tmem, smem_u32(sS), kSboD, smem_u32(sW), kSboD, umma_idesc_tf32(kDv, kC), DK, false);
             umma_commit(bar);
         }
-        if (next) bk_load(j + 1);  // sfb: every read of it was before the barrier above
+        if (next) bk_load(j + 1);
         if (!(ok = tc_wait(bar, phase))) break;
         if (next) issue_w(cn);
         {   // U[r][i] = U~[r][i] - (S W^T)[i][r] for this thread's 16 values of r
@@ -874,6 +878,8 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p)
     const int hk = h / p.G;
     // P^T, K^ rows and Q^^T of chunk ci (tokens t0c .., lenc of them; rows >= lenc zero) by cp.async,
     // and the factors b_r, Gam_r: diag(b) K^ and diag(Gam) Q^ are formed when the copies are rounded
+    float fb_gl = 0.f, fb_gr = 0.f;  // gam_last and gam_r (r = tid < 64) of the chunk being copied
+    bool fb_in = false;
     auto issue_chunk = [&](size_t ci, int t0c, int lenc) {
         PT::issue_async(sPt, p.Pb + ci * kC * kC);
         const float* kr = p.kn + ((size_t)t0c * p.HK + hk) * DK;
@@ -896,11 +902,10 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p)
                 else *reinterpret_cast<float*>(d) = 0.f;
             }
         }
-        if (tid < kC) {
-            const float gl = p.gam[(size_t)(t0c + lenc - 1) * p.HV + h];
-            const float gr = tid < lenc ? p.gam[(size_t)(t0c + tid) * p.HV + h] : 0.f;
-            sfb[tid] = tid < lenc ? __expf(gl - gr) : 0.f;
-            sfg[tid] = tid < lenc ? __expf(gr) : 0.f;
+        if (tid < kC) {  // used a chunk step later: no wait for these loads here
+            fb_in = tid < lenc;
+            fb_gl = p.gam[(size_t)(t0c + lenc - 1) * p.HV + h];
+            fb_gr = fb_in ? p.gam[(size_t)(t0c + tid) * p.HV + h] : 0.f;
         }
     };
     auto scale_round = [&]() {  // this thread's copies: diag(b) K^ and (diag(Gam) Q^)^T, rounded to TF32
@@ -953,6 +958,10 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p)
         else store_state_slice<kS, false>(p.Db + (ci * kDv + i) * DK + cg * kS, D);
         cp_async_wait_all();  // this thread's copies of P, diag(b) K, diag(Gam) Q
         PT::round_in_place(sPt);
+        if (tid < kC) {
+            sfb[tid] = fb_in ? __expf(fb_gl - fb_gr) : 0.f;
+            sfg[tid] = fb_in ? __expf(fb_gr) : 0.f;
+        }
         __syncthreads();  // sfb, sfg of this chunk are complete
         scale_round();
         const float Gl = __expf(p.gam[(size_t)(t0 + len - 1) * p.HV + h]);
@@ -968,7 +977,7 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p)
         w.load(p.Wb + ci * kC * DK);
         if (!(ok = tc_wait(bar, phase))) break;
         w.put(sOt);  // W^T where dO^T was
-        if (prev) issue_chunk(ci - p.HV, tp, kC);  // sfb, sfg: read before the barriers above
+        if (prev) issue_chunk(ci - p.HV, tp, kC);
         {   // dU[s][i] for this thread's 16 values of s; -dU^T as the last product's A
             float x[16];
             tmem_ld<2>(tmem + lane_base + cg * 16, x);
@@ -1171,7 +1180,8 @@ constexpr size_t kWyTcSmem = (size_t)65536 + 2 * 4 * kC * kLdT + 2 * 4 * kC * kC
 __global__ void __launch_bounds__(kNTtc, 1)
     bwd_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q, BwdParams p) {
     constexpr int kD = 128;
-    extern __shared__ __align__(1024) uint8_t smb[];
+    extern __shared__ __align__(1024) uint8_t smb_sw[];  // swizzled operands: 1 KB aligned
+    uint8_t* const smb = smb_sw;
     uint8_t* sX = smb;  // A: [K; Q] 128 x 128 (swizzled, by tensor copies), then K^T | V^T (128 x 64 each)
     float* sAf = reinterpret_cast<float*>(sX + 65536);          // A (fp32, 64 x kLdT)
     float* sTf = sAf + kC * kLdT;                               // T (fp32, 64 x kLdT)
@@ -1625,7 +1635,8 @@ __global__ void __launch_bounds__(kNTtc, 1)
                         BwdParams p) {
     constexpr int kD = 128;
     constexpr uint32_t kSboD = kD * 32;  // 128 values per row
-    extern __shared__ __align__(1024) uint8_t smb[];
+    extern __shared__ __align__(1024) uint8_t smb_sw[];  // swizzled operands: 1 KB aligned
+    uint8_t* const smb = smb_sw;
     uint8_t* R1 = smb;
     uint8_t* R2 = R1 + 32768;
     uint8_t* R3 = R2 + 32768;
@@ -2323,6 +2334,8 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
     // of head hk), copied by bwd_wy_tc_kernel and bwd_intra_tc_kernel
     CUtensorMap mk{}, mq{};
     const bool tc128 = tc_state && s->dk == 128;
+    const uint64_t CH = (uint64_t)L.nchm * s->HV;
+    if (tc128 && CH * 128 >= (1ull << 31)) return GDN_ERR_UNSUPPORTED;  // copy coordinates are 32-bit
     if (tc128 &&
         (encode_rows_sw128(&mk, p.kn, GDN_F32, (uint64_t)s->HK * 128, (uint64_t)std::max(s->T_total, 1),
                            (uint64_t)s->HK * 512, kC) != GDN_OK ||
@@ -2364,8 +2377,6 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
         // tensor maps of the other operands bwd_intra_tc_kernel copies: U and dU ([chunk-head * 64][128]),
         // S0^T ([chunk-head * 128][128]), Q K^T and T ([chunk-head * 64][64]), V ([T][HV * 128] bf16)
         CUtensorMap mu{}, mdu{}, ms{}, mqk{}, mt{}, mv{};
-        const uint64_t CH = (uint64_t)L.nchm * s->HV;
-        if (CH * 128 >= (1ull << 31)) return GDN_ERR_UNSUPPORTED;  // copy coordinates are 32-bit
         if (encode_rows_sw128(&mu, p.Ub, GDN_F32, 128, CH * kC, 512, kC) != GDN_OK ||
             encode_rows_sw128(&mdu, p.dUb, GDN_F32, 128, CH * kC, 512, kC) != GDN_OK ||
             encode_rows_sw128(&ms, p.Sb, GDN_F32, 128, CH * 128, 512, 128) != GDN_OK ||
