@@ -1,6 +1,7 @@
 // gdn_umma.cuh -- fifth-generation tensor core (tcgen05) building blocks for the
-// chunked backward's serial state passes: TF32 products with operands in shared
-// memory, fp32 accumulators in tensor memory (TMEM), completion on an mbarrier.
+// chunked backward: TF32 products with operands in shared memory, fp32
+// accumulators in tensor memory (TMEM), completion on an mbarrier, and the 2-D
+// tensor copies that bring operands into the 128-byte-swizzled layout.
 //
 // Operand layout ("K-major, no swizzle"): a matrix X with rows n and reduction
 // index k is stored as 8-row x 16-byte core matrices (8 rows of 4 fp32 each,
@@ -124,6 +125,15 @@ __host__ __device__ constexpr uint32_t sw128_off(int n, int k, int rows) {
 __device__ __forceinline__ void umma_tf32_op(uint32_t d_tmem, const UmmaOp& a, const UmmaOp& b, uint32_t idesc, int K,
                                              bool accumulate) {
     for (int s = 0; s < K / 8; ++s) umma_tf32(d_tmem, umma_op_desc(a, s), umma_op_desc(b, s), idesc, accumulate || s > 0);
+}
+
+// 2-D tiled tensor copy of one box into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, uint64_t* bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
 }
 
 // Arrive on bar once every MMA this thread issued so far has completed.
