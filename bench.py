@@ -802,7 +802,7 @@ def profile_extras():
     print(json.dumps({"profile_extras": "ok", "tokens": int(L.x.shape[0])}))
 
 
-def bench_backward(gdn, dev, steps=3):
+def bench_backward(gdn, dev, steps=10):
     """gdn_chunk_bwd on 8 x 4096 tokens, HK=16, HV=32, dk=dv=128, bf16, dO ~ randn (seed 6)."""
     from invariant_linear_attention_gb300 import inputs
     x = inputs.make_inputs([BWD_L] * BWD_N, HK=HK, HV=HV, dk=DK, dv=DV, dtype=torch.bfloat16, seed=6)
