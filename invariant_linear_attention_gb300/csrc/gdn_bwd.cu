@@ -18,16 +18,17 @@
 //     dW = -dU S0, dV = diag(beta) T^T dU, dA = -T^T dT T^T, dT = dW (beta Gam K)^T + dU (beta V)^T
 //     plus the dbeta and dgam terms; dg = reverse cumsum of dgam inside the chunk.
 // Dense products run on the tensor cores in TF32 with fp32 accumulation.  For bf16
-// inputs with dv = 128 the serial state passes, and at dk = dv = 128 all four chunk
-// stages (bwd_wy, both state passes, bwd_intra_s, bwd_intra_c), use the fifth-generation
-// tensor cores (tcgen05: operands in shared memory, accumulators in TMEM; gdn_umma.cuh)
-// in *_tc kernels.  Products that produce dk- or dv-wide results are laid out with that
+// inputs with dv = 128 the serial state passes, and at dk = dv = 128 every contracting
+// stage, use the fifth-generation tensor cores (tcgen05: operands in shared memory,
+// accumulators in TMEM; gdn_umma.cuh) in *_tc kernels; there bwd_intra_s and bwd_intra_c
+// are one kernel, bwd_intra_tc, and the operands that come from memory unchanged arrive by
+// tensor copies.  Products that produce dk- or dv-wide results are laid out with that
 // index as their 128 rows; the C x C ones use M = 64.  Other shapes and fp32 inputs go
 // through one CTA-wide mma.sync helper (m16n8k8; 3xTF32 split for fp32 inputs, about
 // fp32 accuracy), or the fp32 SIMT loop below when built with GDN_BWD_SIMT.  Kernels:
 //     bwd_offsets   chunk offsets per sequence (+ cu_seqlens validation)
 //     bwd_norm      q^, k^ and 1/|.| per (token, k-head)
-//     bwd_wy        per (chunk, head): gam, T, W, U~, Q K^T              [chunk-parallel]
+//     bwd_wy        per (chunk, head): gam, T, W, U~, Q K^T (+ diag(b) K, diag(Gam) Q off tcgen05)
 //     bwd_state_fwd per (sequence, head, dv slice): chunk-start states S_c and U   [sequential]
 //     bwd_state_bwd per (sequence, head, dv slice): D_c (end-of-chunk grads) and dU; d_init_state
 //     bwd_intra_s   per (chunk, head): the products with S0 and D (dQ_S, dW, U D)  [chunk-parallel]
@@ -679,7 +680,8 @@ __device__ __forceinline__ void put_slice_tc(uint8_t* dst, int i, int c0, uint32
 // per (sequence, head), chunks in order: S_c out, U = U~ - W S^T, S <- Gam_last S + U^T diag(b) K.
 // Software-pipelined: while chunk j computes, chunk j+1's W and U~ arrive in shared memory by
 // 16-byte cp.async (W into its operand buffer once the first product has read it, U~ into its
-// own buffer once the first epilogue has read it) and its diag(b) K comes into registers.
+// own buffer once the first epilogue has read it), and its normalised keys come into registers;
+// diag(b) K is formed when they are written as the operand.
 template <int DK>
 __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p) {
     constexpr int kDv = 128, kS = DK / 4;
@@ -777,8 +779,6 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p)
         const int t0 = bos + j * kC, len = min(kC, eos - t0);
         const size_t ci = ch_index(p, c, h), cn = ch_index(p, c + 1, h);
         const bool next = has(j + 1);
-        if constexpr (kStateT) store_state_slice<kS, true>(p.Sb + (ci * DK + cg * kS) * kDv + i, S);
-        else store_state_slice<kS, false>(p.Sb + (ci * kDv + i) * DK + cg * kS, S);
         cp_async_wait_all();  // this thread's copies of W and U~ (commits what is still open)
         round_w();
         if (tid < kC) sfb[tid] = fb_in ? __expf(fb_gl - fb_gr) : 0.f;
@@ -790,6 +790,9 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p)
             umma_tf32_k(tmem, smem_u32(sS), kSboD, smem_u32(sW), kSboD, umma_idesc_tf32(kDv, kC), DK, false);
             umma_commit(bar);
         }
+        // chunk-start state out while the product runs
+        if constexpr (kStateT) store_state_slice<kS, true>(p.Sb + (ci * DK + cg * kS) * kDv + i, S);
+        else store_state_slice<kS, false>(p.Sb + (ci * kDv + i) * DK + cg * kS, S);
         if (next) bk_load(j + 1);
         if (!(ok = tc_wait(bar, phase))) break;
         if (next) issue_w(cn);
@@ -830,8 +833,9 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p)
 //   dU^T = dO^T P + D (diag(b) K)^T,   D <- Gam_last D + dO^T diag(Gam) Q - dU^T W
 // The first product and dO^T (diag(Gam) Q) go out together, so once they complete the buffers of
 // dO^T, P^T, diag(b) K and (diag(Gam) Q)^T are free: W^T (loaded into registers meanwhile)
-// takes dO^T's place for the last product, and the next chunk's P, diag(b) K and diag(Gam) Q
-// start arriving by cp.async; the next chunk's dO comes into registers during the last product.
+// takes dO^T's place for the last product, and the next chunk's P and normalised k and q rows
+// start arriving by cp.async (scaled into diag(b) K and diag(Gam) Q when they are rounded); the
+// next chunk's dO comes into registers during the last product.
 template <int DK>
 __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p) {
     constexpr int kDv = 128, kS = DK / 4;
