@@ -1636,7 +1636,7 @@ __global__ void __launch_bounds__(kNTtc, 1)
                         const __grid_constant__ CUtensorMap tm_du, const __grid_constant__ CUtensorMap tm_s,
                         const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ CUtensorMap tm_t,
                         const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_v,
-                        BwdParams p) {
+                        const __grid_constant__ CUtensorMap tm_do, BwdParams p) {
     constexpr int kD = 128;
     constexpr uint32_t kSboD = kD * 32;  // 128 values per row
     extern __shared__ __align__(1024) uint8_t smb_sw[];  // swizzled operands: 1 KB aligned
@@ -1669,10 +1669,9 @@ __global__ void __launch_bounds__(kNTtc, 1)
     const bool row_lane = lane < 16;    // lanes holding a row of an M = 64 result
     const int r64 = 16 * q + (lane & 15);  // that row
     const int jj = 32 * q + lane;          // the dk / dv index of an M = 128 result
-    const size_t sk = (size_t)p.HK * kD, sv = (size_t)p.HV * kD;
+    const size_t sk = (size_t)p.HK * kD;
     const float* kb = p.kn + ((size_t)t0 * p.HK + hk) * kD;  // K^ row s at kb + s * sk
     const float* qb = p.qn + ((size_t)t0 * p.HK + hk) * kD;
-    const size_t ob = ((size_t)t0 * p.HV + h) * kD;           // dO / V row r at ob + r * sv
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
     // the swizzled atoms need 1 KB alignment of the dynamic shared memory (the same for every CTA)
     if (smem_u32(smb) & 1023u) {
@@ -1680,13 +1679,13 @@ __global__ void __launch_bounds__(kNTtc, 1)
         return;
     }
     // phase A: K^ -> R1, U -> R3, dU -> R5 (rows = chunk positions), S0^T in two K-halves -> R4 and
-    // C1|C2 (rows j, k = i), all by tensor copies (four boxes of 32 values per operand); dO -> R2
-    // through registers meanwhile
+    // C1|C2 (rows j, k = i), all by tensor copies (four boxes of 32 values per operand), and dO (bf16,
+    // two boxes of 64 values) -> R2 + 16 KB, converted into R2 once it lands
     if (tid == 0) {
         mbar_init(bar, 1);
         mbar_init(bar_ld, 1);
         fence_barrier_init();
-        mbar_arrive_expect_tx(bar_ld, 5u * 32768u);
+        mbar_arrive_expect_tx(bar_ld, 5u * 32768u + 16384u);
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
             tma_load_2d(R1 + 8192 * a, &tm_k, bar_ld, hk * kD + 32 * a, t0);
@@ -1694,6 +1693,8 @@ __global__ void __launch_bounds__(kNTtc, 1)
             tma_load_2d(R5 + 8192 * a, &tm_du, bar_ld, 32 * a, (int)(ci * kC));
             tma_load_2d((a < 2 ? R4 : C1) + 16384 * (a & 1), &tm_s, bar_ld, 32 * a, (int)(ci * kD));
         }
+        tma_load_2d(R2 + 16384, &tm_do, bar_ld, h * kD, t0);
+        tma_load_2d(R2 + 24576, &tm_do, bar_ld, h * kD + 64, t0);
     }
     if (warp == 0) tmem_alloc(slot, 512);
     const float* Dt = p.Db + ci * kD * kD;    // D^T: row j (dk index), dv index contiguous
@@ -1709,7 +1710,6 @@ __global__ void __launch_bounds__(kNTtc, 1)
             const int k = 32 * (f >> 10) + 4 * ((f & 7) ^ (j & 7));
             dreg[hf][it] = *reinterpret_cast<const float4*>(Dt + j * kD + kC * hf + k);
         }
-    stage_rows_fn<kC, kD>(R2, [&](int r, int k) { return r < len ? ld4_any(p.dout, ob + r * sv + k, p.dtype) : z4; });
     for (int i = tid; i < kC; i += kNTtc) {
         sg[i] = i < len ? p.gam[(size_t)(t0 + i) * p.HV + h] : 0.f;
         sbe[i] = i < len ? p.beta[(size_t)(t0 + i) * p.HV + h] : 0.f;
@@ -1720,6 +1720,25 @@ __global__ void __launch_bounds__(kNTtc, 1)
     int ld_pending = ok ? -1 : 0;  // parity of tensor copies issued and not yet seen complete
     float dot = 0.f;  // this thread's share of <D, S0>, in fp32
     if (ok) {
+        // dO: its bf16 copy in R2 + 16 KB (two swizzled boxes of 64 rows x 64) -> R2 in fp32, rows
+        // >= len zero; every read before any write
+        {
+            using RO = RowsTc<kC, kD>;
+            float4 ov[RO::kItems];
+#pragma unroll
+            for (int u = 0; u < RO::kItems; ++u) {
+                const int r = RO::row(u), k = RO::col(u);
+                const uint2 b = *reinterpret_cast<const uint2*>(
+                    R2 + 16384 + (k >> 6) * 8192 + r * 128 + ((((k & 63) >> 3) ^ (r & 7)) << 4) + (k & 7) * 2);
+                ov[u] = r < len ? make_float4(__uint_as_float(b.x << 16), __uint_as_float(b.x & 0xFFFF0000u),
+                                              __uint_as_float(b.y << 16), __uint_as_float(b.y & 0xFFFF0000u))
+                                : z4;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int u = 0; u < RO::kItems; ++u)
+                *reinterpret_cast<float4*>(R2 + umma_koff(RO::row(u), RO::col(u), kSboD)) = tf32_round4(ov[u]);
+        }
         // TF32 rounding of the copied operands (five 32 KB buffers, any layout), and zero rows of K^
         // past the chunk (the copy fills them from the next sequence)
         uint8_t* const bufs[3] = {R1, R3, R5};
@@ -2379,18 +2398,20 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
 
     if (tc128) {
         // tensor maps of the other operands bwd_intra_tc_kernel copies: U and dU ([chunk-head * 64][128]),
-        // S0^T ([chunk-head * 128][128]), Q K^T and T ([chunk-head * 64][64]), V ([T][HV * 128] bf16)
-        CUtensorMap mu{}, mdu{}, ms{}, mqk{}, mt{}, mv{};
+        // S0^T ([chunk-head * 128][128]), Q K^T and T ([chunk-head * 64][64]), V and dO ([T][HV * 128] bf16)
+        CUtensorMap mu{}, mdu{}, ms{}, mqk{}, mt{}, mv{}, mdo{};
         if (encode_rows_sw128(&mu, p.Ub, GDN_F32, 128, CH * kC, 512, kC) != GDN_OK ||
             encode_rows_sw128(&mdu, p.dUb, GDN_F32, 128, CH * kC, 512, kC) != GDN_OK ||
             encode_rows_sw128(&ms, p.Sb, GDN_F32, 128, CH * 128, 512, 128) != GDN_OK ||
             encode_rows_sw128(&mqk, p.QKb, GDN_F32, kC, CH * kC, 256, kC) != GDN_OK ||
             encode_rows_sw128(&mt, p.Tb, GDN_F32, kC, CH * kC, 256, kC) != GDN_OK ||
             encode_rows_sw128(&mv, v, GDN_BF16, (uint64_t)s->HV * 128, (uint64_t)std::max(s->T_total, 1),
+                              (uint64_t)s->HV * 256, kC) != GDN_OK ||
+            encode_rows_sw128(&mdo, d_out, GDN_BF16, (uint64_t)s->HV * 128, (uint64_t)std::max(s->T_total, 1),
                               (uint64_t)s->HV * 256, kC) != GDN_OK)
             return GDN_ERR_CUDA;
         if (!set_smem(bwd_intra_tc_kernel, kIntraCTcSmem)) return GDN_ERR_CUDA;
-        bwd_intra_tc_kernel<<<gch, kNTtc, kIntraCTcSmem, cs>>>(mk, mu, mdu, ms, mqk, mt, mq, mv, p);
+        bwd_intra_tc_kernel<<<gch, kNTtc, kIntraCTcSmem, cs>>>(mk, mu, mdu, ms, mqk, mt, mq, mv, mdo, p);
     } else {
         const size_t smem_is = sizeof(float) * (kMaxD * kLdD + 4 * kC * kLdD + 2 * kC + 32);
         if (!set_smem(bwd_intra_s_kernel, smem_is)) return GDN_ERR_CUDA;
