@@ -1323,41 +1323,59 @@ __global__ void __launch_bounds__(kNTtc, 1)
                 vr[it] = s < len ? *reinterpret_cast<const uint2*>(vb + ((size_t)(t0 + s) * p.HV + h) * kD + k)
                                  : make_uint2(0u, 0u);
             }
-            // T = (I + A)^-1, one column per forward substitution: column j solves (I + A) t = e_j.
-            // Warp w takes columns {w, 31 - w, 32 + w, 63 - w} as four independent chains; lane l
-            // keeps the partial sums sigma_r = sum_{s < r} A[r][s] t[s] of rows r = l and l + 32.
-            // Right-looking, s = 0 .. 63 in order: the owner of row s holds its final sigma_s, so
-            // t[s] = (s == j) - sigma_s (0 above the diagonal); it is broadcast and every lane adds
-            // A[r][s] t[s] to its rows' partials (A is strictly lower, so rows r <= s add 0).  At
-            // the end T[r][j] = (r == j) - sigma_r for every row.  All indices are compile-time.
+            // T = (I + A)^-1 by 16 x 16 blocks (A is strictly lower).  The diagonal blocks
+            // T_II = (I + A_II)^-1 by forward substitution: each half warp takes two columns of one
+            // block, lane r of the half keeps the partial sums sigma_r = sum_{s < r} A[r][s] t[s] of
+            // block row r, and at step s the owner of row s turns its final sigma_s into
+            // t[s] = (s == j) - sigma_s, broadcasts it, and every lane adds A[r][s] t[s] (rows r <= s
+            // add 0); at the end T[r][j] = (r == j) - sigma_r.  Then block rows I = 1, 2, 3 in order:
+            // X_IJ = sum_{K = J}^{I - 1} A_IK T_KJ and T_IJ = -T_II X_IJ for J < I.
             {
-                const int w = tid >> 5;
-                const int cols[4] = {w, 31 - w, 32 + w, 63 - w};
-                float part[4][2];
+                const int w = tid >> 5, hf = lane >> 4, rr = lane & 15;
+                const int I = w >> 2, ca = 4 * (w & 3) + 2 * hf;  // columns ca, ca + 1 of diagonal block I
+                const int row = 16 * I + rr;
+                float pa = 0.f, pb = 0.f;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) part[c][0] = part[c][1] = 0.f;
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-                    for (int sl = 0; sl < 32; ++sl) {
-                        const int s = 32 * hf + sl;
-                        const float a0 = sAf[lane * kLdT + s], a1 = sAf[(lane + 32) * kLdT + s];
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const float own = (s == cols[c] ? 1.f : 0.f) - part[c][hf];
-                            const float ts = __shfl_sync(kFull, own, sl);
-                            part[c][0] = fmaf(a0, ts, part[c][0]);
-                            part[c][1] = fmaf(a1, ts, part[c][1]);
-                        }
-                    }
+                for (int sl = 0; sl < 16; ++sl) {
+                    const float av = sAf[row * kLdT + 16 * I + sl];
+                    const float ta = __shfl_sync(kFull, (sl == ca ? 1.f : 0.f) - pa, sl + 16 * hf);
+                    const float tb = __shfl_sync(kFull, (sl == ca + 1 ? 1.f : 0.f) - pb, sl + 16 * hf);
+                    pa = fmaf(av, ta, pa);
+                    pb = fmaf(av, tb, pb);
                 }
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int m = 0; m < 2; ++m)
-                        sTf[(lane + 32 * m) * kLdT + cols[c]] = (lane + 32 * m == cols[c] ? 1.f : 0.f) - part[c][m];
+                sTf[row * kLdT + 16 * I + ca] = (rr == ca ? 1.f : 0.f) - pa;
+                sTf[row * kLdT + 16 * I + ca + 1] = (rr == ca + 1 ? 1.f : 0.f) - pb;
+                for (int e = tid; e < kC * kC; e += kNTtc) {  // the blocks above the diagonal are zero
+                    const int r = e >> 6, c2 = e & 63;
+                    if ((c2 >> 4) > (r >> 4)) sTf[r * kLdT + c2] = 0.f;
+                }
             }
             __syncthreads();
+            {
+                float* X = reinterpret_cast<float*>(sB2);  // scratch (X_IJ, 16 x 16 each), free until T is out
+#pragma unroll
+                for (int I = 1; I < 4; ++I) {
+                    for (int e = tid; e < I * 256; e += kNTtc) {
+                        const int J = e >> 8, r = (e >> 4) & 15, c2 = e & 15;
+                        const float* ar = sAf + (16 * I + r) * kLdT;
+                        float x = 0.f;
+                        for (int K = J; K < I; ++K)
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) x = fmaf(ar[16 * K + k], sTf[(16 * K + k) * kLdT + 16 * J + c2], x);
+                        X[e] = x;
+                    }
+                    __syncthreads();
+                    for (int e = tid; e < I * 256; e += kNTtc) {
+                        const int J = e >> 8, r = (e >> 4) & 15, c2 = e & 15;
+                        const float* tr = sTf + (16 * I + r) * kLdT + 16 * I;
+                        float t = 0.f;
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) t = fmaf(tr[k], X[(J << 8) + 16 * k + c2], t);
+                        sTf[(16 * I + r) * kLdT + 16 * J + c2] = -t;
+                    }
+                    __syncthreads();
+                }
+            }
 #pragma unroll
             for (int it = 0; it < RowsK::kItems; ++it) {
                 const int s = RowsK::row(it), k = RowsK::col(it);
