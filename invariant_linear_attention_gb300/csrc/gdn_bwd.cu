@@ -1328,8 +1328,7 @@ __global__ void __launch_bounds__(kNTtc, 1)
             // block, lane r of the half keeps the partial sums sigma_r = sum_{s < r} A[r][s] t[s] of
             // block row r, and at step s the owner of row s turns its final sigma_s into
             // t[s] = (s == j) - sigma_s, broadcasts it, and every lane adds A[r][s] t[s] (rows r <= s
-            // add 0); at the end T[r][j] = (r == j) - sigma_r.  Then block rows I = 1, 2, 3 in order:
-            // X_IJ = sum_{K = J}^{I - 1} A_IK T_KJ and T_IJ = -T_II X_IJ for J < I.
+            // add 0); at the end T[r][j] = (r == j) - sigma_r.  The blocks below follow from them.
             {
                 const int w = tid >> 5, hf = lane >> 4, rr = lane & 15;
                 const int I = w >> 2, ca = 4 * (w & 3) + 2 * hf;  // columns ca, ca + 1 of diagonal block I
@@ -1352,26 +1351,39 @@ __global__ void __launch_bounds__(kNTtc, 1)
             }
             __syncthreads();
             {
-                float* X = reinterpret_cast<float*>(sB2);  // scratch (X_IJ, 16 x 16 each), free until T is out
+                // M_IK = T_II A_IK for every K < I (six blocks, independent of each other), then block
+                // rows I = 1, 2, 3: T_IJ = -sum_{K = J}^{I - 1} M_IK T_KJ.  Two accumulators per sum.
+                float* M = reinterpret_cast<float*>(sB2);  // scratch, free until T is out: block (I, K) at
+                                                           // 256 (I (I - 1) / 2 + K)
+                for (int e = tid; e < 6 * 256; e += kNTtc) {
+                    const int pb = e >> 8, r = (e >> 4) & 15, c2 = e & 15;
+                    const int I = pb < 1 ? 1 : (pb < 3 ? 2 : 3), K = pb - I * (I - 1) / 2;
+                    const float* tr = sTf + (16 * I + r) * kLdT + 16 * I;
+                    const float* ac = sAf + 16 * I * kLdT + 16 * K + c2;
+                    float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+                    for (int k = 0; k < 16; k += 2) {
+                        x0 = fmaf(tr[k], ac[k * kLdT], x0);
+                        x1 = fmaf(tr[k + 1], ac[(k + 1) * kLdT], x1);
+                    }
+                    M[e] = x0 + x1;
+                }
+                __syncthreads();
 #pragma unroll
                 for (int I = 1; I < 4; ++I) {
                     for (int e = tid; e < I * 256; e += kNTtc) {
                         const int J = e >> 8, r = (e >> 4) & 15, c2 = e & 15;
-                        const float* ar = sAf + (16 * I + r) * kLdT;
-                        float x = 0.f;
-                        for (int K = J; K < I; ++K)
+                        float x0 = 0.f, x1 = 0.f;
+                        for (int K = J; K < I; ++K) {
+                            const float* mr = M + 256 * (I * (I - 1) / 2 + K) + 16 * r;
+                            const float* tc = sTf + 16 * K * kLdT + 16 * J + c2;
 #pragma unroll
-                            for (int k = 0; k < 16; ++k) x = fmaf(ar[16 * K + k], sTf[(16 * K + k) * kLdT + 16 * J + c2], x);
-                        X[e] = x;
-                    }
-                    __syncthreads();
-                    for (int e = tid; e < I * 256; e += kNTtc) {
-                        const int J = e >> 8, r = (e >> 4) & 15, c2 = e & 15;
-                        const float* tr = sTf + (16 * I + r) * kLdT + 16 * I;
-                        float t = 0.f;
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) t = fmaf(tr[k], X[(J << 8) + 16 * k + c2], t);
-                        sTf[(16 * I + r) * kLdT + 16 * J + c2] = -t;
+                            for (int k = 0; k < 16; k += 2) {
+                                x0 = fmaf(mr[k], tc[k * kLdT], x0);
+                                x1 = fmaf(mr[k + 1], tc[(k + 1) * kLdT], x1);
+                            }
+                        }
+                        sTf[(16 * I + r) * kLdT + 16 * J + c2] = -(x0 + x1);
                     }
                     __syncthreads();
                 }
