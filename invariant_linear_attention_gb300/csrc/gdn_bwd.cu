@@ -1175,7 +1175,7 @@ __device__ __forceinline__ float half_sum(float x) {
 // per (chunk, head), dk = dv = 128, bf16 inputs: bwd_wy_kernel on tcgen05.
 //   [K; Q] K^T (M = 128: rows 0..63 give K K^T, rows 64..127 give Q K^T; the B operand is the
 //   first 64 rows of the same shared-memory copy), A and P from them, T = (I + A)^-1 by
-//   column-parallel forward substitution, then W^T = K^T (T diag(beta Gam))^T
+//   16 x 16 blocks (below), then W^T = K^T (T diag(beta Gam))^T
 //   and U~^T = V^T (T diag(beta))^T with the dk / dv index as the M = 128 rows, so each epilogue
 //   thread stores one column of W and U~: coalesced.
 constexpr int kLdT = kC + 1;  // fp32 A and T in shared memory: row-per-lane writes hit distinct banks
