@@ -87,6 +87,17 @@ def test_no_l2norm_bf16_head128():
     check(got, ref, x.cu_seqlens)
 
 
+@pytest.mark.parametrize("lengths", [[9, 20], [1], [63]])
+def test_short_batch_head128(lengths):
+    """A packed batch shorter than one chunk through the tcgen05 kernels (bf16, dk = dv = 128):
+    the tensor copies' 64-row boxes reach past T_total (read as zeros) and past each sequence."""
+    x = inputs.make_inputs(lengths, HK=2, HV=4, dk=128, dv=128, dtype=torch.bfloat16, seed=31, init_scale=0.2)
+    dO = inputs.grad_out(sum(lengths), 4, 128, seed=32)
+    dsT = inputs.random_states(len(lengths), 4, 128, 128, seed=33, scale=0.5)
+    got, ref = run(x, dO, dsT)
+    check(got, ref, x.cu_seqlens)
+
+
 def test_backward_workload_sampled():
     """gdn_chunk_bwd on 8 x 4096 tokens, HK=16, HV=32, dk=dv=128, bf16, as the
     benchmark launches it; the oracle recomputes sampled (sequence, k-head)
