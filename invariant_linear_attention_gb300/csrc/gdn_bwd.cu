@@ -551,38 +551,12 @@ constexpr uint32_t kSboC = kC * 32;  // 8 rows x 64 values x 4 bytes
 // Staging of one operand: every thread first loads its items (all loads in flight together),
 // then writes them, rounded to TF32, into the operand's K-major core-matrix layout.
 
-// dst(n, k) = src[n * KK + k] for n < NN, k < KK.  A warp covers 8 rows x 16 values: 64
-// contiguous bytes of each of 8 source rows, one 128-byte core-matrix block per quarter of the
-// warp's 16-byte stores.
+// The thread-to-element map of an NN x KK row-major operand (rows n, four consecutive k per item):
+// a warp covers 8 rows x 16 values, 64 contiguous bytes of each of 8 source rows and one 128-byte
+// core-matrix block per quarter of the warp's 16-byte stores.
 template <int NN, int KK>
 struct RowsTc {
     static constexpr int kItems = NN * KK / 4 / kNTtc;
-    float4 v[kItems];
-    __device__ __forceinline__ void load(const float* __restrict__ src) {
-#pragma unroll
-        for (int it = 0; it < kItems; ++it) {
-            const int n = row(it), k = col(it);
-            v[it] = *reinterpret_cast<const float4*>(src + (size_t)n * KK + k);
-        }
-    }
-    __device__ __forceinline__ void put(uint8_t* dst) const {
-#pragma unroll
-        for (int it = 0; it < kItems; ++it)
-            *reinterpret_cast<float4*>(dst + umma_koff(row(it), col(it), KK * 32)) = tf32_round4(v[it]);
-    }
-    // The same copy by 16-byte cp.async (no registers); round_in_place once this thread's copies landed.
-    __device__ __forceinline__ static void issue_async(uint8_t* dst, const float* __restrict__ src) {
-#pragma unroll
-        for (int it = 0; it < kItems; ++it)
-            cp_async16(dst + umma_koff(row(it), col(it), KK * 32), src + (size_t)row(it) * KK + col(it));
-    }
-    __device__ __forceinline__ static void round_in_place(uint8_t* dst) {
-#pragma unroll
-        for (int it = 0; it < kItems; ++it) {
-            float4* q = reinterpret_cast<float4*>(dst + umma_koff(row(it), col(it), KK * 32));
-            *q = tf32_round4(*q);
-        }
-    }
     __device__ __forceinline__ static int row(int it) {
         const int e = threadIdx.x + it * kNTtc, lane = e & 31, blk = e >> 5;
         return (blk / (KK / 16)) * 8 + (lane & 7);
@@ -1594,18 +1568,6 @@ __global__ void __launch_bounds__(kNT) bwd_intra_c_kernel(BwdParams p) {
     }
 }
 
-// dst(n, k) = get4(n, k) (four consecutive k) for n < NN, k < KK, rounded to TF32, in the RowsTc
-// thread mapping; all loads are issued before any store.
-template <int NN, int KK, typename G>
-__device__ __forceinline__ void stage_rows_fn(uint8_t* dst, G get4) {
-    using R = RowsTc<NN, KK>;
-    float4 v[R::kItems];
-#pragma unroll
-    for (int it = 0; it < R::kItems; ++it) v[it] = get4(R::row(it), R::col(it));
-#pragma unroll
-    for (int it = 0; it < R::kItems; ++it)
-        *reinterpret_cast<float4*>(dst + umma_koff(R::row(it), R::col(it), KK * 32)) = tf32_round4(v[it]);
-}
 // dst(n, k) = get(k, n) for n < NN, k < KK (a transpose), rounded to TF32; consecutive threads
 // take consecutive n.
 template <int NN, int KK, typename G>
@@ -1621,22 +1583,6 @@ __device__ __forceinline__ void stage_cols_fn(uint8_t* dst, G get) {
     for (int it = 0; it < kItems; ++it) {
         const int e = threadIdx.x + it * kNTtc, n = e % NN, k = (e / NN) * 4;
         *reinterpret_cast<float4*>(dst + umma_koff(n, k, KK * 32)) = tf32_round4(v[it]);
-    }
-}
-
-// The RowsTc layout filled by 16-byte cp.async (no registers): ptr(n, k) gives the source of
-// four consecutive k, or nullptr for zeros; the caller rounds with RowsTc::round_in_place once its
-// own copies have landed.
-template <int NN, int KK, typename P>
-__device__ __forceinline__ void async_rows(uint8_t* dst, P ptr) {
-    using R = RowsTc<NN, KK>;
-#pragma unroll
-    for (int it = 0; it < R::kItems; ++it) {
-        const int n = R::row(it), k = R::col(it);
-        const float* src = ptr(n, k);
-        uint8_t* d = dst + umma_koff(n, k, KK * 32);
-        if (src) cp_async16(d, src);
-        else *reinterpret_cast<float4*>(d) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 }
 
