@@ -46,6 +46,12 @@
 namespace gdn {
 
 constexpr int kC = 64;        // chunk length
+#ifndef STAGGER_WY_CYCLES
+#define STAGGER_WY_CYCLES 54000
+#endif
+#ifndef STAGGER_INTRA_CYCLES
+#define STAGGER_INTRA_CYCLES 160000
+#endif
 constexpr int kMaxD = 128;    // max dk, dv
 // smem leading dims = 4 (mod 32): row-major tensor-core fragment loads hit 32 distinct banks
 constexpr int kLdD = kMaxD + 4;  // C x d and d x d matrices
@@ -102,7 +108,22 @@ struct BwdParams {
     float* dqh;        // [T, HV, dk]
     float* dkh;        // [T, HV, dk]
     int N, T, HK, HV, G, dk, dv, use_norm, nchm, dtype;
+    int nsm;                 // SMs of the device
+    long long stagger_wy;    // first-wave start spread of bwd_wy_tc_kernel, SM cycles (0: none)
+    long long stagger_intra; // the same for bwd_intra_tc_kernel
 };
+
+// Spread the start of a chunk kernel's first wave (its first nsm CTAs in launch order) evenly over
+// `cycles` SM cycles.  Every CTA of these kernels takes about the same time, so without a spread
+// the waves stay aligned and all SMs fetch their first operands in the same burst; spread over
+// about two CTA lifetimes, the bursts of different SMs stop coinciding.  The wait is a bounded
+// sleep loop; it changes no result.
+__device__ __forceinline__ void stagger_first_wave(long long cycles, int nsm) {
+    const long long lin = (long long)blockIdx.x + (long long)blockIdx.y * gridDim.x;
+    if (cycles <= 0 || lin >= nsm) return;
+    const long long t0 = clock64(), delay = lin * cycles / nsm;
+    while (clock64() - t0 < delay) __nanosleep(100);
+}
 
 __device__ __forceinline__ size_t ch_index(const BwdParams& p, int c, int h) { return (size_t)c * p.HV + h; }
 
@@ -1182,6 +1203,7 @@ __global__ void __launch_bounds__(kNTtc, 1)
         if (tid == 0) atomicOr(p.err, GDN_DEVERR_SMEM_ALIGN);
         return;
     }
+    stagger_first_wave(p.stagger_wy, p.nsm);
     // K^ (rows 0..63) and Q^ (rows 64..127) by tensor copies, four swizzled boxes of 32 values each,
     // in flight while warp 0 takes the cumsum
     if (tid == 0) {
@@ -1654,6 +1676,7 @@ __global__ void __launch_bounds__(kNTtc, 1)
         if (tid == 0) atomicOr(p.err, GDN_DEVERR_SMEM_ALIGN);
         return;
     }
+    stagger_first_wave(p.stagger_intra, p.nsm);
     // phase A: K^ -> R1, U -> R3, dU -> R5 (rows = chunk positions), S0^T in two K-halves -> R4 and
     // C1|C2 (rows j, k = i), all by tensor copies (four boxes of 32 values per operand), and dO (bf16,
     // two boxes of 64 values) -> R2 + 16 KB, converted into R2 once it lands
@@ -2318,6 +2341,18 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
     p.use_norm = s->use_qk_l2norm ? 1 : 0;
     p.nchm = L.nchm;
     p.dtype = s->dtype;
+    {
+        int dev = 0, nsm = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0)
+            return GDN_ERR_CUDA;
+        p.nsm = nsm;
+        // the chunk kernels' CTAs live about 27K (wy) and 80K (intra) SM cycles at dk = dv = 128; the
+        // first-wave spread (two lifetimes) pays off only when the grid runs many waves
+        const bool many = (long long)L.nchm * s->HV >= 8LL * nsm;
+        p.stagger_wy = many ? STAGGER_WY_CYCLES : 0;
+        p.stagger_intra = many ? STAGGER_INTRA_CYCLES : 0;
+    }
 
     if (cudaMemsetAsync(ws, 0, sizeof(unsigned), cs) != cudaSuccess) return GDN_ERR_CUDA;
     bwd_offsets_kernel<<<1, 32, 0, cs>>>(p);
