@@ -798,7 +798,8 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p)
 #pragma unroll
             for (int m = 0; m < 16; ++m) {
                 x[m] = sUtil[(cg * 16 + m) * kDv + i] - x[m];
-                ug[(size_t)(cg * 16 + m) * kDv] = x[m];
+                // at dk = 128 U only ever enters the tensor cores: stored already rounded to TF32
+                ug[(size_t)(cg * 16 + m) * kDv] = DK == 128 ? tf32_round(x[m]) : x[m];
             }
             put_slice_tc<16>(sUt, i, cg * 16, kSboC, x, 1.f);
         }
@@ -982,7 +983,8 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p)
             tmem_ld<2>(tmem + lane_base + cg * 16, x);
             float* dug = p.dUb + ci * kC * kDv + i;
 #pragma unroll
-            for (int m = 0; m < 16; ++m) dug[(size_t)(cg * 16 + m) * kDv] = x[m];
+            for (int m = 0; m < 16; ++m)  // at dk = 128 only ever a TF32 operand: stored rounded
+                dug[(size_t)(cg * 16 + m) * kDv] = DK == 128 ? tf32_round(x[m]) : x[m];
             put_slice_tc<16>(sdUt, i, cg * 16, kSboC, x, -1.f);
         }
         tc_sync();
@@ -1738,16 +1740,13 @@ __global__ void __launch_bounds__(kNTtc, 1)
             for (int u = 0; u < RO::kItems; ++u)
                 *reinterpret_cast<float4*>(R2 + umma_koff(RO::row(u), RO::col(u), kSboD)) = tf32_round4(ov[u]);
         }
-        // TF32 rounding of the copied operands (five 32 KB buffers, any layout), and zero rows of K^
-        // past the chunk (the copy fills them from the next sequence)
-        uint8_t* const bufs[3] = {R1, R3, R5};
+        // TF32 rounding of the copied K^ and S0^T (U and dU arrive rounded by the state passes), and
+        // zero rows of K^ past the chunk (the copy fills them from the next sequence)
 #pragma unroll
-        for (int b = 0; b < 3; ++b)
-#pragma unroll
-            for (int it = 0; it < 32768 / 16 / kNTtc; ++it) {
-                float4* v = reinterpret_cast<float4*>(bufs[b]) + tid + it * kNTtc;
-                *v = tf32_round4(*v);
-            }
+        for (int it = 0; it < 32768 / 16 / kNTtc; ++it) {
+            float4* v = reinterpret_cast<float4*>(R1) + tid + it * kNTtc;
+            *v = tf32_round4(*v);
+        }
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
