@@ -46,9 +46,6 @@
 namespace gdn {
 
 constexpr int kC = 64;        // chunk length
-#ifndef STAGGER_WY_CYCLES
-#define STAGGER_WY_CYCLES 54000
-#endif
 #ifndef STAGGER_INTRA_CYCLES
 #define STAGGER_INTRA_CYCLES 160000
 #endif
@@ -109,8 +106,7 @@ struct BwdParams {
     float* dkh;        // [T, HV, dk]
     int N, T, HK, HV, G, dk, dv, use_norm, nchm, dtype;
     int nsm;                 // SMs of the device
-    long long stagger_wy;    // first-wave start spread of bwd_wy_tc_kernel, SM cycles (0: none)
-    long long stagger_intra; // the same for bwd_intra_tc_kernel
+    long long stagger_intra; // first-wave start spread of bwd_intra_tc_kernel, SM cycles (0: none)
 };
 
 // Spread the start of a chunk kernel's first wave (its first nsm CTAs in launch order) evenly over
@@ -1175,10 +1171,15 @@ __device__ __forceinline__ float half_sum(float x) {
 //   16 x 16 blocks (below), then W^T = K^T (T diag(beta Gam))^T
 //   and U~^T = V^T (T diag(beta))^T with the dk / dv index as the M = 128 rows, so each epilogue
 //   thread stores one column of W and U~: coalesced.
+//   Two CTAs share an SM (64 registers a thread, 97 KB of shared memory and 256 TMEM columns
+//   each), so that one CTA's copies, solve and epilogues overlap the other's.
 constexpr int kLdT = kC + 1;  // fp32 A and T in shared memory: row-per-lane writes hit distinct banks
-constexpr size_t kWyTcSmem = (size_t)65536 + 2 * 4 * kC * kLdT + 2 * 4 * kC * kC + 4 * 3 * kC + 32;
+constexpr int kWyCtasPerSm = 2;
+constexpr size_t kWyTcSmem = (size_t)65536 + 2 * 4 * kC * kLdT + 4 * 3 * kC + 32;
+// 228 KB of shared memory per SM, 1 KB of it reserved per CTA
+static_assert(kWyCtasPerSm * (kWyTcSmem + 1024) <= 228 * 1024, "two wy CTAs must fit on one SM");
 
-__global__ void __launch_bounds__(kNTtc, 1)
+__global__ void __launch_bounds__(kNTtc, kWyCtasPerSm)
     bwd_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q, BwdParams p) {
     constexpr int kD = 128;
     extern __shared__ __align__(1024) uint8_t smb_sw[];  // swizzled operands: 1 KB aligned
@@ -1186,9 +1187,9 @@ __global__ void __launch_bounds__(kNTtc, 1)
     uint8_t* sX = smb;  // A: [K; Q] 128 x 128 (swizzled, by tensor copies), then K^T | V^T (128 x 64 each)
     float* sAf = reinterpret_cast<float*>(sX + 65536);          // A (fp32, 64 x kLdT)
     float* sTf = sAf + kC * kLdT;                               // T (fp32, 64 x kLdT)
-    uint8_t* sB2 = reinterpret_cast<uint8_t*>(sTf + kC * kLdT); // B: T diag(beta Gam)  64 x 64
-    uint8_t* sB3 = sB2 + 4 * kC * kC;                           // B: T diag(beta)      64 x 64
-    float* sg = reinterpret_cast<float*>(sB3 + 4 * kC * kC);    // gam
+    uint8_t* sB2 = reinterpret_cast<uint8_t*>(sAf);             // B: T diag(beta Gam) 64 x 64, over A
+    uint8_t* sB3 = reinterpret_cast<uint8_t*>(sTf);             // B: T diag(beta)     64 x 64, over T
+    float* sg = sTf + kC * kLdT;                                // gam
     float* sGb = sg + kC;                                       // beta Gam
     float* sb = sGb + kC;                                       // beta
     uint64_t* bar = reinterpret_cast<uint64_t*>(sb + kC);
@@ -1205,7 +1206,6 @@ __global__ void __launch_bounds__(kNTtc, 1)
         if (tid == 0) atomicOr(p.err, GDN_DEVERR_SMEM_ALIGN);
         return;
     }
-    stagger_first_wave(p.stagger_wy, p.nsm);
     // K^ (rows 0..63) and Q^ (rows 64..127) by tensor copies, four swizzled boxes of 32 values each,
     // in flight while warp 0 takes the cumsum
     if (tid == 0) {
@@ -1351,8 +1351,8 @@ __global__ void __launch_bounds__(kNTtc, 1)
             {
                 // M_IK = T_II A_IK for every K < I (six blocks, independent of each other), then block
                 // rows I = 1, 2, 3: T_IJ = -sum_{K = J}^{I - 1} M_IK T_KJ.  Two accumulators per sum.
-                float* M = reinterpret_cast<float*>(sB2);  // scratch, free until T is out: block (I, K) at
-                                                           // 256 (I (I - 1) / 2 + K)
+                float* M = reinterpret_cast<float*>(sX);  // scratch in the copy of K^ and Q^ (read into kr
+                                                          // above): block (I, K) at 256 (I (I - 1) / 2 + K)
                 for (int e = tid; e < 6 * 256; e += kNTtc) {
                     const int pb = e >> 8, r = (e >> 4) & 15, c2 = e & 15;
                     const int I = pb < 1 ? 1 : (pb < 3 ? 2 : 3), K = pb - I * (I - 1) / 2;
@@ -1401,17 +1401,26 @@ __global__ void __launch_bounds__(kNTtc, 1)
         }
         __syncthreads();
         {
-            // T out; B operands T diag(beta Gam) and T diag(beta) (rows r, k = s)
+            // T out; B operands T diag(beta Gam) (over A, unused since the blocks M were formed) and
+            // T diag(beta) (over T itself, once every thread holds its values of T), rows r, k = s
+            constexpr int kIt = kC * kC / 4 / kNTtc;
+            float4 tv[kIt];
             float* Tg = p.Tb + ci * kC * kC;
-            for (int e = tid; e < kC * kC / 4; e += kNTtc) {
-                const int r = e / (kC / 4), s = (e % (kC / 4)) * 4;
+#pragma unroll
+            for (int it = 0; it < kIt; ++it) {
+                const int e = tid + it * kNTtc, r = e / (kC / 4), s = (e % (kC / 4)) * 4;
                 const float* tr = sTf + r * kLdT + s;
-                const float4 tv = make_float4(tr[0], tr[1], tr[2], tr[3]);
-                *reinterpret_cast<float4*>(Tg + r * kC + s) = tv;
-                *reinterpret_cast<float4*>(sB2 + umma_koff(r, s, kSboC)) = tf32_round4(
-                    make_float4(tv.x * sGb[s], tv.y * sGb[s + 1], tv.z * sGb[s + 2], tv.w * sGb[s + 3]));
+                tv[it] = make_float4(tr[0], tr[1], tr[2], tr[3]);
+                *reinterpret_cast<float4*>(Tg + r * kC + s) = tv[it];
+                *reinterpret_cast<float4*>(sB2 + umma_koff(r, s, kSboC)) = tf32_round4(make_float4(
+                    tv[it].x * sGb[s], tv[it].y * sGb[s + 1], tv[it].z * sGb[s + 2], tv[it].w * sGb[s + 3]));
+            }
+            __syncthreads();  // T is read in full before T diag(beta) overwrites it
+#pragma unroll
+            for (int it = 0; it < kIt; ++it) {
+                const int e = tid + it * kNTtc, r = e / (kC / 4), s = (e % (kC / 4)) * 4;
                 *reinterpret_cast<float4*>(sB3 + umma_koff(r, s, kSboC)) = tf32_round4(
-                    make_float4(tv.x * sb[s], tv.y * sb[s + 1], tv.z * sb[s + 2], tv.w * sb[s + 3]));
+                    make_float4(tv[it].x * sb[s], tv[it].y * sb[s + 1], tv[it].z * sb[s + 2], tv[it].w * sb[s + 3]));
             }
         }
         tc_sync();
@@ -1426,8 +1435,7 @@ __global__ void __launch_bounds__(kNTtc, 1)
             // W[r][j] = (W^T)[j][r] and U~[r][i] = (U~^T)[i][r] for r = 16 cg + t
             const int jj = q * 32 + lane;
             float w[16], u[16];
-            tmem_ld<2>(tmem + lane_base + 64 + cg * 16, w);
-            tmem_ld<2>(tmem + lane_base + 128 + cg * 16, u);
+            tmem_ld_pair(tmem + lane_base + 64 + cg * 16, w, tmem + lane_base + 128 + cg * 16, u);
             float* W = p.Wb + ci * kC * kD + jj;
             float* Ut = p.Utb + ci * kC * kD + jj;
 #pragma unroll
@@ -1962,8 +1970,7 @@ __global__ void __launch_bounds__(kNTtc, 1)
         // phase C: column dots with T, dT (-> R4, rows s, k = r); dq update
         {
             float f1[16], f2[16];
-            tmem_ld<2>(tmem + lane_base + 320 + cg * 16, f1);
-            tmem_ld<2>(tmem + lane_base + 384 + cg * 16, f2);
+            tmem_ld_pair(tmem + lane_base + 320 + cg * 16, f1, tmem + lane_base + 384 + cg * 16, f2);
             float v1[16], v2[16];
             if (row_lane) {
                 const int s = r64;
@@ -2073,8 +2080,7 @@ __global__ void __launch_bounds__(kNTtc, 1)
         float* sdKK = reinterpret_cast<float*>(R2);  // 64 x kLdT
         {
             float a[16], kk[16];
-            tmem_ld<2>(tmem + lane_base + 448 + cg * 16, a);
-            tmem_ld<2>(tmem + lane_base + 64 + cg * 16, kk);
+            tmem_ld_pair(tmem + lane_base + 448 + cg * 16, a, tmem + lane_base + 64 + cg * 16, kk);
             float acc = 0.f;
             if (row_lane) {
                 const int r = r64;
@@ -2346,10 +2352,9 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
             cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0)
             return GDN_ERR_CUDA;
         p.nsm = nsm;
-        // the chunk kernels' CTAs live about 27K (wy) and 80K (intra) SM cycles at dk = dv = 128; the
-        // first-wave spread (two lifetimes) pays off only when the grid runs many waves
+        // the intra kernel's CTAs live about 80K SM cycles at dk = dv = 128; the first-wave spread
+        // (two lifetimes) pays off only when the grid runs many waves
         const bool many = (long long)L.nchm * s->HV >= 8LL * nsm;
-        p.stagger_wy = many ? STAGGER_WY_CYCLES : 0;
         p.stagger_intra = many ? STAGGER_INTRA_CYCLES : 0;
     }
 

@@ -56,9 +56,9 @@ __device__ __forceinline__ float4 tf32_round4(float4 v) {
 }
 
 // TMEM allocation by one whole warp; the address lands in *slot (shared memory).  An allocation
-// waits while the SM's 512 columns are taken.  The kernels here allocate 256 columns each and run
-// 512 threads at 72 to 128 registers (over 36K registers per CTA), so no two of their CTAs share
-// an SM and the allocation never waits.
+// waits while the SM's 512 columns are taken.  The kernels here hold 512 columns with one CTA per
+// SM (512 threads at up to 128 registers fill the register file) or 256 columns with at most two
+// CTAs per SM (512 threads at 64 registers), so the allocation never waits.
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)), "r"(ncols)
                  : "memory");
@@ -142,37 +142,89 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
                  : "memory");
 }
 
-// Columns [col, col + 8 * NX) of this warp's 32 lanes, one lane per thread, into v.  Each load
-// and its wait form one asm statement, so no use of the registers can move ahead of the wait.
+// Columns [col, col + 8 * NX) of this warp's 32 lanes, one lane per thread, into v: one load of shape
+// 32x32b.x8, .x16 or .x32 (NX = 1, 2 or 4) and its wait in one asm statement, so no use of the
+// registers can move ahead of the wait.
 template <int NX>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[8 * NX]) {
+    static_assert(NX == 1 || NX == 2 || NX == 4, "8, 16 or 32 columns");
+    uint32_t r[8 * NX];
+    if constexpr (NX == 1) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t"
+                     "tcgen05.wait::ld.sync.aligned;"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                     : "r"(taddr)
+                     : "memory");
+    } else if constexpr (NX == 2) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                     "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+                     "tcgen05.wait::ld.sync.aligned;"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                       "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+                       "=r"(r[14]), "=r"(r[15])
+                     : "r"(taddr)
+                     : "memory");
+    } else {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+                     "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+                     "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+                     "tcgen05.wait::ld.sync.aligned;"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                       "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+                       "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+                       "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+                       "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                     : "r"(taddr)
+                     : "memory");
+    }
 #pragma unroll
-    for (int x = 0; x < NX; ++x) {
-        uint32_t r[8];
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t"
-            "tcgen05.wait::ld.sync.aligned;"
-            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-            : "r"(taddr + 8u * x)
-            : "memory");
+    for (int j = 0; j < 8 * NX; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// Two loads of 16 columns (at ta into va, at tb into vb) and one wait for both.
+__device__ __forceinline__ void tmem_ld_pair(uint32_t ta, float (&va)[16], uint32_t tb, float (&vb)[16]) {
+    uint32_t r[32];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                 "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%32];\n\t"
+                 "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                 "{%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%33];\n\t"
+                 "tcgen05.wait::ld.sync.aligned;"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+                   "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+                   "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+                   "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                 : "r"(ta), "r"(tb)
+                 : "memory");
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[8 * x + j] = __uint_as_float(r[j]);
+    for (int j = 0; j < 16; ++j) {
+        va[j] = __uint_as_float(r[j]);
+        vb[j] = __uint_as_float(r[16 + j]);
     }
 }
 
-// The reverse of tmem_ld: v into columns [col, col + 8 * NX) of this warp's 32 lanes, then a wait
-// for the stores, so that a barrier after it orders them before the next MMA on those columns.
+// The reverse of tmem_ld (NX = 1 or 2): v into columns [col, col + 8 * NX) of this warp's 32 lanes,
+// then a wait for the stores, so that a barrier after it orders them before the next MMA on those
+// columns.
 template <int NX>
 __device__ __forceinline__ void tmem_st(uint32_t taddr, const float (&v)[8 * NX]) {
+    static_assert(NX == 1 || NX == 2, "8 or 16 columns");
+    uint32_t r[8 * NX];
 #pragma unroll
-    for (int x = 0; x < NX; ++x)
-        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr + 8u * x),
-                     "r"(__float_as_uint(v[8 * x])), "r"(__float_as_uint(v[8 * x + 1])), "r"(__float_as_uint(v[8 * x + 2])),
-                     "r"(__float_as_uint(v[8 * x + 3])), "r"(__float_as_uint(v[8 * x + 4])),
-                     "r"(__float_as_uint(v[8 * x + 5])), "r"(__float_as_uint(v[8 * x + 6])),
-                     "r"(__float_as_uint(v[8 * x + 7]))
+    for (int j = 0; j < 8 * NX; ++j) r[j] = __float_as_uint(v[j]);
+    if constexpr (NX == 1) {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n\t"
+                     "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+                     "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
                      : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    } else {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                     "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};\n\t"
+                     "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+                     "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+                     "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+                     : "memory");
+    }
 }
 
 }  // namespace gdn
