@@ -103,6 +103,7 @@ struct BwdParams {
     float* dUb;        // per chunk-head C x dv
     float* dgamA;      // per chunk-head C
     float* dqh;        // [T, HV, dk]
+    unsigned* fcnt;    // [nchm, HK] arrivals of the value-head CTAs of bwd_intra_tc_kernel (zeroed per call)
     float* dkh;        // [T, HV, dk]
     int N, T, HK, HV, G, dk, dv, use_norm, nchm, dtype;
     int nsm;                 // SMs of the device
@@ -1618,6 +1619,56 @@ __device__ __forceinline__ void stage_cols_fn(uint8_t* dst, G get) {
     }
 }
 
+// One warp per (token, k-head) w: sum the G value heads' dq^ and dk^ rows in increasing head order,
+// then the L2-norm backward, into dq and dk.  The partial rows are read at L2 (__ldcg): in
+// bwd_intra_tc_kernel they were written by other CTAs of the same launch.
+__device__ __forceinline__ void fold_token(const BwdParams& p, long long w, int lane) {
+    const int t = (int)(w / p.HK), hk = (int)(w - (long long)t * p.HK);
+    // every load of a head step (dq and dk together) is issued before any is used; each element
+    // still sums the heads in increasing order
+    float dsum[2][4], x[2][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int j = lane + 32 * i;
+        x[0][i] = j < p.dk ? p.qn[(size_t)w * p.dk + j] : 0.f;
+        x[1][i] = j < p.dk ? p.kn[(size_t)w * p.dk + j] : 0.f;
+        dsum[0][i] = dsum[1][i] = 0.f;
+    }
+    for (int hh = hk * p.G; hh < (hk + 1) * p.G; ++hh) {
+        const size_t base = ((size_t)t * p.HV + hh) * p.dk;
+        float a[4], b[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int j = lane + 32 * i;
+            a[i] = j < p.dk ? __ldcg(p.dqh + base + j) : 0.f;
+            b[i] = j < p.dk ? __ldcg(p.dkh + base + j) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            dsum[0][i] += a[i];
+            dsum[1][i] += b[i];
+        }
+    }
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+        float dot = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dot = fmaf(x[which][i], dsum[which][i], dot);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) dot += __shfl_xor_sync(kFull, dot, off);
+        const float inv = (which ? p.kinv : p.qinv)[w];
+        void* dst = which ? p.dk_out : p.dq_out;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int j = lane + 32 * i;
+            if (j < p.dk) {
+                const float gval = p.use_norm ? (dsum[which][i] - x[which][i] * dot) * inv : dsum[which][i];
+                st_any(dst, (size_t)w * p.dk + j, p.dtype, gval);
+            }
+        }
+    }
+}
+
 // per (chunk, head), dk = dv = 128, bf16 inputs: bwd_intra_s_kernel and bwd_intra_c_kernel in one
 // kernel on tcgen05.  The products with the chunk states come first, in transposed form (rows = the
 // dk index j):
@@ -1667,7 +1718,9 @@ __global__ void __launch_bounds__(kNTtc, 1)
     uint64_t* bar = reinterpret_cast<uint64_t*>(rowp + 4 * kC);
     uint64_t* bar_ld = bar + 1;  // the tensor copies of phase A
     uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 2);
-    const int c = blockIdx.x, h = blockIdx.y;
+    uint32_t* s_last = slot + 1;  // this CTA folds the chunk's dq^, dk^ rows of its k-head
+    // one CTA per (chunk, value head), the heads of a chunk adjacent in launch order
+    const int h = (int)(blockIdx.x % (unsigned)p.HV), c = (int)(blockIdx.x / (unsigned)p.HV);
     int n, t0, len;
     if (!chunk_of(p, c, n, t0, len)) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, q = warp & 3, cg = warp >> 2;
@@ -2169,62 +2222,30 @@ __global__ void __launch_bounds__(kNTtc, 1)
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 512);
+    // The last of the G value-head CTAs of this (chunk, k-head) to arrive folds their dq^, dk^ rows
+    // (fold_token: the heads in increasing order, whichever CTA folds).  No CTA waits for another.
+    __threadfence();  // this CTA's rows are visible on the device before it is counted
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned prior = atomicAdd(p.fcnt + (size_t)c * p.HK + hk, 1u);
+        __threadfence();  // and the other CTAs' rows before this one reads them
+        *s_last = prior == (unsigned)(p.G - 1) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (*s_last && ok)
+        for (int r = warp; r < len; r += kNTtc / 32) fold_token(p, (long long)(t0 + r) * p.HK + hk, lane);
 }
 
-// per (token, k-head): sum the G value heads in increasing order, then the L2-norm backward
+// per (token, k-head), for the kernels that leave the fold to a pass of its own
 __global__ void bwd_fold_kernel(BwdParams p) {
     const long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
     if (w >= (long long)p.T * p.HK) return;
-    const int t = (int)(w / p.HK), hk = (int)(w - (long long)t * p.HK);
-    // every load of a head step (dq and dk together) is issued before any is used; each element
-    // still sums the heads in increasing order
-    float dsum[2][4], x[2][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int j = lane + 32 * i;
-        x[0][i] = j < p.dk ? p.qn[(size_t)w * p.dk + j] : 0.f;
-        x[1][i] = j < p.dk ? p.kn[(size_t)w * p.dk + j] : 0.f;
-        dsum[0][i] = dsum[1][i] = 0.f;
-    }
-    for (int hh = hk * p.G; hh < (hk + 1) * p.G; ++hh) {
-        const size_t base = ((size_t)t * p.HV + hh) * p.dk;
-        float a[4], b[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int j = lane + 32 * i;
-            a[i] = j < p.dk ? p.dqh[base + j] : 0.f;
-            b[i] = j < p.dk ? p.dkh[base + j] : 0.f;
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            dsum[0][i] += a[i];
-            dsum[1][i] += b[i];
-        }
-    }
-#pragma unroll
-    for (int which = 0; which < 2; ++which) {
-        float dot = 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) dot = fmaf(x[which][i], dsum[which][i], dot);
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) dot += __shfl_xor_sync(kFull, dot, off);
-        const float inv = (which ? p.kinv : p.qinv)[w];
-        void* dst = which ? p.dk_out : p.dq_out;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int j = lane + 32 * i;
-            if (j < p.dk) {
-                const float gval = p.use_norm ? (dsum[which][i] - x[which][i] * dot) * inv : dsum[which][i];
-                st_any(dst, (size_t)w * p.dk + j, p.dtype, gval);
-            }
-        }
-    }
+    fold_token(p, w, threadIdx.x & 31);
 }
 
 // ---------------------------------------------------------------------------
 struct BwdLayout {
-    size_t coff, qn, kn, qinv, kinv, gam, W, Ut, T, QK, P, BK, GQ, S, D, U, dU, dgA, dqh, dkh, total;
+    size_t coff, qn, kn, qinv, kinv, gam, W, Ut, T, QK, P, BK, GQ, S, D, U, dU, dgA, dqh, dkh, fcnt, total;
     int nchm;
 };
 
@@ -2260,6 +2281,7 @@ static BwdLayout bwd_layout(const gdn_shape* s) {
     L.dgA = take(tc128 ? 0 : CH * kC * 4);
     L.dqh = take(T * HV * dk * 4);
     L.dkh = take(T * HV * dk * 4);
+    L.fcnt = take(tc128 ? (size_t)L.nchm * HK * 4 : 0);  // the on-chip fold's arrival counters
     L.total = o;
     return L;
 }
@@ -2342,6 +2364,7 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
     p.dgamA = reinterpret_cast<float*>(ws + L.dgA);
     p.dqh = reinterpret_cast<float*>(ws + L.dqh);
     p.dkh = reinterpret_cast<float*>(ws + L.dkh);
+    p.fcnt = reinterpret_cast<unsigned*>(ws + L.fcnt);
     p.N = s->N; p.T = s->T_total; p.HK = s->HK; p.HV = s->HV; p.G = s->HV / s->HK; p.dk = s->dk; p.dv = s->dv;
     p.use_norm = s->use_qk_l2norm ? 1 : 0;
     p.nchm = L.nchm;
@@ -2359,6 +2382,7 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
     }
 
     if (cudaMemsetAsync(ws, 0, sizeof(unsigned), cs) != cudaSuccess) return GDN_ERR_CUDA;
+    if (L.fcnt != L.total && cudaMemsetAsync(ws + L.fcnt, 0, L.total - L.fcnt, cs) != cudaSuccess) return GDN_ERR_CUDA;
     bwd_offsets_kernel<<<1, 32, 0, cs>>>(p);
     if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
     if (s->T_total > 0) {
@@ -2426,7 +2450,8 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
                               (uint64_t)s->HV * 256, kC) != GDN_OK)
             return GDN_ERR_CUDA;
         if (!set_smem(bwd_intra_tc_kernel, kIntraCTcSmem)) return GDN_ERR_CUDA;
-        bwd_intra_tc_kernel<<<gch, kNTtc, kIntraCTcSmem, cs>>>(mk, mu, mdu, ms, mqk, mt, mq, mv, mdo, p);
+        // one-dimensional grid, value heads fastest: the G heads of a k-head fold on chip (no fold pass)
+        bwd_intra_tc_kernel<<<(unsigned)CH, kNTtc, kIntraCTcSmem, cs>>>(mk, mu, mdu, ms, mqk, mt, mq, mv, mdo, p);
     } else {
         const size_t smem_is = sizeof(float) * (kMaxD * kLdD + 4 * kC * kLdD + 2 * kC + 32);
         if (!set_smem(bwd_intra_s_kernel, smem_is)) return GDN_ERR_CUDA;
@@ -2437,7 +2462,7 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
         bwd_intra_c_kernel<<<gch, kNT, smem_ic, cs>>>(p);
     }
     if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
-    if (s->T_total > 0) {
+    if (!tc128 && s->T_total > 0) {
         const long long vec = (long long)s->T_total * s->HK;  // one warp each, 8 per CTA
         bwd_fold_kernel<<<(unsigned)((vec + 7) / 8), 256, 0, cs>>>(p);
         if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
