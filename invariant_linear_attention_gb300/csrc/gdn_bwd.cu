@@ -670,29 +670,31 @@ __device__ __forceinline__ void put_slice_tc(uint8_t* dst, int i, int c0, uint32
 }
 
 // per (sequence, head), chunks in order: S_c out, U = U~ - W S^T, S <- Gam_last S + U^T diag(b) K.
-// Software-pipelined: while chunk j computes, chunk j+1's W and U~ arrive in shared memory by
-// 16-byte cp.async (W into its operand buffer once the first product has read it, U~ into its
-// own buffer once the first epilogue has read it), and its normalised keys come into registers;
-// diag(b) K is formed when they are written as the operand.
+// The state lives in TMEM (fp32, row i in lane i, columns [0, DK)): it is the A operand of S W^T
+// (read as TF32: the low 13 mantissa bits unused) and, scaled by Gam_last in place once that product
+// is done, the accumulator of U^T diag(b) K, so no state epilogue or shared-memory copy of S sits
+// between one chunk's last product and the next chunk's first.  While chunk j computes, chunk j+1's
+// W arrives by 16-byte cp.async once the first product has read W, and its normalised keys come
+// into registers; diag(b) K is formed when they are written as the operand.  U~ comes into
+// registers while the first product runs.  At full size the pass streams about 190 KB per chunk
+// step (S_c and U out; W, U~ and K^ in), so one CTA per SM already keeps HBM well loaded.
 template <int DK>
 __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p) {
-    constexpr int kDv = 128, kS = DK / 4;
+    constexpr int kDv = 128, kS = DK / 4, kSc = kS >= 16 ? 16 : 8;  // state columns per thread, per TMEM access
     constexpr uint32_t kSboD = DK * 32;
     constexpr bool kStateT = kStateTransposed<DK>;
     extern __shared__ __align__(128) uint8_t smb[];
-    uint8_t* sS = smb;                          // A of U^T = S W^T:         128 x DK
-    uint8_t* sW = sS + kDv * DK * 4;            // B of U^T:                 64 x DK
+    uint8_t* sW = smb;                          // B of U^T = S W^T:         64 x DK
     uint8_t* sUt = sW + kC * DK * 4;            // A of U^T diag(b) K:       128 x 64
     uint8_t* sBKt = sUt + kDv * kC * 4;         // B (transposed diag(b) K): DK x 64
-    float* sUtil = reinterpret_cast<float*>(sBKt + DK * kC * 4);  // U~, row-major 64 x 128
-    float* sfb = sUtil + kC * kDv;              // b_r = exp(gam_last - gam_r) of the chunk in bk (0 past len)
+    float* sfb = reinterpret_cast<float*>(sBKt + DK * kC * 4);  // b_r = exp(gam_last - gam_r) of the chunk in bk
     uint64_t* bar = reinterpret_cast<uint64_t*>(sfb + kC);
     uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
     const int n = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
     const int i = (warp & 3) * 32 + (tid & 31), cg = warp >> 2;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     using WRows = RowsTc<kC, DK>;
-    // W of chunk ci into its operand layout (unrounded until the copies land)
+    // W of chunk ci into its operand layout (at dk = 128 already TF32, as bwd_wy_tc_kernel stores it)
     auto issue_w = [&](size_t ci) {
         const float* src = p.Wb + ci * kC * DK;
 #pragma unroll
@@ -708,15 +710,6 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p)
             *q = tf32_round4(*q);
         }
     };
-    auto issue_ut = [&](size_t ci) {
-        const float* src = p.Utb + ci * kC * kDv;
-        for (int e = tid; e < kC * kDv / 4; e += kNTtc) cp_async16(sUtil + 4 * e, src + 4 * e);
-    };
-    float S[kS];
-    const float* s0 = p.init_state ? p.init_state + (((size_t)n * p.HV + h) * kDv + i) * DK + cg * kS : nullptr;
-#pragma unroll
-    for (int c = 0; c < kS; ++c) S[c] = s0 ? s0[c] : 0.f;
-    put_slice_tc<kS>(sS, i, cg * kS, kSboD, S, 1.f);
     if (tid == 0) {
         mbar_init(bar, 1);
         fence_barrier_init();
@@ -757,13 +750,21 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p)
         }
     };
     if (has(0)) {
-        const size_t ci = ch_index(p, p.coff[n], h);
-        issue_w(ci);
-        issue_ut(ci);
+        issue_w(ch_index(p, p.coff[n], h));
         bk_load(0);
     }
-    tc_sync();
-    const uint32_t tmem = *slot;
+    tc_sync();  // the TMEM address is in *slot
+    const uint32_t tmem = *slot, tS = tmem + lane_base + cg * kS;
+    {   // S_0 (this thread's kS columns of row i) into TMEM
+        const float* s0 = p.init_state ? p.init_state + (((size_t)n * p.HV + h) * kDv + i) * DK + cg * kS : nullptr;
+#pragma unroll
+        for (int c = 0; c < kS; c += 8) {
+            float x[8];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) x[m] = s0 ? s0[c + m] : 0.f;
+            tmem_st<1>(tS + c, x);
+        }
+    }
     uint32_t phase = 0;
     bool ok = true;
     for (int j = 0; has(j) && ok; ++j) {
@@ -771,49 +772,71 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p)
         const int t0 = bos + j * kC, len = min(kC, eos - t0);
         const size_t ci = ch_index(p, c, h), cn = ch_index(p, c + 1, h);
         const bool next = has(j + 1);
-        cp_async_wait_all();  // this thread's copies of W and U~ (commits what is still open)
-        round_w();
+        cp_async_wait_all();  // this thread's copies of W (commits what is still open)
+        if constexpr (DK != 128) round_w();
         if (tid < kC) sfb[tid] = fb_in ? __expf(fb_gl - fb_gr) : 0.f;
         __syncthreads();  // sfb of this chunk is complete
         bk_put();
         const float Gl = __expf(p.gam[(size_t)(t0 + len - 1) * p.HV + h]);
         tc_sync();
         if (tid == 0) {
-            umma_tf32_k(tmem, smem_u32(sS), kSboD, smem_u32(sW), kSboD, umma_idesc_tf32(kDv, kC), DK, false);
+            const uint32_t id = umma_idesc_tf32(kDv, kC);
+            for (int s8 = 0; s8 < DK / 8; ++s8)
+                umma_tf32_ts(tmem + 128, tmem + 8 * s8, umma_desc(smem_u32(sW) + 256u * s8, kSboD), id, s8 > 0);
             umma_commit(bar);
         }
-        // chunk-start state out while the product runs
-        if constexpr (kStateT) store_state_slice<kS, true>(p.Sb + (ci * DK + cg * kS) * kDv + i, S);
-        else store_state_slice<kS, false>(p.Sb + (ci * kDv + i) * DK + cg * kS, S);
+        // chunk-start state out, U~ into registers and the next chunk's keys, while the product runs
+#pragma unroll
+        for (int c8 = 0; c8 < kS; c8 += kSc) {
+            float x[kSc];
+            tmem_ld<kSc / 8>(tS + c8, x);
+            if constexpr (kStateT) {
+                float* dst = p.Sb + (ci * DK + cg * kS + c8) * kDv + i;
+#pragma unroll
+                for (int m = 0; m < kSc; ++m) dst[(size_t)m * kDv] = x[m];
+            } else {
+                float* dst = p.Sb + (ci * kDv + i) * DK + cg * kS + c8;
+#pragma unroll
+                for (int m = 0; m < kSc; m += 4)
+                    *reinterpret_cast<float4*>(dst + m) = make_float4(x[m], x[m + 1], x[m + 2], x[m + 3]);
+            }
+        }
+        float ut[16];
+        {
+            const float* ug = p.Utb + ci * kC * kDv + i;
+#pragma unroll
+            for (int m = 0; m < 16; ++m) ut[m] = ug[(size_t)(cg * 16 + m) * kDv];
+        }
         if (next) bk_load(j + 1);
         if (!(ok = tc_wait(bar, phase))) break;
         if (next) issue_w(cn);
+        // S <- Gam_last S in place: the first term of the state update
+#pragma unroll
+        for (int c8 = 0; c8 < kS; c8 += kSc) {
+            float x[kSc];
+            tmem_ld<kSc / 8>(tS + c8, x);
+#pragma unroll
+            for (int m = 0; m < kSc; ++m) x[m] *= Gl;
+            tmem_st<kSc / 8>(tS + c8, x);
+        }
         {   // U[r][i] = U~[r][i] - (S W^T)[i][r] for this thread's 16 values of r
             float x[16];
-            tmem_ld<2>(tmem + lane_base + cg * 16, x);
+            tmem_ld<2>(tmem + lane_base + 128 + cg * 16, x);
             float* ug = p.Ub + ci * kC * kDv + i;
 #pragma unroll
             for (int m = 0; m < 16; ++m) {
-                x[m] = sUtil[(cg * 16 + m) * kDv + i] - x[m];
+                x[m] = ut[m] - x[m];
                 // at dk = 128 U only ever enters the tensor cores: stored already rounded to TF32
                 ug[(size_t)(cg * 16 + m) * kDv] = DK == 128 ? tf32_round(x[m]) : x[m];
             }
             put_slice_tc<16>(sUt, i, cg * 16, kSboC, x, 1.f);
         }
         tc_sync();
-        if (tid == 0) {
-            umma_tf32_k(tmem + 128, smem_u32(sUt), kSboC, smem_u32(sBKt), kSboC, umma_idesc_tf32(kDv, DK), kC, false);
+        if (tid == 0) {  // S += U^T diag(b) K
+            umma_tf32_k(tmem, smem_u32(sUt), kSboC, smem_u32(sBKt), kSboC, umma_idesc_tf32(kDv, DK), kC, true);
             umma_commit(bar);
         }
-        if (next) issue_ut(cn);
         if (!(ok = tc_wait(bar, phase))) break;
-        {   // S <- Gam_last S + (U^T diag(b) K)
-            float x[kS];
-            tmem_ld<kS / 8>(tmem + lane_base + 128 + cg * kS, x);
-#pragma unroll
-            for (int m = 0; m < kS; ++m) S[m] = fmaf(Gl, S[m], x[m]);
-            put_slice_tc<kS>(sS, i, cg * kS, kSboD, S, 1.f);
-        }
     }
     cp_async_wait_all();
     if (!ok && tid == 0) atomicOr(p.err, GDN_DEVERR_TIMEOUT);
@@ -824,23 +847,25 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p)
 
 // per (sequence, head), chunks in reverse: D_c out (gradient at chunk end), dU, d_init_state.
 //   dU^T = dO^T P + D (diag(b) K)^T,   D <- Gam_last D + dO^T diag(Gam) Q - dU^T W
-// The first product and dO^T (diag(Gam) Q) go out together, so once they complete the buffers of
-// dO^T, P^T, diag(b) K and (diag(Gam) Q)^T are free: W^T (loaded into registers meanwhile)
-// takes dO^T's place for the last product, and the next chunk's P and normalised k and q rows
-// start arriving by cp.async (scaled into diag(b) K and diag(Gam) Q when they are rounded); the
-// next chunk's dO comes into registers during the last product.
+// D lives in TMEM (fp32, row i in lane i, columns [256, 256 + DK)): the A operand of D (diag(b) K)^T
+// (read as TF32) and, scaled by Gam_last in place once the first product is done, the accumulator
+// of the last two.  D_c goes out while the first product runs.  W^T has a buffer of its own (loaded
+// into registers during the first product), and (diag(Gam) Q)^T two, so the next chunk's P and
+// normalised k and q rows start arriving by cp.async (scaled into diag(b) K and diag(Gam) Q when
+// they are rounded) while the last two products run; the next chunk's dO comes into registers
+// meanwhile and takes dO^T's place once they are done.
 template <int DK>
 __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p) {
-    constexpr int kDv = 128, kS = DK / 4;
+    constexpr int kDv = 128, kS = DK / 4, kSc = kS >= 16 ? 16 : 8;  // state columns per thread, per TMEM access
     constexpr uint32_t kSboD = DK * 32;
     constexpr bool kStateT = kStateTransposed<DK>;
     extern __shared__ __align__(128) uint8_t smb[];
-    uint8_t* sD = smb;                          // A: D                         128 x DK
-    uint8_t* sOt = sD + kDv * DK * 4;           // A: dO^T (128 x 64), then B: W^T (DK x 64)
-    uint8_t* sPt = sOt + kDv * kC * 4;          // B: P^T                       64 x 64
+    uint8_t* sOt = smb;                         // A: dO^T                      128 x 64
+    uint8_t* sW = sOt + kDv * kC * 4;           // B: W^T                       DK x 64
+    uint8_t* sPt = sW + DK * kC * 4;            // B: P^T                       64 x 64
     uint8_t* sBK = sPt + kC * kC * 4;           // B: diag(b) K                 64 x DK
-    uint8_t* sGQt = sBK + kC * DK * 4;          // B: (diag(Gam) Q)^T           DK x 64
-    uint8_t* sdUt = sGQt + DK * kC * 4;         // A: -dU^T                     128 x 64
+    uint8_t* sGQt0 = sBK + kC * DK * 4;         // B: (diag(Gam) Q)^T, two      DK x 64 each
+    uint8_t* sdUt = sGQt0 + 2 * DK * kC * 4;    // A: -dU^T                     128 x 64
     float* sfb = reinterpret_cast<float*>(sdUt + kDv * kC * 4);  // b_r of the chunk in sBK (0 past len)
     float* sfg = sfb + kC;                                       // Gam_r of the chunk in sGQt (0 past len)
     uint64_t* bar = reinterpret_cast<uint64_t*>(sfg + kC);
@@ -877,7 +902,7 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p)
     // and the factors b_r, Gam_r: diag(b) K^ and diag(Gam) Q^ are formed when the copies are rounded
     float fb_gl = 0.f, fb_gr = 0.f;  // gam_last and gam_r (r = tid < 64) of the chunk being copied
     bool fb_in = false;
-    auto issue_chunk = [&](size_t ci, int t0c, int lenc) {
+    auto issue_chunk = [&](size_t ci, int t0c, int lenc, uint8_t* sGQt) {
         PT::issue_async(sPt, p.Pb + ci * kC * kC);
         const float* kr = p.kn + ((size_t)t0c * p.HK + hk) * DK;
         const float* qr = p.qn + ((size_t)t0c * p.HK + hk) * DK;
@@ -905,7 +930,7 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p)
             fb_gr = fb_in ? p.gam[(size_t)(t0c + tid) * p.HV + h] : 0.f;
         }
     };
-    auto scale_round = [&]() {  // this thread's copies: diag(b) K^ and (diag(Gam) Q^)^T, rounded to TF32
+    auto scale_round = [&](uint8_t* sGQt) {  // this thread's copies: diag(b) K^ and (diag(Gam) Q^)^T as TF32
 #pragma unroll
         for (int it = 0; it < BK::kItems; ++it) {
             const int r = BK::row(it);
@@ -922,27 +947,32 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p)
             *q = tf32_round4(make_float4(sfg[k] * v.x, sfg[k + 1] * v.y, sfg[k + 2] * v.z, sfg[k + 3] * v.w));
         }
     };
-    float D[kS];
-    const float* df = p.dfinal ? p.dfinal + (((size_t)n * p.HV + h) * kDv + i) * DK + cg * kS : nullptr;
-#pragma unroll
-    for (int c = 0; c < kS; ++c) D[c] = df ? df[c] : 0.f;
-    put_slice_tc<kS>(sD, i, cg * kS, kSboD, D, 1.f);
     if (tid == 0) {
         mbar_init(bar, 1);
         fence_barrier_init();
     }
-    if (warp == 0) tmem_alloc(slot, 256);
+    if (warp == 0) tmem_alloc(slot, 512);
     const int bos = min(max(p.cu[n], 0), p.T), eos = min(max(p.cu[n + 1], bos), p.T);
     const int nch = (eos - bos + kC - 1) / kC;
     const int jtop = min(nch, p.nchm - p.coff[n]) - 1;  // last chunk inside the workspace
     if (jtop >= 0) {
         const int t0 = bos + jtop * kC;
-        issue_chunk(ch_index(p, p.coff[n] + jtop, h), t0, min(kC, eos - t0));
+        issue_chunk(ch_index(p, p.coff[n] + jtop, h), t0, min(kC, eos - t0), sGQt0);
         load_dO(t0, min(kC, eos - t0));
         put_dO();
     }
-    tc_sync();
-    const uint32_t tmem = *slot;
+    tc_sync();  // the TMEM address is in *slot
+    const uint32_t tmem = *slot, tD = tmem + lane_base + 256 + cg * kS;
+    {   // D at the sequence end (this thread's kS columns of row i) into TMEM
+        const float* df = p.dfinal ? p.dfinal + (((size_t)n * p.HV + h) * kDv + i) * DK + cg * kS : nullptr;
+#pragma unroll
+        for (int c = 0; c < kS; c += 8) {
+            float x[8];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) x[m] = df ? df[c + m] : 0.f;
+            tmem_st<1>(tD + c, x);
+        }
+    }
     uint32_t phase = 0;
     bool ok = true;
     for (int j = jtop; j >= 0 && ok; --j) {
@@ -951,30 +981,52 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p)
         const size_t ci = ch_index(p, c, h);
         const bool prev = j > 0;
         const int tp = t0 - kC;  // the chunk before this one is always full
-        if constexpr (kStateT) store_state_slice<kS, true>(p.Db + (ci * DK + cg * kS) * kDv + i, D);
-        else store_state_slice<kS, false>(p.Db + (ci * kDv + i) * DK + cg * kS, D);
+        uint8_t* sGQt = sGQt0 + ((jtop - j) & 1) * (DK * kC * 4);
         cp_async_wait_all();  // this thread's copies of P, diag(b) K, diag(Gam) Q
-        PT::round_in_place(sPt);
+        if constexpr (DK != 128) PT::round_in_place(sPt);  // at dk = 128 bwd_wy_tc_kernel stores P as TF32
         if (tid < kC) {
             sfb[tid] = fb_in ? __expf(fb_gl - fb_gr) : 0.f;
             sfg[tid] = fb_in ? __expf(fb_gr) : 0.f;
         }
         __syncthreads();  // sfb, sfg of this chunk are complete
-        scale_round();
+        scale_round(sGQt);
         const float Gl = __expf(p.gam[(size_t)(t0 + len - 1) * p.HV + h]);
         tc_sync();
-        if (tid == 0) {
-            const uint32_t i1 = umma_idesc_tf32(kDv, kC), i2 = umma_idesc_tf32(kDv, DK);
+        if (tid == 0) {  // dU^T = dO^T P + D (diag(b) K)^T
+            const uint32_t i1 = umma_idesc_tf32(kDv, kC);
             umma_tf32_k(tmem, smem_u32(sOt), kSboC, smem_u32(sPt), kSboC, i1, kC, false);
-            umma_tf32_k(tmem, smem_u32(sD), kSboD, smem_u32(sBK), kSboD, i1, DK, true);
-            umma_tf32_k(tmem + 128, smem_u32(sOt), kSboC, smem_u32(sGQt), kSboC, i2, kC, false);
+            for (int s8 = 0; s8 < DK / 8; ++s8)
+                umma_tf32_ts(tmem, tmem + 256 + 8 * s8, umma_desc(smem_u32(sBK) + 256u * s8, kSboD), i1, true);
             umma_commit(bar);
+        }
+        // D_c out and W^T into registers while the product runs
+#pragma unroll
+        for (int c8 = 0; c8 < kS; c8 += kSc) {
+            float x[kSc];
+            tmem_ld<kSc / 8>(tD + c8, x);
+            if constexpr (kStateT) {
+                float* dst = p.Db + (ci * DK + cg * kS + c8) * kDv + i;
+#pragma unroll
+                for (int m = 0; m < kSc; ++m) dst[(size_t)m * kDv] = x[m];
+            } else {
+                float* dst = p.Db + (ci * kDv + i) * DK + cg * kS + c8;
+#pragma unroll
+                for (int m = 0; m < kSc; m += 4)
+                    *reinterpret_cast<float4*>(dst + m) = make_float4(x[m], x[m + 1], x[m + 2], x[m + 3]);
+            }
         }
         GT w;
         w.load(p.Wb + ci * kC * DK);
         if (!(ok = tc_wait(bar, phase))) break;
-        w.put(sOt);  // W^T where dO^T was
-        if (prev) issue_chunk(ci - p.HV, tp, kC);
+        // D <- Gam_last D in place: the first term of the update
+#pragma unroll
+        for (int c8 = 0; c8 < kS; c8 += kSc) {
+            float x[kSc];
+            tmem_ld<kSc / 8>(tD + c8, x);
+#pragma unroll
+            for (int m = 0; m < kSc; ++m) x[m] *= Gl;
+            tmem_st<kSc / 8>(tD + c8, x);
+        }
         {   // dU[s][i] for this thread's 16 values of s; -dU^T as the last product's A
             float x[16];
             tmem_ld<2>(tmem + lane_base + cg * 16, x);
@@ -984,28 +1036,35 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p)
                 dug[(size_t)(cg * 16 + m) * kDv] = DK == 128 ? tf32_round(x[m]) : x[m];
             put_slice_tc<16>(sdUt, i, cg * 16, kSboC, x, -1.f);
         }
+        w.put(sW);
         tc_sync();
-        if (tid == 0) {
-            umma_tf32_k(tmem + 128, smem_u32(sdUt), kSboC, smem_u32(sOt), kSboC, umma_idesc_tf32(kDv, DK), kC, true);
+        if (tid == 0) {  // D += dO^T diag(Gam) Q - dU^T W
+            const uint32_t i2 = umma_idesc_tf32(kDv, DK);
+            umma_tf32_k(tmem + 256, smem_u32(sOt), kSboC, smem_u32(sGQt), kSboC, i2, kC, true);
+            umma_tf32_k(tmem + 256, smem_u32(sdUt), kSboC, smem_u32(sW), kSboC, i2, kC, true);
             umma_commit(bar);
         }
-        if (prev) load_dO(tp, kC);
-        if (!(ok = tc_wait(bar, phase))) break;
-        {   // D <- Gam_last D + (dO^T diag(Gam) Q - dU^T W)
-            float x[kS];
-            tmem_ld<kS / 8>(tmem + lane_base + 128 + cg * kS, x);
-#pragma unroll
-            for (int m = 0; m < kS; ++m) D[m] = fmaf(Gl, D[m], x[m]);
-            put_slice_tc<kS>(sD, i, cg * kS, kSboD, D, 1.f);
+        if (prev) {  // the next chunk's operands (its Q^ into the other buffer) while they run
+            issue_chunk(ci - p.HV, tp, kC, sGQt0 + ((jtop - j + 1) & 1) * (DK * kC * 4));
+            load_dO(tp, kC);
         }
-        if (prev) put_dO();  // the last product has read W^T
+        if (!(ok = tc_wait(bar, phase))) break;
+        if (prev) put_dO();  // the last products have read dO^T
     }
     cp_async_wait_all();
-    if (ok && p.dinit) store_slice<kS>(p.dinit + (((size_t)n * p.HV + h) * kDv + i) * DK + cg * kS, D);
+    if (ok && p.dinit) {
+        float* dst = p.dinit + (((size_t)n * p.HV + h) * kDv + i) * DK + cg * kS;
+#pragma unroll
+        for (int c8 = 0; c8 < kS; c8 += kSc) {
+            float x[kSc];
+            tmem_ld<kSc / 8>(tD + c8, x);
+            store_slice<kSc>(dst + c8, x);
+        }
+    }
     if (!ok && tid == 0) atomicOr(p.err, GDN_DEVERR_TIMEOUT);
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 // ---------------------------------------------------------------------------
@@ -1196,7 +1255,9 @@ __global__ void __launch_bounds__(kNTtc, kWyCtasPerSm)
     uint64_t* bar = reinterpret_cast<uint64_t*>(sb + kC);
     uint64_t* bar_ld = bar + 1;  // the tensor copies of K^ and Q^
     uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 2);
-    const int c = blockIdx.x, h = blockIdx.y;
+    // one CTA per (chunk, value head), the heads of a chunk adjacent in launch order (they copy the
+    // same K^ and Q^ rows)
+    const int h = (int)(blockIdx.x % (unsigned)p.HV), c = (int)(blockIdx.x / (unsigned)p.HV);
     int n, t0, len;
     if (!chunk_of(p, c, n, t0, len)) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, q = warp & 3, cg = warp >> 2;
@@ -1301,7 +1362,8 @@ __global__ void __launch_bounds__(kNTtc, kWyCtasPerSm)
                         const int s = cg * 16 + t + u;
                         e[u] = (s <= r && r < len) ? x[t + u] * __expf(sg[r] - sg[s]) : 0.f;
                     }
-                    *reinterpret_cast<float4*>(P + t) = make_float4(e[0], e[1], e[2], e[3]);
+                    // P only ever enters the tensor cores (the backward state pass): stored as TF32
+                    *reinterpret_cast<float4*>(P + t) = tf32_round4(make_float4(e[0], e[1], e[2], e[3]));
                 }
             }
         }
@@ -1441,7 +1503,7 @@ __global__ void __launch_bounds__(kNTtc, kWyCtasPerSm)
             float* Ut = p.Utb + ci * kC * kD + jj;
 #pragma unroll
             for (int t = 0; t < 16; ++t) {
-                W[(size_t)(cg * 16 + t) * kD] = w[t];
+                W[(size_t)(cg * 16 + t) * kD] = tf32_round(w[t]);  // W only ever enters the tensor cores
                 Ut[(size_t)(cg * 16 + t) * kD] = u[t];
             }
         }
@@ -2298,8 +2360,8 @@ template <int DK>
 static gdn_status launch_state_tc(const BwdParams& p, int N, int HV, cudaStream_t cs) {
     const dim3 grid(N, HV);
     const size_t tail = 64;  // mbarrier + TMEM address slot
-    const size_t smem_f = (size_t)4 * (128 * DK + kC * DK + 128 * kC + DK * kC + kC * 128 + kC) + tail;
-    const size_t smem_b = (size_t)4 * (128 * DK + 128 * kC + kC * kC + kC * DK + DK * kC + 128 * kC + 2 * kC) + tail;
+    const size_t smem_f = (size_t)4 * (kC * DK + 128 * kC + DK * kC + kC) + tail;
+    const size_t smem_b = (size_t)4 * (128 * kC + DK * kC + kC * kC + kC * DK + 2 * DK * kC + 128 * kC + 2 * kC) + tail;
     if (!set_smem(bwd_state_fwd_tc_kernel<DK>, smem_f)) return GDN_ERR_CUDA;
     bwd_state_fwd_tc_kernel<DK><<<grid, kNTtc, smem_f, cs>>>(p);
     if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
@@ -2406,7 +2468,7 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
         return GDN_ERR_CUDA;
     if (tc128) {
         if (!set_smem(bwd_wy_tc_kernel, kWyTcSmem)) return GDN_ERR_CUDA;
-        bwd_wy_tc_kernel<<<gch, kNTtc, kWyTcSmem, cs>>>(mk, mq, p);
+        bwd_wy_tc_kernel<<<(unsigned)CH, kNTtc, kWyTcSmem, cs>>>(mk, mq, p);
     } else {
         const size_t smem_wy = sizeof(float) * (2 * kC * kLdD + 2 * kC * kLdC + 3 * kC);
         if (!set_smem(bwd_wy_kernel, smem_wy)) return GDN_ERR_CUDA;

@@ -92,6 +92,18 @@ __device__ __forceinline__ void umma_tf32_k(uint32_t d_tmem, uint32_t a_saddr, u
                   accumulate || s > 0);
 }
 
+// D (+)= A B^T over one K = 8 step with A in TMEM (row m in lane m, its 8 values of k in the columns
+// from a_tmem on, read as TF32) and B in shared memory; issued by a single thread.
+__device__ __forceinline__ void umma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+
 // An MMA operand in shared memory, in one of two layouts:
 //   rows == 0: the layout above, row groups sbo apart;
 //   rows != 0: K-major with the 128-byte swizzle: rows of 32 values (128 bytes) whose 16-byte chunks
