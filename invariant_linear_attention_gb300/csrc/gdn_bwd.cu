@@ -1104,7 +1104,9 @@ __global__ void __launch_bounds__(kNT) bwd_intra_s_kernel(BwdParams p) {
     load_rows_f32(sB, kLdD, p.qn + ((size_t)t0 * p.HK + hk) * dk, (size_t)p.HK * dk, kC, len, dk);
     load_rows_f32(sC, kLdD, p.dUb + ci * kC * dv, dv, kC, kC, dv);
     for (int i = threadIdx.x; i < kC; i += blockDim.x) {
-        sg[i] = i < len ? p.gam[(size_t)(t0 + i) * p.HV + h] : 0.f;
+        // past the chunk's end gam stays at its last value (as the cumsum in bwd_wy_tc_kernel leaves it),
+        // so gam is non-increasing over all 64 rows and exp(gam_r - gam_s), s <= r, never exceeds 1
+        sg[i] = p.gam[(size_t)(t0 + min(i, len - 1)) * p.HV + h];
         sdg[i] = 0.f;
     }
     __syncthreads();
@@ -1542,7 +1544,9 @@ __global__ void __launch_bounds__(kNT) bwd_intra_c_kernel(BwdParams p) {
     load_rows_f32(sT, kLdC, p.Tb + ci * kC * kC, kC, kC, kC, kC);
     const float* dga = p.dgamA + ci * kC;
     for (int i = threadIdx.x; i < kC; i += blockDim.x) {
-        sg[i] = i < len ? p.gam[(size_t)(t0 + i) * p.HV + h] : 0.f;
+        // past the chunk's end gam stays at its last value (as the cumsum in bwd_wy_tc_kernel leaves it),
+        // so gam is non-increasing over all 64 rows and exp(gam_r - gam_s), s <= r, never exceeds 1
+        sg[i] = p.gam[(size_t)(t0 + min(i, len - 1)) * p.HV + h];
         sbe[i] = i < len ? p.beta[(size_t)(t0 + i) * p.HV + h] : 0.f;
         sdg[i] = dga[i];
         sdb[i] = 0.f;
@@ -1644,9 +1648,9 @@ __global__ void __launch_bounds__(kNT) bwd_intra_c_kernel(BwdParams p) {
     for (int r = threadIdx.x >> 4; r < kC; r += blockDim.x >> 4) {
         const int l = threadIdx.x & 15;
         float rs = 0.f, cs = 0.f;
-        for (int s = l; s < kC; s += 16) {
-            rs = fmaf(sE[r * kLdC + s], __expf(sg[r] - sg[s]), rs);
-            cs = fmaf(sE[s * kLdC + r], __expf(sg[s] - sg[r]), cs);
+        for (int s = l; s < kC; s += 16) {  // dE is lower triangular: exp only on its support
+            rs = fmaf(sE[r * kLdC + s], s <= r ? __expf(sg[r] - sg[s]) : 0.f, rs);
+            cs = fmaf(sE[s * kLdC + r], s >= r ? __expf(sg[s] - sg[r]) : 0.f, cs);
         }
         rs = half_sum(rs);
         cs = half_sum(cs);
@@ -1750,7 +1754,7 @@ __device__ __forceinline__ void fold_token(const BwdParams& p, long long w, int 
 // K^, U, dU and S0^T arrive by tensor copies (one thread, one mbarrier) in the 128-byte-swizzled
 // K-major layout (boxes of 32 values x rows, four atom columns per 128 values); D^T takes the same
 // layout, written by threads; every other operand uses the layout of umma_koff.
-constexpr size_t kIntraCTcSmem = (size_t)5 * 32768 + 2 * 16384 + 4 * kC * kLdT + 4 * (4 * kC + 3 * 4 * kC) + 32;
+constexpr size_t kIntraCTcSmem = (size_t)5 * 32768 + 2 * 16384 + 4 * kC * kLdT + 4 * (6 * kC + 3 * 4 * kC) + 32;
 
 __global__ void __launch_bounds__(kNTtc, 1)
     bwd_intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_u,
@@ -1777,7 +1781,9 @@ __global__ void __launch_bounds__(kNTtc, 1)
     float* part1 = sdb + kC;                            // [4][64] column-dot partials (F1)
     float* part2 = part1 + 4 * kC;                      // [4][64] column-dot partials (F2)
     float* rowp = part2 + 4 * kC;                       // [4][64] row-loop partials
-    uint64_t* bar = reinterpret_cast<uint64_t*>(rowp + 4 * kC);
+    float* sgE = rowp + 4 * kC;                         // exp(gam_r)
+    float* sgL = sgE + kC;                              // exp(gam_last - gam_r)
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sgL + kC);
     uint64_t* bar_ld = bar + 1;  // the tensor copies of phase A
     uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 2);
     uint32_t* s_last = slot + 1;  // this CTA folds the chunk's dq^, dk^ rows of its k-head
@@ -1835,7 +1841,12 @@ __global__ void __launch_bounds__(kNTtc, 1)
             dreg[hf][it] = *reinterpret_cast<const float4*>(Dt + j * kD + kC * hf + k);
         }
     for (int i = tid; i < kC; i += kNTtc) {
-        sg[i] = i < len ? p.gam[(size_t)(t0 + i) * p.HV + h] : 0.f;
+        // past the chunk's end gam stays at its last value (as the cumsum in bwd_wy_tc_kernel leaves it),
+        // so gam is non-increasing over all 64 rows and exp(gam_r - gam_s), s <= r, never exceeds 1
+        const float gi = p.gam[(size_t)(t0 + min(i, len - 1)) * p.HV + h];
+        sg[i] = gi;
+        sgE[i] = __expf(gi);
+        sgL[i] = __expf(p.gam[(size_t)(t0 + len - 1) * p.HV + h] - gi);
         sbe[i] = i < len ? p.beta[(size_t)(t0 + i) * p.HV + h] : 0.f;
         sdb[i] = 0.f;
     }
@@ -1954,7 +1965,7 @@ __global__ void __launch_bounds__(kNTtc, 1)
 #pragma unroll
             for (int m = 0; m < 16; ++m) {
                 const int r = cg * 16 + m;
-                const float d = r < len ? __expf(sg[r]) * x[m] : 0.f;
+                const float d = r < len ? sgE[r] * x[m] : 0.f;
                 x[m] = d;
                 qv[m] *= d;
             }
@@ -1985,7 +1996,7 @@ __global__ void __launch_bounds__(kNTtc, 1)
             for (int m = 0; m < 16; ++m) {
                 const int r = cg * 16 + m;
                 kv[m] *= x[m];
-                x[m] = r < len ? __expf(gl - sg[r]) * x[m] : 0.f;
+                x[m] = r < len ? sgL[r] * x[m] : 0.f;
             }
             tmem_st<2>(tmem + lane_base + 192 + cg * 16, x);
             const float part = warp_transpose_sum<16>(kv);
@@ -1996,7 +2007,7 @@ __global__ void __launch_bounds__(kNTtc, 1)
             float dg = 0.f, bd = 0.f;
             if (r < len) {
                 dg = ((part1[r] + part1[kC + r]) + part1[2 * kC + r]) + part1[3 * kC + r];
-                bd = __expf(gl - sg[r]) * (((part2[r] + part2[kC + r]) + part2[2 * kC + r]) + part2[3 * kC + r]);
+                bd = sgL[r] * (((part2[r] + part2[kC + r]) + part2[2 * kC + r]) + part2[3 * kC + r]);
             }
             sdg[r] = dg - bd;
             rowp[r] = bd;
@@ -2102,7 +2113,7 @@ __global__ void __launch_bounds__(kNTtc, 1)
                     const float tv = tr[t];
                     v1[t] = tv * f1[t];
                     v2[t] = tv * f2[t];
-                    dt[t] = sbe[r] * fmaf(__expf(sg[r]), f1[t], f2[t]);
+                    dt[t] = sbe[r] * fmaf(sgE[r], f1[t], f2[t]);
                 }
 #pragma unroll
                 for (int t = 0; t < 16; t += 4)
@@ -2141,7 +2152,7 @@ __global__ void __launch_bounds__(kNTtc, 1)
         {
             const uint8_t* T4 = R4 + 16384;
             auto tv = [&](int s, int r) { return *reinterpret_cast<const float*>(T4 + sw128_off(s, r, kC)); };
-            stage_cols_fn<kC, kC>(C1, [&](int s, int r) { return tv(s, r) * sbe[r] * __expf(sg[r]); });
+            stage_cols_fn<kC, kC>(C1, [&](int s, int r) { return tv(s, r) * sbe[r] * sgE[r]; });
             stage_cols_fn<kC, kC>(C2, [&](int s, int r) { return tv(s, r) * sbe[r]; });
         }
         __syncthreads();
@@ -2153,7 +2164,7 @@ __global__ void __launch_bounds__(kNTtc, 1)
         for (int r = tid; r < kC; r += kNTtc) {
             const float a1 = ((part1[r] + part1[kC + r]) + part1[2 * kC + r]) + part1[3 * kC + r];
             const float a2 = ((part2[r] + part2[kC + r]) + part2[2 * kC + r]) + part2[3 * kC + r];
-            const float Gr = __expf(sg[r]);
+            const float Gr = sgE[r];
             sdb[r] += Gr * a1 + a2;
             sdg[r] += Gr * sbe[r] * a1;
         }
@@ -2202,7 +2213,9 @@ __global__ void __launch_bounds__(kNTtc, 1)
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
                     const int s = cg * 16 + t;
-                    const float da = s < r ? -a[t] : 0.f, e = __expf(sg[r] - sg[s]);
+                    // exp(gam_r - gam_s) only where s < r: above the diagonal it can overflow, and
+                    // 0 * inf would be NaN
+                    const float da = s < r ? -a[t] : 0.f, e = s < r ? __expf(sg[r] - sg[s]) : 0.f;
                     acc = fmaf(da * e, kk[t], acc);
                     sdKK[r * kLdT + s] = da * sbe[r] * e;
                     sE[r * kLdT + s] = fmaf(da * sbe[r], kk[t], sE[r * kLdT + s]);
@@ -2245,9 +2258,9 @@ __global__ void __launch_bounds__(kNTtc, 1)
         for (int r = tid >> 4; r < kC; r += kNTtc >> 4) {
             const int l = tid & 15;
             float rs = 0.f, cs = 0.f;
-            for (int s = l; s < kC; s += 16) {
-                rs = fmaf(sE[r * kLdT + s], __expf(sg[r] - sg[s]), rs);
-                cs = fmaf(sE[s * kLdT + r], __expf(sg[s] - sg[r]), cs);
+            for (int s = l; s < kC; s += 16) {  // dE is lower triangular: exp only on its support
+                rs = fmaf(sE[r * kLdT + s], s <= r ? __expf(sg[r] - sg[s]) : 0.f, rs);
+                cs = fmaf(sE[s * kLdT + r], s >= r ? __expf(sg[s] - sg[r]) : 0.f, cs);
             }
             rs = half_sum(rs);
             cs = half_sum(cs);

@@ -4,6 +4,8 @@ relative error 1e-2 per gradient tensor, per (sequence, head) where the
 tensor has one.  Cases span partial and exact chunks (chunk = 64), empty
 sequences, GQA folding, both dtypes, the l2norm switch, and sampled units of
 the 8 x 4096-token workload."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -135,3 +137,21 @@ def test_deterministic():
     torch.cuda.synchronize()
     for k in NAMES:
         assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("dtype,dk,dv", [(torch.bfloat16, 128, 128), (torch.float32, 64, 64)])
+def test_strong_decay(dtype, dk, dv):
+    """Log-decays about eight times the usual draw (a chunk's cumulative decay reaches several
+    hundred): the decay factors between two positions of a chunk are only ever taken in the
+    decaying direction, so no exp overflows into a NaN.  Both the tcgen05 and the mma.sync
+    kernels."""
+    lengths = [130, 64, 21]
+    x = inputs.make_inputs(lengths, HK=1, HV=2, dk=dk, dv=dv, dtype=dtype, seed=34, init_scale=0.2)
+    x = dataclasses.replace(x, g=(x.g * 8.0).contiguous())
+    assert float(x.g[:64].sum()) < -300.0
+    dO = inputs.grad_out(sum(lengths), 2, dv, dtype=dtype, seed=35)
+    dsT = inputs.random_states(len(lengths), 2, dv, dk, seed=36, scale=0.5)
+    got, ref = run(x, dO, dsT)
+    for name, v in got.items():
+        assert np.isfinite(v).all(), name
+    check(got, ref, x.cu_seqlens)
