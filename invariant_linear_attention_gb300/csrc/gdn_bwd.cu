@@ -1744,8 +1744,8 @@ __device__ __forceinline__ void fold_token(const BwdParams& p, long long w, int 
 // row).  Gam_r X_q and b_r Y go back into TMEM (tcgen05.st) as the first terms of the dq^T and
 // dk^T accumulators; dW stays on chip, as F1's operand and, from X_w, as the transposed one.
 // The C x C products (dP = dO U^T, K K^T, F1 = dW K^T, F2 = dU V^T, Z = dT T^T, T^T Z) use M = 64:
-// row m of the result sits in TMEM lane 32 (m / 16) + m % 16, so lanes 0..15 of each warp hold 16
-// rows.  The products that update dq, dk, dv are taken transposed with the dk / dv index as their
+// row m of the result sits in TMEM lane 32 (m / 16) + m % 16, so lanes 0..15 of each warp quarter
+// hold 16 rows, which the 16x256b loads (tmem_ld16) spread over all 32 threads of the warp.  The products that update dq, dk, dv are taken transposed with the dk / dv index as their
 // 128 rows; dq's two and dk's four terms accumulate in TMEM and meet global memory once.
 //   TMEM columns: 0 dP, then Z | 64 K K^T | 128 X_q, then dq^T | 192 Y, then dk^T | 256 X_w, then
 //   dv^T | 320 dU S0 (128 wide), then F1 | 384 F2 | 448 T^T Z
@@ -1795,8 +1795,9 @@ __global__ void __launch_bounds__(kNTtc, 1)
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const int hk = h / p.G;
     const size_t ci = ch_index(p, c, h);
-    const bool row_lane = lane < 16;    // lanes holding a row of an M = 64 result
-    const int r64 = 16 * q + (lane & 15);  // that row
+    // an M = 64 result comes in by 16x256b loads (tmem_ld16): this thread's rows ra and ra + 8, and
+    // in each block of 8 columns the pair from cp on
+    const int ra = 16 * q + (lane >> 2), cp = 2 * (lane & 3);
     const int jj = 32 * q + lane;          // the dk / dv index of an M = 128 result
     const size_t sk = (size_t)p.HK * kD;
     const float* kb = p.kn + ((size_t)t0 * p.HK + hk) * kD;  // K^ row s at kb + s * sk
@@ -1941,14 +1942,14 @@ __global__ void __launch_bounds__(kNTtc, 1)
             kv[m] = r < len ? kb[(size_t)r * sk + jj] : 0.f;
         }
         {  // dW = -(dU S0) -> R4 (rows s, k = j): F1's A operand
-            float x[32];
-            tmem_ld<4>(tmem + lane_base + 320 + cg * 32, x);
-            if (row_lane) {
+            float y[16];
+            tmem_ld16<4>(tmem + lane_base + 320 + cg * 32, y);
 #pragma unroll
-                for (int t = 0; t < 32; t += 4)
-                    *reinterpret_cast<float4*>(R4 + umma_koff(r64, cg * 32 + t, kSboD)) =
-                        tf32_round4(make_float4(-x[t], -x[t + 1], -x[t + 2], -x[t + 3]));
-            }
+            for (int n = 0; n < 4; ++n)
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr)
+                    *reinterpret_cast<float2*>(R4 + umma_koff(ra + 8 * hr, cg * 32 + 8 * n + cp, kSboD)) =
+                        make_float2(tf32_round(-y[4 * n + 2 * hr]), tf32_round(-y[4 * n + 2 * hr + 1]));
         }
         tc_sync();
         if (tid == 0) {
@@ -2022,29 +2023,25 @@ __global__ void __launch_bounds__(kNTtc, 1)
         ld_pending = -1;
         // phase B: dQK = lower(dP) E, dE = lower(dP) QK; dQK (C1) and its transpose (C2)
         {
-            float x[16];
-            tmem_ld<2>(tmem + lane_base + 0 + cg * 16, x);
-            if (row_lane) {
-                const int r = r64;
-                float qv[16];
+            float y[8];
+            tmem_ld16<2>(tmem + lane_base + 0 + cg * 16, y);
 #pragma unroll
-                for (int t = 0; t < 16; t += 4) {
-                    const float4 v = *reinterpret_cast<const float4*>(R4 + sw128_off(r, cg * 16 + t, kC));
-                    qv[t] = v.x; qv[t + 1] = v.y; qv[t + 2] = v.z; qv[t + 3] = v.w;
+            for (int hr = 0; hr < 2; ++hr) {
+                const int r = ra + 8 * hr;
+#pragma unroll
+                for (int n = 0; n < 2; ++n) {
+                    const int s = cg * 16 + 8 * n + cp;
+                    const float2 qk = *reinterpret_cast<const float2*>(R4 + sw128_off(r, s, kC));
+                    const float x0 = y[4 * n + 2 * hr], x1 = y[4 * n + 2 * hr + 1];
+                    const bool in0 = s <= r && r < len, in1 = s + 1 <= r && r < len;
+                    const float d0 = in0 ? x0 * __expf(sg[r] - sg[s]) : 0.f;
+                    const float d1 = in1 ? x1 * __expf(sg[r] - sg[s + 1]) : 0.f;
+                    sE[r * kLdT + s] = in0 ? x0 * qk.x : 0.f;
+                    sE[r * kLdT + s + 1] = in1 ? x1 * qk.y : 0.f;
+                    *reinterpret_cast<float*>(C2 + umma_koff(s, r, kSboC)) = tf32_round(d0);
+                    *reinterpret_cast<float*>(C2 + umma_koff(s + 1, r, kSboC)) = tf32_round(d1);
+                    *reinterpret_cast<float2*>(C1 + umma_koff(r, s, kSboC)) = make_float2(tf32_round(d0), tf32_round(d1));
                 }
-                float d[16];
-#pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    const int s = cg * 16 + t;
-                    const bool in = s <= r && r < len;
-                    d[t] = in ? x[t] * __expf(sg[r] - sg[s]) : 0.f;
-                    sE[r * kLdT + s] = in ? x[t] * qv[t] : 0.f;
-                    *reinterpret_cast<float*>(C2 + umma_koff(s, r, kSboC)) = tf32_round(d[t]);
-                }
-#pragma unroll
-                for (int t = 0; t < 16; t += 4)
-                    *reinterpret_cast<float4*>(C1 + umma_koff(r, cg * 16 + t, kSboC)) =
-                        tf32_round4(make_float4(d[t], d[t + 1], d[t + 2], d[t + 3]));
             }
         }
         // V -> R2 (rows s, from its bf16 copy in R2 + 16 KB), K^T -> R3 (rows j, k = s) from the copy of K^
@@ -2095,38 +2092,43 @@ __global__ void __launch_bounds__(kNTtc, 1)
         if (!(ok = tc_wait(bar, phase))) break;
         // phase C: column dots with T, dT (-> R4, rows s, k = r); dq update
         {
-            float f1[16], f2[16];
-            tmem_ld_pair(tmem + lane_base + 320 + cg * 16, f1, tmem + lane_base + 384 + cg * 16, f2);
-            float v1[16], v2[16];
-            if (row_lane) {
-                const int s = r64;
-                float tr[16];
+            float f1[8], f2[8];
+            tmem_ld16_pair(tmem + lane_base + 320 + cg * 16, f1, tmem + lane_base + 384 + cg * 16, f2);
+            // partial column sums over this thread's two rows: columns cg * 16 + 8 n + cp (+1) at [2 n (+1)]
+            float c1[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int t = 0; t < 16; t += 4) {
-                    const float4 v = *reinterpret_cast<const float4*>(R4 + 16384 + sw128_off(s, cg * 16 + t, kC));
-                    tr[t] = v.x; tr[t + 1] = v.y; tr[t + 2] = v.z; tr[t + 3] = v.w;
+            for (int hr = 0; hr < 2; ++hr) {
+                const int s = ra + 8 * hr;
+#pragma unroll
+                for (int n = 0; n < 2; ++n) {
+                    const int r = cg * 16 + 8 * n + cp, i = 4 * n + 2 * hr;
+                    const float2 tv = *reinterpret_cast<const float2*>(R4 + 16384 + sw128_off(s, r, kC));
+                    c1[2 * n] = fmaf(tv.x, f1[i], c1[2 * n]);
+                    c1[2 * n + 1] = fmaf(tv.y, f1[i + 1], c1[2 * n + 1]);
+                    c2[2 * n] = fmaf(tv.x, f2[i], c2[2 * n]);
+                    c2[2 * n + 1] = fmaf(tv.y, f2[i + 1], c2[2 * n + 1]);
+                    const float dt0 = sbe[r] * fmaf(sgE[r], f1[i], f2[i]);
+                    const float dt1 = sbe[r + 1] * fmaf(sgE[r + 1], f1[i + 1], f2[i + 1]);
+                    *reinterpret_cast<float2*>(R4 + umma_koff(s, r, kSboC)) = make_float2(tf32_round(dt0), tf32_round(dt1));
                 }
-                float dt[16];
-#pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    const int r = cg * 16 + t;
-                    const float tv = tr[t];
-                    v1[t] = tv * f1[t];
-                    v2[t] = tv * f2[t];
-                    dt[t] = sbe[r] * fmaf(sgE[r], f1[t], f2[t]);
-                }
-#pragma unroll
-                for (int t = 0; t < 16; t += 4)
-                    *reinterpret_cast<float4*>(R4 + umma_koff(s, cg * 16 + t, kSboC)) =
-                        tf32_round4(make_float4(dt[t], dt[t + 1], dt[t + 2], dt[t + 3]));
-            } else {
-#pragma unroll
-                for (int t = 0; t < 16; ++t) v1[t] = v2[t] = 0.f;
             }
-            const float a1 = warp_transpose_sum<16>(v1), a2 = warp_transpose_sum<16>(v2);
-            if (lane < 16) {
-                part1[q * kC + cg * 16 + lane] = a1;
-                part2[q * kC + cg * 16 + lane] = a2;
+            // over the eight row groups of the warp (the lanes with this lane's lane % 4), fixed order
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    c1[j] += __shfl_xor_sync(kFull, c1[j], off);
+                    c2[j] += __shfl_xor_sync(kFull, c2[j], off);
+                }
+            if (lane < 4) {
+#pragma unroll
+                for (int n = 0; n < 2; ++n) {
+                    const int r = cg * 16 + 8 * n + cp;
+                    part1[q * kC + r] = c1[2 * n];
+                    part1[q * kC + r + 1] = c1[2 * n + 1];
+                    part2[q * kC + r] = c2[2 * n];
+                    part2[q * kC + r + 1] = c2[2 * n + 1];
+                }
             }
             float x[16];
             float* dq = p.dqh + ((size_t)t0 * p.HV + h) * kD + jj;
@@ -2185,12 +2187,16 @@ __global__ void __launch_bounds__(kNTtc, 1)
                 const int r = cg * 16 + t;
                 if (r < len) st_any(p.dv_out, ((size_t)(t0 + r) * p.HV + h) * kD + jj, p.dtype, x[t]);
             }
-            tmem_ld<2>(tmem + lane_base + 0 + cg * 16, x);
-            if (row_lane) {
+            float z[8];
+            tmem_ld16<2>(tmem + lane_base + 0 + cg * 16, z);
 #pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    *reinterpret_cast<float*>(R5 + umma_koff(cg * 16 + t, r64, kSboC)) = tf32_round(x[t]);
-            }
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                        *reinterpret_cast<float*>(R5 + umma_koff(cg * 16 + 8 * n + cp + e, ra + 8 * hr, kSboC)) =
+                            tf32_round(z[4 * n + 2 * hr + e]);
         }
         stage_cols_fn<kC, kC>(R5 + 16384, [&](int a, int r) {
             return *reinterpret_cast<const float*>(R4 + 16384 + sw128_off(a, r, kC));
@@ -2205,22 +2211,28 @@ __global__ void __launch_bounds__(kNTtc, 1)
         // dE += dA beta_r KK
         float* sdKK = reinterpret_cast<float*>(R2);  // 64 x kLdT
         {
-            float a[16], kk[16];
-            tmem_ld_pair(tmem + lane_base + 448 + cg * 16, a, tmem + lane_base + 64 + cg * 16, kk);
-            float acc = 0.f;
-            if (row_lane) {
-                const int r = r64;
+            float a[8], kk[8];
+            tmem_ld16_pair(tmem + lane_base + 448 + cg * 16, a, tmem + lane_base + 64 + cg * 16, kk);
 #pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    const int s = cg * 16 + t;
-                    // exp(gam_r - gam_s) only where s < r: above the diagonal it can overflow, and
-                    // 0 * inf would be NaN
-                    const float da = s < r ? -a[t] : 0.f, e = s < r ? __expf(sg[r] - sg[s]) : 0.f;
-                    acc = fmaf(da * e, kk[t], acc);
-                    sdKK[r * kLdT + s] = da * sbe[r] * e;
-                    sE[r * kLdT + s] = fmaf(da * sbe[r], kk[t], sE[r * kLdT + s]);
-                }
-                rowp[cg * kC + r] = acc;
+            for (int hr = 0; hr < 2; ++hr) {
+                const int r = ra + 8 * hr;
+                float acc = 0.f;
+#pragma unroll
+                for (int n = 0; n < 2; ++n)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int s = cg * 16 + 8 * n + cp + e, i = 4 * n + 2 * hr + e;
+                        // exp(gam_r - gam_s) only where s < r: above the diagonal it can overflow, and
+                        // 0 * inf would be NaN
+                        const float da = s < r ? -a[i] : 0.f, ex = s < r ? __expf(sg[r] - sg[s]) : 0.f;
+                        acc = fmaf(da * ex, kk[i], acc);
+                        sdKK[r * kLdT + s] = da * sbe[r] * ex;
+                        sE[r * kLdT + s] = fmaf(da * sbe[r], kk[i], sE[r * kLdT + s]);
+                    }
+                // the row's 16 columns of this warp sit in the four lanes of its row group
+                acc += __shfl_xor_sync(kFull, acc, 1);
+                acc += __shfl_xor_sync(kFull, acc, 2);
+                if ((lane & 3) == 0) rowp[cg * kC + r] = acc;
             }
         }
         __syncthreads();

@@ -215,6 +215,53 @@ __device__ __forceinline__ void tmem_ld_pair(uint32_t ta, float (&va)[16], uint3
     }
 }
 
+// Rows 16 lanes x 8 * NX columns of TMEM from taddr on (an M = 64 accumulator keeps 16 rows in
+// lanes 0..15 of each warp quarter) over all 32 threads, shape 16x256b (NX = 2 or 4): in column
+// block n (columns 8 n ..) thread t holds v[4 n] = (row t / 4, column 8 n + 2 (t % 4)), v[4 n + 1]
+// the next column, v[4 n + 2], v[4 n + 3] the same two columns of row t / 4 + 8.  One load and its
+// wait in one asm statement.
+template <int NX>
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[4 * NX]) {
+    static_assert(NX == 2 || NX == 4, "16 or 32 columns");
+    uint32_t r[4 * NX];
+    if constexpr (NX == 2) {
+        asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t"
+                     "tcgen05.wait::ld.sync.aligned;"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                     : "r"(taddr)
+                     : "memory");
+    } else {
+        asm volatile("tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+                     "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+                     "tcgen05.wait::ld.sync.aligned;"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                       "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+                       "=r"(r[14]), "=r"(r[15])
+                     : "r"(taddr)
+                     : "memory");
+    }
+#pragma unroll
+    for (int j = 0; j < 4 * NX; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// Two 16x256b loads of 16 columns (at ta into va, at tb into vb) and one wait for both.
+__device__ __forceinline__ void tmem_ld16_pair(uint32_t ta, float (&va)[8], uint32_t tb, float (&vb)[8]) {
+    uint32_t r[16];
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%16];\n\t"
+                 "tcgen05.ld.sync.aligned.16x256b.x2.b32 {%8, %9, %10, %11, %12, %13, %14, %15}, [%17];\n\t"
+                 "tcgen05.wait::ld.sync.aligned;"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+                   "=r"(r[15])
+                 : "r"(ta), "r"(tb)
+                 : "memory");
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        va[j] = __uint_as_float(r[j]);
+        vb[j] = __uint_as_float(r[8 + j]);
+    }
+}
+
 // The reverse of tmem_ld (NX = 1 or 2): v into columns [col, col + 8 * NX) of this warp's 32 lanes,
 // then a wait for the stores, so that a barrier after it orders them before the next MMA on those
 // columns.
