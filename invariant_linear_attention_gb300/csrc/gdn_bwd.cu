@@ -2270,9 +2270,9 @@ __global__ void __launch_bounds__(kNTtc, 1)
         for (int r = tid >> 4; r < kC; r += kNTtc >> 4) {
             const int l = tid & 15;
             float rs = 0.f, cs = 0.f;
-            for (int s = l; s < kC; s += 16) {  // dE is lower triangular: exp only on its support
-                rs = fmaf(sE[r * kLdT + s], s <= r ? __expf(sg[r] - sg[s]) : 0.f, rs);
-                cs = fmaf(sE[s * kLdT + r], s >= r ? __expf(sg[s] - sg[r]) : 0.f, cs);
+            for (int s = l; s < kC; s += 16) {  // dE is lower triangular: only its support is summed
+                if (s <= r) rs = fmaf(sE[r * kLdT + s], __expf(sg[r] - sg[s]), rs);
+                if (s >= r) cs = fmaf(sE[s * kLdT + r], __expf(sg[s] - sg[r]), cs);
             }
             rs = half_sum(rs);
             cs = half_sum(cs);
