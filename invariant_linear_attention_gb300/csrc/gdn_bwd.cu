@@ -850,13 +850,15 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p)
 // D lives in TMEM (fp32, row i in lane i, columns [256, 256 + DK)): the A operand of D (diag(b) K)^T
 // (read as TF32) and, scaled by Gam_last in place once the first product is done, the accumulator
 // of the last two.  D_c goes out while the first product runs.  W^T has a buffer of its own (loaded
-// into registers during the first product), and (diag(Gam) Q)^T two, so the next chunk's P and
-// normalised k and q rows start arriving by cp.async (scaled into diag(b) K and diag(Gam) Q when
-// they are rounded) while the last two products run; the next chunk's dO comes into registers
-// meanwhile and takes dO^T's place once they are done.
+// into registers during the first product).  The next chunk's P, and its k and q rows as given
+// (bf16, into staging buffers), arrive by cp.async while the last two products run; at the top of
+// its step they become diag(b) K^ and (diag(Gam) Q^)^T, scaled by 1/|k_r|, 1/|q_r| and the decay
+// factors and rounded.  The next chunk's dO comes into registers meanwhile and takes dO^T's place
+// once the products are done.
 template <int DK>
 __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p) {
     constexpr int kDv = 128, kS = DK / 4, kSc = kS >= 16 ? 16 : 8;  // state columns per thread, per TMEM access
+    constexpr int kStg = DK * 2 + 16;  // staging row pitch (bytes): 16-byte aligned, rows on different banks
     constexpr uint32_t kSboD = DK * 32;
     constexpr bool kStateT = kStateTransposed<DK>;
     extern __shared__ __align__(128) uint8_t smb[];
@@ -864,11 +866,15 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p)
     uint8_t* sW = sOt + kDv * kC * 4;           // B: W^T                       DK x 64
     uint8_t* sPt = sW + DK * kC * 4;            // B: P^T                       64 x 64
     uint8_t* sBK = sPt + kC * kC * 4;           // B: diag(b) K                 64 x DK
-    uint8_t* sGQt0 = sBK + kC * DK * 4;         // B: (diag(Gam) Q)^T, two      DK x 64 each
-    uint8_t* sdUt = sGQt0 + 2 * DK * kC * 4;    // A: -dU^T                     128 x 64
-    float* sfb = reinterpret_cast<float*>(sdUt + kDv * kC * 4);  // b_r of the chunk in sBK (0 past len)
-    float* sfg = sfb + kC;                                       // Gam_r of the chunk in sGQt (0 past len)
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sfg + kC);
+    uint8_t* sGQt = sBK + kC * DK * 4;          // B: (diag(Gam) Q)^T           DK x 64
+    uint8_t* sdUt = sGQt + DK * kC * 4;         // A: -dU^T                     128 x 64
+    uint8_t* sKs = sdUt + kDv * kC * 4;         // k rows of the next chunk, bf16, rows kStg bytes apart
+    uint8_t* sQs = sKs + kC * kStg;             // q rows likewise
+    float* sfb = reinterpret_cast<float*>(sQs + kC * kStg);  // b_r of the chunk in sBK (0 past len)
+    float* sfg = sfb + kC;                                    // Gam_r of the chunk in sGQt (0 past len)
+    float* skinv = sfg + kC;                                  // 1/|k_r|, 1/|q_r| of that chunk
+    float* sqinv = skinv + kC;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sqinv + kC);
     uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
     const int n = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
     const int i = (warp & 3) * 32 + (tid & 31), cg = warp >> 2;
@@ -898,53 +904,61 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p)
         }
     };
     const int hk = h / p.G;
-    // P^T, K^ rows and Q^^T of chunk ci (tokens t0c .., lenc of them; rows >= lenc zero) by cp.async,
-    // and the factors b_r, Gam_r: diag(b) K^ and diag(Gam) Q^ are formed when the copies are rounded
+    // P^T (by cp.async into its operand layout) and the k and q rows of chunk ci as given (bf16, by
+    // 16-byte cp.async into the staging buffers; tokens t0c .., lenc of them, rows >= lenc zero), and
+    // the factors b_r, Gam_r, 1/|k_r|, 1/|q_r| for the top of its step
     float fb_gl = 0.f, fb_gr = 0.f;  // gam_last and gam_r (r = tid < 64) of the chunk being copied
+    float fb_kinv = 0.f, fb_qinv = 0.f;
     bool fb_in = false;
-    auto issue_chunk = [&](size_t ci, int t0c, int lenc, uint8_t* sGQt) {
+    auto issue_chunk = [&](size_t ci, int t0c, int lenc) {
         PT::issue_async(sPt, p.Pb + ci * kC * kC);
-        const float* kr = p.kn + ((size_t)t0c * p.HK + hk) * DK;
-        const float* qr = p.qn + ((size_t)t0c * p.HK + hk) * DK;
+        const __nv_bfloat16* kr = static_cast<const __nv_bfloat16*>(p.k) + ((size_t)t0c * p.HK + hk) * DK;
+        const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(p.q) + ((size_t)t0c * p.HK + hk) * DK;
         const size_t st = (size_t)p.HK * DK;
-#pragma unroll
-        for (int it = 0; it < BK::kItems; ++it) {
-            const int r = BK::row(it), k = BK::col(it);
-            uint8_t* d = sBK + umma_koff(r, k, DK * 32);
-            if (r < lenc) cp_async16(d, kr + r * st + k);
-            else *reinterpret_cast<float4*>(d) = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int it = 0; it < GT::kItems; ++it) {
-            const int e = tid + it * kNTtc, nn = e % DK, k = (e / DK) * 4;
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                uint8_t* d = sGQt + umma_koff(nn, k + t, kC * 32);
-                if (k + t < lenc) cp_async4(d, qr + (k + t) * st + nn);
-                else *reinterpret_cast<float*>(d) = 0.f;
+        constexpr int kPieces = DK / 8;  // 16-byte pieces per row
+        for (int e = tid; e < kC * kPieces; e += kNTtc) {
+            const int r = e / kPieces, c = (e % kPieces) * 8;
+            uint8_t* dk_ = sKs + r * kStg + c * 2;
+            uint8_t* dq_ = sQs + r * kStg + c * 2;
+            if (r < lenc) {
+                cp_async16(dk_, kr + r * st + c);
+                cp_async16(dq_, qr + r * st + c);
+            } else {
+                *reinterpret_cast<uint4*>(dk_) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(dq_) = make_uint4(0u, 0u, 0u, 0u);
             }
         }
         if (tid < kC) {  // used a chunk step later: no wait for these loads here
             fb_in = tid < lenc;
             fb_gl = p.gam[(size_t)(t0c + lenc - 1) * p.HV + h];
             fb_gr = fb_in ? p.gam[(size_t)(t0c + tid) * p.HV + h] : 0.f;
+            fb_kinv = fb_in ? p.kinv[(size_t)(t0c + tid) * p.HK + hk] : 0.f;
+            fb_qinv = fb_in ? p.qinv[(size_t)(t0c + tid) * p.HK + hk] : 0.f;
         }
     };
-    auto scale_round = [&](uint8_t* sGQt) {  // this thread's copies: diag(b) K^ and (diag(Gam) Q^)^T as TF32
+    // diag(b) K^ and (diag(Gam) Q^)^T as TF32 from the staged rows: b_r (k_r 1/|k_r|) and
+    // Gam_r (q_r 1/|q_r|), the same fp32 products as the normalised rows times the factors
+    auto stage_in = [&]() {
+        auto bf = [](uint32_t u, int hi) { return __uint_as_float(hi ? (u & 0xFFFF0000u) : (u << 16)); };
 #pragma unroll
         for (int it = 0; it < BK::kItems; ++it) {
-            const int r = BK::row(it);
-            float4* q = reinterpret_cast<float4*>(sBK + umma_koff(r, BK::col(it), DK * 32));
-            const float4 v = *q;
-            const float f = sfb[r];
-            *q = tf32_round4(make_float4(f * v.x, f * v.y, f * v.z, f * v.w));
+            const int r = BK::row(it), k = BK::col(it);
+            const uint2 raw = *reinterpret_cast<const uint2*>(sKs + r * kStg + k * 2);
+            const float f = sfb[r], iv = skinv[r];
+            *reinterpret_cast<float4*>(sBK + umma_koff(r, k, DK * 32)) = tf32_round4(
+                make_float4(f * (bf(raw.x, 0) * iv), f * (bf(raw.x, 1) * iv), f * (bf(raw.y, 0) * iv),
+                            f * (bf(raw.y, 1) * iv)));
         }
 #pragma unroll
         for (int it = 0; it < GT::kItems; ++it) {
             const int e = tid + it * kNTtc, nn = e % DK, k = (e / DK) * 4;
-            float4* q = reinterpret_cast<float4*>(sGQt + umma_koff(nn, k, kC * 32));
-            const float4 v = *q;
-            *q = tf32_round4(make_float4(sfg[k] * v.x, sfg[k + 1] * v.y, sfg[k + 2] * v.z, sfg[k + 3] * v.w));
+            float v[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const float x = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sQs + (k + t) * kStg + nn * 2));
+                v[t] = sfg[k + t] * (x * sqinv[k + t]);
+            }
+            *reinterpret_cast<float4*>(sGQt + umma_koff(nn, k, kC * 32)) = tf32_round4(make_float4(v[0], v[1], v[2], v[3]));
         }
     };
     if (tid == 0) {
@@ -957,7 +971,7 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p)
     const int jtop = min(nch, p.nchm - p.coff[n]) - 1;  // last chunk inside the workspace
     if (jtop >= 0) {
         const int t0 = bos + jtop * kC;
-        issue_chunk(ch_index(p, p.coff[n] + jtop, h), t0, min(kC, eos - t0), sGQt0);
+        issue_chunk(ch_index(p, p.coff[n] + jtop, h), t0, min(kC, eos - t0));
         load_dO(t0, min(kC, eos - t0));
         put_dO();
     }
@@ -981,15 +995,16 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p)
         const size_t ci = ch_index(p, c, h);
         const bool prev = j > 0;
         const int tp = t0 - kC;  // the chunk before this one is always full
-        uint8_t* sGQt = sGQt0 + ((jtop - j) & 1) * (DK * kC * 4);
-        cp_async_wait_all();  // this thread's copies of P, diag(b) K, diag(Gam) Q
+        cp_async_wait_all();  // this thread's copies of P and of the k and q rows
         if constexpr (DK != 128) PT::round_in_place(sPt);  // at dk = 128 bwd_wy_tc_kernel stores P as TF32
         if (tid < kC) {
             sfb[tid] = fb_in ? __expf(fb_gl - fb_gr) : 0.f;
             sfg[tid] = fb_in ? __expf(fb_gr) : 0.f;
+            skinv[tid] = fb_kinv;
+            sqinv[tid] = fb_qinv;
         }
-        __syncthreads();  // sfb, sfg of this chunk are complete
-        scale_round(sGQt);
+        __syncthreads();  // the factors and every thread's staged rows are in shared memory
+        stage_in();
         const float Gl = __expf(p.gam[(size_t)(t0 + len - 1) * p.HV + h]);
         tc_sync();
         if (tid == 0) {  // dU^T = dO^T P + D (diag(b) K)^T
@@ -1044,8 +1059,8 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p)
             umma_tf32_k(tmem + 256, smem_u32(sdUt), kSboC, smem_u32(sW), kSboC, i2, kC, true);
             umma_commit(bar);
         }
-        if (prev) {  // the next chunk's operands (its Q^ into the other buffer) while they run
-            issue_chunk(ci - p.HV, tp, kC, sGQt0 + ((jtop - j + 1) & 1) * (DK * kC * 4));
+        if (prev) {  // the next chunk's operands while they run
+            issue_chunk(ci - p.HV, tp, kC);
             load_dO(tp, kC);
         }
         if (!(ok = tc_wait(bar, phase))) break;
@@ -2386,7 +2401,8 @@ static gdn_status launch_state_tc(const BwdParams& p, int N, int HV, cudaStream_
     const dim3 grid(N, HV);
     const size_t tail = 64;  // mbarrier + TMEM address slot
     const size_t smem_f = (size_t)4 * (kC * DK + 128 * kC + DK * kC + kC) + tail;
-    const size_t smem_b = (size_t)4 * (128 * kC + DK * kC + kC * kC + kC * DK + 2 * DK * kC + 128 * kC + 2 * kC) + tail;
+    const size_t smem_b = (size_t)4 * (128 * kC + DK * kC + kC * kC + kC * DK + DK * kC + 128 * kC + 4 * kC) +
+                          (size_t)2 * kC * (DK * 2 + 16) + tail;
     if (!set_smem(bwd_state_fwd_tc_kernel<DK>, smem_f)) return GDN_ERR_CUDA;
     bwd_state_fwd_tc_kernel<DK><<<grid, kNTtc, smem_f, cs>>>(p);
     if (launch_status() != GDN_OK) return GDN_ERR_CUDA;
