@@ -1700,51 +1700,70 @@ __device__ __forceinline__ void stage_cols_fn(uint8_t* dst, G get) {
     }
 }
 
-// One warp per (token, k-head) w: sum the G value heads' dq^ and dk^ rows in increasing head order,
-// then the L2-norm backward, into dq and dk.  The partial rows are read at L2 (__ldcg): in
-// bwd_intra_tc_kernel they were written by other CTAs of the same launch.
-__device__ __forceinline__ void fold_token(const BwdParams& p, long long w, int lane) {
-    const int t = (int)(w / p.HK), hk = (int)(w - (long long)t * p.HK);
-    // every load of a head step (dq and dk together) is issued before any is used; each element
-    // still sums the heads in increasing order
-    float dsum[2][4], x[2][4];
+// One warp per (token, k-head) w[u], NT of them at once: sum the G value heads' dq^ and dk^ rows in
+// increasing head order, then the L2-norm backward, into dq and dk.  Tokens with on[u] false are
+// skipped.  Every load of a head step (dq and dk of all NT tokens together) is issued before any
+// is used, and the inverse norms with the first ones, so the NT tokens share their round trips;
+// each element still sums the heads in increasing order.  The partial rows are read at L2
+// (__ldcg): in bwd_intra_tc_kernel they were written by other CTAs of the same launch.
+template <int NT>
+__device__ __forceinline__ void fold_tokens(const BwdParams& p, const long long (&w)[NT], const bool (&on)[NT],
+                                            int lane) {
+    float dsum[NT][2][4], x[NT][2][4], inv[NT][2];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int j = lane + 32 * i;
-        x[0][i] = j < p.dk ? p.qn[(size_t)w * p.dk + j] : 0.f;
-        x[1][i] = j < p.dk ? p.kn[(size_t)w * p.dk + j] : 0.f;
-        dsum[0][i] = dsum[1][i] = 0.f;
-    }
-    for (int hh = hk * p.G; hh < (hk + 1) * p.G; ++hh) {
-        const size_t base = ((size_t)t * p.HV + hh) * p.dk;
-        float a[4], b[4];
+    for (int u = 0; u < NT; ++u) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int j = lane + 32 * i;
-            a[i] = j < p.dk ? __ldcg(p.dqh + base + j) : 0.f;
-            b[i] = j < p.dk ? __ldcg(p.dkh + base + j) : 0.f;
+            const bool in = on[u] && j < p.dk;
+            x[u][0][i] = in ? p.qn[(size_t)w[u] * p.dk + j] : 0.f;
+            x[u][1][i] = in ? p.kn[(size_t)w[u] * p.dk + j] : 0.f;
+            dsum[u][0][i] = dsum[u][1][i] = 0.f;
+        }
+        inv[u][0] = on[u] ? p.qinv[w[u]] : 0.f;
+        inv[u][1] = on[u] ? p.kinv[w[u]] : 0.f;
+    }
+    for (int g = 0; g < p.G; ++g) {
+        float a[NT][4], b[NT][4];
+#pragma unroll
+        for (int u = 0; u < NT; ++u) {
+            const int t = (int)(w[u] / p.HK), hk = (int)(w[u] - (long long)t * p.HK);
+            const size_t base = ((size_t)t * p.HV + hk * p.G + g) * p.dk;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int j = lane + 32 * i;
+                const bool in = on[u] && j < p.dk;
+                a[u][i] = in ? __ldcg(p.dqh + base + j) : 0.f;
+                b[u][i] = in ? __ldcg(p.dkh + base + j) : 0.f;
+            }
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            dsum[0][i] += a[i];
-            dsum[1][i] += b[i];
-        }
+        for (int u = 0; u < NT; ++u)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                dsum[u][0][i] += a[u][i];
+                dsum[u][1][i] += b[u][i];
+            }
     }
 #pragma unroll
-    for (int which = 0; which < 2; ++which) {
-        float dot = 0.f;
+    for (int u = 0; u < NT; ++u) {
+        if (!on[u]) continue;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) dot = fmaf(x[which][i], dsum[which][i], dot);
+        for (int which = 0; which < 2; ++which) {
+            float dot = 0.f;
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) dot += __shfl_xor_sync(kFull, dot, off);
-        const float inv = (which ? p.kinv : p.qinv)[w];
-        void* dst = which ? p.dk_out : p.dq_out;
+            for (int i = 0; i < 4; ++i) dot = fmaf(x[u][which][i], dsum[u][which][i], dot);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int j = lane + 32 * i;
-            if (j < p.dk) {
-                const float gval = p.use_norm ? (dsum[which][i] - x[which][i] * dot) * inv : dsum[which][i];
-                st_any(dst, (size_t)w * p.dk + j, p.dtype, gval);
+            for (int off = 16; off >= 1; off >>= 1) dot += __shfl_xor_sync(kFull, dot, off);
+            void* dst = which ? p.dk_out : p.dq_out;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int j = lane + 32 * i;
+                if (j < p.dk) {
+                    const float gval = p.use_norm ? (dsum[u][which][i] - x[u][which][i] * dot) * inv[u][which]
+                                                  : dsum[u][which][i];
+                    st_any(dst, (size_t)w[u] * p.dk + j, p.dtype, gval);
+                }
             }
         }
     }
@@ -2325,7 +2344,7 @@ __global__ void __launch_bounds__(kNTtc, 1)
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 512);
     // The last of the G value-head CTAs of this (chunk, k-head) to arrive folds their dq^, dk^ rows
-    // (fold_token: the heads in increasing order, whichever CTA folds).  No CTA waits for another.
+    // (fold_tokens: the heads in increasing order, whichever CTA folds).  No CTA waits for another.
     __threadfence();  // this CTA's rows are visible on the device before it is counted
     __syncthreads();
     if (tid == 0) {
@@ -2334,15 +2353,23 @@ __global__ void __launch_bounds__(kNTtc, 1)
         *s_last = prior == (unsigned)(p.G - 1) ? 1u : 0u;
     }
     __syncthreads();
-    if (*s_last && ok)
-        for (int r = warp; r < len; r += kNTtc / 32) fold_token(p, (long long)(t0 + r) * p.HK + hk, lane);
+    if (*s_last && ok) {  // rows warp + 16 u of the chunk, two at a time with their loads together
+        for (int r = warp; r < len; r += 2 * (kNTtc / 32)) {
+            const int r2 = r + kNTtc / 32;
+            const long long ws[2] = {(long long)(t0 + r) * p.HK + hk, (long long)(t0 + min(r2, len - 1)) * p.HK + hk};
+            const bool on[2] = {true, r2 < len};
+            fold_tokens<2>(p, ws, on, lane);
+        }
+    }
 }
 
 // per (token, k-head), for the kernels that leave the fold to a pass of its own
 __global__ void bwd_fold_kernel(BwdParams p) {
     const long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (w >= (long long)p.T * p.HK) return;
-    fold_token(p, w, threadIdx.x & 31);
+    const long long ws[1] = {w};
+    const bool on[1] = {true};
+    fold_tokens<1>(p, ws, on, threadIdx.x & 31);
 }
 
 // ---------------------------------------------------------------------------
