@@ -155,3 +155,15 @@ def test_strong_decay(dtype, dk, dv):
     for name, v in got.items():
         assert np.isfinite(v).all(), name
     check(got, ref, x.cu_seqlens)
+
+
+@pytest.mark.parametrize("HK,HV", [(2, 2), (1, 4)])
+def test_fold_group_sizes_head128(HK, HV):
+    """G = HV / HK value heads per k-head of 1 and 4 through the tcgen05 kernels (bf16, dk = dv =
+    128), whose last value-head CTA of each (chunk, k-head) folds dq and dk on chip."""
+    lengths = [130, 7, 64]
+    x = inputs.make_inputs(lengths, HK=HK, HV=HV, dk=128, dv=128, dtype=torch.bfloat16, seed=37, init_scale=0.2)
+    dO = inputs.grad_out(sum(lengths), HV, 128, seed=38)
+    dsT = inputs.random_states(len(lengths), HV, 128, 128, seed=39, scale=0.5)
+    got, ref = run(x, dO, dsT)
+    check(got, ref, x.cu_seqlens)
