@@ -648,17 +648,6 @@ __device__ __forceinline__ void store_slice(float* dst, const float (&x)[NS]) {
 #pragma unroll
     for (int m = 0; m < NS; m += 4) *reinterpret_cast<float4*>(dst + m) = make_float4(x[m], x[m + 1], x[m + 2], x[m + 3]);
 }
-// Store this thread's slice (row i, columns c0 .. c0 + NS) of a 128 x DK matrix to global: row-major
-// (dst points at element (i, c0)), or transposed, DK x 128 (dst points at element (c0, i)).
-template <int NS, bool kTransposed>
-__device__ __forceinline__ void store_state_slice(float* dst, const float (&x)[NS]) {
-    if constexpr (kTransposed) {
-#pragma unroll
-        for (int m = 0; m < NS; ++m) dst[(size_t)m * 128] = x[m];
-    } else {
-        store_slice<NS>(dst, x);
-    }
-}
 // Write this thread's slice (row i, columns c0 .. c0 + NS) as the TF32 operand copy (sbo per 8 rows).
 template <int NS>
 __device__ __forceinline__ void put_slice_tc(uint8_t* dst, int i, int c0, uint32_t sbo, const float (&x)[NS], float sign) {
