@@ -167,3 +167,15 @@ def test_fold_group_sizes_head128(HK, HV):
     dsT = inputs.random_states(len(lengths), HV, 128, 128, seed=39, scale=0.5)
     got, ref = run(x, dO, dsT)
     check(got, ref, x.cu_seqlens)
+
+
+def test_deterministic_many_ctas():
+    """Bitwise-equal gradients over three calls with thousands of CTAs in flight (4 x 1024 tokens,
+    32 value heads): which value-head CTA folds a (chunk, k-head) changes from run to run, the sums
+    it takes do not."""
+    x = inputs.make_inputs([1024] * 4, HK=16, HV=32, dk=128, dv=128, dtype=torch.bfloat16, seed=40, device=DEV)
+    dO = inputs.grad_out(4096, 32, 128, seed=41, device=DEV)
+    runs = [gdn.gdn_chunk_bwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, dO) for _ in range(3)]
+    torch.cuda.synchronize()
+    for k in ("dq", "dk", "dv", "dg", "dbeta"):
+        assert torch.equal(runs[0][k], runs[1][k]) and torch.equal(runs[0][k], runs[2][k]), k
