@@ -1801,8 +1801,8 @@ __global__ void __launch_bounds__(kNTtc, 1)
     float* sbe = sg + kC;                               // beta
     float* sdg = sbe + kC;                              // dgam
     float* sdb = sdg + kC;                              // dbeta
-    float* part1 = sdb + kC;                            // [4][64] column-dot partials (F1)
-    float* part2 = part1 + 4 * kC;                      // [4][64] column-dot partials (F2)
+    float* part1 = sdb + kC;                            // [4][64] partials: F1 column dots, then dE * E row sums
+    float* part2 = part1 + 4 * kC;                      // [4][64] partials: F2 column dots, then dE * E column sums
     float* rowp = part2 + 4 * kC;                       // [4][64] row-loop partials
     float* sgE = rowp + 4 * kC;                         // exp(gam_r)
     float* sgL = sgE + kC;                              // exp(gam_last - gam_r)
@@ -2231,15 +2231,17 @@ __global__ void __launch_bounds__(kNTtc, 1)
         }
         if (!(ok = tc_wait(bar, phase))) break;
         // phase E: dA = -strict_lower(T^T Z); dbeta_r += sum_s dA E KK; dKK = dA beta_r E (fp32 in R2);
-        // dE += dA beta_r KK
+        // dE += dA beta_r KK, the last term of dE: each element's dE * E goes into this warp's partial
+        // row sums (part1, per column group) and column sums (part2, per row quarter) for dgam
         float* sdKK = reinterpret_cast<float*>(R2);  // 64 x kLdT
         {
             float a[8], kk[8];
             tmem_ld16_pair(tmem + lane_base + 448 + cg * 16, a, tmem + lane_base + 64 + cg * 16, kk);
+            float cacc[4] = {0.f, 0.f, 0.f, 0.f};  // columns cg * 16 + 8 n + cp + e at [2 n + e]
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
                 const int r = ra + 8 * hr;
-                float acc = 0.f;
+                float acc = 0.f, racc = 0.f;
 #pragma unroll
                 for (int n = 0; n < 2; ++n)
 #pragma unroll
@@ -2250,12 +2252,32 @@ __global__ void __launch_bounds__(kNTtc, 1)
                         const float da = s < r ? -a[i] : 0.f, ex = s < r ? __expf(sg[r] - sg[s]) : 0.f;
                         acc = fmaf(da * ex, kk[i], acc);
                         sdKK[r * kLdT + s] = da * sbe[r] * ex;
-                        sE[r * kLdT + s] = fmaf(da * sbe[r], kk[i], sE[r * kLdT + s]);
+                        const float de = fmaf(da * sbe[r], kk[i], sE[r * kLdT + s]);  // dE[r][s], complete
+                        const float pe = s < r ? de * ex : (s == r ? de : 0.f);     // dE * E on its support
+                        racc += pe;
+                        cacc[2 * n + e] += pe;
                     }
                 // the row's 16 columns of this warp sit in the four lanes of its row group
                 acc += __shfl_xor_sync(kFull, acc, 1);
                 acc += __shfl_xor_sync(kFull, acc, 2);
-                if ((lane & 3) == 0) rowp[cg * kC + r] = acc;
+                racc += __shfl_xor_sync(kFull, racc, 1);
+                racc += __shfl_xor_sync(kFull, racc, 2);
+                if ((lane & 3) == 0) {
+                    rowp[cg * kC + r] = acc;
+                    part1[cg * kC + r] = racc;
+                }
+            }
+            // the warp's 16 rows of each column: the eight row groups, fixed order
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) cacc[j] += __shfl_xor_sync(kFull, cacc[j], off);
+            if (lane < 4) {
+#pragma unroll
+                for (int n = 0; n < 2; ++n) {
+                    part2[q * kC + cg * 16 + 8 * n + cp] = cacc[2 * n];
+                    part2[q * kC + cg * 16 + 8 * n + cp + 1] = cacc[2 * n + 1];
+                }
             }
         }
         __syncthreads();
@@ -2289,18 +2311,11 @@ __global__ void __launch_bounds__(kNTtc, 1)
         }
     } while (false);
     if (ok) {
-        // dgam from E (row sums minus column sums of dE * E), then dg = reverse cumsum
-        for (int r = tid >> 4; r < kC; r += kNTtc >> 4) {
-            const int l = tid & 15;
-            float rs = 0.f, cs = 0.f;
-            for (int s = l; s < kC; s += 16) {  // dE is lower triangular: only its support is summed
-                if (s <= r) rs = fmaf(sE[r * kLdT + s], __expf(sg[r] - sg[s]), rs);
-                if (s >= r) cs = fmaf(sE[s * kLdT + r], __expf(sg[s] - sg[r]), cs);
-            }
-            rs = half_sum(rs);
-            cs = half_sum(cs);
-            if (l == 0) sdg[r] += rs - cs;
-        }
+        // dgam from E (row sums minus column sums of dE * E, from phase E's partials), then
+        // dg = reverse cumsum
+        for (int r = tid; r < kC; r += kNTtc)
+            sdg[r] += (((part1[r] + part1[kC + r]) + part1[2 * kC + r]) + part1[3 * kC + r]) -
+                      (((part2[r] + part2[kC + r]) + part2[2 * kC + r]) + part2[3 * kC + r]);
         __syncthreads();
         if (warp == 0) {
             // dg = reverse cumsum of dgam: lane l takes rows len-1-2l and len-2-2l, a warp scan adds
