@@ -2230,10 +2230,10 @@ __global__ void __launch_bounds__(kNTtc, 1)
             umma_commit(bar);
         }
         if (!(ok = tc_wait(bar, phase))) break;
-        // phase E: dA = -strict_lower(T^T Z); dbeta_r += sum_s dA E KK; dKK = dA beta_r E (fp32 in R2);
+        // phase E: dA = -strict_lower(T^T Z); dbeta_r += sum_s dA E KK; dKK = dA beta_r E, as TF32 operands
+        // both ways round (C1: rows r, k = s; R2: its transpose), which the last dk product adds;
         // dE += dA beta_r KK, the last term of dE: each element's dE * E goes into this warp's partial
         // row sums (part1, per column group) and column sums (part2, per row quarter) for dgam
-        float* sdKK = reinterpret_cast<float*>(R2);  // 64 x kLdT
         {
             float a[8], kk[8];
             tmem_ld16_pair(tmem + lane_base + 448 + cg * 16, a, tmem + lane_base + 64 + cg * 16, kk);
@@ -2243,7 +2243,8 @@ __global__ void __launch_bounds__(kNTtc, 1)
                 const int r = ra + 8 * hr;
                 float acc = 0.f, racc = 0.f;
 #pragma unroll
-                for (int n = 0; n < 2; ++n)
+                for (int n = 0; n < 2; ++n) {
+                    float dkk[2];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int s = cg * 16 + 8 * n + cp + e, i = 4 * n + 2 * hr + e;
@@ -2251,12 +2252,15 @@ __global__ void __launch_bounds__(kNTtc, 1)
                         // 0 * inf would be NaN
                         const float da = s < r ? -a[i] : 0.f, ex = s < r ? __expf(sg[r] - sg[s]) : 0.f;
                         acc = fmaf(da * ex, kk[i], acc);
-                        sdKK[r * kLdT + s] = da * sbe[r] * ex;
+                        dkk[e] = tf32_round(da * sbe[r] * ex);
+                        *reinterpret_cast<float*>(R2 + umma_koff(s, r, kSboC)) = dkk[e];
                         const float de = fmaf(da * sbe[r], kk[i], sE[r * kLdT + s]);  // dE[r][s], complete
                         const float pe = s < r ? de * ex : (s == r ? de : 0.f);     // dE * E on its support
                         racc += pe;
                         cacc[2 * n + e] += pe;
                     }
+                    *reinterpret_cast<float2*>(C1 + umma_koff(r, cg * 16 + 8 * n + cp, kSboC)) = make_float2(dkk[0], dkk[1]);
+                }
                 // the row's 16 columns of this warp sit in the four lanes of its row group
                 acc += __shfl_xor_sync(kFull, acc, 1);
                 acc += __shfl_xor_sync(kFull, acc, 2);
@@ -2282,19 +2286,10 @@ __global__ void __launch_bounds__(kNTtc, 1)
         }
         __syncthreads();
         for (int r = tid; r < kC; r += kNTtc) sdb[r] += ((rowp[r] + rowp[kC + r]) + rowp[2 * kC + r]) + rowp[3 * kC + r];
-        // dKK + dKK^T -> C1 (rows r, k = s)
-        for (int e = tid; e < kC * kC / 4; e += kNTtc) {
-            const int r = e / (kC / 4), s = (e % (kC / 4)) * 4;
-            float4 v;
-            v.x = sdKK[r * kLdT + s] + sdKK[s * kLdT + r];
-            v.y = sdKK[r * kLdT + s + 1] + sdKK[(s + 1) * kLdT + r];
-            v.z = sdKK[r * kLdT + s + 2] + sdKK[(s + 2) * kLdT + r];
-            v.w = sdKK[r * kLdT + s + 3] + sdKK[(s + 3) * kLdT + r];
-            *reinterpret_cast<float4*>(C1 + umma_koff(r, s, kSboC)) = tf32_round4(v);
-        }
         tc_sync();
-        if (tid == 0) {
-            umma_tf32_k(tmem + 192, smem_u32(R3), kSboC, smem_u32(C1), kSboC, id128, kC, true);  // dk^T
+        if (tid == 0) {  // dk^T += K^T (dKK + dKK^T)^T, one product per term
+            umma_tf32_k(tmem + 192, smem_u32(R3), kSboC, smem_u32(C1), kSboC, id128, kC, true);
+            umma_tf32_k(tmem + 192, smem_u32(R3), kSboC, smem_u32(R2), kSboC, id128, kC, true);
             umma_commit(bar);
         }
         if (!(ok = tc_wait(bar, phase))) break;
