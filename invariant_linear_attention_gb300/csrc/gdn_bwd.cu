@@ -553,10 +553,10 @@ __global__ void __launch_bounds__(kNTs) bwd_state_bwd_kernel(BwdParams p, int R)
 // The serial state passes on the fifth-generation tensor cores (bf16 inputs, dv = 128, dk in
 // {32, 64, 128}).  One CTA of 512 threads per (sequence, head).  Every product has the M = 128
 // state rows as its rows, so thread (warp w, lane l) owns state row i = 32 (w mod 4) + l in
-// every epilogue, and the column group w / 4 of it: its slice of the fp32 state (or state
-// gradient) stays in registers for the whole sequence.  The tensor core reads TF32-rounded
-// copies of every operand from shared memory in the K-major core-matrix layout of
-// gdn_umma.cuh; accumulators live in TMEM (columns [0, 64) and [128, 128 + dk)).
+// every epilogue, and the column group w / 4 of it.  The fp32 state (or state gradient) stays in
+// TMEM for the whole sequence (each kernel says where); the tensor core reads it there as an A
+// operand, and every other operand as a TF32-rounded copy in shared memory in the K-major
+// core-matrix layout of gdn_umma.cuh.
 // Every *_tc kernel runs exactly kNTtc threads per CTA: their thread-to-element mappings (16
 // warps = 4 TMEM lane quarters x 4 column groups, and the staging strides) assume it.
 constexpr int kNTtc = 512;
