@@ -850,7 +850,8 @@ def bench_backward(gdn, dev, steps=10):
                          "frac": achieved / tf32_peak, "flops_per_chunk_head": 2 * macs,
                          "note": "TF32 with fp32 accumulate (bf16 inputs) on tcgen05 in every contracting kernel; "
                                  "peak = sustained measured bf16 x 1.1/2.25 (nominal tf32/bf16); per-chunk "
-                                 "latency, not tensor throughput, bounds the time"}}
+                                 "latency (the chunk-parallel kernels) and HBM streaming (the serial state "
+                                 "passes), not tensor throughput, bound the time"}}
 
 
 if __name__ == "__main__":
