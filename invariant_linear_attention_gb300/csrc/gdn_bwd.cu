@@ -33,8 +33,10 @@
 //     bwd_state_bwd per (sequence, head, dv slice): D_c (end-of-chunk grads) and dU; d_init_state
 //     bwd_intra_s   per (chunk, head): the products with S0 and D (dQ_S, dW, U D)  [chunk-parallel]
 //     bwd_intra_c   per (chunk, head): the C x C products, dV, dbeta, dg          [chunk-parallel]
-//     bwd_fold      per (token, k-head): sum over the value heads of a k-head, L2-norm backward
-// Gradients are deterministic (fixed orders everywhere, no atomics on data).
+//     bwd_fold      per (token, k-head): sum over the value heads of a k-head, L2-norm backward;
+//                   in bwd_intra_tc the last value-head CTA of each (chunk, k-head) does it on chip
+// Gradients are deterministic (fixed orders everywhere, no atomics on data: the one atomic counts
+// arrivals for the on-chip fold and decides which CTA sums, not the order of the sum).
 #include <algorithm>
 
 #include "gdn_async.cuh"
