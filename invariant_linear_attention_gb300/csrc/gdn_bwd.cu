@@ -49,7 +49,7 @@ namespace gdn {
 
 constexpr int kC = 64;        // chunk length
 #ifndef STAGGER_INTRA_CYCLES
-#define STAGGER_INTRA_CYCLES 160000
+#define STAGGER_INTRA_CYCLES 100000
 #endif
 constexpr int kMaxD = 128;    // max dk, dv
 // smem leading dims = 4 (mod 32): row-major tensor-core fragment loads hit 32 distinct banks
@@ -2506,7 +2506,7 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
             cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0)
             return GDN_ERR_CUDA;
         p.nsm = nsm;
-        // the intra kernel's CTAs live about 80K SM cycles at dk = dv = 128; the first-wave spread
+        // the intra kernel's CTAs live about 50K SM cycles at dk = dv = 128; the first-wave spread
         // (two lifetimes) pays off only when the grid runs many waves
         const bool many = (long long)L.nchm * s->HV >= 8LL * nsm;
         p.stagger_intra = many ? STAGGER_INTRA_CYCLES : 0;
