@@ -179,3 +179,16 @@ def test_deterministic_many_ctas():
     torch.cuda.synchronize()
     for k in ("dq", "dk", "dv", "dg", "dbeta"):
         assert torch.equal(runs[0][k], runs[1][k]) and torch.equal(runs[0][k], runs[2][k]), k
+
+
+def test_many_ragged_sequences_head128():
+    """Forty sequences of 0 to 190 tokens (many partial chunks, some empty, some a single token)
+    through the tcgen05 kernels (bf16, dk = dv = 128), against the oracle per (sequence, head)."""
+    rng = np.random.default_rng(42)
+    lengths = [int(v) for v in rng.integers(0, 191, size=40)]
+    lengths[3], lengths[7], lengths[11] = 0, 1, 64
+    x = inputs.make_inputs(lengths, HK=2, HV=4, dk=128, dv=128, dtype=torch.bfloat16, seed=43, init_scale=0.2)
+    dO = inputs.grad_out(sum(lengths), 4, 128, seed=44)
+    dsT = inputs.random_states(len(lengths), 4, 128, 128, seed=45, scale=0.5)
+    got, ref = run(x, dO, dsT)
+    check(got, ref, x.cu_seqlens)
