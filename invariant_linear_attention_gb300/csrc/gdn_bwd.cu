@@ -1770,8 +1770,10 @@ __device__ __forceinline__ void fold_tokens(const BwdParams& p, const long long 
 // dk^T accumulators; dW stays on chip, as F1's operand and, from X_w, as the transposed one.
 // The C x C products (dP = dO U^T, K K^T, F1 = dW K^T, F2 = dU V^T, Z = dT T^T, T^T Z) use M = 64:
 // row m of the result sits in TMEM lane 32 (m / 16) + m % 16, so lanes 0..15 of each warp quarter
-// hold 16 rows, which the 16x256b loads (tmem_ld16) spread over all 32 threads of the warp.  The products that update dq, dk, dv are taken transposed with the dk / dv index as their
-// 128 rows; dq's two and dk's four terms accumulate in TMEM and meet global memory once.
+// hold 16 rows, which the 16x256b loads (tmem_ld16) spread over all 32 threads of the warp.  The
+// products that update dq, dk, dv are taken transposed with the dk / dv index as their 128 rows;
+// dq's two and dk's five terms (dKK and dKK^T separately) accumulate in TMEM and meet global memory
+// once.
 //   TMEM columns: 0 dP, then Z | 64 K K^T | 128 X_q, then dq^T | 192 Y, then dk^T | 256 X_w, then
 //   dv^T | 320 dU S0 (128 wide), then F1 | 384 F2 | 448 T^T Z
 //   shared memory: five 32 KB operand buffers R1..R5 and two 16 KB ones C1, C2 (together one
