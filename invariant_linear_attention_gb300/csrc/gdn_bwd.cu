@@ -1242,6 +1242,15 @@ __device__ __forceinline__ float half_sum(float x) {
 //   Two CTAs share an SM (64 registers a thread, 97 KB of shared memory and 256 TMEM columns
 //   each), so that one CTA's copies, solve and epilogues overlap the other's.
 constexpr int kLdT = kC + 1;  // fp32 A and T in shared memory: row-per-lane writes hit distinct banks
+
+// Staging of QK^T row r (64 fp32, sixteen 16-byte pieces) in the Q^ half of the swizzled [K^; Q^]
+// copy: rows 0..31 in the first 32-value box, rows 32..63 in the second, 256 bytes a row; P's
+// staging is 32 KB further on (the third and fourth boxes).  Piece pc sits at pc ^ (r mod 16), so
+// that eight consecutive rows writing the same piece, or one row's pieces read in order, fall in
+// distinct banks.
+__device__ __forceinline__ uint8_t* qkp_stage(uint8_t* sX, int r, int pc) {
+    return sX + 16384 * (r >> 5) + 8192 + 256 * (r & 31) + 16 * (pc ^ (r & 15));
+}
 constexpr int kWyCtasPerSm = 2;
 constexpr size_t kWyTcSmem = (size_t)65536 + 2 * 4 * kC * kLdT + 4 * 3 * kC + 32;
 // 228 KB of shared memory per SM, 1 KB of it reserved per CTA
@@ -1359,11 +1368,12 @@ __global__ void __launch_bounds__(kNTtc, kWyCtasPerSm)
                     sAf[r * kLdT + s] = s < r ? sb[r] * __expf(sg[r] - sg[s]) * x[t] : 0.f;
                 }
             } else {
-                float* QK = p.QKb + (ci * kC + r) * kC + cg * 16;
-                float* P = p.Pb + (ci * kC + r) * kC + cg * 16;
+                // QK^T and P rows staged where Q^ was (the first product has read it), and written
+                // out coalesced once the CTA has staged them all
 #pragma unroll
                 for (int t = 0; t < 16; t += 4) {
-                    *reinterpret_cast<float4*>(QK + t) = make_float4(x[t], x[t + 1], x[t + 2], x[t + 3]);
+                    uint8_t* qk = qkp_stage(sX, r, (cg * 16 + t) >> 2);
+                    *reinterpret_cast<float4*>(qk) = make_float4(x[t], x[t + 1], x[t + 2], x[t + 3]);
                     float e[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
@@ -1371,12 +1381,21 @@ __global__ void __launch_bounds__(kNTtc, kWyCtasPerSm)
                         e[u] = (s <= r && r < len) ? x[t + u] * __expf(sg[r] - sg[s]) : 0.f;
                     }
                     // P only ever enters the tensor cores (the backward state pass): stored as TF32
-                    *reinterpret_cast<float4*>(P + t) = tf32_round4(make_float4(e[0], e[1], e[2], e[3]));
+                    *reinterpret_cast<float4*>(qk + 32768) = tf32_round4(make_float4(e[0], e[1], e[2], e[3]));
                 }
             }
         }
         tc_fence_before();
         __syncthreads();  // A complete; the first product has read sX
+        {   // QK^T, then P: row-major 64 x 64 blocks of the (chunk, head), a warp writing two rows
+            constexpr int kIt = 2 * kC * kC / 4 / kNTtc;
+#pragma unroll
+            for (int it = 0; it < kIt; ++it) {
+                const int e = tid + it * kNTtc, pc = e & 15, r = (e >> 4) & (kC - 1), isP = e >> 10;
+                const float4 v = *reinterpret_cast<const float4*>(qkp_stage(sX, r, pc) + 32768 * isP);
+                *reinterpret_cast<float4*>((isP ? p.Pb : p.QKb) + (ci * kC + r) * kC + 4 * pc) = v;
+            }
+        }
         {
             // K (row s, four consecutive j, from the copy in sX) and V rows (bf16 bits, unconverted, by
             // vector loads in flight during the solve), s >= len zero; written transposed into sX after
