@@ -1361,11 +1361,19 @@ __global__ void __launch_bounds__(kNTtc, kWyCtasPerSm)
             float x[16];
             tmem_ld<2>(tmem + lane_base + cg * 16, x);
             const int m = q * 32 + lane, r = m & (kC - 1);
+            // gam of this thread's 16 columns and of its row, and beta_r, read before any store
+            float gs[16];
+#pragma unroll
+            for (int t = 0; t < 16; t += 4) {
+                const float4 g4 = *reinterpret_cast<const float4*>(sg + cg * 16 + t);
+                gs[t] = g4.x, gs[t + 1] = g4.y, gs[t + 2] = g4.z, gs[t + 3] = g4.w;
+            }
+            const float gr = sg[r], br = sb[r];
             if (m < kC) {
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
                     const int s = cg * 16 + t;
-                    sAf[r * kLdT + s] = s < r ? sb[r] * __expf(sg[r] - sg[s]) * x[t] : 0.f;
+                    sAf[r * kLdT + s] = s < r ? br * __expf(gr - gs[t]) * x[t] : 0.f;
                 }
             } else {
                 // QK^T and P rows staged where Q^ was (the first product has read it), and written
@@ -1378,7 +1386,7 @@ __global__ void __launch_bounds__(kNTtc, kWyCtasPerSm)
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int s = cg * 16 + t + u;
-                        e[u] = (s <= r && r < len) ? x[t + u] * __expf(sg[r] - sg[s]) : 0.f;
+                        e[u] = (s <= r && r < len) ? x[t + u] * __expf(gr - gs[t + u]) : 0.f;
                     }
                     // P only ever enters the tensor cores (the backward state pass): stored as TF32
                     *reinterpret_cast<float4*>(qk + 32768) = tf32_round4(make_float4(e[0], e[1], e[2], e[3]));
