@@ -2079,6 +2079,11 @@ __global__ void __launch_bounds__(kNTtc, 1)
         {
             float y[8];
             tmem_ld16<2>(tmem + lane_base + 0 + cg * 16, y);
+            // gam of this thread's two rows and four columns, read before any store
+            const float gR[2] = {sg[ra], sg[ra + 8]};
+            float gS[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) gS[c] = sg[cg * 16 + 8 * (c >> 1) + cp + (c & 1)];
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
                 const int r = ra + 8 * hr;
@@ -2088,8 +2093,8 @@ __global__ void __launch_bounds__(kNTtc, 1)
                     const float2 qk = *reinterpret_cast<const float2*>(R4 + sw128_off(r, s, kC));
                     const float x0 = y[4 * n + 2 * hr], x1 = y[4 * n + 2 * hr + 1];
                     const bool in0 = s <= r && r < len, in1 = s + 1 <= r && r < len;
-                    const float d0 = in0 ? x0 * __expf(sg[r] - sg[s]) : 0.f;
-                    const float d1 = in1 ? x1 * __expf(sg[r] - sg[s + 1]) : 0.f;
+                    const float d0 = in0 ? x0 * __expf(gR[hr] - gS[2 * n]) : 0.f;
+                    const float d1 = in1 ? x1 * __expf(gR[hr] - gS[2 * n + 1]) : 0.f;
                     sE[r * kLdT + s] = in0 ? x0 * qk.x : 0.f;
                     sE[r * kLdT + s + 1] = in1 ? x1 * qk.y : 0.f;
                     *reinterpret_cast<float*>(C2 + umma_koff(s, r, kSboC)) = tf32_round(d0);
@@ -2150,6 +2155,13 @@ __global__ void __launch_bounds__(kNTtc, 1)
             tmem_ld16_pair(tmem + lane_base + 320 + cg * 16, f1, tmem + lane_base + 384 + cg * 16, f2);
             // partial column sums over this thread's two rows: columns cg * 16 + 8 n + cp (+1) at [2 n (+1)]
             float c1[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
+            float fbe[4], fge[4];  // beta_r and Gam_r of those four columns, read before any store
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int r = cg * 16 + 8 * (c >> 1) + cp + (c & 1);
+                fbe[c] = sbe[r];
+                fge[c] = sgE[r];
+            }
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
                 const int s = ra + 8 * hr;
@@ -2161,8 +2173,8 @@ __global__ void __launch_bounds__(kNTtc, 1)
                     c1[2 * n + 1] = fmaf(tv.y, f1[i + 1], c1[2 * n + 1]);
                     c2[2 * n] = fmaf(tv.x, f2[i], c2[2 * n]);
                     c2[2 * n + 1] = fmaf(tv.y, f2[i + 1], c2[2 * n + 1]);
-                    const float dt0 = sbe[r] * fmaf(sgE[r], f1[i], f2[i]);
-                    const float dt1 = sbe[r + 1] * fmaf(sgE[r + 1], f1[i + 1], f2[i + 1]);
+                    const float dt0 = fbe[2 * n] * fmaf(fge[2 * n], f1[i], f2[i]);
+                    const float dt1 = fbe[2 * n + 1] * fmaf(fge[2 * n + 1], f1[i + 1], f2[i + 1]);
                     *reinterpret_cast<float2*>(R4 + umma_koff(s, r, kSboC)) = make_float2(tf32_round(dt0), tf32_round(dt1));
                 }
             }
@@ -2269,6 +2281,15 @@ __global__ void __launch_bounds__(kNTtc, 1)
             float a[8], kk[8];
             tmem_ld16_pair(tmem + lane_base + 448 + cg * 16, a, tmem + lane_base + 64 + cg * 16, kk);
             float cacc[4] = {0.f, 0.f, 0.f, 0.f};  // columns cg * 16 + 8 n + cp + e at [2 n + e]
+            // gam and beta of this thread's two rows, gam of its four columns and its eight values of
+            // dE so far, read before any store
+            const float gR[2] = {sg[ra], sg[ra + 8]}, bR[2] = {sbe[ra], sbe[ra + 8]};
+            float gS[4], e0[8];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) gS[c] = sg[cg * 16 + 8 * (c >> 1) + cp + (c & 1)];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                e0[i] = sE[(ra + 8 * ((i >> 1) & 1)) * kLdT + cg * 16 + 8 * (i >> 2) + cp + (i & 1)];
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
                 const int r = ra + 8 * hr;
@@ -2281,11 +2302,11 @@ __global__ void __launch_bounds__(kNTtc, 1)
                         const int s = cg * 16 + 8 * n + cp + e, i = 4 * n + 2 * hr + e;
                         // exp(gam_r - gam_s) only where s < r: above the diagonal it can overflow, and
                         // 0 * inf would be NaN
-                        const float da = s < r ? -a[i] : 0.f, ex = s < r ? __expf(sg[r] - sg[s]) : 0.f;
+                        const float da = s < r ? -a[i] : 0.f, ex = s < r ? __expf(gR[hr] - gS[2 * n + e]) : 0.f;
                         acc = fmaf(da * ex, kk[i], acc);
-                        dkk[e] = tf32_round(da * sbe[r] * ex);
+                        dkk[e] = tf32_round(da * bR[hr] * ex);
                         *reinterpret_cast<float*>(R2 + umma_koff(s, r, kSboC)) = dkk[e];
-                        const float de = fmaf(da * sbe[r], kk[i], sE[r * kLdT + s]);  // dE[r][s], complete
+                        const float de = fmaf(da * bR[hr], kk[i], e0[i]);  // dE[r][s], complete
                         const float pe = s < r ? de * ex : (s == r ? de : 0.f);     // dE * E on its support
                         racc += pe;
                         cacc[2 * n + e] += pe;
