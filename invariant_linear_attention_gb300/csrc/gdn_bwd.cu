@@ -38,6 +38,7 @@
 // Gradients are deterministic (fixed orders everywhere, no atomics on data: the one atomic counts
 // arrivals for the on-chip fold and decides which CTA sums, not the order of the sum).
 #include <algorithm>
+#include <cuda_fp16.h>
 
 #include "gdn_async.cuh"
 #include "gdn_host.h"
@@ -101,6 +102,10 @@ struct BwdParams {
     float* GQb;        // per chunk-head C x dk: diag(Gam) Q
     float* Sb;         // per chunk-head dv x dk (chunk-start state)
     float* Db;         // per chunk-head dv x dk (dL/d state at chunk end)
+    __half* Sh;        // dk = dv = 128 (bf16), in place of Sb: per chunk-head S^T, 128 x 128, as scaled fp16
+    __half* Dh;        //   likewise D^T, in place of Db
+    float* Ssc;        //   per chunk-head 16 factors of Sh, one per 32 x 32 tile: value = fp16 * factor
+    float* Dsc;        //   likewise for Dh
     float* Ub;         // per chunk-head C x dv
     float* dUb;        // per chunk-head C x dv
     float* dgamA;      // per chunk-head C
@@ -563,7 +568,8 @@ __global__ void __launch_bounds__(kNTs) bwd_state_bwd_kernel(BwdParams p, int R)
 // warps = 4 TMEM lane quarters x 4 column groups, and the staging strides) assume it.
 constexpr int kNTtc = 512;
 // At dk = 128 the chunk states S_c and D_c go out transposed (dk x dv), the layout in which
-// bwd_intra_tc_kernel takes them as K-major operands; other dk keep the row-major layout.
+// bwd_intra_tc_kernel takes them as K-major operands, and as fp16 of their TF32 values with a
+// factor per 32 x 32 tile (store_state_f16); other dk keep the row-major fp32 layout.
 template <int DK>
 constexpr bool kStateTransposed = DK == 128;
 constexpr uint32_t kSboC = kC * 32;  // 8 rows x 64 values x 4 bytes
@@ -658,6 +664,39 @@ __device__ __forceinline__ void put_slice_tc(uint8_t* dst, int i, int c0, uint32
         *reinterpret_cast<float4*>(dst + umma_koff(i, c0 + m, sbo)) =
             make_float4(tf32_round(sign * x[m]), tf32_round(sign * x[m + 1]), tf32_round(sign * x[m + 2]),
                         tf32_round(sign * x[m + 3]));
+}
+
+// This thread's slice of a 128 x 128 state (row i, columns 32 cg .. 32 cg + 31, in TMEM at t) out as
+// the fp16 transpose dst[j][i].  Each value is first rounded to TF32, as a product reads it, then
+// multiplied by a power of two 2^e shared by the warp's 32 x 32 tile (rows 32 (i / 32) .., the
+// same columns), with e chosen so that the tile's largest magnitude lands in [2^14, 2^15).  fp16
+// holds 10 mantissa bits like TF32, so every value within a factor 2^29 of the tile's largest
+// (an fp16 normal number after scaling) is stored exactly; smaller ones keep an absolute error
+// below 2^-40 of it.  The factor back, 2^-e, goes to fac[4 cg + i / 32].
+__device__ __forceinline__ void store_state_f16(__half* dst, float* fac, uint32_t t, int i, int cg) {
+    float m = 0.f;
+#pragma unroll
+    for (int c = 0; c < 32; c += 16) {
+        float x[16];
+        tmem_ld<2>(t + c, x);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) m = fmaxf(m, fabsf(x[u]));
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+    // m = 1.f * 2^(be - 127) for a normal m (be its biased exponent), so e = 14 - (be - 127); a
+    // tile of zeros or of fp32 subnormals takes the largest factor, one with an inf the factor 1
+    const int be = (int)((__float_as_uint(m) >> 23) & 255u);
+    const int e = be == 255 ? 0 : min(141 - be, 126);
+    const float up = __uint_as_float((uint32_t)(127 + e) << 23), down = __uint_as_float((uint32_t)(127 - e) << 23);
+#pragma unroll
+    for (int c = 0; c < 32; c += 16) {
+        float x[16];
+        tmem_ld<2>(t + c, x);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) dst[(size_t)(32 * cg + c + u) * 128 + i] = __float2half_rn(tf32_round(x[u]) * up);
+    }
+    if ((threadIdx.x & 31) == 0) fac[4 * cg + (i >> 5)] = down;
 }
 
 // per (sequence, head), chunks in order: S_c out, U = U~ - W S^T, S <- Gam_last S + U^T diag(b) K.
@@ -777,15 +816,13 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p)
             umma_commit(bar);
         }
         // chunk-start state out, U~ into registers and the next chunk's keys, while the product runs
+        if constexpr (kStateT) {
+            store_state_f16(p.Sh + ci * DK * kDv, p.Ssc + ci * 16, tS, i, cg);
+        } else {
 #pragma unroll
-        for (int c8 = 0; c8 < kS; c8 += kSc) {
-            float x[kSc];
-            tmem_ld<kSc / 8>(tS + c8, x);
-            if constexpr (kStateT) {
-                float* dst = p.Sb + (ci * DK + cg * kS + c8) * kDv + i;
-#pragma unroll
-                for (int m = 0; m < kSc; ++m) dst[(size_t)m * kDv] = x[m];
-            } else {
+            for (int c8 = 0; c8 < kS; c8 += kSc) {
+                float x[kSc];
+                tmem_ld<kSc / 8>(tS + c8, x);
                 float* dst = p.Sb + (ci * kDv + i) * DK + cg * kS + c8;
 #pragma unroll
                 for (int m = 0; m < kSc; m += 4)
@@ -1006,15 +1043,13 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_bwd_tc_kernel(BwdParams p)
             umma_commit(bar);
         }
         // D_c out and W^T into registers while the product runs
+        if constexpr (kStateT) {
+            store_state_f16(p.Dh + ci * DK * kDv, p.Dsc + ci * 16, tD, i, cg);
+        } else {
 #pragma unroll
-        for (int c8 = 0; c8 < kS; c8 += kSc) {
-            float x[kSc];
-            tmem_ld<kSc / 8>(tD + c8, x);
-            if constexpr (kStateT) {
-                float* dst = p.Db + (ci * DK + cg * kS + c8) * kDv + i;
-#pragma unroll
-                for (int m = 0; m < kSc; ++m) dst[(size_t)m * kDv] = x[m];
-            } else {
+            for (int c8 = 0; c8 < kS; c8 += kSc) {
+                float x[kSc];
+                tmem_ld<kSc / 8>(tD + c8, x);
                 float* dst = p.Db + (ci * kDv + i) * DK + cg * kS + c8;
 #pragma unroll
                 for (int m = 0; m < kSc; m += 4)
@@ -1808,6 +1843,26 @@ __device__ __forceinline__ void fold_tokens(const BwdParams& p, const long long 
 // K^, U, dU and S0^T arrive by tensor copies (one thread, one mbarrier) in the 128-byte-swizzled
 // K-major layout (boxes of 32 values x rows, four atom columns per 128 values); D^T takes the same
 // layout, written by threads; every other operand uses the layout of umma_koff.
+// Eight fp16 values (one 16-byte piece of a stored state) times the factor of their tile, in fp32.
+__device__ __forceinline__ void unpack_h8(const uint4& v, float fac, float (&x)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[u]));
+        x[2 * u] = f.x * fac;
+        x[2 * u + 1] = f.y * fac;
+    }
+}
+// Values i = 8 pc .. 8 pc + 7 of row j of a K-half (128 rows x 64 fp32) in the 128-byte-swizzled
+// K-major layout: atom column pc / 4 (32 values, 16 KB), 16-byte pieces 2 (pc % 4) and the next.
+__device__ __forceinline__ void put_piece_sw128(uint8_t* half_base, int j, int pc, const float (&x)[8]) {
+    uint8_t* row = half_base + 16384 * (pc >> 2) + 128 * j;
+#pragma unroll
+    for (int w = 0; w < 2; ++w)
+        *reinterpret_cast<float4*>(row + (((2 * (pc & 3) + w) ^ (j & 7)) << 4)) =
+            make_float4(x[4 * w], x[4 * w + 1], x[4 * w + 2], x[4 * w + 3]);
+}
+
 constexpr size_t kIntraCTcSmem = (size_t)5 * 32768 + 2 * 16384 + 4 * kC * kLdT + 4 * (6 * kC + 3 * 4 * kC) + 32;
 
 __global__ void __launch_bounds__(kNTtc, 1)
@@ -1863,38 +1918,44 @@ __global__ void __launch_bounds__(kNTtc, 1)
         return;
     }
     stagger_first_wave(p.stagger_intra, p.nsm);
-    // phase A: K^ -> R1, U -> R3, dU -> R5 (rows = chunk positions), S0^T in two K-halves -> R4 and
-    // C1|C2 (rows j, k = i), all by tensor copies (four boxes of 32 values per operand), and dO (bf16,
-    // two boxes of 64 values) -> R2 + 16 KB, converted into R2 once it lands
+    // phase A: K^ -> R1, U -> R3, dU -> R5 (rows = chunk positions) by tensor copies (four boxes of 32
+    // values per operand); S0^T (fp16, two boxes of 64 values) -> R4 + 16 KB and C2, and dO (bf16, two
+    // boxes of 64 values) -> R2 + 16 KB, converted once they land: S0^T in two K-halves into R4 and
+    // C1|C2 (rows j, k = i), dO into R2
     if (tid == 0) {
         mbar_init(bar, 1);
         mbar_init(bar_ld, 1);
         fence_barrier_init();
-        mbar_arrive_expect_tx(bar_ld, 5u * 32768u + 16384u);
+        mbar_arrive_expect_tx(bar_ld, 4u * 32768u + 16384u);
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
             tma_load_2d(R1 + 8192 * a, &tm_k, bar_ld, hk * kD + 32 * a, t0);
             tma_load_2d(R3 + 8192 * a, &tm_u, bar_ld, 32 * a, (int)(ci * kC));
             tma_load_2d(R5 + 8192 * a, &tm_du, bar_ld, 32 * a, (int)(ci * kC));
-            tma_load_2d((a < 2 ? R4 : C1) + 16384 * (a & 1), &tm_s, bar_ld, 32 * a, (int)(ci * kD));
         }
+        // S0^T as stored (fp16, two boxes of 64 values x 128 rows) into the second halves of its
+        // targets, R4 and C1|C2
+        tma_load_2d(R4 + 16384, &tm_s, bar_ld, 0, (int)(ci * kD));
+        tma_load_2d(C1 + 16384, &tm_s, bar_ld, 64, (int)(ci * kD));
         tma_load_2d(R2 + 16384, &tm_do, bar_ld, h * kD, t0);
         tma_load_2d(R2 + 24576, &tm_do, bar_ld, h * kD + 64, t0);
     }
     if (warp == 0) tmem_alloc(slot, 512);
-    const float* Dt = p.Db + ci * kD * kD;    // D^T: row j (dk index), dv index contiguous
-    // D^T (fp32) into registers, element by element where this thread finds the copied S0^T below:
-    // float4 f = tid + 512 it of a K-half (atom column f / 1024, row (f / 8) % 128, chunk position
-    // f % 8).  <D, S0> then takes S0 as copied, and D^T lands in the same layout.
-    float4 dreg[2][4];
+    // D^T (fp16, row j = dk index, dv index i contiguous) into registers in pieces of 8 values, the
+    // pieces where this thread converts S0^T below: piece f = tid + 512 it is K-half hb = f / 1024, row
+    // j = (f / 8) % 128, values i = 64 hb + 8 (f % 8) ..; with each piece the factors of its tile of D
+    // and of S0.  <D, S0> takes both as stored, and D^T lands in S0^T's layout.
+    const __half* Dt = p.Dh + ci * kD * kD;
+    uint4 dh[4];
+    float dfac[4], sfac[4];
 #pragma unroll
-    for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-            const int f = tid + it * kNTtc, j = (f >> 3) & (kD - 1);
-            const int k = 32 * (f >> 10) + 4 * ((f & 7) ^ (j & 7));
-            dreg[hf][it] = *reinterpret_cast<const float4*>(Dt + j * kD + kC * hf + k);
-        }
+    for (int it = 0; it < 4; ++it) {
+        const int f = tid + it * kNTtc, hb = f >> 10, j = (f >> 3) & (kD - 1), pc = f & 7;
+        dh[it] = *reinterpret_cast<const uint4*>(Dt + j * kD + 64 * hb + 8 * pc);
+        const int tile = 4 * (j >> 5) + 2 * hb + (pc >> 2);
+        dfac[it] = p.Dsc[ci * 16 + tile];
+        sfac[it] = p.Ssc[ci * 16 + tile];
+    }
     for (int i = tid; i < kC; i += kNTtc) {
         // past the chunk's end gam stays at its last value (as the cumsum in bwd_wy_tc_kernel leaves it),
         // so gam is non-increasing over all 64 rows and exp(gam_r - gam_s), s <= r, never exceeds 1
@@ -1924,30 +1985,34 @@ __global__ void __launch_bounds__(kNTtc, 1)
                                               __uint_as_float(b.y << 16), __uint_as_float(b.y & 0xFFFF0000u))
                                 : z4;
             }
+            uint4 sv[4];  // S0^T's pieces (see dh) from its copy: 128-byte rows, 16-byte pieces swizzled
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+                const int f = tid + it * kNTtc, hb = f >> 10, j = (f >> 3) & (kD - 1), pc = f & 7;
+                sv[it] = *reinterpret_cast<const uint4*>((hb ? C1 : R4) + 16384 + 128 * j + ((pc ^ (j & 7)) << 4));
+            }
             __syncthreads();
 #pragma unroll
             for (int u = 0; u < RO::kItems; ++u)
                 *reinterpret_cast<float4*>(R2 + umma_koff(RO::row(u), RO::col(u), kSboD)) = tf32_round4(ov[u]);
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+                const int f = tid + it * kNTtc, hb = f >> 10, j = (f >> 3) & (kD - 1), pc = f & 7;
+                float sx[8], dx[8];
+                unpack_h8(sv[it], sfac[it], sx);
+                unpack_h8(dh[it], dfac[it], dx);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) dot = fmaf(dx[u], sx[u], dot);
+                put_piece_sw128(hb ? C1 : R4, j, pc, sx);
+            }
         }
-        // TF32 rounding of the copied K^ and S0^T (U and dU arrive rounded by the state passes), and
-        // zero rows of K^ past the chunk (the copy fills them from the next sequence)
+        // TF32 rounding of the copied K^ (U and dU arrive rounded by the state passes, S0^T as TF32
+        // values), and zero rows of K^ past the chunk (the copy fills them from the next sequence)
 #pragma unroll
         for (int it = 0; it < 32768 / 16 / kNTtc; ++it) {
             float4* v = reinterpret_cast<float4*>(R1) + tid + it * kNTtc;
             *v = tf32_round4(*v);
         }
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-            for (int it = 0; it < 4; ++it) {
-                float4* v = reinterpret_cast<float4*>(hf ? C1 : R4) + tid + it * kNTtc;
-                const float4 x = *v, d = dreg[hf][it];
-                dot = fmaf(d.x, x.x, dot);
-                dot = fmaf(d.y, x.y, dot);
-                dot = fmaf(d.z, x.z, dot);
-                dot = fmaf(d.w, x.w, dot);
-                *v = tf32_round4(x);
-            }
         if (len < kC)
             for (int e = tid; e < (kC - len) * (kD / 4); e += kNTtc) {  // whole 128-byte row pieces
                 const int r = len + e / (kD / 4), a = (e >> 3) & 3, u = e & 7;
@@ -1985,10 +2050,12 @@ __global__ void __launch_bounds__(kNTtc, 1)
         // phase A2: the products above have read dO and both halves of S0^T.  D^T -> R2 (first K-half)
         // and C1|C2 (second), in the layout of the S0^T halves
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-            for (int it = 0; it < 4; ++it)
-                reinterpret_cast<float4*>(hf ? C1 : R2)[tid + it * kNTtc] = tf32_round4(dreg[hf][it]);
+        for (int it = 0; it < 4; ++it) {
+            const int f = tid + it * kNTtc, hb = f >> 10, j = (f >> 3) & (kD - 1), pc = f & 7;
+            float dx[8];
+            unpack_h8(dh[it], dfac[it], dx);
+            put_piece_sw128(hb ? C1 : R2, j, pc, dx);
+        }
         float kv[16];  // k^[r][j] for the U D epilogue
 #pragma unroll
         for (int m = 0; m < 16; ++m) {
@@ -2425,7 +2492,7 @@ __global__ void bwd_fold_kernel(BwdParams p) {
 
 // ---------------------------------------------------------------------------
 struct BwdLayout {
-    size_t coff, qn, kn, qinv, kinv, gam, W, Ut, T, QK, P, BK, GQ, S, D, U, dU, dgA, dqh, dkh, fcnt, total;
+    size_t coff, qn, kn, qinv, kinv, gam, W, Ut, T, QK, P, BK, GQ, S, D, Ssc, Dsc, U, dU, dgA, dqh, dkh, fcnt, total;
     int nchm;
 };
 
@@ -2454,8 +2521,11 @@ static BwdLayout bwd_layout(const gdn_shape* s) {
     const bool tc128 = s->dtype == GDN_BF16 && dk == 128 && dv == 128;
     L.BK = take(tc128 ? 0 : CH * kC * dk * 4);
     L.GQ = take(tc128 ? 0 : CH * kC * dk * 4);
-    L.S = take(CH * dv * dk * 4);
-    L.D = take(CH * dv * dk * 4);
+    // the chunk states: fp32, or at dk = dv = 128 (bf16) fp16 with a factor per 32 x 32 tile
+    L.S = take(CH * dv * dk * (tc128 ? 2 : 4));
+    L.D = take(CH * dv * dk * (tc128 ? 2 : 4));
+    L.Ssc = take(tc128 ? CH * 16 * 4 : 0);
+    L.Dsc = take(tc128 ? CH * 16 * 4 : 0);
     L.U = take(CH * kC * dv * 4);
     L.dU = take(CH * kC * dv * 4);
     L.dgA = take(tc128 ? 0 : CH * kC * 4);
@@ -2540,6 +2610,10 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
     p.GQb = reinterpret_cast<float*>(ws + L.GQ);
     p.Sb = reinterpret_cast<float*>(ws + L.S);
     p.Db = reinterpret_cast<float*>(ws + L.D);
+    p.Sh = reinterpret_cast<__half*>(ws + L.S);
+    p.Dh = reinterpret_cast<__half*>(ws + L.D);
+    p.Ssc = reinterpret_cast<float*>(ws + L.Ssc);
+    p.Dsc = reinterpret_cast<float*>(ws + L.Dsc);
     p.Ub = reinterpret_cast<float*>(ws + L.U);
     p.dUb = reinterpret_cast<float*>(ws + L.dU);
     p.dgamA = reinterpret_cast<float*>(ws + L.dgA);
@@ -2618,11 +2692,12 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
 
     if (tc128) {
         // tensor maps of the other operands bwd_intra_tc_kernel copies: U and dU ([chunk-head * 64][128]),
-        // S0^T ([chunk-head * 128][128]), Q K^T and T ([chunk-head * 64][64]), V and dO ([T][HV * 128] bf16)
+        // S0^T ([chunk-head * 128][128] fp16), Q K^T and T ([chunk-head * 64][64]), V and dO ([T][HV * 128]
+        // bf16)
         CUtensorMap mu{}, mdu{}, ms{}, mqk{}, mt{}, mv{}, mdo{};
         if (encode_rows_sw128(&mu, p.Ub, GDN_F32, 128, CH * kC, 512, kC) != GDN_OK ||
             encode_rows_sw128(&mdu, p.dUb, GDN_F32, 128, CH * kC, 512, kC) != GDN_OK ||
-            encode_rows_sw128(&ms, p.Sb, GDN_F32, 128, CH * 128, 512, 128) != GDN_OK ||
+            encode_rows_sw128(&ms, p.Sh, GDN_BF16, 128, CH * 128, 256, 128) != GDN_OK ||  // 2-byte elements: fp16
             encode_rows_sw128(&mqk, p.QKb, GDN_F32, kC, CH * kC, 256, kC) != GDN_OK ||
             encode_rows_sw128(&mt, p.Tb, GDN_F32, kC, CH * kC, 256, kC) != GDN_OK ||
             encode_rows_sw128(&mv, v, GDN_BF16, (uint64_t)s->HV * 128, (uint64_t)std::max(s->T_total, 1),

@@ -192,3 +192,20 @@ def test_many_ragged_sequences_head128():
     dsT = inputs.random_states(len(lengths), 4, 128, 128, seed=45, scale=0.5)
     got, ref = run(x, dO, dsT)
     check(got, ref, x.cu_seqlens)
+
+
+@pytest.mark.parametrize("scale", [1e5, 1e-6])
+def test_state_magnitudes_head128(scale):
+    """Values and output gradients scaled so that the chunk states reach far above fp16's largest
+    value (1e5) or far below its smallest normal one (1e-6) through
+    the tcgen05 kernels (bf16, dk = dv = 128), which store S and D as fp16 with a power-of-two
+    factor per 32 x 32 tile: the relative errors stay those of unscaled inputs."""
+    lengths = [200, 64, 37]
+    x = inputs.make_inputs(lengths, HK=1, HV=2, dk=128, dv=128, dtype=torch.bfloat16, seed=46, init_scale=0.2)
+    x = dataclasses.replace(x, v=(x.v.float() * scale).to(x.v.dtype), init_state=x.init_state * scale)
+    dO = (inputs.grad_out(sum(lengths), 2, 128, seed=47).float() * scale).to(torch.bfloat16)
+    dsT = inputs.random_states(len(lengths), 2, 128, 128, seed=48, scale=0.5) * scale
+    got, ref = run(x, dO, dsT)
+    for name, v in got.items():
+        assert np.isfinite(v).all(), name
+    check(got, ref, x.cu_seqlens)
