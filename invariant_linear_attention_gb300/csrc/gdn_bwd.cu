@@ -706,8 +706,9 @@ __device__ __forceinline__ void store_state_f16(__half* dst, float* fac, uint32_
 // between one chunk's last product and the next chunk's first.  While chunk j computes, chunk j+1's
 // W arrives by 16-byte cp.async once the first product has read W, and its normalised keys come
 // into registers; diag(b) K is formed when they are written as the operand.  U~ comes into
-// registers while the first product runs.  At full size the pass streams about 190 KB per chunk
-// step (S_c and U out; W, U~ and K^ in), so one CTA per SM already keeps HBM well loaded.
+// registers while the first product runs.  At dk = 128 S_c goes out as fp16 with tile factors
+// (store_state_f16), and the pass streams about 160 KB per chunk step (S_c and U out; W, U~ and K^
+// in), so one CTA per SM already keeps HBM well loaded.
 template <int DK>
 __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p) {
     constexpr int kDv = 128, kS = DK / 4, kSc = kS >= 16 ? 16 : 8;  // state columns per thread, per TMEM access
@@ -877,7 +878,8 @@ __global__ void __launch_bounds__(kNTtc, 1) bwd_state_fwd_tc_kernel(BwdParams p)
 //   dU^T = dO^T P + D (diag(b) K)^T,   D <- Gam_last D + dO^T diag(Gam) Q - dU^T W
 // D lives in TMEM (fp32, row i in lane i, columns [256, 256 + DK)): the A operand of D (diag(b) K)^T
 // (read as TF32) and, scaled by Gam_last in place once the first product is done, the accumulator
-// of the last two.  D_c goes out while the first product runs.  W^T has a buffer of its own (loaded
+// of the last two.  D_c goes out while the first product runs (at dk = 128 as fp16 with tile
+// factors, store_state_f16).  W^T has a buffer of its own (loaded
 // into registers during the first product).  The next chunk's P, and its k and q rows as given
 // (bf16, into staging buffers), arrive by cp.async while the last two products run; at the top of
 // its step they become diag(b) K^ and (diag(Gam) Q^)^T, scaled by 1/|k_r|, 1/|q_r| and the decay
@@ -1822,27 +1824,6 @@ __device__ __forceinline__ void fold_tokens(const BwdParams& p, const long long 
     }
 }
 
-// per (chunk, head), dk = dv = 128, bf16 inputs: bwd_intra_s_kernel and bwd_intra_c_kernel in one
-// kernel on tcgen05.  The products with the chunk states come first, in transposed form (rows = the
-// dk index j):
-//   X_q = S0^T dO^T:  dQ_S[r][j] = Gam_r X_q[j][r]      X_w = S0^T dU^T:  dW[s][j] = -X_w[j][s]
-//   Y = D^T U^T:      (diag(b) U D)[r][j] = b_r Y[j][r]  and dW = -(dU S0) once more with M = 64
-// and dgam_r = q^_r . dQ_S,r - b_r k^_r . Y_r (+ sum_r b_r k^_r . Y_r + Gam_last <D, S0> on the last
-// row).  Gam_r X_q and b_r Y go back into TMEM (tcgen05.st) as the first terms of the dq^T and
-// dk^T accumulators; dW stays on chip, as F1's operand and, from X_w, as the transposed one.
-// The C x C products (dP = dO U^T, K K^T, F1 = dW K^T, F2 = dU V^T, Z = dT T^T, T^T Z) use M = 64:
-// row m of the result sits in TMEM lane 32 (m / 16) + m % 16, so lanes 0..15 of each warp quarter
-// hold 16 rows, which the 16x256b loads (tmem_ld16) spread over all 32 threads of the warp.  The
-// products that update dq, dk, dv are taken transposed with the dk / dv index as their 128 rows;
-// dq's two and dk's five terms (dKK and dKK^T separately) accumulate in TMEM and meet global memory
-// once.
-//   TMEM columns: 0 dP, then Z | 64 K K^T | 128 X_q, then dq^T | 192 Y, then dk^T | 256 X_w, then
-//   dv^T | 320 dU S0 (128 wide), then F1 | 384 F2 | 448 T^T Z
-//   shared memory: five 32 KB operand buffers R1..R5 and two 16 KB ones C1, C2 (together one
-//   32 KB buffer at first), reused by phase; S0^T and D^T enter in two K-halves of 32 KB.
-// K^, U, dU and S0^T arrive by tensor copies (one thread, one mbarrier) in the 128-byte-swizzled
-// K-major layout (boxes of 32 values x rows, four atom columns per 128 values); D^T takes the same
-// layout, written by threads; every other operand uses the layout of umma_koff.
 // Eight fp16 values (one 16-byte piece of a stored state) times the factor of their tile, in fp32.
 __device__ __forceinline__ void unpack_h8(const uint4& v, float fac, float (&x)[8]) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -1863,6 +1844,29 @@ __device__ __forceinline__ void put_piece_sw128(uint8_t* half_base, int j, int p
             make_float4(x[4 * w], x[4 * w + 1], x[4 * w + 2], x[4 * w + 3]);
 }
 
+// per (chunk, head), dk = dv = 128, bf16 inputs: bwd_intra_s_kernel and bwd_intra_c_kernel in one
+// kernel on tcgen05.  The products with the chunk states come first, in transposed form (rows = the
+// dk index j):
+//   X_q = S0^T dO^T:  dQ_S[r][j] = Gam_r X_q[j][r]      X_w = S0^T dU^T:  dW[s][j] = -X_w[j][s]
+//   Y = D^T U^T:      (diag(b) U D)[r][j] = b_r Y[j][r]  and dW = -(dU S0) once more with M = 64
+// and dgam_r = q^_r . dQ_S,r - b_r k^_r . Y_r (+ sum_r b_r k^_r . Y_r + Gam_last <D, S0> on the last
+// row).  Gam_r X_q and b_r Y go back into TMEM (tcgen05.st) as the first terms of the dq^T and
+// dk^T accumulators; dW stays on chip, as F1's operand and, from X_w, as the transposed one.
+// The C x C products (dP = dO U^T, K K^T, F1 = dW K^T, F2 = dU V^T, Z = dT T^T, T^T Z) use M = 64:
+// row m of the result sits in TMEM lane 32 (m / 16) + m % 16, so lanes 0..15 of each warp quarter
+// hold 16 rows, which the 16x256b loads (tmem_ld16) spread over all 32 threads of the warp.  The
+// products that update dq, dk, dv are taken transposed with the dk / dv index as their 128 rows;
+// dq's two and dk's five terms (dKK and dKK^T separately) accumulate in TMEM and meet global memory
+// once.
+//   TMEM columns: 0 dP, then Z | 64 K K^T | 128 X_q, then dq^T | 192 Y, then dk^T | 256 X_w, then
+//   dv^T | 320 dU S0 (128 wide), then F1 | 384 F2 | 448 T^T Z
+//   shared memory: five 32 KB operand buffers R1..R5 and two 16 KB ones C1, C2 (together one
+//   32 KB buffer at first), reused by phase; S0^T and D^T enter in two K-halves of 32 KB.
+// K^, U and dU arrive by tensor copies (one thread, one mbarrier) in the 128-byte-swizzled K-major
+// layout (boxes of 32 values x rows, four atom columns per 128 values).  S0^T arrives the same way
+// as stored (fp16, boxes of 64 values) and threads write it, times its tile factors, into that
+// layout; D^T (fp16, through registers) takes the same layout.  Every other operand uses the layout
+// of umma_koff.
 constexpr size_t kIntraCTcSmem = (size_t)5 * 32768 + 2 * 16384 + 4 * kC * kLdT + 4 * (6 * kC + 3 * 4 * kC) + 32;
 
 __global__ void __launch_bounds__(kNTtc, 1)
