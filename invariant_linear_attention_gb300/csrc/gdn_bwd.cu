@@ -1442,17 +1442,26 @@ __global__ void __launch_bounds__(kNTtc, kWyCtasPerSm)
             }
         }
         {
-            // K (row s, four consecutive j, from the copy in sX) and V rows (bf16 bits, unconverted, by
-            // vector loads in flight during the solve), s >= len zero; written transposed into sX after
-            // it: K^T (j, s) and V^T (i, s)
-            using RowsK = RowsTc<kC, kD>;
-            float4 kr[RowsK::kItems];
-            uint2 vr[RowsK::kItems];
+            // K^T for after the solve: column j of four consecutive rows s .. s + 3 per item from the
+            // copy in sX, consecutive threads on consecutive j, written into sX as K^T (j, s) in one
+            // 16-byte store.  V rows (s, four consecutive i; bf16 bits, unconverted) by 8-byte loads
+            // in flight during the solve, s >= len zero, written as V^T (i, s) value by value.
+            constexpr int kIt = kD * kC / 4 / kNTtc;
+            float4 kr[kIt];
+#pragma unroll
+            for (int it = 0; it < kIt; ++it) {
+                const int e = tid + it * kNTtc, n = e % kD, s = (e / kD) * 4;
+                float kv[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) kv[u] = *reinterpret_cast<const float*>(sX + sw128_off(s + u, n, kD));
+                kr[it] = make_float4(kv[0], kv[1], kv[2], kv[3]);
+            }
+            using RowsV = RowsTc<kC, kD>;
+            uint2 vr[RowsV::kItems];
             const __nv_bfloat16* vb = static_cast<const __nv_bfloat16*>(p.v);
 #pragma unroll
-            for (int it = 0; it < RowsK::kItems; ++it) {
-                const int s = RowsK::row(it), k = RowsK::col(it);
-                kr[it] = *reinterpret_cast<const float4*>(sX + sw128_off(s, k, kD));
+            for (int it = 0; it < RowsV::kItems; ++it) {
+                const int s = RowsV::row(it), k = RowsV::col(it);
                 vr[it] = s < len ? *reinterpret_cast<const uint2*>(vb + ((size_t)(t0 + s) * p.HV + h) * kD + k)
                                  : make_uint2(0u, 0u);
             }
@@ -1522,16 +1531,18 @@ __global__ void __launch_bounds__(kNTtc, kWyCtasPerSm)
                 }
             }
 #pragma unroll
-            for (int it = 0; it < RowsK::kItems; ++it) {
-                const int s = RowsK::row(it), k = RowsK::col(it);
-                const float kv[4] = {kr[it].x, kr[it].y, kr[it].z, kr[it].w};
+            for (int it = 0; it < kIt; ++it) {
+                const int e = tid + it * kNTtc, n = e % kD, s = (e / kD) * 4;
+                *reinterpret_cast<float4*>(sX + umma_koff(n, s, kSboC)) = tf32_round4(kr[it]);
+            }
+#pragma unroll
+            for (int it = 0; it < RowsV::kItems; ++it) {
+                const int s = RowsV::row(it), k = RowsV::col(it);
                 const float vv[4] = {__uint_as_float(vr[it].x << 16), __uint_as_float(vr[it].x & 0xFFFF0000u),
                                      __uint_as_float(vr[it].y << 16), __uint_as_float(vr[it].y & 0xFFFF0000u)};
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    *reinterpret_cast<float*>(sX + umma_koff(k + t, s, kSboC)) = tf32_round(kv[t]);
+                for (int t = 0; t < 4; ++t)
                     *reinterpret_cast<float*>(sX + 32768 + umma_koff(k + t, s, kSboC)) = tf32_round(vv[t]);
-                }
             }
         }
         __syncthreads();
