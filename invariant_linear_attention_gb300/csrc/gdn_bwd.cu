@@ -1547,24 +1547,31 @@ __global__ void __launch_bounds__(kNTtc, kWyCtasPerSm)
         }
         __syncthreads();
         {
-            // T out; B operands T diag(beta Gam) (over A, unused since the blocks M were formed) and
-            // T diag(beta) (over T itself, once every thread holds its values of T), rows r, k = s
+            // T out, sixteen threads on a row (coalesced); B operands T diag(beta Gam) (over A, unused
+            // since the blocks M were formed) and T diag(beta) (over T itself, once every thread holds
+            // its values of T), rows r, k = s, consecutive threads on consecutive rows (the 16-byte
+            // stores of a core matrix's eight rows then fill all banks)
             constexpr int kIt = kC * kC / 4 / kNTtc;
-            float4 tv[kIt];
             float* Tg = p.Tb + ci * kC * kC;
 #pragma unroll
             for (int it = 0; it < kIt; ++it) {
                 const int e = tid + it * kNTtc, r = e / (kC / 4), s = (e % (kC / 4)) * 4;
                 const float* tr = sTf + r * kLdT + s;
+                *reinterpret_cast<float4*>(Tg + r * kC + s) = make_float4(tr[0], tr[1], tr[2], tr[3]);
+            }
+            float4 tv[kIt];
+#pragma unroll
+            for (int it = 0; it < kIt; ++it) {
+                const int e = tid + it * kNTtc, r = e % kC, s = (e / kC) * 4;
+                const float* tr = sTf + r * kLdT + s;
                 tv[it] = make_float4(tr[0], tr[1], tr[2], tr[3]);
-                *reinterpret_cast<float4*>(Tg + r * kC + s) = tv[it];
                 *reinterpret_cast<float4*>(sB2 + umma_koff(r, s, kSboC)) = tf32_round4(make_float4(
                     tv[it].x * sGb[s], tv[it].y * sGb[s + 1], tv[it].z * sGb[s + 2], tv[it].w * sGb[s + 3]));
             }
             __syncthreads();  // T is read in full before T diag(beta) overwrites it
 #pragma unroll
             for (int it = 0; it < kIt; ++it) {
-                const int e = tid + it * kNTtc, r = e / (kC / 4), s = (e % (kC / 4)) * 4;
+                const int e = tid + it * kNTtc, r = e % kC, s = (e / kC) * 4;
                 *reinterpret_cast<float4*>(sB3 + umma_koff(r, s, kSboC)) = tf32_round4(
                     make_float4(tv[it].x * sb[s], tv[it].y * sb[s + 1], tv[it].z * sb[s + 2], tv[it].w * sb[s + 3]));
             }
