@@ -1885,7 +1885,11 @@ __device__ __forceinline__ void put_piece_sw128(uint8_t* half_base, int j, int p
 // as stored (fp16, boxes of 64 values) and threads write it, times its tile factors, into that
 // layout; D^T (fp16, through registers) takes the same layout.  Every other operand uses the layout
 // of umma_koff.
-constexpr size_t kIntraCTcSmem = (size_t)5 * 32768 + 2 * 16384 + 4 * kC * kLdT + 4 * (6 * kC + 3 * 4 * kC) + 32;
+// dE's row pitch in bwd_intra_tc_kernel: a warp's float2 accesses (rows lane / 4 and 8 on, column
+// pairs 2 (lane % 4)) take two wavefronts, the least for 256 bytes
+constexpr int kLdE = kC + 8;
+constexpr size_t kIntraCTcSmem = (size_t)5 * 32768 + 2 * 16384 + 4 * kC * kLdE + 4 * (6 * kC + 3 * 4 * kC) + 32;
+static_assert(kIntraCTcSmem <= 227 * 1024, "bwd_intra_tc_kernel's shared memory");
 
 __global__ void __launch_bounds__(kNTtc, 1)
     bwd_intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_u,
@@ -1904,8 +1908,8 @@ __global__ void __launch_bounds__(kNTtc, 1)
     uint8_t* R5 = R4 + 32768;
     uint8_t* C1 = R5 + 32768;
     uint8_t* C2 = C1 + 16384;
-    float* sE = reinterpret_cast<float*>(C2 + 16384);  // dE accumulator, 64 x kLdT
-    float* sg = sE + kC * kLdT;                         // gam
+    float* sE = reinterpret_cast<float*>(C2 + 16384);  // dE accumulator, 64 x kLdE
+    float* sg = sE + kC * kLdE;                         // gam
     float* sbe = sg + kC;                               // beta
     float* sdg = sbe + kC;                              // dgam
     float* sdb = sdg + kC;                              // dbeta
@@ -2184,8 +2188,7 @@ __global__ void __launch_bounds__(kNTtc, 1)
                     const bool in0 = s <= r && r < len, in1 = s + 1 <= r && r < len;
                     const float d0 = in0 ? x0 * __expf(gR[hr] - gS[2 * n]) : 0.f;
                     const float d1 = in1 ? x1 * __expf(gR[hr] - gS[2 * n + 1]) : 0.f;
-                    sE[r * kLdT + s] = in0 ? x0 * qk.x : 0.f;
-                    sE[r * kLdT + s + 1] = in1 ? x1 * qk.y : 0.f;
+                    *reinterpret_cast<float2*>(sE + r * kLdE + s) = make_float2(in0 ? x0 * qk.x : 0.f, in1 ? x1 * qk.y : 0.f);
                     *reinterpret_cast<float*>(C2 + umma_koff(s, r, kSboC)) = tf32_round(d0);
                     *reinterpret_cast<float*>(C2 + umma_koff(s + 1, r, kSboC)) = tf32_round(d1);
                     *reinterpret_cast<float2*>(C1 + umma_koff(r, s, kSboC)) = make_float2(tf32_round(d0), tf32_round(d1));
@@ -2377,8 +2380,11 @@ __global__ void __launch_bounds__(kNTtc, 1)
 #pragma unroll
             for (int c = 0; c < 4; ++c) gS[c] = sg[cg * 16 + 8 * (c >> 1) + cp + (c & 1)];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                e0[i] = sE[(ra + 8 * ((i >> 1) & 1)) * kLdT + cg * 16 + 8 * (i >> 2) + cp + (i & 1)];
+            for (int i = 0; i < 8; i += 2) {
+                const float2 v = *reinterpret_cast<const float2*>(sE + (ra + 8 * ((i >> 1) & 1)) * kLdE + cg * 16 + 8 * (i >> 2) + cp);
+                e0[i] = v.x;
+                e0[i + 1] = v.y;
+            }
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
                 const int r = ra + 8 * hr;
