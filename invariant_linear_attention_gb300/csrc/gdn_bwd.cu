@@ -1854,12 +1854,14 @@ __device__ __forceinline__ void unpack_h8(const uint4& v, float fac, float (&x)[
 }
 // Values i = 8 pc .. 8 pc + 7 of row j of a K-half (128 rows x 64 fp32) in the 128-byte-swizzled
 // K-major layout: atom column pc / 4 (32 values, 16 KB), 16-byte pieces 2 (pc % 4) and the next.
+// The second atom column stores its two pieces in the other order, so that the eight threads of a
+// row (pc = 0 .. 7) fill eight different bank groups with each store.
 __device__ __forceinline__ void put_piece_sw128(uint8_t* half_base, int j, int pc, const float (&x)[8]) {
     uint8_t* row = half_base + 16384 * (pc >> 2) + 128 * j;
-#pragma unroll
-    for (int w = 0; w < 2; ++w)
-        *reinterpret_cast<float4*>(row + (((2 * (pc & 3) + w) ^ (j & 7)) << 4)) =
-            make_float4(x[4 * w], x[4 * w + 1], x[4 * w + 2], x[4 * w + 3]);
+    const float4 lo = make_float4(x[0], x[1], x[2], x[3]), hi = make_float4(x[4], x[5], x[6], x[7]);
+    const int sw = pc >> 2;
+    *reinterpret_cast<float4*>(row + (((2 * (pc & 3) + sw) ^ (j & 7)) << 4)) = sw ? hi : lo;
+    *reinterpret_cast<float4*>(row + (((2 * (pc & 3) + (sw ^ 1)) ^ (j & 7)) << 4)) = sw ? lo : hi;
 }
 
 // per (chunk, head), dk = dv = 128, bf16 inputs: bwd_intra_s_kernel and bwd_intra_c_kernel in one
