@@ -1294,7 +1294,8 @@ constexpr size_t kWyTcSmem = (size_t)65536 + 2 * 4 * kC * kLdT + 4 * 3 * kC + 32
 static_assert(kWyCtasPerSm * (kWyTcSmem + 1024) <= 228 * 1024, "two wy CTAs must fit on one SM");
 
 __global__ void __launch_bounds__(kNTtc, kWyCtasPerSm)
-    bwd_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q, BwdParams p) {
+    bwd_wy_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_v, BwdParams p) {
     constexpr int kD = 128;
     extern __shared__ __align__(1024) uint8_t smb_sw[];  // swizzled operands: 1 KB aligned
     uint8_t* const smb = smb_sw;
@@ -1308,7 +1309,8 @@ __global__ void __launch_bounds__(kNTtc, kWyCtasPerSm)
     float* sb = sGb + kC;                                       // beta
     uint64_t* bar = reinterpret_cast<uint64_t*>(sb + kC);
     uint64_t* bar_ld = bar + 1;  // the tensor copies of K^ and Q^
-    uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 2);
+    uint64_t* bar_v = bar + 2;   // the tensor copy of V
+    uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 3);
     // one CTA per (chunk, value head), the heads of a chunk adjacent in launch order (they copy the
     // same K^ and Q^ rows)
     const int h = (int)(blockIdx.x % (unsigned)p.HV), c = (int)(blockIdx.x / (unsigned)p.HV);
@@ -1327,6 +1329,7 @@ __global__ void __launch_bounds__(kNTtc, kWyCtasPerSm)
     if (tid == 0) {
         mbar_init(bar, 1);
         mbar_init(bar_ld, 1);
+        mbar_init(bar_v, 1);
         fence_barrier_init();
         mbar_arrive_expect_tx(bar_ld, 65536u);
 #pragma unroll
@@ -1385,6 +1388,7 @@ __global__ void __launch_bounds__(kNTtc, kWyCtasPerSm)
     tc_sync();
     const uint32_t tmem = *slot;
     uint32_t phase = 0;
+    bool v_pending = false;  // the copy of V is issued and not yet seen complete
     do {
         if (!ok) break;
         if (tid == 0) {
@@ -1444,8 +1448,7 @@ __global__ void __launch_bounds__(kNTtc, kWyCtasPerSm)
         {
             // K^T for after the solve: column j of four consecutive rows s .. s + 3 per item from the
             // copy in sX, consecutive threads on consecutive j, written into sX as K^T (j, s) in one
-            // 16-byte store.  V rows (s, four consecutive i; bf16 bits, unconverted) by 8-byte loads
-            // in flight during the solve, s >= len zero, written as V^T (i, s) value by value.
+            // 16-byte store.  V comes by tensor copy during the solve and goes the same way (below).
             constexpr int kIt = kD * kC / 4 / kNTtc;
             float4 kr[kIt];
 #pragma unroll
@@ -1455,15 +1458,6 @@ __global__ void __launch_bounds__(kNTtc, kWyCtasPerSm)
 #pragma unroll
                 for (int u = 0; u < 4; ++u) kv[u] = *reinterpret_cast<const float*>(sX + sw128_off(s + u, n, kD));
                 kr[it] = make_float4(kv[0], kv[1], kv[2], kv[3]);
-            }
-            using RowsV = RowsTc<kC, kD>;
-            uint2 vr[RowsV::kItems];
-            const __nv_bfloat16* vb = static_cast<const __nv_bfloat16*>(p.v);
-#pragma unroll
-            for (int it = 0; it < RowsV::kItems; ++it) {
-                const int s = RowsV::row(it), k = RowsV::col(it);
-                vr[it] = s < len ? *reinterpret_cast<const uint2*>(vb + ((size_t)(t0 + s) * p.HV + h) * kD + k)
-                                 : make_uint2(0u, 0u);
             }
             // T = (I + A)^-1 by 16 x 16 blocks (A is strictly lower).  The diagonal blocks
             // T_II = (I + A_II)^-1 by forward substitution: each half warp takes two columns of one
@@ -1492,6 +1486,16 @@ __global__ void __launch_bounds__(kNTtc, kWyCtasPerSm)
                 }
             }
             __syncthreads();
+            // V (bf16, two boxes of 64 values x 64 rows) by tensor copy into the halves of the first
+            // two atom columns that held Q^ (free since QK^T and P went out), during the rest of the
+            // solve
+            if (tid == 0) {
+                fence_async_smem();
+                mbar_arrive_expect_tx(bar_v, 16384u);
+                tma_load_2d(sX + 8192, &tm_v, bar_v, h * kD, t0);
+                tma_load_2d(sX + 24576, &tm_v, bar_v, h * kD + 64, t0);
+            }
+            v_pending = true;
             {
                 // M_IK = T_II A_IK for every K < I (six blocks, independent of each other), then block
                 // rows I = 1, 2, 3: T_IJ = -sum_{K = J}^{I - 1} M_IK T_KJ.  Two accumulators per sum.
@@ -1530,19 +1534,31 @@ __global__ void __launch_bounds__(kNTtc, kWyCtasPerSm)
                     __syncthreads();
                 }
             }
+            if (!(ok = __syncthreads_and(mbar_wait_bounded(bar_v, 0)))) break;
+            v_pending = false;
+            // V's column i = n of rows s .. s + 3 per item (the K^T mapping) from its copy: 128-byte
+            // rows, 16-byte pieces swizzled; s >= len zero (the copy reads on into the next sequence)
+            float4 vr[kIt];
+#pragma unroll
+            for (int it = 0; it < kIt; ++it) {
+                const int e = tid + it * kNTtc, n = e % kD, s = (e / kD) * 4;
+                const uint8_t* box = sX + 8192 + 16384 * (n >> 6);
+                float v4[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int r = s + u;
+                    const unsigned short b = *reinterpret_cast<const unsigned short*>(
+                        box + 128 * r + ((((n & 63) >> 3) ^ (r & 7)) << 4) + (n & 7) * 2);
+                    v4[u] = r < len ? __uint_as_float((uint32_t)b << 16) : 0.f;
+                }
+                vr[it] = make_float4(v4[0], v4[1], v4[2], v4[3]);
+            }
+            __syncthreads();  // every read of the copies of K^ and V is done
 #pragma unroll
             for (int it = 0; it < kIt; ++it) {
                 const int e = tid + it * kNTtc, n = e % kD, s = (e / kD) * 4;
                 *reinterpret_cast<float4*>(sX + umma_koff(n, s, kSboC)) = tf32_round4(kr[it]);
-            }
-#pragma unroll
-            for (int it = 0; it < RowsV::kItems; ++it) {
-                const int s = RowsV::row(it), k = RowsV::col(it);
-                const float vv[4] = {__uint_as_float(vr[it].x << 16), __uint_as_float(vr[it].x & 0xFFFF0000u),
-                                     __uint_as_float(vr[it].y << 16), __uint_as_float(vr[it].y & 0xFFFF0000u)};
-#pragma unroll
-                for (int t = 0; t < 4; ++t)
-                    *reinterpret_cast<float*>(sX + 32768 + umma_koff(k + t, s, kSboC)) = tf32_round(vv[t]);
+                *reinterpret_cast<float4*>(sX + 32768 + umma_koff(n, s, kSboC)) = tf32_round4(vr[it]);
             }
         }
         __syncthreads();
@@ -1598,7 +1614,10 @@ __global__ void __launch_bounds__(kNTtc, kWyCtasPerSm)
             }
         }
     } while (false);
-    if (!ok && tid == 0) atomicOr(p.err, GDN_DEVERR_TIMEOUT);
+    if (!ok && tid == 0) {
+        atomicOr(p.err, GDN_DEVERR_TIMEOUT);
+        if (v_pending) mbar_wait_bounded(bar_v, 0);  // the copy of V lands before the CTA leaves
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
@@ -2690,8 +2709,12 @@ extern "C" gdn_status gdn_chunk_bwd(const gdn_shape* s, const void* q, const voi
                            (uint64_t)s->HK * 512, kC) != GDN_OK))
         return GDN_ERR_CUDA;
     if (tc128) {
+        CUtensorMap mvw{};  // V ([T][HV * 128] bf16), copied by bwd_wy_tc_kernel
+        if (encode_rows_sw128(&mvw, v, GDN_BF16, (uint64_t)s->HV * 128, (uint64_t)std::max(s->T_total, 1),
+                              (uint64_t)s->HV * 256, kC) != GDN_OK)
+            return GDN_ERR_CUDA;
         if (!set_smem(bwd_wy_tc_kernel, kWyTcSmem)) return GDN_ERR_CUDA;
-        bwd_wy_tc_kernel<<<(unsigned)CH, kNTtc, kWyTcSmem, cs>>>(mk, mq, p);
+        bwd_wy_tc_kernel<<<(unsigned)CH, kNTtc, kWyTcSmem, cs>>>(mk, mq, mvw, p);
     } else {
         const size_t smem_wy = sizeof(float) * (2 * kC * kLdD + 2 * kC * kLdC + 3 * kC);
         if (!set_smem(bwd_wy_kernel, smem_wy)) return GDN_ERR_CUDA;
