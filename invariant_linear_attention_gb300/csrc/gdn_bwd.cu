@@ -1276,6 +1276,9 @@ __device__ __forceinline__ float half_sum(float x) {
 //   16 x 16 blocks (below), then W^T = K^T (T diag(beta Gam))^T
 //   and U~^T = V^T (T diag(beta))^T with the dk / dv index as the M = 128 rows, so each epilogue
 //   thread stores one column of W and U~: coalesced.
+//   Shared memory is reused by phase: QK^T and P are staged where Q^ was and leave coalesced, and
+//   V arrives by tensor copy into that space while the solve runs; K^T and V^T are then written
+//   by columns, four values of s per 16-byte store.
 //   Two CTAs share an SM (64 registers a thread, 97 KB of shared memory and 256 TMEM columns
 //   each), so that one CTA's copies, solve and epilogues overlap the other's.
 constexpr int kLdT = kC + 1;  // fp32 A and T in shared memory: row-per-lane writes hit distinct banks
