@@ -1604,16 +1604,25 @@ __global__ void __launch_bounds__(kNTtc, kWyCtasPerSm)
         }
         if (!(ok = tc_wait(bar, phase))) break;
         {
-            // W[r][j] = (W^T)[j][r] and U~[r][i] = (U~^T)[i][r] for r = 16 cg + t
+            // W[r][j] = (W^T)[j][r] and U~[r][i] = (U~^T)[i][r] for r = 16 cg + t, row-major into sX
+            // (free once the products have read K^T and V^T), then out by one 32 KB bulk copy each
             const int jj = q * 32 + lane;
             float w[16], u[16];
             tmem_ld_pair(tmem + lane_base + 64 + cg * 16, w, tmem + lane_base + 128 + cg * 16, u);
-            float* W = p.Wb + ci * kC * kD + jj;
-            float* Ut = p.Utb + ci * kC * kD + jj;
+            float* sWr = reinterpret_cast<float*>(sX);
+            float* sUr = sWr + kC * kD;
 #pragma unroll
             for (int t = 0; t < 16; ++t) {
-                W[(size_t)(cg * 16 + t) * kD] = tf32_round(w[t]);  // W only ever enters the tensor cores
-                Ut[(size_t)(cg * 16 + t) * kD] = u[t];
+                sWr[(cg * 16 + t) * kD + jj] = tf32_round(w[t]);  // W only ever enters the tensor cores
+                sUr[(cg * 16 + t) * kD + jj] = u[t];
+            }
+            __syncthreads();
+            if (tid == 0) {
+                fence_async_smem();
+                bulk_store(p.Wb + ci * kC * kD, sWr, kC * kD * 4);
+                bulk_store(p.Utb + ci * kC * kD, sUr, kC * kD * 4);
+                bulk_commit();
+                bulk_wait_read();  // the CTA's shared memory stays until the copies have read it
             }
         }
     } while (false);
