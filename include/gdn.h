@@ -154,7 +154,12 @@ gdn_status gdn_decode_step(const gdn_shape* shape, const void* q, const void* k,
  * d_final_state may be NULL (zero).  Gradients are not bit-invariant (the
  * pages need invariance only for the forward); they are deterministic.  Dense
  * products run on the tensor cores: TF32 operands with fp32 accumulation for
- * bf16 inputs, a 3xTF32 split (about fp32 accuracy) for fp32 inputs.
+ * bf16 inputs, a 3xTF32 split (about fp32 accuracy) for fp32 inputs.  At
+ * dk = dv = 128 with bf16 inputs, the per-chunk states and state gradients
+ * pass between the kernels (in the workspace) as fp16 of their TF32 values,
+ * with a power-of-two factor per 32 x 32 tile: the products read the same
+ * TF32 operands as from fp32 copies, except for values below 2^-29 of their
+ * tile's largest.
  */
 gdn_status gdn_chunk_bwd(const gdn_shape* shape, const void* q, const void* k, const void* v,
                          const float* g, const float* beta, const float* init_state,
